@@ -1,0 +1,102 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins catch each.
+
+Each mutant is a one-line source edit of the oracle (a dropped term, a wrong
+sign, a wrong index or operand, a wrong comparison).  The mutated copy is
+loaded as a separate module; the pins of test_oracle_pins run against it and at
+least one must fail.  Nothing here touches the GPU or the product library.
+"""
+import importlib.util
+import os
+import sys
+import types
+
+import numpy as np
+import pytest
+
+import test_oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "ttt_oracle.py")
+
+MUTANTS = {
+    "forward drops the residual": (
+        'return h + a @ Wb["W2"].T, {"h": h', 'return a @ Wb["W2"].T, {"h": h'),
+    "forward uses W1 transposed (square shapes hide it)": (
+        'z = h @ Wb["W1"].T', 'z = h @ Wb["W1"][:, :h.shape[1]]'),
+    "backward drops the residual path": (
+        'dh = dout + dz @ Wb["W1"] if need_dh', 'dh = dz @ Wb["W1"] if need_dh'),
+    "GELU derivative drops z*phi": (
+        "return 0.5 * (1.0 + erf(z / SQRT2)) + z * INV_SQRT_2PI", "return 0.5 * (1.0 + erf(z / SQRT2)) + 0 * INV_SQRT_2PI"),
+    "RMSNorm backward sign": (
+        "(dy - xh * np.mean(xh * dy", "(dy + xh * np.mean(xh * dy"),
+    "RMSNorm eps outside the sqrt": (
+        "r = 1.0 / np.sqrt(np.mean(x * x, axis=-1) + eps)", "r = 1.0 / (np.sqrt(np.mean(x * x, axis=-1)) + eps)"),
+    "chunk gradient is a sum, not a mean": (
+        "    dlogits /= b\n", "    dlogits /= 1\n"),
+    "CE picks the wrong target column": (
+        "losses = lse - logits[np.arange(len(targets)), targets]",
+        "losses = lse - logits[np.arange(len(targets)), (targets + 1) % logits.shape[1]]"),
+    "losses scored after the update": (
+        "    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt)\n    s, norm = clip_scale(grads, clip)\n    st.W = sgd_step(st.W, grads, eta, s)\n",
+        "    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt)\n    s, norm = clip_scale(grads, clip)\n    st.W = sgd_step(st.W, grads, eta, s)\n    losses = token_losses(net, st.W, x_in, tgt)\n"),
+    "targets not shifted by one": (
+        "tokens[lo:lo + b], tokens[lo + 1:lo + b + 1],", "tokens[lo:lo + b], tokens[lo:lo + b],"),
+    "clip scale inverted": (
+        "return min(1.0, clip / (norm + CLIP_EPS)), norm", "return min(1.0, (norm + CLIP_EPS) / clip), norm"),
+    "update sign": ("nb[k] = Wb[k] - (eta * s) * v", "nb[k] = Wb[k] + (eta * s) * v"),
+    "Settlement tie rejects": ("accept = bool(A >= 0.0)", "accept = bool(A > 0.0)"),
+    "Settlement A sign": (
+        "A = heldout_loss(net, st.Wc, q) - heldout_loss(net, st.W, q)",
+        "A = heldout_loss(net, st.W, q) - heldout_loss(net, st.Wc, q)"),
+    "SwiGLU up-gradient uses g": ("du = da * silu(cache[\"g\"])", "du = da * cache[\"g\"]"),
+    "SwiGLU gate gradient drops silu'": (
+        'dg = da * cache["u"] * silu_grad(cache["g"])', 'dg = da * cache["u"] * silu(cache["g"])'),
+    "p_next with the initial weights": (
+        "p_next = softmax_next(net, st.W, st.x_last)", "p_next = softmax_next(net, net.fast0, st.x_last)"),
+}
+
+PINS = [
+    ("test_fast_weight_gradients_match_central_differences", ("gelu", 3)),
+    ("test_fast_weight_gradients_match_central_differences", ("swiglu", 3)),
+    ("test_gelu_closed_form_values", ()),
+    ("test_rmsnorm_unit_rms_and_scale_invariance", ()),
+    ("test_rmsnorm_backward_finite_differences", ()),
+    ("test_cross_entropy_identities", ()),
+    ("test_b1_is_the_per_token_update_of_eq2", ()),
+    ("test_eta0_gives_the_static_ttt_naive_loss_of_eq4", ()),
+    ("test_single_chunk_b_equals_T", ()),
+    ("test_prequential_losses_use_the_previous_chunks_weights_eq3_eq6", ()),
+    ("test_clip_bounds_the_step", ()),
+    ("test_p_next_is_f_of_last_token_with_final_weights", ()),
+    ("test_settlement_commits_a_descent_step", ()),
+    ("test_settlement_rejects_an_ascent_step_and_reverts_exactly", ()),
+    ("test_settlement_tie_commits", ()),
+    ("test_settlement_two_token_case_by_hand", ()),
+    ("test_forward_by_hand_nonsquare", ()),
+    ("test_decoding_a_full_chunk_equals_a_longer_prefill", ()),
+]
+
+
+def _load_mutant(old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, old
+    mod = types.ModuleType("ttt_oracle_mutant")
+    mod.__dict__["__name__"] = "ttt_oracle_mutant"
+    sys.modules["ttt_oracle_mutant"] = mod
+    exec(compile(src.replace(old, new), "ttt_oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_every_planted_mistake_fails_a_pin(name, monkeypatch):
+    mod = _load_mutant(*MUTANTS[name])
+    monkeypatch.setattr(P, "O", mod)
+    caught = []
+    for pin, args in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                getattr(P, pin)(*args)
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            caught.append(pin)
+    assert caught, f"no pin caught mutant '{name}'"
