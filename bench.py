@@ -1,0 +1,388 @@
+"""Benchmark: TTT prefill tokens/s (forward + backward + clipped update) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+One step is one full prefill of the workload's B sequences of T tokens: every
+chunk runs the frozen prefix, the fast blocks forward, RMSNorm, the LM head, the
+fused cross-entropy, the backward to the fast weights and the clipped SGD step.
+Inputs (seeded synthetic Markov tokens, N(0, 0.02^2) weights) are resident on
+the device before the timed region; L2 is flushed (a 512 MB write) before every
+timed step, outside the step's events.  `e2e` times the same call with pinned
+host buffers (tokens in, losses and p_{T+1} out) through the C ABI.
+
+With --gpus N under torchrun every rank runs its own B sequences (weak scaling:
+the sequences are independent, so no collective is on the data path); rank 0
+prints the max-over-ranks time.  --impl reference times the float64 CPU oracle
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+from synth import configs as C  # noqa: E402
+
+METRIC = "TTT prefill tokens/s (fwd+bwd+update) on 1 B300; % of chunk roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0}
+
+
+def peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    p = dict(FALLBACK)
+    p["source"] = "fallback"
+    return p
+
+
+# ---------------------------------------------------------------- accounting
+def chunk_flops(wl, rows=None):
+    """Dense-contraction FLOPs of one chunk step for all B sequences, by class."""
+    M = wl.B * (wl.chunk if rows is None else rows)
+    mdf = 2.0 * M * wl.d * wl.d_ff
+    per = {}
+    if wl.block == "gelu":
+        per["gemm_prefix"] = wl.n_prefix * 2 * mdf
+        per["gemm_fast_fwd"] = wl.n_fast * 2 * mdf
+        per["gemm_bwd_dx"] = (2 * wl.n_fast - 1) * mdf
+        per["gemm_dw"] = 2 * wl.n_fast * mdf
+    else:
+        per["gemm_prefix"] = wl.n_prefix * 3 * mdf
+        per["gemm_fast_fwd"] = wl.n_fast * 3 * mdf
+        per["gemm_bwd_dx"] = 0.0
+        per["gemm_dw"] = wl.n_fast * mdf
+    per["gemm_head"] = 2.0 * M * wl.d * wl.vocab
+    per["gemm_head_bwd"] = 2.0 * M * wl.d * wl.vocab
+    return per
+
+
+def chunk_bytes(wl):
+    """Algorithmic HBM bytes of one chunk step, by class (see DESIGN: each
+    tensor read or written once; the V-wide logits buffer counted once in
+    the CE class as read + write)."""
+    es = 2 if wl.dtype == "bf16" else 4
+    M = wl.B * wl.chunk
+    nf = len(wl.fast_mats) * wl.n_fast
+    params = nf * wl.B * wl.d * wl.d_ff
+    return {
+        "ce_fused": 2.0 * M * wl.vocab * es,
+        "clip_sgd_update": params * (4 + 4 + 4 + 4 + es),   # read W32, dW; write W32; op copy
+        "rmsnorm_fwd": M * wl.d * (4 + es),
+        "rmsnorm_bwd": M * wl.d * (4 * 3 + 4 + es),
+        "embed": M * wl.d * (es + 4 + es),
+        "grad_norm": 0.0,
+    }
+
+
+def chunk_roofline_seconds(wl, pk):
+    fl = sum(chunk_flops(wl).values())
+    es = 2 if wl.dtype == "bf16" else 4
+    M = wl.B * wl.chunk
+    nf = len(wl.fast_mats) * wl.n_fast
+    params = nf * wl.B * wl.d * wl.d_ff
+    # weights read once per chunk (frozen prefix, head, fast masters r+w), token ids, losses,
+    # and the block inputs written and read once
+    frozen = (wl.n_prefix * (2 if wl.block == "gelu" else 3) * wl.d * wl.d_ff + wl.vocab * wl.d) * es
+    by = frozen + params * 8 + M * 8 + M * wl.d * es * 2
+    return max(fl / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9)), fl, by
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, inp, n_seq, n_chunks):
+    import oracle
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    tok = inp["tokens"][:n_seq, :n_chunks * wl.chunk + 1]
+    t0 = time.perf_counter()
+    oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
+    dt = time.perf_counter() - t0
+    return n_seq * n_chunks * wl.chunk / dt, dt
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, wl, rank):
+    if rank != 0:
+        return
+    inp = synth.make_inputs(wl.replace(B=1))
+    n_chunks = max(1, min(wl.n_chunks, 4))
+    for _ in range(args.warmup):
+        oracle_sample(wl, inp, 1, 1)
+    vals, times = [], []
+    for _ in range(args.steps):
+        v, dt = oracle_sample(wl, inp, 1, n_chunks)
+        vals.append(v)
+        times.append(dt)
+    v = len(vals) * n_chunks * wl.chunk / sum(times)
+    sample = f"1 sequence x {n_chunks} chunks ({n_chunks * wl.chunk} tokens) of {wl.name} per step"
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "chunk": wl.chunk},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+
+    from chunked_next_token_ttt_b300 import Handle, kernel_classes
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    # every rank owns its own B sequences: shift the stream seeds by rank
+    inp = synth.make_inputs(wl)
+    if rank:
+        inp["tokens"] = synth.sample_stream(inp["chain"], wl.seed_id + 1000 * rank, wl.B, wl.T)
+    h = Handle.from_workload(wl, inp["weights"])
+    tok = torch.from_numpy(inp["tokens"]).to(dev)
+    losses = torch.empty((wl.B, wl.T), dtype=torch.float32, device=dev)
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device=dev)
+    n_ev = wl.n_settle_events
+    q = torch.from_numpy(inp["settle_q"]).to(dev) if n_ev else None
+    acc = torch.empty((max(1, n_ev), wl.B), dtype=torch.uint8, device=dev)
+    A = torch.empty((max(1, n_ev), wl.B), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        h.prefill(tok, losses, p, q, acc if n_ev else None, A if n_ev else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # which kernel class dominates: one untimed profiled prefill per class
+    classes = kernel_classes()
+    per_class = {}
+    for ci, name in enumerate(classes):
+        h.profile_enable(ci)
+        step()
+        n, ms = h.profile_read()
+        if n:
+            per_class[name] = (n, ms)
+    h.profile_enable(-1)
+    dom = max(per_class, key=lambda k: per_class[k][1])
+
+    # timed region: K steps, L2 flushed before each, the dominant class timed live
+    h.profile_enable(classes.index(dom))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(st)
+            step()
+            ev[i][1].record(st)
+            launches += h.last_launch_count()
+        torch.cuda.synchronize(dev)
+    dom_n, dom_ms = h.profile_read()
+    h.profile_enable(-1)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    tokens = wl.B * wl.T * world * args.steps
+    value = tokens / (total_ms / 1e3)
+
+    # end to end: pinned host buffers through the C ABI
+    tok_h = torch.from_numpy(inp["tokens"]).pin_memory()
+    loss_h = torch.empty((wl.B, wl.T), dtype=torch.float32).pin_memory()
+    p_h = torch.empty((wl.B, wl.vocab), dtype=torch.float32).pin_memory()
+    q_h = torch.from_numpy(inp["settle_q"]).pin_memory() if n_ev else None
+    acc_h = torch.empty((max(1, n_ev), wl.B), dtype=torch.uint8).pin_memory()
+    A_h = torch.empty((max(1, n_ev), wl.B), dtype=torch.float32).pin_memory()
+    h.prefill(tok_h, loss_h, p_h, q_h, acc_h if n_ev else None, A_h if n_ev else None)
+    e2e_t = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        h.prefill(tok_h, loss_h, p_h, q_h, acc_h if n_ev else None, A_h if n_ev else None)
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_total = sum(e2e_t)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = tokens / e2e_total
+    h2d = tok_h.numel() * 4 + (q_h.numel() * 4 if n_ev else 0)
+    d2h = loss_h.numel() * 4 + p_h.numel() * 4 + (n_ev * wl.B * 5 if n_ev else 0)
+
+    # roofline of the dominant class
+    flops = chunk_flops(wl)
+    byts = chunk_bytes(wl)
+    clk_sum = clk.summary()
+    dom_avg_s = dom_ms / 1e3 / max(1, dom_n)
+    launches_per_step_dom = dom_n / args.steps
+    if dom in flops:
+        per_launch = flops[dom] * wl.n_chunks / launches_per_step_dom
+        achieved = per_launch / dom_avg_s / 1e12
+        if wl.dtype == "fp32":
+            # fp32 FMA on the SIMT pipes: 148 SMs x 128 lanes x 2 FLOP x max SM clock
+            peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"}
+        else:
+            peak = pk["bf16_tflops_sustained"]
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": f"{pk['source']} bf16 sustained"}
+    else:
+        per_launch = byts.get(dom, 0.0) * wl.n_chunks / max(1e-9, launches_per_step_dom)
+        achieved = per_launch / dom_avg_s / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "peak_source": f"{pk['source']} copy bandwidth"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["traffic"] = None
+    roof["launches_per_step"] = launches_per_step_dom
+    roof["avg_launch_ms"] = dom_avg_s * 1e3
+    t_roof, fl_chunk, by_chunk = chunk_roofline_seconds(wl, pk)
+    chunk_frac = t_roof * wl.n_chunks / (total_ms / 1e3 / args.steps)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.dtype == "fp32" else "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "chunk": wl.chunk, "d": wl.d,
+                       "d_ff": wl.d_ff, "vocab": wl.vocab, "n_prefix": wl.n_prefix, "n_fast": wl.n_fast,
+                       "tokens_per_step": wl.B * wl.T * world, "l2": "flushed (512 MB write) before every step",
+                       "chunk_roofline_frac": chunk_frac, "chunk_roofline_ms": t_roof * 1e3,
+                       "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"],
+                                 "source": pk["source"]}},
+            "roofline": roof, "clocks": clk_sum,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "per_class_ms": {k: round(v[1], 3) for k, v in sorted(per_class.items(), key=lambda kv: -kv[1][1])}}
+    if rank == 0 and not args.no_cpu_baseline:
+        n_chunks = 12 if wl.name == C.CHUNKED_FP32.name else 2
+        n_seq = min(wl.B, 4)
+        v, dt = oracle_sample(wl, inp, n_seq, min(n_chunks, wl.n_chunks))
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"{n_seq} sequences x {min(n_chunks, wl.n_chunks)} chunks of "
+                                          f"{wl.name} ({dt:.1f} s)"}
+    h.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=C.CHUNKED_FP32.name, choices=list(C.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = C.BY_NAME[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, wl, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,758 @@
+// libttt C ABI: handle life cycle and the stream-ordered chunk sequencer.
+//
+// One chunk step ("End-to-End Test-Time Training for Long Context" review,
+// Method 3, eq. (5)) for all B sequences at once:
+//   embed + frozen prefix -> fast blocks forward (stash z, a, h) -> RMSNorm
+//   -> LM head -> fused CE (losses, dlogits in place) -> dy = dlogits U
+//   -> RMSNorm backward -> fast blocks backward (dW per sequence, dh)
+//   -> per-sequence global norm -> clip + SGD on the fp32 masters.
+// Every step runs in stream order on the caller's stream; the host only
+// synchronises at the end of a call that returns host data or a status flag.
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "engine.h"
+
+namespace ttt {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+ttt_status cuda_fail(cudaError_t e, const char* what, const char* file, int line) {
+  char buf[512];
+  snprintf(buf, sizeof buf, "%s: %s (%s:%d)", what, cudaGetErrorString(e), file, line);
+  set_error(buf);
+  return e == cudaErrorMemoryAllocation ? TTT_ERR_OOM : TTT_ERR_CUDA;
+}
+
+static ttt_status fail(ttt_status s, const std::string& msg) {
+  set_error(msg);
+  return s;
+}
+
+static bool is_device_ptr(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+template <typename T>
+static ttt_status dalloc(ttt_handle* h, T** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) return TTT_OK;
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TTT_ERR_OOM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+  }
+  h->allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return TTT_OK;
+}
+
+// Runs one launcher as kernel class `cls`, bracketing it with events when that
+// class is being profiled.
+template <class F>
+static ttt_status run(ttt_handle* h, int cls, cudaStream_t st, int nkernels, F&& f) {
+  const bool prof = h->prof_class == cls && h->ev_used + 2 <= (int)h->ev.size();
+  if (prof) TTT_CUDA(cudaEventRecord(h->ev[h->ev_used], st));
+  TTT_TRY(f());
+  if (prof) {
+    TTT_CUDA(cudaEventRecord(h->ev[h->ev_used + 1], st));
+    h->ev_used += 2;
+    h->prof_launches += 1;
+  }
+  h->launches += nkernels;
+  return TTT_OK;
+}
+
+static void* op_at(const ttt_handle* h, void* base, long long elems) {
+  return static_cast<char*>(base) + elems * (long long)h->esz;
+}
+
+static int gemm_count(const GemmDesc&) { return 1; }
+
+static ttt_status rungemm(ttt_handle* h, int cls, const GemmDesc& g, cudaStream_t st) {
+  return run(h, cls, st, gemm_count(g), [&] { return gemm(g, st); });
+}
+
+// ---------------------------------------------------------------- forward
+// Forward over B * tv.rows rows with the current (or committed) fast weights.
+// train: keep the stash for backward and turn logits into dlogits in place.
+// head_f32: write fp32 logits into logits32 (rows must be 1) instead of the CE.
+static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, bool train,
+                          float* losses, long long loss_ld, long long loss_off, bool head_f32,
+                          cudaStream_t st) {
+  TokView tv = tv_in;
+  tv.vocab = h->V;
+  tv.err = h->flag;
+  const int B = h->B, rows = tv.rows, M = B * rows, d = h->d, f = h->f, V = h->V;
+  const int dt = h->dtype;
+  void* Wop = committed ? h->Wcop : h->Wop;
+  void* cur_op = h->dm.n_prefix > 0 ? h->xop : h->hlvl[0];
+  TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(dt, B, tv, h->E, d, h->x32, cur_op, st); }));
+
+  for (int p = 0; p < h->dm.n_prefix; ++p) {
+    void* const* W = &h->prefix[(size_t)p * h->nm];
+    void* next_op = (p == h->dm.n_prefix - 1) ? h->hlvl[0] : h->xop;
+    if (h->dm.block_kind == TTT_BLOCK_GELU) {
+      GemmDesc g;
+      g.M = M; g.N = f; g.K = d; g.dtype = dt;
+      g.A = cur_op; g.lda = d; g.B = W[0]; g.ldb = d;
+      g.epi = EPI_GELU; g.out = nullptr; g.out2 = h->tmp_a; g.ldo2 = f;
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
+    } else {
+      GemmDesc g;
+      g.M = M; g.N = f; g.K = d; g.dtype = dt;
+      g.A = cur_op; g.lda = d; g.B = W[0]; g.ldb = d;
+      g.epi = EPI_STORE_F32; g.out = h->tmp_g; g.ldo = f;
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
+      g.B = W[1]; g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; g.out = h->tmp_a; g.ldo = f;
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
+    }
+    GemmDesc g2;
+    g2.M = M; g2.N = d; g2.K = f; g2.dtype = dt;
+    g2.A = h->tmp_a; g2.lda = f; g2.B = W[h->nm - 1]; g2.ldb = f;
+    g2.epi = EPI_RESID; g2.aux = h->x32; g2.ldx = d; g2.out = h->x32; g2.ldo = d;
+    g2.out2 = next_op; g2.ldo2 = d;
+    TTT_TRY(rungemm(h, K_GEMM_PREFIX, g2, st));
+    cur_op = next_op;
+  }
+
+  for (int l = 0; l < h->dm.n_fast; ++l) {
+    void* hin = h->hlvl[l];
+    void* a_out = train ? h->ast[l] : h->tmp_a;
+    void* next_op = (l + 1 < h->dm.n_fast) ? h->hlvl[l + 1] : nullptr;
+    const int s_down = h->slot_of[(size_t)l * h->nm + (h->nm - 1)];
+    if (h->dm.block_kind == TTT_BLOCK_GELU) {
+      const int s_up = h->slot_of[(size_t)l * h->nm + 0];
+      GemmDesc g;
+      g.M = rows; g.N = f; g.K = d; g.batch = B; g.dtype = dt;
+      g.A = hin; g.lda = d; g.sA = (long long)rows * d;
+      g.B = op_at(h, Wop, (long long)s_up * B * h->n); g.ldb = d; g.sB = h->n;
+      g.epi = EPI_GELU;
+      g.out = train ? h->zst[l] : nullptr; g.ldo = f; g.sO = (long long)rows * f;
+      g.out2 = a_out; g.ldo2 = f; g.sO2 = (long long)rows * f;
+      TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
+    } else {
+      void* const* W = &h->fastfrozen[(size_t)l * h->nm];
+      GemmDesc g;
+      g.M = M; g.N = f; g.K = d; g.dtype = dt;
+      g.A = hin; g.lda = d; g.B = W[0]; g.ldb = d;
+      g.epi = EPI_STORE_F32; g.out = h->tmp_g; g.ldo = f;
+      TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
+      g.B = W[1]; g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; g.out = a_out; g.ldo = f;
+      TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
+    }
+    GemmDesc g2;
+    g2.M = rows; g2.N = d; g2.K = f; g2.batch = B; g2.dtype = dt;
+    g2.A = a_out; g2.lda = f; g2.sA = (long long)rows * f;
+    g2.B = op_at(h, Wop, (long long)s_down * B * h->n); g2.ldb = f; g2.sB = h->n;
+    g2.epi = EPI_RESID; g2.aux = h->x32; g2.ldx = d; g2.sX = (long long)rows * d;
+    g2.out = h->x32; g2.ldo = d; g2.sO = (long long)rows * d;
+    g2.out2 = next_op; g2.ldo2 = d; g2.sO2 = (long long)rows * d;
+    TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g2, st));
+  }
+
+  TTT_TRY(run(h, K_RMSNORM_FWD, st, 1,
+              [&] { return launch_rmsnorm_fwd(dt, M, d, h->x32, h->dm.rms_eps, h->y, h->rstd, st); }));
+
+  GemmDesc gh;
+  gh.M = M; gh.N = V; gh.K = d; gh.dtype = dt;
+  gh.A = h->y; gh.lda = d; gh.B = h->U; gh.ldb = d;
+  if (head_f32) {
+    gh.epi = EPI_STORE_F32; gh.out = h->logits32; gh.ldo = V;
+    return rungemm(h, K_GEMM_HEAD, gh, st);
+  }
+  gh.epi = EPI_STORE; gh.out = h->logits; gh.ldo = V;
+  TTT_TRY(rungemm(h, K_GEMM_HEAD, gh, st));
+  const float scale = tv.n_valid > 0 ? 1.0f / (float)tv.n_valid : 0.0f;
+  return run(h, K_CE, st, 1, [&] {
+    return launch_ce(dt, B, tv, V, h->logits, V, scale, train, losses, loss_ld, loss_off, h->row_loss, st);
+  });
+}
+
+// ---------------------------------------------------------------- backward + update
+static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
+  const int B = h->B, M = B * rows, d = h->d, f = h->f, V = h->V, dt = h->dtype;
+  GemmDesc gy;
+  gy.M = M; gy.N = d; gy.K = V; gy.dtype = dt;
+  gy.A = h->logits; gy.lda = V; gy.B = h->U; gy.b_kmajor = false; gy.ldb = d;
+  gy.epi = EPI_STORE_F32; gy.out = h->dy32; gy.ldo = d;
+  TTT_TRY(rungemm(h, K_GEMM_HEAD_BWD, gy, st));
+  TTT_TRY(run(h, K_RMSNORM_BWD, st, 1, [&] {
+    return launch_rmsnorm_bwd(dt, M, d, h->x32, h->rstd, h->dy32, h->dh32, h->dhop, st);
+  }));
+
+  PartialSlots ps{};
+  long long poff = 0;
+  auto dw_gemm = [&](GemmDesc& g, int slot) -> ttt_status {
+    const int tiles = gemm_partial_tiles(g);
+    if (ps.n >= 16 || poff + (long long)tiles * B > h->partial_cap)
+      return fail(TTT_ERR_UNSUPPORTED, "too many gradient-norm partial slots");
+    g.epi = EPI_DW;
+    g.out = h->dW + (long long)slot * B * h->n; g.sO = h->n;
+    g.partials = h->partials + poff;
+    ps.off[ps.n] = poff;
+    ps.tiles[ps.n] = tiles;
+    ps.n++;
+    poff += (long long)tiles * B;
+    return rungemm(h, K_GEMM_DW, g, st);
+  };
+
+  for (int l = h->dm.n_fast - 1; l >= 0; --l) {
+    if (h->dm.block_kind == TTT_BLOCK_GELU) {
+      const int s1 = h->slot_of[(size_t)l * 2 + 0], s2 = h->slot_of[(size_t)l * 2 + 1];
+      // dW2 = dh^T a   [d, f], K = rows
+      GemmDesc g;
+      g.M = d; g.N = f; g.K = rows; g.batch = B; g.dtype = dt;
+      g.a_kmajor = false; g.A = h->dhop; g.lda = d; g.sA = (long long)rows * d;
+      g.b_kmajor = false; g.B = h->ast[l]; g.ldb = f; g.sB = (long long)rows * f;
+      g.ldo = f;
+      TTT_TRY(dw_gemm(g, s2));
+      // dz = (dh W2) * GELU'(z), in place over the z stash
+      GemmDesc gz;
+      gz.M = rows; gz.N = f; gz.K = d; gz.batch = B; gz.dtype = dt;
+      gz.A = h->dhop; gz.lda = d; gz.sA = (long long)rows * d;
+      gz.b_kmajor = false; gz.B = op_at(h, h->Wop, (long long)s2 * B * h->n); gz.ldb = f; gz.sB = h->n;
+      gz.epi = EPI_DGELU; gz.aux = h->zst[l]; gz.ldx = f; gz.sX = (long long)rows * f;
+      gz.out = h->zst[l]; gz.ldo = f; gz.sO = (long long)rows * f;
+      TTT_TRY(rungemm(h, K_GEMM_BWD_DX, gz, st));
+      // dW1 = dz^T h_in   [f, d]
+      GemmDesc g1;
+      g1.M = f; g1.N = d; g1.K = rows; g1.batch = B; g1.dtype = dt;
+      g1.a_kmajor = false; g1.A = h->zst[l]; g1.lda = f; g1.sA = (long long)rows * f;
+      g1.b_kmajor = false; g1.B = h->hlvl[l]; g1.ldb = d; g1.sB = (long long)rows * d;
+      g1.ldo = d;
+      TTT_TRY(dw_gemm(g1, s1));
+      if (l > 0) {
+        // dh_below = dh + dz W1
+        GemmDesc gb;
+        gb.M = rows; gb.N = d; gb.K = f; gb.batch = B; gb.dtype = dt;
+        gb.A = h->zst[l]; gb.lda = f; gb.sA = (long long)rows * f;
+        gb.b_kmajor = false; gb.B = op_at(h, h->Wop, (long long)s1 * B * h->n); gb.ldb = d; gb.sB = h->n;
+        gb.epi = EPI_RESID; gb.aux = h->dh32; gb.ldx = d; gb.sX = (long long)rows * d;
+        gb.out = h->dh32; gb.ldo = d; gb.sO = (long long)rows * d;
+        gb.out2 = h->dhop; gb.ldo2 = d; gb.sO2 = (long long)rows * d;
+        TTT_TRY(rungemm(h, K_GEMM_BWD_DX, gb, st));
+      }
+    } else {
+      const int sd = h->slot_of[(size_t)l * 3 + 2];
+      GemmDesc g;
+      g.M = d; g.N = f; g.K = rows; g.batch = B; g.dtype = dt;
+      g.a_kmajor = false; g.A = h->dhop; g.lda = d; g.sA = (long long)rows * d;
+      g.b_kmajor = false; g.B = h->ast[l]; g.ldb = f; g.sB = (long long)rows * f;
+      g.ldo = f;
+      TTT_TRY(dw_gemm(g, sd));
+    }
+  }
+  TTT_TRY(run(h, K_NORM, st, 1, [&] {
+    return launch_norm_finalize(B, ps, h->partials, h->hp.clip, h->scale, h->gnorm, h->flag, st);
+  }));
+  TTT_TRY(run(h, K_SGD, st, 1, [&] {
+    return launch_sgd_update(dt, h->nslots, B, h->n, h->W32, h->Wop, h->dW, h->scale, h->hp.eta, st);
+  }));
+  h->chunks_done++;
+  return TTT_OK;
+}
+
+static ttt_status chunk_step(ttt_handle* h, const TokView& tv, float* losses, long long loss_ld,
+                             long long loss_off, cudaStream_t st) {
+  TTT_TRY(forward(h, tv, false, true, losses, loss_ld, loss_off, false, st));
+  return backward_update(h, tv.rows, st);
+}
+
+// Settlement on held-out q [B, Lq] (device): writes A[B], accept[B].
+static ttt_status settle_event(ttt_handle* h, const int32_t* q, int Lq, float* A, uint8_t* acc,
+                               cudaStream_t st) {
+  TokView tv;
+  tv.tok = q; tv.tok_ld = Lq; tv.tok_off = 0; tv.rows = Lq; tv.n_valid = Lq - 1;
+  TTT_TRY(forward(h, tv, true, false, nullptr, 0, 0, false, st));
+  TTT_TRY(run(h, K_SETTLE, st, 1, [&] { return launch_seq_mean(h->B, Lq, Lq - 1, h->row_loss, h->Lc, st); }));
+  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, false, st));
+  TTT_TRY(run(h, K_SETTLE, st, 1, [&] { return launch_seq_mean(h->B, Lq, Lq - 1, h->row_loss, h->Lw, st); }));
+  return run(h, K_SETTLE, st, 2, [&] {
+    return launch_settle_apply(h->dtype, h->nslots, h->B, h->n, h->Lc, h->Lw, A, acc, h->W32, h->Wop,
+                               h->Wc32, h->Wcop, st);
+  });
+}
+
+static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t st) {
+  TokView tv;
+  tv.tok = h->pend; tv.tok_ld = h->b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 0;
+  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, true, st));
+  return run(h, K_OTHER, st, 1, [&] { return launch_softmax(h->B, h->V, h->logits32, p_out, st); });
+}
+
+static ttt_status reset_weights(ttt_handle* h, cudaStream_t st) {
+  TTT_TRY(run(h, K_OTHER, st, 1, [&] {
+    return launch_broadcast_w0(h->dtype, h->nslots, h->B, h->n, h->W0, h->W32, h->Wop, st);
+  }));
+  if (h->Wc32) {
+    TTT_TRY(run(h, K_OTHER, st, 1, [&] {
+      return launch_broadcast_w0(h->dtype, h->nslots, h->B, h->n, h->W0, h->Wc32, h->Wcop, st);
+    }));
+  }
+  h->pend_count = 0;
+  h->chunks_done = 0;
+  return TTT_OK;
+}
+
+// Wait for the stream and turn the device status word into a status code.
+static ttt_status finish(ttt_handle* h, cudaStream_t st) {
+  TTT_CUDA(cudaMemcpyAsync(h->flag_host, h->flag, 4, cudaMemcpyDeviceToHost, st));
+  TTT_CUDA(cudaStreamSynchronize(st));
+  if (*h->flag_host & 2) return fail(TTT_ERR_BAD_ARG, "token id outside [0, vocab)");
+  if (*h->flag_host & 1) return fail(TTT_ERR_NONFINITE, "non-finite gradient norm: update skipped");
+  return TTT_OK;
+}
+
+static ttt_status ensure_staging(ttt_handle* h, void** p, size_t* cap, size_t bytes) {
+  if (*cap >= bytes) return TTT_OK;
+  if (*p) {
+    for (auto& a : h->allocs)
+      if (a == *p) a = nullptr;
+    cudaFree(*p);
+    *p = nullptr;
+    *cap = 0;
+  }
+  void* q = nullptr;
+  TTT_TRY(dalloc(h, &q, bytes));
+  *p = q;
+  *cap = bytes;
+  return TTT_OK;
+}
+
+static ttt_status copy_in(ttt_handle* h, const void* src, void** stage, size_t* cap, size_t bytes,
+                          const void** dev, cudaStream_t st) {
+  if (is_device_ptr(src)) {
+    *dev = src;
+    return TTT_OK;
+  }
+  TTT_TRY(ensure_staging(h, stage, cap, bytes));
+  TTT_CUDA(cudaMemcpyAsync(*stage, src, bytes, cudaMemcpyHostToDevice, st));
+  *dev = *stage;
+  return TTT_OK;
+}
+
+}  // namespace ttt
+
+using namespace ttt;
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* ttt_status_string(ttt_status s) {
+  switch (s) {
+    case TTT_OK: return "ok";
+    case TTT_ERR_BAD_ARG: return "bad argument";
+    case TTT_ERR_BAD_SHAPE: return "bad shape";
+    case TTT_ERR_OOM: return "out of device memory";
+    case TTT_ERR_CUDA: return "CUDA error";
+    case TTT_ERR_NONFINITE: return "non-finite gradient norm (update skipped)";
+    case TTT_ERR_TIMEOUT: return "device wait timed out";
+    case TTT_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TTT_ERR_STATE: return "call out of order";
+  }
+  return "unknown status";
+}
+
+const char* ttt_last_error(void) { return g_last_error.c_str(); }
+
+static const char* kKClassNames[K_COUNT] = {
+    "embed", "gemm_prefix", "gemm_fast_fwd", "rmsnorm_fwd", "gemm_head", "ce_fused",
+    "gemm_head_bwd", "rmsnorm_bwd", "gemm_bwd_dx", "gemm_dw", "grad_norm", "clip_sgd_update",
+    "settle", "other"};
+
+const char* ttt_kernel_class_name(int c) { return (c >= 0 && c < K_COUNT) ? kKClassNames[c] : ""; }
+int ttt_kernel_class_count(void) { return K_COUNT; }
+
+ttt_status ttt_destroy(ttt_handle* h) {
+  if (!h) return TTT_OK;
+  for (void* p : h->allocs)
+    if (p) cudaFree(p);
+  for (auto e : h->ev) cudaEventDestroy(e);
+  if (h->flag_host) cudaFreeHost(h->flag_host);
+  delete h;
+  return TTT_OK;
+}
+
+ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_weights* w, ttt_handle** out) {
+  if (!dims || !hp || !w || !out) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_create");
+  *out = nullptr;
+  const ttt_dims& D = *dims;
+  if (D.d <= 0 || D.d_ff <= 0 || D.vocab <= 0 || D.n_prefix < 0 || D.n_fast < 1 || D.rms_eps < 0.0f)
+    return fail(TTT_ERR_BAD_ARG, "bad dims");
+  if (D.block_kind != TTT_BLOCK_GELU && D.block_kind != TTT_BLOCK_SWIGLU)
+    return fail(TTT_ERR_BAD_ARG, "bad block_kind");
+  if (D.dtype != TTT_DTYPE_FP32 && D.dtype != TTT_DTYPE_BF16) return fail(TTT_ERR_BAD_ARG, "bad dtype");
+  if (hp->chunk < 1 || hp->max_batch < 1 || hp->settle_every < 0 || hp->settle_len < 0 || hp->clip < 0.0f)
+    return fail(TTT_ERR_BAD_ARG, "bad hparams");
+  if (hp->settle_every > 0 && hp->settle_len < 2)
+    return fail(TTT_ERR_BAD_ARG, "settle_len must be >= 2 when settle_every > 0");
+  if (D.block_kind == TTT_BLOCK_GELU && D.fast_mask != (TTT_FAST_W1 | TTT_FAST_W2))
+    return fail(TTT_ERR_UNSUPPORTED, "GELU blocks run with both W1 and W2 fast (fast_mask 3)");
+  if (D.block_kind == TTT_BLOCK_SWIGLU && (D.fast_mask != TTT_FAST_WD || D.n_fast != 1))
+    return fail(TTT_ERR_UNSUPPORTED, "SwiGLU runs with one fast block whose down projection is fast");
+  if (!w->E || !w->U || (D.n_prefix > 0 && !w->prefix) || !w->fast)
+    return fail(TTT_ERR_BAD_ARG, "null weight pointer");
+
+  ttt_handle* h = new ttt_handle();
+  h->dm = D;
+  h->hp = *hp;
+  h->B = hp->max_batch; h->b = hp->chunk; h->d = D.d; h->f = D.d_ff; h->V = D.vocab;
+  h->nm = D.block_kind == TTT_BLOCK_GELU ? 2 : 3;
+  h->n = (long long)D.d * D.d_ff;
+  h->dtype = D.dtype;
+  h->esz = D.dtype == TTT_DTYPE_BF16 ? 2 : 4;
+  h->slot_of.assign((size_t)D.n_fast * h->nm, -1);
+  for (int l = 0; l < D.n_fast; ++l)
+    for (int m = 0; m < h->nm; ++m) {
+      const int bit = (D.block_kind == TTT_BLOCK_GELU) ? (1 << m) : (m == 0 ? 1 : (m == 1 ? 4 : 2));
+      if (D.fast_mask & bit) h->slot_of[(size_t)l * h->nm + m] = h->nslots++;
+    }
+
+  auto bail = [&](ttt_status s) { ttt_destroy(h); return s; };
+  const int B = h->B, d = h->d, f = h->f, V = h->V;
+  const size_t es = h->esz;
+  cudaStream_t st = 0;
+
+  // ---- weights
+  float* stage = nullptr;
+  const size_t big = (size_t)V * d > (size_t)h->n ? (size_t)V * d : (size_t)h->n;
+  ttt_status s;
+  if ((s = dalloc(h, &stage, big * 4)) != TTT_OK) return bail(s);
+  auto upload = [&](const float* src, size_t count, void* dst) -> ttt_status {
+    if (!src) return fail(TTT_ERR_BAD_ARG, "null weight matrix");
+    TTT_CUDA(cudaMemcpy(stage, src, count * 4, cudaMemcpyDefault));
+    TTT_TRY(launch_cast(h->dtype, (long long)count, stage, dst, st));
+    TTT_CUDA(cudaStreamSynchronize(st));
+    return TTT_OK;
+  };
+  if ((s = dalloc(h, &h->E, (size_t)V * d * es)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->U, (size_t)V * d * es)) != TTT_OK) return bail(s);
+  if ((s = upload(w->E, (size_t)V * d, h->E)) != TTT_OK) return bail(s);
+  if ((s = upload(w->U, (size_t)V * d, h->U)) != TTT_OK) return bail(s);
+  h->prefix.assign((size_t)D.n_prefix * h->nm, nullptr);
+  for (size_t i = 0; i < h->prefix.size(); ++i) {
+    if ((s = dalloc(h, &h->prefix[i], (size_t)h->n * es)) != TTT_OK) return bail(s);
+    if ((s = upload(w->prefix[i], (size_t)h->n, h->prefix[i])) != TTT_OK) return bail(s);
+  }
+  h->fastfrozen.assign((size_t)D.n_fast * h->nm, nullptr);
+  if ((s = dalloc(h, &h->W0, (size_t)h->nslots * h->n * 4)) != TTT_OK) return bail(s);
+  for (size_t i = 0; i < h->fastfrozen.size(); ++i) {
+    const int slot = h->slot_of[i];
+    if (slot >= 0) {
+      if (!w->fast[i]) return bail(fail(TTT_ERR_BAD_ARG, "null fast weight matrix"));
+      cudaError_t e = cudaMemcpy(h->W0 + (size_t)slot * h->n, w->fast[i], (size_t)h->n * 4, cudaMemcpyDefault);
+      if (e != cudaSuccess) return bail(cuda_fail(e, "upload W0", __FILE__, __LINE__));
+    } else {
+      if ((s = dalloc(h, &h->fastfrozen[i], (size_t)h->n * es)) != TTT_OK) return bail(s);
+      if ((s = upload(w->fast[i], (size_t)h->n, h->fastfrozen[i])) != TTT_OK) return bail(s);
+    }
+  }
+  const size_t arena = (size_t)h->nslots * B * h->n;
+  if ((s = dalloc(h, &h->W32, arena * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->Wop, arena * es)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->dW, arena * 4)) != TTT_OK) return bail(s);
+  // the committed copy serves Settlement (prefill events and ttt_settle)
+  if ((s = dalloc(h, &h->Wc32, arena * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->Wcop, arena * es)) != TTT_OK) return bail(s);
+
+  // ---- workspace
+  int rows_max = h->b;
+  if (hp->settle_len > rows_max) rows_max = hp->settle_len;
+  if (rows_max < 2) rows_max = 2;
+  h->Mmax = B * rows_max;
+  const size_t Mm = (size_t)h->Mmax;
+  if ((s = dalloc(h, &h->x32, Mm * d * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->xop, Mm * d * es)) != TTT_OK) return bail(s);
+  h->hlvl.assign(D.n_fast, nullptr);
+  h->zst.assign(D.n_fast, nullptr);
+  h->ast.assign(D.n_fast, nullptr);
+  for (int l = 0; l < D.n_fast; ++l) {
+    if ((s = dalloc(h, &h->hlvl[l], Mm * d * es)) != TTT_OK) return bail(s);
+    if (D.block_kind == TTT_BLOCK_GELU)
+      if ((s = dalloc(h, &h->zst[l], Mm * f * es)) != TTT_OK) return bail(s);
+    if ((s = dalloc(h, &h->ast[l], Mm * f * es)) != TTT_OK) return bail(s);
+  }
+  if ((s = dalloc(h, &h->tmp_a, Mm * f * es)) != TTT_OK) return bail(s);
+  if (D.block_kind == TTT_BLOCK_SWIGLU)
+    if ((s = dalloc(h, &h->tmp_g, Mm * f * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->y, Mm * d * es)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->rstd, Mm * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->logits, Mm * V * es)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->row_loss, Mm * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->dy32, Mm * d * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->dh32, Mm * d * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->dhop, Mm * d * es)) != TTT_OK) return bail(s);
+  // partial sums of squares: at most one per 64x64 output tile per matrix and sequence
+  h->partial_cap = (long long)h->nslots * B * ceil_div(d, 64) * ceil_div(f, 64);
+  if ((s = dalloc(h, &h->partials, (size_t)h->partial_cap * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->scale, (size_t)B * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->gnorm, (size_t)B * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->flag, 4)) != TTT_OK) return bail(s);
+  if (cudaMallocHost(&h->flag_host, 4) != cudaSuccess) {
+    cudaGetLastError();
+    return bail(fail(TTT_ERR_OOM, "cudaMallocHost"));
+  }
+  if ((s = dalloc(h, &h->logits32, (size_t)B * V * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->p_dev, (size_t)B * V * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->Lc, (size_t)B * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->Lw, (size_t)B * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->pend, (size_t)B * (h->b + 1) * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->x_dev, (size_t)B * 4)) != TTT_OK) return bail(s);
+  if ((s = reset_weights(h, st)) != TTT_OK) return bail(s);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "create sync", __FILE__, __LINE__));
+  // the weight staging buffer is no longer needed
+  for (auto& a : h->allocs)
+    if (a == stage) a = nullptr;
+  cudaFree(stage);
+  h->launches = 0;
+  *out = h;
+  return TTT_OK;
+}
+
+ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float* losses, float* p_next,
+                       const int32_t* settle_q, int Lq, uint8_t* accept, float* A, ttt_stream stream) {
+  if (!h || !tokens || !losses) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_prefill");
+  if (B != h->B || T < 1) return fail(TTT_ERR_BAD_SHAPE, "B must equal max_batch and T >= 1");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int b = h->b, n_full = T / b, rem = T % b;
+  const int n_events = h->hp.settle_every > 0 ? n_full / h->hp.settle_every : 0;
+  if (n_events > 0) {
+    if (!settle_q) return fail(TTT_ERR_BAD_ARG, "settle_q is required when Settlement events occur");
+    if (Lq != h->hp.settle_len) return fail(TTT_ERR_BAD_SHAPE, "Lq must equal settle_len");
+  }
+  h->launches = 0;
+  h->ev_used = 0;
+  h->prof_launches = 0;
+
+  const int32_t* tok = nullptr;
+  TTT_TRY(copy_in(h, tokens, (void**)&h->tok_dev, &h->tok_cap, (size_t)B * (T + 1) * 4, (const void**)&tok, st));
+  const int32_t* q = nullptr;
+  if (n_events > 0)
+    TTT_TRY(copy_in(h, settle_q, (void**)&h->q_dev, &h->q_cap, (size_t)n_events * B * Lq * 4,
+                    (const void**)&q, st));
+  const bool loss_host = !is_device_ptr(losses);
+  float* loss_d = losses;
+  if (loss_host) {
+    TTT_TRY(ensure_staging(h, (void**)&h->loss_dev, &h->loss_cap, (size_t)B * T * 4));
+    loss_d = h->loss_dev;
+  }
+  if (n_events > 0) {
+    TTT_TRY(ensure_staging(h, (void**)&h->A_dev, &h->A_cap, (size_t)n_events * B * 4));
+    TTT_TRY(ensure_staging(h, (void**)&h->acc_dev, &h->acc_cap, (size_t)n_events * B));
+  }
+
+  TTT_TRY(reset_weights(h, st));
+  TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
+  for (int i = 0; i < n_full; ++i) {
+    TokView tv;
+    tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = (long long)i * b; tv.rows = b; tv.n_valid = b;
+    TTT_TRY(chunk_step(h, tv, loss_d, T, (long long)i * b, st));
+    if (h->hp.settle_every > 0 && (i + 1) % h->hp.settle_every == 0) {
+      const int e = (i + 1) / h->hp.settle_every - 1;
+      TTT_TRY(settle_event(h, q + (size_t)e * B * Lq, Lq, h->A_dev + (size_t)e * B, h->acc_dev + (size_t)e * B, st));
+    }
+  }
+  if (rem > 0) {
+    TokView tv;
+    tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = (long long)n_full * b; tv.rows = rem; tv.n_valid = rem;
+    TTT_TRY(forward(h, tv, false, false, loss_d, T, (long long)n_full * b, false, st));
+  }
+  // pending decode buffer: tokens x_{n_full b} .. x_T
+  TTT_CUDA(cudaMemcpy2DAsync(h->pend, (size_t)(b + 1) * 4, tok + (size_t)n_full * b, (size_t)(T + 1) * 4,
+                             (size_t)(rem + 1) * 4, B, cudaMemcpyDeviceToDevice, st));
+  h->pend_count = rem;
+  h->has_context = true;
+  if (p_next) {
+    const bool dev = is_device_ptr(p_next);
+    TTT_TRY(p_next_from_pending(h, dev ? p_next : h->p_dev, st));
+    if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
+  }
+  if (loss_host) TTT_CUDA(cudaMemcpyAsync(losses, loss_d, (size_t)B * T * 4, cudaMemcpyDeviceToHost, st));
+  if (n_events > 0 && A) TTT_CUDA(cudaMemcpyAsync(A, h->A_dev, (size_t)n_events * B * 4, cudaMemcpyDefault, st));
+  if (n_events > 0 && accept)
+    TTT_CUDA(cudaMemcpyAsync(accept, h->acc_dev, (size_t)n_events * B, cudaMemcpyDefault, st));
+  return finish(h, st);
+}
+
+ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, float* loss, ttt_stream stream) {
+  if (!h || !x_new || !p_next) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_decode_step");
+  if (!h->has_context) return fail(TTT_ERR_STATE, "decode before prefill");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int B = h->B, b = h->b;
+  h->launches = 0;
+  // x_new -> pend[s][pend_count + 1]
+  TTT_CUDA(cudaMemcpy2DAsync(h->pend + h->pend_count + 1, (size_t)(b + 1) * 4, x_new, 4, 4, B,
+                             is_device_ptr(x_new) ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+  TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
+  // loss of (x_prev -> x_new) with the weights that score it
+  if (loss) {
+    TokView tv;
+    tv.tok = h->pend; tv.tok_ld = b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 1;
+    const bool dev = is_device_ptr(loss);
+    float* dst = dev ? loss : h->Lc;
+    TTT_TRY(forward(h, tv, false, false, dst, 1, 0, false, st));
+    if (!dev) TTT_CUDA(cudaMemcpyAsync(loss, dst, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
+  }
+  h->pend_count++;
+  if (h->pend_count == b) {
+    TokView tv;
+    tv.tok = h->pend; tv.tok_ld = b + 1; tv.tok_off = 0; tv.rows = b; tv.n_valid = b;
+    TTT_TRY(chunk_step(h, tv, nullptr, 0, 0, st));
+    TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_pending_shift(B, b, h->pend, st); }));
+    h->pend_count = 0;
+  }
+  const bool dev = is_device_ptr(p_next);
+  TTT_TRY(p_next_from_pending(h, dev ? p_next : h->p_dev, st));
+  if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
+  return finish(h, st);
+}
+
+ttt_status ttt_settle(ttt_handle* h, const int32_t* q, int Lq, uint8_t* accept, float* A, ttt_stream stream) {
+  if (!h || !q || !accept || !A) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_settle");
+  if (Lq != h->hp.settle_len || Lq < 2) return fail(TTT_ERR_BAD_SHAPE, "Lq must equal settle_len (>= 2)");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int B = h->B;
+  h->launches = 0;
+  const int32_t* qd = nullptr;
+  TTT_TRY(copy_in(h, q, (void**)&h->q_dev, &h->q_cap, (size_t)B * Lq * 4, (const void**)&qd, st));
+  TTT_TRY(ensure_staging(h, (void**)&h->A_dev, &h->A_cap, (size_t)B * 4));
+  TTT_TRY(ensure_staging(h, (void**)&h->acc_dev, &h->acc_cap, (size_t)B));
+  TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
+  TTT_TRY(settle_event(h, qd, Lq, h->A_dev, h->acc_dev, st));
+  TTT_CUDA(cudaMemcpyAsync(A, h->A_dev, (size_t)B * 4, cudaMemcpyDefault, st));
+  TTT_CUDA(cudaMemcpyAsync(accept, h->acc_dev, (size_t)B, cudaMemcpyDefault, st));
+  return finish(h, st);
+}
+
+ttt_status ttt_get_fast_weights(ttt_handle* h, int seq, int block, int mat, float* dst, ttt_stream stream) {
+  if (!h || !dst) return fail(TTT_ERR_BAD_ARG, "null argument");
+  if (seq < 0 || seq >= h->B || block < 0 || block >= h->dm.n_fast || mat < 0 || mat >= h->nm)
+    return fail(TTT_ERR_BAD_ARG, "index out of range");
+  const int slot = h->slot_of[(size_t)block * h->nm + mat];
+  if (slot < 0) return fail(TTT_ERR_BAD_ARG, "that matrix is not a fast weight");
+  cudaStream_t st = (cudaStream_t)stream;
+  TTT_CUDA(cudaMemcpyAsync(dst, h->W32 + ((size_t)slot * h->B + seq) * h->n, (size_t)h->n * 4,
+                           cudaMemcpyDefault, st));
+  TTT_CUDA(cudaStreamSynchronize(st));
+  return TTT_OK;
+}
+
+ttt_status ttt_reset(ttt_handle* h, ttt_stream stream) {
+  if (!h) return fail(TTT_ERR_BAD_ARG, "null handle");
+  cudaStream_t st = (cudaStream_t)stream;
+  TTT_TRY(reset_weights(h, st));
+  h->has_context = false;
+  TTT_CUDA(cudaStreamSynchronize(st));
+  return TTT_OK;
+}
+
+// ---- checkpoint blob: header, W32, Wc32, pending tokens
+struct StateHeader {
+  uint64_t magic;
+  int32_t d, d_ff, vocab, n_fast, block_kind, fast_mask, dtype, B, b, nslots;
+  int32_t pend_count, has_context;
+  int64_t chunks_done;
+};
+static const uint64_t kStateMagic = 0x7474745354415445ULL;  // "tttSTATE"
+
+ttt_status ttt_state_size(ttt_handle* h, size_t* bytes) {
+  if (!h || !bytes) return fail(TTT_ERR_BAD_ARG, "null argument");
+  const size_t arena = (size_t)h->nslots * h->B * h->n * 4;
+  *bytes = sizeof(StateHeader) + 2 * arena + (size_t)h->B * (h->b + 1) * 4;
+  return TTT_OK;
+}
+
+ttt_status ttt_get_state(ttt_handle* h, void* dst, size_t bytes, ttt_stream stream) {
+  size_t need = 0;
+  TTT_TRY(ttt_state_size(h, &need));
+  if (!dst) return fail(TTT_ERR_BAD_ARG, "null dst");
+  if (bytes != need) return fail(TTT_ERR_BAD_SHAPE, "state size mismatch");
+  cudaStream_t st = (cudaStream_t)stream;
+  StateHeader hd{kStateMagic, h->d, h->f, h->V, h->dm.n_fast, h->dm.block_kind, h->dm.fast_mask, h->dtype,
+                 h->B, h->b, h->nslots, h->pend_count, h->has_context ? 1 : 0, h->chunks_done};
+  char* p = static_cast<char*>(dst);
+  memcpy(p, &hd, sizeof hd);
+  p += sizeof hd;
+  const size_t arena = (size_t)h->nslots * h->B * h->n * 4;
+  TTT_CUDA(cudaMemcpyAsync(p, h->W32, arena, cudaMemcpyDefault, st));
+  TTT_CUDA(cudaMemcpyAsync(p + arena, h->Wc32, arena, cudaMemcpyDefault, st));
+  TTT_CUDA(cudaMemcpyAsync(p + 2 * arena, h->pend, (size_t)h->B * (h->b + 1) * 4, cudaMemcpyDefault, st));
+  TTT_CUDA(cudaStreamSynchronize(st));
+  return TTT_OK;
+}
+
+ttt_status ttt_set_state(ttt_handle* h, const void* src, size_t bytes, ttt_stream stream) {
+  size_t need = 0;
+  TTT_TRY(ttt_state_size(h, &need));
+  if (!src) return fail(TTT_ERR_BAD_ARG, "null src");
+  if (bytes != need) return fail(TTT_ERR_BAD_SHAPE, "state size mismatch");
+  StateHeader hd;
+  memcpy(&hd, src, sizeof hd);
+  if (hd.magic != kStateMagic || hd.d != h->d || hd.d_ff != h->f || hd.vocab != h->V ||
+      hd.n_fast != h->dm.n_fast || hd.block_kind != h->dm.block_kind || hd.fast_mask != h->dm.fast_mask ||
+      hd.dtype != h->dtype || hd.B != h->B || hd.b != h->b || hd.nslots != h->nslots ||
+      hd.pend_count < 0 || hd.pend_count >= h->b)
+    return fail(TTT_ERR_BAD_SHAPE, "state blob does not match this handle");
+  cudaStream_t st = (cudaStream_t)stream;
+  const char* p = static_cast<const char*>(src) + sizeof hd;
+  const size_t arena = (size_t)h->nslots * h->B * h->n * 4;
+  TTT_CUDA(cudaMemcpyAsync(h->W32, p, arena, cudaMemcpyDefault, st));
+  TTT_CUDA(cudaMemcpyAsync(h->Wc32, p + arena, arena, cudaMemcpyDefault, st));
+  TTT_CUDA(cudaMemcpyAsync(h->pend, p + 2 * arena, (size_t)h->B * (h->b + 1) * 4, cudaMemcpyDefault, st));
+  const long long total = (long long)h->nslots * h->B * h->n;
+  TTT_TRY(launch_cast(h->dtype, total, h->W32, h->Wop, st));
+  TTT_TRY(launch_cast(h->dtype, total, h->Wc32, h->Wcop, st));
+  TTT_CUDA(cudaStreamSynchronize(st));
+  h->pend_count = hd.pend_count;
+  h->has_context = hd.has_context != 0;
+  h->chunks_done = hd.chunks_done;
+  return TTT_OK;
+}
+
+ttt_status ttt_profile_enable(ttt_handle* h, int kernel_class) {
+  if (!h || kernel_class < -1 || kernel_class >= K_COUNT) return fail(TTT_ERR_BAD_ARG, "bad kernel class");
+  h->prof_class = kernel_class;
+  if (kernel_class >= 0 && h->ev.empty()) {
+    h->ev.resize(8192);
+    for (auto& e : h->ev) TTT_CUDA(cudaEventCreate(&e));
+  }
+  h->ev_used = 0;
+  h->prof_launches = 0;
+  return TTT_OK;
+}
+
+ttt_status ttt_profile_read(ttt_handle* h, int* launches, double* total_ms) {
+  if (!h || !launches || !total_ms) return fail(TTT_ERR_BAD_ARG, "null argument");
+  double tot = 0.0;
+  for (int i = 0; i + 1 < h->ev_used; i += 2) {
+    TTT_CUDA(cudaEventSynchronize(h->ev[i + 1]));
+    float ms = 0.0f;
+    TTT_CUDA(cudaEventElapsedTime(&ms, h->ev[i], h->ev[i + 1]));
+    tot += ms;
+  }
+  *launches = h->prof_launches;
+  *total_ms = tot;
+  h->ev_used = 0;
+  h->prof_launches = 0;
+  return TTT_OK;
+}
+
+ttt_status ttt_last_launch_count(ttt_handle* h, long long* launches) {
+  if (!h || !launches) return fail(TTT_ERR_BAD_ARG, "null argument");
+  *launches = h->launches;
+  return TTT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// The libttt handle and the chunk-step sequencer (host side).
+#pragma once
+
+#include <vector>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "kernels.h"
+
+// Kernel classes for launch accounting and per-class timing.
+enum KClass {
+  K_EMBED = 0, K_GEMM_PREFIX, K_GEMM_FAST_FWD, K_RMSNORM_FWD, K_GEMM_HEAD, K_CE, K_GEMM_HEAD_BWD,
+  K_RMSNORM_BWD, K_GEMM_BWD_DX, K_GEMM_DW, K_NORM, K_SGD, K_SETTLE, K_OTHER, K_COUNT
+};
+
+struct ttt_handle {
+  ttt_dims dm{};
+  ttt_hparams hp{};
+  int B = 0, b = 0, d = 0, f = 0, V = 0;
+  int nm = 0;             // matrices per block (2 GELU, 3 SwiGLU)
+  int nslots = 0;         // fast matrices in total (arena slots)
+  long long n = 0;        // elements of one matrix (d * d_ff)
+  int dtype = 0;
+  size_t esz = 4;         // operand element size
+  std::vector<int> slot_of;   // [n_fast * nm] -> arena slot or -1
+
+  // frozen weights (operand type)
+  void* E = nullptr;
+  void* U = nullptr;
+  std::vector<void*> prefix;       // [n_prefix * nm]
+  std::vector<void*> fastfrozen;   // [n_fast * nm], null where fast
+
+  // fast weights: arenas [slot][B][n]
+  float* W0 = nullptr;     // [slot][n]
+  float* W32 = nullptr;
+  void* Wop = nullptr;
+  float* Wc32 = nullptr;
+  void* Wcop = nullptr;
+  float* dW = nullptr;
+
+  // chunk workspace for up to Mmax rows
+  int Mmax = 0;
+  float* x32 = nullptr;
+  void* xop = nullptr;
+  std::vector<void*> hlvl, zst, ast;
+  void* tmp_a = nullptr;
+  float* tmp_g = nullptr;
+  void* y = nullptr;
+  float* rstd = nullptr;
+  void* logits = nullptr;
+  float* row_loss = nullptr;
+  float* dy32 = nullptr;
+  float* dh32 = nullptr;
+  void* dhop = nullptr;
+  float* partials = nullptr;
+  long long partial_cap = 0;
+  ttt::PartialSlots pslots{};
+  float* scale = nullptr;
+  float* gnorm = nullptr;
+  int* flag = nullptr;
+  int* flag_host = nullptr;
+  float* logits32 = nullptr;
+  float* p_dev = nullptr;
+  float* Lc = nullptr;
+  float* Lw = nullptr;
+
+  // staging for host-side inputs and outputs
+  int32_t* tok_dev = nullptr; size_t tok_cap = 0;
+  float* loss_dev = nullptr; size_t loss_cap = 0;
+  int32_t* q_dev = nullptr; size_t q_cap = 0;
+  float* A_dev = nullptr; size_t A_cap = 0;
+  uint8_t* acc_dev = nullptr; size_t acc_cap = 0;
+  int32_t* x_dev = nullptr;
+
+  // decoding
+  int32_t* pend = nullptr;     // [B][b+1]
+  int pend_count = 0;
+  bool has_context = false;
+  long long chunks_done = 0;
+
+  // accounting
+  long long launches = 0;
+  int prof_class = -1;
+  std::vector<cudaEvent_t> ev;
+  int ev_used = 0;
+  int prof_launches = 0;
+
+  std::vector<void*> allocs;
+};

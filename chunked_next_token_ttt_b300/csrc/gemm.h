@@ -1,0 +1,42 @@
+// Internal GEMM interface of libttt: C[M, N] = sum_k A(m, k) B(n, k), batched,
+// with the fused epilogues the TTT chunk step needs.
+#pragma once
+
+#include "common.cuh"
+
+namespace ttt {
+
+enum EpiKind {
+  EPI_STORE = 0,   // out(op type) = acc
+  EPI_STORE_F32,   // out(float) = acc
+  EPI_GELU,        // out(op) = z = acc (stash), out2(op) = GELU(z)
+  EPI_RESID,       // out(float) = aux(float) + acc; out2(op) = same, if non-null
+  EPI_SWIGLU,      // out(op) = silu(aux(float)) * acc
+  EPI_DGELU,       // out(op) = acc * GELU'(aux(op))
+  EPI_DW,          // out(float) = acc; partials += per-tile sum of acc^2
+};
+
+struct GemmDesc {
+  int M = 0, N = 0, K = 0, batch = 1;
+  int dtype = TTT_DTYPE_FP32;      // operand element type of A and B
+  bool a_kmajor = true;            // A(m,k) at A[m*lda + k] (else A[k*lda + m])
+  bool b_kmajor = true;            // B(n,k) at B[n*ldb + k] (else B[k*ldb + n])
+  const void* A = nullptr; long long lda = 0, sA = 0;   // strides in elements
+  const void* B = nullptr; long long ldb = 0, sB = 0;
+  EpiKind epi = EPI_STORE;
+  void* out = nullptr; long long ldo = 0, sO = 0;
+  void* out2 = nullptr; long long ldo2 = 0, sO2 = 0;
+  const void* aux = nullptr; long long ldx = 0, sX = 0;
+  float* partials = nullptr;       // EPI_DW: [batch][gemm_partial_tiles()]
+};
+
+// Which implementation ran a GEMM (for launch accounting and tests).
+enum GemmImpl { GEMM_IMPL_SIMT = 0, GEMM_IMPL_TC = 1 };
+
+// Number of per-batch partial slots an EPI_DW launch writes.
+int gemm_partial_tiles(const GemmDesc& g);
+ttt_status gemm(const GemmDesc& g, cudaStream_t st);
+ttt_status gemm_simt(const GemmDesc& g, cudaStream_t st);
+int gemm_simt_partial_tiles(const GemmDesc& g);
+
+}  // namespace ttt

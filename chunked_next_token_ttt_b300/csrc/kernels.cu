@@ -1,0 +1,380 @@
+// Non-GEMM kernels of the TTT chunk step: embedding gather, RMSNorm forward
+// and backward, the fused softmax cross-entropy (loss + dlogits in place),
+// the per-sequence global-norm reduction, clip+SGD on the fp32 masters, and
+// the Settlement helpers.  All are HBM-bound row or elementwise kernels.
+#include <cfloat>
+
+#include "kernels.h"
+
+namespace ttt {
+namespace {
+
+template <typename OpT>
+__global__ void embed_kernel(TokView tv, const OpT* __restrict__ E, int d, float* __restrict__ h32,
+                             OpT* __restrict__ hop) {
+  const int m = blockIdx.x;
+  const int s = m / tv.rows, j = m % tv.rows;
+  int x = tv.tok[s * tv.tok_ld + tv.tok_off + j];
+  if ((unsigned)x >= (unsigned)tv.vocab) {
+    if (threadIdx.x == 0) atomicOr(tv.err, 2);
+    x = 0;
+  }
+  const OpT* src = E + (long long)x * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float v = to_f(src[c]);
+    h32[(long long)m * d + c] = v;
+    if (hop) hop[(long long)m * d + c] = from_f<OpT>(v);
+  }
+}
+
+template <typename OpT>
+__global__ void rmsnorm_fwd_kernel(int d, const float* __restrict__ x, float eps, OpT* __restrict__ y,
+                                   float* __restrict__ rstd) {
+  __shared__ float red[32];
+  const long long m = blockIdx.x;
+  const float* xr = x + m * d;
+  float sq = 0.0f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) sq += xr[c] * xr[c];
+  sq = block_sum(sq, red);
+  const float r = rsqrtf(sq / d + eps);
+  if (threadIdx.x == 0) rstd[m] = r;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) y[m * d + c] = from_f<OpT>(xr[c] * r);
+}
+
+template <typename OpT>
+__global__ void rmsnorm_bwd_kernel(int d, const float* __restrict__ x, const float* __restrict__ rstd,
+                                   const float* __restrict__ dy, float* __restrict__ dx32,
+                                   OpT* __restrict__ dxop) {
+  __shared__ float red[32];
+  const long long m = blockIdx.x;
+  const float r = rstd[m];
+  const float* xr = x + m * d;
+  const float* dyr = dy + m * d;
+  float dot = 0.0f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) dot += xr[c] * r * dyr[c];
+  dot = block_sum(dot, red) / d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float v = r * (dyr[c] - xr[c] * r * dot);
+    dx32[m * d + c] = v;
+    if (dxop) dxop[m * d + c] = from_f<OpT>(v);
+  }
+}
+
+// Combine two online-softmax partial states (max, sum of exp(x - max)).
+__device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
+  if (m2 > m) {
+    s = s * __expf(m - m2) + s2;
+    m = m2;
+  } else if (m2 > -FLT_MAX) {
+    s += s2 * __expf(m2 - m);
+  }
+}
+
+template <typename OpT>
+__global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long ldl, float scale,
+                          bool grad, float* __restrict__ losses, long long loss_ld, long long loss_off,
+                          float* __restrict__ row_loss) {
+  __shared__ float sm_m[32], sm_s[32];
+  const int m = blockIdx.x;
+  const int s = m / tv.rows, j = m % tv.rows;
+  const bool valid = j < tv.n_valid;
+  OpT* row = logits + (long long)m * ldl;
+  if (!valid) {
+    if (grad)
+      for (int v = threadIdx.x; v < V; v += blockDim.x) row[v] = from_f<OpT>(0.0f);
+    return;
+  }
+  int tgt = tv.tok[s * tv.tok_ld + tv.tok_off + j + 1];
+  if ((unsigned)tgt >= (unsigned)V) {
+    if (threadIdx.x == 0) atomicOr(tv.err, 2);
+    tgt = 0;
+  }
+  float mx = -FLT_MAX, se = 0.0f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = to_f(row[v]);
+    if (x > mx) {
+      se = se * __expf(mx - x) + 1.0f;
+      mx = x;
+    } else {
+      se += __expf(x - mx);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, se, o);
+    lse_combine(mx, se, m2, s2);
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) { sm_m[wid] = mx; sm_s[wid] = se; }
+  __syncthreads();
+  if (wid == 0) {
+    mx = lane < nw ? sm_m[lane] : -FLT_MAX;
+    se = lane < nw ? sm_s[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, se, o);
+      lse_combine(mx, se, m2, s2);
+    }
+    if (lane == 0) { sm_m[0] = mx; sm_s[0] = se; }
+  }
+  __syncthreads();
+  const float lse = sm_m[0] + logf(sm_s[0]);
+  if (threadIdx.x == 0) {
+    const float loss = lse - to_f(row[tgt]);
+    if (losses) losses[s * loss_ld + loss_off + j] = loss;
+    if (row_loss) row_loss[m] = loss;
+  }
+  if (!grad) return;
+  __syncthreads();   // the target logit is read above before being overwritten
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float p = __expf(to_f(row[v]) - lse);
+    row[v] = from_f<OpT>((p - (v == tgt ? 1.0f : 0.0f)) * scale);
+  }
+}
+
+__global__ void norm_finalize_kernel(PartialSlots ps, const float* __restrict__ partials, float clip,
+                                     float* __restrict__ scale, float* __restrict__ norm,
+                                     int* __restrict__ flag) {
+  __shared__ float red[32];
+  const int s = blockIdx.x;
+  float acc = 0.0f;
+  for (int k = 0; k < ps.n; ++k) {
+    const float* p = partials + ps.off[k] + (long long)s * ps.tiles[k];
+    for (int t = threadIdx.x; t < ps.tiles[k]; t += blockDim.x) acc += p[t];
+  }
+  acc = block_sum(acc, red);
+  if (threadIdx.x == 0) {
+    const float n = sqrtf(acc);
+    float sc = 1.0f;
+    if (!isfinite(n)) {
+      sc = 0.0f;
+      atomicOr(flag, 1);
+    } else if (clip > 0.0f) {
+      sc = fminf(1.0f, clip / (n + 1e-6f));
+    }
+    scale[s] = sc;
+    if (norm) norm[s] = n;
+  }
+}
+
+template <typename OpT>
+__global__ void sgd_update_kernel(long long total, int B, long long n, float* __restrict__ W32,
+                                  OpT* __restrict__ Wop, const float* __restrict__ dW,
+                                  const float* __restrict__ scale, float eta) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int s = (int)((i / n) % B);
+    const float w = W32[i] - eta * scale[s] * dW[i];
+    W32[i] = w;
+    Wop[i] = from_f<OpT>(w);
+  }
+}
+
+template <typename OpT>
+__global__ void broadcast_w0_kernel(long long total, int B, long long n, const float* __restrict__ W0,
+                                    float* __restrict__ W32, OpT* __restrict__ Wop) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long slot = i / (n * B), e = i % n;
+    const float w = W0[slot * n + e];
+    W32[i] = w;
+    Wop[i] = from_f<OpT>(w);
+  }
+}
+
+template <typename OpT>
+__global__ void cast_kernel(long long n, const float* __restrict__ in, OpT* __restrict__ out) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    out[i] = from_f<OpT>(in[i]);
+}
+
+__global__ void seq_mean_kernel(int rows, int n_valid, const float* __restrict__ row_loss,
+                                float* __restrict__ mean) {
+  __shared__ float red[32];
+  const int s = blockIdx.x;
+  float acc = 0.0f;
+  for (int j = threadIdx.x; j < n_valid; j += blockDim.x) acc += row_loss[(long long)s * rows + j];
+  acc = block_sum(acc, red);
+  if (threadIdx.x == 0) mean[s] = acc / n_valid;
+}
+
+__global__ void settle_decide_kernel(int B, const float* __restrict__ Lc, const float* __restrict__ Lw,
+                                     float* __restrict__ A, uint8_t* __restrict__ accept) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= B) return;
+  const float a = Lc[s] - Lw[s];
+  A[s] = a;
+  accept[s] = a >= 0.0f ? 1 : 0;
+}
+
+template <typename OpT>
+__global__ void settle_apply_kernel(long long total, int B, long long n, const uint8_t* __restrict__ accept,
+                                    float* __restrict__ W32, OpT* __restrict__ Wop,
+                                    float* __restrict__ Wc32, OpT* __restrict__ Wcop) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int s = (int)((i / n) % B);
+    if (accept[s]) {
+      Wc32[i] = W32[i];
+      Wcop[i] = Wop[i];
+    } else {
+      W32[i] = Wc32[i];
+      Wop[i] = Wcop[i];
+    }
+  }
+}
+
+__global__ void softmax_kernel(int V, const float* __restrict__ logits, float* __restrict__ p) {
+  __shared__ float red[32];
+  const long long m = blockIdx.x;
+  const float* row = logits + m * V;
+  float mx = -FLT_MAX;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) mx = fmaxf(mx, row[v]);
+  mx = warp_max(mx);
+  __shared__ float wm[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) wm[wid] = mx;
+  __syncthreads();
+  mx = -FLT_MAX;
+  for (int k = 0; k < nw; ++k) mx = fmaxf(mx, wm[k]);
+  float se = 0.0f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) se += expf(row[v] - mx);
+  se = block_sum(se, red);
+  const float inv = 1.0f / se;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) p[m * V + v] = expf(row[v] - mx) * inv;
+}
+
+__global__ void pending_shift_kernel(int B, int b, int32_t* pend) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s < B) pend[(long long)s * (b + 1)] = pend[(long long)s * (b + 1) + b];
+}
+
+int grid_for(long long n, int threads) {
+  long long g = (n + threads - 1) / threads;
+  const long long cap = 148LL * 16;
+  return (int)(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+}  // namespace
+
+#define DISPATCH_OP(dtype, KERNEL_CALL_BF16, KERNEL_CALL_F32) \
+  do {                                                        \
+    if ((dtype) == TTT_DTYPE_BF16) { KERNEL_CALL_BF16; } else { KERNEL_CALL_F32; } \
+  } while (0)
+
+ttt_status launch_embed(int dtype, int B, const TokView& tv, const void* E, int d, float* h32,
+                        void* hop, cudaStream_t st) {
+  const int M = B * tv.rows;
+  if (M == 0) return TTT_OK;
+  DISPATCH_OP(dtype,
+      (embed_kernel<bf16><<<M, 256, 0, st>>>(tv, (const bf16*)E, d, h32, (bf16*)hop)),
+      (embed_kernel<float><<<M, 256, 0, st>>>(tv, (const float*)E, d, h32, (float*)hop)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_rmsnorm_fwd(int dtype, int M, int d, const float* x, float eps, void* y, float* rstd,
+                              cudaStream_t st) {
+  if (M == 0) return TTT_OK;
+  DISPATCH_OP(dtype, (rmsnorm_fwd_kernel<bf16><<<M, 256, 0, st>>>(d, x, eps, (bf16*)y, rstd)),
+              (rmsnorm_fwd_kernel<float><<<M, 256, 0, st>>>(d, x, eps, (float*)y, rstd)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_rmsnorm_bwd(int dtype, int M, int d, const float* x, const float* rstd, const float* dy,
+                              float* dx32, void* dxop, cudaStream_t st) {
+  if (M == 0) return TTT_OK;
+  DISPATCH_OP(dtype,
+      (rmsnorm_bwd_kernel<bf16><<<M, 256, 0, st>>>(d, x, rstd, dy, dx32, (bf16*)dxop)),
+      (rmsnorm_bwd_kernel<float><<<M, 256, 0, st>>>(d, x, rstd, dy, dx32, (float*)dxop)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_ce(int dtype, int B, const TokView& tv, int V, void* logits, long long ldl, float scale,
+                     bool grad, float* losses, long long loss_ld, long long loss_off, float* row_loss,
+                     cudaStream_t st) {
+  const int M = B * tv.rows;
+  if (M == 0) return TTT_OK;
+  DISPATCH_OP(dtype,
+      (ce_kernel<bf16><<<M, 512, 0, st>>>(tv, V, (bf16*)logits, ldl, scale, grad, losses, loss_ld, loss_off, row_loss)),
+      (ce_kernel<float><<<M, 512, 0, st>>>(tv, V, (float*)logits, ldl, scale, grad, losses, loss_ld, loss_off, row_loss)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* partials, float clip, float* scale,
+                                float* norm, int* flag, cudaStream_t st) {
+  norm_finalize_kernel<<<B, 256, 0, st>>>(ps, partials, clip, scale, norm, flag);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_sgd_update(int dtype, int nslots, int B, long long n, float* W32, void* Wop, const float* dW,
+                             const float* scale, float eta, cudaStream_t st) {
+  const long long total = (long long)nslots * B * n;
+  const int g = grid_for(total, 256);
+  DISPATCH_OP(dtype,
+      (sgd_update_kernel<bf16><<<g, 256, 0, st>>>(total, B, n, W32, (bf16*)Wop, dW, scale, eta)),
+      (sgd_update_kernel<float><<<g, 256, 0, st>>>(total, B, n, W32, (float*)Wop, dW, scale, eta)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_broadcast_w0(int dtype, int nslots, int B, long long n, const float* W0, float* W32, void* Wop,
+                               cudaStream_t st) {
+  const long long total = (long long)nslots * B * n;
+  const int g = grid_for(total, 256);
+  DISPATCH_OP(dtype,
+      (broadcast_w0_kernel<bf16><<<g, 256, 0, st>>>(total, B, n, W0, W32, (bf16*)Wop)),
+      (broadcast_w0_kernel<float><<<g, 256, 0, st>>>(total, B, n, W0, W32, (float*)Wop)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_cast(int dtype, long long n, const float* in, void* out, cudaStream_t st) {
+  const int g = grid_for(n, 256);
+  DISPATCH_OP(dtype, (cast_kernel<bf16><<<g, 256, 0, st>>>(n, in, (bf16*)out)),
+              (cast_kernel<float><<<g, 256, 0, st>>>(n, in, (float*)out)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, float* mean, cudaStream_t st) {
+  seq_mean_kernel<<<B, 256, 0, st>>>(rows, n_valid, row_loss, mean);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_settle_apply(int dtype, int nslots, int B, long long n, const float* Lc, const float* Lw,
+                               float* A, uint8_t* accept, float* W32, void* Wop, float* Wc32, void* Wcop,
+                               cudaStream_t st) {
+  settle_decide_kernel<<<ceil_div(B, 128), 128, 0, st>>>(B, Lc, Lw, A, accept);
+  TTT_CHECK_LAUNCH();
+  const long long total = (long long)nslots * B * n;
+  const int g = grid_for(total, 256);
+  DISPATCH_OP(dtype,
+      (settle_apply_kernel<bf16><<<g, 256, 0, st>>>(total, B, n, accept, W32, (bf16*)Wop, Wc32, (bf16*)Wcop)),
+      (settle_apply_kernel<float><<<g, 256, 0, st>>>(total, B, n, accept, W32, (float*)Wop, Wc32, (float*)Wcop)));
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_softmax(int M, int V, const float* logits32, float* p, cudaStream_t st) {
+  if (M == 0) return TTT_OK;
+  softmax_kernel<<<M, 512, 0, st>>>(V, logits32, p);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st) {
+  pending_shift_kernel<<<ceil_div(B, 128), 128, 0, st>>>(B, b, pend);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+}  // namespace ttt

@@ -1,0 +1,80 @@
+// Internal launchers of the non-GEMM kernels of libttt.
+#pragma once
+
+#include "common.cuh"
+
+namespace ttt {
+
+// Row m = s * rows + j of a per-sequence row block reads token
+// tok[s * tok_ld + tok_off + j]; its target is the next token of the same
+// sequence, tok[s * tok_ld + tok_off + j + 1], for j < n_valid, and none after.
+struct TokView {
+  const int32_t* tok = nullptr;
+  long long tok_ld = 0;
+  long long tok_off = 0;
+  int rows = 0;
+  int n_valid = 0;
+  int vocab = 0;          // tokens outside [0, vocab) are replaced by 0 and
+  int* err = nullptr;     // raise bit 2 of *err (no out-of-range access)
+};
+
+// h32[m, :] = E[x_m, :] (float), hop[m, :] = same in the operand type.
+ttt_status launch_embed(int dtype, int B, const TokView& tv, const void* E, int d, float* h32,
+                        void* hop, cudaStream_t st);
+
+// y = x * rstd (operand type), rstd = 1/sqrt(mean(x^2) + eps).
+ttt_status launch_rmsnorm_fwd(int dtype, int M, int d, const float* x, float eps, void* y,
+                              float* rstd, cudaStream_t st);
+
+// dx = rstd * (dy - xhat * mean(xhat * dy)), xhat = x * rstd; dx32 and its
+// operand-type copy dxop (may be null).
+ttt_status launch_rmsnorm_bwd(int dtype, int M, int d, const float* x, const float* rstd,
+                              const float* dy, float* dx32, void* dxop, cudaStream_t st);
+
+// Row-wise cross-entropy of logits [B*rows, V] (operand type, leading dim ldl).
+// For valid rows: loss -> losses[s * loss_ld + loss_off + j] (if losses != null)
+// and row_loss[m] (if != null); when `grad` the row is overwritten in place by
+// dlogits = (softmax - onehot(target)) * scale.  Invalid rows get dlogits 0.
+ttt_status launch_ce(int dtype, int B, const TokView& tv, int V, void* logits, long long ldl,
+                     float scale, bool grad, float* losses, long long loss_ld, long long loss_off,
+                     float* row_loss, cudaStream_t st);
+
+// Per-sequence global gradient norm from the dW GEMM partials, then the
+// clip scale s = min(1, clip/(norm+1e-6)) (1 when clip == 0).  A non-finite
+// norm sets s = 0 (update skipped) and raises *flag.
+struct PartialSlots {
+  int n = 0;
+  long long off[16];
+  int tiles[16];
+};
+ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* partials, float clip,
+                                float* scale, float* norm, int* flag, cudaStream_t st);
+
+// W32 -= eta * scale[s] * dW over the arena [slot][B][n]; Wop = cast(W32).
+ttt_status launch_sgd_update(int dtype, int nslots, int B, long long n, float* W32, void* Wop,
+                             const float* dW, const float* scale, float eta, cudaStream_t st);
+
+// W32[slot][s] = W0[slot] for every s; Wop = cast.
+ttt_status launch_broadcast_w0(int dtype, int nslots, int B, long long n, const float* W0,
+                               float* W32, void* Wop, cudaStream_t st);
+
+// out[i] = cast(in[i]) for n floats.
+ttt_status launch_cast(int dtype, long long n, const float* in, void* out, cudaStream_t st);
+
+// mean over the n_valid valid rows of each sequence's row_loss block.
+ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, float* mean,
+                           cudaStream_t st);
+
+// A = Lc - Lw; accept = (A >= 0).  Then per sequence: accept ? Wc <- W : W <- Wc
+// over fp32 masters and operand copies.
+ttt_status launch_settle_apply(int dtype, int nslots, int B, long long n, const float* Lc,
+                               const float* Lw, float* A, uint8_t* accept, float* W32, void* Wop,
+                               float* Wc32, void* Wcop, cudaStream_t st);
+
+// p[m, :] = softmax(logits32[m, :]).
+ttt_status launch_softmax(int M, int V, const float* logits32, float* p, cudaStream_t st);
+
+// Shift the pending decode buffer: tok[s][0] = tok[s][b].
+ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st);
+
+}  // namespace ttt

@@ -1,0 +1,243 @@
+"""Thin ctypes binding of libttt (argument marshalling only).
+
+Every step of the TTT inner loop runs inside libttt's CUDA kernels; this
+module only converts numpy arrays / torch tensors into pointers and sizes,
+calls the C ABI declared in include/ttt.h, and raises TTTError on a non-OK
+status.  There is no CPU fallback: without the built library (or without a
+GPU) every call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libttt.so")
+
+STATUS = {0: "ok", 1: "bad argument", 2: "bad shape", 3: "out of device memory", 4: "CUDA error",
+          5: "non-finite gradient norm", 6: "timeout", 7: "unsupported", 8: "call out of order"}
+BLOCK = {"gelu": 0, "swiglu": 1}
+DTYPE = {"fp32": 0, "bf16": 1}
+MATS = {"gelu": ("W1", "W2"), "swiglu": ("Wg", "Wu", "Wd")}
+FAST_BIT = {"W1": 1, "W2": 2, "Wg": 1, "Wd": 2, "Wu": 4}
+
+
+class TTTError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("d_ff", ctypes.c_int), ("vocab", ctypes.c_int),
+                ("n_prefix", ctypes.c_int), ("n_fast", ctypes.c_int), ("block_kind", ctypes.c_int),
+                ("fast_mask", ctypes.c_int), ("dtype", ctypes.c_int), ("rms_eps", ctypes.c_float)]
+
+
+class HParams(ctypes.Structure):
+    _fields_ = [("eta", ctypes.c_float), ("clip", ctypes.c_float), ("chunk", ctypes.c_int),
+                ("settle_every", ctypes.c_int), ("max_batch", ctypes.c_int), ("settle_len", ctypes.c_int)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_void_p), ("U", ctypes.c_void_p),
+                ("prefix", ctypes.POINTER(ctypes.c_void_p)), ("fast", ctypes.POINTER(ctypes.c_void_p))]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libttt.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libttt.so is not built ({path}); run "
+                           "`python -m chunked_next_token_ttt_b300.build`")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "ttt_create": ([ctypes.POINTER(Dims), ctypes.POINTER(HParams), ctypes.POINTER(Weights),
+                        ctypes.POINTER(_P)], _I),
+        "ttt_destroy": ([_P], _I),
+        "ttt_prefill": ([_P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
+        "ttt_decode_step": ([_P, _P, _P, _P, _P], _I),
+        "ttt_settle": ([_P, _P, _I, _P, _P, _P], _I),
+        "ttt_get_fast_weights": ([_P, _I, _I, _I, _P, _P], _I),
+        "ttt_reset": ([_P, _P], _I),
+        "ttt_state_size": ([_P, ctypes.POINTER(ctypes.c_size_t)], _I),
+        "ttt_get_state": ([_P, _P, ctypes.c_size_t, _P], _I),
+        "ttt_set_state": ([_P, _P, ctypes.c_size_t, _P], _I),
+        "ttt_profile_enable": ([_P, _I], _I),
+        "ttt_profile_read": ([_P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)], _I),
+        "ttt_kernel_class_name": ([_I], ctypes.c_char_p),
+        "ttt_kernel_class_count": ([], _I),
+        "ttt_last_launch_count": ([_P, ctypes.POINTER(ctypes.c_longlong)], _I),
+        "ttt_status_string": ([_I], ctypes.c_char_p),
+        "ttt_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        detail = _lib.ttt_last_error().decode(errors="replace") if _lib else ""
+        raise TTTError(status, where, detail)
+
+
+def _ptr(x):
+    """Data pointer of a torch tensor or numpy array (None -> NULL)."""
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        if not x.flags["C_CONTIGUOUS"]:
+            raise ValueError("arrays passed to libttt must be C-contiguous")
+        return x.ctypes.data
+    raise TypeError(f"unsupported buffer type {type(x)}")
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+    except Exception:
+        pass
+    return None
+
+
+def kernel_classes() -> list:
+    lib = load_library()
+    return [lib.ttt_kernel_class_name(i).decode() for i in range(lib.ttt_kernel_class_count())]
+
+
+class Handle:
+    """One libttt handle: a network, its TTT hyper-parameters and B sequences."""
+
+    def __init__(self, *, d, d_ff, vocab, n_prefix, n_fast, block, fast_mats, dtype, eta, clip, chunk,
+                 B, weights, settle_every=0, settle_len=0, rms_eps=1e-6):
+        self.lib = load_library()
+        self.block = block
+        self.mats = MATS[block]
+        self.B, self.V, self.chunk = B, vocab, chunk
+        self.d, self.d_ff, self.n_fast = d, d_ff, n_fast
+        self.fast_mats = tuple(fast_mats)
+        mask = 0
+        for m in fast_mats:
+            mask |= FAST_BIT[m]
+        self._dims = Dims(d, d_ff, vocab, n_prefix, n_fast, BLOCK[block], mask, DTYPE[dtype], rms_eps)
+        self._hp = HParams(eta, clip, chunk, settle_every, B, settle_len)
+        keep = []
+
+        def f32(a):
+            if hasattr(a, "data_ptr"):
+                import torch
+                t = a.detach().to(torch.float32).contiguous()
+                keep.append(t)
+                return t.data_ptr()
+            arr = np.ascontiguousarray(a, dtype=np.float32)
+            keep.append(arr)
+            return arr.ctypes.data
+
+        pre = [f32(b[m]) for b in weights["prefix"] for m in self.mats]
+        fst = [f32(b[m]) for b in weights["fast"] for m in self.mats]
+        pre_arr = (ctypes.c_void_p * max(1, len(pre)))(*pre)
+        fst_arr = (ctypes.c_void_p * len(fst))(*fst)
+        w = Weights(f32(weights["E"]), f32(weights["U"]),
+                    ctypes.cast(pre_arr, ctypes.POINTER(ctypes.c_void_p)),
+                    ctypes.cast(fst_arr, ctypes.POINTER(ctypes.c_void_p)))
+        h = ctypes.c_void_p()
+        _check(self.lib.ttt_create(ctypes.byref(self._dims), ctypes.byref(self._hp), ctypes.byref(w),
+                                   ctypes.byref(h)), "ttt_create")
+        self._h = h
+        del keep
+
+    @classmethod
+    def from_workload(cls, wl, weights, B=None):
+        return cls(d=wl.d, d_ff=wl.d_ff, vocab=wl.vocab, n_prefix=wl.n_prefix, n_fast=wl.n_fast,
+                   block=wl.block, fast_mats=wl.fast_mats, dtype=wl.dtype, eta=wl.eta, clip=wl.clip,
+                   chunk=wl.chunk, B=wl.B if B is None else B, weights=weights,
+                   settle_every=wl.settle_every, settle_len=wl.settle_len, rms_eps=wl.rms_eps)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self.lib.ttt_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---------------------------------------------------------------- calls
+    def prefill(self, tokens, losses, p_next=None, settle_q=None, accept=None, A=None, stream=None):
+        """tokens [B, T+1] int32; losses [B, T] float32 out; the rest optional."""
+        B, T1 = tokens.shape
+        Lq = 0 if settle_q is None else settle_q.shape[-1]
+        _check(self.lib.ttt_prefill(self._h, _ptr(tokens), B, T1 - 1, _ptr(losses), _ptr(p_next),
+                                    _ptr(settle_q), Lq, _ptr(accept), _ptr(A), _stream(stream)),
+               "ttt_prefill")
+
+    def decode_step(self, x_new, p_next, loss=None, stream=None):
+        _check(self.lib.ttt_decode_step(self._h, _ptr(x_new), _ptr(p_next), _ptr(loss), _stream(stream)),
+               "ttt_decode_step")
+
+    def settle(self, q, accept, A, stream=None):
+        _check(self.lib.ttt_settle(self._h, _ptr(q), q.shape[-1], _ptr(accept), _ptr(A), _stream(stream)),
+               "ttt_settle")
+
+    def fast_weight(self, seq, block, mat, out=None):
+        """fp32 master of one fast matrix of one sequence (numpy unless `out` given)."""
+        mi = self.mats.index(mat) if isinstance(mat, str) else mat
+        shape = (self.d_ff, self.d) if self.mats[mi] in ("W1", "Wg", "Wu") else (self.d, self.d_ff)
+        dst = np.empty(shape, dtype=np.float32) if out is None else out
+        _check(self.lib.ttt_get_fast_weights(self._h, seq, block, mi, _ptr(dst), _stream(None)),
+               "ttt_get_fast_weights")
+        return dst
+
+    def fast_weights(self, seq):
+        return [{m: self.fast_weight(seq, l, m) for m in self.fast_mats} for l in range(self.n_fast)]
+
+    def reset(self):
+        _check(self.lib.ttt_reset(self._h, _stream(None)), "ttt_reset")
+
+    def get_state(self) -> bytes:
+        n = ctypes.c_size_t()
+        _check(self.lib.ttt_state_size(self._h, ctypes.byref(n)), "ttt_state_size")
+        buf = np.empty(n.value, dtype=np.uint8)
+        _check(self.lib.ttt_get_state(self._h, buf.ctypes.data, n.value, _stream(None)), "ttt_get_state")
+        return buf
+
+    def set_state(self, blob):
+        blob = np.ascontiguousarray(blob, dtype=np.uint8)
+        _check(self.lib.ttt_set_state(self._h, blob.ctypes.data, blob.size, _stream(None)), "ttt_set_state")
+
+    def profile_enable(self, kernel_class):
+        if isinstance(kernel_class, str):
+            kernel_class = kernel_classes().index(kernel_class)
+        _check(self.lib.ttt_profile_enable(self._h, kernel_class), "ttt_profile_enable")
+
+    def profile_read(self):
+        n = ctypes.c_int()
+        ms = ctypes.c_double()
+        _check(self.lib.ttt_profile_read(self._h, ctypes.byref(n), ctypes.byref(ms)), "ttt_profile_read")
+        return n.value, ms.value
+
+    def last_launch_count(self) -> int:
+        n = ctypes.c_longlong()
+        _check(self.lib.ttt_last_launch_count(self._h, ctypes.byref(n)), "ttt_last_launch_count")
+        return n.value

@@ -1,0 +1,166 @@
+"""libttt (CUDA, through the C ABI) against the float64 oracle on seeded inputs.
+
+Workloads run either at their stated sizes or, where the oracle would take
+minutes, at the same structure (block kind, dtype, fast set, clip, eta) with
+smaller widths and a documented chunk prefix; every case spans several GEMM
+tiles and ragged tile tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import configs as C
+
+from gpu_harness import compare, compare_settlement, make, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def test_toy_bigram_fp32_full_size():
+    """The pages' toy: b = 1, per-token update (eq. (2)), 1024 tokens."""
+    wl = C.TOY_BIGRAM
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_chunked_fp32_prefix_chunks():
+    wl = C.CHUNKED_FP32.replace(T=4 * C.CHUNKED_FP32.chunk)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_chunked_fp32_odd_shapes_ragged_tail():
+    """Widths that are not multiples of any tile, T not a multiple of b."""
+    wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=40, B=3, T=130, n_prefix=1)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_e2e125m_bf16_small_widths():
+    wl = C.E2E_125M.replace(d=256, d_ff=1024, vocab=2000, chunk=256, B=3, T=3 * 256, n_prefix=2)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_inplace_swiglu_down_proj_bf16_small_widths():
+    wl = C.INPLACE_4B.replace(d=256, d_ff=640, vocab=3000, chunk=128, B=2, T=3 * 128 + 17, n_prefix=2)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_settlement_bf16_small_widths():
+    """Settlement after every 8th chunk; half the sequences score their candidate
+    on held-out text from a different chain, so both commits and reverts occur."""
+    wl = C.SETTLE_760M.replace(d=128, d_ff=512, vocab=512, chunk=64, B=4, T=16 * 64, n_prefix=1,
+                               settle_len=64, eta=0.5, init_std=0.08)
+    inp = make(wl)
+    other = synth.make_chain(wl.seed_id + 100, wl.vocab, wl.chain_k, wl.chain_alpha)
+    q = inp["settle_q"].copy()
+    q_other = synth.sample_heldout(other, wl.seed_id + 100, q.shape[0], wl.B, wl.settle_len)
+    q[:, 1::2] = q_other[:, 1::2]
+    gpu = run_gpu(wl, inp, q=q)
+    ref = run_oracle(wl, inp, q=q)
+    decided = compare_settlement(gpu, ref, range(wl.B), noise=5e-3)
+    assert decided >= 6
+    assert ref["accept"].any() and (~ref["accept"]).any()
+    compare(wl, gpu, ref)
+
+
+def test_host_and_device_buffers_agree():
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=32, B=2, T=100, n_prefix=1)
+    inp = make(wl)
+    a = run_gpu(wl, inp, device=True)
+    b = run_gpu(wl, inp, device=False)
+    np.testing.assert_array_equal(a["losses"], b["losses"])
+    np.testing.assert_array_equal(a["p_next"], b["p_next"])
+
+
+def test_sequences_are_independent_on_gpu():
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=32, B=3, T=96, n_prefix=1)
+    inp = make(wl)
+    full = run_gpu(wl, inp)
+    one = run_gpu(wl, inp, tokens=inp["tokens"][1:2])
+    np.testing.assert_array_equal(one["losses"][0], full["losses"][1])
+    for l in range(wl.n_fast):
+        for k in wl.fast_mats:
+            np.testing.assert_array_equal(one["W"][0][l][k], full["W"][1][l][k])
+
+
+def test_decode_completes_the_ragged_chunk_and_continues():
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=16 * 3 + 5, n_prefix=1)
+    inp = make(wl)
+    extra = 16 + 11 + 16
+    chain = inp["chain"]
+    long_tok = synth.sample_stream(chain, wl.seed_id, wl.B, wl.T + extra)
+    tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
+    gpu = run_gpu(wl, inp, tokens=tok)
+    h = gpu["handle"]
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
+    for t in range(wl.T + 1, wl.T + extra + 1):
+        x = torch.from_numpy(long_tok[:, t].copy()).cuda()
+        h.decode_step(x, p, loss)
+        torch.cuda.synchronize()
+        for s in range(wl.B):
+            l_ref, p_ref = oracle.decode_step(net, ref["states"][s], long_tok[s, t], wl.eta, wl.clip, wl.chunk)
+            assert abs(float(loss[s]) - l_ref) <= 1e-4
+            assert np.abs(p[s].cpu().numpy() - p_ref).max() <= 1e-5
+    for s in range(wl.B):
+        rel = oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats)
+        assert rel <= 1e-4
+
+
+def test_state_roundtrip_and_reset():
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=40, n_prefix=1)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    h = gpu["handle"]
+    blob = h.get_state()
+    W_before = h.fast_weights(1)
+    h.reset()
+    W0 = h.fast_weights(1)
+    for l in range(wl.n_fast):
+        np.testing.assert_array_equal(W0[l]["W1"], inp["weights"]["fast"][l]["W1"])
+    h.set_state(blob)
+    W_after = h.fast_weights(1)
+    for l in range(wl.n_fast):
+        for k in wl.fast_mats:
+            np.testing.assert_array_equal(W_after[l][k], W_before[l][k])
+
+
+def test_bad_arguments_raise_status_codes():
+    from chunked_next_token_ttt_b300 import TTTError
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=32, n_prefix=1)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    h = gpu["handle"]
+    bad = torch.zeros((3, 33), dtype=torch.int32, device="cuda")
+    losses = torch.empty((3, 32), device="cuda")
+    with pytest.raises(TTTError) as e:
+        h.prefill(bad, losses)
+    assert e.value.status == 2
+    with pytest.raises(TTTError) as e:
+        wl2 = wl.replace(block="swiglu", fast_mats=("Wg", "Wd"))
+        from chunked_next_token_ttt_b300 import Handle
+        Handle.from_workload(wl2, synth.make_weights(wl2))
+    assert e.value.status == 7
