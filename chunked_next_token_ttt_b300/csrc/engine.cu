@@ -79,7 +79,9 @@ static void* op_at(const ttt_handle* h, void* base, long long elems) {
 
 static int gemm_count(const GemmDesc&) { return 1; }
 
-static ttt_status rungemm(ttt_handle* h, int cls, const GemmDesc& g, cudaStream_t st) {
+static ttt_status rungemm(ttt_handle* h, int cls, const GemmDesc& g_in, cudaStream_t st) {
+  GemmDesc g = g_in;
+  g.err = h->flag;
   return run(h, cls, st, gemm_count(g), [&] { return gemm(g, st); });
 }
 
@@ -194,6 +196,8 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
   PartialSlots ps{};
   long long poff = 0;
   auto dw_gemm = [&](GemmDesc& g, int slot) -> ttt_status {
+    g.epi = EPI_DW;
+    g.partials = h->partials + poff;
     const int tiles = gemm_partial_tiles(g);
     if (ps.n >= 16 || poff + (long long)tiles * B > h->partial_cap)
       return fail(TTT_ERR_UNSUPPORTED, "too many gradient-norm partial slots");
@@ -309,6 +313,7 @@ static ttt_status reset_weights(ttt_handle* h, cudaStream_t st) {
 static ttt_status finish(ttt_handle* h, cudaStream_t st) {
   TTT_CUDA(cudaMemcpyAsync(h->flag_host, h->flag, 4, cudaMemcpyDeviceToHost, st));
   TTT_CUDA(cudaStreamSynchronize(st));
+  if (*h->flag_host & kErrGemmTimeout) return fail(TTT_ERR_TIMEOUT, "a GEMM pipeline wait timed out");
   if (*h->flag_host & 2) return fail(TTT_ERR_BAD_ARG, "token id outside [0, vocab)");
   if (*h->flag_host & 1) return fail(TTT_ERR_NONFINITE, "non-finite gradient norm: update skipped");
   return TTT_OK;

@@ -28,7 +28,12 @@ struct GemmDesc {
   void* out2 = nullptr; long long ldo2 = 0, sO2 = 0;
   const void* aux = nullptr; long long ldx = 0, sX = 0;
   float* partials = nullptr;       // EPI_DW: [batch][gemm_partial_tiles()]
+  int* err = nullptr;              // device status word for bounded-wait timeouts
+  int impl = 0;                    // 0 auto, 1 SIMT, 2 tensor cores
 };
+
+// Status bits the tensor-core kernel raises in *err when a bounded wait gives up.
+constexpr int kErrGemmTimeout = 8 | 16 | 32;
 
 // Which implementation ran a GEMM (for launch accounting and tests).
 enum GemmImpl { GEMM_IMPL_SIMT = 0, GEMM_IMPL_TC = 1 };
@@ -38,5 +43,8 @@ int gemm_partial_tiles(const GemmDesc& g);
 ttt_status gemm(const GemmDesc& g, cudaStream_t st);
 ttt_status gemm_simt(const GemmDesc& g, cudaStream_t st);
 int gemm_simt_partial_tiles(const GemmDesc& g);
+bool gemm_tc_supported(const GemmDesc& g);
+int gemm_tc_partial_tiles(const GemmDesc& g);
+ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st);
 
 }  // namespace ttt

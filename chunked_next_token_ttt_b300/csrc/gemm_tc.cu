@@ -1,0 +1,385 @@
+// tcgen05 tensor-core GEMM for sm_103a: bf16 operands, fp32 accumulation in
+// TMEM, operands staged by TMA into 128B-swizzled shared memory, with the TTT
+// epilogues applied on the way out of TMEM.
+//
+// One CTA computes one 128 x BN output tile of one batch entry:
+//   warp 0 (one lane)  TMA producer: a STAGES-deep ring of (A, B) k-slices of
+//                      64 elements, each slot guarded by a full/empty mbarrier
+//   warp 1             allocates BN TMEM columns; one lane issues
+//                      tcgen05.mma (M=128, N=BN, K=16) x 4 per slice and
+//                      releases the slot with tcgen05.commit
+//   warps 2..5         epilogue: tcgen05.ld of their 32-lane TMEM quadrant,
+//                      per-element epilogue, stores to global memory
+// Operands may be K-major or MN-major (the backward's transposed products);
+// TMA loads MN-major operands as 64-element-wide column panels and the UMMA
+// descriptor's leading/stride byte offsets walk them.
+//
+// Every mbarrier wait is bounded (about 2 s of %globaltimer); on timeout the
+// waiting thread records a code in the error word and the CTA unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "epilogue.cuh"
+#include "gemm.h"
+
+namespace ttt {
+namespace tc {
+
+constexpr int BM = 128;        // UMMA M (one CTA, TMEM lanes 0..127 = rows)
+constexpr int BK = 64;         // k-slice: 64 bf16 = 128 bytes = one swizzle span
+constexpr int PANEL = 64;      // MN-major panel width (elements)
+constexpr int NUM_THREADS = 192;
+constexpr long long kTimeoutNs = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on phase `parity`; false (and *err |= code) after the timeout.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > (uint64_t)kTimeoutNs) {
+      atomicOr(err, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// UMMA shared-memory descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                       // D = F32
+         | (1u << 7)                     // A = BF16
+         | (1u << 10)                    // B = BF16
+         | ((a_mn ? 1u : 0u) << 15)      // A major: 0 = K, 1 = MN
+         | ((b_mn ? 1u : 0u) << 16)      // B major
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BN, int STAGES>
+struct Smem {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 1) * 8 + 16 + 4 * 4;
+  static constexpr int ALLOC = TOTAL + 1024;  // slack to align the base to 1024 bytes
+};
+
+template <int BN, int STAGES, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmDesc g, int num_kb, int* err) {
+  using L = Smem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accb = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN, bz = blockIdx.z;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accb, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x < 4) red[threadIdx.x] = 0.0f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % STAGES;
+      if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) & 1) ^ 1, err, 8)) break;
+      uint8_t* sa = smem + s * L::STAGE_BYTES;
+      uint8_t* sb = sa + L::A_BYTES;
+      mbar_expect_tx(&full[s], L::STAGE_BYTES);
+      const int k0 = kb * BK;
+      if (!A_MN) {
+        tma_load_3d(sa, &tmA, &full[s], k0, m0, bz);
+      } else {
+#pragma unroll
+        for (int j = 0; j < BM / PANEL; ++j) tma_load_3d(sa + j * PANEL * BK * 2, &tmA, &full[s], m0 + j * PANEL, k0, bz);
+      }
+      if (!B_MN) {
+        tma_load_3d(sb, &tmB, &full[s], k0, n0, bz);
+      } else {
+#pragma unroll
+        for (int j = 0; j < BN / PANEL; ++j) tma_load_3d(sb + j * PANEL * BK * 2, &tmB, &full[s], n0 + j * PANEL, k0, bz);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = umma_idesc(BM, BN, A_MN, B_MN);
+    bool ok = true;
+    for (int kb = 0; kb < num_kb && ok; ++kb) {
+      const int s = kb % STAGES;
+      ok = mbar_wait(&full[s], (kb / STAGES) & 1, err, 16);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t sa = smem_u32(smem + s * L::STAGE_BYTES);
+      const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k) {
+        // K-major: the 16-element k-step is 32 bytes inside the swizzle span.
+        // MN-major: 16 k-rows of 128 bytes; panels of 64 MN-elements are BK*128 bytes apart.
+        const uint64_t ad = A_MN ? umma_desc(sa + k * 2048, PANEL * BK * 2, 1024) : umma_desc(sa + k * 32, 16, 1024);
+        const uint64_t bd = B_MN ? umma_desc(sb + k * 2048, PANEL * BK * 2, 1024) : umma_desc(sb + k * 32, 16, 1024);
+        umma_bf16(tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      }
+      umma_commit(&empty[s]);
+    }
+    umma_commit(accb);
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue
+    bool ok = mbar_wait(accb, 0, err, 32);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (ok) {
+      const int quad = warp & 3;
+      const int row = m0 + quad * 32 + lane;
+      float sq = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c, v);
+        if (row < g.M) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = n0 + c + i;
+            if (n < g.N) sq += epi_value<bf16>(g, bz, row, n, v[i]);
+          }
+        }
+      }
+      if (g.epi == EPI_DW) {
+        sq = warp_sum(sq);
+        if (lane == 0) red[warp - 2] = sq;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (g.epi == EPI_DW && threadIdx.x == 0)
+    g.partials[(long long)bz * gridDim.x * gridDim.y + blockIdx.y * gridDim.x + blockIdx.x] =
+        red[0] + red[1] + red[2] + red[3];
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+int* g_err = nullptr;
+
+ttt_status init_driver() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  if (!g_encode) {
+    set_error("cuTensorMapEncodeTiled is not available");
+    return TTT_ERR_CUDA;
+  }
+  return TTT_OK;
+}
+
+// 3-D bf16 tensor map over X[batch][outer][inner] (leading dim ld, batch stride sz, in elements).
+ttt_status make_map(CUtensorMap* m, const void* base, long long inner, long long outer, int batch, long long ld,
+                    long long sz, int box_inner, int box_outer) {
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)batch};
+  const long long bstride = batch > 1 ? sz : ld * outer;
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bstride * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed with code " + std::to_string((int)r));
+    return TTT_ERR_CUDA;
+  }
+  return TTT_OK;
+}
+
+constexpr int kBN = 128;
+constexpr int kStages = 4;
+
+template <bool A_MN, bool B_MN>
+ttt_status launch_variant(const GemmDesc& g, const CUtensorMap& ta, const CUtensorMap& tb, int nkb,
+                          cudaStream_t st) {
+  using L = Smem<kBN, kStages>;
+  auto kern = gemm_tc_kernel<kBN, kStages, A_MN, B_MN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
+    attr_set = true;
+  }
+  dim3 grid(ceil_div(g.N, kBN), ceil_div(g.M, BM), g.batch);
+  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(ta, tb, g, nkb, g_err);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+}  // namespace tc
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool gemm_tc_supported(const GemmDesc& g) {
+  if (g.dtype != TTT_DTYPE_BF16) return false;
+  if (g.M < 64 || g.N < 64 || g.K < 16 || g.batch < 1) return false;
+  if (!aligned16(g.A) || !aligned16(g.B)) return false;
+  if (g.lda % 8 || g.ldb % 8) return false;
+  if (g.batch > 1 && (g.sA % 8 || g.sB % 8 || g.sA <= 0 || g.sB <= 0)) return false;
+  if (g.epi == EPI_DW && !g.partials) return false;
+  return true;
+}
+
+int gemm_tc_partial_tiles(const GemmDesc& g) { return ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM); }
+
+ttt_status gemm_tc_error_word(int** err) {
+  if (!tc::g_err) {
+    cudaError_t e = cudaMalloc(&tc::g_err, 4);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc", __FILE__, __LINE__);
+    e = cudaMemset(tc::g_err, 0, 4);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset", __FILE__, __LINE__);
+  }
+  *err = tc::g_err;
+  return TTT_OK;
+}
+
+ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
+  if (!gemm_tc_supported(g)) {
+    set_error("shape/alignment not supported by the tensor-core GEMM");
+    return TTT_ERR_UNSUPPORTED;
+  }
+  TTT_TRY(tc::init_driver());
+  int* err = g.err;
+  if (!err) TTT_TRY(gemm_tc_error_word(&err));
+  const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
+  CUtensorMap ta, tb;
+  // A: K-major [batch][M][K] boxes {64, 128}; MN-major [batch][K][M] panels {64, 64}
+  if (!a_mn) TTT_TRY(tc::make_map(&ta, g.A, g.K, g.M, g.batch, g.lda, g.sA, tc::BK, tc::BM));
+  else TTT_TRY(tc::make_map(&ta, g.A, g.M, g.K, g.batch, g.lda, g.sA, tc::PANEL, tc::BK));
+  if (!b_mn) TTT_TRY(tc::make_map(&tb, g.B, g.K, g.N, g.batch, g.ldb, g.sB, tc::BK, tc::kBN));
+  else TTT_TRY(tc::make_map(&tb, g.B, g.N, g.K, g.batch, g.ldb, g.sB, tc::PANEL, tc::BK));
+  const int nkb = ceil_div(g.K, tc::BK);
+  if (!a_mn && !b_mn) return tc::launch_variant<false, false>(g, ta, tb, nkb, st);
+  if (!a_mn && b_mn) return tc::launch_variant<false, true>(g, ta, tb, nkb, st);
+  if (a_mn && !b_mn) return tc::launch_variant<true, false>(g, ta, tb, nkb, st);
+  return tc::launch_variant<true, true>(g, ta, tb, nkb, st);
+}
+
+}  // namespace ttt

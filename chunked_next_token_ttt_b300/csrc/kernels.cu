@@ -166,7 +166,9 @@ __global__ void sgd_update_kernel(long long total, int B, long long n, float* __
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int s = (int)((i / n) % B);
-    const float w = W32[i] - eta * scale[s] * dW[i];
+    const float sc = scale[s];
+    if (sc == 0.0f) continue;  // skipped update (non-finite norm): W stays as it is
+    const float w = W32[i] - eta * sc * dW[i];
     W32[i] = w;
     Wop[i] = from_f<OpT>(w);
   }

@@ -241,3 +241,91 @@ class Handle:
         n = ctypes.c_longlong()
         _check(self.lib.ttt_last_launch_count(self._h, ctypes.byref(n)), "ttt_last_launch_count")
         return n.value
+
+
+# ---------------------------------------------------------------- single operations
+EPI = {"store": 0, "store_f32": 1, "gelu": 2, "resid": 3, "swiglu": 4, "dgelu": 5, "dw": 6}
+GEMM_IMPL = {"auto": 0, "simt": 1, "tensor": 2}
+
+
+class GemmArgs(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int), ("batch", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("a_kmajor", ctypes.c_int), ("b_kmajor", ctypes.c_int),
+                ("epi", ctypes.c_int), ("impl", ctypes.c_int),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_longlong), ("sA", ctypes.c_longlong),
+                ("B", ctypes.c_void_p), ("ldb", ctypes.c_longlong), ("sB", ctypes.c_longlong),
+                ("out", ctypes.c_void_p), ("ldo", ctypes.c_longlong), ("sO", ctypes.c_longlong),
+                ("out2", ctypes.c_void_p), ("ldo2", ctypes.c_longlong), ("sO2", ctypes.c_longlong),
+                ("aux", ctypes.c_void_p), ("ldx", ctypes.c_longlong), ("sX", ctypes.c_longlong),
+                ("partials", ctypes.c_void_p)]
+
+
+def _ops_lib():
+    lib = load_library()
+    if not getattr(lib, "_ops_ready", False):
+        sig = {
+            "ttt_op_gemm": ([ctypes.POINTER(GemmArgs), _P], _I),
+            "ttt_op_gemm_partial_tiles": ([ctypes.POINTER(GemmArgs)], _I),
+            "ttt_op_cross_entropy": ([_I, _I, _I, _P, _P, ctypes.c_float, _I, _P, _P], _I),
+            "ttt_op_rmsnorm_forward": ([_I, _I, _I, _P, ctypes.c_float, _P, _P, _P], _I),
+            "ttt_op_rmsnorm_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+            "ttt_clip_sgd": ([_I, _I, _I, ctypes.c_longlong, _P, _P, _P, ctypes.c_float, ctypes.c_float,
+                              _P, _P, _P, ctypes.c_size_t, _P], _I),
+            "ttt_clip_sgd_workspace_size": ([_I, _I, ctypes.c_longlong], ctypes.c_size_t),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        lib._ops_ready = True
+    return lib
+
+
+def gemm_args(M, N, K, A, B, out, *, batch=1, dtype="bf16", a_kmajor=True, b_kmajor=True, epi="store",
+              impl="auto", lda=None, sA=0, ldb=None, sB=0, ldo=None, sO=0, out2=None, ldo2=0, sO2=0,
+              aux=None, ldx=0, sX=0, partials=None):
+    return GemmArgs(M, N, K, batch, DTYPE[dtype], int(a_kmajor), int(b_kmajor), EPI[epi], GEMM_IMPL[impl],
+                    _ptr(A), lda if lda is not None else (K if a_kmajor else M), sA,
+                    _ptr(B), ldb if ldb is not None else (K if b_kmajor else N), sB,
+                    _ptr(out), ldo if ldo is not None else N, sO, _ptr(out2), ldo2, sO2,
+                    _ptr(aux), ldx, sX, _ptr(partials))
+
+
+def op_gemm(args: GemmArgs, stream=None):
+    _check(_ops_lib().ttt_op_gemm(ctypes.byref(args), _stream(stream)), "ttt_op_gemm")
+
+
+def op_gemm_partial_tiles(args: GemmArgs) -> int:
+    return _ops_lib().ttt_op_gemm_partial_tiles(ctypes.byref(args))
+
+
+def op_cross_entropy(dtype, logits, targets, scale, grad, losses, stream=None):
+    M, V = logits.shape
+    _check(_ops_lib().ttt_op_cross_entropy(DTYPE[dtype], M, V, _ptr(logits), _ptr(targets), scale, int(grad),
+                                           _ptr(losses), _stream(stream)), "ttt_op_cross_entropy")
+
+
+def op_rmsnorm_forward(dtype, x, eps, y, rstd, stream=None):
+    M, d = x.shape
+    _check(_ops_lib().ttt_op_rmsnorm_forward(DTYPE[dtype], M, d, _ptr(x), eps, _ptr(y), _ptr(rstd),
+                                             _stream(stream)), "ttt_op_rmsnorm_forward")
+
+
+def op_rmsnorm_backward(dtype, x, rstd, dy, dx, dx_op=None, stream=None):
+    M, d = x.shape
+    _check(_ops_lib().ttt_op_rmsnorm_backward(DTYPE[dtype], M, d, _ptr(x), _ptr(rstd), _ptr(dy), _ptr(dx),
+                                              _ptr(dx_op), _stream(stream)), "ttt_op_rmsnorm_backward")
+
+
+def clip_sgd_workspace_size(nslots, B, n) -> int:
+    return _ops_lib().ttt_clip_sgd_workspace_size(nslots, B, n)
+
+
+def clip_sgd(dtype, W32, Wop, dW, eta, clip, norm_out=None, scale_out=None, workspace=None, stream=None):
+    """W32, Wop, dW: [nslots, B, n] device tensors; workspace: device byte tensor."""
+    nslots, B, n = W32.shape
+    _check(_ops_lib().ttt_clip_sgd(DTYPE[dtype], nslots, B, n, _ptr(W32), _ptr(Wop), _ptr(dW), eta, clip,
+                                   _ptr(norm_out), _ptr(scale_out), _ptr(workspace),
+                                   0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "ttt_clip_sgd")
+

@@ -1,0 +1,220 @@
+"""Single-kernel tests through the op-level C ABI (include/ttt_ops.h).
+
+GEMMs (SIMT and tcgen05, every operand major-ness, batched, ragged tails,
+every epilogue) against float64 products of the same (bf16-exact) inputs;
+cross-entropy, RMSNorm and the clipped SGD step against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_next_token_ttt_b300 import ttt as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def bf16_exact(shape, rng, scale=1.0):
+    x = torch.from_numpy(rng.normal(0, scale, shape).astype(np.float32)).to(torch.bfloat16)
+    return x
+
+
+def to64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def operands(rng, M, N, K, batch, a_k, b_k, dtype):
+    """A(m,k) and B(n,k) stored K-major or MN-major; returns device tensors and
+    the float64 [batch, M, K] / [batch, N, K] views."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    A = bf16_exact((batch, M, K), rng).to(tdt)
+    B = bf16_exact((batch, N, K), rng).to(tdt)
+    A_store = A if a_k else A.transpose(1, 2)
+    B_store = B if b_k else B.transpose(1, 2)
+    return A_store.contiguous().cuda(), B_store.contiguous().cuda(), to64(A), to64(B)
+
+
+def run_gemm(M, N, K, batch, a_k, b_k, impl, epi="store_f32", dtype="bf16", seed=0, **kw):
+    rng = np.random.default_rng(seed)
+    Ad, Bd, A64, B64 = operands(rng, M, N, K, batch, a_k, b_k, dtype)
+    ref = np.einsum("bmk,bnk->bmn", A64, B64)
+    out = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+    args = T.gemm_args(M, N, K, Ad, Bd, out, batch=batch, dtype=dtype, a_kmajor=a_k, b_kmajor=b_k,
+                       epi=epi, impl=impl, sA=M * K, sB=N * K, sO=M * N, **kw)
+    T.op_gemm(args)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64), ref
+
+
+def test_tensor_core_gemm_single_tile_first():
+    """Smallest tcgen05 case first: one 128x128 tile, K = 64, both K-major."""
+    got, ref = run_gemm(128, 128, 64, 1, True, True, "tensor")
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max() + 1e-6
+
+
+@pytest.mark.parametrize("a_k", [True, False], ids=["A_kmaj", "A_mnmaj"])
+@pytest.mark.parametrize("b_k", [True, False], ids=["B_kmaj", "B_mnmaj"])
+@pytest.mark.parametrize("impl", ["tensor", "simt"])
+def test_gemm_every_major_batched(a_k, b_k, impl):
+    got, ref = run_gemm(256, 384, 320, 2, a_k, b_k, impl, seed=1)
+    assert np.abs(got - ref).max() <= 2e-5 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("a_k", [True, False], ids=["A_kmaj", "A_mnmaj"])
+@pytest.mark.parametrize("b_k", [True, False], ids=["B_kmaj", "B_mnmaj"])
+def test_tensor_core_gemm_ragged_tails(a_k, b_k):
+    """M, N, K not multiples of the 128 x 128 x 64 tile (TMA zero-fills the rest)."""
+    got, ref = run_gemm(200, 136, 72, 3, a_k, b_k, "tensor", seed=2)
+    assert np.abs(got - ref).max() <= 2e-5 * np.abs(ref).max()
+
+
+def test_tensor_core_gemm_long_k_pipeline_wraps():
+    """K = 2048: 32 k-slices through the 4-deep ring (every slot reused 8 times)."""
+    got, ref = run_gemm(128, 256, 2048, 1, True, False, "tensor", seed=3)
+    assert np.abs(got - ref).max() <= 2e-5 * np.abs(ref).max()
+
+
+def test_fp32_simt_gemm_exact_inputs():
+    got, ref = run_gemm(70, 90, 50, 2, False, True, "simt", dtype="fp32", seed=4)
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def _bf(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("impl", ["tensor", "simt"])
+def test_epilogues(impl):
+    rng = np.random.default_rng(5)
+    M, N, K, batch = 256, 256, 128, 2
+    Ad, Bd, A64, B64 = operands(rng, M, N, K, batch, True, True, "bf16")
+    acc = np.einsum("bmk,bnk->bmn", A64, B64)
+    common = dict(batch=batch, impl=impl, sA=M * K, sB=N * K, sO=M * N)
+    bf = torch.bfloat16
+
+    # GELU: stash z and a
+    z = torch.zeros((batch, M, N), dtype=bf, device="cuda")
+    a = torch.zeros((batch, M, N), dtype=bf, device="cuda")
+    T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, z, epi="gelu", out2=a, ldo2=N, sO2=M * N, **common))
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to64(z), _bf(acc), rtol=1e-2, atol=1e-2)
+    np.testing.assert_allclose(to64(a), _bf(oracle.gelu(acc)), rtol=1e-2, atol=1e-2)
+
+    # RESID: fp32 out = aux + acc, and its bf16 copy
+    r = torch.from_numpy(rng.normal(0, 1, (batch, M, N)).astype(np.float32)).cuda()
+    out = torch.zeros_like(r)
+    cp = torch.zeros((batch, M, N), dtype=bf, device="cuda")
+    T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, out, epi="resid", aux=r, ldx=N, sX=M * N, out2=cp, ldo2=N,
+                          sO2=M * N, **common))
+    torch.cuda.synchronize()
+    want = r.cpu().numpy().astype(np.float64) + acc
+    np.testing.assert_allclose(out.cpu().numpy(), want, rtol=1e-5, atol=1e-4)
+    np.testing.assert_allclose(to64(cp), _bf(want), rtol=1e-2, atol=1e-2)
+
+    # SWIGLU: silu(aux) * acc
+    g = torch.from_numpy(rng.normal(0, 1, (batch, M, N)).astype(np.float32)).cuda()
+    sw = torch.zeros((batch, M, N), dtype=bf, device="cuda")
+    T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, sw, epi="swiglu", aux=g, ldx=N, sX=M * N, **common))
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to64(sw), _bf(oracle.silu(g.cpu().numpy().astype(np.float64)) * acc),
+                               rtol=2e-2, atol=2e-2)
+
+    # DGELU: acc * GELU'(aux), in place over aux
+    zz = torch.from_numpy(rng.normal(0, 1, (batch, M, N)).astype(np.float32)).to(bf).cuda()
+    z64 = to64(zz)
+    T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, zz, epi="dgelu", aux=zz, ldx=N, sX=M * N, **common))
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to64(zz), _bf(acc * oracle.gelu_grad(z64)), rtol=2e-2, atol=2e-2)
+
+    # DW: fp32 out and per-tile sums of squares
+    dw = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+    args = T.gemm_args(M, N, K, Ad, Bd, dw, epi="dw", **common)
+    tiles = T.op_gemm_partial_tiles(args)
+    part = torch.zeros((batch, tiles), dtype=torch.float32, device="cuda")
+    args = T.gemm_args(M, N, K, Ad, Bd, dw, epi="dw", partials=part, **common)
+    T.op_gemm(args)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(dw.cpu().numpy(), acc, rtol=1e-5, atol=1e-4)
+    np.testing.assert_allclose(part.cpu().numpy().sum(1), (acc ** 2).sum(axis=(1, 2)), rtol=1e-5)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_cross_entropy_op(dtype):
+    rng = np.random.default_rng(6)
+    M, V = 37, 3001
+    logits = rng.normal(0, 2, (M, V)).astype(np.float32)
+    tgt = rng.integers(0, V, M).astype(np.int32)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    L = torch.from_numpy(logits).to(tdt).cuda()
+    L64 = to64(L)
+    losses = torch.zeros(M, dtype=torch.float32, device="cuda")
+    T.op_cross_entropy(dtype, L, torch.from_numpy(tgt).cuda(), 0.25, True, losses)
+    torch.cuda.synchronize()
+    ref_l, p = oracle.cross_entropy(L64, tgt.astype(np.int64))
+    dl = p.copy()
+    dl[np.arange(M), tgt] -= 1
+    tol = 1e-5 if dtype == "fp32" else 1e-2
+    np.testing.assert_allclose(losses.cpu().numpy(), ref_l, rtol=tol, atol=tol)
+    np.testing.assert_allclose(to64(L), dl * 0.25, atol=1e-6 if dtype == "fp32" else 1e-3)
+
+
+def test_rmsnorm_ops():
+    rng = np.random.default_rng(7)
+    M, d, eps = 33, 777, 1e-6
+    x = torch.from_numpy(rng.normal(0, 0.05, (M, d)).astype(np.float32)).cuda()
+    y = torch.zeros_like(x)
+    r = torch.zeros(M, device="cuda")
+    T.op_rmsnorm_forward("fp32", x, eps, y, r)
+    dy = torch.from_numpy(rng.normal(0, 1, (M, d)).astype(np.float32)).cuda()
+    dx = torch.zeros_like(x)
+    T.op_rmsnorm_backward("fp32", x, r, dy, dx)
+    torch.cuda.synchronize()
+    x64 = x.cpu().numpy().astype(np.float64)
+    y_ref, r_ref = oracle.rmsnorm(x64, eps)
+    np.testing.assert_allclose(y.cpu().numpy(), y_ref, rtol=1e-5, atol=1e-6)
+    dx_ref = oracle.rmsnorm_backward(x64, r_ref, dy.cpu().numpy().astype(np.float64))
+    np.testing.assert_allclose(dx.cpu().numpy(), dx_ref, rtol=1e-4, atol=1e-4 * np.abs(dx_ref).max())
+
+
+@pytest.mark.parametrize("clip", [0.0, 1e-3, 1e6])
+def test_clip_sgd_op_matches_oracle(clip):
+    rng = np.random.default_rng(8)
+    nslots, B, n, eta = 3, 4, 10000, 0.05
+    W = rng.normal(0, 0.02, (nslots, B, n)).astype(np.float32)
+    G = rng.normal(0, 0.01, (nslots, B, n)).astype(np.float32)
+    W32 = torch.from_numpy(W).cuda()
+    Wop = torch.zeros((nslots, B, n), dtype=torch.bfloat16, device="cuda")
+    dW = torch.from_numpy(G).cuda()
+    ws = torch.empty(T.clip_sgd_workspace_size(nslots, B, n), dtype=torch.uint8, device="cuda")
+    norm = torch.zeros(B, device="cuda")
+    scale = torch.zeros(B, device="cuda")
+    T.clip_sgd("bf16", W32, Wop, dW, eta, clip, norm, scale, ws)
+    for s in range(B):
+        grads = [{"g": G[j, s].astype(np.float64)} for j in range(nslots)]
+        sc, nr = oracle.clip_scale(grads, clip)
+        assert abs(float(norm[s]) - nr) <= 1e-5 * nr
+        assert abs(float(scale[s]) - sc) <= 1e-5 * sc
+        want = W[:, s].astype(np.float64) - eta * sc * G[:, s].astype(np.float64)
+        np.testing.assert_allclose(W32[:, s].cpu().numpy(), want, rtol=1e-6, atol=1e-8)
+        np.testing.assert_array_equal(Wop[:, s].float().cpu().numpy(),
+                                      W32[:, s].to(torch.bfloat16).float().cpu().numpy())
+
+
+def test_clip_sgd_nonfinite_sequence_is_skipped():
+    nslots, B, n = 2, 3, 5000
+    W = torch.ones((nslots, B, n), device="cuda")
+    Wop = torch.zeros((nslots, B, n), dtype=torch.bfloat16, device="cuda")
+    dW = torch.full((nslots, B, n), 0.5, device="cuda")
+    dW[1, 1, 7] = float("nan")
+    ws = torch.empty(T.clip_sgd_workspace_size(nslots, B, n), dtype=torch.uint8, device="cuda")
+    with pytest.raises(T.TTTError) as e:
+        T.clip_sgd("bf16", W, Wop, dW, 0.1, 1.0, workspace=ws)
+    assert e.value.status == 5
+    assert torch.all(W[:, 1] == 1.0)
+    assert torch.all(W[:, 0] < 1.0) and torch.all(W[:, 2] < 1.0)
