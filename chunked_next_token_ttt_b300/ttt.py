@@ -272,6 +272,8 @@ def _ops_lib():
             "ttt_clip_sgd": ([_I, _I, _I, ctypes.c_longlong, _P, _P, _P, ctypes.c_float, ctypes.c_float,
                               _P, _P, _P, ctypes.c_size_t, _P], _I),
             "ttt_clip_sgd_workspace_size": ([_I, _I, ctypes.c_longlong], ctypes.c_size_t),
+            "ttt_clip_sgd_noalloc": ([_I, _I, _I, ctypes.c_longlong, _P, _P, _P, ctypes.c_float,
+                                      ctypes.c_float, _P, _P, _P], _I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -329,3 +331,10 @@ def clip_sgd(dtype, W32, Wop, dW, eta, clip, norm_out=None, scale_out=None, work
                                    0 if workspace is None else workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "ttt_clip_sgd")
 
+
+def clip_sgd_noalloc(dtype, W32, Wop, dW, eta, clip, norm_out=None, scale_out=None, stream=None):
+    """ttt_clip_sgd with the library's fixed device scratch instead of a workspace."""
+    nslots, B, n = W32.shape
+    _check(_ops_lib().ttt_clip_sgd_noalloc(DTYPE[dtype], nslots, B, n, _ptr(W32), _ptr(Wop), _ptr(dW), eta,
+                                           clip, _ptr(norm_out), _ptr(scale_out), _stream(stream)),
+           "ttt_clip_sgd_noalloc")

@@ -87,6 +87,28 @@ ttt_status ttt_clip_sgd(int dtype, int nslots, int B, long long n, float* W32, v
                         void* workspace, size_t workspace_bytes, ttt_stream stream);
 size_t ttt_clip_sgd_workspace_size(int nslots, int B, long long n);
 
+/* ttt_clip_sgd without a workspace, for callers that cannot allocate device
+ * memory: their device memory is owned by their own allocator or budget and
+ * they have no buffer to hand over, or they cannot accept cudaMalloc's
+ * implicit synchronisation in their loop.  The pages have no counterpart: this
+ * is a property of the library, not of the method.
+ * Same arguments, results and status codes as ttt_clip_sgd.  The scratch is a
+ * fixed device array of TTT_CLIP_SGD_NOALLOC_MAX_FLOATS floats (4 MiB) inside
+ * the library, held by every GPU that loads it until the process exits; the
+ * call allocates nothing (no cudaMalloc, cudaFree or allocating routine).
+ * Sizes needing more than the maximum, i.e. nslots * B * ceil(n / 8192) + B + 1
+ * floats, return TTT_ERR_BAD_SHAPE with a message naming the limit.
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls share the one array: calls that overlap on the GPU (on
+ * different streams or from different host threads) race and must be
+ * serialised by the caller.  Nothing in the array needs to start at zero:
+ * each call writes every word before it reads it. */
+#define TTT_CLIP_SGD_NOALLOC_MAX_FLOATS (1 << 20)
+ttt_status ttt_clip_sgd_noalloc(int dtype, int nslots, int B, long long n, float* W32, void* Wop,
+                                const float* dW, float eta, float clip, float* norm_out,
+                                float* scale_out, ttt_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
