@@ -72,6 +72,12 @@ def chunk_flops(wl, rows=None):
     return per
 
 
+def chunk_flops_fwd_one(wl):
+    """FLOPs of the p_{T+1} forward (one row per sequence) by class."""
+    f = chunk_flops(wl, rows=1)
+    return {k: f[k] for k in ("gemm_prefix", "gemm_fast_fwd", "gemm_head")}
+
+
 def chunk_bytes(wl):
     """Algorithmic HBM bytes of one chunk step, by class (see DESIGN: each
     tensor read or written once; the V-wide logits buffer counted once in
@@ -305,14 +311,24 @@ def run_ours(args, wl, rank, world, local_rank):
     clk_sum = clk.summary()
     dom_avg_s = dom_ms / 1e3 / max(1, dom_n)
     launches_per_step_dom = dom_n / args.steps
+    if dom_n % args.steps:
+        raise RuntimeError("profiled launches are not a whole number per step")
     if dom in flops:
-        per_launch = flops[dom] * wl.n_chunks / launches_per_step_dom
+        # the class's algorithmic FLOPs per step: every chunk plus the p_{T+1} forward (rows = 1)
+        fl_step = flops[dom] * wl.n_chunks + chunk_flops_fwd_one(wl).get(dom, 0.0)
+        per_launch = fl_step / launches_per_step_dom
         achieved = per_launch / dom_avg_s / 1e12
-        if wl.dtype == "fp32":
+        split = wl.dtype == "fp32" and os.environ.get("TTT_FP32_STORAGE") != "f32" and wl.chunk >= 64
+        if wl.dtype == "fp32" and not split:
             # fp32 FMA on the SIMT pipes: 148 SMs x 128 lanes x 2 FLOP x max SM clock
             peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
             roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"}
+        elif split:
+            # fp32-accurate products as three bf16 tensor-core products each
+            peak = pk["bf16_tflops_sustained"] / 3.0
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": f"{pk['source']} bf16 sustained / 3 (bf16x3 split products)"}
         else:
             peak = pk["bf16_tflops_sustained"]
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -73,7 +73,7 @@ ttt_status launch_clip_sgd(int dtype, int nslots, int B, long long n, float* W32
   clip_finalize_kernel<<<1, kThreads, 0, st>>>(B, nslots * pieces, partials, clip, scale, norm_out, scale_out,
                                                flag);
   TTT_CHECK_LAUNCH();
-  return launch_sgd_update(dtype, nslots, B, n, W32, Wop, dW, scale, eta, st);
+  return launch_sgd_update(dtype, nslots, B, n, W32, Wop, 0, dW, scale, eta, st);
 }
 
 }  // namespace ttt

@@ -45,6 +45,60 @@ template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
 
+// Storage of "operand" tensors (GEMM inputs and the outputs that feed them):
+//   float  fp32 values;
+//   bf16   bf16 values;
+//   Split  fp32-accurate pairs kept as two bf16 planes, hi = bf16(v) at p[i]
+//          and lo = bf16(v - hi) at p[lo + i]; a product of two split values is
+//          taken as hi*hi + hi*lo + lo*hi (the bf16x3 scheme of Henry, Tang and
+//          Heinecke, "Leveraging the bfloat16 Artificial Intelligence Datatype
+//          for Higher-Precision Computations", 2019), about 2^-17 relative.
+struct Split {};
+
+enum Storage { ST_F32 = 0, ST_BF16 = 1, ST_SPLIT = 2 };
+
+template <typename S> struct OpIO;
+template <> struct OpIO<float> {
+  __device__ __forceinline__ static float load(const void* p, long long, long long i) {
+    return static_cast<const float*>(p)[i];
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float v) {
+    static_cast<float*>(p)[i] = v;
+  }
+  __device__ __forceinline__ static void copy(void* d, long long dlo, const void* s, long long slo, long long i) {
+    static_cast<float*>(d)[i] = static_cast<const float*>(s)[i];
+  }
+};
+template <> struct OpIO<bf16> {
+  __device__ __forceinline__ static float load(const void* p, long long, long long i) {
+    return __bfloat162float(static_cast<const bf16*>(p)[i]);
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float v) {
+    static_cast<bf16*>(p)[i] = __float2bfloat16_rn(v);
+  }
+  __device__ __forceinline__ static void copy(void* d, long long, const void* s, long long, long long i) {
+    static_cast<bf16*>(d)[i] = static_cast<const bf16*>(s)[i];
+  }
+};
+template <> struct OpIO<Split> {
+  __device__ __forceinline__ static float load(const void* p, long long lo, long long i) {
+    const bf16* q = static_cast<const bf16*>(p);
+    return __bfloat162float(q[i]) + __bfloat162float(q[lo + i]);
+  }
+  __device__ __forceinline__ static void store(void* p, long long lo, long long i, float v) {
+    bf16* q = static_cast<bf16*>(p);
+    const bf16 h = __float2bfloat16_rn(v);
+    q[i] = h;
+    q[lo + i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+  __device__ __forceinline__ static void copy(void* d, long long dlo, const void* s, long long slo, long long i) {
+    bf16* dq = static_cast<bf16*>(d);
+    const bf16* sq = static_cast<const bf16*>(s);
+    dq[i] = sq[i];
+    dq[dlo + i] = sq[slo + i];
+  }
+};
+
 // Exact (erf) GELU and its derivative, z * Phi(z) and Phi(z) + z phi(z).
 __device__ __forceinline__ float gelu_f(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));

@@ -73,8 +73,12 @@ static ttt_status run(ttt_handle* h, int cls, cudaStream_t st, int nkernels, F&&
   return TTT_OK;
 }
 
-static void* op_at(const ttt_handle* h, void* base, long long elems) {
-  return static_cast<char*>(base) + elems * (long long)h->esz;
+// Slice of an operand buffer starting `elems` elements in (same lo plane offset).
+static OpBuf op_at(const ttt_handle* h, const OpBuf& b, long long elems) {
+  OpBuf r;
+  r.p = static_cast<char*>(b.p) + elems * (long long)h->esz;
+  r.lo = b.lo;
+  return r;
 }
 
 static int gemm_count(const GemmDesc&) { return 1; }
@@ -82,8 +86,15 @@ static int gemm_count(const GemmDesc&) { return 1; }
 static ttt_status rungemm(ttt_handle* h, int cls, const GemmDesc& g_in, cudaStream_t st) {
   GemmDesc g = g_in;
   g.err = h->flag;
+  g.dtype = h->stg;
   return run(h, cls, st, gemm_count(g), [&] { return gemm(g, st); });
 }
+
+// Operand setters for a GemmDesc from OpBufs.
+static void setA(GemmDesc& g, const OpBuf& b, long long ld, long long s = 0) { g.A = b.p; g.loA = b.lo; g.lda = ld; g.sA = s; }
+static void setB(GemmDesc& g, const OpBuf& b, long long ld, long long s = 0) { g.B = b.p; g.loB = b.lo; g.ldb = ld; g.sB = s; }
+static void setOut(GemmDesc& g, const OpBuf& b, long long ld, long long s = 0) { g.out = b.p; g.loO = b.lo; g.ldo = ld; g.sO = s; }
+static void setOut2(GemmDesc& g, const OpBuf& b, long long ld, long long s = 0) { g.out2 = b.p; g.loO2 = b.lo; g.ldo2 = ld; g.sO2 = s; }
 
 // ---------------------------------------------------------------- forward
 // Forward over B * tv.rows rows with the current (or committed) fast weights.
@@ -96,114 +107,125 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
   tv.vocab = h->V;
   tv.err = h->flag;
   const int B = h->B, rows = tv.rows, M = B * rows, d = h->d, f = h->f, V = h->V;
-  const int dt = h->dtype;
-  void* Wop = committed ? h->Wcop : h->Wop;
-  void* cur_op = h->dm.n_prefix > 0 ? h->xop : h->hlvl[0];
-  TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(dt, B, tv, h->E, d, h->x32, cur_op, st); }));
+  const int stg = h->stg;
+  const OpBuf& Wop = committed ? h->Wcop : h->Wop;
+  OpBuf cur = h->dm.n_prefix > 0 ? h->xop : h->hlvl[0];
+  TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(stg, B, tv, h->E, d, h->x32, cur.p, cur.lo, st); }));
 
   for (int p = 0; p < h->dm.n_prefix; ++p) {
-    void* const* W = &h->prefix[(size_t)p * h->nm];
-    void* next_op = (p == h->dm.n_prefix - 1) ? h->hlvl[0] : h->xop;
+    const OpBuf* W = &h->prefix[(size_t)p * h->nm];
+    const OpBuf next = (p == h->dm.n_prefix - 1) ? h->hlvl[0] : h->xop;
     if (h->dm.block_kind == TTT_BLOCK_GELU) {
       GemmDesc g;
-      g.M = M; g.N = f; g.K = d; g.dtype = dt;
-      g.A = cur_op; g.lda = d; g.B = W[0]; g.ldb = d;
-      g.epi = EPI_GELU; g.out = nullptr; g.out2 = h->tmp_a; g.ldo2 = f;
+      g.M = M; g.N = f; g.K = d;
+      setA(g, cur, d); setB(g, W[0], d);
+      g.epi = EPI_GELU; g.out = nullptr; setOut2(g, h->tmp_a, f);
       TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
     } else {
       GemmDesc g;
-      g.M = M; g.N = f; g.K = d; g.dtype = dt;
-      g.A = cur_op; g.lda = d; g.B = W[0]; g.ldb = d;
+      g.M = M; g.N = f; g.K = d;
+      setA(g, cur, d); setB(g, W[0], d);
       g.epi = EPI_STORE_F32; g.out = h->tmp_g; g.ldo = f;
       TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
-      g.B = W[1]; g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; g.out = h->tmp_a; g.ldo = f;
+      setB(g, W[1], d); g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; setOut(g, h->tmp_a, f);
       TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
     }
     GemmDesc g2;
-    g2.M = M; g2.N = d; g2.K = f; g2.dtype = dt;
-    g2.A = h->tmp_a; g2.lda = f; g2.B = W[h->nm - 1]; g2.ldb = f;
+    g2.M = M; g2.N = d; g2.K = f;
+    setA(g2, h->tmp_a, f); setB(g2, W[h->nm - 1], f);
     g2.epi = EPI_RESID; g2.aux = h->x32; g2.ldx = d; g2.out = h->x32; g2.ldo = d;
-    g2.out2 = next_op; g2.ldo2 = d;
+    setOut2(g2, next, d);
     TTT_TRY(rungemm(h, K_GEMM_PREFIX, g2, st));
-    cur_op = next_op;
+    cur = next;
   }
 
   for (int l = 0; l < h->dm.n_fast; ++l) {
-    void* hin = h->hlvl[l];
-    void* a_out = train ? h->ast[l] : h->tmp_a;
-    void* next_op = (l + 1 < h->dm.n_fast) ? h->hlvl[l + 1] : nullptr;
+    const OpBuf hin = h->hlvl[l];
+    const OpBuf a_out = train ? h->ast[l] : h->tmp_a;
+    const bool has_next = l + 1 < h->dm.n_fast;
     const int s_down = h->slot_of[(size_t)l * h->nm + (h->nm - 1)];
     if (h->dm.block_kind == TTT_BLOCK_GELU) {
       const int s_up = h->slot_of[(size_t)l * h->nm + 0];
       GemmDesc g;
-      g.M = rows; g.N = f; g.K = d; g.batch = B; g.dtype = dt;
-      g.A = hin; g.lda = d; g.sA = (long long)rows * d;
-      g.B = op_at(h, Wop, (long long)s_up * B * h->n); g.ldb = d; g.sB = h->n;
+      g.M = rows; g.N = f; g.K = d; g.batch = B;
+      setA(g, hin, d, (long long)rows * d);
+      setB(g, op_at(h, Wop, (long long)s_up * B * h->n), d, h->n);
       g.epi = EPI_GELU;
-      g.out = train ? h->zst[l] : nullptr; g.ldo = f; g.sO = (long long)rows * f;
-      g.out2 = a_out; g.ldo2 = f; g.sO2 = (long long)rows * f;
+      if (train) setOut(g, h->zst[l], f, (long long)rows * f);
+      else g.out = nullptr;
+      setOut2(g, a_out, f, (long long)rows * f);
       TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
     } else {
-      void* const* W = &h->fastfrozen[(size_t)l * h->nm];
+      const OpBuf* W = &h->fastfrozen[(size_t)l * h->nm];
       GemmDesc g;
-      g.M = M; g.N = f; g.K = d; g.dtype = dt;
-      g.A = hin; g.lda = d; g.B = W[0]; g.ldb = d;
+      g.M = M; g.N = f; g.K = d;
+      setA(g, hin, d); setB(g, W[0], d);
       g.epi = EPI_STORE_F32; g.out = h->tmp_g; g.ldo = f;
       TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
-      g.B = W[1]; g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; g.out = a_out; g.ldo = f;
+      setB(g, W[1], d); g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; setOut(g, a_out, f);
       TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
     }
     GemmDesc g2;
-    g2.M = rows; g2.N = d; g2.K = f; g2.batch = B; g2.dtype = dt;
-    g2.A = a_out; g2.lda = f; g2.sA = (long long)rows * f;
-    g2.B = op_at(h, Wop, (long long)s_down * B * h->n); g2.ldb = f; g2.sB = h->n;
+    g2.M = rows; g2.N = d; g2.K = f; g2.batch = B;
+    setA(g2, a_out, f, (long long)rows * f);
+    setB(g2, op_at(h, Wop, (long long)s_down * B * h->n), f, h->n);
     g2.epi = EPI_RESID; g2.aux = h->x32; g2.ldx = d; g2.sX = (long long)rows * d;
     g2.out = h->x32; g2.ldo = d; g2.sO = (long long)rows * d;
-    g2.out2 = next_op; g2.ldo2 = d; g2.sO2 = (long long)rows * d;
+    if (has_next) setOut2(g2, h->hlvl[l + 1], d, (long long)rows * d);
     TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g2, st));
   }
 
-  TTT_TRY(run(h, K_RMSNORM_FWD, st, 1,
-              [&] { return launch_rmsnorm_fwd(dt, M, d, h->x32, h->dm.rms_eps, h->y, h->rstd, st); }));
+  TTT_TRY(run(h, K_RMSNORM_FWD, st, 1, [&] {
+    return launch_rmsnorm_fwd(stg, M, d, h->x32, h->dm.rms_eps, h->y.p, h->y.lo, h->rstd, st);
+  }));
 
   GemmDesc gh;
-  gh.M = M; gh.N = V; gh.K = d; gh.dtype = dt;
-  gh.A = h->y; gh.lda = d; gh.B = h->U; gh.ldb = d;
+  gh.M = M; gh.N = V; gh.K = d;
+  setA(gh, h->y, d); setB(gh, h->U, d);
   if (head_f32) {
     gh.epi = EPI_STORE_F32; gh.out = h->logits32; gh.ldo = V;
     return rungemm(h, K_GEMM_HEAD, gh, st);
   }
-  gh.epi = EPI_STORE; gh.out = h->logits; gh.ldo = V;
+  if (stg == ST_SPLIT) {
+    gh.epi = EPI_STORE_F32; gh.out = h->logits; gh.ldo = V;
+  } else {
+    gh.epi = EPI_STORE; gh.out = h->logits; gh.ldo = V;
+  }
   TTT_TRY(rungemm(h, K_GEMM_HEAD, gh, st));
   const float scale = tv.n_valid > 0 ? 1.0f / (float)tv.n_valid : 0.0f;
   return run(h, K_CE, st, 1, [&] {
-    return launch_ce(dt, B, tv, V, h->logits, V, scale, train, losses, loss_ld, loss_off, h->row_loss, st);
+    return launch_ce(stg, B, tv, V, h->logits, V, scale, train, losses, loss_ld, loss_off, h->row_loss, st);
   });
 }
 
 // ---------------------------------------------------------------- backward + update
 static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
-  const int B = h->B, M = B * rows, d = h->d, f = h->f, V = h->V, dt = h->dtype;
+  const int B = h->B, M = B * rows, d = h->d, f = h->f, V = h->V, stg = h->stg;
   GemmDesc gy;
-  gy.M = M; gy.N = d; gy.K = V; gy.dtype = dt;
-  gy.A = h->logits; gy.lda = V; gy.B = h->U; gy.b_kmajor = false; gy.ldb = d;
+  gy.M = M; gy.N = d; gy.K = V;
+  if (stg == ST_SPLIT) {
+    // dlogits were written inside each fp32 row as [hi: V bf16 | lo: V bf16]
+    gy.A = h->logits; gy.lda = 2LL * V; gy.loA = V;
+  } else {
+    gy.A = h->logits; gy.lda = V;
+  }
+  setB(gy, h->U, d); gy.b_kmajor = false;
   gy.epi = EPI_STORE_F32; gy.out = h->dy32; gy.ldo = d;
   TTT_TRY(rungemm(h, K_GEMM_HEAD_BWD, gy, st));
   TTT_TRY(run(h, K_RMSNORM_BWD, st, 1, [&] {
-    return launch_rmsnorm_bwd(dt, M, d, h->x32, h->rstd, h->dy32, h->dh32, h->dhop, st);
+    return launch_rmsnorm_bwd(stg, M, d, h->x32, h->rstd, h->dy32, h->dh32, h->dhop.p, h->dhop.lo, st);
   }));
 
   PartialSlots ps{};
   long long poff = 0;
   auto dw_gemm = [&](GemmDesc& g, int slot) -> ttt_status {
     g.epi = EPI_DW;
+    g.dtype = h->stg;
     g.partials = h->partials + poff;
     const int tiles = gemm_partial_tiles(g);
     if (ps.n >= 16 || poff + (long long)tiles * B > h->partial_cap)
       return fail(TTT_ERR_UNSUPPORTED, "too many gradient-norm partial slots");
-    g.epi = EPI_DW;
     g.out = h->dW + (long long)slot * B * h->n; g.sO = h->n;
-    g.partials = h->partials + poff;
     ps.off[ps.n] = poff;
     ps.tiles[ps.n] = tiles;
     ps.n++;
@@ -216,43 +238,43 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
       const int s1 = h->slot_of[(size_t)l * 2 + 0], s2 = h->slot_of[(size_t)l * 2 + 1];
       // dW2 = dh^T a   [d, f], K = rows
       GemmDesc g;
-      g.M = d; g.N = f; g.K = rows; g.batch = B; g.dtype = dt;
-      g.a_kmajor = false; g.A = h->dhop; g.lda = d; g.sA = (long long)rows * d;
-      g.b_kmajor = false; g.B = h->ast[l]; g.ldb = f; g.sB = (long long)rows * f;
+      g.M = d; g.N = f; g.K = rows; g.batch = B;
+      g.a_kmajor = false; setA(g, h->dhop, d, (long long)rows * d);
+      g.b_kmajor = false; setB(g, h->ast[l], f, (long long)rows * f);
       g.ldo = f;
       TTT_TRY(dw_gemm(g, s2));
       // dz = (dh W2) * GELU'(z), in place over the z stash
       GemmDesc gz;
-      gz.M = rows; gz.N = f; gz.K = d; gz.batch = B; gz.dtype = dt;
-      gz.A = h->dhop; gz.lda = d; gz.sA = (long long)rows * d;
-      gz.b_kmajor = false; gz.B = op_at(h, h->Wop, (long long)s2 * B * h->n); gz.ldb = f; gz.sB = h->n;
-      gz.epi = EPI_DGELU; gz.aux = h->zst[l]; gz.ldx = f; gz.sX = (long long)rows * f;
-      gz.out = h->zst[l]; gz.ldo = f; gz.sO = (long long)rows * f;
+      gz.M = rows; gz.N = f; gz.K = d; gz.batch = B;
+      setA(gz, h->dhop, d, (long long)rows * d);
+      gz.b_kmajor = false; setB(gz, op_at(h, h->Wop, (long long)s2 * B * h->n), f, h->n);
+      gz.epi = EPI_DGELU; gz.aux = h->zst[l].p; gz.loX = h->zst[l].lo; gz.ldx = f; gz.sX = (long long)rows * f;
+      setOut(gz, h->zst[l], f, (long long)rows * f);
       TTT_TRY(rungemm(h, K_GEMM_BWD_DX, gz, st));
       // dW1 = dz^T h_in   [f, d]
       GemmDesc g1;
-      g1.M = f; g1.N = d; g1.K = rows; g1.batch = B; g1.dtype = dt;
-      g1.a_kmajor = false; g1.A = h->zst[l]; g1.lda = f; g1.sA = (long long)rows * f;
-      g1.b_kmajor = false; g1.B = h->hlvl[l]; g1.ldb = d; g1.sB = (long long)rows * d;
+      g1.M = f; g1.N = d; g1.K = rows; g1.batch = B;
+      g1.a_kmajor = false; setA(g1, h->zst[l], f, (long long)rows * f);
+      g1.b_kmajor = false; setB(g1, h->hlvl[l], d, (long long)rows * d);
       g1.ldo = d;
       TTT_TRY(dw_gemm(g1, s1));
       if (l > 0) {
         // dh_below = dh + dz W1
         GemmDesc gb;
-        gb.M = rows; gb.N = d; gb.K = f; gb.batch = B; gb.dtype = dt;
-        gb.A = h->zst[l]; gb.lda = f; gb.sA = (long long)rows * f;
-        gb.b_kmajor = false; gb.B = op_at(h, h->Wop, (long long)s1 * B * h->n); gb.ldb = d; gb.sB = h->n;
+        gb.M = rows; gb.N = d; gb.K = f; gb.batch = B;
+        setA(gb, h->zst[l], f, (long long)rows * f);
+        gb.b_kmajor = false; setB(gb, op_at(h, h->Wop, (long long)s1 * B * h->n), d, h->n);
         gb.epi = EPI_RESID; gb.aux = h->dh32; gb.ldx = d; gb.sX = (long long)rows * d;
         gb.out = h->dh32; gb.ldo = d; gb.sO = (long long)rows * d;
-        gb.out2 = h->dhop; gb.ldo2 = d; gb.sO2 = (long long)rows * d;
+        setOut2(gb, h->dhop, d, (long long)rows * d);
         TTT_TRY(rungemm(h, K_GEMM_BWD_DX, gb, st));
       }
     } else {
       const int sd = h->slot_of[(size_t)l * 3 + 2];
       GemmDesc g;
-      g.M = d; g.N = f; g.K = rows; g.batch = B; g.dtype = dt;
-      g.a_kmajor = false; g.A = h->dhop; g.lda = d; g.sA = (long long)rows * d;
-      g.b_kmajor = false; g.B = h->ast[l]; g.ldb = f; g.sB = (long long)rows * f;
+      g.M = d; g.N = f; g.K = rows; g.batch = B;
+      g.a_kmajor = false; setA(g, h->dhop, d, (long long)rows * d);
+      g.b_kmajor = false; setB(g, h->ast[l], f, (long long)rows * f);
       g.ldo = f;
       TTT_TRY(dw_gemm(g, sd));
     }
@@ -261,7 +283,7 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
     return launch_norm_finalize(B, ps, h->partials, h->hp.clip, h->scale, h->gnorm, h->flag, st);
   }));
   TTT_TRY(run(h, K_SGD, st, 1, [&] {
-    return launch_sgd_update(dt, h->nslots, B, h->n, h->W32, h->Wop, h->dW, h->scale, h->hp.eta, st);
+    return launch_sgd_update(stg, h->nslots, B, h->n, h->W32, h->Wop.p, h->Wop.lo, h->dW, h->scale, h->hp.eta, st);
   }));
   h->chunks_done++;
   return TTT_OK;
@@ -283,8 +305,8 @@ static ttt_status settle_event(ttt_handle* h, const int32_t* q, int Lq, float* A
   TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, false, st));
   TTT_TRY(run(h, K_SETTLE, st, 1, [&] { return launch_seq_mean(h->B, Lq, Lq - 1, h->row_loss, h->Lw, st); }));
   return run(h, K_SETTLE, st, 2, [&] {
-    return launch_settle_apply(h->dtype, h->nslots, h->B, h->n, h->Lc, h->Lw, A, acc, h->W32, h->Wop,
-                               h->Wc32, h->Wcop, st);
+    return launch_settle_apply(h->stg, h->nslots, h->B, h->n, h->Lc, h->Lw, A, acc, h->W32, h->Wop.p,
+                               h->Wc32, h->Wcop.p, h->Wop.lo, st);
   });
 }
 
@@ -297,11 +319,11 @@ static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t 
 
 static ttt_status reset_weights(ttt_handle* h, cudaStream_t st) {
   TTT_TRY(run(h, K_OTHER, st, 1, [&] {
-    return launch_broadcast_w0(h->dtype, h->nslots, h->B, h->n, h->W0, h->W32, h->Wop, st);
+    return launch_broadcast_w0(h->stg, h->nslots, h->B, h->n, h->W0, h->W32, h->Wop.p, h->Wop.lo, st);
   }));
   if (h->Wc32) {
     TTT_TRY(run(h, K_OTHER, st, 1, [&] {
-      return launch_broadcast_w0(h->dtype, h->nslots, h->B, h->n, h->W0, h->Wc32, h->Wcop, st);
+      return launch_broadcast_w0(h->stg, h->nslots, h->B, h->n, h->W0, h->Wc32, h->Wcop.p, h->Wcop.lo, st);
     }));
   }
   h->pend_count = 0;
@@ -416,7 +438,19 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   h->nm = D.block_kind == TTT_BLOCK_GELU ? 2 : 3;
   h->n = (long long)D.d * D.d_ff;
   h->dtype = D.dtype;
-  h->esz = D.dtype == TTT_DTYPE_BF16 ? 2 : 4;
+  // fp32-accurate workloads run their GEMMs on the tensor cores as bf16 hi/lo
+  // pairs when every leading dimension suits TMA and the chunk fills a tile
+  // row block; otherwise they stay in plain fp32 (SIMT GEMMs).
+  const char* env_stg = getenv("TTT_FP32_STORAGE");
+  const bool force_f32 = env_stg && std::string(env_stg) == "f32";
+  if (D.dtype == TTT_DTYPE_BF16)
+    h->stg = ST_BF16;
+  else if (!force_f32 && hp->chunk >= 64 && D.d % 8 == 0 && D.d_ff % 8 == 0 && D.vocab % 8 == 0 &&
+           D.vocab <= ce_split_max_vocab())
+    h->stg = ST_SPLIT;
+  else
+    h->stg = ST_F32;
+  h->esz = h->stg == ST_F32 ? 4 : 2;
   h->slot_of.assign((size_t)D.n_fast * h->nm, -1);
   for (int l = 0; l < D.n_fast; ++l)
     for (int m = 0; m < h->nm; ++m) {
@@ -427,30 +461,43 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   auto bail = [&](ttt_status s) { ttt_destroy(h); return s; };
   const int B = h->B, d = h->d, f = h->f, V = h->V;
   const size_t es = h->esz;
+  const bool split = h->stg == ST_SPLIT;
   cudaStream_t st = 0;
+  // an operand buffer of `count` elements (two planes for ST_SPLIT)
+  auto op_alloc = [&](OpBuf* b, size_t count) -> ttt_status {
+    TTT_TRY(dalloc(h, &b->p, count * es * (split ? 2 : 1)));
+    b->lo = split ? (long long)count : 0;
+    return TTT_OK;
+  };
 
   // ---- weights
   float* stage = nullptr;
   const size_t big = (size_t)V * d > (size_t)h->n ? (size_t)V * d : (size_t)h->n;
   ttt_status s;
   if ((s = dalloc(h, &stage, big * 4)) != TTT_OK) return bail(s);
-  auto upload = [&](const float* src, size_t count, void* dst) -> ttt_status {
+  auto upload = [&](const float* src, size_t count, const OpBuf& dst, int stg) -> ttt_status {
     if (!src) return fail(TTT_ERR_BAD_ARG, "null weight matrix");
     TTT_CUDA(cudaMemcpy(stage, src, count * 4, cudaMemcpyDefault));
-    TTT_TRY(launch_cast(h->dtype, (long long)count, stage, dst, st));
+    TTT_TRY(launch_cast(stg, (long long)count, stage, dst.p, dst.lo, st));
     TTT_CUDA(cudaStreamSynchronize(st));
     return TTT_OK;
   };
-  if ((s = dalloc(h, &h->E, (size_t)V * d * es)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->U, (size_t)V * d * es)) != TTT_OK) return bail(s);
-  if ((s = upload(w->E, (size_t)V * d, h->E)) != TTT_OK) return bail(s);
-  if ((s = upload(w->U, (size_t)V * d, h->U)) != TTT_OK) return bail(s);
-  h->prefix.assign((size_t)D.n_prefix * h->nm, nullptr);
-  for (size_t i = 0; i < h->prefix.size(); ++i) {
-    if ((s = dalloc(h, &h->prefix[i], (size_t)h->n * es)) != TTT_OK) return bail(s);
-    if ((s = upload(w->prefix[i], (size_t)h->n, h->prefix[i])) != TTT_OK) return bail(s);
+  {
+    // E feeds only the embedding gather: bf16 for bf16 workloads, fp32 otherwise
+    const int e_stg = h->stg == ST_BF16 ? ST_BF16 : ST_F32;
+    OpBuf eb;
+    if ((s = dalloc(h, &eb.p, (size_t)V * d * (e_stg == ST_BF16 ? 2 : 4))) != TTT_OK) return bail(s);
+    if ((s = upload(w->E, (size_t)V * d, eb, e_stg)) != TTT_OK) return bail(s);
+    h->E = eb.p;
   }
-  h->fastfrozen.assign((size_t)D.n_fast * h->nm, nullptr);
+  if ((s = op_alloc(&h->U, (size_t)V * d)) != TTT_OK) return bail(s);
+  if ((s = upload(w->U, (size_t)V * d, h->U, h->stg)) != TTT_OK) return bail(s);
+  h->prefix.assign((size_t)D.n_prefix * h->nm, OpBuf());
+  for (size_t i = 0; i < h->prefix.size(); ++i) {
+    if ((s = op_alloc(&h->prefix[i], (size_t)h->n)) != TTT_OK) return bail(s);
+    if ((s = upload(w->prefix[i], (size_t)h->n, h->prefix[i], h->stg)) != TTT_OK) return bail(s);
+  }
+  h->fastfrozen.assign((size_t)D.n_fast * h->nm, OpBuf());
   if ((s = dalloc(h, &h->W0, (size_t)h->nslots * h->n * 4)) != TTT_OK) return bail(s);
   for (size_t i = 0; i < h->fastfrozen.size(); ++i) {
     const int slot = h->slot_of[i];
@@ -459,17 +506,17 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
       cudaError_t e = cudaMemcpy(h->W0 + (size_t)slot * h->n, w->fast[i], (size_t)h->n * 4, cudaMemcpyDefault);
       if (e != cudaSuccess) return bail(cuda_fail(e, "upload W0", __FILE__, __LINE__));
     } else {
-      if ((s = dalloc(h, &h->fastfrozen[i], (size_t)h->n * es)) != TTT_OK) return bail(s);
-      if ((s = upload(w->fast[i], (size_t)h->n, h->fastfrozen[i])) != TTT_OK) return bail(s);
+      if ((s = op_alloc(&h->fastfrozen[i], (size_t)h->n)) != TTT_OK) return bail(s);
+      if ((s = upload(w->fast[i], (size_t)h->n, h->fastfrozen[i], h->stg)) != TTT_OK) return bail(s);
     }
   }
   const size_t arena = (size_t)h->nslots * B * h->n;
   if ((s = dalloc(h, &h->W32, arena * 4)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->Wop, arena * es)) != TTT_OK) return bail(s);
+  if ((s = op_alloc(&h->Wop, arena)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dW, arena * 4)) != TTT_OK) return bail(s);
   // the committed copy serves Settlement (prefill events and ttt_settle)
   if ((s = dalloc(h, &h->Wc32, arena * 4)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->Wcop, arena * es)) != TTT_OK) return bail(s);
+  if ((s = op_alloc(&h->Wcop, arena)) != TTT_OK) return bail(s);
 
   // ---- workspace
   int rows_max = h->b;
@@ -478,26 +525,26 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   h->Mmax = B * rows_max;
   const size_t Mm = (size_t)h->Mmax;
   if ((s = dalloc(h, &h->x32, Mm * d * 4)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->xop, Mm * d * es)) != TTT_OK) return bail(s);
-  h->hlvl.assign(D.n_fast, nullptr);
-  h->zst.assign(D.n_fast, nullptr);
-  h->ast.assign(D.n_fast, nullptr);
+  if ((s = op_alloc(&h->xop, Mm * d)) != TTT_OK) return bail(s);
+  h->hlvl.assign(D.n_fast, OpBuf());
+  h->zst.assign(D.n_fast, OpBuf());
+  h->ast.assign(D.n_fast, OpBuf());
   for (int l = 0; l < D.n_fast; ++l) {
-    if ((s = dalloc(h, &h->hlvl[l], Mm * d * es)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->hlvl[l], Mm * d)) != TTT_OK) return bail(s);
     if (D.block_kind == TTT_BLOCK_GELU)
-      if ((s = dalloc(h, &h->zst[l], Mm * f * es)) != TTT_OK) return bail(s);
-    if ((s = dalloc(h, &h->ast[l], Mm * f * es)) != TTT_OK) return bail(s);
+      if ((s = op_alloc(&h->zst[l], Mm * f)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->ast[l], Mm * f)) != TTT_OK) return bail(s);
   }
-  if ((s = dalloc(h, &h->tmp_a, Mm * f * es)) != TTT_OK) return bail(s);
+  if ((s = op_alloc(&h->tmp_a, Mm * f)) != TTT_OK) return bail(s);
   if (D.block_kind == TTT_BLOCK_SWIGLU)
     if ((s = dalloc(h, &h->tmp_g, Mm * f * 4)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->y, Mm * d * es)) != TTT_OK) return bail(s);
+  if ((s = op_alloc(&h->y, Mm * d)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->rstd, Mm * 4)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->logits, Mm * V * es)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->logits, Mm * V * (split ? 4 : es))) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->row_loss, Mm * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dy32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dh32, Mm * d * 4)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->dhop, Mm * d * es)) != TTT_OK) return bail(s);
+  if ((s = op_alloc(&h->dhop, Mm * d)) != TTT_OK) return bail(s);
   // partial sums of squares: at most one per 64x64 output tile per matrix and sequence
   h->partial_cap = (long long)h->nslots * B * ceil_div(d, 64) * ceil_div(f, 64);
   if ((s = dalloc(h, &h->partials, (size_t)h->partial_cap * 4)) != TTT_OK) return bail(s);
@@ -538,8 +585,6 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
     if (Lq != h->hp.settle_len) return fail(TTT_ERR_BAD_SHAPE, "Lq must equal settle_len");
   }
   h->launches = 0;
-  h->ev_used = 0;
-  h->prof_launches = 0;
 
   const int32_t* tok = nullptr;
   TTT_TRY(copy_in(h, tokens, (void**)&h->tok_dev, &h->tok_cap, (size_t)B * (T + 1) * 4, (const void**)&tok, st));
@@ -717,8 +762,8 @@ ttt_status ttt_set_state(ttt_handle* h, const void* src, size_t bytes, ttt_strea
   TTT_CUDA(cudaMemcpyAsync(h->Wc32, p + arena, arena, cudaMemcpyDefault, st));
   TTT_CUDA(cudaMemcpyAsync(h->pend, p + 2 * arena, (size_t)h->B * (h->b + 1) * 4, cudaMemcpyDefault, st));
   const long long total = (long long)h->nslots * h->B * h->n;
-  TTT_TRY(launch_cast(h->dtype, total, h->W32, h->Wop, st));
-  TTT_TRY(launch_cast(h->dtype, total, h->Wc32, h->Wcop, st));
+  TTT_TRY(launch_cast(h->stg, total, h->W32, h->Wop.p, h->Wop.lo, st));
+  TTT_TRY(launch_cast(h->stg, total, h->Wc32, h->Wcop.p, h->Wcop.lo, st));
   TTT_CUDA(cudaStreamSynchronize(st));
   h->pend_count = hd.pend_count;
   h->has_context = hd.has_context != 0;

@@ -13,6 +13,13 @@ enum KClass {
   K_RMSNORM_BWD, K_GEMM_BWD_DX, K_GEMM_DW, K_NORM, K_SGD, K_SETTLE, K_OTHER, K_COUNT
 };
 
+// An operand-storage buffer: its pointer and, for ST_SPLIT, the element
+// offset of its lo plane (0 otherwise).
+struct OpBuf {
+  void* p = nullptr;
+  long long lo = 0;
+};
+
 struct ttt_handle {
   ttt_dims dm{};
   ttt_hparams hp{};
@@ -20,38 +27,39 @@ struct ttt_handle {
   int nm = 0;             // matrices per block (2 GELU, 3 SwiGLU)
   int nslots = 0;         // fast matrices in total (arena slots)
   long long n = 0;        // elements of one matrix (d * d_ff)
-  int dtype = 0;
-  size_t esz = 4;         // operand element size
+  int dtype = 0;          // TTT_DTYPE_* requested at create
+  int stg = 0;            // operand storage (ST_F32, ST_BF16, ST_SPLIT)
+  size_t esz = 4;         // bytes per element of one operand plane
   std::vector<int> slot_of;   // [n_fast * nm] -> arena slot or -1
 
-  // frozen weights (operand type)
-  void* E = nullptr;
-  void* U = nullptr;
-  std::vector<void*> prefix;       // [n_prefix * nm]
-  std::vector<void*> fastfrozen;   // [n_fast * nm], null where fast
+  // frozen weights
+  void* E = nullptr;                 // bf16 for ST_BF16, float otherwise
+  OpBuf U;
+  std::vector<OpBuf> prefix;         // [n_prefix * nm]
+  std::vector<OpBuf> fastfrozen;     // [n_fast * nm], empty where fast
 
   // fast weights: arenas [slot][B][n]
   float* W0 = nullptr;     // [slot][n]
   float* W32 = nullptr;
-  void* Wop = nullptr;
+  OpBuf Wop;
   float* Wc32 = nullptr;
-  void* Wcop = nullptr;
+  OpBuf Wcop;
   float* dW = nullptr;
 
   // chunk workspace for up to Mmax rows
   int Mmax = 0;
   float* x32 = nullptr;
-  void* xop = nullptr;
-  std::vector<void*> hlvl, zst, ast;
-  void* tmp_a = nullptr;
+  OpBuf xop;
+  std::vector<OpBuf> hlvl, zst, ast;
+  OpBuf tmp_a;
   float* tmp_g = nullptr;
-  void* y = nullptr;
+  OpBuf y;
   float* rstd = nullptr;
-  void* logits = nullptr;
+  void* logits = nullptr;            // [Mmax, V]: float for ST_SPLIT, operand type otherwise
   float* row_loss = nullptr;
   float* dy32 = nullptr;
   float* dh32 = nullptr;
-  void* dhop = nullptr;
+  OpBuf dhop;
   float* partials = nullptr;
   long long partial_cap = 0;
   ttt::PartialSlots pslots{};

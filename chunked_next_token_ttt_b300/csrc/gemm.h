@@ -18,7 +18,7 @@ enum EpiKind {
 
 struct GemmDesc {
   int M = 0, N = 0, K = 0, batch = 1;
-  int dtype = TTT_DTYPE_FP32;      // operand element type of A and B
+  int dtype = ST_F32;              // operand storage of A, B and op-typed outputs (Storage)
   bool a_kmajor = true;            // A(m,k) at A[m*lda + k] (else A[k*lda + m])
   bool b_kmajor = true;            // B(n,k) at B[n*ldb + k] (else B[k*ldb + n])
   const void* A = nullptr; long long lda = 0, sA = 0;   // strides in elements
@@ -28,6 +28,8 @@ struct GemmDesc {
   void* out2 = nullptr; long long ldo2 = 0, sO2 = 0;
   const void* aux = nullptr; long long ldx = 0, sX = 0;
   float* partials = nullptr;       // EPI_DW: [batch][gemm_partial_tiles()]
+  // ST_SPLIT only: element offset of each op-typed pointer's lo plane
+  long long loA = 0, loB = 0, loO = 0, loO2 = 0, loX = 0;
   int* err = nullptr;              // device status word for bounded-wait timeouts
   int impl = 0;                    // 0 auto, 1 SIMT, 2 tensor cores
 };

@@ -12,14 +12,14 @@ namespace {
 
 constexpr int TM = 64, TN = 64, TK = 16;
 
-template <typename OpT, bool AK, bool BK>
+template <typename S, bool AK, bool BK>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmDesc g) {
+  using IO = OpIO<S>;
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   __shared__ float red[32];
   const int bz = blockIdx.z;
-  const OpT* A = static_cast<const OpT*>(g.A) + bz * g.sA;
-  const OpT* B = static_cast<const OpT*>(g.B) + bz * g.sB;
+  const long long a0 = bz * g.sA, b0 = bz * g.sB;
   const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   float acc[4][4];
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmDesc g) {
       const int gm = m0 + mm, gk = k0 + kk;
       float v = 0.0f;
       if (gm < g.M && gk < g.K)
-        v = to_f(AK ? A[(long long)gm * g.lda + gk] : A[(long long)gk * g.lda + gm]);
+        v = IO::load(g.A, g.loA, a0 + (AK ? (long long)gm * g.lda + gk : (long long)gk * g.lda + gm));
       As[kk][mm] = v;
     }
     for (int i = tid; i < TN * TK; i += 256) {
@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmDesc g) {
       const int gn = n0 + nn, gk = k0 + kk;
       float v = 0.0f;
       if (gn < g.N && gk < g.K)
-        v = to_f(BK ? B[(long long)gn * g.ldb + gk] : B[(long long)gk * g.ldb + gn]);
+        v = IO::load(g.B, g.loB, b0 + (BK ? (long long)gn * g.ldb + gk : (long long)gk * g.ldb + gn));
       Bs[kk][nn] = v;
     }
     __syncthreads();
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmDesc g) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
-      if (n < g.N) sq += epi_value<OpT>(g, bz, m, n, acc[i][j]);
+      if (n < g.N) sq += epi_value<S>(g, bz, m, n, acc[i][j]);
     }
   }
   if (g.epi == EPI_DW) {
@@ -81,12 +81,12 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmDesc g) {
   }
 }
 
-template <typename OpT>
+template <typename S>
 void launch(const GemmDesc& g, dim3 grid, cudaStream_t st) {
-  if (g.a_kmajor && g.b_kmajor) gemm_simt_kernel<OpT, true, true><<<grid, 256, 0, st>>>(g);
-  else if (g.a_kmajor) gemm_simt_kernel<OpT, true, false><<<grid, 256, 0, st>>>(g);
-  else if (g.b_kmajor) gemm_simt_kernel<OpT, false, true><<<grid, 256, 0, st>>>(g);
-  else gemm_simt_kernel<OpT, false, false><<<grid, 256, 0, st>>>(g);
+  if (g.a_kmajor && g.b_kmajor) gemm_simt_kernel<S, true, true><<<grid, 256, 0, st>>>(g);
+  else if (g.a_kmajor) gemm_simt_kernel<S, true, false><<<grid, 256, 0, st>>>(g);
+  else if (g.b_kmajor) gemm_simt_kernel<S, false, true><<<grid, 256, 0, st>>>(g);
+  else gemm_simt_kernel<S, false, false><<<grid, 256, 0, st>>>(g);
 }
 
 }  // namespace
@@ -96,7 +96,8 @@ int gemm_simt_partial_tiles(const GemmDesc& g) { return ceil_div(g.M, TM) * ceil
 ttt_status gemm_simt(const GemmDesc& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return TTT_OK;
   dim3 grid(ceil_div(g.N, TN), ceil_div(g.M, TM), g.batch);
-  if (g.dtype == TTT_DTYPE_BF16) launch<bf16>(g, grid, st);
+  if (g.dtype == ST_BF16) launch<bf16>(g, grid, st);
+  else if (g.dtype == ST_SPLIT) launch<Split>(g, grid, st);
   else launch<float>(g, grid, st);
   TTT_CHECK_LAUNCH();
   return TTT_OK;

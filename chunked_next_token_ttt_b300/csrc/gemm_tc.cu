@@ -8,8 +8,10 @@
 //   warp 1             allocates BN TMEM columns; one lane issues
 //                      tcgen05.mma (M=128, N=BN, K=16) x 4 per slice and
 //                      releases the slot with tcgen05.commit
-//   warps 2..5         epilogue: tcgen05.ld of their 32-lane TMEM quadrant,
-//                      per-element epilogue, stores to global memory
+//   warps 2..9         epilogue: tcgen05.ld of their 32-lane TMEM quadrant
+//                      (two warps per quadrant, splitting the columns), staged
+//                      through shared memory so that each warp then stores
+//                      whole row segments (coalesced), per-element epilogue
 // Operands may be K-major or MN-major (the backward's transposed products);
 // TMA loads MN-major operands as 64-element-wide column panels and the UMMA
 // descriptor's leading/stride byte offsets walk them.
@@ -30,7 +32,9 @@ namespace tc {
 constexpr int BM = 128;        // UMMA M (one CTA, TMEM lanes 0..127 = rows)
 constexpr int BK = 64;         // k-slice: 64 bf16 = 128 bytes = one swizzle span
 constexpr int PANEL = 64;      // MN-major panel width (elements)
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;  // two per 32-lane TMEM quadrant, splitting the columns
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int STAGE_LD = 65;      // staging row stride in floats (64 columns + 1 against bank conflicts)
 constexpr long long kTimeoutNs = 2000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -129,17 +133,24 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Barrier among the epilogue warps only (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * NUM_EPI_WARPS) : "memory");
 }
 
 template <int BN, int STAGES>
@@ -148,14 +159,20 @@ struct Smem {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 1) * 8 + 16 + 4 * 4;
+  static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 1) * 8 + 16 + NUM_EPI_WARPS * 4;
+  static_assert(BM * STAGE_LD * 4 <= BAR_OFF, "epilogue staging must fit in the operand ring");
   static constexpr int ALLOC = TOTAL + 1024;  // slack to align the base to 1024 bytes
 };
 
-template <int BN, int STAGES, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// SPLIT: operands are bf16 hi/lo plane pairs; the k loop runs three times
+// (hi*hi, hi*lo, lo*hi) into the same TMEM accumulator.  tmA2/tmB2 map the lo
+// planes (unused otherwise).
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool SPLIT>
+__global__ void __launch_bounds__(NUM_THREADS, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmDesc g, int num_kb, int* err) {
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                   const GemmDesc g, int nkb, int* err) {
+  const int num_kb = SPLIT ? 3 * nkb : nkb;
   using L = Smem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -183,7 +200,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (threadIdx.x < 4) red[threadIdx.x] = 0.0f;
+  if (threadIdx.x < NUM_EPI_WARPS) red[threadIdx.x] = 0.0f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -197,18 +214,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint8_t* sa = smem + s * L::STAGE_BYTES;
       uint8_t* sb = sa + L::A_BYTES;
       mbar_expect_tx(&full[s], L::STAGE_BYTES);
-      const int k0 = kb * BK;
+      const int term = SPLIT ? kb / nkb : 0;
+      const int k0 = (SPLIT ? kb - term * nkb : kb) * BK;
+      const CUtensorMap* ma = (SPLIT && term == 2) ? &tmA2 : &tmA;
+      const CUtensorMap* mb = (SPLIT && term == 1) ? &tmB2 : &tmB;
       if (!A_MN) {
-        tma_load_3d(sa, &tmA, &full[s], k0, m0, bz);
+        tma_load_3d(sa, ma, &full[s], k0, m0, bz);
       } else {
 #pragma unroll
-        for (int j = 0; j < BM / PANEL; ++j) tma_load_3d(sa + j * PANEL * BK * 2, &tmA, &full[s], m0 + j * PANEL, k0, bz);
+        for (int j = 0; j < BM / PANEL; ++j) tma_load_3d(sa + j * PANEL * BK * 2, ma, &full[s], m0 + j * PANEL, k0, bz);
       }
       if (!B_MN) {
-        tma_load_3d(sb, &tmB, &full[s], k0, n0, bz);
+        tma_load_3d(sb, mb, &full[s], k0, n0, bz);
       } else {
 #pragma unroll
-        for (int j = 0; j < BN / PANEL; ++j) tma_load_3d(sb + j * PANEL * BK * 2, &tmB, &full[s], n0 + j * PANEL, k0, bz);
+        for (int j = 0; j < BN / PANEL; ++j) tma_load_3d(sb + j * PANEL * BK * 2, mb, &full[s], n0 + j * PANEL, k0, bz);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -235,36 +255,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     umma_commit(accb);
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
+    // TMEM -> shared staging (the operand ring is idle once the accumulator
+    // is complete) -> row-contiguous, coalesced global stores.
     bool ok = mbar_wait(accb, 0, err, 32);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
-      const int quad = warp & 3;
-      const int row = m0 + quad * 32 + lane;
+      const int quad = warp & 3;              // TMEM lanes this warp may read
+      const int half = (warp - 2) >> 2;       // which 32 of each 64 columns it reads
+      const int ew = warp - 2;                // rows it stores: ew*16 .. ew*16+15
+      float* stage = reinterpret_cast<float*>(smem);
       float sq = 0.0f;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c, v);
-        if (row < g.M) {
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(c0 + 32 * half), v);
+        float* srow = stage + (quad * 32 + lane) * STAGE_LD + 32 * half;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = n0 + c + i;
-            if (n < g.N) sq += epi_value<bf16>(g, bz, row, n, v[i]);
+        for (int i = 0; i < 32; ++i) srow[i] = v[i];
+        epi_bar();
+#pragma unroll 1
+        for (int k = 0; k < BM / NUM_EPI_WARPS; ++k) {
+          const int r = ew * (BM / NUM_EPI_WARPS) + k;
+          const int row = m0 + r;
+          if (row < g.M) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int n = n0 + c0 + cc * 32 + lane;
+              const float a = stage[r * STAGE_LD + cc * 32 + lane];
+              if (n < g.N) sq += SPLIT ? epi_value<Split>(g, bz, row, n, a) : epi_value<bf16>(g, bz, row, n, a);
+            }
           }
         }
+        epi_bar();
       }
       if (g.epi == EPI_DW) {
         sq = warp_sum(sq);
-        if (lane == 0) red[warp - 2] = sq;
+        if (lane == 0) red[ew] = sq;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (g.epi == EPI_DW && threadIdx.x == 0)
-    g.partials[(long long)bz * gridDim.x * gridDim.y + blockIdx.y * gridDim.x + blockIdx.x] =
-        red[0] + red[1] + red[2] + red[3];
+  if (g.epi == EPI_DW && threadIdx.x == 0) {
+    float t = 0.0f;
+    for (int w = 0; w < NUM_EPI_WARPS; ++w) t += red[w];
+    g.partials[(long long)bz * gridDim.x * gridDim.y + blockIdx.y * gridDim.x + blockIdx.x] = t;
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -314,13 +351,12 @@ ttt_status make_map(CUtensorMap* m, const void* base, long long inner, long long
 }
 
 constexpr int kBN = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 
-template <bool A_MN, bool B_MN>
-ttt_status launch_variant(const GemmDesc& g, const CUtensorMap& ta, const CUtensorMap& tb, int nkb,
-                          cudaStream_t st) {
+template <bool A_MN, bool B_MN, bool SPLIT>
+ttt_status launch_variant(const GemmDesc& g, const CUtensorMap* maps, int nkb, cudaStream_t st) {
   using L = Smem<kBN, kStages>;
-  auto kern = gemm_tc_kernel<kBN, kStages, A_MN, B_MN>;
+  auto kern = gemm_tc_kernel<kBN, kStages, A_MN, B_MN, SPLIT>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
@@ -328,7 +364,7 @@ ttt_status launch_variant(const GemmDesc& g, const CUtensorMap& ta, const CUtens
     attr_set = true;
   }
   dim3 grid(ceil_div(g.N, kBN), ceil_div(g.M, BM), g.batch);
-  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(ta, tb, g, nkb, g_err);
+  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], g, nkb, g.err);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -338,7 +374,8 @@ ttt_status launch_variant(const GemmDesc& g, const CUtensorMap& ta, const CUtens
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 bool gemm_tc_supported(const GemmDesc& g) {
-  if (g.dtype != TTT_DTYPE_BF16) return false;
+  if (g.dtype != ST_BF16 && g.dtype != ST_SPLIT) return false;
+  if (g.dtype == ST_SPLIT && (g.loA % 8 || g.loB % 8 || g.loA <= 0 || g.loB <= 0)) return false;
   if (g.M < 64 || g.N < 64 || g.K < 16 || g.batch < 1) return false;
   if (!aligned16(g.A) || !aligned16(g.B)) return false;
   if (g.lda % 8 || g.ldb % 8) return false;
@@ -366,20 +403,30 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
     return TTT_ERR_UNSUPPORTED;
   }
   TTT_TRY(tc::init_driver());
-  int* err = g.err;
-  if (!err) TTT_TRY(gemm_tc_error_word(&err));
+  GemmDesc gd = g;
+  if (!gd.err) TTT_TRY(gemm_tc_error_word(&gd.err));
   const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
-  CUtensorMap ta, tb;
-  // A: K-major [batch][M][K] boxes {64, 128}; MN-major [batch][K][M] panels {64, 64}
-  if (!a_mn) TTT_TRY(tc::make_map(&ta, g.A, g.K, g.M, g.batch, g.lda, g.sA, tc::BK, tc::BM));
-  else TTT_TRY(tc::make_map(&ta, g.A, g.M, g.K, g.batch, g.lda, g.sA, tc::PANEL, tc::BK));
-  if (!b_mn) TTT_TRY(tc::make_map(&tb, g.B, g.K, g.N, g.batch, g.ldb, g.sB, tc::BK, tc::kBN));
-  else TTT_TRY(tc::make_map(&tb, g.B, g.N, g.K, g.batch, g.ldb, g.sB, tc::PANEL, tc::BK));
+  const bool split = g.dtype == ST_SPLIT;
+  // maps: A hi, B hi, A lo, B lo.  A: K-major [batch][M][K] boxes {64, 128};
+  // MN-major [batch][K][M] panels {64, 64}.  Likewise B with BN rows.
+  CUtensorMap maps[4];
+  const bf16* planesA[2] = {static_cast<const bf16*>(g.A), static_cast<const bf16*>(g.A) + (split ? g.loA : 0)};
+  const bf16* planesB[2] = {static_cast<const bf16*>(g.B), static_cast<const bf16*>(g.B) + (split ? g.loB : 0)};
+  for (int p = 0; p < 2; ++p) {
+    if (!a_mn) TTT_TRY(tc::make_map(&maps[2 * p], planesA[p], g.K, g.M, g.batch, g.lda, g.sA, tc::BK, tc::BM));
+    else TTT_TRY(tc::make_map(&maps[2 * p], planesA[p], g.M, g.K, g.batch, g.lda, g.sA, tc::PANEL, tc::BK));
+    if (!b_mn) TTT_TRY(tc::make_map(&maps[2 * p + 1], planesB[p], g.K, g.N, g.batch, g.ldb, g.sB, tc::BK, tc::kBN));
+    else TTT_TRY(tc::make_map(&maps[2 * p + 1], planesB[p], g.N, g.K, g.batch, g.ldb, g.sB, tc::PANEL, tc::BK));
+  }
   const int nkb = ceil_div(g.K, tc::BK);
-  if (!a_mn && !b_mn) return tc::launch_variant<false, false>(g, ta, tb, nkb, st);
-  if (!a_mn && b_mn) return tc::launch_variant<false, true>(g, ta, tb, nkb, st);
-  if (a_mn && !b_mn) return tc::launch_variant<true, false>(g, ta, tb, nkb, st);
-  return tc::launch_variant<true, true>(g, ta, tb, nkb, st);
+#define TTT_TC_LAUNCH(AMN, BMN)                                                              \
+  return split ? tc::launch_variant<AMN, BMN, true>(gd, maps, nkb, st)                      \
+               : tc::launch_variant<AMN, BMN, false>(gd, maps, nkb, st)
+  if (!a_mn && !b_mn) TTT_TC_LAUNCH(false, false);
+  if (!a_mn && b_mn) TTT_TC_LAUNCH(false, true);
+  if (a_mn && !b_mn) TTT_TC_LAUNCH(true, false);
+  TTT_TC_LAUNCH(true, true);
+#undef TTT_TC_LAUNCH
 }
 
 }  // namespace ttt

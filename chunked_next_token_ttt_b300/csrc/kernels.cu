@@ -9,9 +9,9 @@
 namespace ttt {
 namespace {
 
-template <typename OpT>
-__global__ void embed_kernel(TokView tv, const OpT* __restrict__ E, int d, float* __restrict__ h32,
-                             OpT* __restrict__ hop) {
+template <typename ET, typename S>
+__global__ void embed_kernel(TokView tv, const ET* __restrict__ E, int d, float* __restrict__ h32, void* hop,
+                             long long hop_lo) {
   const int m = blockIdx.x;
   const int s = m / tv.rows, j = m % tv.rows;
   int x = tv.tok[s * tv.tok_ld + tv.tok_off + j];
@@ -19,16 +19,16 @@ __global__ void embed_kernel(TokView tv, const OpT* __restrict__ E, int d, float
     if (threadIdx.x == 0) atomicOr(tv.err, 2);
     x = 0;
   }
-  const OpT* src = E + (long long)x * d;
+  const ET* src = E + (long long)x * d;
   for (int c = threadIdx.x; c < d; c += blockDim.x) {
     const float v = to_f(src[c]);
     h32[(long long)m * d + c] = v;
-    if (hop) hop[(long long)m * d + c] = from_f<OpT>(v);
+    if (hop) OpIO<S>::store(hop, hop_lo, (long long)m * d + c, v);
   }
 }
 
-template <typename OpT>
-__global__ void rmsnorm_fwd_kernel(int d, const float* __restrict__ x, float eps, OpT* __restrict__ y,
+template <typename S>
+__global__ void rmsnorm_fwd_kernel(int d, const float* __restrict__ x, float eps, void* y, long long y_lo,
                                    float* __restrict__ rstd) {
   __shared__ float red[32];
   const long long m = blockIdx.x;
@@ -38,13 +38,13 @@ __global__ void rmsnorm_fwd_kernel(int d, const float* __restrict__ x, float eps
   sq = block_sum(sq, red);
   const float r = rsqrtf(sq / d + eps);
   if (threadIdx.x == 0) rstd[m] = r;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) y[m * d + c] = from_f<OpT>(xr[c] * r);
+  for (int c = threadIdx.x; c < d; c += blockDim.x) OpIO<S>::store(y, y_lo, m * d + c, xr[c] * r);
 }
 
-template <typename OpT>
+template <typename S>
 __global__ void rmsnorm_bwd_kernel(int d, const float* __restrict__ x, const float* __restrict__ rstd,
-                                   const float* __restrict__ dy, float* __restrict__ dx32,
-                                   OpT* __restrict__ dxop) {
+                                   const float* __restrict__ dy, float* __restrict__ dx32, void* dxop,
+                                   long long dx_lo) {
   __shared__ float red[32];
   const long long m = blockIdx.x;
   const float r = rstd[m];
@@ -56,7 +56,7 @@ __global__ void rmsnorm_bwd_kernel(int d, const float* __restrict__ x, const flo
   for (int c = threadIdx.x; c < d; c += blockDim.x) {
     const float v = r * (dyr[c] - xr[c] * r * dot);
     dx32[m * d + c] = v;
-    if (dxop) dxop[m * d + c] = from_f<OpT>(v);
+    if (dxop) OpIO<S>::store(dxop, dx_lo, m * d + c, v);
   }
 }
 
@@ -70,35 +70,8 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
   }
 }
 
-template <typename OpT>
-__global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long ldl, float scale,
-                          bool grad, float* __restrict__ losses, long long loss_ld, long long loss_off,
-                          float* __restrict__ row_loss) {
-  __shared__ float sm_m[32], sm_s[32];
-  const int m = blockIdx.x;
-  const int s = m / tv.rows, j = m % tv.rows;
-  const bool valid = j < tv.n_valid;
-  OpT* row = logits + (long long)m * ldl;
-  if (!valid) {
-    if (grad)
-      for (int v = threadIdx.x; v < V; v += blockDim.x) row[v] = from_f<OpT>(0.0f);
-    return;
-  }
-  int tgt = tv.tok[s * tv.tok_ld + tv.tok_off + j + 1];
-  if ((unsigned)tgt >= (unsigned)V) {
-    if (threadIdx.x == 0) atomicOr(tv.err, 2);
-    tgt = 0;
-  }
-  float mx = -FLT_MAX, se = 0.0f;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    const float x = to_f(row[v]);
-    if (x > mx) {
-      se = se * __expf(mx - x) + 1.0f;
-      mx = x;
-    } else {
-      se += __expf(x - mx);
-    }
-  }
+// Block-wide (max, sum-exp) reduction of per-thread online states; returns lse.
+__device__ __forceinline__ float block_lse(float mx, float se, float* sm_m, float* sm_s) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
@@ -120,7 +93,44 @@ __global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long
     if (lane == 0) { sm_m[0] = mx; sm_s[0] = se; }
   }
   __syncthreads();
-  const float lse = sm_m[0] + logf(sm_s[0]);
+  return sm_m[0] + logf(sm_s[0]);
+}
+
+__device__ __forceinline__ void online_push(float x, float& mx, float& se) {
+  if (x > mx) {
+    se = se * __expf(mx - x) + 1.0f;
+    mx = x;
+  } else {
+    se += __expf(x - mx);
+  }
+}
+
+__device__ __forceinline__ int target_of(const TokView& tv, int s, int j, int V) {
+  int tgt = tv.tok[s * tv.tok_ld + tv.tok_off + j + 1];
+  if ((unsigned)tgt >= (unsigned)V) {
+    if (threadIdx.x == 0) atomicOr(tv.err, 2);
+    tgt = 0;
+  }
+  return tgt;
+}
+
+template <typename OpT>
+__global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long ldl, float scale, bool grad,
+                          float* __restrict__ losses, long long loss_ld, long long loss_off,
+                          float* __restrict__ row_loss) {
+  __shared__ float sm_m[32], sm_s[32];
+  const int m = blockIdx.x;
+  const int s = m / tv.rows, j = m % tv.rows;
+  OpT* row = logits + (long long)m * ldl;
+  if (j >= tv.n_valid) {
+    if (grad)
+      for (int v = threadIdx.x; v < V; v += blockDim.x) row[v] = from_f<OpT>(0.0f);
+    return;
+  }
+  const int tgt = target_of(tv, s, j, V);
+  float mx = -FLT_MAX, se = 0.0f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) online_push(to_f(row[v]), mx, se);
+  const float lse = block_lse(mx, se, sm_m, sm_s);
   if (threadIdx.x == 0) {
     const float loss = lse - to_f(row[tgt]);
     if (losses) losses[s * loss_ld + loss_off + j] = loss;
@@ -134,9 +144,52 @@ __global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long
   }
 }
 
+// fp32 logits in, split dlogits written into the row's own bytes: the row is
+// staged in shared memory first, so no thread overwrites a value another
+// thread has yet to read.
+constexpr int kCeSplitMaxV = 32768;
+
+__global__ void ce_split_kernel(TokView tv, int V, float* __restrict__ logits, long long ldl, float scale,
+                                bool grad, float* __restrict__ losses, long long loss_ld, long long loss_off,
+                                float* __restrict__ row_loss) {
+  extern __shared__ float srow[];
+  __shared__ float sm_m[32], sm_s[32];
+  const int m = blockIdx.x;
+  const int s = m / tv.rows, j = m % tv.rows;
+  float* row = logits + (long long)m * ldl;
+  bf16* out = reinterpret_cast<bf16*>(row);
+  if (j >= tv.n_valid) {
+    if (grad)
+      for (int v = threadIdx.x; v < V; v += blockDim.x) {
+        out[v] = __float2bfloat16_rn(0.0f);
+        out[V + v] = __float2bfloat16_rn(0.0f);
+      }
+    return;
+  }
+  const int tgt = target_of(tv, s, j, V);
+  float mx = -FLT_MAX, se = 0.0f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = row[v];
+    srow[v] = x;
+    online_push(x, mx, se);
+  }
+  const float lse = block_lse(mx, se, sm_m, sm_s);   // contains __syncthreads
+  if (threadIdx.x == 0) {
+    const float loss = lse - srow[tgt];
+    if (losses) losses[s * loss_ld + loss_off + j] = loss;
+    if (row_loss) row_loss[m] = loss;
+  }
+  if (!grad) return;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float g = (__expf(srow[v] - lse) - (v == tgt ? 1.0f : 0.0f)) * scale;
+    const bf16 h = __float2bfloat16_rn(g);
+    out[v] = h;
+    out[V + v] = __float2bfloat16_rn(g - __bfloat162float(h));
+  }
+}
+
 __global__ void norm_finalize_kernel(PartialSlots ps, const float* __restrict__ partials, float clip,
-                                     float* __restrict__ scale, float* __restrict__ norm,
-                                     int* __restrict__ flag) {
+                                     float* __restrict__ scale, float* __restrict__ norm, int* __restrict__ flag) {
   __shared__ float red[32];
   const int s = blockIdx.x;
   float acc = 0.0f;
@@ -159,10 +212,10 @@ __global__ void norm_finalize_kernel(PartialSlots ps, const float* __restrict__ 
   }
 }
 
-template <typename OpT>
-__global__ void sgd_update_kernel(long long total, int B, long long n, float* __restrict__ W32,
-                                  OpT* __restrict__ Wop, const float* __restrict__ dW,
-                                  const float* __restrict__ scale, float eta) {
+template <typename S>
+__global__ void sgd_update_kernel(long long total, int B, long long n, float* __restrict__ W32, void* Wop,
+                                  long long wop_lo, const float* __restrict__ dW, const float* __restrict__ scale,
+                                  float eta) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int s = (int)((i / n) % B);
@@ -170,31 +223,30 @@ __global__ void sgd_update_kernel(long long total, int B, long long n, float* __
     if (sc == 0.0f) continue;  // skipped update (non-finite norm): W stays as it is
     const float w = W32[i] - eta * sc * dW[i];
     W32[i] = w;
-    Wop[i] = from_f<OpT>(w);
+    OpIO<S>::store(Wop, wop_lo, i, w);
   }
 }
 
-template <typename OpT>
+template <typename S>
 __global__ void broadcast_w0_kernel(long long total, int B, long long n, const float* __restrict__ W0,
-                                    float* __restrict__ W32, OpT* __restrict__ Wop) {
+                                    float* __restrict__ W32, void* Wop, long long wop_lo) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const long long slot = i / (n * B), e = i % n;
     const float w = W0[slot * n + e];
     W32[i] = w;
-    Wop[i] = from_f<OpT>(w);
+    OpIO<S>::store(Wop, wop_lo, i, w);
   }
 }
 
-template <typename OpT>
-__global__ void cast_kernel(long long n, const float* __restrict__ in, OpT* __restrict__ out) {
+template <typename S>
+__global__ void cast_kernel(long long n, const float* __restrict__ in, void* out, long long out_lo) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-    out[i] = from_f<OpT>(in[i]);
+    OpIO<S>::store(out, out_lo, i, in[i]);
 }
 
-__global__ void seq_mean_kernel(int rows, int n_valid, const float* __restrict__ row_loss,
-                                float* __restrict__ mean) {
+__global__ void seq_mean_kernel(int rows, int n_valid, const float* __restrict__ row_loss, float* __restrict__ mean) {
   __shared__ float red[32];
   const int s = blockIdx.x;
   float acc = 0.0f;
@@ -212,31 +264,31 @@ __global__ void settle_decide_kernel(int B, const float* __restrict__ Lc, const 
   accept[s] = a >= 0.0f ? 1 : 0;
 }
 
-template <typename OpT>
+template <typename S>
 __global__ void settle_apply_kernel(long long total, int B, long long n, const uint8_t* __restrict__ accept,
-                                    float* __restrict__ W32, OpT* __restrict__ Wop,
-                                    float* __restrict__ Wc32, OpT* __restrict__ Wcop) {
+                                    float* __restrict__ W32, void* Wop, float* __restrict__ Wc32, void* Wcop,
+                                    long long lo) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int s = (int)((i / n) % B);
     if (accept[s]) {
       Wc32[i] = W32[i];
-      Wcop[i] = Wop[i];
+      OpIO<S>::copy(Wcop, lo, Wop, lo, i);
     } else {
       W32[i] = Wc32[i];
-      Wop[i] = Wcop[i];
+      OpIO<S>::copy(Wop, lo, Wcop, lo, i);
     }
   }
 }
 
 __global__ void softmax_kernel(int V, const float* __restrict__ logits, float* __restrict__ p) {
   __shared__ float red[32];
+  __shared__ float wm[32];
   const long long m = blockIdx.x;
   const float* row = logits + m * V;
   float mx = -FLT_MAX;
   for (int v = threadIdx.x; v < V; v += blockDim.x) mx = fmaxf(mx, row[v]);
   mx = warp_max(mx);
-  __shared__ float wm[32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   if (lane == 0) wm[wid] = mx;
   __syncthreads();
@@ -262,49 +314,71 @@ int grid_for(long long n, int threads) {
 
 }  // namespace
 
-#define DISPATCH_OP(dtype, KERNEL_CALL_BF16, KERNEL_CALL_F32) \
-  do {                                                        \
-    if ((dtype) == TTT_DTYPE_BF16) { KERNEL_CALL_BF16; } else { KERNEL_CALL_F32; } \
+// Instantiates KERNEL<S> for the storage code and launches it.
+#define LAUNCH_BY_STORAGE(stg, KERNEL, GRID, BLOCK, SMEM, STREAM, ...)                      \
+  do {                                                                                      \
+    if ((stg) == ST_BF16) KERNEL<bf16><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);         \
+    else if ((stg) == ST_SPLIT) KERNEL<Split><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);  \
+    else KERNEL<float><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);                         \
   } while (0)
 
-ttt_status launch_embed(int dtype, int B, const TokView& tv, const void* E, int d, float* h32,
-                        void* hop, cudaStream_t st) {
+ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d, float* h32, void* hop,
+                        long long hop_lo, cudaStream_t st) {
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
-  DISPATCH_OP(dtype,
-      (embed_kernel<bf16><<<M, 256, 0, st>>>(tv, (const bf16*)E, d, h32, (bf16*)hop)),
-      (embed_kernel<float><<<M, 256, 0, st>>>(tv, (const float*)E, d, h32, (float*)hop)));
+  if (stg == ST_BF16)
+    embed_kernel<bf16, bf16><<<M, 256, 0, st>>>(tv, static_cast<const bf16*>(E), d, h32, hop, hop_lo);
+  else if (stg == ST_SPLIT)
+    embed_kernel<float, Split><<<M, 256, 0, st>>>(tv, static_cast<const float*>(E), d, h32, hop, hop_lo);
+  else
+    embed_kernel<float, float><<<M, 256, 0, st>>>(tv, static_cast<const float*>(E), d, h32, hop, hop_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
-ttt_status launch_rmsnorm_fwd(int dtype, int M, int d, const float* x, float eps, void* y, float* rstd,
+ttt_status launch_rmsnorm_fwd(int stg, int M, int d, const float* x, float eps, void* y, long long y_lo, float* rstd,
                               cudaStream_t st) {
   if (M == 0) return TTT_OK;
-  DISPATCH_OP(dtype, (rmsnorm_fwd_kernel<bf16><<<M, 256, 0, st>>>(d, x, eps, (bf16*)y, rstd)),
-              (rmsnorm_fwd_kernel<float><<<M, 256, 0, st>>>(d, x, eps, (float*)y, rstd)));
+  LAUNCH_BY_STORAGE(stg, rmsnorm_fwd_kernel, M, 256, 0, st, d, x, eps, y, y_lo, rstd);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
-ttt_status launch_rmsnorm_bwd(int dtype, int M, int d, const float* x, const float* rstd, const float* dy,
-                              float* dx32, void* dxop, cudaStream_t st) {
+ttt_status launch_rmsnorm_bwd(int stg, int M, int d, const float* x, const float* rstd, const float* dy, float* dx32,
+                              void* dxop, long long dx_lo, cudaStream_t st) {
   if (M == 0) return TTT_OK;
-  DISPATCH_OP(dtype,
-      (rmsnorm_bwd_kernel<bf16><<<M, 256, 0, st>>>(d, x, rstd, dy, dx32, (bf16*)dxop)),
-      (rmsnorm_bwd_kernel<float><<<M, 256, 0, st>>>(d, x, rstd, dy, dx32, (float*)dxop)));
+  LAUNCH_BY_STORAGE(stg, rmsnorm_bwd_kernel, M, 256, 0, st, d, x, rstd, dy, dx32, dxop, dx_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
-ttt_status launch_ce(int dtype, int B, const TokView& tv, int V, void* logits, long long ldl, float scale,
-                     bool grad, float* losses, long long loss_ld, long long loss_off, float* row_loss,
-                     cudaStream_t st) {
+int ce_split_max_vocab() { return kCeSplitMaxV; }
+
+ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, long long ldl, float scale, bool grad,
+                     float* losses, long long loss_ld, long long loss_off, float* row_loss, cudaStream_t st) {
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
-  DISPATCH_OP(dtype,
-      (ce_kernel<bf16><<<M, 512, 0, st>>>(tv, V, (bf16*)logits, ldl, scale, grad, losses, loss_ld, loss_off, row_loss)),
-      (ce_kernel<float><<<M, 512, 0, st>>>(tv, V, (float*)logits, ldl, scale, grad, losses, loss_ld, loss_off, row_loss)));
+  if (stg == ST_SPLIT) {
+    if (V > kCeSplitMaxV) {
+      set_error("vocabulary too large for the split cross-entropy kernel");
+      return TTT_ERR_UNSUPPORTED;
+    }
+    const size_t smem = (size_t)V * sizeof(float);
+    static size_t smem_set = 0;
+    if (smem > 48 * 1024 && smem > smem_set) {
+      cudaError_t e = cudaFuncSetAttribute(ce_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
+      smem_set = smem;
+    }
+    ce_split_kernel<<<M, 512, smem, st>>>(tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
+                                          loss_off, row_loss);
+  } else if (stg == ST_BF16) {
+    ce_kernel<bf16><<<M, 512, 0, st>>>(tv, V, static_cast<bf16*>(logits), ldl, scale, grad, losses, loss_ld,
+                                       loss_off, row_loss);
+  } else {
+    ce_kernel<float><<<M, 512, 0, st>>>(tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
+                                        loss_off, row_loss);
+  }
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -316,32 +390,27 @@ ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* part
   return TTT_OK;
 }
 
-ttt_status launch_sgd_update(int dtype, int nslots, int B, long long n, float* W32, void* Wop, const float* dW,
-                             const float* scale, float eta, cudaStream_t st) {
+ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
+                             const float* dW, const float* scale, float eta, cudaStream_t st) {
   const long long total = (long long)nslots * B * n;
   const int g = grid_for(total, 256);
-  DISPATCH_OP(dtype,
-      (sgd_update_kernel<bf16><<<g, 256, 0, st>>>(total, B, n, W32, (bf16*)Wop, dW, scale, eta)),
-      (sgd_update_kernel<float><<<g, 256, 0, st>>>(total, B, n, W32, (float*)Wop, dW, scale, eta)));
+  LAUNCH_BY_STORAGE(stg, sgd_update_kernel, g, 256, 0, st, total, B, n, W32, Wop, wop_lo, dW, scale, eta);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
-ttt_status launch_broadcast_w0(int dtype, int nslots, int B, long long n, const float* W0, float* W32, void* Wop,
-                               cudaStream_t st) {
+ttt_status launch_broadcast_w0(int stg, int nslots, int B, long long n, const float* W0, float* W32, void* Wop,
+                               long long wop_lo, cudaStream_t st) {
   const long long total = (long long)nslots * B * n;
   const int g = grid_for(total, 256);
-  DISPATCH_OP(dtype,
-      (broadcast_w0_kernel<bf16><<<g, 256, 0, st>>>(total, B, n, W0, W32, (bf16*)Wop)),
-      (broadcast_w0_kernel<float><<<g, 256, 0, st>>>(total, B, n, W0, W32, (float*)Wop)));
+  LAUNCH_BY_STORAGE(stg, broadcast_w0_kernel, g, 256, 0, st, total, B, n, W0, W32, Wop, wop_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
-ttt_status launch_cast(int dtype, long long n, const float* in, void* out, cudaStream_t st) {
+ttt_status launch_cast(int stg, long long n, const float* in, void* out, long long out_lo, cudaStream_t st) {
   const int g = grid_for(n, 256);
-  DISPATCH_OP(dtype, (cast_kernel<bf16><<<g, 256, 0, st>>>(n, in, (bf16*)out)),
-              (cast_kernel<float><<<g, 256, 0, st>>>(n, in, (float*)out)));
+  LAUNCH_BY_STORAGE(stg, cast_kernel, g, 256, 0, st, n, in, out, out_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -352,16 +421,14 @@ ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, 
   return TTT_OK;
 }
 
-ttt_status launch_settle_apply(int dtype, int nslots, int B, long long n, const float* Lc, const float* Lw,
-                               float* A, uint8_t* accept, float* W32, void* Wop, float* Wc32, void* Wcop,
+ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const float* Lc, const float* Lw, float* A,
+                               uint8_t* accept, float* W32, void* Wop, float* Wc32, void* Wcop, long long op_lo,
                                cudaStream_t st) {
   settle_decide_kernel<<<ceil_div(B, 128), 128, 0, st>>>(B, Lc, Lw, A, accept);
   TTT_CHECK_LAUNCH();
   const long long total = (long long)nslots * B * n;
   const int g = grid_for(total, 256);
-  DISPATCH_OP(dtype,
-      (settle_apply_kernel<bf16><<<g, 256, 0, st>>>(total, B, n, accept, W32, (bf16*)Wop, Wc32, (bf16*)Wcop)),
-      (settle_apply_kernel<float><<<g, 256, 0, st>>>(total, B, n, accept, W32, (float*)Wop, Wc32, (float*)Wcop)));
+  LAUNCH_BY_STORAGE(stg, settle_apply_kernel, g, 256, 0, st, total, B, n, accept, W32, Wop, Wc32, Wcop, op_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

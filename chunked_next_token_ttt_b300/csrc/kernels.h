@@ -18,26 +18,36 @@ struct TokView {
   int* err = nullptr;     // raise bit 2 of *err (no out-of-range access)
 };
 
-// h32[m, :] = E[x_m, :] (float), hop[m, :] = same in the operand type.
-ttt_status launch_embed(int dtype, int B, const TokView& tv, const void* E, int d, float* h32,
-                        void* hop, cudaStream_t st);
+// Storage codes (Storage in common.cuh): ST_F32, ST_BF16, ST_SPLIT.  `lo` is
+// the element offset of an op-typed pointer's lo plane (ST_SPLIT only).
+
+// h32[m, :] = E[x_m, :] (float), hop[m, :] = same in the operand storage.  E is
+// bf16 for ST_BF16 and float otherwise.
+ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d, float* h32,
+                        void* hop, long long hop_lo, cudaStream_t st);
 
 // y = x * rstd (operand type), rstd = 1/sqrt(mean(x^2) + eps).
-ttt_status launch_rmsnorm_fwd(int dtype, int M, int d, const float* x, float eps, void* y,
+ttt_status launch_rmsnorm_fwd(int stg, int M, int d, const float* x, float eps, void* y, long long y_lo,
                               float* rstd, cudaStream_t st);
 
 // dx = rstd * (dy - xhat * mean(xhat * dy)), xhat = x * rstd; dx32 and its
 // operand-type copy dxop (may be null).
-ttt_status launch_rmsnorm_bwd(int dtype, int M, int d, const float* x, const float* rstd,
-                              const float* dy, float* dx32, void* dxop, cudaStream_t st);
+ttt_status launch_rmsnorm_bwd(int stg, int M, int d, const float* x, const float* rstd,
+                              const float* dy, float* dx32, void* dxop, long long dx_lo, cudaStream_t st);
 
-// Row-wise cross-entropy of logits [B*rows, V] (operand type, leading dim ldl).
+// Row-wise cross-entropy of logits [B*rows, V] (leading dim ldl elements).
 // For valid rows: loss -> losses[s * loss_ld + loss_off + j] (if losses != null)
 // and row_loss[m] (if != null); when `grad` the row is overwritten in place by
 // dlogits = (softmax - onehot(target)) * scale.  Invalid rows get dlogits 0.
-ttt_status launch_ce(int dtype, int B, const TokView& tv, int V, void* logits, long long ldl,
+// ST_F32 / ST_BF16: logits and dlogits in that type.  ST_SPLIT: logits are
+// float (ldl floats per row); dlogits are written inside each row's own bytes
+// as a split pair, hi plane at bf16 offset 0 and lo plane at bf16 offset V of
+// the row (a bf16 matrix with leading dim 2*ldl and lo offset V); V must fit
+// the kernel's shared-memory row buffer (ce_split_max_vocab()).
+ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, long long ldl,
                      float scale, bool grad, float* losses, long long loss_ld, long long loss_off,
                      float* row_loss, cudaStream_t st);
+int ce_split_max_vocab();
 
 // Per-sequence global gradient norm from the dW GEMM partials, then the
 // clip scale s = min(1, clip/(norm+1e-6)) (1 when clip == 0).  A non-finite
@@ -51,15 +61,15 @@ ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* part
                                 float* scale, float* norm, int* flag, cudaStream_t st);
 
 // W32 -= eta * scale[s] * dW over the arena [slot][B][n]; Wop = cast(W32).
-ttt_status launch_sgd_update(int dtype, int nslots, int B, long long n, float* W32, void* Wop,
+ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
                              const float* dW, const float* scale, float eta, cudaStream_t st);
 
 // W32[slot][s] = W0[slot] for every s; Wop = cast.
-ttt_status launch_broadcast_w0(int dtype, int nslots, int B, long long n, const float* W0,
-                               float* W32, void* Wop, cudaStream_t st);
+ttt_status launch_broadcast_w0(int stg, int nslots, int B, long long n, const float* W0,
+                               float* W32, void* Wop, long long wop_lo, cudaStream_t st);
 
 // out[i] = cast(in[i]) for n floats.
-ttt_status launch_cast(int dtype, long long n, const float* in, void* out, cudaStream_t st);
+ttt_status launch_cast(int stg, long long n, const float* in, void* out, long long out_lo, cudaStream_t st);
 
 // mean over the n_valid valid rows of each sequence's row_loss block.
 ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, float* mean,
@@ -67,9 +77,9 @@ ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, 
 
 // A = Lc - Lw; accept = (A >= 0).  Then per sequence: accept ? Wc <- W : W <- Wc
 // over fp32 masters and operand copies.
-ttt_status launch_settle_apply(int dtype, int nslots, int B, long long n, const float* Lc,
+ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const float* Lc,
                                const float* Lw, float* A, uint8_t* accept, float* W32, void* Wop,
-                               float* Wc32, void* Wcop, cudaStream_t st);
+                               float* Wc32, void* Wcop, long long op_lo, cudaStream_t st);
 
 // p[m, :] = softmax(logits32[m, :]).
 ttt_status launch_softmax(int M, int V, const float* logits32, float* p, cudaStream_t st);

@@ -13,7 +13,7 @@ static ttt_status bad(ttt_status s, const char* msg) {
 
 static bool to_desc(const ttt_gemm_args* a, GemmDesc* g) {
   if (!a || a->M < 0 || a->N < 0 || a->K < 0 || a->batch < 1 || a->epi < 0 || a->epi > TTT_EPI_DW) return false;
-  if (a->dtype != TTT_DTYPE_FP32 && a->dtype != TTT_DTYPE_BF16) return false;
+  if (a->dtype != ST_F32 && a->dtype != ST_BF16 && a->dtype != ST_SPLIT) return false;
   if (!a->A || !a->B || !a->out) return false;
   g->M = a->M; g->N = a->N; g->K = a->K; g->batch = a->batch; g->dtype = a->dtype;
   g->a_kmajor = a->a_kmajor != 0; g->b_kmajor = a->b_kmajor != 0;
@@ -25,6 +25,7 @@ static bool to_desc(const ttt_gemm_args* a, GemmDesc* g) {
   g->aux = a->aux; g->ldx = a->ldx; g->sX = a->sX;
   g->partials = a->partials;
   g->impl = a->impl;
+  g->loA = a->loA; g->loB = a->loB; g->loO = a->loO; g->loO2 = a->loO2; g->loX = a->loX;
   return true;
 }
 
@@ -74,13 +75,13 @@ ttt_status ttt_op_cross_entropy(int dtype, int M, int V, void* logits, const int
 ttt_status ttt_op_rmsnorm_forward(int dtype, int M, int d, const float* x, float eps, void* y, float* rstd,
                                   ttt_stream stream) {
   if (M < 0 || d < 1 || !x || !y || !rstd) return bad(TTT_ERR_BAD_ARG, "bad rmsnorm arguments");
-  return launch_rmsnorm_fwd(dtype, M, d, x, eps, y, rstd, (cudaStream_t)stream);
+  return launch_rmsnorm_fwd(dtype, M, d, x, eps, y, 0, rstd, (cudaStream_t)stream);
 }
 
 ttt_status ttt_op_rmsnorm_backward(int dtype, int M, int d, const float* x, const float* rstd, const float* dy,
                                    float* dx, void* dx_op, ttt_stream stream) {
   if (M < 0 || d < 1 || !x || !rstd || !dy || !dx) return bad(TTT_ERR_BAD_ARG, "bad rmsnorm arguments");
-  return launch_rmsnorm_bwd(dtype, M, d, x, rstd, dy, dx, dx_op, (cudaStream_t)stream);
+  return launch_rmsnorm_bwd(dtype, M, d, x, rstd, dy, dx, dx_op, 0, (cudaStream_t)stream);
 }
 
 size_t ttt_clip_sgd_workspace_size(int nslots, int B, long long n) {

@@ -28,14 +28,20 @@ enum {
                             sum of acc^2 (tiles = ttt_op_gemm_partial_tiles)     */
 };
 enum { TTT_GEMM_AUTO = 0, TTT_GEMM_SIMT = 1, TTT_GEMM_TENSOR = 2 };
+/* Operand storage code accepted by ttt_op_gemm besides TTT_DTYPE_FP32/BF16:
+ * fp32-accurate values kept as two bf16 planes, hi = bf16(v) at p[i] and
+ * lo = bf16(v - hi) at p[lo + i] (lo offsets in ttt_gemm_args.lo*); products
+ * are taken as hi*hi + hi*lo + lo*hi with fp32 accumulation. */
+enum { TTT_STORAGE_BF16X3 = 2 };
 
 /* A batched GEMM C[b][m][n] = epilogue(sum_k A[b](m,k) B[b](n,k)).
  * A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m]; likewise B(n,k) with
  * b_kmajor.  s* are per-batch strides; all strides are in elements.  dtype is
- * the operand type of A, B and every "op"-typed output (TTT_DTYPE_FP32 or
- * TTT_DTYPE_BF16).  impl selects the kernel: TTT_GEMM_TENSOR (tcgen05, bf16
- * only; leading dims and batch strides multiples of 8, 16-byte aligned bases)
- * returns TTT_ERR_UNSUPPORTED when the shape does not qualify. */
+ * the operand storage of A, B and every "op"-typed output (TTT_DTYPE_FP32,
+ * TTT_DTYPE_BF16 or TTT_STORAGE_BF16X3).  impl selects the kernel:
+ * TTT_GEMM_TENSOR (tcgen05; bf16 or bf16x3 storage, leading dims, batch
+ * strides and lo offsets multiples of 8, 16-byte aligned bases) returns
+ * TTT_ERR_UNSUPPORTED when the shape does not qualify. */
 typedef struct {
   int M, N, K, batch;
   int dtype, a_kmajor, b_kmajor, epi, impl;
@@ -45,6 +51,7 @@ typedef struct {
   void* out2; long long ldo2, sO2;
   const void* aux; long long ldx, sX;
   float* partials;
+  long long loA, loB, loO, loO2, loX;   /* lo-plane offsets (TTT_STORAGE_BF16X3 only) */
 } ttt_gemm_args;
 
 ttt_status ttt_op_gemm(const ttt_gemm_args* args, ttt_stream stream);

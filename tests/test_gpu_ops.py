@@ -218,3 +218,49 @@ def test_clip_sgd_nonfinite_sequence_is_skipped():
     assert e.value.status == 5
     assert torch.all(W[:, 1] == 1.0)
     assert torch.all(W[:, 0] < 1.0) and torch.all(W[:, 2] < 1.0)
+
+
+def split_planes(x64):
+    """fp32 values as bf16 hi/lo planes stacked [2, ...] (hi = bf16(v), lo = bf16(v - hi))."""
+    v = torch.from_numpy(np.asarray(x64, dtype=np.float32))
+    hi = v.to(torch.bfloat16)
+    lo = (v - hi.float()).to(torch.bfloat16)
+    return torch.stack([hi, lo]).contiguous()
+
+
+@pytest.mark.parametrize("a_k", [True, False], ids=["A_kmaj", "A_mnmaj"])
+@pytest.mark.parametrize("b_k", [True, False], ids=["B_kmaj", "B_mnmaj"])
+@pytest.mark.parametrize("impl", ["tensor", "simt"])
+def test_bf16x3_split_gemm_is_fp32_accurate(a_k, b_k, impl):
+    """hi*hi + hi*lo + lo*hi on the tensor cores: error ~2^-17 of the operands'
+    scale, far inside the fp32 workloads' 1e-4 tolerance (plain bf16 would be
+    ~2^-9)."""
+    rng = np.random.default_rng(9)
+    M, N, K, batch = 256, 200, 320, 2
+    A = rng.normal(0, 1, (batch, M, K)).astype(np.float32)
+    Bm = rng.normal(0, 1, (batch, N, K)).astype(np.float32)
+    ref = np.einsum("bmk,bnk->bmn", A.astype(np.float64), Bm.astype(np.float64))
+    As = split_planes(A if a_k else A.transpose(0, 2, 1)).cuda()
+    Bs = split_planes(Bm if b_k else Bm.transpose(0, 2, 1)).cuda()
+    out = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+    args = T.gemm_args(M, N, K, As, Bs, out, batch=batch, dtype="bf16x3", a_kmajor=a_k, b_kmajor=b_k,
+                       epi="store_f32", impl=impl, sA=M * K, sB=N * K, sO=M * N,
+                       loA=batch * M * K, loB=batch * N * K)
+    T.op_gemm(args)
+    torch.cuda.synchronize()
+    err = np.abs(out.cpu().numpy() - ref).max()
+    # per product: dropped lo*lo and the two lo roundings, about 3 * 2^-18 of |a b|;
+    # summed over K random-sign terms and taken as the max over ~1e5 outputs
+    scale = np.sqrt(K)
+    assert err <= 6e-5 * scale, err
+    hi_only = np.einsum("bmk,bnk->bmn", _bf(A), _bf(Bm))
+    assert err * 20 < np.abs(hi_only - ref).max()
+    # and the split store epilogue writes hi/lo planes that add back to the value
+    o2 = torch.zeros((2, batch, M, N), dtype=torch.bfloat16, device="cuda")
+    args = T.gemm_args(M, N, K, As, Bs, o2, batch=batch, dtype="bf16x3", a_kmajor=a_k, b_kmajor=b_k,
+                       epi="store", impl=impl, sA=M * K, sB=N * K, sO=M * N,
+                       loA=batch * M * K, loB=batch * N * K, loO=batch * M * N)
+    T.op_gemm(args)
+    torch.cuda.synchronize()
+    v = (o2[0].float() + o2[1].float()).cpu().numpy()
+    assert np.abs(v - ref).max() <= 6e-5 * scale + 1e-5 * np.abs(ref).max()

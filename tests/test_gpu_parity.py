@@ -41,6 +41,26 @@ def test_chunked_fp32_prefix_chunks():
     compare(wl, gpu, ref)
 
 
+def test_chunked_fp32_full_size():
+    """The benchmark workload at its stated size: B = 4, T = 8192, 32 chunks,
+    every loss and the final fast weights within the fp32 tolerance."""
+    wl = C.CHUNKED_FP32
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_chunked_fp32_plain_storage_matches_too(monkeypatch):
+    """The same workload with fp32 storage forced (SIMT GEMMs) also passes."""
+    monkeypatch.setenv("TTT_FP32_STORAGE", "f32")
+    wl = C.CHUNKED_FP32.replace(T=2 * C.CHUNKED_FP32.chunk, B=2)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
 def test_chunked_fp32_odd_shapes_ragged_tail():
     """Widths that are not multiples of any tile, T not a multiple of b."""
     wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=40, B=3, T=130, n_prefix=1)
