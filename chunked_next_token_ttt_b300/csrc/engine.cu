@@ -81,12 +81,14 @@ static OpBuf op_at(const ttt_handle* h, const OpBuf& b, long long elems) {
   return r;
 }
 
-static int gemm_count(const GemmDesc&) { return 1; }
+static int gemm_count(const GemmDesc& g) { return gemm_launches(g); }
 
 static ttt_status rungemm(ttt_handle* h, int cls, const GemmDesc& g_in, cudaStream_t st) {
   GemmDesc g = g_in;
   g.err = h->flag;
   g.dtype = h->stg;
+  g.ws = h->gemm_ws;
+  g.ws_elems = h->gemm_ws_elems;
   return run(h, cls, st, gemm_count(g), [&] { return gemm(g, st); });
 }
 
@@ -545,6 +547,10 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = dalloc(h, &h->dy32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dh32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = op_alloc(&h->dhop, Mm * d)) != TTT_OK) return bail(s);
+  // split-K workspace: up to 8 fp32 partial slices of a [Mmax, d] output, at most 64 MB
+  h->gemm_ws_elems = 8LL * (long long)Mm * d;
+  if (h->gemm_ws_elems > (16LL << 20)) h->gemm_ws_elems = 16LL << 20;
+  if ((s = dalloc(h, &h->gemm_ws, (size_t)h->gemm_ws_elems * 4)) != TTT_OK) return bail(s);
   // partial sums of squares: at most one per 64x64 output tile per matrix and sequence
   h->partial_cap = (long long)h->nslots * B * ceil_div(d, 64) * ceil_div(f, 64);
   if ((s = dalloc(h, &h->partials, (size_t)h->partial_cap * 4)) != TTT_OK) return bail(s);

@@ -60,6 +60,8 @@ struct ttt_handle {
   float* dy32 = nullptr;
   float* dh32 = nullptr;
   OpBuf dhop;
+  float* gemm_ws = nullptr;          // split-K partial products
+  long long gemm_ws_elems = 0;
   float* partials = nullptr;
   long long partial_cap = 0;
   ttt::PartialSlots pslots{};

@@ -1,19 +1,36 @@
-// GEMM dispatch: the tcgen05 tensor-core kernel where the operand type, shape
-// and alignment allow it, the SIMT kernel otherwise (or when forced by impl).
+// GEMM dispatch: the weight-streaming small-M kernel for a few rows per batch
+// entry, the tcgen05 tensor-core kernel where the operand storage, shape and
+// alignment allow it, the SIMT kernel otherwise (or when forced by impl).
 #include "gemm.h"
 
 namespace ttt {
 
-static bool use_tc(const GemmDesc& g) {
-  if (g.impl == 1) return false;
-  if (g.impl == 2) return true;
-  return gemm_tc_supported(g);
+enum Route { ROUTE_SIMT, ROUTE_TC, ROUTE_SMALL };
+
+static Route route(const GemmDesc& g) {
+  if (g.impl == 1) return ROUTE_SIMT;
+  if (g.impl == 2) return ROUTE_TC;
+  if (gemm_small_supported(g)) return ROUTE_SMALL;
+  if (gemm_tc_supported(g)) return ROUTE_TC;
+  return ROUTE_SIMT;
 }
 
 int gemm_partial_tiles(const GemmDesc& g) {
-  return use_tc(g) ? gemm_tc_partial_tiles(g) : gemm_simt_partial_tiles(g);
+  switch (route(g)) {
+    case ROUTE_TC: return gemm_tc_partial_tiles(g);
+    case ROUTE_SMALL: return gemm_small_partial_tiles(g);
+    default: return gemm_simt_partial_tiles(g);
+  }
 }
 
-ttt_status gemm(const GemmDesc& g, cudaStream_t st) { return use_tc(g) ? gemm_tc(g, st) : gemm_simt(g, st); }
+int gemm_launches(const GemmDesc& g) { return (route(g) == ROUTE_TC && gemm_tc_splitk(g) > 1) ? 2 : 1; }
+
+ttt_status gemm(const GemmDesc& g, cudaStream_t st) {
+  switch (route(g)) {
+    case ROUTE_TC: return gemm_tc(g, st);
+    case ROUTE_SMALL: return gemm_small(g, st);
+    default: return gemm_simt(g, st);
+  }
+}
 
 }  // namespace ttt

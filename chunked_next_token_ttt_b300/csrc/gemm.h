@@ -32,6 +32,10 @@ struct GemmDesc {
   long long loA = 0, loB = 0, loO = 0, loO2 = 0, loX = 0;
   int* err = nullptr;              // device status word for bounded-wait timeouts
   int impl = 0;                    // 0 auto, 1 SIMT, 2 tensor cores
+  // optional fp32 workspace; the tensor-core path uses it to split K when a
+  // GEMM has too few output tiles to fill the GPU
+  float* ws = nullptr;
+  long long ws_elems = 0;
 };
 
 // Status bits the tensor-core kernel raises in *err when a bounded wait gives up.
@@ -43,8 +47,14 @@ enum GemmImpl { GEMM_IMPL_SIMT = 0, GEMM_IMPL_TC = 1 };
 // Number of per-batch partial slots an EPI_DW launch writes.
 int gemm_partial_tiles(const GemmDesc& g);
 ttt_status gemm(const GemmDesc& g, cudaStream_t st);
+// Kernels one gemm() call launches (2 when the tensor-core path splits K).
+int gemm_launches(const GemmDesc& g);
+int gemm_tc_splitk(const GemmDesc& g);
 ttt_status gemm_simt(const GemmDesc& g, cudaStream_t st);
 int gemm_simt_partial_tiles(const GemmDesc& g);
+bool gemm_small_supported(const GemmDesc& g);
+int gemm_small_partial_tiles(const GemmDesc& g);
+ttt_status gemm_small(const GemmDesc& g, cudaStream_t st);
 bool gemm_tc_supported(const GemmDesc& g);
 int gemm_tc_partial_tiles(const GemmDesc& g);
 ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st);

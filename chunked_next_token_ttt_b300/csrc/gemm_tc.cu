@@ -171,8 +171,13 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                   const GemmDesc g, int nkb, int* err) {
-  const int num_kb = SPLIT ? 3 * nkb : nkb;
+                   const GemmDesc g, int nkb, int splitk, int* err) {
+  // K range of this CTA (split-K: blockIdx.z = ks * batch + bz)
+  const int ks = blockIdx.z / g.batch;
+  const int kper = (nkb + splitk - 1) / splitk;
+  const int kb_lo = ks * kper;
+  const int nk_local = min(nkb, kb_lo + kper) - kb_lo;
+  const int num_kb = SPLIT ? 3 * nk_local : nk_local;
   using L = Smem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -183,7 +188,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
   float* red = reinterpret_cast<float*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN, bz = blockIdx.z;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN, bz = blockIdx.z % g.batch;
+  // split-K partials go to slice ks * batch + bz of the fp32 workspace
+  const int bz_out = blockIdx.z;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -214,8 +221,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       uint8_t* sa = smem + s * L::STAGE_BYTES;
       uint8_t* sb = sa + L::A_BYTES;
       mbar_expect_tx(&full[s], L::STAGE_BYTES);
-      const int term = SPLIT ? kb / nkb : 0;
-      const int k0 = (SPLIT ? kb - term * nkb : kb) * BK;
+      const int term = SPLIT ? kb / nk_local : 0;
+      const int k0 = (kb_lo + (SPLIT ? kb - term * nk_local : kb)) * BK;
       const CUtensorMap* ma = (SPLIT && term == 2) ? &tmA2 : &tmA;
       const CUtensorMap* mb = (SPLIT && term == 1) ? &tmB2 : &tmB;
       if (!A_MN) {
@@ -283,7 +290,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
             for (int cc = 0; cc < 2; ++cc) {
               const int n = n0 + c0 + cc * 32 + lane;
               const float a = stage[r * STAGE_LD + cc * 32 + lane];
-              if (n < g.N) sq += SPLIT ? epi_value<Split>(g, bz, row, n, a) : epi_value<bf16>(g, bz, row, n, a);
+              if (n < g.N) {
+                if (splitk > 1) static_cast<float*>(g.out)[(long long)bz_out * g.sO + (long long)row * g.ldo + n] = a;
+                else sq += SPLIT ? epi_value<Split>(g, bz, row, n, a) : epi_value<bf16>(g, bz, row, n, a);
+              }
             }
           }
         }
@@ -353,8 +363,21 @@ ttt_status make_map(CUtensorMap* m, const void* base, long long inner, long long
 constexpr int kBN = 128;
 constexpr int kStages = 3;
 
+// acc = sum over the split-K partial slices (fixed order); then the epilogue.
+template <typename S>
+__global__ void splitk_reduce_kernel(const GemmDesc g, const float* __restrict__ ws, int splitk) {
+  const int bz = blockIdx.y / g.M, m = blockIdx.y % g.M;
+  const long long slice = (long long)g.M * g.N;
+  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < g.N; n += gridDim.x * blockDim.x) {
+    const long long off = (long long)m * g.N + n;
+    float acc = 0.0f;
+    for (int k = 0; k < splitk; ++k) acc += ws[((long long)k * g.batch + bz) * slice + off];
+    epi_value<S>(g, bz, m, n, acc);
+  }
+}
+
 template <bool A_MN, bool B_MN, bool SPLIT>
-ttt_status launch_variant(const GemmDesc& g, const CUtensorMap* maps, int nkb, cudaStream_t st) {
+ttt_status launch_variant(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
   using L = Smem<kBN, kStages>;
   auto kern = gemm_tc_kernel<kBN, kStages, A_MN, B_MN, SPLIT>;
   static bool attr_set = false;
@@ -363,8 +386,21 @@ ttt_status launch_variant(const GemmDesc& g, const CUtensorMap* maps, int nkb, c
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
     attr_set = true;
   }
-  dim3 grid(ceil_div(g.N, kBN), ceil_div(g.M, BM), g.batch);
-  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], g, nkb, g.err);
+  dim3 grid(ceil_div(g.N, kBN), ceil_div(g.M, BM), g.batch * splitk);
+  if (splitk == 1) {
+    kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], g, nkb, 1, g.err);
+    TTT_CHECK_LAUNCH();
+    return TTT_OK;
+  }
+  GemmDesc gp = g;   // partial products into the workspace, fp32, one slice per (split, batch)
+  gp.out = g.ws;
+  gp.ldo = g.N;
+  gp.sO = (long long)g.M * g.N;
+  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], gp, nkb, splitk, g.err);
+  TTT_CHECK_LAUNCH();
+  dim3 rgrid(ceil_div(g.N, 256), g.batch * g.M);
+  if (SPLIT) splitk_reduce_kernel<Split><<<rgrid, 256, 0, st>>>(g, g.ws, splitk);
+  else splitk_reduce_kernel<bf16><<<rgrid, 256, 0, st>>>(g, g.ws, splitk);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -382,6 +418,23 @@ bool gemm_tc_supported(const GemmDesc& g) {
   if (g.batch > 1 && (g.sA % 8 || g.sB % 8 || g.sA <= 0 || g.sB <= 0)) return false;
   if (g.epi == EPI_DW && !g.partials) return false;
   return true;
+}
+
+// Split K when the output has too few 128x128 tiles to cover the SMs twice:
+// every split keeps at least 4 k-slices, the partial slices must fit the
+// workspace, and the dW epilogue (per-tile norm partials) never splits.
+int gemm_tc_splitk(const GemmDesc& g) {
+  if (!g.ws || g.epi == EPI_DW) return 1;
+  const long long tiles = (long long)ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM) * g.batch;
+  const int nkb = ceil_div(g.K, tc::BK);
+  if (tiles >= 148 || nkb < 8) return 1;
+  int want = (int)((2 * 148 + tiles - 1) / tiles);
+  if (want > nkb / 4) want = nkb / 4;
+  const long long slice = (long long)g.M * g.N * g.batch;
+  while (want > 1 && slice * want > g.ws_elems) --want;
+  if (want <= 1) return 1;
+  const int kper = ceil_div(nkb, want);
+  return ceil_div(nkb, kper);
 }
 
 int gemm_tc_partial_tiles(const GemmDesc& g) { return ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM); }
@@ -419,9 +472,10 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
     else TTT_TRY(tc::make_map(&maps[2 * p + 1], planesB[p], g.N, g.K, g.batch, g.ldb, g.sB, tc::PANEL, tc::BK));
   }
   const int nkb = ceil_div(g.K, tc::BK);
+  const int splitk = gemm_tc_splitk(g);
 #define TTT_TC_LAUNCH(AMN, BMN)                                                              \
-  return split ? tc::launch_variant<AMN, BMN, true>(gd, maps, nkb, st)                      \
-               : tc::launch_variant<AMN, BMN, false>(gd, maps, nkb, st)
+  return split ? tc::launch_variant<AMN, BMN, true>(gd, maps, nkb, splitk, st)              \
+               : tc::launch_variant<AMN, BMN, false>(gd, maps, nkb, splitk, st)
   if (!a_mn && !b_mn) TTT_TC_LAUNCH(false, false);
   if (!a_mn && b_mn) TTT_TC_LAUNCH(false, true);
   if (a_mn && !b_mn) TTT_TC_LAUNCH(true, false);

@@ -212,18 +212,37 @@ __global__ void norm_finalize_kernel(PartialSlots ps, const float* __restrict__ 
   }
 }
 
+// One (slot, sequence) segment of n elements per blockIdx.y; float4 accesses
+// when n is a multiple of 4 (every fast matrix: n = d * d_ff).
 template <typename S>
-__global__ void sgd_update_kernel(long long total, int B, long long n, float* __restrict__ W32, void* Wop,
-                                  long long wop_lo, const float* __restrict__ dW, const float* __restrict__ scale,
-                                  float eta) {
+__global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, void* Wop, long long wop_lo,
+                                  const float* __restrict__ dW, const float* __restrict__ scale, float eta) {
+  const int s = blockIdx.y % B;
+  const float sc = scale[s];
+  if (sc == 0.0f) return;  // skipped update (non-finite norm): W stays as it is
+  const float step = eta * sc;
+  const long long base = (long long)blockIdx.y * n;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int s = (int)((i / n) % B);
-    const float sc = scale[s];
-    if (sc == 0.0f) continue;  // skipped update (non-finite norm): W stays as it is
-    const float w = W32[i] - eta * sc * dW[i];
-    W32[i] = w;
-    OpIO<S>::store(Wop, wop_lo, i, w);
+  if ((n & 3) == 0) {
+    float4* w4 = reinterpret_cast<float4*>(W32 + base);
+    const float4* g4 = reinterpret_cast<const float4*>(dW + base);
+    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n / 4; q += stride) {
+      float4 w = w4[q];
+      const float4 gr = g4[q];
+      w.x -= step * gr.x; w.y -= step * gr.y; w.z -= step * gr.z; w.w -= step * gr.w;
+      w4[q] = w;
+      const long long i = base + 4 * q;
+      OpIO<S>::store(Wop, wop_lo, i, w.x);
+      OpIO<S>::store(Wop, wop_lo, i + 1, w.y);
+      OpIO<S>::store(Wop, wop_lo, i + 2, w.z);
+      OpIO<S>::store(Wop, wop_lo, i + 3, w.w);
+    }
+  } else {
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
+      const float w = W32[base + e] - step * dW[base + e];
+      W32[base + e] = w;
+      OpIO<S>::store(Wop, wop_lo, base + e, w);
+    }
   }
 }
 
@@ -392,9 +411,14 @@ ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* part
 
 ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
                              const float* dW, const float* scale, float eta, cudaStream_t st) {
-  const long long total = (long long)nslots * B * n;
-  const int g = grid_for(total, 256);
-  LAUNCH_BY_STORAGE(stg, sgd_update_kernel, g, 256, 0, st, total, B, n, W32, Wop, wop_lo, dW, scale, eta);
+  // blocks per segment: enough for ~16 blocks per SM over all segments
+  const int segs = nslots * B;
+  long long per = ((n + 3) / 4 + 255) / 256;
+  const long long cap = (148LL * 16 + segs - 1) / segs;
+  if (per > cap) per = cap;
+  if (per < 1) per = 1;
+  dim3 grid((unsigned)per, (unsigned)segs);
+  LAUNCH_BY_STORAGE(stg, sgd_update_kernel, grid, 256, 0, st, B, n, W32, Wop, wop_lo, dW, scale, eta);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

@@ -26,6 +26,7 @@ static bool to_desc(const ttt_gemm_args* a, GemmDesc* g) {
   g->partials = a->partials;
   g->impl = a->impl;
   g->loA = a->loA; g->loB = a->loB; g->loO = a->loO; g->loO2 = a->loO2; g->loX = a->loX;
+  g->ws = a->workspace; g->ws_elems = a->workspace ? a->workspace_elems : 0;
   return true;
 }
 

@@ -259,7 +259,8 @@ class GemmArgs(ctypes.Structure):
                 ("aux", ctypes.c_void_p), ("ldx", ctypes.c_longlong), ("sX", ctypes.c_longlong),
                 ("partials", ctypes.c_void_p),
                 ("loA", ctypes.c_longlong), ("loB", ctypes.c_longlong), ("loO", ctypes.c_longlong),
-                ("loO2", ctypes.c_longlong), ("loX", ctypes.c_longlong)]
+                ("loO2", ctypes.c_longlong), ("loX", ctypes.c_longlong),
+                ("workspace", ctypes.c_void_p), ("workspace_elems", ctypes.c_longlong)]
 
 
 def _ops_lib():
@@ -287,14 +288,15 @@ def _ops_lib():
 
 def gemm_args(M, N, K, A, B, out, *, batch=1, dtype="bf16", a_kmajor=True, b_kmajor=True, epi="store",
               impl="auto", lda=None, sA=0, ldb=None, sB=0, ldo=None, sO=0, out2=None, ldo2=0, sO2=0,
-              aux=None, ldx=0, sX=0, partials=None, loA=0, loB=0, loO=0, loO2=0, loX=0):
+              aux=None, ldx=0, sX=0, partials=None, loA=0, loB=0, loO=0, loO2=0, loX=0, workspace=None):
     """dtype: "fp32", "bf16" or "bf16x3" (fp32 values as bf16 hi/lo planes, lo offsets lo*)."""
     code = {"fp32": 0, "bf16": 1, "bf16x3": 2}[dtype]
     return GemmArgs(M, N, K, batch, code, int(a_kmajor), int(b_kmajor), EPI[epi], GEMM_IMPL[impl],
                     _ptr(A), lda if lda is not None else (K if a_kmajor else M), sA,
                     _ptr(B), ldb if ldb is not None else (K if b_kmajor else N), sB,
                     _ptr(out), ldo if ldo is not None else N, sO, _ptr(out2), ldo2, sO2,
-                    _ptr(aux), ldx, sX, _ptr(partials), loA, loB, loO, loO2, loX)
+                    _ptr(aux), ldx, sX, _ptr(partials), loA, loB, loO, loO2, loX,
+                    _ptr(workspace), 0 if workspace is None else workspace.numel())
 
 
 def op_gemm(args: GemmArgs, stream=None):

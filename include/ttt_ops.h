@@ -52,6 +52,9 @@ typedef struct {
   const void* aux; long long ldx, sX;
   float* partials;
   long long loA, loB, loO, loO2, loX;   /* lo-plane offsets (TTT_STORAGE_BF16X3 only) */
+  float* workspace;                     /* optional fp32 device buffer: lets the tensor-core
+                                           path split K when the output has few tiles */
+  long long workspace_elems;
 } ttt_gemm_args;
 
 ttt_status ttt_op_gemm(const ttt_gemm_args* args, ttt_stream stream);

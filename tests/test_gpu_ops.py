@@ -264,3 +264,65 @@ def test_bf16x3_split_gemm_is_fp32_accurate(a_k, b_k, impl):
     torch.cuda.synchronize()
     v = (o2[0].float() + o2[1].float()).cpu().numpy()
     assert np.abs(v - ref).max() <= 6e-5 * scale + 1e-5 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "bf16x3"])
+def test_split_k_narrow_long_k_gemm(dtype):
+    """N = 512, K = 2048, 2 x 2 tiles per batch: the tensor-core path splits K
+    into workspace slices and reduces them in a fixed order; results equal the
+    unsplit kernel's within fp32 rounding, and the GELU epilogue sees the sum."""
+    rng = np.random.default_rng(10)
+    M, N, K, batch = 256, 512, 2048, 2
+    A = rng.normal(0, 1, (batch, M, K)).astype(np.float32)
+    Bm = rng.normal(0, 1, (batch, N, K)).astype(np.float32)
+    if dtype == "bf16":
+        A, Bm = _bf(A).astype(np.float32), _bf(Bm).astype(np.float32)
+        Ad = torch.from_numpy(A).to(torch.bfloat16).cuda()
+        Bd = torch.from_numpy(Bm).to(torch.bfloat16).cuda()
+        lo = {}
+    else:
+        Ad, Bd = split_planes(A).cuda(), split_planes(Bm).cuda()
+        lo = dict(loA=batch * M * K, loB=batch * N * K)
+    ref = np.einsum("bmk,bnk->bmn", A.astype(np.float64), Bm.astype(np.float64))
+    ws = torch.zeros(16 * batch * M * N, dtype=torch.float32, device="cuda")
+    outs = []
+    for w in (None, ws):
+        out = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+        T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, out, batch=batch, dtype=dtype, epi="store_f32", impl="tensor",
+                              sA=M * K, sB=N * K, sO=M * N, workspace=w, **lo))
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy().astype(np.float64))
+    tol = (6e-5 if dtype == "bf16x3" else 2e-5) * np.sqrt(K)
+    assert np.abs(outs[0] - ref).max() <= tol * (1 if dtype == "bf16x3" else np.abs(ref).max() / np.sqrt(K))
+    np.testing.assert_allclose(outs[1], outs[0], rtol=1e-5, atol=1e-3)
+    # the workspace was used: its slices are non-zero
+    assert float(ws.abs().sum()) > 0
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("b_k", [True, False], ids=["B_kmaj", "B_nmaj"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "bf16x3"])
+def test_small_m_gemm(M, b_k, dtype):
+    """A few rows per batch entry (one token per sequence): weight-streaming kernel."""
+    rng = np.random.default_rng(11)
+    N, K, batch = 1000, 520, 3
+    A = rng.normal(0, 1, (batch, M, K)).astype(np.float32)
+    Bm = rng.normal(0, 1, (batch, N, K)).astype(np.float32)
+    Bs = Bm if b_k else np.ascontiguousarray(Bm.transpose(0, 2, 1))
+    if dtype == "fp32":
+        Ad, Bd, lo = torch.from_numpy(A).cuda(), torch.from_numpy(Bs).cuda(), {}
+        A64, B64 = A.astype(np.float64), Bm.astype(np.float64)
+    elif dtype == "bf16":
+        Ad, Bd, lo = (torch.from_numpy(A).to(torch.bfloat16).cuda(), torch.from_numpy(Bs).to(torch.bfloat16).cuda(), {})
+        A64, B64 = _bf(A), _bf(Bm)
+    else:
+        Ad, Bd = split_planes(A).cuda(), split_planes(Bs).cuda()
+        lo = dict(loA=batch * M * K, loB=batch * N * K)
+        A64, B64 = A.astype(np.float64), Bm.astype(np.float64)
+    ref = np.einsum("bmk,bnk->bmn", A64, B64)
+    out = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+    T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, out, batch=batch, dtype=dtype, b_kmajor=b_k, epi="store_f32",
+                          sA=M * K, sB=N * K, sO=M * N, **lo))
+    torch.cuda.synchronize()
+    tol = {"fp32": 1e-5, "bf16": 1e-5, "bf16x3": 6e-5}[dtype] * np.sqrt(K) * (np.abs(ref).max() if dtype != "bf16x3" else 1)
+    assert np.abs(out.cpu().numpy() - ref).max() <= tol
