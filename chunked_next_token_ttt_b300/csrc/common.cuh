@@ -99,6 +99,41 @@ template <> struct OpIO<Split> {
   }
 };
 
+// Two adjacent elements (i, i+1) at once; i even and the base (and, for Split,
+// the lo offset) aligned to the pair size.
+template <typename S> struct PairIO;
+template <> struct PairIO<float> {
+  __device__ __forceinline__ static float2 load(const void* p, long long, long long i) {
+    return *reinterpret_cast<const float2*>(static_cast<const float*>(p) + i);
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float a, float b) {
+    *reinterpret_cast<float2*>(static_cast<float*>(p) + i) = make_float2(a, b);
+  }
+};
+template <> struct PairIO<bf16> {
+  __device__ __forceinline__ static float2 load(const void* p, long long, long long i) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(static_cast<const bf16*>(p) + i));
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162*>(static_cast<bf16*>(p) + i) = __floats2bfloat162_rn(a, b);
+  }
+};
+template <> struct PairIO<Split> {
+  __device__ __forceinline__ static float2 load(const void* p, long long lo, long long i) {
+    const bf16* q = static_cast<const bf16*>(p);
+    const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q + i));
+    const float2 l = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q + lo + i));
+    return make_float2(h.x + l.x, h.y + l.y);
+  }
+  __device__ __forceinline__ static void store(void* p, long long lo, long long i, float a, float b) {
+    bf16* q = static_cast<bf16*>(p);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    *reinterpret_cast<__nv_bfloat162*>(q + i) = h;
+    *reinterpret_cast<__nv_bfloat162*>(q + lo + i) = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  }
+};
+
 // Exact (erf) GELU and its derivative, z * Phi(z) and Phi(z) + z phi(z).
 __device__ __forceinline__ float gelu_f(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));

@@ -1,0 +1,446 @@
+#pragma once
+// tcgen05 tensor-core GEMM kernel for sm_103a (template; instantiated per
+// operand-major combination in gemm_tc_{kk,km,mk,mm}.cu): bf16 operands (or bf16 hi/lo pairs
+// for fp32-accurate products), fp32 accumulation in TMEM, operands staged by
+// TMA into 128B-swizzled shared memory, with the TTT epilogues applied on the
+// way out of TMEM.
+//
+// Persistent: one CTA per SM walks the work units (output tile x K split) of
+// the GEMM in a static round robin.
+//   warp 0 (one lane)  TMA producer: a STAGES-deep ring of k-slices of 64
+//                      elements; a slot holds the A and B tiles (A_hi, A_lo,
+//                      B_hi, B_lo for split products), guarded by full/empty
+//                      mbarriers
+//   warp 1             allocates 2 x BN TMEM columns (two accumulators); one
+//                      lane issues tcgen05.mma (M=128, N=BN, K=16) into the
+//                      accumulator of the current unit, releases ring slots
+//                      with tcgen05.commit and hands the accumulator to the
+//                      epilogue with another commit
+//   warps 2..17        epilogue: tcgen05.ld of their 32-lane TMEM quadrant (four
+//                      warps per quadrant, splitting the columns), staged
+//                      through shared memory so that each warp then stores whole
+//                      row segments, two columns per lane (coalesced, vector
+//                      stores); they free the accumulator for the unit after
+//                      next, so unit i's epilogue overlaps unit i+1's MMAs.
+//                      The epilogue kind is a template argument (EK).
+// Operands may be K-major or MN-major (the backward's transposed products);
+// TMA loads MN-major operands as 64-element-wide column panels and the UMMA
+// descriptor's leading/stride byte offsets walk them.
+//
+// Every mbarrier wait is bounded (about 2 s of %globaltimer); on timeout the
+// waiting thread records a code in the error word and the CTA unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "epilogue.cuh"
+#include "gemm.h"
+
+namespace ttt {
+namespace tc {
+
+constexpr int BM = 128;        // UMMA M (one CTA, TMEM lanes 0..127 = rows)
+constexpr int BK = 64;         // k-slice: 64 bf16 = 128 bytes = one swizzle span
+constexpr int PANEL = 64;      // MN-major panel width (elements)
+constexpr int NUM_EPI_WARPS = 16;  // four per 32-lane TMEM quadrant, splitting the columns
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int STAGE_LD = 66;       // staging row stride in floats: 64 columns + 2 (conflict-free float2 access)
+constexpr int kBN = 128;           // output tile width
+constexpr int EK_PARTIAL = 100;    // epilogue kind: fp32 split-K partial slice
+constexpr long long kTimeoutNs = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on phase `parity`; false (and *err |= code) after the timeout.
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > (uint64_t)kTimeoutNs) {
+      atomicOr(err, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// UMMA shared-memory descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                       // D = F32
+         | (1u << 7)                     // A = BF16
+         | (1u << 10)                    // B = BF16
+         | ((a_mn ? 1u : 0u) << 15)      // A major: 0 = K, 1 = MN
+         | ((b_mn ? 1u : 0u) << 16)      // B major
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Barrier among the epilogue warps only (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * NUM_EPI_WARPS) : "memory");
+}
+
+template <int BN, bool SPLIT>
+struct Smem {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int NPL = SPLIT ? 2 : 1;                  // planes per operand
+  static constexpr int STAGE_BYTES = NPL * (A_BYTES + B_BYTES);
+  static constexpr int STAGING = BM * STAGE_LD * 4;         // epilogue staging
+  static constexpr int MAX_DYN = 232448;                     // per-block opt-in limit
+  static constexpr int OVERHEAD = 1024 + 512;                // base alignment + barriers
+  static constexpr int STAGES = (MAX_DYN - OVERHEAD - STAGING) / STAGE_BYTES;
+  static constexpr int RING = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = RING + STAGING;
+  static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 4) * 8 + 16 + NUM_EPI_WARPS * 4;
+  static constexpr int ALLOC = TOTAL + 1024;
+  static_assert(STAGES >= 2, "ring too shallow");
+  static_assert(ALLOC <= MAX_DYN, "shared memory over the per-block limit");
+};
+
+// Work unit u: n-tile fastest, then m-tile, then batch entry, then K split.
+struct Unit {
+  int m0, n0, bz, ks, mt, nt;
+};
+__device__ __forceinline__ Unit decode_unit(int u, int mtiles, int ntiles, int batch, int BN) {
+  Unit w;
+  w.nt = u % ntiles;
+  w.mt = (u / ntiles) % mtiles;
+  const int z = u / (ntiles * mtiles);
+  w.bz = z % batch;
+  w.ks = z / batch;
+  w.m0 = w.mt * BM;
+  w.n0 = w.nt * BN;
+  return w;
+}
+
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, int EK>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                   const GemmDesc g, int nkb, int splitk, int mtiles, int ntiles, int* err) {
+  using L = Smem<BN, SPLIT>;
+  constexpr int STAGES = L::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* stage = reinterpret_cast<float*>(smem + L::RING);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accf = empty + STAGES;     // [2] accumulator ready (MMA -> epilogue)
+  uint64_t* acce = accf + 2;           // [2] accumulator free (epilogue -> MMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int units = splitk * g.batch * mtiles * ntiles;
+  const int kper = (nkb + splitk - 1) / splitk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], NUM_EPI_WARPS);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(2 * BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    uint32_t kit = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(u, mtiles, ntiles, g.batch, BN);
+      const int kb_lo = w.ks * kper;
+      const int nk = min(nkb, kb_lo + kper) - kb_lo;
+      for (int kb = 0; kb < nk; ++kb, ++kit) {
+        const int s = kit % STAGES;
+        if (kit >= (uint32_t)STAGES && !mbar_wait(&empty[s], ((kit / STAGES) & 1) ^ 1, err, 8)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + s * L::STAGE_BYTES;
+        uint8_t* sb = sa + L::NPL * L::A_BYTES;
+        mbar_expect_tx(&full[s], L::STAGE_BYTES);
+        const int k0 = (kb_lo + kb) * BK;
+#pragma unroll
+        for (int p = 0; p < L::NPL; ++p) {
+          const CUtensorMap* ma = p ? &tmA2 : &tmA;
+          const CUtensorMap* mb = p ? &tmB2 : &tmB;
+          uint8_t* da = sa + p * L::A_BYTES;
+          uint8_t* db = sb + p * L::B_BYTES;
+          if (!A_MN) {
+            tma_load_3d(da, ma, &full[s], k0, w.m0, w.bz);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / PANEL; ++j) tma_load_3d(da + j * PANEL * BK * 2, ma, &full[s], w.m0 + j * PANEL, k0, w.bz);
+          }
+          if (!B_MN) {
+            tma_load_3d(db, mb, &full[s], k0, w.n0, w.bz);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / PANEL; ++j) tma_load_3d(db + j * PANEL * BK * 2, mb, &full[s], w.n0 + j * PANEL, k0, w.bz);
+          }
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = umma_idesc(BM, BN, A_MN, B_MN);
+    uint32_t kit = 0;
+    bool ok = true;
+    int i = 0;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+      const Unit w = decode_unit(u, mtiles, ntiles, g.batch, BN);
+      const int kb_lo = w.ks * kper;
+      const int nk = min(nkb, kb_lo + kper) - kb_lo;
+      const int ab = i & 1, use = i >> 1;
+      if (use >= 1 && !mbar_wait(&acce[ab], (use - 1) & 1, err, 16)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)(ab * BN);
+      for (int kb = 0; kb < nk; ++kb, ++kit) {
+        const int s = kit % STAGES;
+        if (!mbar_wait(&full[s], (kit / STAGES) & 1, err, 16)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * L::STAGE_BYTES);
+        const uint32_t sb = sa + L::NPL * L::A_BYTES;
+#pragma unroll
+        for (int t = 0; t < (SPLIT ? 3 : 1); ++t) {
+          // split products: hi*hi, hi*lo, lo*hi
+          const uint32_t pa = sa + (t == 2 ? L::A_BYTES : 0);
+          const uint32_t pb = sb + (t == 1 ? L::B_BYTES : 0);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // K-major: the 16-element k-step is 32 bytes inside the swizzle span.
+            // MN-major: 16 k-rows of 128 bytes; panels of 64 MN-elements are BK*128 bytes apart.
+            const uint64_t ad = A_MN ? umma_desc(pa + k * 2048, PANEL * BK * 2, 1024) : umma_desc(pa + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? umma_desc(pb + k * 2048, PANEL * BK * 2, 1024) : umma_desc(pb + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || t > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty[s]);
+      }
+      umma_commit(&accf[ab]);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue
+    // TMEM -> shared staging -> row segments, two columns per lane.
+    using S = typename std::conditional<SPLIT, Split, bf16>::type;
+    const int ew = warp - 2;                // 0..15; stores rows ew*8 .. ew*8+7 of each chunk
+    const int quad = warp & 3;              // TMEM lanes this warp may read
+    const int q4 = ew >> 2;                 // which 16 of each 64 columns it reads
+    constexpr int ROWS = BM / NUM_EPI_WARPS;
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      const Unit w = decode_unit(u, mtiles, ntiles, g.batch, BN);
+      const int ab = i & 1, use = i >> 1;
+      const bool ok = mbar_wait(&accf[ab], use & 1, err, 32);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t a_tmem = tmem + (uint32_t)(ab * BN) + ((uint32_t)(quad * 32) << 16);
+      float sq = 0.0f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        float v[16];
+        tmem_ld16(a_tmem + (uint32_t)(c0 + 16 * q4), v);
+        if (c0 + 64 >= BN) {
+          // every TMEM read of this accumulator is done: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[ab]);
+        }
+        float2* srow = reinterpret_cast<float2*>(stage + (quad * 32 + lane) * STAGE_LD + 16 * q4);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) srow[q] = make_float2(v[2 * q], v[2 * q + 1]);
+        epi_bar();
+        const int n = w.n0 + c0 + 2 * lane;
+#pragma unroll 2
+        for (int k = 0; k < ROWS; ++k) {
+          const int r = ew * ROWS + k;
+          const int row = w.m0 + r;
+          if (row < g.M && n < g.N) {
+            const float2 a = *reinterpret_cast<const float2*>(stage + r * STAGE_LD + 2 * lane);
+            if (EK == EK_PARTIAL) {
+              float* dst = static_cast<float*>(g.out) + ((long long)w.ks * g.batch + w.bz) * g.sO +
+                           (long long)row * g.ldo + n;
+              if (n + 1 < g.N) *reinterpret_cast<float2*>(dst) = a;
+              else dst[0] = a.x;
+            } else if (n + 1 < g.N) {
+              sq += epi_pair<S, EK>(g, w.bz, row, n, a.x, a.y);
+            } else {
+              sq += epi_value<S>(g, w.bz, row, n, a.x);
+            }
+          }
+        }
+        epi_bar();
+      }
+      if (EK == EPI_DW || (EK == EK_ANY && g.epi == EPI_DW)) {
+        sq = warp_sum(sq);
+        if (lane == 0) red[ew] = sq;
+        epi_bar();
+        if (ew == 0 && lane == 0) {
+          float t = 0.0f;
+          for (int q = 0; q < NUM_EPI_WARPS; ++q) t += red[q];
+          g.partials[(long long)w.bz * mtiles * ntiles + w.mt * ntiles + w.nt] = t;
+        }
+        epi_bar();
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN) : "memory");
+  }
+}
+
+extern int g_num_sms;
+
+// Launch one instantiation (persistent grid, one CTA per SM at most).
+template <bool A_MN, bool B_MN, bool SPLIT, int EK>
+ttt_status launch_kernel(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
+  using L = Smem<kBN, SPLIT>;
+  auto kern = gemm_tc_kernel<kBN, A_MN, B_MN, SPLIT, EK>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
+    attr_set = true;
+  }
+  const int mtiles = ceil_div(g.M, BM), ntiles = ceil_div(g.N, kBN);
+  const long long units = (long long)mtiles * ntiles * g.batch * splitk;
+  const int grid = (int)(units < g_num_sms ? units : g_num_sms);
+  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], g, nkb, splitk, mtiles, ntiles, g.err);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+// Per operand-major combination: picks the instantiation for (storage, epilogue).
+ttt_status launch_kk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st);
+ttt_status launch_km(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st);
+ttt_status launch_mk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st);
+ttt_status launch_mm(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st);
+
+}  // namespace tc
+}  // namespace ttt

@@ -1,0 +1,28 @@
+// tcgen05 GEMM instantiations: A K-major, B K-major (forward products).
+#include "gemm_tc_kernel.cuh"
+
+namespace ttt {
+namespace tc {
+
+template <bool SPLIT>
+static ttt_status dispatch_kk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
+  if (splitk > 1) return launch_kernel<false, false, SPLIT, EK_PARTIAL>(g, maps, nkb, splitk, st);
+  switch (g.epi) {
+    case EPI_STORE: return launch_kernel<false, false, SPLIT, EPI_STORE>(g, maps, nkb, splitk, st);
+    case EPI_STORE_F32: return launch_kernel<false, false, SPLIT, EPI_STORE_F32>(g, maps, nkb, splitk, st);
+    case EPI_GELU: return launch_kernel<false, false, SPLIT, EPI_GELU>(g, maps, nkb, splitk, st);
+    case EPI_RESID: return launch_kernel<false, false, SPLIT, EPI_RESID>(g, maps, nkb, splitk, st);
+    case EPI_SWIGLU: return launch_kernel<false, false, SPLIT, EPI_SWIGLU>(g, maps, nkb, splitk, st);
+    case EPI_DGELU: return launch_kernel<false, false, SPLIT, EPI_DGELU>(g, maps, nkb, splitk, st);
+    case EPI_DW: return launch_kernel<false, false, SPLIT, EPI_DW>(g, maps, nkb, splitk, st);
+    default: return launch_kernel<false, false, SPLIT, EK_ANY>(g, maps, nkb, splitk, st);
+  }
+}
+
+ttt_status launch_kk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
+  return g.dtype == ST_SPLIT ? dispatch_kk<true>(g, maps, nkb, splitk, st)
+                             : dispatch_kk<false>(g, maps, nkb, splitk, st);
+}
+
+}  // namespace tc
+}  // namespace ttt
