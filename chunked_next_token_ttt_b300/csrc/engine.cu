@@ -61,7 +61,13 @@ static ttt_status dalloc(ttt_handle* h, T** p, size_t bytes) {
 // class is being profiled.
 template <class F>
 static ttt_status run(ttt_handle* h, int cls, cudaStream_t st, int nkernels, F&& f) {
-  const bool prof = h->prof_class == cls && h->ev_used + 2 <= (int)h->ev.size();
+  const bool prof = h->prof_class == cls;
+  if (prof && h->ev_used + 2 > (int)h->ev.size()) {
+    // grow the event pool: every profiled launch of a long call keeps its pair
+    const size_t old = h->ev.size();
+    h->ev.resize(old + 4096);
+    for (size_t i = old; i < h->ev.size(); ++i) TTT_CUDA(cudaEventCreate(&h->ev[i]));
+  }
   if (prof) TTT_CUDA(cudaEventRecord(h->ev[h->ev_used], st));
   TTT_TRY(f());
   if (prof) {
@@ -89,6 +95,7 @@ static ttt_status rungemm(ttt_handle* h, int cls, const GemmDesc& g_in, cudaStre
   g.dtype = h->stg;
   g.ws = h->gemm_ws;
   g.ws_elems = h->gemm_ws_elems;
+  g.cnt = h->split_cnt;
   return run(h, cls, st, gemm_count(g), [&] { return gemm(g, st); });
 }
 
@@ -177,13 +184,33 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
     TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g2, st));
   }
 
-  TTT_TRY(run(h, K_RMSNORM_FWD, st, 1, [&] {
-    return launch_rmsnorm_fwd(stg, M, d, h->x32, h->dm.rms_eps, h->y.p, h->y.lo, h->rstd, st);
-  }));
-
   GemmDesc gh;
   gh.M = M; gh.N = V; gh.K = d;
   setA(gh, h->y, d); setB(gh, h->U, d);
+  // bf16 workloads fold the softmax statistics into the head GEMM's epilogue
+  // when it runs on the tensor cores (the per-row cross-entropy kernel otherwise)
+  GemmDesc gl = gh;
+  gl.dtype = stg;
+  gl.epi = EPI_LOGITS; gl.out = train ? h->logits : nullptr; gl.ldo = V;
+  gl.lse_part = h->lse_part; gl.lse_ld = h->lse_ld; gl.tgt = h->tgt; gl.tlogit = h->tlogit;
+  const bool fused = !head_f32 && stg == ST_BF16 && V % 8 == 0 && gemm_tc_supported(gl);
+
+  TTT_TRY(run(h, K_RMSNORM_FWD, st, 1, [&] {
+    return launch_rmsnorm_fwd(stg, M, d, h->x32, h->dm.rms_eps, h->y.p, h->y.lo, h->rstd, fused ? &tv : nullptr,
+                              h->tgt, st);
+  }));
+
+  const float scale = tv.n_valid > 0 ? 1.0f / (float)tv.n_valid : 0.0f;
+  if (fused) {
+    TTT_TRY(rungemm(h, K_GEMM_HEAD, gl, st));
+    const int nt = ceil_div(V, gemm_tc_tile_n());
+    TTT_TRY(run(h, K_CE, st, 1, [&] {
+      return launch_lse_combine(B, tv, h->lse_part, h->lse_ld, nt, h->tlogit, h->lse, losses, loss_ld, loss_off,
+                                h->row_loss, st);
+    }));
+    if (!train) return TTT_OK;
+    return run(h, K_CE, st, 1, [&] { return launch_dlogits(M, V, h->logits, h->lse, h->tgt, scale, st); });
+  }
   if (head_f32) {
     gh.epi = EPI_STORE_F32; gh.out = h->logits32; gh.ldo = V;
     return rungemm(h, K_GEMM_HEAD, gh, st);
@@ -194,7 +221,6 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
     gh.epi = EPI_STORE; gh.out = h->logits; gh.ldo = V;
   }
   TTT_TRY(rungemm(h, K_GEMM_HEAD, gh, st));
-  const float scale = tv.n_valid > 0 ? 1.0f / (float)tv.n_valid : 0.0f;
   return run(h, K_CE, st, 1, [&] {
     return launch_ce(stg, B, tv, V, h->logits, V, scale, train, losses, loss_ld, loss_off, h->row_loss, st);
   });
@@ -544,13 +570,23 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = dalloc(h, &h->rstd, Mm * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->logits, Mm * V * (split ? 4 : es))) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->row_loss, Mm * 4)) != TTT_OK) return bail(s);
+  // fused cross-entropy state: one online-softmax pair per row and head column tile
+  h->lse_ld = ceil_div(V, gemm_tc_tile_n());
+  if ((s = dalloc(h, &h->lse_part, Mm * (size_t)h->lse_ld * sizeof(float2))) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->lse, Mm * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->tlogit, Mm * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->tgt, Mm * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dy32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dh32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = op_alloc(&h->dhop, Mm * d)) != TTT_OK) return bail(s);
   // split-K workspace: up to 8 fp32 partial slices of a [Mmax, d] output, at most 64 MB
-  h->gemm_ws_elems = 8LL * (long long)Mm * d;
-  if (h->gemm_ws_elems > (16LL << 20)) h->gemm_ws_elems = 16LL << 20;
+  // room for the largest split the tensor-core path makes: fewer than 148 output
+  // tiles of 128 x 128 fp32, up to 4 K ranges each
+  h->gemm_ws_elems = 148LL * 4 * 128 * 128;
   if ((s = dalloc(h, &h->gemm_ws, (size_t)h->gemm_ws_elems * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->split_cnt, (size_t)gemm_tc_max_split_tiles() * 4)) != TTT_OK) return bail(s);
+  if (cudaMemset(h->split_cnt, 0, (size_t)gemm_tc_max_split_tiles() * 4) != cudaSuccess)
+    return bail(fail(TTT_ERR_CUDA, "cudaMemset of the split-K counters failed"));
   // partial sums of squares: at most one per 64x64 output tile per matrix and sequence
   h->partial_cap = (long long)h->nslots * B * ceil_div(d, 64) * ceil_div(f, 64);
   if ((s = dalloc(h, &h->partials, (size_t)h->partial_cap * 4)) != TTT_OK) return bail(s);

@@ -57,11 +57,17 @@ struct ttt_handle {
   float* rstd = nullptr;
   void* logits = nullptr;            // [Mmax, V]: float for ST_SPLIT, operand type otherwise
   float* row_loss = nullptr;
+  float2* lse_part = nullptr;        // [Mmax][lse_ld] head-tile softmax states
+  long long lse_ld = 0;
+  float* lse = nullptr;              // [Mmax]
+  float* tlogit = nullptr;           // [Mmax] fp32 target logits
+  int32_t* tgt = nullptr;            // [Mmax] target token per row, -1 = none
   float* dy32 = nullptr;
   float* dh32 = nullptr;
   OpBuf dhop;
   float* gemm_ws = nullptr;          // split-K partial products
   long long gemm_ws_elems = 0;
+  int* split_cnt = nullptr;          // split-K arrival counters (zero between GEMMs)
   float* partials = nullptr;
   long long partial_cap = 0;
   ttt::PartialSlots pslots{};

@@ -82,3 +82,113 @@ __device__ __forceinline__ float epi_pair(const GemmDesc& g, int bz, int m, int 
 }
 
 }  // namespace ttt
+
+namespace ttt {
+
+// Eight consecutive elements i .. i+7 of a buffer at once (16-byte accesses;
+// i, the base and, for Split, the lo offset are multiples of 8 elements).
+template <typename S> struct OctIO;
+template <> struct OctIO<float> {
+  __device__ __forceinline__ static void load(const void* p, long long, long long i, float* v) {
+    const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
+    const float4 a = q[0], b = q[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, const float* v) {
+    float4* q = reinterpret_cast<float4*>(static_cast<float*>(p) + i);
+    q[0] = make_float4(v[0], v[1], v[2], v[3]);
+    q[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+};
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  uint4 r;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+  return r;
+}
+__device__ __forceinline__ void unpack_bf16x8(uint4 r, float* v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = __bfloat1622float2(h[j]);
+    v[2 * j] = f.x;
+    v[2 * j + 1] = f.y;
+  }
+}
+template <> struct OctIO<bf16> {
+  __device__ __forceinline__ static void load(const void* p, long long, long long i, float* v) {
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(static_cast<const bf16*>(p) + i), v);
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, const float* v) {
+    *reinterpret_cast<uint4*>(static_cast<bf16*>(p) + i) = pack_bf16x8(v);
+  }
+};
+template <> struct OctIO<Split> {
+  __device__ __forceinline__ static void load(const void* p, long long lo, long long i, float* v) {
+    const bf16* q = static_cast<const bf16*>(p);
+    float h[8], l[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(q + i), h);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(q + lo + i), l);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = h[j] + l[j];
+  }
+  __device__ __forceinline__ static void store(void* p, long long lo, long long i, const float* v) {
+    bf16* q = static_cast<bf16*>(p);
+    const uint4 hp = pack_bf16x8(v);
+    float h[8], l[8];
+    unpack_bf16x8(hp, h);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) l[j] = v[j] - h[j];
+    *reinterpret_cast<uint4*>(q + i) = hp;
+    *reinterpret_cast<uint4*>(q + lo + i) = pack_bf16x8(l);
+  }
+};
+
+// epi_value for the eight elements (m, n) .. (m, n+7) at once; requires
+// GemmDesc::vec (every pointer, leading dim, batch stride and lo offset of the
+// epilogue a multiple of 8 elements) and n + 8 <= N.  Returns the sum of acc^2
+// for EPI_DW, 0 otherwise.
+template <typename S, int EK>
+__device__ __forceinline__ float epi_oct(const GemmDesc& g, int bz, int m, int n, const float* a) {
+  using O = OctIO<S>;
+  const int ek = EK == EK_ANY ? (int)g.epi : EK;
+  const long long io = bz * g.sO + (long long)m * g.ldo + n;
+  float t[8];
+  if (ek == EPI_STORE) {
+    O::store(g.out, g.loO, io, a);
+  } else if (ek == EPI_STORE_F32) {
+    OctIO<float>::store(g.out, 0, io, a);
+  } else if (ek == EPI_GELU) {
+    if (g.out) O::store(g.out, g.loO, io, a);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = gelu_f(a[j]);
+    O::store(g.out2, g.loO2, bz * g.sO2 + (long long)m * g.ldo2 + n, t);
+  } else if (ek == EPI_RESID) {
+    OctIO<float>::load(g.aux, 0, bz * g.sX + (long long)m * g.ldx + n, t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] += a[j];
+    OctIO<float>::store(g.out, 0, io, t);
+    if (g.out2) O::store(g.out2, g.loO2, bz * g.sO2 + (long long)m * g.ldo2 + n, t);
+  } else if (ek == EPI_SWIGLU) {
+    OctIO<float>::load(g.aux, 0, bz * g.sX + (long long)m * g.ldx + n, t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = silu_f(t[j]) * a[j];
+    O::store(g.out, g.loO, io, t);
+  } else if (ek == EPI_DGELU) {
+    O::load(g.aux, g.loX, bz * g.sX + (long long)m * g.ldx + n, t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = a[j] * gelu_grad_f(t[j]);
+    O::store(g.out, g.loO, io, t);
+  } else if (ek == EPI_DW) {
+    OctIO<float>::store(g.out, 0, io, a);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += a[j] * a[j];
+    return s;
+  }
+  return 0.0f;
+}
+
+}  // namespace ttt

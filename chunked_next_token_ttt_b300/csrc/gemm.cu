@@ -9,7 +9,7 @@ enum Route { ROUTE_SIMT, ROUTE_TC, ROUTE_SMALL };
 
 static Route route(const GemmDesc& g) {
   if (g.impl == 1) return ROUTE_SIMT;
-  if (g.impl == 2) return ROUTE_TC;
+  if (g.impl == 2 || g.epi == EPI_LOGITS) return ROUTE_TC;
   if (gemm_small_supported(g)) return ROUTE_SMALL;
   if (gemm_tc_supported(g)) return ROUTE_TC;
   return ROUTE_SIMT;
@@ -23,9 +23,13 @@ int gemm_partial_tiles(const GemmDesc& g) {
   }
 }
 
-int gemm_launches(const GemmDesc& g) { return (route(g) == ROUTE_TC && gemm_tc_splitk(g) > 1) ? 2 : 1; }
+int gemm_launches(const GemmDesc&) { return 1; }
 
 ttt_status gemm(const GemmDesc& g, cudaStream_t st) {
+  if (g.epi == EPI_LOGITS && route(g) != ROUTE_TC) {
+    set_error("the fused logits epilogue runs on the tensor-core GEMM only");
+    return TTT_ERR_UNSUPPORTED;
+  }
   switch (route(g)) {
     case ROUTE_TC: return gemm_tc(g, st);
     case ROUTE_SMALL: return gemm_small(g, st);

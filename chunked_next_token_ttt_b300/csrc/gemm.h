@@ -14,6 +14,9 @@ enum EpiKind {
   EPI_SWIGLU,      // out(op) = silu(aux(float)) * acc
   EPI_DGELU,       // out(op) = acc * GELU'(aux(op))
   EPI_DW,          // out(float) = acc; partials += per-tile sum of acc^2
+  EPI_LOGITS,      // tensor-core path only, batch 1: out(bf16) = acc when out is
+                   // non-null; lse_part[m][tile] = (max, sum exp(acc - max)) over the
+                   // tile's columns; tlogit[m] = acc at column tgt[m] (tgt[m] < 0: none)
 };
 
 struct GemmDesc {
@@ -30,12 +33,22 @@ struct GemmDesc {
   float* partials = nullptr;       // EPI_DW: [batch][gemm_partial_tiles()]
   // ST_SPLIT only: element offset of each op-typed pointer's lo plane
   long long loA = 0, loB = 0, loO = 0, loO2 = 0, loX = 0;
+  float2* lse_part = nullptr;      // EPI_LOGITS: [M][lse_ld] online-softmax states
+  long long lse_ld = 0;
+  const int32_t* tgt = nullptr;    // EPI_LOGITS: [M] target column per row, -1 = none
+  float* tlogit = nullptr;         // EPI_LOGITS: [M] fp32 logit of the target
   int* err = nullptr;              // device status word for bounded-wait timeouts
   int impl = 0;                    // 0 auto, 1 SIMT, 2 tensor cores
   // optional fp32 workspace; the tensor-core path uses it to split K when a
   // GEMM has too few output tiles to fill the GPU
   float* ws = nullptr;
   long long ws_elems = 0;
+  // split-K arrival counters, one per output tile, zero between launches; GEMMs
+  // that share them must run in stream order (null: a library-wide array)
+  int* cnt = nullptr;
+  // set by the tensor-core host code: every epilogue pointer, leading dim,
+  // batch stride and lo offset is a multiple of 8 elements (16-byte accesses)
+  bool vec = false;
 };
 
 // Status bits the tensor-core kernel raises in *err when a bounded wait gives up.
@@ -47,7 +60,7 @@ enum GemmImpl { GEMM_IMPL_SIMT = 0, GEMM_IMPL_TC = 1 };
 // Number of per-batch partial slots an EPI_DW launch writes.
 int gemm_partial_tiles(const GemmDesc& g);
 ttt_status gemm(const GemmDesc& g, cudaStream_t st);
-// Kernels one gemm() call launches (2 when the tensor-core path splits K).
+// Kernels one gemm() call launches.
 int gemm_launches(const GemmDesc& g);
 int gemm_tc_splitk(const GemmDesc& g);
 ttt_status gemm_simt(const GemmDesc& g, cudaStream_t st);
@@ -56,6 +69,12 @@ bool gemm_small_supported(const GemmDesc& g);
 int gemm_small_partial_tiles(const GemmDesc& g);
 ttt_status gemm_small(const GemmDesc& g, cudaStream_t st);
 bool gemm_tc_supported(const GemmDesc& g);
+// Output-tile width of the tensor-core kernel (the column tiles of EPI_LOGITS).
+int gemm_tc_tile_n();
+// Split-K arrival counters: the library-wide array (allocated and zeroed on
+// first use) and its capacity in output tiles.
+ttt_status gemm_tc_split_counters(int** cnt);
+int gemm_tc_max_split_tiles();
 int gemm_tc_partial_tiles(const GemmDesc& g);
 ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st);
 

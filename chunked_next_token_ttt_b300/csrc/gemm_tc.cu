@@ -1,5 +1,5 @@
-// Host side of the tcgen05 GEMM: tensor maps, shape checks, split-K choice,
-// the split-K reduction and the dispatch to the per-major instantiations.
+// Host side of the tcgen05 GEMM: tensor maps, shape checks, the split-K choice
+// and the dispatch to the per-major instantiations.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -50,19 +50,6 @@ ttt_status make_map(CUtensorMap* m, const void* base, long long inner, long long
   return TTT_OK;
 }
 
-// acc = sum over the split-K partial slices (fixed order); then the epilogue.
-template <typename S>
-__global__ void splitk_reduce_kernel(const GemmDesc g, const float* __restrict__ ws, int splitk) {
-  const int bz = blockIdx.y / g.M, m = blockIdx.y % g.M;
-  const long long slice = (long long)g.M * g.N;
-  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < g.N; n += gridDim.x * blockDim.x) {
-    const long long off = (long long)m * g.N + n;
-    float acc = 0.0f;
-    for (int k = 0; k < splitk; ++k) acc += ws[((long long)k * g.batch + bz) * slice + off];
-    epi_value<S>(g, bz, m, n, acc);
-  }
-}
-
 int g_num_sms = 0;
 
 }  // namespace tc
@@ -77,27 +64,38 @@ bool gemm_tc_supported(const GemmDesc& g) {
   if (g.lda % 8 || g.ldb % 8) return false;
   if (g.batch > 1 && (g.sA % 8 || g.sB % 8 || g.sA <= 0 || g.sB <= 0)) return false;
   if (g.epi == EPI_DW && !g.partials) return false;
+  if (g.epi == EPI_LOGITS &&
+      (g.dtype != ST_BF16 || g.batch != 1 || !g.a_kmajor || !g.b_kmajor || !g.lse_part || !g.tgt || !g.tlogit ||
+       g.lse_ld < ceil_div(g.N, tc::kBN)))
+    return false;
   // the epilogue stores column pairs: even leading dims, batch strides and lo offsets
   if ((g.ldo | g.sO | g.ldo2 | g.sO2 | g.ldx | g.sX | g.loO | g.loO2 | g.loX) & 1) return false;
   return true;
 }
 
-// Split K when the output has too few 128x128 tiles to cover the SMs twice:
+// Split K when the output has too few 128x128 tiles to cover half the SMs:
 // every split keeps at least 4 k-slices, the partial slices must fit the
 // workspace, and the dW epilogue (per-tile norm partials) never splits.
+static constexpr int kMaxSplitK = 4;
+
 int gemm_tc_splitk(const GemmDesc& g) {
-  if (!g.ws || g.epi == EPI_DW || (g.N & 1)) return 1;
+  if (!g.ws || g.epi == EPI_DW || g.epi == EPI_LOGITS || (g.N & 1)) return 1;
   const long long tiles = (long long)ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM) * g.batch;
   const int nkb = ceil_div(g.K, tc::BK);
-  if (tiles >= 148 || nkb < 8) return 1;
+  // (measured: splitting pays when at most half the SMs would get a tile)
+  if (2 * tiles > 148 || tiles > tc::kMaxSplitTiles || nkb < 8) return 1;
+  // the last CTA of a tile reads every partial back: keep the splits few
   int want = (int)((2 * 148 + tiles - 1) / tiles);
+  if (want > kMaxSplitK) want = kMaxSplitK;
   if (want > nkb / 4) want = nkb / 4;
-  const long long slice = (long long)g.M * g.N * g.batch;
+  const long long slice = tiles * tc::BM * tc::kBN;   // whole (padded) tiles per split
   while (want > 1 && slice * want > g.ws_elems) --want;
   if (want <= 1) return 1;
   const int kper = ceil_div(nkb, want);
   return ceil_div(nkb, kper);
 }
+
+int gemm_tc_tile_n() { return tc::kBN; }
 
 int gemm_tc_partial_tiles(const GemmDesc& g) { return ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM); }
 
@@ -111,6 +109,20 @@ ttt_status gemm_tc_error_word(int** err) {
   *err = tc::g_err;
   return TTT_OK;
 }
+
+ttt_status gemm_tc_split_counters(int** cnt) {
+  static int* g_cnt = nullptr;
+  if (!g_cnt) {
+    cudaError_t e = cudaMalloc(&g_cnt, tc::kMaxSplitTiles * sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc", __FILE__, __LINE__);
+    e = cudaMemset(g_cnt, 0, tc::kMaxSplitTiles * sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset", __FILE__, __LINE__);
+  }
+  *cnt = g_cnt;
+  return TTT_OK;
+}
+
+int gemm_tc_max_split_tiles() { return tc::kMaxSplitTiles; }
 
 ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (!gemm_tc_supported(g)) {
@@ -135,29 +147,38 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   }
   const int nkb = ceil_div(g.K, tc::BK);
   const int splitk = gemm_tc_splitk(g);
+  // 16-byte epilogue accesses need every epilogue address, leading dim, batch
+  // stride and lo offset on an 8-element boundary
+  {
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    const long long m8 = g.ldo | g.sO | g.ldo2 | g.sO2 | g.ldx | g.sX | g.loO | g.loO2 | g.loX;
+    gd.vec = (m8 & 7) == 0 && al(g.out) && al(g.out2) && al(g.aux);
+  }
   if (!tc::g_num_sms) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&tc::g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (tc::g_num_sms <= 0) tc::g_num_sms = 148;
+    // TTT_TC_MAX_CTAS caps the persistent grid (for per-SM throughput measurements)
+    if (const char* e = getenv("TTT_TC_MAX_CTAS")) {
+      const int cap = atoi(e);
+      if (cap > 0 && cap < tc::g_num_sms) tc::g_num_sms = cap;
+    }
   }
-  GemmDesc gk = gd;
-  if (splitk > 1) {   // partial products into the workspace, fp32, one slice per (split, batch)
-    gk.out = g.ws;
-    gk.ldo = g.N;
-    gk.sO = (long long)g.M * g.N;
+  if (splitk > 1) {
+    // partial tiles go to the workspace; the per-tile arrival counters start at
+    // zero and every split-K launch leaves them at zero
+    const long long tiles = (long long)ceil_div(g.M, tc::BM) * ceil_div(g.N, tc::kBN) * g.batch;
+    if (tiles > tc::kMaxSplitTiles) {
+      set_error("split-K GEMM with too many output tiles");
+      return TTT_ERR_UNSUPPORTED;
+    }
+    if (!gd.cnt) TTT_TRY(gemm_tc_split_counters(&gd.cnt));
   }
-  ttt_status s;
-  if (!a_mn && !b_mn) s = tc::launch_kk(gk, maps, nkb, splitk, st);
-  else if (!a_mn) s = tc::launch_km(gk, maps, nkb, splitk, st);
-  else if (!b_mn) s = tc::launch_mk(gk, maps, nkb, splitk, st);
-  else s = tc::launch_mm(gk, maps, nkb, splitk, st);
-  if (s != TTT_OK || splitk == 1) return s;
-  dim3 rgrid(ceil_div(g.N, 256), g.batch * g.M);
-  if (split) tc::splitk_reduce_kernel<Split><<<rgrid, 256, 0, st>>>(gd, g.ws, splitk);
-  else tc::splitk_reduce_kernel<bf16><<<rgrid, 256, 0, st>>>(gd, g.ws, splitk);
-  TTT_CHECK_LAUNCH();
-  return TTT_OK;
+  if (!a_mn && !b_mn) return tc::launch_kk(gd, maps, nkb, splitk, st);
+  if (!a_mn) return tc::launch_km(gd, maps, nkb, splitk, st);
+  if (!b_mn) return tc::launch_mk(gd, maps, nkb, splitk, st);
+  return tc::launch_mm(gd, maps, nkb, splitk, st);
 }
 
 }  // namespace ttt

@@ -16,13 +16,20 @@
 //                      accumulator of the current unit, releases ring slots
 //                      with tcgen05.commit and hands the accumulator to the
 //                      epilogue with another commit
-//   warps 2..17        epilogue: tcgen05.ld of their 32-lane TMEM quadrant (four
-//                      warps per quadrant, splitting the columns), staged
-//                      through shared memory so that each warp then stores whole
-//                      row segments, two columns per lane (coalesced, vector
-//                      stores); they free the accumulator for the unit after
-//                      next, so unit i's epilogue overlaps unit i+1's MMAs.
-//                      The epilogue kind is a template argument (EK).
+//   warps 2..9         epilogue: warp w reads TMEM lane quadrant w % 4 (the
+//                      hardware's rule) and one 64-column half of the tile, so
+//                      each thread holds 64 consecutive accumulators of one row
+//                      (two tcgen05.ld.32x32b.x32); it hands the accumulator back
+//                      to the MMA warp at once and applies the epilogue straight
+//                      from registers with 16-byte loads and stores (whole
+//                      sectors of a row per thread).  Unit i's epilogue
+//                      overlaps unit i+1's MMAs.  The epilogue kind is a
+//                      template argument (EK).
+// Split K: with splitk > 1 each unit is one K range of an output tile; its
+// epilogue writes the fp32 partial tile to the workspace, and the CTA that
+// completes a tile's last partial (a per-tile arrival counter) sums the
+// partials in split order and applies the epilogue, so the result does not
+// depend on which CTA finished last.
 // Operands may be K-major or MN-major (the backward's transposed products);
 // TMA loads MN-major operands as 64-element-wide column panels and the UMMA
 // descriptor's leading/stride byte offsets walk them.
@@ -32,6 +39,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cfloat>
 #include <type_traits>
 
 #include "epilogue.cuh"
@@ -43,11 +51,11 @@ namespace tc {
 constexpr int BM = 128;        // UMMA M (one CTA, TMEM lanes 0..127 = rows)
 constexpr int BK = 64;         // k-slice: 64 bf16 = 128 bytes = one swizzle span
 constexpr int PANEL = 64;      // MN-major panel width (elements)
-constexpr int NUM_EPI_WARPS = 16;  // four per 32-lane TMEM quadrant, splitting the columns
+constexpr int NUM_EPI_WARPS = 8;   // two per 32-lane TMEM quadrant, splitting the columns
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
-constexpr int STAGE_LD = 66;       // staging row stride in floats: 64 columns + 2 (conflict-free float2 access)
 constexpr int kBN = 128;           // output tile width
-constexpr int EK_PARTIAL = 100;    // epilogue kind: fp32 split-K partial slice
+constexpr int kCols = 64;          // accumulator columns per epilogue thread
+constexpr int kMaxSplitTiles = 256;  // output tiles of a split-K GEMM (arrival counters)
 constexpr long long kTimeoutNs = 2000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -150,19 +158,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -183,13 +178,29 @@ __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * NUM_EPI_WARPS) : "memory");
 }
 
+// Barrier among the epilogue warps that returns the AND of `ok` over all of
+// them, so that every epilogue warp takes the same exit after a bounded wait
+// and none is left waiting at a later barrier.
+__device__ __forceinline__ bool epi_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "n"(32 * NUM_EPI_WARPS)
+      : "memory");
+  return r != 0;
+}
+
 template <int BN, bool SPLIT>
 struct Smem {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int NPL = SPLIT ? 2 : 1;                  // planes per operand
   static constexpr int STAGE_BYTES = NPL * (A_BYTES + B_BYTES);
-  static constexpr int STAGING = BM * STAGE_LD * 4;         // epilogue staging
+  static constexpr int STAGING = 2 * (BN / kCols) * BM * 4;  // per-row softmax states of EPI_LOGITS
   static constexpr int MAX_DYN = 232448;                     // per-block opt-in limit
   static constexpr int OVERHEAD = 1024 + 512;                // base alignment + barriers
   static constexpr int STAGES = (MAX_DYN - OVERHEAD - STAGING) / STAGE_BYTES;
@@ -343,55 +354,138 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
-    // TMEM -> shared staging -> row segments, two columns per lane.
     using S = typename std::conditional<SPLIT, Split, bf16>::type;
-    const int ew = warp - 2;                // 0..15; stores rows ew*8 .. ew*8+7 of each chunk
+    constexpr int NG = BN / kCols;          // column groups per tile
+    static_assert(NUM_EPI_WARPS == 4 * NG, "one warp per (lane quadrant, column group)");
+    const int ew = warp - 2;                // 0..7
     const int quad = warp & 3;              // TMEM lanes this warp may read
-    const int q4 = ew >> 2;                 // which 16 of each 64 columns it reads
-    constexpr int ROWS = BM / NUM_EPI_WARPS;
+    const int cg = ew >> 2;                 // column group
+    const int r = quad * 32 + lane;         // tile row of this thread
+    float* lse_m = stage;                   // EPI_LOGITS: [NG][BM] row maxima
+    float* lse_s = stage + NG * BM;         //             [NG][BM] row sums of exp
     int i = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
       const Unit w = decode_unit(u, mtiles, ntiles, g.batch, BN);
       const int ab = i & 1, use = i >> 1;
-      const bool ok = mbar_wait(&accf[ab], use & 1, err, 32);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!epi_all(mbar_wait(&accf[ab], use & 1, err, 32))) break;
       tc_fence_after();
-      const uint32_t a_tmem = tmem + (uint32_t)(ab * BN) + ((uint32_t)(quad * 32) << 16);
+      float v[kCols];
+      {
+        const uint32_t ta = tmem + (uint32_t)(ab * BN + cg * kCols) + ((uint32_t)(quad * 32) << 16);
+        float (&v0)[32] = *reinterpret_cast<float(*)[32]>(v);
+        float (&v1)[32] = *reinterpret_cast<float(*)[32]>(v + 32);
+        tmem_ld32(ta, v0);
+        tmem_ld32(ta + 32, v1);
+      }
+      // every TMEM read of this accumulator is done: hand it back to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[ab]);
+
+      const int row = w.m0 + r;
+      const int n = w.n0 + cg * kCols;
+      const bool full_vec = g.vec && n + kCols <= g.N;
       float sq = 0.0f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        float v[16];
-        tmem_ld16(a_tmem + (uint32_t)(c0 + 16 * q4), v);
-        if (c0 + 64 >= BN) {
-          // every TMEM read of this accumulator is done: hand it back to the MMA warp
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acce[ab]);
-        }
-        float2* srow = reinterpret_cast<float2*>(stage + (quad * 32 + lane) * STAGE_LD + 16 * q4);
+      if (splitk > 1) {
+        // fp32 partial tile of this K range in the workspace, column-major inside
+        // the tile (column c holds the tile's BM rows), so that for every column
+        // a warp's 32 rows are one 128-byte line
+        const long long tiles = (long long)g.batch * mtiles * ntiles;
+        const long long tix = ((long long)w.bz * mtiles + w.mt) * ntiles + w.nt;
+        float* dst = g.ws + ((long long)w.ks * tiles + tix) * (BM * BN) + (long long)(cg * kCols) * BM + r;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) srow[q] = make_float2(v[2 * q], v[2 * q + 1]);
+        for (int j = 0; j < kCols; ++j) dst[j * BM] = v[j];
+        // Publish it; the CTA completing the tile's last partial reduces them.
+        // The barrier orders every epilogue thread's partial stores before one
+        // thread's GPU-scope release fence and arrival (fences are cumulative);
+        // the last arrival's acquire fence and the barrier after it order the
+        // other CTAs' partials before this CTA's loads.
         epi_bar();
-        const int n = w.n0 + c0 + 2 * lane;
-#pragma unroll 2
-        for (int k = 0; k < ROWS; ++k) {
-          const int r = ew * ROWS + k;
-          const int row = w.m0 + r;
-          if (row < g.M && n < g.N) {
-            const float2 a = *reinterpret_cast<const float2*>(stage + r * STAGE_LD + 2 * lane);
-            if (EK == EK_PARTIAL) {
-              float* dst = static_cast<float*>(g.out) + ((long long)w.ks * g.batch + w.bz) * g.sO +
-                           (long long)row * g.ldo + n;
-              if (n + 1 < g.N) *reinterpret_cast<float2*>(dst) = a;
-              else dst[0] = a.x;
-            } else if (n + 1 < g.N) {
-              sq += epi_pair<S, EK>(g, w.bz, row, n, a.x, a.y);
-            } else {
-              sq += epi_value<S>(g, w.bz, row, n, a.x);
-            }
+        if (ew == 0 && lane == 0) {
+          const int tile = (w.bz * mtiles + w.mt) * ntiles + w.nt;
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          const int last = atomicAdd(&g.cnt[tile], 1) == splitk - 1;
+          if (last) {
+            g.cnt[tile] = 0;  // ready for the next split-K GEMM in stream order
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          }
+          tmem_slot[1] = (uint32_t)last;
+        }
+        epi_bar();
+        if (tmem_slot[1] && row < g.M) {
+          // sum the partials in split order; one split's loads are all in flight at once
+          const float* src = g.ws + tix * (BM * BN) + (long long)(cg * kCols) * BM + r;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) v[j] = 0.0f;
+#pragma unroll 1
+          for (int q = 0; q < splitk; ++q) {
+            const float* sl = src + q * tiles * (BM * BN);
+#pragma unroll
+            for (int j = 0; j < kCols; ++j) v[j] += __ldcg(sl + j * BM);
+          }
+          if (full_vec) {
+#pragma unroll
+            for (int j = 0; j < kCols; j += 8) epi_oct<S, EK>(g, w.bz, row, n + j, v + j);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)
+              if (n + j < g.N) epi_value<S>(g, w.bz, row, n + j, v[j]);
           }
         }
+      } else if constexpr (EK == EPI_LOGITS) {
+        // bf16 logits out (when kept); online-softmax state of this thread's 32
+        // values, combined over the row's column groups; the target's fp32 logit
+        float mx = -FLT_MAX;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j)
+          if (n + j < g.N) mx = fmaxf(mx, v[j]);
+        float se = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j)
+          if (n + j < g.N) se += __expf(v[j] - mx);
+        if (row < g.M) {
+          if (g.out) {
+            if (full_vec) {
+#pragma unroll
+              for (int j = 0; j < kCols; j += 8) OctIO<bf16>::store(g.out, 0, (long long)row * g.ldo + n + j, v + j);
+            } else {
+              bf16* dst = static_cast<bf16*>(g.out) + (long long)row * g.ldo + n;
+#pragma unroll
+              for (int j = 0; j < kCols; ++j)
+                if (n + j < g.N) dst[j] = __float2bfloat16_rn(v[j]);
+            }
+          }
+          const int t = g.tgt[row] - n;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)
+            if (t == j && n + j < g.N) g.tlogit[row] = v[j];
+        }
+        lse_m[cg * BM + r] = mx;
+        lse_s[cg * BM + r] = se;
         epi_bar();
+        if (cg == 0 && row < g.M) {
+          float m0 = -FLT_MAX, s0 = 0.0f;
+#pragma unroll
+          for (int c = 0; c < NG; ++c) {
+            const float m2 = lse_m[c * BM + r], s2 = lse_s[c * BM + r];
+            if (m2 > -FLT_MAX) {
+              const float mm = fmaxf(m0, m2);
+              s0 = (m0 > -FLT_MAX ? s0 * __expf(m0 - mm) : 0.0f) + s2 * __expf(m2 - mm);
+              m0 = mm;
+            }
+          }
+          g.lse_part[(long long)row * g.lse_ld + w.nt] = make_float2(m0, s0);
+        }
+        epi_bar();
+      } else if (row < g.M) {
+        if (full_vec) {
+#pragma unroll
+          for (int j = 0; j < kCols; j += 8) sq += epi_oct<S, EK>(g, w.bz, row, n + j, v + j);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)
+            if (n + j < g.N) sq += epi_value<S>(g, w.bz, row, n + j, v[j]);
+        }
       }
       if (EK == EPI_DW || (EK == EK_ANY && g.epi == EPI_DW)) {
         sq = warp_sum(sq);

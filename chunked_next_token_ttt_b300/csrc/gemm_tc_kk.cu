@@ -6,7 +6,6 @@ namespace tc {
 
 template <bool SPLIT>
 static ttt_status dispatch_kk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
-  if (splitk > 1) return launch_kernel<false, false, SPLIT, EK_PARTIAL>(g, maps, nkb, splitk, st);
   switch (g.epi) {
     case EPI_STORE: return launch_kernel<false, false, SPLIT, EPI_STORE>(g, maps, nkb, splitk, st);
     case EPI_STORE_F32: return launch_kernel<false, false, SPLIT, EPI_STORE_F32>(g, maps, nkb, splitk, st);
@@ -15,6 +14,10 @@ static ttt_status dispatch_kk(const GemmDesc& g, const CUtensorMap* maps, int nk
     case EPI_SWIGLU: return launch_kernel<false, false, SPLIT, EPI_SWIGLU>(g, maps, nkb, splitk, st);
     case EPI_DGELU: return launch_kernel<false, false, SPLIT, EPI_DGELU>(g, maps, nkb, splitk, st);
     case EPI_DW: return launch_kernel<false, false, SPLIT, EPI_DW>(g, maps, nkb, splitk, st);
+    case EPI_LOGITS:
+      if constexpr (!SPLIT) return launch_kernel<false, false, false, EPI_LOGITS>(g, maps, nkb, splitk, st);
+      set_error("the fused logits epilogue takes bf16 operands");
+      return TTT_ERR_UNSUPPORTED;
     default: return launch_kernel<false, false, SPLIT, EK_ANY>(g, maps, nkb, splitk, st);
   }
 }

@@ -6,7 +6,6 @@ namespace tc {
 
 template <bool SPLIT>
 static ttt_status dispatch_km(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
-  if (splitk > 1) return launch_kernel<false, true, SPLIT, EK_PARTIAL>(g, maps, nkb, splitk, st);
   switch (g.epi) {
     case EPI_STORE_F32: return launch_kernel<false, true, SPLIT, EPI_STORE_F32>(g, maps, nkb, splitk, st);
     case EPI_DGELU: return launch_kernel<false, true, SPLIT, EPI_DGELU>(g, maps, nkb, splitk, st);

@@ -6,7 +6,6 @@ namespace tc {
 
 template <bool SPLIT>
 static ttt_status dispatch_mk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
-  if (splitk > 1) return launch_kernel<true, false, SPLIT, EK_PARTIAL>(g, maps, nkb, splitk, st);
   return launch_kernel<true, false, SPLIT, EK_ANY>(g, maps, nkb, splitk, st);
 }
 

@@ -6,7 +6,6 @@ namespace tc {
 
 template <bool SPLIT>
 static ttt_status dispatch_mm(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
-  if (splitk > 1) return launch_kernel<true, true, SPLIT, EK_PARTIAL>(g, maps, nkb, splitk, st);
   switch (g.epi) {
     case EPI_DW: return launch_kernel<true, true, SPLIT, EPI_DW>(g, maps, nkb, splitk, st);
     default: return launch_kernel<true, true, SPLIT, EK_ANY>(g, maps, nkb, splitk, st);

@@ -27,11 +27,18 @@ __global__ void embed_kernel(TokView tv, const ET* __restrict__ E, int d, float*
   }
 }
 
+__device__ __forceinline__ int target_of(const TokView& tv, int s, int j, int V);
+
 template <typename S>
 __global__ void rmsnorm_fwd_kernel(int d, const float* __restrict__ x, float eps, void* y, long long y_lo,
-                                   float* __restrict__ rstd) {
+                                   float* __restrict__ rstd, TokView tv, int32_t* __restrict__ tgt) {
   __shared__ float red[32];
   const long long m = blockIdx.x;
+  if (tgt && threadIdx.x == 0) {
+    // the target column of this row for the fused logits epilogue (-1: no target)
+    const int s = (int)(m / tv.rows), j = (int)(m % tv.rows);
+    tgt[m] = j < tv.n_valid ? target_of(tv, s, j, tv.vocab) : -1;
+  }
   const float* xr = x + m * d;
   float sq = 0.0f;
   for (int c = threadIdx.x; c < d; c += blockDim.x) sq += xr[c] * xr[c];
@@ -185,6 +192,68 @@ __global__ void ce_split_kernel(TokView tv, int V, float* __restrict__ logits, l
     const bf16 h = __float2bfloat16_rn(g);
     out[v] = h;
     out[V + v] = __float2bfloat16_rn(g - __bfloat162float(h));
+  }
+}
+
+// One warp per row: the row's logsumexp from the per-column-tile online
+// softmax states the head GEMM left, then the loss lse - logit[target].
+__global__ void lse_combine_kernel(TokView tv, int M, const float2* __restrict__ part, long long ld, int nt,
+                                   const float* __restrict__ tlogit, float* __restrict__ lse,
+                                   float* __restrict__ losses, long long loss_ld, long long loss_off,
+                                   float* __restrict__ row_loss) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (m >= M) return;
+  float mx = -FLT_MAX, se = 0.0f;
+  for (int t = lane; t < nt; t += 32) {
+    const float2 p = part[(long long)m * ld + t];
+    lse_combine(mx, se, p.x, p.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, se, o);
+    lse_combine(mx, se, m2, s2);
+  }
+  if (lane == 0) {
+    const float l = mx + logf(se);
+    lse[m] = l;
+    const int s = m / tv.rows, j = m % tv.rows;
+    if (j < tv.n_valid) {
+      const float loss = l - tlogit[m];
+      if (losses) losses[s * loss_ld + loss_off + j] = loss;
+      if (row_loss) row_loss[m] = loss;
+    }
+  }
+}
+
+// dlogits = (softmax - onehot(target)) * scale over bf16 logits [M, V] in place,
+// eight elements (16 bytes) per access; rows without a target get 0.
+__global__ void dlogits_kernel(int M, int V, bf16* __restrict__ logits, const float* __restrict__ lse,
+                               const int32_t* __restrict__ tgt, float scale) {
+  const long long nv = V / 8;
+  const long long total = (long long)M * nv;
+  uint4* base = reinterpret_cast<uint4*>(logits);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long m = i / nv;
+    const int c = (int)(i - m * nv) * 8;
+    const int t = tgt[m];
+    uint4 raw = base[i];
+    if (t < 0) {
+      base[i] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const float l = lse[m];
+    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 x = __bfloat1622float2(h2[q]);
+      const float g0 = (__expf(x.x - l) - (c + 2 * q == t ? 1.0f : 0.0f)) * scale;
+      const float g1 = (__expf(x.y - l) - (c + 2 * q + 1 == t ? 1.0f : 0.0f)) * scale;
+      h2[q] = __floats2bfloat162_rn(g0, g1);
+    }
+    base[i] = raw;
   }
 }
 
@@ -356,9 +425,10 @@ ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d,
 }
 
 ttt_status launch_rmsnorm_fwd(int stg, int M, int d, const float* x, float eps, void* y, long long y_lo, float* rstd,
-                              cudaStream_t st) {
+                              const TokView* tv, int32_t* tgt, cudaStream_t st) {
   if (M == 0) return TTT_OK;
-  LAUNCH_BY_STORAGE(stg, rmsnorm_fwd_kernel, M, 256, 0, st, d, x, eps, y, y_lo, rstd);
+  const TokView tvv = tv ? *tv : TokView();
+  LAUNCH_BY_STORAGE(stg, rmsnorm_fwd_kernel, M, 256, 0, st, d, x, eps, y, y_lo, rstd, tvv, tv ? tgt : nullptr);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -398,6 +468,30 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
     ce_kernel<float><<<M, 512, 0, st>>>(tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
                                         loss_off, row_loss);
   }
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long long ld, int nt,
+                              const float* tlogit, float* lse, float* losses, long long loss_ld, long long loss_off,
+                              float* row_loss, cudaStream_t st) {
+  const int M = B * tv.rows;
+  if (M == 0) return TTT_OK;
+  lse_combine_kernel<<<ceil_div(M, 8), 256, 0, st>>>(tv, M, part, ld, nt, tlogit, lse, losses, loss_ld, loss_off,
+                                                    row_loss);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const int32_t* tgt, float scale,
+                          cudaStream_t st) {
+  if (M == 0) return TTT_OK;
+  if (V % 8 || (reinterpret_cast<uintptr_t>(logits) & 15)) {
+    set_error("dlogits: V must be a multiple of 8 and the logits 16-byte aligned");
+    return TTT_ERR_UNSUPPORTED;
+  }
+  const long long total = (long long)M * (V / 8);
+  dlogits_kernel<<<grid_for(total, 256), 256, 0, st>>>(M, V, static_cast<bf16*>(logits), lse, tgt, scale);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

@@ -26,9 +26,10 @@ struct TokView {
 ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d, float* h32,
                         void* hop, long long hop_lo, cudaStream_t st);
 
-// y = x * rstd (operand type), rstd = 1/sqrt(mean(x^2) + eps).
+// y = x * rstd (operand type), rstd = 1/sqrt(mean(x^2) + eps).  With tv
+// non-null it also writes tgt[m], the target token of row m (-1 past n_valid).
 ttt_status launch_rmsnorm_fwd(int stg, int M, int d, const float* x, float eps, void* y, long long y_lo,
-                              float* rstd, cudaStream_t st);
+                              float* rstd, const TokView* tv, int32_t* tgt, cudaStream_t st);
 
 // dx = rstd * (dy - xhat * mean(xhat * dy)), xhat = x * rstd; dx32 and its
 // operand-type copy dxop (may be null).
@@ -48,6 +49,17 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
                      float scale, bool grad, float* losses, long long loss_ld, long long loss_off,
                      float* row_loss, cudaStream_t st);
 int ce_split_max_vocab();
+
+// Fused cross-entropy after the EPI_LOGITS head GEMM (bf16 logits):
+// lse[m] from the nt per-column-tile states part[m * ld + t]; for valid rows
+// the loss lse - tlogit[m] goes to losses / row_loss as in launch_ce.
+ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long long ld, int nt,
+                              const float* tlogit, float* lse, float* losses, long long loss_ld,
+                              long long loss_off, float* row_loss, cudaStream_t st);
+// In place over bf16 logits [M, V] (leading dim V, V % 8 == 0, 16-byte aligned):
+// dlogits = (exp(x - lse[m]) - [v == tgt[m]]) * scale; rows with tgt[m] < 0 get 0.
+ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const int32_t* tgt, float scale,
+                          cudaStream_t st);
 
 // Per-sequence global gradient norm from the dW GEMM partials, then the
 // clip scale s = min(1, clip/(norm+1e-6)) (1 when clip == 0).  A non-finite

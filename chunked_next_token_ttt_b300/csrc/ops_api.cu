@@ -76,7 +76,7 @@ ttt_status ttt_op_cross_entropy(int dtype, int M, int V, void* logits, const int
 ttt_status ttt_op_rmsnorm_forward(int dtype, int M, int d, const float* x, float eps, void* y, float* rstd,
                                   ttt_stream stream) {
   if (M < 0 || d < 1 || !x || !y || !rstd) return bad(TTT_ERR_BAD_ARG, "bad rmsnorm arguments");
-  return launch_rmsnorm_fwd(dtype, M, d, x, eps, y, 0, rstd, (cudaStream_t)stream);
+  return launch_rmsnorm_fwd(dtype, M, d, x, eps, y, 0, rstd, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 ttt_status ttt_op_rmsnorm_backward(int dtype, int M, int d, const float* x, const float* rstd, const float* dy,

@@ -299,6 +299,35 @@ def test_split_k_narrow_long_k_gemm(dtype):
     assert float(ws.abs().sum()) > 0
 
 
+def test_split_k_ragged_residual_twice_in_a_row():
+    """Split K with ragged row and column tiles (M = 200, N = 136) and the
+    residual epilogue, issued twice back to back: the last CTA of each tile sums
+    the partials in split order, so both calls give the same bits, and both
+    match the unsplit kernel within fp32 rounding (the per-tile arrival counters
+    are back at zero after each call)."""
+    rng = np.random.default_rng(11)
+    M, N, K, batch = 200, 136, 1536, 3
+    A = _bf(rng.normal(0, 1, (batch, M, K))).astype(np.float32)
+    Bm = _bf(rng.normal(0, 1, (batch, N, K))).astype(np.float32)
+    X = rng.normal(0, 1, (batch, M, N)).astype(np.float32)
+    Ad = torch.from_numpy(A).to(torch.bfloat16).cuda()
+    Bd = torch.from_numpy(Bm).to(torch.bfloat16).cuda()
+    Xd = torch.from_numpy(X).cuda()
+    ref = X + np.einsum("bmk,bnk->bmn", A.astype(np.float64), Bm.astype(np.float64))
+    ws = torch.zeros(16 * batch * M * N, dtype=torch.float32, device="cuda")
+    outs = []
+    for w in (None, ws, ws):
+        out = torch.zeros((batch, M, N), dtype=torch.float32, device="cuda")
+        T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, out, batch=batch, dtype="bf16", epi="resid", impl="tensor",
+                              sA=M * K, sB=N * K, sO=M * N, aux=Xd, ldx=N, sX=M * N, workspace=w))
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy().astype(np.float64))
+    assert float(ws.abs().sum()) > 0
+    np.testing.assert_array_equal(outs[1], outs[2])
+    np.testing.assert_allclose(outs[1], outs[0], rtol=1e-5, atol=2e-3)
+    assert np.abs(outs[0] - ref).max() <= 2e-3 * np.abs(ref).max()
+
+
 @pytest.mark.parametrize("M", [1, 3, 8])
 @pytest.mark.parametrize("b_k", [True, False], ids=["B_kmaj", "B_nmaj"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "bf16x3"])
