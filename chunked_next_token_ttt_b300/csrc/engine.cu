@@ -106,65 +106,131 @@ static void setOut(GemmDesc& g, const OpBuf& b, long long ld, long long s = 0) {
 static void setOut2(GemmDesc& g, const OpBuf& b, long long ld, long long s = 0) { g.out2 = b.p; g.loO2 = b.lo; g.ldo2 = ld; g.sO2 = s; }
 
 // ---------------------------------------------------------------- forward
+// Buffers of one pass of the embedding and the frozen prefix over B * rows rows
+// (row s * rows + j): the fp32 residual stream, an operand-type ping-pong
+// buffer, the operand copy of the prefix output, the hidden-width temporaries,
+// and, for a SwiGLU fast block whose gate and up projections are frozen, the
+// activation silu(gate h) * (up h) it feeds to its (fast) down projection.
+struct PrefixBufs {
+  float* x32 = nullptr;
+  OpBuf xop, hout, tmp_a;
+  float* tmp_g = nullptr;
+  OpBuf swiglu_a;        // p == nullptr: not computed here
+};
+
+// Embedding + frozen prefix (and the frozen SwiGLU front of fast block 0 when
+// pb.swiglu_a is set) for the tokens of tv: W-independent work.
+static ttt_status prefix_pass(ttt_handle* h, const TokView& tv, const PrefixBufs& pb, cudaStream_t st) {
+  const int B = h->B, M = B * tv.rows, d = h->d, f = h->f, stg = h->stg;
+  OpBuf cur = h->dm.n_prefix > 0 ? pb.xop : pb.hout;
+  TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(stg, B, tv, h->E, d, pb.x32, cur.p, cur.lo, st); }));
+  for (int p = 0; p < h->dm.n_prefix; ++p) {
+    const OpBuf* W = &h->prefix[(size_t)p * h->nm];
+    const OpBuf next = (p == h->dm.n_prefix - 1) ? pb.hout : pb.xop;
+    if (h->dm.block_kind == TTT_BLOCK_GELU) {
+      GemmDesc g;
+      g.M = M; g.N = f; g.K = d;
+      setA(g, cur, d); setB(g, W[0], d);
+      g.epi = EPI_GELU; g.out = nullptr; setOut2(g, pb.tmp_a, f);
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
+    } else {
+      GemmDesc g;
+      g.M = M; g.N = f; g.K = d;
+      setA(g, cur, d); setB(g, W[0], d);
+      g.epi = EPI_STORE_F32; g.out = pb.tmp_g; g.ldo = f;
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
+      setB(g, W[1], d); g.epi = EPI_SWIGLU; g.aux = pb.tmp_g; g.ldx = f; setOut(g, pb.tmp_a, f);
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
+    }
+    GemmDesc g2;
+    g2.M = M; g2.N = d; g2.K = f;
+    setA(g2, pb.tmp_a, f); setB(g2, W[h->nm - 1], f);
+    g2.epi = EPI_RESID; g2.aux = pb.x32; g2.ldx = d; g2.out = pb.x32; g2.ldo = d;
+    setOut2(g2, next, d);
+    TTT_TRY(rungemm(h, K_GEMM_PREFIX, g2, st));
+    cur = next;
+  }
+  if (pb.swiglu_a.p) {
+    const OpBuf* W = &h->fastfrozen[0];
+    GemmDesc g;
+    g.M = M; g.N = f; g.K = d;
+    setA(g, pb.hout, d); setB(g, W[0], d);
+    g.epi = EPI_STORE_F32; g.out = pb.tmp_g; g.ldo = f;
+    TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
+    setB(g, W[1], d); g.epi = EPI_SWIGLU; g.aux = pb.tmp_g; g.ldx = f; setOut(g, pb.swiglu_a, f);
+    TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
+  }
+  return TTT_OK;
+}
+
+// Rows of one chunk taken from a hoisted prefix pass over a group of chunks:
+// per sequence the group holds `rows_total` rows and this chunk starts at row0.
+struct Hoisted {
+  bool on = false;
+  long long row0 = 0, rows_total = 0;
+};
+
 // Forward over B * tv.rows rows with the current (or committed) fast weights.
 // train: keep the stash for backward and turn logits into dlogits in place.
 // head_f32: write fp32 logits into logits32 (rows must be 1) instead of the CE.
+// hz.on: the prefix output (and SwiGLU activation) of these rows is already in
+// the hoisted buffers; otherwise the embedding and the prefix run here.
 static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, bool train,
                           float* losses, long long loss_ld, long long loss_off, bool head_f32,
-                          cudaStream_t st) {
+                          cudaStream_t st, const Hoisted& hz = Hoisted()) {
   TokView tv = tv_in;
   tv.vocab = h->V;
   tv.err = h->flag;
   const int B = h->B, rows = tv.rows, M = B * rows, d = h->d, f = h->f, V = h->V;
   const int stg = h->stg;
   const OpBuf& Wop = committed ? h->Wcop : h->Wop;
-  OpBuf cur = h->dm.n_prefix > 0 ? h->xop : h->hlvl[0];
-  TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(stg, B, tv, h->E, d, h->x32, cur.p, cur.lo, st); }));
-
-  for (int p = 0; p < h->dm.n_prefix; ++p) {
-    const OpBuf* W = &h->prefix[(size_t)p * h->nm];
-    const OpBuf next = (p == h->dm.n_prefix - 1) ? h->hlvl[0] : h->xop;
-    if (h->dm.block_kind == TTT_BLOCK_GELU) {
-      GemmDesc g;
-      g.M = M; g.N = f; g.K = d;
-      setA(g, cur, d); setB(g, W[0], d);
-      g.epi = EPI_GELU; g.out = nullptr; setOut2(g, h->tmp_a, f);
-      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
-    } else {
-      GemmDesc g;
-      g.M = M; g.N = f; g.K = d;
-      setA(g, cur, d); setB(g, W[0], d);
-      g.epi = EPI_STORE_F32; g.out = h->tmp_g; g.ldo = f;
-      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
-      setB(g, W[1], d); g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; setOut(g, h->tmp_a, f);
-      TTT_TRY(rungemm(h, K_GEMM_PREFIX, g, st));
+  // inputs of fast block 0: its operand rows, their batch stride, the fp32 residual
+  OpBuf hin0 = h->hlvl[0];
+  long long hin0_s = (long long)rows * d;
+  const float* x0 = h->x32;
+  OpBuf a0;          // SwiGLU activation of block 0 when hoisted
+  long long a0_s = 0;
+  if (hz.on) {
+    hin0 = op_at(h, h->hx_op, hz.row0 * d);
+    hin0_s = hz.rows_total * d;
+    x0 = h->hx32 + hz.row0 * d;
+    if (h->ha.p) {
+      a0 = op_at(h, h->ha, hz.row0 * f);
+      a0_s = hz.rows_total * f;
     }
-    GemmDesc g2;
-    g2.M = M; g2.N = d; g2.K = f;
-    setA(g2, h->tmp_a, f); setB(g2, W[h->nm - 1], f);
-    g2.epi = EPI_RESID; g2.aux = h->x32; g2.ldx = d; g2.out = h->x32; g2.ldo = d;
-    setOut2(g2, next, d);
-    TTT_TRY(rungemm(h, K_GEMM_PREFIX, g2, st));
-    cur = next;
+  } else {
+    PrefixBufs pb;
+    pb.x32 = h->x32; pb.xop = h->xop; pb.hout = h->hlvl[0]; pb.tmp_a = h->tmp_a; pb.tmp_g = h->tmp_g;
+    TTT_TRY(prefix_pass(h, tv, pb, st));
   }
+  h->hin0 = hin0;
+  h->hin0_s = hin0_s;
+  h->a0 = a0;
+  h->a0_s = a0_s;
 
   for (int l = 0; l < h->dm.n_fast; ++l) {
-    const OpBuf hin = h->hlvl[l];
-    const OpBuf a_out = train ? h->ast[l] : h->tmp_a;
+    const OpBuf hin = l == 0 ? hin0 : h->hlvl[l];
+    const long long hin_s = l == 0 ? hin0_s : (long long)rows * d;
+    OpBuf a_out = train ? h->ast[l] : h->tmp_a;
+    long long a_s = (long long)rows * f;
     const bool has_next = l + 1 < h->dm.n_fast;
     const int s_down = h->slot_of[(size_t)l * h->nm + (h->nm - 1)];
     if (h->dm.block_kind == TTT_BLOCK_GELU) {
       const int s_up = h->slot_of[(size_t)l * h->nm + 0];
       GemmDesc g;
       g.M = rows; g.N = f; g.K = d; g.batch = B;
-      setA(g, hin, d, (long long)rows * d);
+      setA(g, hin, d, hin_s);
       setB(g, op_at(h, Wop, (long long)s_up * B * h->n), d, h->n);
       g.epi = EPI_GELU;
       if (train) setOut(g, h->zst[l], f, (long long)rows * f);
       else g.out = nullptr;
-      setOut2(g, a_out, f, (long long)rows * f);
+      setOut2(g, a_out, f, a_s);
       TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
+    } else if (l == 0 && a0.p) {
+      a_out = a0;
+      a_s = a0_s;
     } else {
+      // the frozen gate and up projections (rows contiguous across sequences here)
       const OpBuf* W = &h->fastfrozen[(size_t)l * h->nm];
       GemmDesc g;
       g.M = M; g.N = f; g.K = d;
@@ -174,11 +240,17 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
       setB(g, W[1], d); g.epi = EPI_SWIGLU; g.aux = h->tmp_g; g.ldx = f; setOut(g, a_out, f);
       TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
     }
+    if (l == 0 && h->dm.block_kind != TTT_BLOCK_GELU) {
+      h->a0 = a_out;
+      h->a0_s = a_s;
+    }
     GemmDesc g2;
     g2.M = rows; g2.N = d; g2.K = f; g2.batch = B;
-    setA(g2, a_out, f, (long long)rows * f);
+    setA(g2, a_out, f, a_s);
     setB(g2, op_at(h, Wop, (long long)s_down * B * h->n), f, h->n);
-    g2.epi = EPI_RESID; g2.aux = h->x32; g2.ldx = d; g2.sX = (long long)rows * d;
+    g2.epi = EPI_RESID;
+    g2.aux = l == 0 ? x0 : h->x32; g2.ldx = d; g2.sX = l == 0 ? (hz.on ? hz.rows_total * d : (long long)rows * d)
+                                                               : (long long)rows * d;
     g2.out = h->x32; g2.ldo = d; g2.sO = (long long)rows * d;
     if (has_next) setOut2(g2, h->hlvl[l + 1], d, (long long)rows * d);
     TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g2, st));
@@ -203,7 +275,7 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
   const float scale = tv.n_valid > 0 ? 1.0f / (float)tv.n_valid : 0.0f;
   if (fused) {
     TTT_TRY(rungemm(h, K_GEMM_HEAD, gl, st));
-    const int nt = ceil_div(V, gemm_tc_tile_n());
+    const int nt = ceil_div(V, gemm_tc_tile_n(gl));
     TTT_TRY(run(h, K_CE, st, 1, [&] {
       return launch_lse_combine(B, tv, h->lse_part, h->lse_ld, nt, h->tlogit, h->lse, losses, loss_ld, loss_off,
                                 h->row_loss, st);
@@ -283,7 +355,8 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
       GemmDesc g1;
       g1.M = f; g1.N = d; g1.K = rows; g1.batch = B;
       g1.a_kmajor = false; setA(g1, h->zst[l], f, (long long)rows * f);
-      g1.b_kmajor = false; setB(g1, h->hlvl[l], d, (long long)rows * d);
+      if (l == 0) { g1.b_kmajor = false; setB(g1, h->hin0, d, h->hin0_s); }
+      else { g1.b_kmajor = false; setB(g1, h->hlvl[l], d, (long long)rows * d); }
       g1.ldo = d;
       TTT_TRY(dw_gemm(g1, s1));
       if (l > 0) {
@@ -302,7 +375,8 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
       GemmDesc g;
       g.M = d; g.N = f; g.K = rows; g.batch = B;
       g.a_kmajor = false; setA(g, h->dhop, d, (long long)rows * d);
-      g.b_kmajor = false; setB(g, h->ast[l], f, (long long)rows * f);
+      if (l == 0) { g.b_kmajor = false; setB(g, h->a0, f, h->a0_s); }
+      else { g.b_kmajor = false; setB(g, h->ast[l], f, (long long)rows * f); }
       g.ldo = f;
       TTT_TRY(dw_gemm(g, sd));
     }
@@ -318,9 +392,24 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
 }
 
 static ttt_status chunk_step(ttt_handle* h, const TokView& tv, float* losses, long long loss_ld,
-                             long long loss_off, cudaStream_t st) {
-  TTT_TRY(forward(h, tv, false, true, losses, loss_ld, loss_off, false, st));
+                             long long loss_off, cudaStream_t st, const Hoisted& hz = Hoisted()) {
+  TTT_TRY(forward(h, tv, false, true, losses, loss_ld, loss_off, false, st, hz));
   return backward_update(h, tv.rows, st);
+}
+
+// The embedding and frozen prefix of chunks i0 .. i0+g-1 of every sequence in
+// one pass over B * g * b rows (they do not depend on the fast weights), into
+// the hoisted buffers laid out [B][g * b][.].
+static ttt_status hoisted_prefix(ttt_handle* h, const int32_t* tok, long long tok_ld, int i0, int g,
+                                 cudaStream_t st) {
+  TokView tv;
+  tv.tok = tok; tv.tok_ld = tok_ld; tv.tok_off = (long long)i0 * h->b; tv.rows = g * h->b; tv.n_valid = g * h->b;
+  tv.vocab = h->V;
+  tv.err = h->flag;
+  PrefixBufs pb;
+  pb.x32 = h->hx32; pb.xop = h->hx_xop; pb.hout = h->hx_op; pb.tmp_a = h->hx_tmp_a; pb.tmp_g = h->hx_tmp_g;
+  pb.swiglu_a = h->ha;
+  return prefix_pass(h, tv, pb, st);
 }
 
 // Settlement on held-out q [B, Lq] (device): writes A[B], accept[B].
@@ -564,6 +653,33 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
     if ((s = op_alloc(&h->ast[l], Mm * f)) != TTT_OK) return bail(s);
   }
   if ((s = op_alloc(&h->tmp_a, Mm * f)) != TTT_OK) return bail(s);
+  // hoisted prefix: groups of up to hoist_chunks chunks, within a 4 GiB budget
+  {
+    const size_t P = split ? 2 : 1;
+    size_t per_row = (size_t)d * 4 + (size_t)d * es * P + (D.n_prefix > 0 ? (size_t)d * es * P : 0) +
+                     (size_t)f * es * P;
+    if (D.block_kind == TTT_BLOCK_SWIGLU) per_row += (size_t)f * 4 + (size_t)f * es * P;
+    const size_t per_chunk = per_row * (size_t)B * h->b;
+    long long gmax = (long long)((4ull << 30) / per_chunk);
+    if (gmax > 64) gmax = 64;
+    // TTT_HOIST_CHUNKS caps the group (tests use it to cross group boundaries)
+    if (const char* e = getenv("TTT_HOIST_CHUNKS")) {
+      const long long cap = atoll(e);
+      if (cap > 0 && cap < gmax) gmax = cap;
+    }
+    if (gmax < 1) gmax = 1;
+    h->hoist_chunks = (int)gmax;
+    const size_t Mh = (size_t)B * h->b * gmax;
+    if ((s = dalloc(h, &h->hx32, Mh * d * 4)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->hx_op, Mh * d)) != TTT_OK) return bail(s);
+    if (D.n_prefix > 0)
+      if ((s = op_alloc(&h->hx_xop, Mh * d)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->hx_tmp_a, Mh * f)) != TTT_OK) return bail(s);
+    if (D.block_kind == TTT_BLOCK_SWIGLU) {
+      if ((s = dalloc(h, &h->hx_tmp_g, Mh * f * 4)) != TTT_OK) return bail(s);
+      if ((s = op_alloc(&h->ha, Mh * f)) != TTT_OK) return bail(s);
+    }
+  }
   if (D.block_kind == TTT_BLOCK_SWIGLU)
     if ((s = dalloc(h, &h->tmp_g, Mm * f * 4)) != TTT_OK) return bail(s);
   if ((s = op_alloc(&h->y, Mm * d)) != TTT_OK) return bail(s);
@@ -571,7 +687,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = dalloc(h, &h->logits, Mm * V * (split ? 4 : es))) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->row_loss, Mm * 4)) != TTT_OK) return bail(s);
   // fused cross-entropy state: one online-softmax pair per row and head column tile
-  h->lse_ld = ceil_div(V, gemm_tc_tile_n());
+  h->lse_ld = ceil_div(V, 128);  // the narrowest tensor-core tile
   if ((s = dalloc(h, &h->lse_part, Mm * (size_t)h->lse_ld * sizeof(float2))) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->lse, Mm * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->tlogit, Mm * 4)) != TTT_OK) return bail(s);
@@ -581,8 +697,8 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = op_alloc(&h->dhop, Mm * d)) != TTT_OK) return bail(s);
   // split-K workspace: up to 8 fp32 partial slices of a [Mmax, d] output, at most 64 MB
   // room for the largest split the tensor-core path makes: fewer than 148 output
-  // tiles of 128 x 128 fp32, up to 4 K ranges each
-  h->gemm_ws_elems = 148LL * 4 * 128 * 128;
+  // tiles of 128 x 128 fp32, up to 16 K ranges each (155 MB)
+  h->gemm_ws_elems = 148LL * 16 * 128 * 128;
   if ((s = dalloc(h, &h->gemm_ws, (size_t)h->gemm_ws_elems * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->split_cnt, (size_t)gemm_tc_max_split_tiles() * 4)) != TTT_OK) return bail(s);
   if (cudaMemset(h->split_cnt, 0, (size_t)gemm_tc_max_split_tiles() * 4) != cudaSuccess)
@@ -647,13 +763,22 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
 
   TTT_TRY(reset_weights(h, st));
   TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
-  for (int i = 0; i < n_full; ++i) {
-    TokView tv;
-    tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = (long long)i * b; tv.rows = b; tv.n_valid = b;
-    TTT_TRY(chunk_step(h, tv, loss_d, T, (long long)i * b, st));
-    if (h->hp.settle_every > 0 && (i + 1) % h->hp.settle_every == 0) {
-      const int e = (i + 1) / h->hp.settle_every - 1;
-      TTT_TRY(settle_event(h, q + (size_t)e * B * Lq, Lq, h->A_dev + (size_t)e * B, h->acc_dev + (size_t)e * B, st));
+  // chunks in groups whose frozen prefix runs as one pass before the group's TTT steps
+  const int G = h->hoist_chunks;
+  for (int i0 = 0; i0 < n_full; i0 += G) {
+    const int g = n_full - i0 < G ? n_full - i0 : G;
+    TTT_TRY(hoisted_prefix(h, tok, T + 1, i0, g, st));
+    for (int i = i0; i < i0 + g; ++i) {
+      TokView tv;
+      tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = (long long)i * b; tv.rows = b; tv.n_valid = b;
+      Hoisted hz;
+      hz.on = true; hz.row0 = (long long)(i - i0) * b; hz.rows_total = (long long)g * b;
+      TTT_TRY(chunk_step(h, tv, loss_d, T, (long long)i * b, st, hz));
+      if (h->hp.settle_every > 0 && (i + 1) % h->hp.settle_every == 0) {
+        const int e = (i + 1) / h->hp.settle_every - 1;
+        TTT_TRY(settle_event(h, q + (size_t)e * B * Lq, Lq, h->A_dev + (size_t)e * B, h->acc_dev + (size_t)e * B,
+                             st));
+      }
     }
   }
   if (rem > 0) {

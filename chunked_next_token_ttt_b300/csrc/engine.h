@@ -53,6 +53,16 @@ struct ttt_handle {
   std::vector<OpBuf> hlvl, zst, ast;
   OpBuf tmp_a;
   float* tmp_g = nullptr;
+  // hoisted prefix of a group of up to hoist_chunks chunks, rows [B][g * b]
+  int hoist_chunks = 1;
+  float* hx32 = nullptr;             // residual stream after the frozen prefix
+  OpBuf hx_op;                       // its operand copy (input of fast block 0)
+  OpBuf hx_xop, hx_tmp_a;            // prefix ping-pong and hidden-width temporaries
+  float* hx_tmp_g = nullptr;         // SwiGLU gate temporary
+  OpBuf ha;                          // SwiGLU fast block 0: silu(gate h) * (up h)
+  // inputs of fast block 0 in the last forward (backward reads them)
+  OpBuf hin0, a0;
+  long long hin0_s = 0, a0_s = 0;
   OpBuf y;
   float* rstd = nullptr;
   void* logits = nullptr;            // [Mmax, V]: float for ST_SPLIT, operand type otherwise

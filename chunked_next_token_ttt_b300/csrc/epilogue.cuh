@@ -192,3 +192,142 @@ __device__ __forceinline__ float epi_oct(const GemmDesc& g, int bz, int m, int n
 }
 
 }  // namespace ttt
+
+namespace ttt {
+
+// 32-byte (256-bit) global accesses: one whole sector per thread.  The address
+// must be 32-byte aligned.
+__device__ __forceinline__ void ld256(const void* p, uint32_t (&w)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st256(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Sixteen consecutive elements i .. i+15 at once with 32-byte accesses (i, the
+// base and, for Split, the lo offset are multiples of 16 elements; bases
+// 32-byte aligned).
+template <typename S> struct HexIO;
+template <> struct HexIO<float> {
+  __device__ __forceinline__ static void load(const void* p, long long, long long i, float* v) {
+    const float* q = static_cast<const float*>(p) + i;
+    uint32_t w[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      ld256(q + 8 * h, w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[8 * h + j] = __uint_as_float(w[j]);
+    }
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, const float* v) {
+    float* q = static_cast<float*>(p) + i;
+    uint32_t w[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = __float_as_uint(v[8 * h + j]);
+      st256(q + 8 * h, w);
+    }
+  }
+};
+__device__ __forceinline__ void pack_bf16x16(const float* v, uint32_t (&w)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    w[j] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+__device__ __forceinline__ void unpack_bf16x16(const uint32_t (&w)[8], float* v) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+    v[2 * j] = f.x;
+    v[2 * j + 1] = f.y;
+  }
+}
+template <> struct HexIO<bf16> {
+  __device__ __forceinline__ static void load(const void* p, long long, long long i, float* v) {
+    uint32_t w[8];
+    ld256(static_cast<const bf16*>(p) + i, w);
+    unpack_bf16x16(w, v);
+  }
+  __device__ __forceinline__ static void store(void* p, long long, long long i, const float* v) {
+    uint32_t w[8];
+    pack_bf16x16(v, w);
+    st256(static_cast<bf16*>(p) + i, w);
+  }
+};
+template <> struct HexIO<Split> {
+  __device__ __forceinline__ static void load(const void* p, long long lo, long long i, float* v) {
+    const bf16* q = static_cast<const bf16*>(p);
+    uint32_t w[8];
+    float l[16];
+    ld256(q + i, w);
+    unpack_bf16x16(w, v);
+    ld256(q + lo + i, w);
+    unpack_bf16x16(w, l);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] += l[j];
+  }
+  __device__ __forceinline__ static void store(void* p, long long lo, long long i, const float* v) {
+    bf16* q = static_cast<bf16*>(p);
+    uint32_t w[8];
+    float h[16], l[16];
+    pack_bf16x16(v, w);
+    unpack_bf16x16(w, h);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) l[j] = v[j] - h[j];
+    st256(q + i, w);
+    pack_bf16x16(l, w);
+    st256(q + lo + i, w);
+  }
+};
+
+// epi_oct for sixteen elements (m, n) .. (m, n+15) with 32-byte accesses;
+// requires GemmDesc::vec == 2 and n + 16 <= N.
+template <typename S, int EK>
+__device__ __forceinline__ float epi_hex(const GemmDesc& g, int bz, int m, int n, const float* a) {
+  using O = HexIO<S>;
+  const int ek = EK == EK_ANY ? (int)g.epi : EK;
+  const long long io = bz * g.sO + (long long)m * g.ldo + n;
+  float t[16];
+  if (ek == EPI_STORE) {
+    O::store(g.out, g.loO, io, a);
+  } else if (ek == EPI_STORE_F32) {
+    HexIO<float>::store(g.out, 0, io, a);
+  } else if (ek == EPI_GELU) {
+    if (g.out) O::store(g.out, g.loO, io, a);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = gelu_f(a[j]);
+    O::store(g.out2, g.loO2, bz * g.sO2 + (long long)m * g.ldo2 + n, t);
+  } else if (ek == EPI_RESID) {
+    HexIO<float>::load(g.aux, 0, bz * g.sX + (long long)m * g.ldx + n, t);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] += a[j];
+    HexIO<float>::store(g.out, 0, io, t);
+    if (g.out2) O::store(g.out2, g.loO2, bz * g.sO2 + (long long)m * g.ldo2 + n, t);
+  } else if (ek == EPI_SWIGLU) {
+    HexIO<float>::load(g.aux, 0, bz * g.sX + (long long)m * g.ldx + n, t);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = silu_f(t[j]) * a[j];
+    O::store(g.out, g.loO, io, t);
+  } else if (ek == EPI_DGELU) {
+    O::load(g.aux, g.loX, bz * g.sX + (long long)m * g.ldx + n, t);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = a[j] * gelu_grad_f(t[j]);
+    O::store(g.out, g.loO, io, t);
+  } else if (ek == EPI_DW) {
+    HexIO<float>::store(g.out, 0, io, a);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s += a[j] * a[j];
+    return s;
+  }
+  return 0.0f;
+}
+
+}  // namespace ttt

@@ -47,8 +47,11 @@ struct GemmDesc {
   // that share them must run in stream order (null: a library-wide array)
   int* cnt = nullptr;
   // set by the tensor-core host code: every epilogue pointer, leading dim,
-  // batch stride and lo offset is a multiple of 8 elements (16-byte accesses)
-  bool vec = false;
+  // batch stride and lo offset is a multiple of 16 elements with 32-byte aligned
+  // pointers (2: 32-byte accesses), else of 8 elements with 16-byte aligned
+  // pointers (1: 16-byte accesses), else 0 (element by element)
+  int vec = 0;
+  int bn = 128;                    // output tile width chosen by the tensor-core host code
 };
 
 // Status bits the tensor-core kernel raises in *err when a bounded wait gives up.
@@ -69,8 +72,9 @@ bool gemm_small_supported(const GemmDesc& g);
 int gemm_small_partial_tiles(const GemmDesc& g);
 ttt_status gemm_small(const GemmDesc& g, cudaStream_t st);
 bool gemm_tc_supported(const GemmDesc& g);
-// Output-tile width of the tensor-core kernel (the column tiles of EPI_LOGITS).
-int gemm_tc_tile_n();
+// Output-tile width the tensor-core kernel uses for g (the column tiles of
+// EPI_LOGITS, the per-tile partials of EPI_DW).
+int gemm_tc_tile_n(const GemmDesc& g);
 // Split-K arrival counters: the library-wide array (allocated and zeroed on
 // first use) and its capacity in output tiles.
 ttt_status gemm_tc_split_counters(int** cnt);

@@ -54,6 +54,13 @@ int g_num_sms = 0;
 
 }  // namespace tc
 
+// 128 x 256 tiles for bf16 GEMMs that still have two waves of them.
+static int choose_bn(const GemmDesc& g) {
+  if (g.dtype != ST_BF16) return tc::kBN;
+  const long long t256 = (long long)ceil_div(g.N, 256) * ceil_div(g.M, tc::BM) * g.batch;
+  return t256 >= 2 * 148 ? 256 : tc::kBN;
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 bool gemm_tc_supported(const GemmDesc& g) {
@@ -66,38 +73,48 @@ bool gemm_tc_supported(const GemmDesc& g) {
   if (g.epi == EPI_DW && !g.partials) return false;
   if (g.epi == EPI_LOGITS &&
       (g.dtype != ST_BF16 || g.batch != 1 || !g.a_kmajor || !g.b_kmajor || !g.lse_part || !g.tgt || !g.tlogit ||
-       g.lse_ld < ceil_div(g.N, tc::kBN)))
+       g.lse_ld < ceil_div(g.N, choose_bn(g))))
     return false;
   // the epilogue stores column pairs: even leading dims, batch strides and lo offsets
   if ((g.ldo | g.sO | g.ldo2 | g.sO2 | g.ldx | g.sX | g.loO | g.loO2 | g.loX) & 1) return false;
   return true;
 }
 
-// Split K when the output has too few 128x128 tiles to cover half the SMs:
-// every split keeps at least 4 k-slices, the partial slices must fit the
-// workspace, and the dW epilogue (per-tile norm partials) never splits.
-static constexpr int kMaxSplitK = 4;
+// Split K when the output has fewer 128x128 tiles than SMs.  The number of K
+// ranges s minimises a cost in k-slice times: waves(s) * ceil(nkb / s) for the
+// main loop, plus, when split, one partial tile written per unit and s partial
+// tiles read back by a tile's last CTA (measured at about 1.5 k-slices each).
+// Every range keeps at least 4 k-slices, the partial tiles must fit the
+// workspace, and the dW and logits epilogues (per-tile partial sums) never split.
+static constexpr int kMaxSplitK = 16;
 
 int gemm_tc_splitk(const GemmDesc& g) {
   if (!g.ws || g.epi == EPI_DW || g.epi == EPI_LOGITS || (g.N & 1)) return 1;
+  if (choose_bn(g) != tc::kBN) return 1;
   const long long tiles = (long long)ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM) * g.batch;
   const int nkb = ceil_div(g.K, tc::BK);
-  // (measured: splitting pays when at most half the SMs would get a tile)
-  if (2 * tiles > 148 || tiles > tc::kMaxSplitTiles || nkb < 8) return 1;
-  // the last CTA of a tile reads every partial back: keep the splits few
-  int want = (int)((2 * 148 + tiles - 1) / tiles);
-  if (want > kMaxSplitK) want = kMaxSplitK;
-  if (want > nkb / 4) want = nkb / 4;
+  if (tiles >= 148 || tiles > tc::kMaxSplitTiles || nkb < 8) return 1;
   const long long slice = tiles * tc::BM * tc::kBN;   // whole (padded) tiles per split
-  while (want > 1 && slice * want > g.ws_elems) --want;
-  if (want <= 1) return 1;
-  const int kper = ceil_div(nkb, want);
-  return ceil_div(nkb, kper);
+  int best = 1;
+  double best_cost = (double)nkb;
+  for (int sk = 2; sk <= kMaxSplitK && sk <= nkb / 4; ++sk) {
+    if (slice * sk > g.ws_elems) break;
+    const int kper = ceil_div(nkb, sk);
+    const int ranges = ceil_div(nkb, kper);
+    const long long units = tiles * ranges;
+    const long long waves = (units + 147) / 148;
+    const double cost = (double)waves * kper + 1.0 + 1.5 * ranges;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = ranges;
+    }
+  }
+  return best;
 }
 
-int gemm_tc_tile_n() { return tc::kBN; }
+int gemm_tc_tile_n(const GemmDesc& g) { return choose_bn(g); }
 
-int gemm_tc_partial_tiles(const GemmDesc& g) { return ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM); }
+int gemm_tc_partial_tiles(const GemmDesc& g) { return ceil_div(g.N, choose_bn(g)) * ceil_div(g.M, tc::BM); }
 
 ttt_status gemm_tc_error_word(int** err) {
   if (!tc::g_err) {
@@ -134,6 +151,7 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (!gd.err) TTT_TRY(gemm_tc_error_word(&gd.err));
   const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
   const bool split = g.dtype == ST_SPLIT;
+  gd.bn = choose_bn(g);
   // maps: A hi, B hi, A lo, B lo.  A: K-major [batch][M][K] boxes {64, 128};
   // MN-major [batch][K][M] panels {64, 64}.  Likewise B with BN rows.
   CUtensorMap maps[4];
@@ -142,7 +160,7 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   for (int p = 0; p < 2; ++p) {
     if (!a_mn) TTT_TRY(tc::make_map(&maps[2 * p], planesA[p], g.K, g.M, g.batch, g.lda, g.sA, tc::BK, tc::BM));
     else TTT_TRY(tc::make_map(&maps[2 * p], planesA[p], g.M, g.K, g.batch, g.lda, g.sA, tc::PANEL, tc::BK));
-    if (!b_mn) TTT_TRY(tc::make_map(&maps[2 * p + 1], planesB[p], g.K, g.N, g.batch, g.ldb, g.sB, tc::BK, tc::kBN));
+    if (!b_mn) TTT_TRY(tc::make_map(&maps[2 * p + 1], planesB[p], g.K, g.N, g.batch, g.ldb, g.sB, tc::BK, gd.bn));
     else TTT_TRY(tc::make_map(&maps[2 * p + 1], planesB[p], g.N, g.K, g.batch, g.ldb, g.sB, tc::PANEL, tc::BK));
   }
   const int nkb = ceil_div(g.K, tc::BK);
@@ -150,9 +168,11 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   // 16-byte epilogue accesses need every epilogue address, leading dim, batch
   // stride and lo offset on an 8-element boundary
   {
-    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-    const long long m8 = g.ldo | g.sO | g.ldo2 | g.sO2 | g.ldx | g.sX | g.loO | g.loO2 | g.loX;
-    gd.vec = (m8 & 7) == 0 && al(g.out) && al(g.out2) && al(g.aux);
+    auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+    const long long m = g.ldo | g.sO | g.ldo2 | g.sO2 | g.ldx | g.sX | g.loO | g.loO2 | g.loX;
+    if ((m & 15) == 0 && al(g.out, 32) && al(g.out2, 32) && al(g.aux, 32)) gd.vec = 2;
+    else if ((m & 7) == 0 && al(g.out, 16) && al(g.out2, 16) && al(g.aux, 16)) gd.vec = 1;
+    else gd.vec = 0;
   }
   if (!tc::g_num_sms) {
     int dev = 0;

@@ -200,7 +200,7 @@ struct Smem {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int NPL = SPLIT ? 2 : 1;                  // planes per operand
   static constexpr int STAGE_BYTES = NPL * (A_BYTES + B_BYTES);
-  static constexpr int STAGING = 2 * (BN / kCols) * BM * 4;  // per-row softmax states of EPI_LOGITS
+  static constexpr int STAGING = 2 * (NUM_EPI_WARPS / 4) * BM * 4;  // per-row softmax states of EPI_LOGITS
   static constexpr int MAX_DYN = 232448;                     // per-block opt-in limit
   static constexpr int OVERHEAD = 1024 + 512;                // base alignment + barriers
   static constexpr int STAGES = (MAX_DYN - OVERHEAD - STAGING) / STAGE_BYTES;
@@ -355,58 +355,117 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
     using S = typename std::conditional<SPLIT, Split, bf16>::type;
-    constexpr int NG = BN / kCols;          // column groups per tile
-    static_assert(NUM_EPI_WARPS == 4 * NG, "one warp per (lane quadrant, column group)");
-    const int ew = warp - 2;                // 0..7
-    const int quad = warp & 3;              // TMEM lanes this warp may read
-    const int cg = ew >> 2;                 // column group
-    const int r = quad * 32 + lane;         // tile row of this thread
-    float* lse_m = stage;                   // EPI_LOGITS: [NG][BM] row maxima
-    float* lse_s = stage + NG * BM;         //             [NG][BM] row sums of exp
+    constexpr int HALVES = NUM_EPI_WARPS / 4;   // warps per TMEM lane quadrant
+    constexpr int GPW = BN / kCols / HALVES;    // 64-column groups per thread
+    static_assert(GPW >= 1 && GPW * kCols * HALVES == BN, "tile width not covered by the epilogue warps");
+    const int ew = warp - 2;                    // 0..7
+    const int quad = warp & 3;                  // TMEM lanes this warp may read
+    const int half = ew >> 2;                   // which half of the tile's columns
+    const int r = quad * 32 + lane;             // tile row of this thread
+    float* lse_m = stage;                       // EPI_LOGITS: [HALVES][BM] row maxima
+    float* lse_s = stage + HALVES * BM;         //             [HALVES][BM] row sums of exp
+    const long long tiles = (long long)g.batch * mtiles * ntiles;
     int i = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
       const Unit w = decode_unit(u, mtiles, ntiles, g.batch, BN);
       const int ab = i & 1, use = i >> 1;
       if (!epi_all(mbar_wait(&accf[ab], use & 1, err, 32))) break;
       tc_fence_after();
-      float v[kCols];
-      {
-        const uint32_t ta = tmem + (uint32_t)(ab * BN + cg * kCols) + ((uint32_t)(quad * 32) << 16);
-        float (&v0)[32] = *reinterpret_cast<float(*)[32]>(v);
-        float (&v1)[32] = *reinterpret_cast<float(*)[32]>(v + 32);
-        tmem_ld32(ta, v0);
-        tmem_ld32(ta + 32, v1);
-      }
-      // every TMEM read of this accumulator is done: hand it back to the MMA warp
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[ab]);
-
       const int row = w.m0 + r;
-      const int n = w.n0 + cg * kCols;
-      const bool full_vec = g.vec && n + kCols <= g.N;
+      const long long tix = ((long long)w.bz * mtiles + w.mt) * ntiles + w.nt;
       float sq = 0.0f;
-      if (splitk > 1) {
-        // fp32 partial tile of this K range in the workspace, column-major inside
-        // the tile (column c holds the tile's BM rows), so that for every column
-        // a warp's 32 rows are one 128-byte line
-        const long long tiles = (long long)g.batch * mtiles * ntiles;
-        const long long tix = ((long long)w.bz * mtiles + w.mt) * ntiles + w.nt;
-        float* dst = g.ws + ((long long)w.ks * tiles + tix) * (BM * BN) + (long long)(cg * kCols) * BM + r;
+      float rmax = -FLT_MAX, rsum = 0.0f;       // EPI_LOGITS: this row over this thread's columns
+#pragma unroll 1
+      for (int gi = 0; gi < GPW; ++gi) {
+        const int c = half * GPW + gi;          // column group of the tile
+        float v[kCols];
+        {
+          const uint32_t ta = tmem + (uint32_t)(ab * BN + c * kCols) + ((uint32_t)(quad * 32) << 16);
+          float (&v0)[32] = *reinterpret_cast<float(*)[32]>(v);
+          float (&v1)[32] = *reinterpret_cast<float(*)[32]>(v + 32);
+          tmem_ld32(ta, v0);
+          tmem_ld32(ta + 32, v1);
+        }
+        if (gi == GPW - 1) {
+          // every TMEM read of this accumulator is done: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[ab]);
+        }
+        const int n = w.n0 + c * kCols;
+        const bool full_vec = g.vec && n + kCols <= g.N;
+        const bool wide = g.vec == 2 && n + kCols <= g.N;
+        if (splitk > 1) {
+          // fp32 partial tile of this K range in the workspace, column-major inside
+          // the tile (column j holds the tile's BM rows), so that for every column
+          // a warp's 32 rows are one 128-byte line
+          float* dst = g.ws + ((long long)w.ks * tiles + tix) * (BM * BN) + (long long)(c * kCols) * BM + r;
 #pragma unroll
-        for (int j = 0; j < kCols; ++j) dst[j * BM] = v[j];
-        // Publish it; the CTA completing the tile's last partial reduces them.
-        // The barrier orders every epilogue thread's partial stores before one
-        // thread's GPU-scope release fence and arrival (fences are cumulative);
-        // the last arrival's acquire fence and the barrier after it order the
-        // other CTAs' partials before this CTA's loads.
+          for (int j = 0; j < kCols; ++j) dst[j * BM] = v[j];
+        } else if constexpr (EK == EPI_LOGITS) {
+          // bf16 logits out (when kept); online-softmax state of these values,
+          // folded into the row's running state; the target's fp32 logit
+          float mx = -FLT_MAX;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)
+            if (n + j < g.N) mx = fmaxf(mx, v[j]);
+          float se = 0.0f;
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)
+            if (n + j < g.N) se += __expf(v[j] - mx);
+          if (mx > -FLT_MAX) {
+            const float mm = fmaxf(rmax, mx);
+            rsum = (rmax > -FLT_MAX ? rsum * __expf(rmax - mm) : 0.0f) + se * __expf(mx - mm);
+            rmax = mm;
+          }
+          if (row < g.M) {
+            if (g.out) {
+              if (wide) {
+#pragma unroll
+                for (int j = 0; j < kCols; j += 16)
+                  HexIO<bf16>::store(g.out, 0, (long long)row * g.ldo + n + j, v + j);
+              } else if (full_vec) {
+#pragma unroll
+                for (int j = 0; j < kCols; j += 8)
+                  OctIO<bf16>::store(g.out, 0, (long long)row * g.ldo + n + j, v + j);
+              } else {
+                bf16* dst = static_cast<bf16*>(g.out) + (long long)row * g.ldo + n;
+#pragma unroll
+                for (int j = 0; j < kCols; ++j)
+                  if (n + j < g.N) dst[j] = __float2bfloat16_rn(v[j]);
+              }
+            }
+            const int t = g.tgt[row] - n;
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)
+              if (t == j && n + j < g.N) g.tlogit[row] = v[j];
+          }
+        } else if (row < g.M) {
+          if (wide) {
+#pragma unroll
+            for (int j = 0; j < kCols; j += 16) sq += epi_hex<S, EK>(g, w.bz, row, n + j, v + j);
+          } else if (full_vec) {
+#pragma unroll
+            for (int j = 0; j < kCols; j += 8) sq += epi_oct<S, EK>(g, w.bz, row, n + j, v + j);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)
+              if (n + j < g.N) sq += epi_value<S>(g, w.bz, row, n + j, v[j]);
+          }
+        }
+      }
+      if (splitk > 1) {
+        // Publish the partial; the CTA completing the tile's last partial reduces
+        // them.  The barrier orders every epilogue thread's partial stores before
+        // one thread's GPU-scope release fence and arrival (fences are
+        // cumulative); the last arrival's acquire fence and the barrier after it
+        // order the other CTAs' partials before this CTA's loads.
         epi_bar();
         if (ew == 0 && lane == 0) {
-          const int tile = (w.bz * mtiles + w.mt) * ntiles + w.nt;
           asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          const int last = atomicAdd(&g.cnt[tile], 1) == splitk - 1;
+          const int last = atomicAdd(&g.cnt[tix], 1) == splitk - 1;
           if (last) {
-            g.cnt[tile] = 0;  // ready for the next split-K GEMM in stream order
+            g.cnt[tix] = 0;  // ready for the next split-K GEMM in stream order
             asm volatile("fence.acq_rel.gpu;" ::: "memory");
           }
           tmem_slot[1] = (uint32_t)last;
@@ -414,59 +473,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         epi_bar();
         if (tmem_slot[1] && row < g.M) {
           // sum the partials in split order; one split's loads are all in flight at once
-          const float* src = g.ws + tix * (BM * BN) + (long long)(cg * kCols) * BM + r;
-#pragma unroll
-          for (int j = 0; j < kCols; ++j) v[j] = 0.0f;
 #pragma unroll 1
-          for (int q = 0; q < splitk; ++q) {
-            const float* sl = src + q * tiles * (BM * BN);
+          for (int gi = 0; gi < GPW; ++gi) {
+            const int c = half * GPW + gi;
+            const int n = w.n0 + c * kCols;
+            const float* src = g.ws + tix * (BM * BN) + (long long)(c * kCols) * BM + r;
+            float v[kCols];
 #pragma unroll
-            for (int j = 0; j < kCols; ++j) v[j] += __ldcg(sl + j * BM);
-          }
-          if (full_vec) {
+            for (int j = 0; j < kCols; ++j) v[j] = 0.0f;
+#pragma unroll 1
+            for (int q = 0; q < splitk; ++q) {
+              const float* sl = src + q * tiles * (BM * BN);
 #pragma unroll
-            for (int j = 0; j < kCols; j += 8) epi_oct<S, EK>(g, w.bz, row, n + j, v + j);
-          } else {
+              for (int j = 0; j < kCols; ++j) v[j] += __ldcg(sl + j * BM);
+            }
+            if (g.vec == 2 && n + kCols <= g.N) {
 #pragma unroll
-            for (int j = 0; j < kCols; ++j)
-              if (n + j < g.N) epi_value<S>(g, w.bz, row, n + j, v[j]);
-          }
-        }
-      } else if constexpr (EK == EPI_LOGITS) {
-        // bf16 logits out (when kept); online-softmax state of this thread's 32
-        // values, combined over the row's column groups; the target's fp32 logit
-        float mx = -FLT_MAX;
+              for (int j = 0; j < kCols; j += 16) epi_hex<S, EK>(g, w.bz, row, n + j, v + j);
+            } else if (g.vec && n + kCols <= g.N) {
 #pragma unroll
-        for (int j = 0; j < kCols; ++j)
-          if (n + j < g.N) mx = fmaxf(mx, v[j]);
-        float se = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kCols; ++j)
-          if (n + j < g.N) se += __expf(v[j] - mx);
-        if (row < g.M) {
-          if (g.out) {
-            if (full_vec) {
-#pragma unroll
-              for (int j = 0; j < kCols; j += 8) OctIO<bf16>::store(g.out, 0, (long long)row * g.ldo + n + j, v + j);
+              for (int j = 0; j < kCols; j += 8) epi_oct<S, EK>(g, w.bz, row, n + j, v + j);
             } else {
-              bf16* dst = static_cast<bf16*>(g.out) + (long long)row * g.ldo + n;
 #pragma unroll
               for (int j = 0; j < kCols; ++j)
-                if (n + j < g.N) dst[j] = __float2bfloat16_rn(v[j]);
+                if (n + j < g.N) epi_value<S>(g, w.bz, row, n + j, v[j]);
             }
           }
-          const int t = g.tgt[row] - n;
-#pragma unroll
-          for (int j = 0; j < kCols; ++j)
-            if (t == j && n + j < g.N) g.tlogit[row] = v[j];
         }
-        lse_m[cg * BM + r] = mx;
-        lse_s[cg * BM + r] = se;
         epi_bar();
-        if (cg == 0 && row < g.M) {
+      }
+      if constexpr (EK == EPI_LOGITS) {
+        // combine the row's state over the tile's column halves
+        lse_m[half * BM + r] = rmax;
+        lse_s[half * BM + r] = rsum;
+        epi_bar();
+        if (half == 0 && row < g.M) {
           float m0 = -FLT_MAX, s0 = 0.0f;
 #pragma unroll
-          for (int c = 0; c < NG; ++c) {
+          for (int c = 0; c < HALVES; ++c) {
             const float m2 = lse_m[c * BM + r], s2 = lse_s[c * BM + r];
             if (m2 > -FLT_MAX) {
               const float mm = fmaxf(m0, m2);
@@ -477,15 +521,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           g.lse_part[(long long)row * g.lse_ld + w.nt] = make_float2(m0, s0);
         }
         epi_bar();
-      } else if (row < g.M) {
-        if (full_vec) {
-#pragma unroll
-          for (int j = 0; j < kCols; j += 8) sq += epi_oct<S, EK>(g, w.bz, row, n + j, v + j);
-        } else {
-#pragma unroll
-          for (int j = 0; j < kCols; ++j)
-            if (n + j < g.N) sq += epi_value<S>(g, w.bz, row, n + j, v[j]);
-        }
       }
       if (EK == EPI_DW || (EK == EK_ANY && g.epi == EPI_DW)) {
         sq = warp_sum(sq);
@@ -512,22 +547,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 extern int g_num_sms;
 
 // Launch one instantiation (persistent grid, one CTA per SM at most).
-template <bool A_MN, bool B_MN, bool SPLIT, int EK>
-ttt_status launch_kernel(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
-  using L = Smem<kBN, SPLIT>;
-  auto kern = gemm_tc_kernel<kBN, A_MN, B_MN, SPLIT, EK>;
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, int EK>
+ttt_status launch_bn(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
+  using L = Smem<BN, SPLIT>;
+  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, SPLIT, EK>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
     attr_set = true;
   }
-  const int mtiles = ceil_div(g.M, BM), ntiles = ceil_div(g.N, kBN);
+  const int mtiles = ceil_div(g.M, BM), ntiles = ceil_div(g.N, BN);
   const long long units = (long long)mtiles * ntiles * g.batch * splitk;
   const int grid = (int)(units < g_num_sms ? units : g_num_sms);
   kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], g, nkb, splitk, mtiles, ntiles, g.err);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
+}
+
+// bf16 GEMMs with many output tiles use 128 x 256 tiles (g.bn == 256): a third
+// less shared-memory operand traffic per FLOP than 128 x 128.  bf16x3 products
+// keep 128 x 128 (their ring stages are twice as large).
+template <bool A_MN, bool B_MN, bool SPLIT, int EK>
+ttt_status launch_kernel(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
+  if constexpr (!SPLIT) {
+    if (g.bn == 256) return launch_bn<256, A_MN, B_MN, false, EK>(g, maps, nkb, splitk, st);
+  }
+  return launch_bn<kBN, A_MN, B_MN, SPLIT, EK>(g, maps, nkb, splitk, st);
 }
 
 // Per operand-major combination: picks the instantiation for (storage, epilogue).

@@ -13,7 +13,9 @@ import oracle
 import synth
 from synth import configs as C
 
-from gpu_harness import compare, compare_settlement, make, run_gpu, run_oracle
+from gpu_harness import TOL, compare, compare_settlement, make, run_gpu, run_oracle
+
+TOL_BF16_LOSS_MEAN = TOL["bf16"]["loss_mean"]
 
 pytestmark = pytest.mark.gpu
 
@@ -102,6 +104,56 @@ def test_settlement_bf16_small_widths():
     assert decided >= 6
     assert ref["accept"].any() and (~ref["accept"]).any()
     compare(wl, gpu, ref)
+
+
+def test_hoisted_prefix_groups_bf16(monkeypatch):
+    """The frozen prefix runs once per group of chunks; groups of 2 over 5
+    chunks (2 + 2 + 1) give the same result as the oracle's chunk-by-chunk loop."""
+    monkeypatch.setenv("TTT_HOIST_CHUNKS", "2")
+    wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1024, chunk=128, B=3, T=5 * 128, n_prefix=2)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_hoisted_swiglu_activation_groups_ragged_tail(monkeypatch):
+    """SwiGLU block whose frozen gate/up activation is hoisted with the prefix:
+    groups of 2 over 5 chunks, then a ragged tail scored by the per-call path."""
+    monkeypatch.setenv("TTT_HOIST_CHUNKS", "2")
+    wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=64, B=2, T=5 * 64 + 9, n_prefix=1)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
+def test_decode_swiglu_bf16_steps_with_the_per_call_prefix():
+    """Decoding runs its chunk steps without the hoisted prefix (one token at a
+    time): SwiGLU bf16 decode losses and final weights against the oracle."""
+    wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=64, B=2, T=64 + 10, n_prefix=1)
+    inp = make(wl)
+    extra = 64
+    long_tok = synth.sample_stream(inp["chain"], wl.seed_id, wl.B, wl.T + extra)
+    tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
+    gpu = run_gpu(wl, inp, tokens=tok)
+    h = gpu["handle"]
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
+    errs = []
+    for t in range(wl.T + 1, wl.T + extra + 1):
+        h.decode_step(torch.from_numpy(long_tok[:, t].copy()).cuda(), p, loss)
+        torch.cuda.synchronize()
+        for s in range(wl.B):
+            l_ref, p_ref = oracle.decode_step(net, ref["states"][s], long_tok[s, t], wl.eta, wl.clip, wl.chunk)
+            errs.append(abs(float(loss[s]) - l_ref))
+            assert np.abs(p[s].cpu().numpy() - p_ref).sum() <= 5e-2
+    assert np.mean(errs) <= TOL_BF16_LOSS_MEAN
+    for s in range(wl.B):
+        rel = oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats)
+        assert rel <= 3e-2
 
 
 def test_host_and_device_buffers_agree():
