@@ -40,6 +40,38 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0}
 
 
+def source_hash():
+    """SHA-256 over the CUDA sources and headers of libttt (kernel identity for
+    counters taken by a profiler)."""
+    import glob
+    import hashlib
+    hsh = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "chunked_next_token_ttt_b300", "csrc", "*")) +
+                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        hsh.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            hsh.update(fh.read())
+    return hsh.hexdigest()[:16]
+
+
+def profiled_traffic(workload, kernel_class):
+    """DRAM bytes per launch of a kernel class from the committed ncu summary of
+    this workload (profiles/launches_<workload>.md), or None when there is none
+    or the kernels changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"launches_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    meta = {}
+    for line in open(path):
+        if line.startswith("<!-- traffic "):
+            meta = json.loads(line[len("<!-- traffic "):].rsplit("-->", 1)[0])
+    if meta.get("source_hash") != source_hash():
+        return None
+    v = meta.get("dram_bytes_per_launch", {}).get(kernel_class)
+    return float(v) if v is not None else None
+
+
 def peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
@@ -235,8 +267,14 @@ def run_ours(args, wl, rank, world, local_rank):
     def step():
         h.prefill(tok, losses, p, q, acc if n_ev else None, A if n_ev else None)
 
-    for _ in range(args.warmup):
+    for w in range(args.warmup):
+        if w == 0 and args.launch_log:
+            h.launch_log_enable(True)
         step()
+        if w == 0 and args.launch_log:
+            with open(args.launch_log, "w") as f:
+                f.write("\n".join(h.launch_log()) + "\n")
+            h.launch_log_enable(False)
     torch.cuda.synchronize(dev)
 
     # which kernel class dominates: one untimed profiled prefill per class
@@ -341,7 +379,9 @@ def run_ours(args, wl, rank, world, local_rank):
                 "peak_source": f"{pk['source']} copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = dom
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic(wl.name, dom)
+    roof["traffic_source"] = (f"profiles/launches_{wl.name}.md (ncu dram__bytes_read.sum + dram__bytes_write.sum "
+                              f"per launch); null when the kernels changed since")
     roof["launches_per_step"] = launches_per_step_dom
     roof["avg_launch_ms"] = dom_avg_s * 1e3
     t_roof, fl_chunk, by_chunk = chunk_roofline_seconds(wl, pk)
@@ -381,6 +421,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=C.CHUNKED_FP32.name, choices=list(C.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch-log", default=None,
+                    help="write the kernel class of every launch of the first prefill to this file")
     ap.add_argument("--T", type=int, default=None,
                     help="tokens per sequence instead of the workload's (small cases for profiler captures)")
     args = ap.parse_args()

@@ -76,6 +76,8 @@ static ttt_status run(ttt_handle* h, int cls, cudaStream_t st, int nkernels, F&&
     h->prof_launches += 1;
   }
   h->launches += nkernels;
+  if (h->log_on)
+    for (int k = 0; k < nkernels; ++k) h->launch_log.push_back((int8_t)cls);
   return TTT_OK;
 }
 
@@ -964,6 +966,20 @@ ttt_status ttt_profile_read(ttt_handle* h, int* launches, double* total_ms) {
   h->ev_used = 0;
   h->prof_launches = 0;
   return TTT_OK;
+}
+
+ttt_status ttt_launch_log_enable(ttt_handle* h, int on) {
+  if (!h) return fail(TTT_ERR_BAD_ARG, "null handle");
+  h->log_on = on != 0;
+  h->launch_log.clear();
+  return TTT_OK;
+}
+
+int ttt_launch_log_read(ttt_handle* h, int8_t* out, int cap) {
+  if (!h) return -1;
+  const int n = (int)h->launch_log.size();
+  for (int i = 0; i < n && i < cap && out; ++i) out[i] = h->launch_log[(size_t)i];
+  return n;
 }
 
 ttt_status ttt_last_launch_count(ttt_handle* h, long long* launches) {

@@ -110,6 +110,8 @@ struct ttt_handle {
   std::vector<cudaEvent_t> ev;
   int ev_used = 0;
   int prof_launches = 0;
+  bool log_on = false;
+  std::vector<int8_t> launch_log;   // kernel class of every launch, in order
 
   std::vector<void*> allocs;
 };

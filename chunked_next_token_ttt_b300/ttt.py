@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ttt_kernel_class_name": ([_I], ctypes.c_char_p),
         "ttt_kernel_class_count": ([], _I),
         "ttt_last_launch_count": ([_P, ctypes.POINTER(ctypes.c_longlong)], _I),
+        "ttt_launch_log_enable": ([_P, _I], _I),
+        "ttt_launch_log_read": ([_P, ctypes.POINTER(ctypes.c_int8), _I], _I),
         "ttt_status_string": ([_I], ctypes.c_char_p),
         "ttt_last_error": ([], ctypes.c_char_p),
     }
@@ -241,6 +243,17 @@ class Handle:
         n = ctypes.c_longlong()
         _check(self.lib.ttt_last_launch_count(self._h, ctypes.byref(n)), "ttt_last_launch_count")
         return n.value
+
+    def launch_log_enable(self, on: bool = True):
+        _check(self.lib.ttt_launch_log_enable(self._h, int(on)), "ttt_launch_log_enable")
+
+    def launch_log(self) -> list:
+        """Kernel class names of the logged launches, in launch order."""
+        n = self.lib.ttt_launch_log_read(self._h, None, 0)
+        buf = (ctypes.c_int8 * max(n, 1))()
+        self.lib.ttt_launch_log_read(self._h, buf, n)
+        names = kernel_classes()
+        return [names[buf[i]] for i in range(n)]
 
 
 # ---------------------------------------------------------------- single operations

@@ -197,6 +197,15 @@ int ttt_kernel_class_count(void);
 /* Number of kernels the last ttt_prefill launched on the GPU. */
 ttt_status ttt_last_launch_count(ttt_handle* h, long long* launches);
 
+/* Launch-class log, for matching a profiler's launch list to kernel classes.
+ * While enabled (on != 0; enabling clears it), every kernel the handle
+ * launches appends its class (ttt_kernel_class_name) in launch order, one
+ * entry per kernel, on the host.  ttt_launch_log_read copies up to cap entries
+ * into out (host memory) and returns the number of entries logged (which may
+ * exceed cap), or -1 for a null handle. */
+ttt_status ttt_launch_log_enable(ttt_handle* h, int on);
+int ttt_launch_log_read(ttt_handle* h, int8_t* out, int cap);
+
 /* Static text for a status code, and the last error message of this thread. */
 const char* ttt_status_string(ttt_status s);
 const char* ttt_last_error(void);
