@@ -15,6 +15,8 @@ constexpr int kThreads = 256;
 
 __global__ void sumsq_partials_kernel(long long n, int pieces, const float* __restrict__ dW,
                                       float* __restrict__ partials) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   const int piece = blockIdx.x, slot = blockIdx.y, s = blockIdx.z;
   const int nslots = gridDim.y, B = gridDim.z;
@@ -30,6 +32,8 @@ __global__ void sumsq_partials_kernel(long long n, int pieces, const float* __re
 __global__ void clip_finalize_kernel(int B, int per_seq, const float* __restrict__ partials, float clip,
                                      float* __restrict__ scale, float* __restrict__ norm_out,
                                      float* __restrict__ scale_out, int* __restrict__ flag) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   int bad = 0;
   for (int s = 0; s < B; ++s) {
@@ -68,9 +72,9 @@ ttt_status launch_clip_sgd(int dtype, int nslots, int B, long long n, float* W32
   float* partials = scratch;
   float* scale = scratch + (size_t)nslots * B * pieces;
   int* flag = reinterpret_cast<int*>(scale + B);
-  sumsq_partials_kernel<<<dim3(pieces, nslots, B), kThreads, 0, st>>>(n, pieces, dW, partials);
+  launch_pdl(sumsq_partials_kernel, dim3(pieces, nslots, B), kThreads, 0, st, n, pieces, dW, partials);
   TTT_CHECK_LAUNCH();
-  clip_finalize_kernel<<<1, kThreads, 0, st>>>(B, nslots * pieces, partials, clip, scale, norm_out, scale_out,
+  launch_pdl(clip_finalize_kernel, 1, kThreads, 0, st, B, nslots * pieces, partials, clip, scale, norm_out, scale_out,
                                                flag);
   TTT_CHECK_LAUNCH();
   return launch_sgd_update(dtype, nslots, B, n, W32, Wop, 0, dW, scale, eta, st);

@@ -20,6 +20,14 @@ static thread_local std::string g_last_error;
 
 void set_error(const std::string& msg) { g_last_error = msg; }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("TTT_PDL");
+    return !(e && std::string(e) == "0");
+  }();
+  return on;
+}
+
 ttt_status cuda_fail(cudaError_t e, const char* what, const char* file, int line) {
   char buf[512];
   snprintf(buf, sizeof buf, "%s: %s (%s:%d)", what, cudaGetErrorString(e), file, line);
@@ -266,7 +274,7 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
   GemmDesc gl = gh;
   gl.dtype = stg;
   gl.epi = EPI_LOGITS; gl.out = train ? h->logits : nullptr; gl.ldo = V;
-  gl.lse_part = h->lse_part; gl.lse_ld = h->lse_ld; gl.tgt = h->tgt; gl.tlogit = h->tlogit;
+  gl.lse_part = h->lse_part; gl.lse_ld = h->lse_ld;
   const bool fused = !head_f32 && stg == ST_BF16 && V % 8 == 0 && gemm_tc_supported(gl);
 
   TTT_TRY(run(h, K_RMSNORM_FWD, st, 1, [&] {
@@ -279,8 +287,8 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
     TTT_TRY(rungemm(h, K_GEMM_HEAD, gl, st));
     const int nt = ceil_div(V, gemm_tc_tile_n(gl));
     TTT_TRY(run(h, K_CE, st, 1, [&] {
-      return launch_lse_combine(B, tv, h->lse_part, h->lse_ld, nt, h->tlogit, h->lse, losses, loss_ld, loss_off,
-                                h->row_loss, st);
+      return launch_lse_combine(B, tv, h->lse_part, h->lse_ld, nt, h->y.p, h->U.p, d, h->tgt, h->lse, losses,
+                                loss_ld, loss_off, h->row_loss, st);
     }));
     if (!train) return TTT_OK;
     return run(h, K_CE, st, 1, [&] { return launch_dlogits(M, V, h->logits, h->lse, h->tgt, scale, st); });
@@ -692,7 +700,6 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   h->lse_ld = ceil_div(V, 128);  // the narrowest tensor-core tile
   if ((s = dalloc(h, &h->lse_part, Mm * (size_t)h->lse_ld * sizeof(float2))) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->lse, Mm * 4)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->tlogit, Mm * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->tgt, Mm * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dy32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dh32, Mm * d * 4)) != TTT_OK) return bail(s);

@@ -70,7 +70,6 @@ struct ttt_handle {
   float2* lse_part = nullptr;        // [Mmax][lse_ld] head-tile softmax states
   long long lse_ld = 0;
   float* lse = nullptr;              // [Mmax]
-  float* tlogit = nullptr;           // [Mmax] fp32 target logits
   int32_t* tgt = nullptr;            // [Mmax] target token per row, -1 = none
   float* dy32 = nullptr;
   float* dh32 = nullptr;

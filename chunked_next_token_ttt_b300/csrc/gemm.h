@@ -16,7 +16,7 @@ enum EpiKind {
   EPI_DW,          // out(float) = acc; partials += per-tile sum of acc^2
   EPI_LOGITS,      // tensor-core path only, batch 1: out(bf16) = acc when out is
                    // non-null; lse_part[m][tile] = (max, sum exp(acc - max)) over the
-                   // tile's columns; tlogit[m] = acc at column tgt[m] (tgt[m] < 0: none)
+                   // tile's columns
 };
 
 struct GemmDesc {
@@ -35,8 +35,6 @@ struct GemmDesc {
   long long loA = 0, loB = 0, loO = 0, loO2 = 0, loX = 0;
   float2* lse_part = nullptr;      // EPI_LOGITS: [M][lse_ld] online-softmax states
   long long lse_ld = 0;
-  const int32_t* tgt = nullptr;    // EPI_LOGITS: [M] target column per row, -1 = none
-  float* tlogit = nullptr;         // EPI_LOGITS: [M] fp32 logit of the target
   int* err = nullptr;              // device status word for bounded-wait timeouts
   int impl = 0;                    // 0 auto, 1 SIMT, 2 tensor cores
   // optional fp32 workspace; the tensor-core path uses it to split K when a

@@ -14,6 +14,8 @@ constexpr int TM = 64, TN = 64, TK = 16;
 
 template <typename S, bool AK, bool BK>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmDesc g) {
+  pdl_wait();
+  pdl_launch();
   using IO = OpIO<S>;
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
@@ -83,10 +85,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmDesc g) {
 
 template <typename S>
 void launch(const GemmDesc& g, dim3 grid, cudaStream_t st) {
-  if (g.a_kmajor && g.b_kmajor) gemm_simt_kernel<S, true, true><<<grid, 256, 0, st>>>(g);
-  else if (g.a_kmajor) gemm_simt_kernel<S, true, false><<<grid, 256, 0, st>>>(g);
-  else if (g.b_kmajor) gemm_simt_kernel<S, false, true><<<grid, 256, 0, st>>>(g);
-  else gemm_simt_kernel<S, false, false><<<grid, 256, 0, st>>>(g);
+  if (g.a_kmajor && g.b_kmajor) launch_pdl(gemm_simt_kernel<S, true, true>, grid, 256, 0, st, g);
+  else if (g.a_kmajor) launch_pdl(gemm_simt_kernel<S, true, false>, grid, 256, 0, st, g);
+  else if (g.b_kmajor) launch_pdl(gemm_simt_kernel<S, false, true>, grid, 256, 0, st, g);
+  else launch_pdl(gemm_simt_kernel<S, false, false>, grid, 256, 0, st, g);
 }
 
 }  // namespace

@@ -18,6 +18,8 @@ constexpr int kMaxRows = 8;
 
 template <typename S>
 __global__ void __launch_bounds__(256) gemm_small_kmajor_kernel(GemmDesc g) {
+  pdl_wait();
+  pdl_launch();
   using IO = OpIO<S>;
   __shared__ float red[8][kMaxRows];
   const int bz = blockIdx.y;
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(256) gemm_small_kmajor_kernel(GemmDesc g) {
 
 template <typename S>
 __global__ void __launch_bounds__(256) gemm_small_nmajor_kernel(GemmDesc g) {
+  pdl_wait();
+  pdl_launch();
   using IO = OpIO<S>;
   __shared__ float red[32];
   const int bz = blockIdx.y;
@@ -96,9 +100,9 @@ ttt_status gemm_small(const GemmDesc& g, cudaStream_t st) {
   dim3 grid(small_grid_x(g), g.batch);
 #define TTT_SMALL(KERNEL)                                                                  \
   do {                                                                                     \
-    if (g.dtype == ST_BF16) KERNEL<bf16><<<grid, 256, 0, st>>>(g);                         \
-    else if (g.dtype == ST_SPLIT) KERNEL<Split><<<grid, 256, 0, st>>>(g);                  \
-    else KERNEL<float><<<grid, 256, 0, st>>>(g);                                           \
+    if (g.dtype == ST_BF16) launch_pdl(KERNEL<bf16>, grid, 256, 0, st, g);                         \
+    else if (g.dtype == ST_SPLIT) launch_pdl(KERNEL<Split>, grid, 256, 0, st, g);                  \
+    else launch_pdl(KERNEL<float>, grid, 256, 0, st, g);                                           \
   } while (0)
   if (g.b_kmajor) TTT_SMALL(gemm_small_kmajor_kernel);
   else TTT_SMALL(gemm_small_nmajor_kernel);

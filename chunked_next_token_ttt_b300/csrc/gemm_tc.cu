@@ -72,7 +72,7 @@ bool gemm_tc_supported(const GemmDesc& g) {
   if (g.batch > 1 && (g.sA % 8 || g.sB % 8 || g.sA <= 0 || g.sB <= 0)) return false;
   if (g.epi == EPI_DW && !g.partials) return false;
   if (g.epi == EPI_LOGITS &&
-      (g.dtype != ST_BF16 || g.batch != 1 || !g.a_kmajor || !g.b_kmajor || !g.lse_part || !g.tgt || !g.tlogit ||
+      (g.dtype != ST_BF16 || g.batch != 1 || !g.a_kmajor || !g.b_kmajor || !g.lse_part ||
        g.lse_ld < ceil_div(g.N, choose_bn(g))))
     return false;
   // the epilogue stores column pairs: even leading dims, batch strides and lo offsets

@@ -212,14 +212,22 @@ struct Smem {
   static_assert(ALLOC <= MAX_DYN, "shared memory over the per-block limit");
 };
 
-// Work unit u: n-tile fastest, then m-tile, then batch entry, then K split.
+// Work unit u: the output dimension with fewer tiles fastest (so the CTAs that
+// run at the same time share the larger operand's tiles through L2: an LM head
+// with a few row tiles streams each vocabulary tile of U from DRAM once), then
+// the other, then batch entry, then K split.
 struct Unit {
   int m0, n0, bz, ks, mt, nt;
 };
 __device__ __forceinline__ Unit decode_unit(int u, int mtiles, int ntiles, int batch, int BN) {
   Unit w;
-  w.nt = u % ntiles;
-  w.mt = (u / ntiles) % mtiles;
+  if (mtiles < ntiles) {
+    w.mt = u % mtiles;
+    w.nt = (u / mtiles) % ntiles;
+  } else {
+    w.nt = u % ntiles;
+    w.mt = (u / ntiles) % mtiles;
+  }
   const int z = u / (ntiles * mtiles);
   w.bz = z % batch;
   w.ks = z / batch;
@@ -271,6 +279,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above touches only this CTA's shared memory and TMEM; global
+  // memory (operands, outputs, counters) waits for the previous kernel
+  pdl_wait();
+  pdl_launch();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ TMA producer
@@ -404,15 +416,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < kCols; ++j) dst[j * BM] = v[j];
         } else if constexpr (EK == EPI_LOGITS) {
           // bf16 logits out (when kept); online-softmax state of these values,
-          // folded into the row's running state; the target's fp32 logit
-          float mx = -FLT_MAX;
+          // folded into the row's running state
+          float mx = -FLT_MAX, se = 0.0f;
+          if (n + kCols <= g.N) {
 #pragma unroll
-          for (int j = 0; j < kCols; ++j)
-            if (n + j < g.N) mx = fmaxf(mx, v[j]);
-          float se = 0.0f;
+            for (int j = 0; j < kCols; ++j) mx = fmaxf(mx, v[j]);
 #pragma unroll
-          for (int j = 0; j < kCols; ++j)
-            if (n + j < g.N) se += __expf(v[j] - mx);
+            for (int j = 0; j < kCols; ++j) se += __expf(v[j] - mx);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)
+              if (n + j < g.N) mx = fmaxf(mx, v[j]);
+#pragma unroll
+            for (int j = 0; j < kCols; ++j)
+              if (n + j < g.N) se += __expf(v[j] - mx);
+          }
           if (mx > -FLT_MAX) {
             const float mm = fmaxf(rmax, mx);
             rsum = (rmax > -FLT_MAX ? rsum * __expf(rmax - mm) : 0.0f) + se * __expf(mx - mm);
@@ -435,10 +453,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   if (n + j < g.N) dst[j] = __float2bfloat16_rn(v[j]);
               }
             }
-            const int t = g.tgt[row] - n;
-#pragma unroll
-            for (int j = 0; j < kCols; ++j)
-              if (t == j && n + j < g.N) g.tlogit[row] = v[j];
           }
         } else if (row < g.M) {
           if (wide) {
@@ -560,7 +574,7 @@ ttt_status launch_bn(const GemmDesc& g, const CUtensorMap* maps, int nkb, int sp
   const int mtiles = ceil_div(g.M, BM), ntiles = ceil_div(g.N, BN);
   const long long units = (long long)mtiles * ntiles * g.batch * splitk;
   const int grid = (int)(units < g_num_sms ? units : g_num_sms);
-  kern<<<grid, NUM_THREADS, L::ALLOC, st>>>(maps[0], maps[1], maps[2], maps[3], g, nkb, splitk, mtiles, ntiles, g.err);
+  launch_pdl(kern, grid, NUM_THREADS, L::ALLOC, st, maps[0], maps[1], maps[2], maps[3], g, nkb, splitk, mtiles, ntiles, g.err);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

@@ -12,6 +12,8 @@ namespace {
 template <typename ET, typename S>
 __global__ void embed_kernel(TokView tv, const ET* __restrict__ E, int d, float* __restrict__ h32, void* hop,
                              long long hop_lo) {
+  pdl_wait();
+  pdl_launch();
   const int m = blockIdx.x;
   const int s = m / tv.rows, j = m % tv.rows;
   int x = tv.tok[s * tv.tok_ld + tv.tok_off + j];
@@ -32,6 +34,8 @@ __device__ __forceinline__ int target_of(const TokView& tv, int s, int j, int V)
 template <typename S>
 __global__ void rmsnorm_fwd_kernel(int d, const float* __restrict__ x, float eps, void* y, long long y_lo,
                                    float* __restrict__ rstd, TokView tv, int32_t* __restrict__ tgt) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   const long long m = blockIdx.x;
   if (tgt && threadIdx.x == 0) {
@@ -52,6 +56,8 @@ template <typename S>
 __global__ void rmsnorm_bwd_kernel(int d, const float* __restrict__ x, const float* __restrict__ rstd,
                                    const float* __restrict__ dy, float* __restrict__ dx32, void* dxop,
                                    long long dx_lo) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   const long long m = blockIdx.x;
   const float r = rstd[m];
@@ -125,6 +131,8 @@ template <typename OpT>
 __global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long ldl, float scale, bool grad,
                           float* __restrict__ losses, long long loss_ld, long long loss_off,
                           float* __restrict__ row_loss) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float sm_m[32], sm_s[32];
   const int m = blockIdx.x;
   const int s = m / tv.rows, j = m % tv.rows;
@@ -159,6 +167,8 @@ constexpr int kCeSplitMaxV = 32768;
 __global__ void ce_split_kernel(TokView tv, int V, float* __restrict__ logits, long long ldl, float scale,
                                 bool grad, float* __restrict__ losses, long long loss_ld, long long loss_off,
                                 float* __restrict__ row_loss) {
+  pdl_wait();
+  pdl_launch();
   extern __shared__ float srow[];
   __shared__ float sm_m[32], sm_s[32];
   const int m = blockIdx.x;
@@ -196,14 +206,26 @@ __global__ void ce_split_kernel(TokView tv, int V, float* __restrict__ logits, l
 }
 
 // One warp per row: the row's logsumexp from the per-column-tile online
-// softmax states the head GEMM left, then the loss lse - logit[target].
+// softmax states the head GEMM left, the target's logit y[m] . U[target] (fp32
+// sum of the same bf16 products the GEMM takes), then the loss lse - logit.
 __global__ void lse_combine_kernel(TokView tv, int M, const float2* __restrict__ part, long long ld, int nt,
-                                   const float* __restrict__ tlogit, float* __restrict__ lse,
+                                   const bf16* __restrict__ y, const bf16* __restrict__ U, int d,
+                                   const int32_t* __restrict__ tgt, float* __restrict__ lse,
                                    float* __restrict__ losses, long long loss_ld, long long loss_off,
                                    float* __restrict__ row_loss) {
+  pdl_wait();
+  pdl_launch();
   const int lane = threadIdx.x & 31;
   const int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (m >= M) return;
+  const int t = tgt[m];
+  float dot = 0.0f;
+  if (t >= 0) {
+    const bf16* yr = y + (long long)m * d;
+    const bf16* ur = U + (long long)t * d;
+    for (int k = lane; k < d; k += 32) dot = fmaf(__bfloat162float(yr[k]), __bfloat162float(ur[k]), dot);
+    dot = warp_sum(dot);
+  }
   float mx = -FLT_MAX, se = 0.0f;
   for (int t = lane; t < nt; t += 32) {
     const float2 p = part[(long long)m * ld + t];
@@ -220,7 +242,7 @@ __global__ void lse_combine_kernel(TokView tv, int M, const float2* __restrict__
     lse[m] = l;
     const int s = m / tv.rows, j = m % tv.rows;
     if (j < tv.n_valid) {
-      const float loss = l - tlogit[m];
+      const float loss = l - dot;
       if (losses) losses[s * loss_ld + loss_off + j] = loss;
       if (row_loss) row_loss[m] = loss;
     }
@@ -228,37 +250,42 @@ __global__ void lse_combine_kernel(TokView tv, int M, const float2* __restrict__
 }
 
 // dlogits = (softmax - onehot(target)) * scale over bf16 logits [M, V] in place,
-// eight elements (16 bytes) per access; rows without a target get 0.
+// eight elements (16 bytes) per access; rows without a target get 0.  Grid:
+// x over the row's 16-byte vectors, y over rows.
 __global__ void dlogits_kernel(int M, int V, bf16* __restrict__ logits, const float* __restrict__ lse,
                                const int32_t* __restrict__ tgt, float scale) {
-  const long long nv = V / 8;
-  const long long total = (long long)M * nv;
-  uint4* base = reinterpret_cast<uint4*>(logits);
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const long long m = i / nv;
-    const int c = (int)(i - m * nv) * 8;
+  pdl_wait();
+  pdl_launch();
+  const int nv = V / 8;
+  for (int m = blockIdx.y; m < M; m += gridDim.y) {
+    uint4* row = reinterpret_cast<uint4*>(logits + (long long)m * V);
     const int t = tgt[m];
-    uint4 raw = base[i];
-    if (t < 0) {
-      base[i] = make_uint4(0u, 0u, 0u, 0u);
-      continue;
-    }
     const float l = lse[m];
-    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
+      if (t < 0) {
+        row[i] = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      uint4 raw = row[i];
+      const int c = i * 8;
+      __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 x = __bfloat1622float2(h2[q]);
-      const float g0 = (__expf(x.x - l) - (c + 2 * q == t ? 1.0f : 0.0f)) * scale;
-      const float g1 = (__expf(x.y - l) - (c + 2 * q + 1 == t ? 1.0f : 0.0f)) * scale;
-      h2[q] = __floats2bfloat162_rn(g0, g1);
+      for (int q = 0; q < 4; ++q) {
+        const float2 x = __bfloat1622float2(h2[q]);
+        float g0 = __expf(x.x - l), g1 = __expf(x.y - l);
+        if (c + 2 * q == t) g0 -= 1.0f;
+        if (c + 2 * q + 1 == t) g1 -= 1.0f;
+        h2[q] = __floats2bfloat162_rn(g0 * scale, g1 * scale);
+      }
+      row[i] = raw;
     }
-    base[i] = raw;
   }
 }
 
 __global__ void norm_finalize_kernel(PartialSlots ps, const float* __restrict__ partials, float clip,
                                      float* __restrict__ scale, float* __restrict__ norm, int* __restrict__ flag) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   const int s = blockIdx.x;
   float acc = 0.0f;
@@ -286,6 +313,8 @@ __global__ void norm_finalize_kernel(PartialSlots ps, const float* __restrict__ 
 template <typename S>
 __global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, void* Wop, long long wop_lo,
                                   const float* __restrict__ dW, const float* __restrict__ scale, float eta) {
+  pdl_wait();
+  pdl_launch();
   const int s = blockIdx.y % B;
   const float sc = scale[s];
   if (sc == 0.0f) return;  // skipped update (non-finite norm): W stays as it is
@@ -318,6 +347,8 @@ __global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, v
 template <typename S>
 __global__ void broadcast_w0_kernel(long long total, int B, long long n, const float* __restrict__ W0,
                                     float* __restrict__ W32, void* Wop, long long wop_lo) {
+  pdl_wait();
+  pdl_launch();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const long long slot = i / (n * B), e = i % n;
@@ -329,12 +360,16 @@ __global__ void broadcast_w0_kernel(long long total, int B, long long n, const f
 
 template <typename S>
 __global__ void cast_kernel(long long n, const float* __restrict__ in, void* out, long long out_lo) {
+  pdl_wait();
+  pdl_launch();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     OpIO<S>::store(out, out_lo, i, in[i]);
 }
 
 __global__ void seq_mean_kernel(int rows, int n_valid, const float* __restrict__ row_loss, float* __restrict__ mean) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   const int s = blockIdx.x;
   float acc = 0.0f;
@@ -345,6 +380,8 @@ __global__ void seq_mean_kernel(int rows, int n_valid, const float* __restrict__
 
 __global__ void settle_decide_kernel(int B, const float* __restrict__ Lc, const float* __restrict__ Lw,
                                      float* __restrict__ A, uint8_t* __restrict__ accept) {
+  pdl_wait();
+  pdl_launch();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= B) return;
   const float a = Lc[s] - Lw[s];
@@ -356,6 +393,8 @@ template <typename S>
 __global__ void settle_apply_kernel(long long total, int B, long long n, const uint8_t* __restrict__ accept,
                                     float* __restrict__ W32, void* Wop, float* __restrict__ Wc32, void* Wcop,
                                     long long lo) {
+  pdl_wait();
+  pdl_launch();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int s = (int)((i / n) % B);
@@ -370,6 +409,8 @@ __global__ void settle_apply_kernel(long long total, int B, long long n, const u
 }
 
 __global__ void softmax_kernel(int V, const float* __restrict__ logits, float* __restrict__ p) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   __shared__ float wm[32];
   const long long m = blockIdx.x;
@@ -390,6 +431,8 @@ __global__ void softmax_kernel(int V, const float* __restrict__ logits, float* _
 }
 
 __global__ void pending_shift_kernel(int B, int b, int32_t* pend) {
+  pdl_wait();
+  pdl_launch();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < B) pend[(long long)s * (b + 1)] = pend[(long long)s * (b + 1) + b];
 }
@@ -405,9 +448,9 @@ int grid_for(long long n, int threads) {
 // Instantiates KERNEL<S> for the storage code and launches it.
 #define LAUNCH_BY_STORAGE(stg, KERNEL, GRID, BLOCK, SMEM, STREAM, ...)                      \
   do {                                                                                      \
-    if ((stg) == ST_BF16) KERNEL<bf16><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);         \
-    else if ((stg) == ST_SPLIT) KERNEL<Split><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);  \
-    else KERNEL<float><<<GRID, BLOCK, SMEM, STREAM>>>(__VA_ARGS__);                         \
+    if ((stg) == ST_BF16) launch_pdl(KERNEL<bf16>, GRID, BLOCK, SMEM, STREAM, __VA_ARGS__);         \
+    else if ((stg) == ST_SPLIT) launch_pdl(KERNEL<Split>, GRID, BLOCK, SMEM, STREAM, __VA_ARGS__);  \
+    else launch_pdl(KERNEL<float>, GRID, BLOCK, SMEM, STREAM, __VA_ARGS__);                         \
   } while (0)
 
 ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d, float* h32, void* hop,
@@ -415,11 +458,11 @@ ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d,
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
   if (stg == ST_BF16)
-    embed_kernel<bf16, bf16><<<M, 256, 0, st>>>(tv, static_cast<const bf16*>(E), d, h32, hop, hop_lo);
+    launch_pdl(embed_kernel<bf16, bf16>, M, 256, 0, st, tv, static_cast<const bf16*>(E), d, h32, hop, hop_lo);
   else if (stg == ST_SPLIT)
-    embed_kernel<float, Split><<<M, 256, 0, st>>>(tv, static_cast<const float*>(E), d, h32, hop, hop_lo);
+    launch_pdl(embed_kernel<float, Split>, M, 256, 0, st, tv, static_cast<const float*>(E), d, h32, hop, hop_lo);
   else
-    embed_kernel<float, float><<<M, 256, 0, st>>>(tv, static_cast<const float*>(E), d, h32, hop, hop_lo);
+    launch_pdl(embed_kernel<float, float>, M, 256, 0, st, tv, static_cast<const float*>(E), d, h32, hop, hop_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -459,26 +502,27 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
       smem_set = smem;
     }
-    ce_split_kernel<<<M, 512, smem, st>>>(tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
+    launch_pdl(ce_split_kernel, M, 512, smem, st, tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
                                           loss_off, row_loss);
   } else if (stg == ST_BF16) {
-    ce_kernel<bf16><<<M, 512, 0, st>>>(tv, V, static_cast<bf16*>(logits), ldl, scale, grad, losses, loss_ld,
+    launch_pdl(ce_kernel<bf16>, M, 512, 0, st, tv, V, static_cast<bf16*>(logits), ldl, scale, grad, losses, loss_ld,
                                        loss_off, row_loss);
   } else {
-    ce_kernel<float><<<M, 512, 0, st>>>(tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
+    launch_pdl(ce_kernel<float>, M, 512, 0, st, tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
                                         loss_off, row_loss);
   }
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
-ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long long ld, int nt,
-                              const float* tlogit, float* lse, float* losses, long long loss_ld, long long loss_off,
-                              float* row_loss, cudaStream_t st) {
+ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long long ld, int nt, const void* y,
+                              const void* U, int d, const int32_t* tgt, float* lse, float* losses, long long loss_ld,
+                              long long loss_off, float* row_loss, cudaStream_t st) {
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
-  lse_combine_kernel<<<ceil_div(M, 8), 256, 0, st>>>(tv, M, part, ld, nt, tlogit, lse, losses, loss_ld, loss_off,
-                                                    row_loss);
+  launch_pdl(lse_combine_kernel, ceil_div(M, 8), 256, 0, st, tv, M, part, ld, nt, static_cast<const bf16*>(y),
+                                                    static_cast<const bf16*>(U), d, tgt, lse, losses, loss_ld,
+                                                    loss_off, row_loss);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -490,15 +534,17 @@ ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const in
     set_error("dlogits: V must be a multiple of 8 and the logits 16-byte aligned");
     return TTT_ERR_UNSUPPORTED;
   }
-  const long long total = (long long)M * (V / 8);
-  dlogits_kernel<<<grid_for(total, 256), 256, 0, st>>>(M, V, static_cast<bf16*>(logits), lse, tgt, scale);
+  // 256-thread blocks each cover 2048 elements of a row; rows fill the rest of the grid
+  const int bx = ceil_div(V / 8, 256);
+  const int by = M < 65535 ? M : 65535;
+  launch_pdl(dlogits_kernel, dim3(bx, by), 256, 0, st, M, V, static_cast<bf16*>(logits), lse, tgt, scale);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
 ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* partials, float clip, float* scale,
                                 float* norm, int* flag, cudaStream_t st) {
-  norm_finalize_kernel<<<B, 256, 0, st>>>(ps, partials, clip, scale, norm, flag);
+  launch_pdl(norm_finalize_kernel, B, 256, 0, st, ps, partials, clip, scale, norm, flag);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -534,7 +580,7 @@ ttt_status launch_cast(int stg, long long n, const float* in, void* out, long lo
 }
 
 ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, float* mean, cudaStream_t st) {
-  seq_mean_kernel<<<B, 256, 0, st>>>(rows, n_valid, row_loss, mean);
+  launch_pdl(seq_mean_kernel, B, 256, 0, st, rows, n_valid, row_loss, mean);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -542,7 +588,7 @@ ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, 
 ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const float* Lc, const float* Lw, float* A,
                                uint8_t* accept, float* W32, void* Wop, float* Wc32, void* Wcop, long long op_lo,
                                cudaStream_t st) {
-  settle_decide_kernel<<<ceil_div(B, 128), 128, 0, st>>>(B, Lc, Lw, A, accept);
+  launch_pdl(settle_decide_kernel, ceil_div(B, 128), 128, 0, st, B, Lc, Lw, A, accept);
   TTT_CHECK_LAUNCH();
   const long long total = (long long)nslots * B * n;
   const int g = grid_for(total, 256);
@@ -553,13 +599,13 @@ ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const fl
 
 ttt_status launch_softmax(int M, int V, const float* logits32, float* p, cudaStream_t st) {
   if (M == 0) return TTT_OK;
-  softmax_kernel<<<M, 512, 0, st>>>(V, logits32, p);
+  launch_pdl(softmax_kernel, M, 512, 0, st, V, logits32, p);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
 ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st) {
-  pending_shift_kernel<<<ceil_div(B, 128), 128, 0, st>>>(B, b, pend);
+  launch_pdl(pending_shift_kernel, ceil_div(B, 128), 128, 0, st, B, b, pend);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

@@ -50,12 +50,13 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
                      float* row_loss, cudaStream_t st);
 int ce_split_max_vocab();
 
-// Fused cross-entropy after the EPI_LOGITS head GEMM (bf16 logits):
-// lse[m] from the nt per-column-tile states part[m * ld + t]; for valid rows
-// the loss lse - tlogit[m] goes to losses / row_loss as in launch_ce.
-ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long long ld, int nt,
-                              const float* tlogit, float* lse, float* losses, long long loss_ld,
-                              long long loss_off, float* row_loss, cudaStream_t st);
+// Fused cross-entropy after the EPI_LOGITS head GEMM (bf16 operands):
+// lse[m] from the nt per-column-tile states part[m * ld + t]; the target logit
+// y[m] . U[tgt[m]] (y [M, d], U [V, d] bf16); for valid rows the loss lse - logit
+// goes to losses / row_loss as in launch_ce.
+ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long long ld, int nt, const void* y,
+                              const void* U, int d, const int32_t* tgt, float* lse, float* losses,
+                              long long loss_ld, long long loss_off, float* row_loss, cudaStream_t st);
 // In place over bf16 logits [M, V] (leading dim V, V % 8 == 0, 16-byte aligned):
 // dlogits = (exp(x - lse[m]) - [v == tgt[m]]) * scale; rows with tgt[m] < 0 get 0.
 ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const int32_t* tgt, float scale,
