@@ -215,6 +215,28 @@ def cpu_threads():
     return os.cpu_count()
 
 
+# ---------------------------------------------------------------- ranks
+def rank_inputs(wl, rank):
+    """Seeded inputs of one rank: every rank owns its own B sequences (the
+    sequences are independent), so rank r > 0 draws its streams with a seed
+    shifted by 1000 r; weights and the chain are shared."""
+    inp = synth.make_inputs(wl)
+    if rank:
+        inp["tokens"] = synth.sample_stream(inp["chain"], wl.seed_id + 1000 * rank, wl.B, wl.T)
+    return inp
+
+
+def max_over_ranks(x, world, device):
+    """Largest x over the ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- arms
 def run_reference(args, wl, rank):
     if rank != 0:
@@ -249,10 +271,7 @@ def run_ours(args, wl, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     pk = peaks()
-    # every rank owns its own B sequences: shift the stream seeds by rank
-    inp = synth.make_inputs(wl)
-    if rank:
-        inp["tokens"] = synth.sample_stream(inp["chain"], wl.seed_id + 1000 * rank, wl.B, wl.T)
+    inp = rank_inputs(wl, rank)
     h = Handle.from_workload(wl, inp["weights"])
     tok = torch.from_numpy(inp["tokens"]).to(dev)
     losses = torch.empty((wl.B, wl.T), dtype=torch.float32, device=dev)
@@ -308,12 +327,9 @@ def run_ours(args, wl, rank, world, local_rank):
     dom_n, dom_ms = h.profile_read()
     h.profile_enable(-1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
     tokens = wl.B * wl.T * world * args.steps
     value = tokens / (total_ms / 1e3)
@@ -333,12 +349,7 @@ def run_ours(args, wl, rank, world, local_rank):
         t0 = time.perf_counter()
         h.prefill(tok_h, loss_h, p_h, q_h, acc_h if n_ev else None, A_h if n_ev else None)
         e2e_t.append(time.perf_counter() - t0)
-    e2e_total = sum(e2e_t)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = max_over_ranks(sum(e2e_t), world, dev)
     e2e_value = tokens / e2e_total
     h2d = tok_h.numel() * 4 + (q_h.numel() * 4 if n_ev else 0)
     d2h = loss_h.numel() * 4 + p_h.numel() * 4 + (n_ev * wl.B * 5 if n_ev else 0)
