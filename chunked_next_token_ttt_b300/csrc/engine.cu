@@ -705,9 +705,8 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = dalloc(h, &h->dh32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = op_alloc(&h->dhop, Mm * d)) != TTT_OK) return bail(s);
   // split-K workspace: up to 8 fp32 partial slices of a [Mmax, d] output, at most 64 MB
-  // room for the largest split the tensor-core path makes: fewer than 148 output
-  // tiles of 128 x 128 fp32, up to 16 K ranges each (155 MB)
-  h->gemm_ws_elems = 148LL * 16 * 128 * 128;
+  // split-K partial tiles (fp32): the planner splits only while they fit (256 MB)
+  h->gemm_ws_elems = 64LL << 20;
   if ((s = dalloc(h, &h->gemm_ws, (size_t)h->gemm_ws_elems * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->split_cnt, (size_t)gemm_tc_max_split_tiles() * 4)) != TTT_OK) return bail(s);
   if (cudaMemset(h->split_cnt, 0, (size_t)gemm_tc_max_split_tiles() * 4) != cudaSuccess)

@@ -54,12 +54,12 @@ int g_num_sms = 0;
 
 }  // namespace tc
 
-// 128 x 256 tiles for bf16 GEMMs that still have two waves of them.
-static int choose_bn(const GemmDesc& g) {
-  if (g.dtype != ST_BF16) return tc::kBN;
-  const long long t256 = (long long)ceil_div(g.N, 256) * ceil_div(g.M, tc::BM) * g.batch;
-  return t256 >= 2 * 148 ? 256 : tc::kBN;
-}
+struct TcPlan {
+  int bn = 128;      // output tile width
+  int splitk = 1;    // K ranges
+};
+static TcPlan plan(const GemmDesc& g);
+static int choose_bn(const GemmDesc& g) { return plan(g).bn; }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -80,37 +80,51 @@ bool gemm_tc_supported(const GemmDesc& g) {
   return true;
 }
 
-// Split K when the output has fewer 128x128 tiles than SMs.  The number of K
-// ranges s minimises a cost in k-slice times: waves(s) * ceil(nkb / s) for the
-// main loop, plus, when split, one partial tile written per unit and s partial
-// tiles read back by a tile's last CTA (measured at about 1.5 k-slices each).
-// Every range keeps at least 4 k-slices, the partial tiles must fit the
-// workspace, and the dW and logits epilogues (per-tile partial sums) never split.
-static constexpr int kMaxSplitK = 16;
+// Tile width and split of K, chosen together by a cost in units of one
+// 128-wide k-slice's time: waves(units) x k-slices per unit x (1.21 for a
+// 256-wide k-slice: twice the work at the measured 1.65x throughput), plus, when
+// K is split, the partial tiles written and read back by each tile's last CTA
+// (2 + 3 per partial, twice that for 256-wide tiles).  Measured on the TTT
+// shapes: splitting pays for GEMMs with fewer tiles than SMs, and for larger
+// ones only with long K ranges, so a GEMM that already fills a wave splits only
+// if every range keeps at least 64 k-slices.  256-wide tiles are bf16 only;
+// every K range keeps at least 4 k-slices; split partial tiles must fit the
+// workspace and the arrival counters; the dW and logits epilogues (per-tile
+// partial sums) never split.
+static constexpr int kMaxSplitK = 32;
 
-int gemm_tc_splitk(const GemmDesc& g) {
-  if (!g.ws || g.epi == EPI_DW || g.epi == EPI_LOGITS || (g.N & 1)) return 1;
-  if (choose_bn(g) != tc::kBN) return 1;
-  const long long tiles = (long long)ceil_div(g.N, tc::kBN) * ceil_div(g.M, tc::BM) * g.batch;
+static TcPlan plan(const GemmDesc& g) {
+  TcPlan best;
+  double best_cost = 1e300;
   const int nkb = ceil_div(g.K, tc::BK);
-  if (tiles >= 148 || tiles > tc::kMaxSplitTiles || nkb < 8) return 1;
-  const long long slice = tiles * tc::BM * tc::kBN;   // whole (padded) tiles per split
-  int best = 1;
-  double best_cost = (double)nkb;
-  for (int sk = 2; sk <= kMaxSplitK && sk <= nkb / 4; ++sk) {
-    if (slice * sk > g.ws_elems) break;
-    const int kper = ceil_div(nkb, sk);
-    const int ranges = ceil_div(nkb, kper);
-    const long long units = tiles * ranges;
-    const long long waves = (units + 147) / 148;
-    const double cost = (double)waves * kper + 1.0 + 1.5 * ranges;
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = ranges;
+  const bool can_split = g.ws && g.epi != EPI_DW && g.epi != EPI_LOGITS && !(g.N & 1) && nkb >= 8;
+  for (int bn : {256, 128}) {
+    if (bn == 256 && g.dtype != ST_BF16) continue;
+    const long long tiles = (long long)ceil_div(g.N, bn) * ceil_div(g.M, tc::BM) * g.batch;
+    const double kslice = bn == 256 ? 1.21 : 1.0;
+    const double fix = bn == 256 ? 2.0 : 1.0;
+    for (int sk = 1; sk <= kMaxSplitK; ++sk) {
+      if (sk > 1 && (!can_split || sk > nkb / 4 || tiles > tc::kMaxSplitTiles ||
+                     tiles * tc::BM * bn * sk > g.ws_elems))
+        break;
+      const int kper = ceil_div(nkb, sk);
+      const int ranges = ceil_div(nkb, kper);
+      if (sk > 1 && ranges != sk) continue;
+      if (sk > 1 && tiles >= 148 && kper < 64) continue;
+      const long long units = tiles * ranges;
+      const long long waves = (units + 147) / 148;
+      const double cost = (double)waves * kper * kslice + (ranges > 1 ? fix * (2.0 + 3.0 * ranges) : 0.0);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best.bn = bn;
+        best.splitk = ranges;
+      }
     }
   }
   return best;
 }
+
+int gemm_tc_splitk(const GemmDesc& g) { return plan(g).splitk; }
 
 int gemm_tc_tile_n(const GemmDesc& g) { return choose_bn(g); }
 
@@ -151,7 +165,8 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (!gd.err) TTT_TRY(gemm_tc_error_word(&gd.err));
   const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
   const bool split = g.dtype == ST_SPLIT;
-  gd.bn = choose_bn(g);
+  const TcPlan pl = plan(g);
+  gd.bn = pl.bn;
   // maps: A hi, B hi, A lo, B lo.  A: K-major [batch][M][K] boxes {64, 128};
   // MN-major [batch][K][M] panels {64, 64}.  Likewise B with BN rows.
   CUtensorMap maps[4];
@@ -164,7 +179,7 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
     else TTT_TRY(tc::make_map(&maps[2 * p + 1], planesB[p], g.N, g.K, g.batch, g.ldb, g.sB, tc::PANEL, tc::BK));
   }
   const int nkb = ceil_div(g.K, tc::BK);
-  const int splitk = gemm_tc_splitk(g);
+  const int splitk = pl.splitk;
   // 16-byte epilogue accesses need every epilogue address, leading dim, batch
   // stride and lo offset on an 8-element boundary
   {
@@ -188,7 +203,7 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (splitk > 1) {
     // partial tiles go to the workspace; the per-tile arrival counters start at
     // zero and every split-K launch leaves them at zero
-    const long long tiles = (long long)ceil_div(g.M, tc::BM) * ceil_div(g.N, tc::kBN) * g.batch;
+    const long long tiles = (long long)ceil_div(g.M, tc::BM) * ceil_div(g.N, gd.bn) * g.batch;
     if (tiles > tc::kMaxSplitTiles) {
       set_error("split-K GEMM with too many output tiles");
       return TTT_ERR_UNSUPPORTED;

@@ -55,7 +55,7 @@ constexpr int NUM_EPI_WARPS = 8;   // two per 32-lane TMEM quadrant, splitting t
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int kBN = 128;           // output tile width
 constexpr int kCols = 64;          // accumulator columns per epilogue thread
-constexpr int kMaxSplitTiles = 256;  // output tiles of a split-K GEMM (arrival counters)
+constexpr int kMaxSplitTiles = 4096;  // output tiles of a split-K GEMM (arrival counters)
 constexpr long long kTimeoutNs = 2000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
