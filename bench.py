@@ -101,6 +101,10 @@ def chunk_flops(wl, rows=None):
         per["gemm_dw"] = wl.n_fast * mdf
     per["gemm_head"] = 2.0 * M * wl.d * wl.vocab
     per["gemm_head_bwd"] = 2.0 * M * wl.d * wl.vocab
+    if wl.chunk == 1:
+        # the persistent per-token kernel: W1 and W2 forward, head, dy = U^T dl,
+        # da = W2^T dh, and the two outer-product updates (2 FLOP per FMA)
+        per["token_step"] = wl.B * (10.0 * wl.d * wl.d_ff + 4.0 * wl.d * wl.vocab)
     return per
 
 
@@ -368,7 +372,13 @@ def run_ours(args, wl, rank, world, local_rank):
         per_launch = fl_step / launches_per_step_dom
         achieved = per_launch / dom_avg_s / 1e12
         split = wl.dtype == "fp32" and os.environ.get("TTT_FP32_STORAGE") != "f32" and wl.chunk >= 64
-        if wl.dtype == "fp32" and not split:
+        if dom == "token_step":
+            # one CTA per sequence: the FP32 FMA lanes of the SMs it occupies
+            sms = min(wl.B, 148)
+            peak = sms * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": f"fp32 FMA: {sms} SM(s) x 128 lanes x 2 x max SM clock"}
+        elif wl.dtype == "fp32" and not split:
             # fp32 FMA on the SIMT pipes: 148 SMs x 128 lanes x 2 FLOP x max SM clock
             peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
             roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -523,7 +523,7 @@ const char* ttt_last_error(void) { return g_last_error.c_str(); }
 static const char* kKClassNames[K_COUNT] = {
     "embed", "gemm_prefix", "gemm_fast_fwd", "rmsnorm_fwd", "gemm_head", "ce_fused",
     "gemm_head_bwd", "rmsnorm_bwd", "gemm_bwd_dx", "gemm_dw", "grad_norm", "clip_sgd_update",
-    "settle", "other"};
+    "settle", "other", "token_step"};
 
 const char* ttt_kernel_class_name(int c) { return (c >= 0 && c < K_COUNT) ? kKClassNames[c] : ""; }
 int ttt_kernel_class_count(void) { return K_COUNT; }
@@ -771,9 +771,24 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
 
   TTT_TRY(reset_weights(h, st));
   TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
+  // b = 1 on a network whose fast block and head fit in shared memory: one
+  // persistent CTA per sequence steps through every token
+  const char* env_tok = getenv("TTT_TOKEN_KERNEL");
+  const bool token_path = b == 1 && h->dm.n_prefix == 0 && h->dm.n_fast == 1 &&
+                          h->dm.block_kind == TTT_BLOCK_GELU && h->stg == ST_F32 && h->hp.settle_every == 0 &&
+                          token_steps_supported(h->d, h->f, h->V) && !(env_tok && std::string(env_tok) == "0");
+  if (token_path && n_full > 0) {
+    TTT_TRY(run(h, K_TOKEN, st, 1, [&] {
+      return launch_token_steps(B, tok, T + 1, n_full, static_cast<const float*>(h->E),
+                                static_cast<const float*>(h->U.p), h->W32, static_cast<float*>(h->Wop.p),
+                                h->slot_of[0], h->slot_of[1], loss_d, T, h->d, h->f, h->V, h->dm.rms_eps,
+                                h->hp.eta, h->hp.clip, h->flag, st);
+    }));
+    h->chunks_done += n_full;
+  }
   // chunks in groups whose frozen prefix runs as one pass before the group's TTT steps
   const int G = h->hoist_chunks;
-  for (int i0 = 0; i0 < n_full; i0 += G) {
+  for (int i0 = token_path ? n_full : 0; i0 < n_full; i0 += G) {
     const int g = n_full - i0 < G ? n_full - i0 : G;
     TTT_TRY(hoisted_prefix(h, tok, T + 1, i0, g, st));
     for (int i = i0; i < i0 + g; ++i) {

@@ -10,7 +10,7 @@
 // Kernel classes for launch accounting and per-class timing.
 enum KClass {
   K_EMBED = 0, K_GEMM_PREFIX, K_GEMM_FAST_FWD, K_RMSNORM_FWD, K_GEMM_HEAD, K_CE, K_GEMM_HEAD_BWD,
-  K_RMSNORM_BWD, K_GEMM_BWD_DX, K_GEMM_DW, K_NORM, K_SGD, K_SETTLE, K_OTHER, K_COUNT
+  K_RMSNORM_BWD, K_GEMM_BWD_DX, K_GEMM_DW, K_NORM, K_SGD, K_SETTLE, K_OTHER, K_TOKEN, K_COUNT
 };
 
 // An operand-storage buffer: its pointer and, for ST_SPLIT, the element

@@ -97,6 +97,16 @@ ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const fl
 // p[m, :] = softmax(logits32[m, :]).
 ttt_status launch_softmax(int M, int V, const float* logits32, float* p, cudaStream_t st);
 
+// Per-token TTT (b = 1) for a network without frozen prefix and one GELU block
+// whose matrices W1 (slot_w1) and W2 (slot_w2) are fast, fp32 storage: one CTA
+// per sequence keeps W1, W2 and U in shared memory and runs tokens 0 .. T-1 of
+// tok[s * tok_ld + .] (forward, loss, backward, clipped step), writing
+// losses[s * loss_ld + t] and, at the end, the fp32 masters and their copy.
+bool token_steps_supported(int d, int f, int V);
+ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T, const float* E, const float* U,
+                              float* W32, float* Wop, int slot_w1, int slot_w2, float* losses, long long loss_ld,
+                              int d, int f, int V, float eps, float eta, float clip, int* err, cudaStream_t st);
+
 // Shift the pending decode buffer: tok[s][0] = tok[s][b].
 ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st);
 

@@ -35,6 +35,43 @@ def test_toy_bigram_fp32_full_size():
     compare(wl, gpu, ref)
 
 
+@pytest.mark.parametrize("token_kernel", ["1", "0"], ids=["persistent", "general"])
+def test_per_token_clipped_b1_both_paths(monkeypatch, token_kernel):
+    """b = 1 with a clip that binds, three sequences, odd widths: the persistent
+    per-token kernel (closed-form outer-product norm) and the general chunk path
+    both match the oracle within the fp32 tolerance."""
+    monkeypatch.setenv("TTT_TOKEN_KERNEL", token_kernel)
+    wl = C.TOY_BIGRAM.replace(d=40, d_ff=100, vocab=90, B=3, T=150, clip=0.05, eta=0.2)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    assert max(max(st.norms) for st in ref["states"]) > wl.clip      # the clip binds
+    compare(wl, gpu, ref)
+
+
+def test_decode_after_persistent_per_token_prefill():
+    """The persistent kernel writes the fast weights back: decoding continues
+    from them (general path) and matches the oracle token by token."""
+    wl = C.TOY_BIGRAM.replace(B=2, T=64)
+    inp = make(wl)
+    extra = 12
+    long_tok = synth.sample_stream(inp["chain"], wl.seed_id, wl.B, wl.T + extra)
+    tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
+    gpu = run_gpu(wl, inp, tokens=tok)
+    h = gpu["handle"]
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
+    for t in range(wl.T + 1, wl.T + extra + 1):
+        h.decode_step(torch.from_numpy(long_tok[:, t].copy()).cuda(), p, loss)
+        torch.cuda.synchronize()
+        for s in range(wl.B):
+            l_ref, p_ref = oracle.decode_step(net, ref["states"][s], long_tok[s, t], wl.eta, wl.clip, wl.chunk)
+            assert abs(float(loss[s]) - l_ref) <= 1e-4
+            assert np.abs(p[s].cpu().numpy() - p_ref).max() <= 1e-5
+
+
 def test_chunked_fp32_prefix_chunks():
     wl = C.CHUNKED_FP32.replace(T=4 * C.CHUNKED_FP32.chunk)
     inp = make(wl)
