@@ -173,11 +173,15 @@ static ttt_status prefix_pass(ttt_handle* h, const TokView& tv, const PrefixBufs
   return TTT_OK;
 }
 
-// Rows of one chunk taken from a hoisted prefix pass over a group of chunks:
-// per sequence the group holds `rows_total` rows and this chunk starts at row0.
+// Rows taken from a hoisted prefix pass (over a group of chunks, or over a
+// Settlement chunk q): per sequence the pass holds `rows_total` rows and these
+// rows start at row0; x32 / op / a are the pass's fp32 residual, its operand
+// copy and (SwiGLU) the block-0 activation.
 struct Hoisted {
   bool on = false;
   long long row0 = 0, rows_total = 0;
+  const float* x32 = nullptr;
+  OpBuf op, a;
 };
 
 // Forward over B * tv.rows rows with the current (or committed) fast weights.
@@ -201,11 +205,11 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
   OpBuf a0;          // SwiGLU activation of block 0 when hoisted
   long long a0_s = 0;
   if (hz.on) {
-    hin0 = op_at(h, h->hx_op, hz.row0 * d);
+    hin0 = op_at(h, hz.op, hz.row0 * d);
     hin0_s = hz.rows_total * d;
-    x0 = h->hx32 + hz.row0 * d;
-    if (h->ha.p) {
-      a0 = op_at(h, h->ha, hz.row0 * f);
+    x0 = hz.x32 + hz.row0 * d;
+    if (hz.a.p) {
+      a0 = op_at(h, hz.a, hz.row0 * f);
       a0_s = hz.rows_total * f;
     }
   } else {
@@ -391,11 +395,10 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
       TTT_TRY(dw_gemm(g, sd));
     }
   }
-  TTT_TRY(run(h, K_NORM, st, 1, [&] {
-    return launch_norm_finalize(B, ps, h->partials, h->hp.clip, h->scale, h->gnorm, h->flag, st);
-  }));
+  // the per-sequence norm is reduced inside the update kernel (grad_norm has no launch of its own)
   TTT_TRY(run(h, K_SGD, st, 1, [&] {
-    return launch_sgd_update(stg, h->nslots, B, h->n, h->W32, h->Wop.p, h->Wop.lo, h->dW, h->scale, h->hp.eta, st);
+    return launch_clip_sgd_update(stg, h->nslots, B, h->n, h->W32, h->Wop.p, h->Wop.lo, h->dW, ps, h->partials,
+                                  h->hp.clip, h->hp.eta, h->scale, h->gnorm, h->flag, st);
   }));
   h->chunks_done++;
   return TTT_OK;
@@ -427,9 +430,22 @@ static ttt_status settle_event(ttt_handle* h, const int32_t* q, int Lq, float* A
                                cudaStream_t st) {
   TokView tv;
   tv.tok = q; tv.tok_ld = Lq; tv.tok_off = 0; tv.rows = Lq; tv.n_valid = Lq - 1;
-  TTT_TRY(forward(h, tv, true, false, nullptr, 0, 0, false, st));
+  tv.vocab = h->V;
+  tv.err = h->flag;
+  // q's frozen prefix does not depend on the fast weights: one pass serves the
+  // committed and the current forward
+  Hoisted hz;
+  if (h->qx32) {
+    PrefixBufs pb;
+    pb.x32 = h->qx32; pb.xop = h->xop; pb.hout = h->qx_op; pb.tmp_a = h->tmp_a; pb.tmp_g = h->tmp_g;
+    pb.swiglu_a = h->qa;
+    TTT_TRY(prefix_pass(h, tv, pb, st));
+    hz.on = true; hz.row0 = 0; hz.rows_total = Lq;
+    hz.x32 = h->qx32; hz.op = h->qx_op; hz.a = h->qa;
+  }
+  TTT_TRY(forward(h, tv, true, false, nullptr, 0, 0, false, st, hz));
   TTT_TRY(run(h, K_SETTLE, st, 1, [&] { return launch_seq_mean(h->B, Lq, Lq - 1, h->row_loss, h->Lc, st); }));
-  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, false, st));
+  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, false, st, hz));
   TTT_TRY(run(h, K_SETTLE, st, 1, [&] { return launch_seq_mean(h->B, Lq, Lq - 1, h->row_loss, h->Lw, st); }));
   return run(h, K_SETTLE, st, 2, [&] {
     return launch_settle_apply(h->stg, h->nslots, h->B, h->n, h->Lc, h->Lw, A, acc, h->W32, h->Wop.p,
@@ -663,6 +679,14 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
     if ((s = op_alloc(&h->ast[l], Mm * f)) != TTT_OK) return bail(s);
   }
   if ((s = op_alloc(&h->tmp_a, Mm * f)) != TTT_OK) return bail(s);
+  // Settlement chunk q: its prefix output, shared by the event's two forwards
+  if (hp->settle_len > 0) {
+    const size_t Mq = (size_t)B * hp->settle_len;
+    if ((s = dalloc(h, &h->qx32, Mq * d * 4)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->qx_op, Mq * d)) != TTT_OK) return bail(s);
+    if (D.block_kind == TTT_BLOCK_SWIGLU)
+      if ((s = op_alloc(&h->qa, Mq * f)) != TTT_OK) return bail(s);
+  }
   // hoisted prefix: groups of up to hoist_chunks chunks, within a 4 GiB budget
   {
     const size_t P = split ? 2 : 1;
@@ -796,6 +820,7 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
       tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = (long long)i * b; tv.rows = b; tv.n_valid = b;
       Hoisted hz;
       hz.on = true; hz.row0 = (long long)(i - i0) * b; hz.rows_total = (long long)g * b;
+      hz.x32 = h->hx32; hz.op = h->hx_op; hz.a = h->ha;
       TTT_TRY(chunk_step(h, tv, loss_d, T, (long long)i * b, st, hz));
       if (h->hp.settle_every > 0 && (i + 1) % h->hp.settle_every == 0) {
         const int e = (i + 1) / h->hp.settle_every - 1;

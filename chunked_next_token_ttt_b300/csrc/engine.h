@@ -60,6 +60,9 @@ struct ttt_handle {
   OpBuf hx_xop, hx_tmp_a;            // prefix ping-pong and hidden-width temporaries
   float* hx_tmp_g = nullptr;         // SwiGLU gate temporary
   OpBuf ha;                          // SwiGLU fast block 0: silu(gate h) * (up h)
+  // prefix output of a Settlement chunk q [B][Lq][.] (shared by its two forwards)
+  float* qx32 = nullptr;
+  OpBuf qx_op, qa;
   // inputs of fast block 0 in the last forward (backward reads them)
   OpBuf hin0, a0;
   long long hin0_s = 0, a0_s = 0;

@@ -331,3 +331,47 @@ __device__ __forceinline__ float epi_hex(const GemmDesc& g, int bz, int m, int n
 }
 
 }  // namespace ttt
+
+namespace ttt {
+
+// Epilogue kinds whose fp32 second input (aux) the tensor-core epilogue loads
+// ahead of the accumulator (GELU' reads its z stash in place: prefetching it as
+// well costs registers its arithmetic needs, measured slower).
+template <int EK>
+__host__ __device__ constexpr bool epi_reads_aux() {
+  return EK == EPI_RESID || EK == EPI_SWIGLU;
+}
+
+// The aux values of elements (m, n) .. (m, n+15) as fp32 (32-byte loads; the
+// same conditions as epi_hex).  Independent of the accumulator, so the
+// tensor-core epilogue issues these loads before it waits for the MMAs.
+template <typename S, int EK>
+__device__ __forceinline__ void load_aux16(const GemmDesc& g, int bz, int m, int n, float* x) {
+  const long long ix = bz * g.sX + (long long)m * g.ldx + n;
+  if (EK == EPI_DGELU) HexIO<S>::load(g.aux, g.loX, ix, x);
+  else HexIO<float>::load(g.aux, 0, ix, x);
+}
+
+// epi_hex with the aux values already loaded (x, fp32).
+template <typename S, int EK>
+__device__ __forceinline__ void epi_hex_x(const GemmDesc& g, int bz, int m, int n, const float* a, const float* x) {
+  using O = HexIO<S>;
+  const long long io = bz * g.sO + (long long)m * g.ldo + n;
+  float t[16];
+  if (EK == EPI_RESID) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = x[j] + a[j];
+    HexIO<float>::store(g.out, 0, io, t);
+    if (g.out2) O::store(g.out2, g.loO2, bz * g.sO2 + (long long)m * g.ldo2 + n, t);
+  } else if (EK == EPI_SWIGLU) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = silu_f(x[j]) * a[j];
+    O::store(g.out, g.loO, io, t);
+  } else if (EK == EPI_DGELU) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = a[j] * gelu_grad_f(x[j]);
+    O::store(g.out, g.loO, io, t);
+  }
+}
+
+}  // namespace ttt

@@ -378,18 +378,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     float* lse_s = stage + HALVES * BM;         //             [HALVES][BM] row sums of exp
     const long long tiles = (long long)g.batch * mtiles * ntiles;
     int i = 0;
+    constexpr bool AUX = epi_reads_aux<EK>();
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
       const Unit w = decode_unit(u, mtiles, ntiles, g.batch, BN);
       const int ab = i & 1, use = i >> 1;
+      const int row = w.m0 + r;
+      // the aux input of a 64-column group (written by earlier kernels, not by
+      // this GEMM): its loads for the first group are issued before waiting for
+      // the accumulator, so they overlap the MMAs
+      float xa[AUX ? kCols : 1];
+      auto load_x = [&](int c) {
+        const int n = w.n0 + c * kCols;
+        if (splitk == 1 && g.vec == 2 && n + kCols <= g.N && row < g.M) {
+#pragma unroll
+          for (int j = 0; j < kCols; j += 16) load_aux16<S, EK>(g, w.bz, row, n + j, xa + j);
+        }
+      };
+      if constexpr (AUX) load_x(half * GPW);
       if (!epi_all(mbar_wait(&accf[ab], use & 1, err, 32))) break;
       tc_fence_after();
-      const int row = w.m0 + r;
       const long long tix = ((long long)w.bz * mtiles + w.mt) * ntiles + w.nt;
       float sq = 0.0f;
       float rmax = -FLT_MAX, rsum = 0.0f;       // EPI_LOGITS: this row over this thread's columns
 #pragma unroll 1
       for (int gi = 0; gi < GPW; ++gi) {
         const int c = half * GPW + gi;          // column group of the tile
+        if constexpr (AUX) {
+          if (gi > 0) load_x(c);
+        }
         float v[kCols];
         {
           const uint32_t ta = tmem + (uint32_t)(ab * BN + c * kCols) + ((uint32_t)(quad * 32) << 16);
@@ -456,8 +472,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         } else if (row < g.M) {
           if (wide) {
+            if constexpr (AUX) {
 #pragma unroll
-            for (int j = 0; j < kCols; j += 16) sq += epi_hex<S, EK>(g, w.bz, row, n + j, v + j);
+              for (int j = 0; j < kCols; j += 16) epi_hex_x<S, EK>(g, w.bz, row, n + j, v + j, xa + j);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kCols; j += 16) sq += epi_hex<S, EK>(g, w.bz, row, n + j, v + j);
+            }
           } else if (full_vec) {
 #pragma unroll
             for (int j = 0; j < kCols; j += 8) sq += epi_oct<S, EK>(g, w.bz, row, n + j, v + j);

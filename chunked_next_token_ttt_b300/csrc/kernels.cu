@@ -250,69 +250,49 @@ __global__ void lse_combine_kernel(TokView tv, int M, const float2* __restrict__
 }
 
 // dlogits = (softmax - onehot(target)) * scale over bf16 logits [M, V] in place,
-// eight elements (16 bytes) per access; rows without a target get 0.  Grid:
-// x over the row's 16-byte vectors, y over rows.
+// eight elements (16 bytes) per access; rows without a target get 0.  The
+// scale is folded into the exponent, exp(x - (lse - ln scale)), and the one
+// target element of a row is corrected on its own.  Grid: x over the row's
+// 16-byte vectors, y over rows.
 __global__ void dlogits_kernel(int M, int V, bf16* __restrict__ logits, const float* __restrict__ lse,
                                const int32_t* __restrict__ tgt, float scale) {
   pdl_wait();
   pdl_launch();
   const int nv = V / 8;
+  const float lscale = logf(scale);
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
     uint4* row = reinterpret_cast<uint4*>(logits + (long long)m * V);
     const int t = tgt[m];
-    const float l = lse[m];
+    const float l = lse[m] - lscale;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
       if (t < 0) {
         row[i] = make_uint4(0u, 0u, 0u, 0u);
         continue;
       }
       uint4 raw = row[i];
-      const int c = i * 8;
       __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
+      const int c = i * 8;
+      float tx = 0.0f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float2 x = __bfloat1622float2(h2[q]);
-        float g0 = __expf(x.x - l), g1 = __expf(x.y - l);
-        if (c + 2 * q == t) g0 -= 1.0f;
-        if (c + 2 * q + 1 == t) g1 -= 1.0f;
-        h2[q] = __floats2bfloat162_rn(g0 * scale, g1 * scale);
+        if ((unsigned)(t - c - 2 * q) < 2u) tx = (t - c - 2 * q) ? x.y : x.x;
+        h2[q] = __floats2bfloat162_rn(__expf(x.x - l), __expf(x.y - l));
+      }
+      if ((unsigned)(t - c) < 8u) {
+        bf16* e = reinterpret_cast<bf16*>(&raw) + (t - c);
+        *e = __float2bfloat16_rn(__expf(tx - l) - scale);
       }
       row[i] = raw;
     }
   }
 }
 
-__global__ void norm_finalize_kernel(PartialSlots ps, const float* __restrict__ partials, float clip,
-                                     float* __restrict__ scale, float* __restrict__ norm, int* __restrict__ flag) {
-  pdl_wait();
-  pdl_launch();
-  __shared__ float red[32];
-  const int s = blockIdx.x;
-  float acc = 0.0f;
-  for (int k = 0; k < ps.n; ++k) {
-    const float* p = partials + ps.off[k] + (long long)s * ps.tiles[k];
-    for (int t = threadIdx.x; t < ps.tiles[k]; t += blockDim.x) acc += p[t];
-  }
-  acc = block_sum(acc, red);
-  if (threadIdx.x == 0) {
-    const float n = sqrtf(acc);
-    float sc = 1.0f;
-    if (!isfinite(n)) {
-      sc = 0.0f;
-      atomicOr(flag, 1);
-    } else if (clip > 0.0f) {
-      sc = fminf(1.0f, clip / (n + 1e-6f));
-    }
-    scale[s] = sc;
-    if (norm) norm[s] = n;
-  }
-}
-
-// One (slot, sequence) segment of n elements per blockIdx.y; float4 accesses
-// when n is a multiple of 4 (every fast matrix: n = d * d_ff).
+// One (slot, sequence) segment of n elements per blockIdx.y: W32 -= eta *
+// scale[s] * dW, operand copy re-cast; float4 accesses when n is a multiple of 4.
 template <typename S>
-__global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, void* Wop, long long wop_lo,
-                                  const float* __restrict__ dW, const float* __restrict__ scale, float eta) {
+__global__ void sgd_scale_kernel(int B, long long n, float* __restrict__ W32, void* Wop, long long wop_lo,
+                                 const float* __restrict__ dW, const float* __restrict__ scale, float eta) {
   pdl_wait();
   pdl_launch();
   const int s = blockIdx.y % B;
@@ -334,6 +314,96 @@ __global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, v
       OpIO<S>::store(Wop, wop_lo, i + 1, w.y);
       OpIO<S>::store(Wop, wop_lo, i + 2, w.z);
       OpIO<S>::store(Wop, wop_lo, i + 3, w.w);
+    }
+  } else {
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
+      const float w = W32[base + e] - step * dW[base + e];
+      W32[base + e] = w;
+      OpIO<S>::store(Wop, wop_lo, base + e, w);
+    }
+  }
+}
+
+// Four consecutive elements i .. i+3 of an operand buffer in one store per
+// plane (i a multiple of 4; base and lo offset 4-element aligned).
+template <typename S> struct QuadIO;
+template <> struct QuadIO<float> {
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float4 w) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p) + i) = w;
+  }
+};
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+template <> struct QuadIO<bf16> {
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float4 w) {
+    *reinterpret_cast<uint2*>(static_cast<bf16*>(p) + i) = pack_bf16x4(w.x, w.y, w.z, w.w);
+  }
+};
+template <> struct QuadIO<Split> {
+  __device__ __forceinline__ static void store(void* p, long long lo, long long i, float4 w) {
+    bf16* q = static_cast<bf16*>(p);
+    const uint2 h = pack_bf16x4(w.x, w.y, w.z, w.w);
+    const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&h);
+    const float2 h0 = __bfloat1622float2(hb[0]), h1 = __bfloat1622float2(hb[1]);
+    *reinterpret_cast<uint2*>(q + i) = h;
+    *reinterpret_cast<uint2*>(q + lo + i) = pack_bf16x4(w.x - h0.x, w.y - h0.y, w.z - h1.x, w.w - h1.y);
+  }
+};
+
+// Per-sequence clip scale from the dW GEMMs' per-tile sums of squares:
+// s = min(1, clip / (norm + 1e-6)) (1 when clip == 0), 0 when the norm is not
+// finite.  Every thread of the block receives it; red: >= 32 floats.
+__device__ __forceinline__ float seq_clip_scale(const PartialSlots& ps, const float* __restrict__ partials, int s,
+                                                float clip, float* red, float* norm_out) {
+  float acc = 0.0f;
+  for (int k = 0; k < ps.n; ++k) {
+    const float* p = partials + ps.off[k] + (long long)s * ps.tiles[k];
+    for (int t = threadIdx.x; t < ps.tiles[k]; t += blockDim.x) acc += p[t];
+  }
+  acc = block_sum(acc, red);
+  const float n = sqrtf(acc);
+  if (norm_out) *norm_out = n;
+  if (!isfinite(n)) return 0.0f;
+  return clip > 0.0f ? fminf(1.0f, clip / (n + 1e-6f)) : 1.0f;
+}
+
+// One (slot, sequence) segment of n elements per blockIdx.y; every block first
+// reduces its sequence's gradient norm from the per-tile partials (a few
+// hundred to a few thousand floats, from L2), then W32 -= eta * s * dW and the
+// operand copy is re-cast.  float4 accesses when n is a multiple of 4 (every
+// fast matrix: n = d * d_ff).
+template <typename S>
+__global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, void* Wop, long long wop_lo,
+                                  const float* __restrict__ dW, PartialSlots ps, const float* __restrict__ partials,
+                                  float clip, float eta, float* __restrict__ scale_out, float* __restrict__ norm_out,
+                                  int* __restrict__ flag) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ float red[32];
+  const int s = blockIdx.y % B;
+  const bool first = blockIdx.x == 0 && blockIdx.y == s;   // slot 0, first block of the sequence
+  float nrm = 0.0f;
+  const float sc = seq_clip_scale(ps, partials, s, clip, red, &nrm);
+  if (first && threadIdx.x == 0) {
+    if (scale_out) scale_out[s] = sc;
+    if (norm_out) norm_out[s] = nrm;
+    if (sc == 0.0f && !isfinite(nrm)) atomicOr(flag, 1);
+  }
+  if (sc == 0.0f) return;  // skipped update (non-finite norm): W stays as it is
+  const float step = eta * sc;
+  const long long base = (long long)blockIdx.y * n;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if ((n & 3) == 0 && (wop_lo & 3) == 0) {
+    float4* w4 = reinterpret_cast<float4*>(W32 + base);
+    const float4* g4 = reinterpret_cast<const float4*>(dW + base);
+    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n / 4; q += stride) {
+      float4 w = w4[q];
+      const float4 gr = g4[q];
+      w.x -= step * gr.x; w.y -= step * gr.y; w.z -= step * gr.z; w.w -= step * gr.w;
+      w4[q] = w;
+      QuadIO<S>::store(Wop, wop_lo, base + 4 * q, w);
     }
   } else {
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
@@ -542,23 +612,30 @@ ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const in
   return TTT_OK;
 }
 
-ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* partials, float clip, float* scale,
-                                float* norm, int* flag, cudaStream_t st) {
-  launch_pdl(norm_finalize_kernel, B, 256, 0, st, ps, partials, clip, scale, norm, flag);
-  TTT_CHECK_LAUNCH();
-  return TTT_OK;
-}
-
-ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
-                             const float* dW, const float* scale, float eta, cudaStream_t st) {
+static dim3 update_grid(int nslots, int B, long long n) {
   // blocks per segment: enough for ~16 blocks per SM over all segments
   const int segs = nslots * B;
   long long per = ((n + 3) / 4 + 255) / 256;
   const long long cap = (148LL * 16 + segs - 1) / segs;
   if (per > cap) per = cap;
   if (per < 1) per = 1;
-  dim3 grid((unsigned)per, (unsigned)segs);
-  LAUNCH_BY_STORAGE(stg, sgd_update_kernel, grid, 256, 0, st, B, n, W32, Wop, wop_lo, dW, scale, eta);
+  return dim3((unsigned)per, (unsigned)segs);
+}
+
+ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
+                             const float* dW, const float* scale, float eta, cudaStream_t st) {
+  const dim3 grid = update_grid(nslots, B, n);
+  LAUNCH_BY_STORAGE(stg, sgd_scale_kernel, grid, 256, 0, st, B, n, W32, Wop, wop_lo, dW, scale, eta);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_clip_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
+                                  const float* dW, const PartialSlots& ps, const float* partials, float clip,
+                                  float eta, float* scale_out, float* norm_out, int* flag, cudaStream_t st) {
+  const dim3 grid = update_grid(nslots, B, n);
+  LAUNCH_BY_STORAGE(stg, sgd_update_kernel, grid, 256, 0, st, B, n, W32, Wop, wop_lo, dW, ps, partials, clip, eta,
+                    scale_out, norm_out, flag);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

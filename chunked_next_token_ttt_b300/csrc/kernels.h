@@ -62,20 +62,25 @@ ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long
 ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const int32_t* tgt, float scale,
                           cudaStream_t st);
 
-// Per-sequence global gradient norm from the dW GEMM partials, then the
-// clip scale s = min(1, clip/(norm+1e-6)) (1 when clip == 0).  A non-finite
-// norm sets s = 0 (update skipped) and raises *flag.
+// Where the dW GEMMs left their per-tile sums of squares: for GEMM k, the
+// partials of sequence s are partials[off[k] + s * tiles[k] + t], t < tiles[k].
 struct PartialSlots {
   int n = 0;
   long long off[16];
   int tiles[16];
 };
-ttt_status launch_norm_finalize(int B, const PartialSlots& ps, const float* partials, float clip,
-                                float* scale, float* norm, int* flag, cudaStream_t st);
-
 // W32 -= eta * scale[s] * dW over the arena [slot][B][n]; Wop = cast(W32).
 ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
                              const float* dW, const float* scale, float eta, cudaStream_t st);
+
+// Per sequence s: norm = sqrt(sum of its dW partials), the clip scale
+// s_s = min(1, clip/(norm+1e-6)) (1 when clip == 0), then W32 -= eta * s_s * dW over the arena
+// [slot][B][n] and Wop = cast(W32), in one launch.  scale_out / norm_out [B]
+// (may be null) receive s_s and the norm; a non-finite norm skips that
+// sequence's update and raises bit 1 of *flag.
+ttt_status launch_clip_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
+                                  const float* dW, const PartialSlots& ps, const float* partials, float clip,
+                                  float eta, float* scale_out, float* norm_out, int* flag, cudaStream_t st);
 
 // W32[slot][s] = W0[slot] for every s; Wop = cast.
 ttt_status launch_broadcast_w0(int stg, int nslots, int B, long long n, const float* W0,

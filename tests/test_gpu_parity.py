@@ -193,6 +193,39 @@ def test_decode_swiglu_bf16_steps_with_the_per_call_prefix():
         assert rel <= 3e-2
 
 
+def test_settle_entry_point_after_prefill():
+    """ttt_settle on its own, after a prefill of 3 chunks whose 2nd chunk ended
+    with an in-prefill event: the candidate is the 3rd chunk's update; A and the
+    decision for every sequence, and the weights kept or restored, against the
+    oracle's Settlement on the same state (half the sequences score held-out
+    text from another chain, so both outcomes occur)."""
+    wl = C.SETTLE_760M.replace(d=128, d_ff=512, vocab=512, chunk=64, B=4, T=3 * 64, n_prefix=1,
+                               settle_len=64, settle_every=2, eta=0.5, init_std=0.08)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    h = gpu["handle"]
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, inp["tokens"], wl.settle_every, inp["settle_q"])
+    other = synth.make_chain(wl.seed_id + 100, wl.vocab, wl.chain_k, wl.chain_alpha)
+    q = synth.sample_heldout(inp["chain"], wl.seed_id + 7, 1, wl.B, wl.settle_len)[0]
+    q[1::2] = synth.sample_heldout(other, wl.seed_id + 7, 1, wl.B, wl.settle_len)[0][1::2]
+    qd = torch.from_numpy(np.ascontiguousarray(q)).cuda()
+    acc = torch.empty(wl.B, dtype=torch.uint8, device="cuda")
+    A = torch.empty(wl.B, dtype=torch.float32, device="cuda")
+    h.settle(qd, acc, A)
+    torch.cuda.synchronize()
+    A_ref = np.zeros((1, wl.B))
+    acc_ref = np.zeros((1, wl.B), dtype=bool)
+    for s in range(wl.B):
+        A_ref[0, s], acc_ref[0, s] = oracle.settle(net, ref["states"][s], q[s])
+    decided = compare_settlement({"A": A.cpu().numpy()[None], "accept": acc.cpu().numpy()[None].astype(bool)},
+                                 {"A": A_ref, "accept": acc_ref}, range(wl.B), noise=5e-3)
+    assert decided >= 2
+    for s in range(wl.B):
+        rel = oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats)
+        assert rel <= 3e-2, f"seq {s}: W after settle {rel:.3e}"
+
+
 def test_host_and_device_buffers_agree():
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=32, B=2, T=100, n_prefix=1)
     inp = make(wl)
