@@ -40,14 +40,19 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0}
 
 
+# host-side orchestration (which kernels run, not what a kernel does): left
+# out of the kernel identity below
+HOST_SOURCES = {"engine.cu", "engine.h", "ops_api.cu", "noalloc.cu"}
+
+
 def source_hash():
-    """SHA-256 over the CUDA sources and headers of libttt (kernel identity for
+    """SHA-256 over the libttt sources that define kernels (kernel identity for
     counters taken by a profiler)."""
     import glob
     import hashlib
     hsh = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "chunked_next_token_ttt_b300", "csrc", "*")) +
-                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    files = sorted(f for f in glob.glob(os.path.join(ROOT, "chunked_next_token_ttt_b300", "csrc", "*"))
+                   if os.path.basename(f) not in HOST_SOURCES)
     for f in files:
         hsh.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
