@@ -363,6 +363,41 @@ def run_ours(args, wl, rank, world, local_rank):
     h2d = tok_h.numel() * 4 + (q_h.numel() * 4 if n_ev else 0)
     d2h = loss_h.numel() * 4 + p_h.numel() * 4 + (n_ev * wl.B * 5 if n_ev else 0)
 
+    # decoding: one full cycle of b steps (one TTT update) after the prefill,
+    # device buffers through ttt_decode_step; every call scores the new token,
+    # steps when b are pending and returns p_{t+1}
+    dec = None
+    if not args.no_decode and wl.settle_every == 0:
+        h.prefill(tok, losses, p)
+        xs = torch.from_numpy(np.ascontiguousarray(inp["tokens"][:, 1:wl.chunk + 1].T)).to(dev)   # [b, B]
+        dloss = torch.empty((wl.B,), dtype=torch.float32, device=dev)
+        for t in range(min(3, wl.chunk)):
+            h.decode_step(xs[t], p, dloss)
+        h.prefill(tok, losses, p)
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(wl.chunk)]
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for t in range(wl.chunk):
+            dev_ev[t][0].record(st)
+            h.decode_step(xs[t], p, dloss)
+            dev_ev[t][1].record(st)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        dms = sum(a.elapsed_time(b) for a, b in dev_ev)
+        es = 2 if wl.dtype == "bf16" else 4
+        nf = len(wl.fast_mats) * wl.n_fast
+        frozen = (wl.n_prefix * (2 if wl.block == "gelu" else 3) * wl.d * wl.d_ff
+                  + wl.n_fast * ((2 if wl.block == "gelu" else 3) - len(wl.fast_mats)) * wl.d * wl.d_ff
+                  + wl.vocab * wl.d) * es
+        fast = wl.B * nf * wl.d * wl.d_ff * es
+        by = frozen + fast + wl.B * wl.vocab * 4 * 2
+        bound = wl.B / (by / (pk["hbm_gbs"] * 1e9))
+        v = wl.B * wl.chunk / (dms / 1e3)
+        dec = {"tokens_per_s": v, "tokens_per_s_wall": wl.B * wl.chunk / wall, "steps": wl.chunk,
+               "ms_per_step": dms / wl.chunk,
+               "weight_stream_bound_tokens_per_s": bound, "frac_of_bound": v / bound,
+               "note": "b decode steps (one TTT update amortised); bound = every weight read once per step"}
+
     # roofline of the dominant class
     flops = chunk_flops(wl)
     byts = chunk_bytes(wl)
@@ -426,6 +461,7 @@ def run_ours(args, wl, rank, world, local_rank):
             "roofline": roof, "clocks": clk_sum,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "decode": dec,
             "per_class_ms": {k: round(v[1], 3) for k, v in sorted(per_class.items(), key=lambda kv: -kv[1][1])}}
     if rank == 0 and not args.no_cpu_baseline:
         n_chunks = 12 if wl.name == C.CHUNKED_FP32.name else 2
@@ -447,6 +483,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=C.CHUNKED_FP32.name, choices=list(C.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
     ap.add_argument("--launch-log", default=None,
                     help="write the kernel class of every launch of the first prefill to this file")
     ap.add_argument("--T", type=int, default=None,

@@ -457,7 +457,69 @@ static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t 
   TokView tv;
   tv.tok = h->pend; tv.tok_ld = h->b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 0;
   TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, true, st));
-  return run(h, K_OTHER, st, 1, [&] { return launch_softmax(h->B, h->V, h->logits32, p_out, st); });
+  TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_softmax(h->B, h->V, h->logits32, p_out, h->lse_next, st); }));
+  // logits32 / lse_next now hold the next-token distribution under the current
+  // weights: the next decode step scores its token from them
+  h->next_valid = true;
+  return TTT_OK;
+}
+
+// Decoding's next-token forward (embedding -> blocks -> head -> softmax of one
+// row per sequence, token from the fixed slot x_dev) as a CUDA graph: captured
+// on first use on the handle's own stream, then replayed after the caller's
+// stream (event edges both ways).  Every pointer it reads is the handle's, so
+// one capture serves every later step.  Writes p_dev, logits32 and lse_next.
+static ttt_status decode_forward_graph(ttt_handle* h, cudaStream_t st) {
+  if (!h->dec_exec) {
+    if (!h->gstream) {
+      TTT_CUDA(cudaStreamCreateWithFlags(&h->gstream, cudaStreamNonBlocking));
+      TTT_CUDA(cudaEventCreateWithFlags(&h->gev[0], cudaEventDisableTiming));
+      TTT_CUDA(cudaEventCreateWithFlags(&h->gev[1], cudaEventDisableTiming));
+    }
+    const int saved_prof = h->prof_class;   // no profiling events inside the graph
+    const bool saved_log = h->log_on;
+    h->prof_class = -1;
+    h->log_on = false;
+    const long long l0 = h->launches;
+    TTT_CUDA(cudaStreamBeginCapture(h->gstream, cudaStreamCaptureModeThreadLocal));
+    TokView tv;
+    tv.tok = h->x_dev; tv.tok_ld = 1; tv.tok_off = 0; tv.rows = 1; tv.n_valid = 0;
+    ttt_status s = forward(h, tv, false, false, nullptr, 0, 0, true, h->gstream);
+    if (s == TTT_OK)
+      s = run(h, K_OTHER, h->gstream, 1,
+              [&] { return launch_softmax(h->B, h->V, h->logits32, h->p_dev, h->lse_next, h->gstream); });
+    cudaGraph_t graph = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(h->gstream, &graph);
+    h->prof_class = saved_prof;
+    h->log_on = saved_log;
+    h->dec_kernels = h->launches - l0;
+    h->launches = l0;
+    if (s != TTT_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return s;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture", __FILE__, __LINE__);
+    const cudaError_t ei = cudaGraphInstantiate(&h->dec_exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) {
+      h->dec_exec = nullptr;
+      return cuda_fail(ei, "cudaGraphInstantiate", __FILE__, __LINE__);
+    }
+  }
+  TTT_CUDA(cudaEventRecord(h->gev[0], st));
+  TTT_CUDA(cudaStreamWaitEvent(h->gstream, h->gev[0], 0));
+  TTT_CUDA(cudaGraphLaunch(h->dec_exec, h->gstream));
+  TTT_CUDA(cudaEventRecord(h->gev[1], h->gstream));
+  TTT_CUDA(cudaStreamWaitEvent(st, h->gev[1], 0));
+  h->launches += h->dec_kernels;
+  h->next_valid = true;
+  return TTT_OK;
+}
+
+// TTT_DECODE_GRAPH=0 runs the next-token forward launch by launch instead.
+static bool decode_graph_enabled() {
+  const char* e = getenv("TTT_DECODE_GRAPH");
+  return !(e && std::string(e) == "0");
 }
 
 static ttt_status reset_weights(ttt_handle* h, cudaStream_t st) {
@@ -549,6 +611,10 @@ ttt_status ttt_destroy(ttt_handle* h) {
   for (void* p : h->allocs)
     if (p) cudaFree(p);
   for (auto e : h->ev) cudaEventDestroy(e);
+  if (h->dec_exec) cudaGraphExecDestroy(h->dec_exec);
+  for (auto e : h->gev)
+    if (e) cudaEventDestroy(e);
+  if (h->gstream) cudaStreamDestroy(h->gstream);
   if (h->flag_host) cudaFreeHost(h->flag_host);
   delete h;
   return TTT_OK;
@@ -747,6 +813,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   }
   if ((s = dalloc(h, &h->logits32, (size_t)B * V * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->p_dev, (size_t)B * V * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->lse_next, (size_t)B * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->Lc, (size_t)B * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->Lw, (size_t)B * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->pend, (size_t)B * (h->b + 1) * 4)) != TTT_OK) return bail(s);
@@ -794,6 +861,7 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
   }
 
   TTT_TRY(reset_weights(h, st));
+  h->next_valid = false;
   TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
   // b = 1 on a network whose fast block and head fit in shared memory: one
   // persistent CTA per sequence steps through every token
@@ -858,16 +926,25 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   const int B = h->B, b = h->b;
   h->launches = 0;
   // x_new -> pend[s][pend_count + 1]
+  const bool x_dev_ptr = is_device_ptr(x_new);
   TTT_CUDA(cudaMemcpy2DAsync(h->pend + h->pend_count + 1, (size_t)(b + 1) * 4, x_new, 4, 4, B,
-                             is_device_ptr(x_new) ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+                             x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
   TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
-  // loss of (x_prev -> x_new) with the weights that score it
+  // loss of (x_prev -> x_new) with the weights that score it: the previous
+  // step's (or the prefill's) next-token softmax already holds them
   if (loss) {
-    TokView tv;
-    tv.tok = h->pend; tv.tok_ld = b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 1;
     const bool dev = is_device_ptr(loss);
     float* dst = dev ? loss : h->Lc;
-    TTT_TRY(forward(h, tv, false, false, dst, 1, 0, false, st));
+    if (h->next_valid) {
+      TTT_TRY(run(h, K_OTHER, st, 1, [&] {
+        return launch_next_token_loss(B, h->V, h->logits32, h->lse_next, h->pend, b + 1, h->pend_count + 1, dst,
+                                      h->flag, st);
+      }));
+    } else {
+      TokView tv;
+      tv.tok = h->pend; tv.tok_ld = b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 1;
+      TTT_TRY(forward(h, tv, false, false, dst, 1, 0, false, st));
+    }
     if (!dev) TTT_CUDA(cudaMemcpyAsync(loss, dst, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
   }
   h->pend_count++;
@@ -879,8 +956,17 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
     h->pend_count = 0;
   }
   const bool dev = is_device_ptr(p_next);
-  TTT_TRY(p_next_from_pending(h, dev ? p_next : h->p_dev, st));
-  if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
+  if (decode_graph_enabled()) {
+    // the newest token into the fixed slot the captured forward reads
+    TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4,
+                             x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+    TTT_TRY(decode_forward_graph(h, st));
+    TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4,
+                             dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, st));
+  } else {
+    TTT_TRY(p_next_from_pending(h, dev ? p_next : h->p_dev, st));
+    if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
+  }
   return finish(h, st);
 }
 
@@ -892,6 +978,7 @@ ttt_status ttt_settle(ttt_handle* h, const int32_t* q, int Lq, uint8_t* accept, 
   h->launches = 0;
   const int32_t* qd = nullptr;
   TTT_TRY(copy_in(h, q, (void**)&h->q_dev, &h->q_cap, (size_t)B * Lq * 4, (const void**)&qd, st));
+  h->next_valid = false;   // a revert changes the weights that scored the cached softmax
   TTT_TRY(ensure_staging(h, (void**)&h->A_dev, &h->A_cap, (size_t)B * 4));
   TTT_TRY(ensure_staging(h, (void**)&h->acc_dev, &h->acc_cap, (size_t)B));
   TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
@@ -916,6 +1003,7 @@ ttt_status ttt_get_fast_weights(ttt_handle* h, int seq, int block, int mat, floa
 
 ttt_status ttt_reset(ttt_handle* h, ttt_stream stream) {
   if (!h) return fail(TTT_ERR_BAD_ARG, "null handle");
+  h->next_valid = false;
   cudaStream_t st = (cudaStream_t)stream;
   TTT_TRY(reset_weights(h, st));
   h->has_context = false;
@@ -971,6 +1059,7 @@ ttt_status ttt_set_state(ttt_handle* h, const void* src, size_t bytes, ttt_strea
       hd.pend_count < 0 || hd.pend_count >= h->b)
     return fail(TTT_ERR_BAD_SHAPE, "state blob does not match this handle");
   cudaStream_t st = (cudaStream_t)stream;
+  h->next_valid = false;
   const char* p = static_cast<const char*>(src) + sizeof hd;
   const size_t arena = (size_t)h->nslots * h->B * h->n * 4;
   TTT_CUDA(cudaMemcpyAsync(h->W32, p, arena, cudaMemcpyDefault, st));

@@ -89,6 +89,13 @@ struct ttt_handle {
   int* flag_host = nullptr;
   float* logits32 = nullptr;
   float* p_dev = nullptr;
+  float* lse_next = nullptr;         // [B] logsumexp of logits32 (next-token softmax)
+  bool next_valid = false;           // logits32 / lse_next score the next decoded token
+  // decoding's next-token forward, captured once as a CUDA graph
+  cudaStream_t gstream = nullptr;
+  cudaEvent_t gev[2] = {nullptr, nullptr};
+  cudaGraphExec_t dec_exec = nullptr;
+  long long dec_kernels = 0;
   float* Lc = nullptr;
   float* Lw = nullptr;
 

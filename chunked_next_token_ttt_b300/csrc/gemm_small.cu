@@ -53,6 +53,99 @@ __global__ void __launch_bounds__(256) gemm_small_kmajor_kernel(GemmDesc g) {
   }
 }
 
+// Eight consecutive elements (16 bytes per plane) as fp32.
+template <typename S> struct Vec8;
+template <> struct Vec8<bf16> {
+  __device__ __forceinline__ static void load(const void* p, long long, long long i, float* v) {
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(static_cast<const bf16*>(p) + i), v);
+  }
+};
+template <> struct Vec8<Split> {
+  __device__ __forceinline__ static void load(const void* p, long long lo, long long i, float* v) {
+    OctIO<Split>::load(p, lo, i, v);
+  }
+};
+template <> struct Vec8<float> {
+  __device__ __forceinline__ static void load(const void* p, long long, long long i, float* v) {
+    OctIO<float>::load(p, 0, i, v);
+  }
+};
+
+// B K-major with 16-byte loads: each warp computes CW adjacent output columns
+// at once, each lane taking eight consecutive k per step (a warp reads 256
+// consecutive k of CW weight rows per step and plane); every 16-byte chunk of
+// the M activation rows (through L1) serves all CW columns.  CW = 4 for wide
+// outputs (N >= kWideN: vocabulary heads, wide projections) of one or two
+// rows, 1 otherwise so that narrow outputs still spread over enough warps.  Needs K, lda, ldb, the
+// batch strides and lo offsets multiples of 8 and 16-byte aligned bases
+// (gemm_small_vec_ok).
+constexpr int kWideN = 8192;
+
+template <typename S, int kCW>
+__global__ void __launch_bounds__(256) gemm_small_kvec_kernel(GemmDesc g) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ float red[8];
+  const int bz = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long a0 = bz * g.sA, b0 = bz * g.sB;
+  float sq = 0.0f;
+  for (int n0 = (blockIdx.x * 8 + warp) * kCW; n0 < g.N; n0 += gridDim.x * 8 * kCW) {
+    float acc[kCW][kMaxRows];
+#pragma unroll
+    for (int c = 0; c < kCW; ++c)
+#pragma unroll
+      for (int m = 0; m < kMaxRows; ++m) acc[c][m] = 0.0f;
+    for (int k = lane * 8; k < g.K; k += 256) {
+      float bv[kCW][8];
+#pragma unroll
+      for (int c = 0; c < kCW; ++c) {
+        const int n = n0 + c < g.N ? n0 + c : g.N - 1;   // clamp: the extra columns are not stored
+        Vec8<S>::load(g.B, g.loB, b0 + (long long)n * g.ldb + k, bv[c]);
+      }
+#pragma unroll
+      for (int m = 0; m < kMaxRows; ++m) {
+        if (m < g.M) {
+          float av[8];
+          Vec8<S>::load(g.A, g.loA, a0 + (long long)m * g.lda + k, av);
+#pragma unroll
+          for (int c = 0; c < kCW; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[c][m] = fmaf(av[j], bv[c][j], acc[c][m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kCW; ++c)
+#pragma unroll
+      for (int m = 0; m < kMaxRows; ++m)
+        if (m < g.M) acc[c][m] = warp_sum(acc[c][m]);
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < kCW; ++c)
+#pragma unroll
+        for (int m = 0; m < kMaxRows; ++m)
+          if (n0 + c < g.N && m < g.M) sq += epi_value<S>(g, bz, m, n0 + c, acc[c][m]);
+    }
+  }
+  if (g.epi == EPI_DW) {
+    sq = warp_sum(sq);
+    if (lane == 0) red[warp] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.0f;
+      for (int w = 0; w < 8; ++w) t += red[w];
+      g.partials[(long long)bz * gridDim.x + blockIdx.x] = t;
+    }
+  }
+}
+
+bool gemm_small_vec_ok(const GemmDesc& g) {
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  const long long m = (long long)g.K | g.lda | g.ldb | g.sA | g.sB | g.loA | g.loB;
+  return g.b_kmajor && (m & 7) == 0 && al(g.A) && al(g.B);
+}
+
 template <typename S>
 __global__ void __launch_bounds__(256) gemm_small_nmajor_kernel(GemmDesc g) {
   pdl_wait();
@@ -80,8 +173,14 @@ __global__ void __launch_bounds__(256) gemm_small_nmajor_kernel(GemmDesc g) {
   }
 }
 
+bool gemm_small_vec_ok(const GemmDesc& g);
+
+// four columns per warp pay for wide outputs with one or two rows; with more
+// rows the 4 x M accumulators crowd the registers (measured slower)
+int small_cols_per_warp(const GemmDesc& g) { return (g.N >= kWideN && g.M <= 2) ? 4 : 1; }
+
 int small_grid_x(const GemmDesc& g) {
-  const int per_block = g.b_kmajor ? 8 : 256;
+  const int per_block = gemm_small_vec_ok(g) ? 8 * small_cols_per_warp(g) : (g.b_kmajor ? 8 : 256);
   int gx = ceil_div(g.N, per_block);
   // enough blocks to cover the SMs a few times over, at least one column each
   const int target = ceil_div(148 * 4, g.batch);
@@ -104,7 +203,16 @@ ttt_status gemm_small(const GemmDesc& g, cudaStream_t st) {
     else if (g.dtype == ST_SPLIT) launch_pdl(KERNEL<Split>, grid, 256, 0, st, g);                  \
     else launch_pdl(KERNEL<float>, grid, 256, 0, st, g);                                           \
   } while (0)
-  if (g.b_kmajor) TTT_SMALL(gemm_small_kmajor_kernel);
+  if (gemm_small_vec_ok(g) && small_cols_per_warp(g) == 4) {
+    if (g.dtype == ST_BF16) launch_pdl(gemm_small_kvec_kernel<bf16, 4>, grid, 256, 0, st, g);
+    else if (g.dtype == ST_SPLIT) launch_pdl(gemm_small_kvec_kernel<Split, 4>, grid, 256, 0, st, g);
+    else launch_pdl(gemm_small_kvec_kernel<float, 4>, grid, 256, 0, st, g);
+  } else if (gemm_small_vec_ok(g)) {
+    if (g.dtype == ST_BF16) launch_pdl(gemm_small_kvec_kernel<bf16, 1>, grid, 256, 0, st, g);
+    else if (g.dtype == ST_SPLIT) launch_pdl(gemm_small_kvec_kernel<Split, 1>, grid, 256, 0, st, g);
+    else launch_pdl(gemm_small_kvec_kernel<float, 1>, grid, 256, 0, st, g);
+  }
+  else if (g.b_kmajor) TTT_SMALL(gemm_small_kmajor_kernel);
   else TTT_SMALL(gemm_small_nmajor_kernel);
 #undef TTT_SMALL
   TTT_CHECK_LAUNCH();

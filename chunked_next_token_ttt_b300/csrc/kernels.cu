@@ -478,7 +478,8 @@ __global__ void settle_apply_kernel(long long total, int B, long long n, const u
   }
 }
 
-__global__ void softmax_kernel(int V, const float* __restrict__ logits, float* __restrict__ p) {
+__global__ void softmax_kernel(int V, const float* __restrict__ logits, float* __restrict__ p,
+                               float* __restrict__ lse_out) {
   pdl_wait();
   pdl_launch();
   __shared__ float red[32];
@@ -496,8 +497,26 @@ __global__ void softmax_kernel(int V, const float* __restrict__ logits, float* _
   float se = 0.0f;
   for (int v = threadIdx.x; v < V; v += blockDim.x) se += expf(row[v] - mx);
   se = block_sum(se, red);
+  if (lse_out && threadIdx.x == 0) lse_out[m] = mx + logf(se);
   const float inv = 1.0f / se;
   for (int v = threadIdx.x; v < V; v += blockDim.x) p[m * V + v] = expf(row[v] - mx) * inv;
+}
+
+// loss[s] = lse[s] - logits[s][x]: the next-token loss of x from a softmax
+// already taken (the row's logits and logsumexp), x = tok[s * tok_ld + off].
+__global__ void next_token_loss_kernel(int B, int V, const float* __restrict__ logits, const float* __restrict__ lse,
+                                       const int32_t* __restrict__ tok, long long tok_ld, long long off,
+                                       float* __restrict__ loss, int* __restrict__ err) {
+  pdl_wait();
+  pdl_launch();
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= B) return;
+  int x = tok[s * tok_ld + off];
+  if ((unsigned)x >= (unsigned)V) {
+    atomicOr(err, 2);
+    x = 0;
+  }
+  loss[s] = lse[s] - logits[(long long)s * V + x];
 }
 
 __global__ void pending_shift_kernel(int B, int b, int32_t* pend) {
@@ -674,9 +693,16 @@ ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const fl
   return TTT_OK;
 }
 
-ttt_status launch_softmax(int M, int V, const float* logits32, float* p, cudaStream_t st) {
+ttt_status launch_next_token_loss(int B, int V, const float* logits32, const float* lse, const int32_t* tok,
+                                  long long tok_ld, long long off, float* loss, int* err, cudaStream_t st) {
+  launch_pdl(next_token_loss_kernel, ceil_div(B, 128), 128, 0, st, B, V, logits32, lse, tok, tok_ld, off, loss, err);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* lse, cudaStream_t st) {
   if (M == 0) return TTT_OK;
-  launch_pdl(softmax_kernel, M, 512, 0, st, V, logits32, p);
+  launch_pdl(softmax_kernel, M, 512, 0, st, V, logits32, p, lse);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

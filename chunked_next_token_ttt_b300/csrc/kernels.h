@@ -99,8 +99,12 @@ ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const fl
                                const float* Lw, float* A, uint8_t* accept, float* W32, void* Wop,
                                float* Wc32, void* Wcop, long long op_lo, cudaStream_t st);
 
-// p[m, :] = softmax(logits32[m, :]).
-ttt_status launch_softmax(int M, int V, const float* logits32, float* p, cudaStream_t st);
+// p[m, :] = softmax(logits32[m, :]); lse[m] = logsumexp of the row (lse may be null).
+ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* lse, cudaStream_t st);
+// loss[s] = lse[s] - logits32[s * V + x_s] with x_s = tok[s * tok_ld + off]
+// (ids outside [0, V) read as 0 and raise bit 2 of *err).
+ttt_status launch_next_token_loss(int B, int V, const float* logits32, const float* lse, const int32_t* tok,
+                                  long long tok_ld, long long off, float* loss, int* err, cudaStream_t st);
 
 // Per-token TTT (b = 1) for a network without frozen prefix and one GELU block
 // whose matrices W1 (slot_w1) and W2 (slot_w2) are fast, fp32 storage: one CTA

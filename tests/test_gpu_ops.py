@@ -328,13 +328,14 @@ def test_split_k_ragged_residual_twice_in_a_row():
     assert np.abs(outs[0] - ref).max() <= 2e-3 * np.abs(ref).max()
 
 
+@pytest.mark.parametrize("N", [1000, 9000], ids=["narrow", "wide"])
 @pytest.mark.parametrize("M", [1, 3, 8])
 @pytest.mark.parametrize("b_k", [True, False], ids=["B_kmaj", "B_nmaj"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "bf16x3"])
-def test_small_m_gemm(M, b_k, dtype):
+def test_small_m_gemm(M, b_k, dtype, N):
     """A few rows per batch entry (one token per sequence): weight-streaming kernel."""
     rng = np.random.default_rng(11)
-    N, K, batch = 1000, 520, 3
+    K, batch = 520, 3   # N = 9000 with M <= 2: four columns per warp, ragged last group
     A = rng.normal(0, 1, (batch, M, K)).astype(np.float32)
     Bm = rng.normal(0, 1, (batch, N, K)).astype(np.float32)
     Bs = Bm if b_k else np.ascontiguousarray(Bm.transpose(0, 2, 1))

@@ -246,7 +246,12 @@ def test_sequences_are_independent_on_gpu():
             np.testing.assert_array_equal(one["W"][0][l][k], full["W"][1][l][k])
 
 
-def test_decode_completes_the_ragged_chunk_and_continues():
+@pytest.mark.parametrize("graph", ["1", "0"], ids=["graph", "launches"])
+def test_decode_completes_the_ragged_chunk_and_continues(monkeypatch, graph):
+    """Decoding after a prefill with a ragged tail: every step's loss and p_next
+    against the oracle, through the captured next-token graph and launch by
+    launch."""
+    monkeypatch.setenv("TTT_DECODE_GRAPH", graph)
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=16 * 3 + 5, n_prefix=1)
     inp = make(wl)
     extra = 16 + 11 + 16
@@ -261,6 +266,10 @@ def test_decode_completes_the_ragged_chunk_and_continues():
     loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
     for t in range(wl.T + 1, wl.T + extra + 1):
         x = torch.from_numpy(long_tok[:, t].copy()).cuda()
+        if t == wl.T + 8:
+            # a state round trip drops the cached next-token softmax: this step
+            # scores its token with a forward pass instead
+            h.set_state(h.get_state())
         h.decode_step(x, p, loss)
         torch.cuda.synchronize()
         for s in range(wl.B):
