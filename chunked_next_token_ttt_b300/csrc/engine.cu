@@ -287,6 +287,8 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
   }));
 
   const float scale = tv.n_valid > 0 ? 1.0f / (float)tv.n_valid : 0.0f;
+  // Source Masking: per-row scales of this chunk (set by chunk_step) replace 1/b
+  const float* rscale = train && h->rscale_on ? h->rscale : nullptr;
   if (fused) {
     TTT_TRY(rungemm(h, K_GEMM_HEAD, gl, st));
     const int nt = ceil_div(V, gemm_tc_tile_n(gl));
@@ -295,7 +297,7 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
                                 loss_ld, loss_off, h->row_loss, st);
     }));
     if (!train) return TTT_OK;
-    return run(h, K_CE, st, 1, [&] { return launch_dlogits(M, V, h->logits, h->lse, h->tgt, scale, st); });
+    return run(h, K_CE, st, 1, [&] { return launch_dlogits(M, V, h->logits, h->lse, h->tgt, scale, rscale, st); });
   }
   if (head_f32) {
     gh.epi = EPI_STORE_F32; gh.out = h->logits32; gh.ldo = V;
@@ -308,7 +310,7 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
   }
   TTT_TRY(rungemm(h, K_GEMM_HEAD, gh, st));
   return run(h, K_CE, st, 1, [&] {
-    return launch_ce(stg, B, tv, V, h->logits, V, scale, train, losses, loss_ld, loss_off, h->row_loss, st);
+    return launch_ce(stg, B, tv, V, h->logits, V, scale, rscale, train, losses, loss_ld, loss_off, h->row_loss, st);
   });
 }
 
@@ -404,9 +406,20 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
   return TTT_OK;
 }
 
+// One chunk step; with `mask` (Source Masking, [B][mask_ld], the chunk's
+// targets at offset tv.tok_off) the chunk's loss is the mean over its unmasked
+// targets instead of all b.
 static ttt_status chunk_step(ttt_handle* h, const TokView& tv, float* losses, long long loss_ld,
-                             long long loss_off, cudaStream_t st, const Hoisted& hz = Hoisted()) {
-  TTT_TRY(forward(h, tv, false, true, losses, loss_ld, loss_off, false, st, hz));
+                             long long loss_off, cudaStream_t st, const Hoisted& hz = Hoisted(),
+                             const uint8_t* mask = nullptr, long long mask_ld = 0) {
+  if (mask)
+    TTT_TRY(run(h, K_OTHER, st, 1, [&] {
+      return launch_chunk_row_scale(h->B, tv.rows, mask, mask_ld, tv.tok_off, h->rscale, st);
+    }));
+  h->rscale_on = mask != nullptr;
+  const ttt_status fs = forward(h, tv, false, true, losses, loss_ld, loss_off, false, st, hz);
+  h->rscale_on = false;
+  TTT_TRY(fs);
   return backward_update(h, tv.rows, st);
 }
 
@@ -786,6 +799,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = dalloc(h, &h->rstd, Mm * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->logits, Mm * V * (split ? 4 : es))) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->row_loss, Mm * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->rscale, Mm * 4)) != TTT_OK) return bail(s);
   // fused cross-entropy state: one online-softmax pair per row and head column tile
   h->lse_ld = ceil_div(V, 128);  // the narrowest tensor-core tile
   if ((s = dalloc(h, &h->lse_part, Mm * (size_t)h->lse_ld * sizeof(float2))) != TTT_OK) return bail(s);
@@ -832,6 +846,12 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
 
 ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float* losses, float* p_next,
                        const int32_t* settle_q, int Lq, uint8_t* accept, float* A, ttt_stream stream) {
+  return ttt_prefill_masked(h, tokens, nullptr, B, T, losses, p_next, settle_q, Lq, accept, A, stream);
+}
+
+ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_t* loss_mask, int B, int T,
+                              float* losses, float* p_next, const int32_t* settle_q, int Lq, uint8_t* accept,
+                              float* A, ttt_stream stream) {
   if (!h || !tokens || !losses) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_prefill");
   if (B != h->B || T < 1) return fail(TTT_ERR_BAD_SHAPE, "B must equal max_batch and T >= 1");
   cudaStream_t st = (cudaStream_t)stream;
@@ -845,6 +865,9 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
 
   const int32_t* tok = nullptr;
   TTT_TRY(copy_in(h, tokens, (void**)&h->tok_dev, &h->tok_cap, (size_t)B * (T + 1) * 4, (const void**)&tok, st));
+  const uint8_t* mask = nullptr;
+  if (loss_mask)
+    TTT_TRY(copy_in(h, loss_mask, (void**)&h->mask_dev, &h->mask_cap, (size_t)B * T, (const void**)&mask, st));
   const int32_t* q = nullptr;
   if (n_events > 0)
     TTT_TRY(copy_in(h, settle_q, (void**)&h->q_dev, &h->q_cap, (size_t)n_events * B * Lq * 4,
@@ -871,7 +894,7 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
                           token_steps_supported(h->d, h->f, h->V) && !(env_tok && std::string(env_tok) == "0");
   if (token_path && n_full > 0) {
     TTT_TRY(run(h, K_TOKEN, st, 1, [&] {
-      return launch_token_steps(B, tok, T + 1, n_full, static_cast<const float*>(h->E),
+      return launch_token_steps(B, tok, T + 1, n_full, mask, T, static_cast<const float*>(h->E),
                                 static_cast<const float*>(h->U.p), h->W32, static_cast<float*>(h->Wop.p),
                                 h->slot_of[0], h->slot_of[1], loss_d, T, h->d, h->f, h->V, h->dm.rms_eps,
                                 h->hp.eta, h->hp.clip, h->flag, st);
@@ -880,6 +903,7 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
   }
   // chunks in groups whose frozen prefix runs as one pass before the group's TTT steps
   const int G = h->hoist_chunks;
+
   for (int i0 = token_path ? n_full : 0; i0 < n_full; i0 += G) {
     const int g = n_full - i0 < G ? n_full - i0 : G;
     TTT_TRY(hoisted_prefix(h, tok, T + 1, i0, g, st));
@@ -889,7 +913,7 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
       Hoisted hz;
       hz.on = true; hz.row0 = (long long)(i - i0) * b; hz.rows_total = (long long)g * b;
       hz.x32 = h->hx32; hz.op = h->hx_op; hz.a = h->ha;
-      TTT_TRY(chunk_step(h, tv, loss_d, T, (long long)i * b, st, hz));
+      TTT_TRY(chunk_step(h, tv, loss_d, T, (long long)i * b, st, hz, mask, T));
       if (h->hp.settle_every > 0 && (i + 1) % h->hp.settle_every == 0) {
         const int e = (i + 1) / h->hp.settle_every - 1;
         TTT_TRY(settle_event(h, q + (size_t)e * B * Lq, Lq, h->A_dev + (size_t)e * B, h->acc_dev + (size_t)e * B,
@@ -897,7 +921,7 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T, float
       }
     }
   }
-  if (rem > 0) {
+  if (rem > 0) {   // the tail is scored only (and, as decoding, never masked)
     TokView tv;
     tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = (long long)n_full * b; tv.rows = rem; tv.n_valid = rem;
     TTT_TRY(forward(h, tv, false, false, loss_d, T, (long long)n_full * b, false, st));

@@ -70,6 +70,9 @@ struct ttt_handle {
   float* rstd = nullptr;
   void* logits = nullptr;            // [Mmax, V]: float for ST_SPLIT, operand type otherwise
   float* row_loss = nullptr;
+  float* rscale = nullptr;           // [Mmax] Source Masking: per-row loss scales of a chunk
+  bool rscale_on = false;            // set only while a masked chunk step runs its forward
+  uint8_t* mask_dev = nullptr; size_t mask_cap = 0;   // staging for a host mask
   float2* lse_part = nullptr;        // [Mmax][lse_ld] head-tile softmax states
   long long lse_ld = 0;
   float* lse = nullptr;              // [Mmax]

@@ -128,9 +128,9 @@ __device__ __forceinline__ int target_of(const TokView& tv, int s, int j, int V)
 }
 
 template <typename OpT>
-__global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long ldl, float scale, bool grad,
-                          float* __restrict__ losses, long long loss_ld, long long loss_off,
-                          float* __restrict__ row_loss) {
+__global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long ldl, float scale,
+                          const float* __restrict__ rscale, bool grad, float* __restrict__ losses,
+                          long long loss_ld, long long loss_off, float* __restrict__ row_loss) {
   pdl_wait();
   pdl_launch();
   __shared__ float sm_m[32], sm_s[32];
@@ -152,10 +152,11 @@ __global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long
     if (row_loss) row_loss[m] = loss;
   }
   if (!grad) return;
+  const float sc = rscale ? rscale[m] : scale;
   __syncthreads();   // the target logit is read above before being overwritten
   for (int v = threadIdx.x; v < V; v += blockDim.x) {
     const float p = __expf(to_f(row[v]) - lse);
-    row[v] = from_f<OpT>((p - (v == tgt ? 1.0f : 0.0f)) * scale);
+    row[v] = from_f<OpT>((p - (v == tgt ? 1.0f : 0.0f)) * sc);
   }
 }
 
@@ -165,8 +166,8 @@ __global__ void ce_kernel(TokView tv, int V, OpT* __restrict__ logits, long long
 constexpr int kCeSplitMaxV = 32768;
 
 __global__ void ce_split_kernel(TokView tv, int V, float* __restrict__ logits, long long ldl, float scale,
-                                bool grad, float* __restrict__ losses, long long loss_ld, long long loss_off,
-                                float* __restrict__ row_loss) {
+                                const float* __restrict__ rscale, bool grad, float* __restrict__ losses,
+                                long long loss_ld, long long loss_off, float* __restrict__ row_loss) {
   pdl_wait();
   pdl_launch();
   extern __shared__ float srow[];
@@ -197,8 +198,9 @@ __global__ void ce_split_kernel(TokView tv, int V, float* __restrict__ logits, l
     if (row_loss) row_loss[m] = loss;
   }
   if (!grad) return;
+  const float sc = rscale ? rscale[m] : scale;
   for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    const float g = (__expf(srow[v] - lse) - (v == tgt ? 1.0f : 0.0f)) * scale;
+    const float g = (__expf(srow[v] - lse) - (v == tgt ? 1.0f : 0.0f)) * sc;
     const bf16 h = __float2bfloat16_rn(g);
     out[v] = h;
     out[V + v] = __float2bfloat16_rn(g - __bfloat162float(h));
@@ -249,21 +251,37 @@ __global__ void lse_combine_kernel(TokView tv, int M, const float2* __restrict__
   }
 }
 
+// Source Masking: rscale[s * rows + j] = mask_j / max(1, sum of the mask over
+// the chunk's rows of sequence s), mask_j = mask[s * mask_ld + off + j] != 0.
+__global__ void chunk_row_scale_kernel(int rows, const uint8_t* __restrict__ mask, long long mask_ld, long long off,
+                                       float* __restrict__ rscale) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ float red[32];
+  const int s = blockIdx.x;
+  const uint8_t* mr = mask + s * mask_ld + off;
+  float cnt = 0.0f;
+  for (int j = threadIdx.x; j < rows; j += blockDim.x) cnt += mr[j] ? 1.0f : 0.0f;
+  cnt = block_sum(cnt, red);
+  const float inv = 1.0f / fmaxf(cnt, 1.0f);
+  for (int j = threadIdx.x; j < rows; j += blockDim.x) rscale[(long long)s * rows + j] = mr[j] ? inv : 0.0f;
+}
+
 // dlogits = (softmax - onehot(target)) * scale over bf16 logits [M, V] in place,
 // eight elements (16 bytes) per access; rows without a target get 0.  The
 // scale is folded into the exponent, exp(x - (lse - ln scale)), and the one
 // target element of a row is corrected on its own.  Grid: x over the row's
 // 16-byte vectors, y over rows.
 __global__ void dlogits_kernel(int M, int V, bf16* __restrict__ logits, const float* __restrict__ lse,
-                               const int32_t* __restrict__ tgt, float scale) {
+                               const int32_t* __restrict__ tgt, float scale, const float* __restrict__ rscale) {
   pdl_wait();
   pdl_launch();
   const int nv = V / 8;
-  const float lscale = logf(scale);
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
     uint4* row = reinterpret_cast<uint4*>(logits + (long long)m * V);
-    const int t = tgt[m];
-    const float l = lse[m] - lscale;
+    const float sc = rscale ? rscale[m] : scale;
+    const int t = sc > 0.0f ? tgt[m] : -1;   // a zero scale (masked row) writes zeros
+    const float l = lse[m] - logf(sc > 0.0f ? sc : 1.0f);
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
       if (t < 0) {
         row[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -281,7 +299,7 @@ __global__ void dlogits_kernel(int M, int V, bf16* __restrict__ logits, const fl
       }
       if ((unsigned)(t - c) < 8u) {
         bf16* e = reinterpret_cast<bf16*>(&raw) + (t - c);
-        *e = __float2bfloat16_rn(__expf(tx - l) - scale);
+        *e = __float2bfloat16_rn(__expf(tx - l) - sc);
       }
       row[i] = raw;
     }
@@ -575,8 +593,9 @@ ttt_status launch_rmsnorm_bwd(int stg, int M, int d, const float* x, const float
 
 int ce_split_max_vocab() { return kCeSplitMaxV; }
 
-ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, long long ldl, float scale, bool grad,
-                     float* losses, long long loss_ld, long long loss_off, float* row_loss, cudaStream_t st) {
+ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, long long ldl, float scale,
+                     const float* rscale, bool grad, float* losses, long long loss_ld, long long loss_off,
+                     float* row_loss, cudaStream_t st) {
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
   if (stg == ST_SPLIT) {
@@ -591,13 +610,13 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
       smem_set = smem;
     }
-    launch_pdl(ce_split_kernel, M, 512, smem, st, tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
+    launch_pdl(ce_split_kernel, M, 512, smem, st, tv, V, static_cast<float*>(logits), ldl, scale, rscale, grad, losses, loss_ld,
                                           loss_off, row_loss);
   } else if (stg == ST_BF16) {
-    launch_pdl(ce_kernel<bf16>, M, 512, 0, st, tv, V, static_cast<bf16*>(logits), ldl, scale, grad, losses, loss_ld,
+    launch_pdl(ce_kernel<bf16>, M, 512, 0, st, tv, V, static_cast<bf16*>(logits), ldl, scale, rscale, grad, losses, loss_ld,
                                        loss_off, row_loss);
   } else {
-    launch_pdl(ce_kernel<float>, M, 512, 0, st, tv, V, static_cast<float*>(logits), ldl, scale, grad, losses, loss_ld,
+    launch_pdl(ce_kernel<float>, M, 512, 0, st, tv, V, static_cast<float*>(logits), ldl, scale, rscale, grad, losses, loss_ld,
                                         loss_off, row_loss);
   }
   TTT_CHECK_LAUNCH();
@@ -616,8 +635,16 @@ ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long
   return TTT_OK;
 }
 
+ttt_status launch_chunk_row_scale(int B, int rows, const uint8_t* mask, long long mask_ld, long long off,
+                                  float* rscale, cudaStream_t st) {
+  if (B == 0 || rows == 0) return TTT_OK;
+  launch_pdl(chunk_row_scale_kernel, B, 256, 0, st, rows, mask, mask_ld, off, rscale);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
 ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const int32_t* tgt, float scale,
-                          cudaStream_t st) {
+                          const float* rscale, cudaStream_t st) {
   if (M == 0) return TTT_OK;
   if (V % 8 || (reinterpret_cast<uintptr_t>(logits) & 15)) {
     set_error("dlogits: V must be a multiple of 8 and the logits 16-byte aligned");
@@ -626,7 +653,7 @@ ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const in
   // 256-thread blocks each cover 2048 elements of a row; rows fill the rest of the grid
   const int bx = ceil_div(V / 8, 256);
   const int by = M < 65535 ? M : 65535;
-  launch_pdl(dlogits_kernel, dim3(bx, by), 256, 0, st, M, V, static_cast<bf16*>(logits), lse, tgt, scale);
+  launch_pdl(dlogits_kernel, dim3(bx, by), 256, 0, st, M, V, static_cast<bf16*>(logits), lse, tgt, scale, rscale);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

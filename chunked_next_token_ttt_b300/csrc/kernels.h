@@ -39,15 +39,16 @@ ttt_status launch_rmsnorm_bwd(int stg, int M, int d, const float* x, const float
 // Row-wise cross-entropy of logits [B*rows, V] (leading dim ldl elements).
 // For valid rows: loss -> losses[s * loss_ld + loss_off + j] (if losses != null)
 // and row_loss[m] (if != null); when `grad` the row is overwritten in place by
-// dlogits = (softmax - onehot(target)) * scale.  Invalid rows get dlogits 0.
+// dlogits = (softmax - onehot(target)) * scale (rscale[m] per row when rscale
+// is non-null).  Invalid rows get dlogits 0.
 // ST_F32 / ST_BF16: logits and dlogits in that type.  ST_SPLIT: logits are
 // float (ldl floats per row); dlogits are written inside each row's own bytes
 // as a split pair, hi plane at bf16 offset 0 and lo plane at bf16 offset V of
 // the row (a bf16 matrix with leading dim 2*ldl and lo offset V); V must fit
 // the kernel's shared-memory row buffer (ce_split_max_vocab()).
 ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, long long ldl,
-                     float scale, bool grad, float* losses, long long loss_ld, long long loss_off,
-                     float* row_loss, cudaStream_t st);
+                     float scale, const float* rscale, bool grad, float* losses, long long loss_ld,
+                     long long loss_off, float* row_loss, cudaStream_t st);
 int ce_split_max_vocab();
 
 // Fused cross-entropy after the EPI_LOGITS head GEMM (bf16 operands):
@@ -60,7 +61,12 @@ ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long
 // In place over bf16 logits [M, V] (leading dim V, V % 8 == 0, 16-byte aligned):
 // dlogits = (exp(x - lse[m]) - [v == tgt[m]]) * scale; rows with tgt[m] < 0 get 0.
 ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const int32_t* tgt, float scale,
-                          cudaStream_t st);
+                          const float* rscale, cudaStream_t st);
+// Source Masking: per-row loss scales of one chunk, rscale[s * rows + j] =
+// m / max(1, count of set mask entries of sequence s in the chunk), m =
+// (mask[s * mask_ld + off + j] != 0).
+ttt_status launch_chunk_row_scale(int B, int rows, const uint8_t* mask, long long mask_ld, long long off,
+                                  float* rscale, cudaStream_t st);
 
 // Where the dW GEMMs left their per-tile sums of squares: for GEMM k, the
 // partials of sequence s are partials[off[k] + s * tiles[k] + t], t < tiles[k].
@@ -109,10 +115,12 @@ ttt_status launch_next_token_loss(int B, int V, const float* logits32, const flo
 // Per-token TTT (b = 1) for a network without frozen prefix and one GELU block
 // whose matrices W1 (slot_w1) and W2 (slot_w2) are fast, fp32 storage: one CTA
 // per sequence keeps W1, W2 and U in shared memory and runs tokens 0 .. T-1 of
-// tok[s * tok_ld + .] (forward, loss, backward, clipped step), writing
+// tok[s * tok_ld + .] (forward, loss, backward, clipped step; with mask non-null
+// a token whose mask[s * mask_ld + t] is 0 is scored without a step), writing
 // losses[s * loss_ld + t] and, at the end, the fp32 masters and their copy.
 bool token_steps_supported(int d, int f, int V);
-ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T, const float* E, const float* U,
+ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T, const uint8_t* mask,
+                              long long mask_ld, const float* E, const float* U,
                               float* W32, float* Wop, int slot_w1, int slot_w2, float* losses, long long loss_ld,
                               int d, int f, int V, float eps, float eta, float clip, int* err, cudaStream_t st);
 

@@ -70,7 +70,8 @@ ttt_status ttt_op_cross_entropy(int dtype, int M, int V, void* logits, const int
     cudaMemset(err, 0, 4);
   }
   tv.err = err;
-  return launch_ce(dtype, 1, tv, V, logits, V, scale, grad != 0, losses, 0, 0, nullptr, (cudaStream_t)stream);
+  return launch_ce(dtype, 1, tv, V, logits, V, scale, nullptr, grad != 0, losses, 0, 0, nullptr,
+                   (cudaStream_t)stream);
 }
 
 ttt_status ttt_op_rmsnorm_forward(int dtype, int M, int d, const float* x, float eps, void* y, float* rstd,

@@ -17,6 +17,9 @@
 // 1e-6)) ("Self-Generated Feedback Destabilizes TTT" summary: one clipped step
 // per chunk) is applied to the shared-memory copies without forming dW.
 //
+// With a loss mask, a masked token is scored but takes no step (Source
+// Masking: its chunk of one target has no unmasked target).
+//
 // Shared memory (fp32): W1 [f][d+1], W2 [d][f+1], U [V][d+1] (the +1 pads keep
 // row-wise and column-wise walks free of most bank conflicts) and the token's
 // vectors.  The fp32 masters are read from the arena at the start and written
@@ -37,6 +40,8 @@ struct TokenArgs {
   const int32_t* tok;
   long long tok_ld;
   int T;
+  const uint8_t* mask;  // [B][mask_ld] or null: target t+1 enters the update iff mask[t]
+  long long mask_ld;
   const float* E;       // [V][d]
   const float* U;       // [V][d]
   float* W32;           // arena [slot][B][d*f]
@@ -190,6 +195,8 @@ __global__ void __launch_bounds__(kTokThreads) token_steps_kernel(TokenArgs a) {
     const float lse = mx + logf(se);
     if (tid == 0) a.losses[(long long)s * a.loss_ld + t] = lse - lg[tgt];
     __syncthreads();
+    // Source Masking: a masked target is scored but takes no step (uniform per block)
+    if (a.mask && !a.mask[(long long)s * a.mask_ld + t]) continue;
     // ---- backward (the mean over a one-token chunk is the token itself)
     for (int v = tid; v < V; v += nt) lg[v] = expf(lg[v] - lse) - (v == tgt ? 1.0f : 0.0f);
     __syncthreads();
@@ -267,7 +274,8 @@ bool token_steps_supported(int d, int f, int V) {
   return d >= 1 && f >= 1 && V >= 1 && token_smem_bytes(d, f, V) <= 227 * 1024;
 }
 
-ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T, const float* E, const float* U,
+ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T, const uint8_t* mask,
+                              long long mask_ld, const float* E, const float* U,
                               float* W32, float* Wop, int slot_w1, int slot_w2, float* losses, long long loss_ld,
                               int d, int f, int V, float eps, float eta, float clip, int* err, cudaStream_t st) {
   if (!token_steps_supported(d, f, V)) {
@@ -282,7 +290,8 @@ ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
     smem_set = smem;
   }
-  TokenArgs a{tok, tok_ld, T, E, U, W32, Wop, slot_w1, slot_w2, B, losses, loss_ld, d, f, V, eps, eta, clip, err};
+  TokenArgs a{tok, tok_ld, T, mask, mask_ld, E, U, W32, Wop, slot_w1, slot_w2, B, losses, loss_ld, d, f, V, eps, eta,
+              clip, err};
   launch_pdl(token_steps_kernel, B, kTokThreads, smem, st, a);
   TTT_CHECK_LAUNCH();
   return TTT_OK;

@@ -65,6 +65,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                         ctypes.POINTER(_P)], _I),
         "ttt_destroy": ([_P], _I),
         "ttt_prefill": ([_P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
+        "ttt_prefill_masked": ([_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
         "ttt_decode_step": ([_P, _P, _P, _P, _P], _I),
         "ttt_settle": ([_P, _P, _I, _P, _P, _P], _I),
         "ttt_get_fast_weights": ([_P, _I, _I, _I, _P, _P], _I),
@@ -186,13 +187,21 @@ class Handle:
             pass
 
     # ---------------------------------------------------------------- calls
-    def prefill(self, tokens, losses, p_next=None, settle_q=None, accept=None, A=None, stream=None):
-        """tokens [B, T+1] int32; losses [B, T] float32 out; the rest optional."""
+    def prefill(self, tokens, losses, p_next=None, settle_q=None, accept=None, A=None, stream=None,
+                loss_mask=None):
+        """tokens [B, T+1] int32; losses [B, T] float32 out; the rest optional.
+        loss_mask [B, T] uint8 (Source Masking): only targets whose entry is
+        non-zero enter the updates (every token is still scored)."""
         B, T1 = tokens.shape
         Lq = 0 if settle_q is None else settle_q.shape[-1]
-        _check(self.lib.ttt_prefill(self._h, _ptr(tokens), B, T1 - 1, _ptr(losses), _ptr(p_next),
-                                    _ptr(settle_q), Lq, _ptr(accept), _ptr(A), _stream(stream)),
-               "ttt_prefill")
+        if loss_mask is None:
+            _check(self.lib.ttt_prefill(self._h, _ptr(tokens), B, T1 - 1, _ptr(losses), _ptr(p_next),
+                                        _ptr(settle_q), Lq, _ptr(accept), _ptr(A), _stream(stream)),
+                   "ttt_prefill")
+        else:
+            _check(self.lib.ttt_prefill_masked(self._h, _ptr(tokens), _ptr(loss_mask), B, T1 - 1, _ptr(losses),
+                                               _ptr(p_next), _ptr(settle_q), Lq, _ptr(accept), _ptr(A),
+                                               _stream(stream)), "ttt_prefill_masked")
 
     def decode_step(self, x_new, p_next, loss=None, stream=None):
         _check(self.lib.ttt_decode_step(self._h, _ptr(x_new), _ptr(p_next), _ptr(loss), _stream(stream)),

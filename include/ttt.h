@@ -145,6 +145,19 @@ ttt_status ttt_prefill(ttt_handle* h, const int32_t* tokens, int B, int T,
                        const int32_t* settle_q, int Lq,
                        uint8_t* accept, float* A, ttt_stream stream);
 
+/* ttt_prefill with Source Masking ("Self-Generated Feedback Destabilizes TTT"
+ * summary, Settlement paragraph: Source Masking, which keeps the tokens a
+ * source label marks as generated out of the update).  loss_mask [B, T] uint8
+ * (host or device; NULL = all ones): target x_{t+1} of sequence s enters the
+ * update iff loss_mask[s, t] != 0.  Every token is still scored into losses;
+ * a chunk's TTT loss is the mean over its unmasked targets (1/n sum, n =
+ * their count), and a chunk without any leaves the weights unchanged.  The
+ * trailing T mod b targets and decoded tokens are not masked.  Other
+ * arguments, results and errors as ttt_prefill. */
+ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_t* loss_mask, int B, int T,
+                              float* losses, float* p_next, const int32_t* settle_q, int Lq, uint8_t* accept,
+                              float* A, ttt_stream stream);
+
 /* One decoded token per sequence ("End-to-End TTT" review, 3.2).  Appends the
  * pair (x_prev, x_new); when b pairs are pending it takes one clipped step on
  * them with the weights that scored them.

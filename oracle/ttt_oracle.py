@@ -49,6 +49,14 @@ Readings taken where the pages leave a step open:
       pairs are pending, one (clipped) step is taken on them with the weights
       that scored them; p_next = softmax(f(x_new; W)) uses the weights after
       that step.  Settlement is not applied while decoding.
+  R8  Source Masking (the [SGF] Settlement paragraph compares Settlement with
+      Source Masking, which uses per-token source labels, but gives no
+      formula): a per-token mask marks the targets whose loss enters the
+      update; every token is still scored (prequential losses are unchanged
+      in definition), and a chunk's TTT loss is the mean over its unmasked
+      targets, (1/n) sum_{t: m_t = 1} l_t with n = max(1, sum m_t), so a chunk
+      without any unmasked target leaves W unchanged.  All-ones masks are the
+      unmasked method.
 """
 from __future__ import annotations
 
@@ -204,8 +212,10 @@ def token_losses(net: Net, fast, x_in, targets):
     return cross_entropy(logits, targets)[0]
 
 
-def chunk_loss_and_grads(net: Net, fast, h_in, targets):
-    """Losses of one chunk and the gradient of their mean (eq. (5)'s (1/b) sum)."""
+def chunk_loss_and_grads(net: Net, fast, h_in, targets, weights=None):
+    """Losses of one chunk and the gradient of their mean (eq. (5)'s (1/b) sum);
+    with `weights` [b], the gradient of sum_t weights[t] * l_t instead (the
+    Source Masking reading R8 passes mask / max(1, sum(mask)))."""
     b = len(targets)
     caches = []
     h = h_in
@@ -217,7 +227,10 @@ def chunk_loss_and_grads(net: Net, fast, h_in, targets):
     losses, p = cross_entropy(logits, targets)
     dlogits = p
     dlogits[np.arange(b), targets] -= 1.0
-    dlogits /= b
+    if weights is None:
+        dlogits /= b
+    else:
+        dlogits *= np.asarray(weights, dtype=np.float64)[:, None]
     dh = rmsnorm_backward(h, r, dlogits @ net.U)
     grads = [None] * len(fast)
     for l in range(len(fast) - 1, -1, -1):
@@ -286,9 +299,17 @@ def settle(net, st: SeqState, q):
     return A, accept
 
 
-def _step(net, st: SeqState, x_in, tgt, eta, clip):
+def mask_weights(mask):
+    """Source Masking (R8): the chunk's TTT loss is the mean over the targets
+    whose mask is 1; a chunk without any contributes no gradient."""
+    m = np.asarray(mask, dtype=np.float64)
+    return m / max(1.0, float(m.sum()))
+
+
+def _step(net, st: SeqState, x_in, tgt, eta, clip, mask=None):
     h_in = frozen_prefix(net, x_in)
-    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt)
+    w = None if mask is None else mask_weights(mask)
+    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt, w)
     s, norm = clip_scale(grads, clip)
     st.W = sgd_step(st.W, grads, eta, s)
     st.chunks_done += 1
@@ -298,8 +319,9 @@ def _step(net, st: SeqState, x_in, tgt, eta, clip):
 
 
 def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=None,
-                     snapshots=False):
-    """Run one sequence's prefill.  tokens: [T+1] with tokens[0] = BOS."""
+                     snapshots=False, loss_mask=None):
+    """Run one sequence's prefill.  tokens: [T+1] with tokens[0] = BOS;
+    loss_mask [T] (optional, R8): target t+1 enters the update iff mask[t]."""
     tokens = np.asarray(tokens, dtype=np.int64)
     T = len(tokens) - 1
     n_full, rem = divmod(T, b)
@@ -312,7 +334,7 @@ def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=No
     for i in range(n_full):
         lo = i * b
         losses[lo:lo + b] = _step(net, st, tokens[lo:lo + b], tokens[lo + 1:lo + b + 1],
-                                  eta, clip)
+                                  eta, clip, None if loss_mask is None else loss_mask[lo:lo + b])
         if settle_every and (i + 1) % settle_every == 0:
             e = (i + 1) // settle_every - 1
             A, accept = settle(net, st, settle_q[e])
@@ -332,10 +354,11 @@ def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=No
 
 
 def prefill(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=None, snapshots=False,
-            seqs=None):
+            seqs=None, loss_mask=None):
     """Batched prefill: every sequence runs independently (reading R1).
 
-    tokens [B, T+1]; settle_q [E, B, Lq] when settle_every > 0.  `seqs`
+    tokens [B, T+1]; settle_q [E, B, Lq] when settle_every > 0; loss_mask
+    [B, T] (optional, R8) selects the targets whose loss enters the update.  `seqs`
     restricts the run to some sequences (the others are left zero / None).
     Returns losses [B, T], per-sequence final fast weights, p_next [B, V],
     A and accept [E, B].
@@ -351,7 +374,7 @@ def prefill(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=None, snaps
     for s in seqs:
         r = prefill_sequence(net, eta, clip, b, tokens[s], settle_every,
                              None if settle_q is None else np.asarray(settle_q)[:, s],
-                             snapshots)
+                             snapshots, None if loss_mask is None else np.asarray(loss_mask)[s])
         out["losses"][s] = r["losses"]
         out["W"][s] = r["state"].W
         out["p_next"][s] = r["p_next"]

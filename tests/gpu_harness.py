@@ -26,15 +26,15 @@ def oracle_net(wl, inp):
     return oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
 
 
-def run_oracle(wl, inp, seqs=None, tokens=None, q=None):
+def run_oracle(wl, inp, seqs=None, tokens=None, q=None, loss_mask=None):
     net = oracle_net(wl, inp)
     tok = inp["tokens"] if tokens is None else tokens
     sq = inp["settle_q"] if q is None else q
     return oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok, wl.settle_every,
-                          sq if wl.settle_every else None, seqs=seqs)
+                          sq if wl.settle_every else None, seqs=seqs, loss_mask=loss_mask)
 
 
-def run_gpu(wl, inp, device=True, tokens=None, q=None, handle=None):
+def run_gpu(wl, inp, device=True, tokens=None, q=None, handle=None, loss_mask=None):
     tok = inp["tokens"] if tokens is None else tokens
     sq = inp["settle_q"] if q is None else q
     B, T1 = tok.shape
@@ -47,7 +47,8 @@ def run_gpu(wl, inp, device=True, tokens=None, q=None, handle=None):
         qd = torch.from_numpy(np.ascontiguousarray(sq[:n_ev])).cuda() if n_ev else None
         A = torch.empty((max(n_ev, 1), B), dtype=torch.float32, device="cuda")
         acc = torch.empty((max(n_ev, 1), B), dtype=torch.uint8, device="cuda")
-        h.prefill(t, losses, p, qd, acc if n_ev else None, A if n_ev else None)
+        md = None if loss_mask is None else torch.from_numpy(np.ascontiguousarray(loss_mask, dtype=np.uint8)).cuda()
+        h.prefill(t, losses, p, qd, acc if n_ev else None, A if n_ev else None, loss_mask=md)
         torch.cuda.synchronize()
         out = {"losses": losses.cpu().numpy().astype(np.float64), "p_next": p.cpu().numpy(),
                "A": A.cpu().numpy()[:n_ev], "accept": acc.cpu().numpy()[:n_ev].astype(bool)}
@@ -58,7 +59,8 @@ def run_gpu(wl, inp, device=True, tokens=None, q=None, handle=None):
         acc = np.empty((max(n_ev, 1), B), dtype=np.uint8)
         h.prefill(np.ascontiguousarray(tok), losses, p,
                   np.ascontiguousarray(sq[:n_ev]) if n_ev else None,
-                  acc if n_ev else None, A if n_ev else None)
+                  acc if n_ev else None, A if n_ev else None,
+                  loss_mask=None if loss_mask is None else np.ascontiguousarray(loss_mask, dtype=np.uint8))
         out = {"losses": losses.astype(np.float64), "p_next": p, "A": A[:n_ev],
                "accept": acc[:n_ev].astype(bool)}
     out["W"] = [h.fast_weights(s) for s in range(B)]

@@ -226,6 +226,48 @@ def test_settle_entry_point_after_prefill():
         assert rel <= 3e-2, f"seq {s}: W after settle {rel:.3e}"
 
 
+def _random_mask(B, T, b, seed):
+    """Random per-token mask with a fully masked chunk and a fully unmasked one."""
+    rng = np.random.default_rng(seed)
+    m = (rng.random((B, T)) < 0.6).astype(np.uint8)
+    m[0, :b] = 0
+    m[-1, b:2 * b] = 1
+    return m
+
+
+@pytest.mark.parametrize("case", ["bf16_gelu_fused_ce", "bf16_swiglu_hoisted", "fp32_split_ce", "fp32_rows",
+                                  "fp32_rows_host", "b1_persistent", "b1_general"])
+def test_source_masking_against_the_oracle(monkeypatch, case):
+    """Source Masking (a per-token mask on the chunk loss): every CE path of the
+    GPU (fused dlogits, bf16x3 row CE, fp32 row CE, the per-token kernel) and
+    the hoisted prefix, against the oracle's masked loop; a fully masked chunk
+    leaves the weights untouched, every token is still scored."""
+    if case == "bf16_gelu_fused_ce":
+        wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1024, chunk=128, B=3, T=3 * 128, n_prefix=1)
+    elif case == "bf16_swiglu_hoisted":
+        wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=64, B=2, T=3 * 64 + 9, n_prefix=1)
+    elif case == "fp32_split_ce":
+        wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=128, B=2, T=3 * 128)
+    elif case.startswith("fp32_rows"):
+        wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=40, B=3, T=130, n_prefix=1)
+    else:
+        monkeypatch.setenv("TTT_TOKEN_KERNEL", "1" if case == "b1_persistent" else "0")
+        wl = C.TOY_BIGRAM.replace(B=2, T=200, clip=0.5)
+    inp = make(wl)
+    mask = _random_mask(wl.B, wl.T, wl.chunk, seed=len(case) * 7 + wl.seed_id)
+    gpu = run_gpu(wl, inp, device=not case.endswith("_host"), loss_mask=mask)
+    ref = run_oracle(wl, inp, loss_mask=mask)
+    compare(wl, gpu, ref)
+    # The GPU's weights sit much nearer the masked trajectory than the unmasked one.
+    plain = run_oracle(wl, inp)
+    for s in range(wl.B):
+        for g, r, u in zip(gpu["W"][s], ref["W"][s], plain["W"][s]):
+            for k in wl.fast_mats:
+                d_masked = np.linalg.norm(g[k] - r[k])
+                d_plain = np.linalg.norm(g[k] - u[k])
+                assert d_masked < 0.5 * d_plain, (s, k, d_masked, d_plain)
+
+
 def test_host_and_device_buffers_agree():
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=32, B=2, T=100, n_prefix=1)
     inp = make(wl)

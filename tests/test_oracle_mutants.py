@@ -37,8 +37,8 @@ MUTANTS = {
         "losses = lse - logits[np.arange(len(targets)), targets]",
         "losses = lse - logits[np.arange(len(targets)), (targets + 1) % logits.shape[1]]"),
     "losses scored after the update": (
-        "    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt)\n    s, norm = clip_scale(grads, clip)\n    st.W = sgd_step(st.W, grads, eta, s)\n",
-        "    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt)\n    s, norm = clip_scale(grads, clip)\n    st.W = sgd_step(st.W, grads, eta, s)\n    losses = token_losses(net, st.W, x_in, tgt)\n"),
+        "    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt, w)\n    s, norm = clip_scale(grads, clip)\n    st.W = sgd_step(st.W, grads, eta, s)\n",
+        "    losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt, w)\n    s, norm = clip_scale(grads, clip)\n    st.W = sgd_step(st.W, grads, eta, s)\n    losses = token_losses(net, st.W, x_in, tgt)\n"),
     "targets not shifted by one": (
         "tokens[lo:lo + b], tokens[lo + 1:lo + b + 1],", "tokens[lo:lo + b], tokens[lo:lo + b],"),
     "clip scale inverted": (
@@ -51,6 +51,10 @@ MUTANTS = {
     "SwiGLU up-gradient uses g": ("du = da * silu(cache[\"g\"])", "du = da * cache[\"g\"]"),
     "SwiGLU gate gradient drops silu'": (
         'dg = da * cache["u"] * silu_grad(cache["g"])', 'dg = da * cache["u"] * silu(cache["g"])'),
+    "masked chunk mean divides by the chunk length": (
+        "return m / max(1.0, float(m.sum()))", "return m / len(m)"),
+    "mask ignored in the update": (
+        "w = None if mask is None else mask_weights(mask)", "w = None"),
     "p_next with the initial weights": (
         "p_next = softmax_next(net, st.W, st.x_last)", "p_next = softmax_next(net, net.fast0, st.x_last)"),
 }
@@ -74,6 +78,10 @@ PINS = [
     ("test_settlement_two_token_case_by_hand", ()),
     ("test_forward_by_hand_nonsquare", ()),
     ("test_decoding_a_full_chunk_equals_a_longer_prefill", ()),
+    ("test_all_ones_mask_is_the_unmasked_method", ()),
+    ("test_all_zeros_mask_never_updates_and_scores_like_eq4", ()),
+    ("test_single_unmasked_target_is_that_tokens_own_gradient", ()),
+    ("test_masked_chunk_gradient_matches_central_differences", ()),
 ]
 
 

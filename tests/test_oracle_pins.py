@@ -380,3 +380,68 @@ def test_forward_by_hand_nonsquare():
     lse = math.log(np.sum(np.exp(logits)))
     got = O.token_losses(net, net.fast0, np.array([0, 0, 0]), np.array([0, 1, 2]))
     np.testing.assert_allclose(got, lse - logits, rtol=1e-14)
+
+
+# ------------------------------------------------------------------ Source Masking (reading R8)
+def test_all_ones_mask_is_the_unmasked_method():
+    net = rand_net("gelu", seed=80)
+    tok = rand_tokens(16, 2, 13, seed=81)
+    a = O.prefill(net, 0.2, 0.5, 4, tok)
+    b = O.prefill(net, 0.2, 0.5, 4, tok, loss_mask=np.ones((2, 13), dtype=np.uint8))
+    np.testing.assert_array_equal(a["losses"], b["losses"])
+    for s in range(2):
+        assert O.weights_rel_frobenius(b["W"][s], a["W"][s], net.fast_mats) == 0.0
+
+
+def test_all_zeros_mask_never_updates_and_scores_like_eq4():
+    """No target enters any update: W stays W_0 and every loss is the static
+    (eq. (4)) loss, although every token is still scored."""
+    net = rand_net("swiglu", n_fast=1, fast_mats=("Wd",), seed=82)
+    tok = rand_tokens(16, 2, 12, seed=83)
+    out = O.prefill(net, 0.3, 0.0, 4, tok, loss_mask=np.zeros((2, 12), dtype=np.uint8))
+    for s in range(2):
+        np.testing.assert_allclose(out["losses"][s], O.static_losses(net, tok[s]), rtol=0, atol=1e-13)
+        assert O.weights_rel_frobenius(out["W"][s], net.fast0, net.fast_mats) == 0.0
+
+
+def test_single_unmasked_target_is_that_tokens_own_gradient():
+    """Only target j of a chunk unmasked: the chunk gradient equals the
+    gradient of token j alone (a one-token chunk, eq. (2)); tokens do not mix
+    inside the MLP-only network."""
+    net = rand_net("gelu", n_fast=2, seed=84)
+    tok = rand_tokens(16, 1, 6, seed=85)[0]
+    x_in, tgt = tok[:-1], tok[1:]
+    j = 3
+    mask = np.zeros(6)
+    mask[j] = 1
+    _, g = O.chunk_loss_and_grads(net, net.fast0, O.frozen_prefix(net, x_in), tgt, O.mask_weights(mask))
+    _, g1 = O.chunk_loss_and_grads(net, net.fast0, O.frozen_prefix(net, x_in[j:j + 1]), tgt[j:j + 1])
+    for l in range(2):
+        for k in net.fast_mats:
+            np.testing.assert_allclose(g[l][k], g1[l][k], rtol=1e-12, atol=1e-15)
+
+
+def test_masked_chunk_gradient_matches_central_differences():
+    """The gradient of (1/n) sum_{m_t = 1} l_t, every fast matrix, rel <= 1e-6."""
+    net = rand_net("gelu", d=8, f=16, V=16, n_prefix=1, n_fast=1, seed=86)
+    tok = rand_tokens(16, 1, 5, seed=87)[0]
+    x_in, tgt = tok[:-1], tok[1:]
+    mask = np.array([1, 0, 1, 1, 0])
+    w = O.mask_weights(mask)
+    fast = copy.deepcopy(net.fast0)
+    _, grads = O.chunk_loss_and_grads(net, fast, O.frozen_prefix(net, x_in), tgt, w)
+    obj = lambda: float(np.sum(w * O.token_losses(net, fast, x_in, tgt)))
+    h = 1e-5
+    for k in net.fast_mats:
+        fd = np.zeros_like(fast[0][k])
+        for idx in np.ndindex(fast[0][k].shape):
+            orig = fast[0][k][idx]
+            fast[0][k][idx] = orig + h
+            lp = obj()
+            fast[0][k][idx] = orig - h
+            lm = obj()
+            fast[0][k][idx] = orig
+            fd[idx] = (lp - lm) / (2 * h)
+        rel = np.linalg.norm(fd - grads[0][k]) / np.linalg.norm(grads[0][k])
+        assert rel <= 1e-6, (k, rel)
+    assert abs(w.sum() - 1.0) < 1e-15
