@@ -57,6 +57,11 @@ Readings taken where the pages leave a step open:
       targets, (1/n) sum_{t: m_t = 1} l_t with n = max(1, sum m_t), so a chunk
       without any unmasked target leaves W unchanged.  All-ones masks are the
       unmasked method.
+  R9  Periodic reset (the [SGF] limits paragraph reports an 8-chunk reset as a
+      mitigation, without a formula): after every `reset_every`-th chunk
+      update of a sequence (prefill and decoding counted together) its fast
+      weights return to W_0.  Reset and Settlement are alternatives, never
+      combined in one run.
 """
 from __future__ import annotations
 
@@ -285,6 +290,7 @@ class SeqState:
     chunks_done: int = 0
     norms: list = field(default_factory=list)
     scales: list = field(default_factory=list)
+    reset_every: int = 0
 
 
 def settle(net, st: SeqState, q):
@@ -315,19 +321,24 @@ def _step(net, st: SeqState, x_in, tgt, eta, clip, mask=None):
     st.chunks_done += 1
     st.norms.append(norm)
     st.scales.append(s)
+    if st.reset_every and st.chunks_done % st.reset_every == 0:
+        st.W = copy.deepcopy(net.fast0)       # R9
     return losses
 
 
 def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=None,
-                     snapshots=False, loss_mask=None):
+                     snapshots=False, loss_mask=None, reset_every=0):
     """Run one sequence's prefill.  tokens: [T+1] with tokens[0] = BOS;
-    loss_mask [T] (optional, R8): target t+1 enters the update iff mask[t]."""
+    loss_mask [T] (optional, R8): target t+1 enters the update iff mask[t];
+    reset_every (R9): chunk updates between returns to W_0, 0 = never."""
     tokens = np.asarray(tokens, dtype=np.int64)
     T = len(tokens) - 1
     n_full, rem = divmod(T, b)
+    if settle_every and reset_every:
+        raise ValueError("reset and Settlement are alternatives (R9)")
     st = SeqState(W=copy.deepcopy(net.fast0),
                   Wc=copy.deepcopy(net.fast0) if settle_every else None,
-                  x_last=int(tokens[-1]))
+                  x_last=int(tokens[-1]), reset_every=reset_every)
     losses = np.zeros(T)
     snaps = [copy.deepcopy(st.W)] if snapshots else None
     A_list, acc_list = [], []
@@ -354,11 +365,12 @@ def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=No
 
 
 def prefill(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=None, snapshots=False,
-            seqs=None, loss_mask=None):
+            seqs=None, loss_mask=None, reset_every=0):
     """Batched prefill: every sequence runs independently (reading R1).
 
     tokens [B, T+1]; settle_q [E, B, Lq] when settle_every > 0; loss_mask
-    [B, T] (optional, R8) selects the targets whose loss enters the update.  `seqs`
+    [B, T] (optional, R8) selects the targets whose loss enters the update;
+    reset_every (R9) returns the fast weights to W_0 periodically.  `seqs`
     restricts the run to some sequences (the others are left zero / None).
     Returns losses [B, T], per-sequence final fast weights, p_next [B, V],
     A and accept [E, B].
@@ -374,7 +386,8 @@ def prefill(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=None, snaps
     for s in seqs:
         r = prefill_sequence(net, eta, clip, b, tokens[s], settle_every,
                              None if settle_q is None else np.asarray(settle_q)[:, s],
-                             snapshots, None if loss_mask is None else np.asarray(loss_mask)[s])
+                             snapshots, None if loss_mask is None else np.asarray(loss_mask)[s],
+                             reset_every)
         out["losses"][s] = r["losses"]
         out["W"][s] = r["state"].W
         out["p_next"][s] = r["p_next"]
@@ -387,7 +400,8 @@ def prefill(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=None, snaps
 
 
 def decode_step(net: Net, st: SeqState, x_new, eta, clip, b):
-    """One decoded token for one sequence (reading R7).
+    """One decoded token for one sequence (reading R7; a reset of R9 applies
+    to the steps taken here as well).
 
     Returns (l of the new token under the weights that scored it, p_next).
     """

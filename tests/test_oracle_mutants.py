@@ -55,6 +55,11 @@ MUTANTS = {
         "return m / max(1.0, float(m.sum()))", "return m / len(m)"),
     "mask ignored in the update": (
         "w = None if mask is None else mask_weights(mask)", "w = None"),
+    "reset one chunk late": (
+        "if st.reset_every and st.chunks_done % st.reset_every == 0:",
+        "if st.reset_every and (st.chunks_done - 1) % st.reset_every == 0 and st.chunks_done > 1:"),
+    "reset keeps the current weights": (
+        "st.W = copy.deepcopy(net.fast0)       # R9", "st.W = copy.deepcopy(st.W)       # R9"),
     "p_next with the initial weights": (
         "p_next = softmax_next(net, st.W, st.x_last)", "p_next = softmax_next(net, net.fast0, st.x_last)"),
 }
@@ -78,6 +83,9 @@ PINS = [
     ("test_settlement_two_token_case_by_hand", ()),
     ("test_forward_by_hand_nonsquare", ()),
     ("test_decoding_a_full_chunk_equals_a_longer_prefill", ()),
+    ("test_reset_every_chunk_scores_like_eq4_and_ends_at_w0", ()),
+    ("test_reset_splits_the_stream_into_independent_runs", ()),
+    ("test_reset_counts_decoded_chunks_too", ()),
     ("test_all_ones_mask_is_the_unmasked_method", ()),
     ("test_all_zeros_mask_never_updates_and_scores_like_eq4", ()),
     ("test_single_unmasked_target_is_that_tokens_own_gradient", ()),

@@ -445,3 +445,68 @@ def test_masked_chunk_gradient_matches_central_differences():
         rel = np.linalg.norm(fd - grads[0][k]) / np.linalg.norm(grads[0][k])
         assert rel <= 1e-6, (k, rel)
     assert abs(w.sum() - 1.0) < 1e-15
+
+
+# ------------------------------------------------------------------ periodic reset (R9)
+def test_reset_every_chunk_scores_like_eq4_and_ends_at_w0():
+    """A reset after every update: each chunk is scored by W_0, so the losses
+    are the static (eq. (4)) losses, and the run ends on W_0."""
+    net = rand_net("gelu", seed=90)
+    tok = rand_tokens(16, 2, 12, seed=91)
+    out = O.prefill(net, 0.4, 0.0, 3, tok, reset_every=1)
+    for s in range(2):
+        np.testing.assert_allclose(out["losses"][s], O.static_losses(net, tok[s]), rtol=0, atol=1e-13)
+        assert O.weights_rel_frobenius(out["W"][s], net.fast0, net.fast_mats) == 0.0
+
+
+def test_reset_splits_the_stream_into_independent_runs():
+    """reset_every = k: every k-chunk segment is a fresh run from W_0 on that
+    segment's tokens (the MLP-only network sees no earlier context), so the
+    losses and the weights equal those of independent prefills."""
+    net = rand_net("swiglu", n_fast=1, fast_mats=("Wd",), seed=92)
+    b, k, eta, c = 2, 3, 0.5, 0.8
+    T = 2 * k * b + 2 * b + 1                   # two whole segments, a partial one, a ragged tail
+    tok = rand_tokens(16, 1, T, seed=93)
+    out = O.prefill(net, eta, c, b, tok, reset_every=k)
+    seg = k * b
+    for m, lo in enumerate(range(0, T, seg)):
+        hi = min(lo + seg, T)
+        part = O.prefill(net, eta, c, b, tok[:, lo:hi + 1])
+        np.testing.assert_allclose(out["losses"][0, lo:hi], part["losses"][0], rtol=0, atol=1e-13)
+    # the run ends inside the third segment: its weights are that segment's own run
+    assert O.weights_rel_frobenius(out["W"][0], part["W"][0], net.fast_mats) < 1e-14
+    assert out["states"][0].chunks_done == T // b
+
+
+def test_reset_beyond_the_stream_is_no_reset():
+    net = rand_net("gelu", seed=94)
+    tok = rand_tokens(16, 1, 12, seed=95)
+    a = O.prefill(net, 0.3, 0.5, 4, tok)
+    r = O.prefill(net, 0.3, 0.5, 4, tok, reset_every=4)
+    np.testing.assert_array_equal(a["losses"], r["losses"])
+    assert O.weights_rel_frobenius(r["W"][0], a["W"][0], net.fast_mats) == 0.0
+
+
+def test_reset_counts_decoded_chunks_too():
+    """Decoding's steps advance the same counter: a prefill of one chunk and a
+    decoded second chunk with reset_every = 2 land back on W_0, and the next
+    decoded token is scored like the static model."""
+    net = rand_net("gelu", seed=96)
+    b = 3
+    tok = rand_tokens(16, 1, 3 * b + 1, seed=97)
+    out = O.prefill(net, 0.5, 0.0, b, tok[:, :b + 1], reset_every=2)
+    st = out["states"][0]
+    assert O.weights_rel_frobenius(st.W, net.fast0, net.fast_mats) > 0.0
+    for t in range(b + 1, 2 * b + 1):
+        O.decode_step(net, st, tok[0, t], 0.5, 0.0, b)
+    assert st.chunks_done == 2
+    assert O.weights_rel_frobenius(st.W, net.fast0, net.fast_mats) == 0.0
+    l, _ = O.decode_step(net, st, tok[0, 2 * b + 1], 0.5, 0.0, b)
+    np.testing.assert_allclose(l, O.static_losses(net, tok[0, 2 * b:2 * b + 2])[0], rtol=0, atol=1e-13)
+
+
+def test_reset_and_settlement_are_exclusive():
+    net = rand_net("gelu", seed=98)
+    tok = rand_tokens(16, 1, 8, seed=99)
+    with pytest.raises(ValueError):
+        O.prefill(net, 0.3, 0.0, 2, tok, settle_every=2, settle_q=np.zeros((2, 1, 4), np.int64), reset_every=2)
