@@ -403,6 +403,10 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
                                   h->hp.clip, h->hp.eta, h->scale, h->gnorm, h->flag, st);
   }));
   h->chunks_done++;
+  if (h->hp.reset_every > 0 && h->chunks_done % h->hp.reset_every == 0)
+    TTT_TRY(run(h, K_OTHER, st, 1, [&] {
+      return launch_broadcast_w0(stg, h->nslots, B, h->n, h->W0, h->W32, h->Wop.p, h->Wop.lo, st);
+    }));
   return TTT_OK;
 }
 
@@ -644,6 +648,8 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if (D.dtype != TTT_DTYPE_FP32 && D.dtype != TTT_DTYPE_BF16) return fail(TTT_ERR_BAD_ARG, "bad dtype");
   if (hp->chunk < 1 || hp->max_batch < 1 || hp->settle_every < 0 || hp->settle_len < 0 || hp->clip < 0.0f)
     return fail(TTT_ERR_BAD_ARG, "bad hparams");
+  if (hp->reset_every < 0 || (hp->reset_every > 0 && hp->settle_every > 0))
+    return fail(TTT_ERR_BAD_ARG, "reset_every must be >= 0 and is not combined with settle_every");
   if (hp->settle_every > 0 && hp->settle_len < 2)
     return fail(TTT_ERR_BAD_ARG, "settle_len must be >= 2 when settle_every > 0");
   if (D.block_kind == TTT_BLOCK_GELU && D.fast_mask != (TTT_FAST_W1 | TTT_FAST_W2))
@@ -891,6 +897,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   const char* env_tok = getenv("TTT_TOKEN_KERNEL");
   const bool token_path = b == 1 && h->dm.n_prefix == 0 && h->dm.n_fast == 1 &&
                           h->dm.block_kind == TTT_BLOCK_GELU && h->stg == ST_F32 && h->hp.settle_every == 0 &&
+                          h->hp.reset_every == 0 &&
                           token_steps_supported(h->d, h->f, h->V) && !(env_tok && std::string(env_tok) == "0");
   if (token_path && n_full > 0) {
     TTT_TRY(run(h, K_TOKEN, st, 1, [&] {

@@ -38,7 +38,8 @@ class Dims(ctypes.Structure):
 
 class HParams(ctypes.Structure):
     _fields_ = [("eta", ctypes.c_float), ("clip", ctypes.c_float), ("chunk", ctypes.c_int),
-                ("settle_every", ctypes.c_int), ("max_batch", ctypes.c_int), ("settle_len", ctypes.c_int)]
+                ("settle_every", ctypes.c_int), ("max_batch", ctypes.c_int), ("settle_len", ctypes.c_int),
+                ("reset_every", ctypes.c_int)]
 
 
 class Weights(ctypes.Structure):
@@ -131,7 +132,7 @@ class Handle:
     """One libttt handle: a network, its TTT hyper-parameters and B sequences."""
 
     def __init__(self, *, d, d_ff, vocab, n_prefix, n_fast, block, fast_mats, dtype, eta, clip, chunk,
-                 B, weights, settle_every=0, settle_len=0, rms_eps=1e-6):
+                 B, weights, settle_every=0, settle_len=0, rms_eps=1e-6, reset_every=0):
         self.lib = load_library()
         self.block = block
         self.mats = MATS[block]
@@ -142,7 +143,7 @@ class Handle:
         for m in fast_mats:
             mask |= FAST_BIT[m]
         self._dims = Dims(d, d_ff, vocab, n_prefix, n_fast, BLOCK[block], mask, DTYPE[dtype], rms_eps)
-        self._hp = HParams(eta, clip, chunk, settle_every, B, settle_len)
+        self._hp = HParams(eta, clip, chunk, settle_every, B, settle_len, reset_every)
         keep = []
 
         def f32(a):
@@ -173,7 +174,8 @@ class Handle:
         return cls(d=wl.d, d_ff=wl.d_ff, vocab=wl.vocab, n_prefix=wl.n_prefix, n_fast=wl.n_fast,
                    block=wl.block, fast_mats=wl.fast_mats, dtype=wl.dtype, eta=wl.eta, clip=wl.clip,
                    chunk=wl.chunk, B=wl.B if B is None else B, weights=weights,
-                   settle_every=wl.settle_every, settle_len=wl.settle_len, rms_eps=wl.rms_eps)
+                   settle_every=wl.settle_every, settle_len=wl.settle_len, rms_eps=wl.rms_eps,
+                   reset_every=wl.reset_every)
 
     def close(self):
         if getattr(self, "_h", None):

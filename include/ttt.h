@@ -102,6 +102,12 @@ typedef struct {
   int settle_every;   /* chunks between Settlement events in prefill; 0 = off */
   int max_batch;      /* B, sequences; fixed for the handle's life             */
   int settle_len;     /* Lq, tokens per held-out chunk (0 when unused)        */
+  int reset_every;    /* periodic reset ("Self-Generated Feedback Destabilizes
+                         TTT" summary, limits paragraph: the 8-chunk reset):
+                         after every reset_every-th chunk update, prefill and
+                         decoding counted together, the fast weights of every
+                         sequence return to W_0.  0 = off; > 0 requires
+                         settle_every == 0 (the two are alternatives)         */
 } ttt_hparams;
 
 /* Initial weights, float32 values (host or device).  The library copies them

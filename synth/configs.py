@@ -35,6 +35,7 @@ class Workload:
     chain_alpha: float      # Dirichlet concentration of the successor weights
     settle_every: int = 0   # chunks between Settlement events, 0 = off
     settle_len: int = 0     # tokens of each held-out chunk q
+    reset_every: int = 0    # chunk updates between resets of the fast weights to W_0, 0 = off
     rms_eps: float = 1e-6
     uniform_mix: float = 0.05
     init_std: float = 0.02

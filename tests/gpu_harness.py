@@ -31,7 +31,8 @@ def run_oracle(wl, inp, seqs=None, tokens=None, q=None, loss_mask=None):
     tok = inp["tokens"] if tokens is None else tokens
     sq = inp["settle_q"] if q is None else q
     return oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok, wl.settle_every,
-                          sq if wl.settle_every else None, seqs=seqs, loss_mask=loss_mask)
+                          sq if wl.settle_every else None, seqs=seqs, loss_mask=loss_mask,
+                          reset_every=wl.reset_every)
 
 
 def run_gpu(wl, inp, device=True, tokens=None, q=None, handle=None, loss_mask=None):

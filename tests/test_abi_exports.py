@@ -62,3 +62,15 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             ttt.load_library(str(tmp_path / "missing.so"))
         finally:
             ttt._lib = ttt._lib_saved
+
+
+def test_reset_with_settlement_is_rejected_before_any_cuda_call():
+    """The periodic reset and Settlement are alternatives: ttt_create refuses
+    the pair with BAD_ARG during validation, which runs without a GPU."""
+    import synth
+    from synth import configs as C
+    from chunked_next_token_ttt_b300 import Handle, TTTError
+    wl = C.SETTLE_760M.replace(d=16, d_ff=32, vocab=64, n_prefix=1, n_fast=1, B=2, reset_every=8)
+    with pytest.raises(TTTError) as e:
+        Handle.from_workload(wl, synth.make_weights(wl))
+    assert e.value.status == 1

@@ -268,6 +268,58 @@ def test_source_masking_against_the_oracle(monkeypatch, case):
                 assert d_masked < 0.5 * d_plain, (s, k, d_masked, d_plain)
 
 
+@pytest.mark.parametrize("case", ["fp32_split_ce", "bf16_gelu_hoisted", "bf16_swiglu", "b1_general"])
+def test_periodic_reset_against_the_oracle(case):
+    """The 8-chunk-reset mitigation at reset periods that fall inside hoisted
+    chunk groups, before a ragged tail, and on the b = 1 path."""
+    if case == "fp32_split_ce":
+        wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=7 * 64 + 5, reset_every=2)
+    elif case == "bf16_gelu_hoisted":
+        wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1024, chunk=64, B=3, T=9 * 64, n_prefix=1, reset_every=4,
+                                eta=0.3)
+    elif case == "bf16_swiglu":
+        wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=32, B=2, T=6 * 32, n_prefix=1, reset_every=3,
+                                  eta=0.5)
+    else:
+        wl = C.TOY_BIGRAM.replace(B=2, T=150, reset_every=8)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+    if wl.n_chunks % wl.reset_every == 0:       # the run ends on a reset: W_0 exactly
+        for s in range(wl.B):
+            for l, blk in enumerate(gpu["W"][s]):
+                for k in wl.fast_mats:
+                    np.testing.assert_array_equal(blk[k], np.float32(inp["weights"]["fast"][l][k]))
+
+
+def test_periodic_reset_counts_decoded_chunks():
+    """A reset period that ends inside decoding: the decoded chunk's step is
+    followed by the reset, and decoding goes on from W_0 like the oracle."""
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=8, B=2, T=3 * 8 + 3, n_prefix=1,
+                                reset_every=4, eta=0.5)
+    inp = make(wl)
+    extra = 14
+    long_tok = synth.sample_stream(inp["chain"], wl.seed_id, wl.B, wl.T + extra)
+    tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
+    gpu = run_gpu(wl, inp, tokens=tok)
+    h = gpu["handle"]
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok, reset_every=wl.reset_every)
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
+    for t in range(wl.T + 1, wl.T + extra + 1):
+        h.decode_step(torch.from_numpy(long_tok[:, t].copy()).cuda(), p, loss)
+        torch.cuda.synchronize()
+        for s in range(wl.B):
+            l_ref, p_ref = oracle.decode_step(net, ref["states"][s], long_tok[s, t], wl.eta, wl.clip, wl.chunk)
+            assert abs(float(loss[s]) - l_ref) <= TOL["fp32"]["loss_max"]
+            np.testing.assert_allclose(p[s].cpu().numpy(), p_ref, atol=1e-5)
+    assert ref["states"][0].chunks_done == 5
+    for s in range(wl.B):
+        assert oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats) <= 1e-4
+
+
 def test_host_and_device_buffers_agree():
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=32, B=2, T=100, n_prefix=1)
     inp = make(wl)
