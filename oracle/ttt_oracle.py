@@ -62,6 +62,13 @@ Readings taken where the pages leave a step open:
       update of a sequence (prefill and decoding counted together) its fast
       weights return to W_0.  Reset and Settlement are alternatives, never
       combined in one run.
+  R10 Two MLPs per updated block ([E2E] 3.1, "Two MLP layers per block": a
+      static MLP is added to every block that TTT updates, to keep what
+      pre-training stored): a fast block is two residual sublayers, the
+      frozen MLP first and the fast MLP second, h <- h + MLP_s(h) then
+      h <- h + MLP_f(h), both of the block's kind and widths.  The page does
+      not give the order; static-first is this reading.  Gradients reach
+      earlier fast blocks through the later static MLPs.
 """
 from __future__ import annotations
 
@@ -181,14 +188,17 @@ class Net:
     prefix: list
     fast0: list               # per fast block: dict of all its matrices
     fast_mats: tuple          # which matrices of a fast block are fast
+    static: list | None = None  # per fast block: its frozen MLP (R10), or None
 
     @staticmethod
     def from_weights(w: dict, kind: str, fast_mats, eps: float) -> "Net":
         f64 = lambda a: np.asarray(a, dtype=np.float64)
+        st = w.get("static")
         return Net(kind=kind, eps=eps, E=np.asarray(w["E"]), U=f64(w["U"]),
                    prefix=[{k: f64(v) for k, v in b.items()} for b in w["prefix"]],
                    fast0=[{k: f64(v) for k, v in b.items()} for b in w["fast"]],
-                   fast_mats=tuple(fast_mats))
+                   fast_mats=tuple(fast_mats),
+                   static=None if st is None else [{k: f64(v) for k, v in b.items()} for b in st])
 
     @property
     def vocab(self):
@@ -205,7 +215,9 @@ def frozen_prefix(net: Net, x):
 
 def forward_logits(net: Net, fast, h_in):
     h = h_in
-    for Wb in fast:
+    for l, Wb in enumerate(fast):
+        if net.static is not None:
+            h, _ = block_forward(net.kind, net.static[l], h)      # R10
         h, _ = block_forward(net.kind, Wb, h)
     y, _ = rmsnorm(h, net.eps)
     return y @ net.U.T
@@ -222,9 +234,12 @@ def chunk_loss_and_grads(net: Net, fast, h_in, targets, weights=None):
     with `weights` [b], the gradient of sum_t weights[t] * l_t instead (the
     Source Masking reading R8 passes mask / max(1, sum(mask)))."""
     b = len(targets)
-    caches = []
+    caches, static_caches = [], []
     h = h_in
-    for Wb in fast:
+    for l, Wb in enumerate(fast):
+        if net.static is not None:
+            h, c = block_forward(net.kind, net.static[l], h)      # R10
+            static_caches.append(c)
         h, c = block_forward(net.kind, Wb, h)
         caches.append(c)
     y, r = rmsnorm(h, net.eps)
@@ -241,6 +256,9 @@ def chunk_loss_and_grads(net: Net, fast, h_in, targets, weights=None):
     for l in range(len(fast) - 1, -1, -1):
         grads[l], dh = block_backward(net.kind, fast[l], caches[l], dh, net.fast_mats,
                                       need_dh=l > 0)
+        if net.static is not None and l > 0:
+            # through the frozen MLP to the fast blocks below (no gradient of its own)
+            _, dh = block_backward(net.kind, net.static[l], static_caches[l], dh, (), need_dh=True)
     return losses, grads
 
 

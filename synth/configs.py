@@ -36,6 +36,7 @@ class Workload:
     settle_every: int = 0   # chunks between Settlement events, 0 = off
     settle_len: int = 0     # tokens of each held-out chunk q
     reset_every: int = 0    # chunk updates between resets of the fast weights to W_0, 0 = off
+    static_mlp: bool = False  # each fast block also holds a frozen MLP, run before its fast one
     rms_eps: float = 1e-6
     uniform_mix: float = 0.05
     init_std: float = 0.02

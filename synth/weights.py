@@ -10,8 +10,10 @@ Layout (row-major, linear maps stored [out, in]):
 
 Matrix m of the workload is drawn from SeedSequence([seed id, 0, m]) with
 m = 0 for E, 1 for U, then 2 + 3 * block + position-in-block over the prefix
-blocks followed by the fast blocks.  Only the generator lives here; the
-arithmetic of the method does not.
+blocks followed by the fast blocks; with static MLPs in the fast blocks, the
+static MLP of fast block l continues after them at 2 + 3 * (n_prefix + n_fast
++ l) + position.  Only the generator lives here; the arithmetic of the method
+does not.
 """
 from __future__ import annotations
 
@@ -71,6 +73,10 @@ def make_weights(wl: Workload) -> dict:
     for blk in range(wl.n_prefix + wl.n_fast):
         bw = {name: _draw(wl, 2 + 3 * blk + pos, shapes[name]) for pos, name in enumerate(mats)}
         (w["prefix"] if blk < wl.n_prefix else w["fast"]).append(bw)
+    if wl.static_mlp:
+        base = 2 + 3 * (wl.n_prefix + wl.n_fast)
+        w["static"] = [{name: _draw(wl, base + 3 * l + pos, shapes[name]) for pos, name in enumerate(mats)}
+                       for l in range(wl.n_fast)]
     return w
 
 

@@ -60,6 +60,12 @@ MUTANTS = {
         "if st.reset_every and (st.chunks_done - 1) % st.reset_every == 0 and st.chunks_done > 1:"),
     "reset keeps the current weights": (
         "st.W = copy.deepcopy(net.fast0)       # R9", "st.W = copy.deepcopy(st.W)       # R9"),
+    "static MLP skipped in the backward": (
+        "if net.static is not None and l > 0:", "if False:"),
+    "static MLP after the fast one": (
+        "            h, _ = block_forward(net.kind, net.static[l], h)      # R10\n        h, _ = block_forward(net.kind, Wb, h)\n",
+        "            pass\n        h, _ = block_forward(net.kind, Wb, h)\n"
+        "        if net.static is not None:\n            h, _ = block_forward(net.kind, net.static[l], h)\n"),
     "p_next with the initial weights": (
         "p_next = softmax_next(net, st.W, st.x_last)", "p_next = softmax_next(net, net.fast0, st.x_last)"),
 }
@@ -84,6 +90,8 @@ PINS = [
     ("test_forward_by_hand_nonsquare", ()),
     ("test_decoding_a_full_chunk_equals_a_longer_prefill", ()),
     ("test_reset_every_chunk_scores_like_eq4_and_ends_at_w0", ()),
+    ("test_static_mlp_gradients_match_central_differences", ()),
+    ("test_static_mlp_runs_before_the_fast_one", ()),
     ("test_reset_splits_the_stream_into_independent_runs", ()),
     ("test_reset_counts_decoded_chunks_too", ()),
     ("test_all_ones_mask_is_the_unmasked_method", ()),

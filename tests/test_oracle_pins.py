@@ -510,3 +510,75 @@ def test_reset_and_settlement_are_exclusive():
     tok = rand_tokens(16, 1, 8, seed=99)
     with pytest.raises(ValueError):
         O.prefill(net, 0.3, 0.0, 2, tok, settle_every=2, settle_q=np.zeros((2, 1, 4), np.int64), reset_every=2)
+
+
+# ------------------------------------------------------------------ two MLPs per fast block (R10)
+def _with_static(net, seed, std=0.5):
+    rng = np.random.default_rng(seed)
+    net.static = [{k: rng.normal(0, std, v.shape) for k, v in b.items()} for b in net.fast0]
+    return net
+
+
+def test_static_mlp_gradients_match_central_differences():
+    """With a frozen MLP before every fast one, the fast gradients (which pass
+    through the later static MLPs to the earlier fast blocks) match central
+    differences at rel <= 1e-6, and the static MLPs get no gradient."""
+    net = _with_static(rand_net("gelu", d=8, f=16, V=16, n_prefix=1, n_fast=3, seed=60), seed=61)
+    tok = rand_tokens(16, 1, 3, seed=62)[0]
+    x_in, tgt = tok[:-1], tok[1:]
+    fast = copy.deepcopy(net.fast0)
+    _, grads = O.chunk_loss_and_grads(net, fast, O.frozen_prefix(net, x_in), tgt)
+    h = 1e-5
+    for l, Wb in enumerate(fast):
+        assert set(grads[l]) == set(net.fast_mats)
+        for k in net.fast_mats:
+            fd = np.zeros_like(Wb[k])
+            for idx in np.ndindex(Wb[k].shape):
+                orig = Wb[k][idx]
+                Wb[k][idx] = orig + h
+                lp = _chunk_mean_loss(net, fast, x_in, tgt)
+                Wb[k][idx] = orig - h
+                lm = _chunk_mean_loss(net, fast, x_in, tgt)
+                Wb[k][idx] = orig
+                fd[idx] = (lp - lm) / (2 * h)
+            rel = np.linalg.norm(fd - grads[l][k]) / np.linalg.norm(grads[l][k])
+            assert rel <= 1e-6, (l, k, rel)
+
+
+def test_static_mlp_runs_before_the_fast_one():
+    """Static-first (R10): fast block 0's static MLP acts like one more frozen
+    prefix block, so moving it into the prefix (and leaving an identity static
+    MLP, W2 = 0, in its place) changes no loss and no weight of a whole run."""
+    net = _with_static(rand_net("gelu", n_prefix=1, n_fast=2, seed=63), seed=64)
+    moved = copy.deepcopy(net)
+    moved.prefix = moved.prefix + [copy.deepcopy(net.static[0])]
+    moved.static[0] = {"W1": net.static[0]["W1"], "W2": np.zeros_like(net.static[0]["W2"])}
+    tok = rand_tokens(16, 2, 12, seed=65)
+    a = O.prefill(net, 0.3, 0.5, 4, tok)
+    b = O.prefill(moved, 0.3, 0.5, 4, tok)
+    np.testing.assert_allclose(a["losses"], b["losses"], rtol=0, atol=1e-13)
+    for s in range(2):
+        assert O.weights_rel_frobenius(a["W"][s], b["W"][s], net.fast_mats) < 1e-14
+
+
+def test_identity_static_mlps_are_the_plain_network():
+    """W2 = 0 in every static MLP makes each one the identity: the run equals
+    the network without static MLPs, exactly."""
+    net = rand_net("gelu", n_prefix=1, n_fast=2, seed=66)
+    with_id = copy.deepcopy(net)
+    with_id.static = [{"W1": np.ones_like(b["W1"]), "W2": np.zeros_like(b["W2"])} for b in net.fast0]
+    tok = rand_tokens(16, 1, 12, seed=67)
+    a = O.prefill(net, 0.3, 0.5, 3, tok)
+    b = O.prefill(with_id, 0.3, 0.5, 3, tok)
+    np.testing.assert_array_equal(a["losses"], b["losses"])
+    assert O.weights_rel_frobenius(b["W"][0], a["W"][0], net.fast_mats) == 0.0
+
+
+def test_static_mlps_change_the_result():
+    """Non-trivial static MLPs do change the losses (they are not skipped)."""
+    net = rand_net("gelu", n_prefix=0, n_fast=2, seed=68)
+    with_s = _with_static(copy.deepcopy(net), seed=69)
+    tok = rand_tokens(16, 1, 8, seed=70)
+    a = O.prefill(net, 0.3, 0.0, 4, tok)
+    b = O.prefill(with_s, 0.3, 0.0, 4, tok)
+    assert np.max(np.abs(a["losses"] - b["losses"])) > 1e-3
