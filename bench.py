@@ -99,6 +99,11 @@ def chunk_flops(wl, rows=None):
         per["gemm_fast_fwd"] = wl.n_fast * 2 * mdf
         per["gemm_bwd_dx"] = (2 * wl.n_fast - 1) * mdf
         per["gemm_dw"] = 2 * wl.n_fast * mdf
+        if wl.static_mlp:
+            # fast block 0's static MLP joins the prefix; the later ones run forward and dX backward
+            per["gemm_prefix"] += 2 * mdf
+            per["gemm_fast_fwd"] += (wl.n_fast - 1) * 2 * mdf
+            per["gemm_bwd_dx"] += (wl.n_fast - 1) * 2 * mdf
     else:
         per["gemm_prefix"] = wl.n_prefix * 3 * mdf
         per["gemm_fast_fwd"] = wl.n_fast * 3 * mdf
@@ -145,7 +150,8 @@ def chunk_roofline_seconds(wl, pk):
     params = nf * wl.B * wl.d * wl.d_ff
     # weights read once per chunk (frozen prefix, head, fast masters r+w), token ids, losses,
     # and the block inputs written and read once
-    frozen = (wl.n_prefix * (2 if wl.block == "gelu" else 3) * wl.d * wl.d_ff + wl.vocab * wl.d) * es
+    n_frozen_blocks = wl.n_prefix + (wl.n_fast if wl.static_mlp else 0)
+    frozen = (n_frozen_blocks * (2 if wl.block == "gelu" else 3) * wl.d * wl.d_ff + wl.vocab * wl.d) * es
     by = frozen + params * 8 + M * 8 + M * wl.d * es * 2
     return max(fl / (pk["bf16_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9)), fl, by
 
@@ -386,7 +392,8 @@ def run_ours(args, wl, rank, world, local_rank):
         dms = sum(a.elapsed_time(b) for a, b in dev_ev)
         es = 2 if wl.dtype == "bf16" else 4
         nf = len(wl.fast_mats) * wl.n_fast
-        frozen = (wl.n_prefix * (2 if wl.block == "gelu" else 3) * wl.d * wl.d_ff
+        frozen = ((wl.n_prefix + (wl.n_fast if wl.static_mlp else 0)) * (2 if wl.block == "gelu" else 3)
+                  * wl.d * wl.d_ff
                   + wl.n_fast * ((2 if wl.block == "gelu" else 3) - len(wl.fast_mats)) * wl.d * wl.d_ff
                   + wl.vocab * wl.d) * es
         fast = wl.B * nf * wl.d * wl.d_ff * es

@@ -132,11 +132,11 @@ struct PrefixBufs {
 // pb.swiglu_a is set) for the tokens of tv: W-independent work.
 static ttt_status prefix_pass(ttt_handle* h, const TokView& tv, const PrefixBufs& pb, cudaStream_t st) {
   const int B = h->B, M = B * tv.rows, d = h->d, f = h->f, stg = h->stg;
-  OpBuf cur = h->dm.n_prefix > 0 ? pb.xop : pb.hout;
+  OpBuf cur = h->n_pre > 0 ? pb.xop : pb.hout;
   TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(stg, B, tv, h->E, d, pb.x32, cur.p, cur.lo, st); }));
-  for (int p = 0; p < h->dm.n_prefix; ++p) {
+  for (int p = 0; p < h->n_pre; ++p) {
     const OpBuf* W = &h->prefix[(size_t)p * h->nm];
-    const OpBuf next = (p == h->dm.n_prefix - 1) ? pb.hout : pb.xop;
+    const OpBuf next = (p == h->n_pre - 1) ? pb.hout : pb.xop;
     if (h->dm.block_kind == TTT_BLOCK_GELU) {
       GemmDesc g;
       g.M = M; g.N = f; g.K = d;
@@ -223,7 +223,25 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
   h->a0_s = a0_s;
 
   for (int l = 0; l < h->dm.n_fast; ++l) {
-    const OpBuf hin = l == 0 ? hin0 : h->hlvl[l];
+    if (l > 0 && h->dm.static_mlp) {
+      // the block's frozen MLP (shared weights: one GEMM over all B * rows rows)
+      const OpBuf* W = &h->statics[(size_t)l * h->nm];
+      GemmDesc g;
+      g.M = M; g.N = f; g.K = d;
+      setA(g, h->hlvl[l], d); setB(g, W[0], d);
+      g.epi = EPI_GELU;
+      if (train) setOut(g, h->szst[l], f);
+      else g.out = nullptr;
+      setOut2(g, h->tmp_a, f);
+      TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g, st));
+      GemmDesc g2;
+      g2.M = M; g2.N = d; g2.K = f;
+      setA(g2, h->tmp_a, f); setB(g2, W[1], f);
+      g2.epi = EPI_RESID; g2.aux = h->x32; g2.ldx = d; g2.out = h->x32; g2.ldo = d;
+      setOut2(g2, h->shin[l], d);
+      TTT_TRY(rungemm(h, K_GEMM_FAST_FWD, g2, st));
+    }
+    const OpBuf hin = l == 0 ? hin0 : (h->dm.static_mlp ? h->shin[l] : h->hlvl[l]);
     const long long hin_s = l == 0 ? hin0_s : (long long)rows * d;
     OpBuf a_out = train ? h->ast[l] : h->tmp_a;
     long long a_s = (long long)rows * f;
@@ -372,7 +390,7 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
       g1.M = f; g1.N = d; g1.K = rows; g1.batch = B;
       g1.a_kmajor = false; setA(g1, h->zst[l], f, (long long)rows * f);
       if (l == 0) { g1.b_kmajor = false; setB(g1, h->hin0, d, h->hin0_s); }
-      else { g1.b_kmajor = false; setB(g1, h->hlvl[l], d, (long long)rows * d); }
+      else { g1.b_kmajor = false; setB(g1, h->dm.static_mlp ? h->shin[l] : h->hlvl[l], d, (long long)rows * d); }
       g1.ldo = d;
       TTT_TRY(dw_gemm(g1, s1));
       if (l > 0) {
@@ -385,6 +403,24 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
         gb.out = h->dh32; gb.ldo = d; gb.sO = (long long)rows * d;
         setOut2(gb, h->dhop, d, (long long)rows * d);
         TTT_TRY(rungemm(h, K_GEMM_BWD_DX, gb, st));
+        if (h->dm.static_mlp) {
+          // through the block's frozen MLP: dz_s = (dh W2s) * GELU'(z_s); dh += dz_s W1s
+          const OpBuf* W = &h->statics[(size_t)l * 2];
+          GemmDesc sz;
+          sz.M = M; sz.N = f; sz.K = d;
+          setA(sz, h->dhop, d);
+          sz.b_kmajor = false; setB(sz, W[1], f);
+          sz.epi = EPI_DGELU; sz.aux = h->szst[l].p; sz.loX = h->szst[l].lo; sz.ldx = f;
+          setOut(sz, h->szst[l], f);
+          TTT_TRY(rungemm(h, K_GEMM_BWD_DX, sz, st));
+          GemmDesc sb;
+          sb.M = M; sb.N = d; sb.K = f;
+          setA(sb, h->szst[l], f);
+          sb.b_kmajor = false; setB(sb, W[0], d);
+          sb.epi = EPI_RESID; sb.aux = h->dh32; sb.ldx = d; sb.out = h->dh32; sb.ldo = d;
+          setOut2(sb, h->dhop, d);
+          TTT_TRY(rungemm(h, K_GEMM_BWD_DX, sb, st));
+        }
       }
     } else {
       const int sd = h->slot_of[(size_t)l * 3 + 2];
@@ -656,7 +692,10 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
     return fail(TTT_ERR_UNSUPPORTED, "GELU blocks run with both W1 and W2 fast (fast_mask 3)");
   if (D.block_kind == TTT_BLOCK_SWIGLU && (D.fast_mask != TTT_FAST_WD || D.n_fast != 1))
     return fail(TTT_ERR_UNSUPPORTED, "SwiGLU runs with one fast block whose down projection is fast");
-  if (!w->E || !w->U || (D.n_prefix > 0 && !w->prefix) || !w->fast)
+  if (D.static_mlp != 0 && D.static_mlp != 1) return fail(TTT_ERR_BAD_ARG, "static_mlp must be 0 or 1");
+  if (D.static_mlp && D.block_kind != TTT_BLOCK_GELU)
+    return fail(TTT_ERR_UNSUPPORTED, "static MLPs run in GELU fast blocks");
+  if (!w->E || !w->U || (D.n_prefix > 0 && !w->prefix) || !w->fast || (D.static_mlp && !w->statics))
     return fail(TTT_ERR_BAD_ARG, "null weight pointer");
 
   ttt_handle* h = new ttt_handle();
@@ -720,10 +759,20 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   }
   if ((s = op_alloc(&h->U, (size_t)V * d)) != TTT_OK) return bail(s);
   if ((s = upload(w->U, (size_t)V * d, h->U, h->stg)) != TTT_OK) return bail(s);
-  h->prefix.assign((size_t)D.n_prefix * h->nm, OpBuf());
+  // fast block 0's static MLP depends on no fast weight: it runs as one more prefix block
+  h->n_pre = D.n_prefix + (D.static_mlp ? 1 : 0);
+  h->prefix.assign((size_t)h->n_pre * h->nm, OpBuf());
   for (size_t i = 0; i < h->prefix.size(); ++i) {
+    const float* src = i < (size_t)D.n_prefix * h->nm ? w->prefix[i] : w->statics[i - (size_t)D.n_prefix * h->nm];
     if ((s = op_alloc(&h->prefix[i], (size_t)h->n)) != TTT_OK) return bail(s);
-    if ((s = upload(w->prefix[i], (size_t)h->n, h->prefix[i], h->stg)) != TTT_OK) return bail(s);
+    if ((s = upload(src, (size_t)h->n, h->prefix[i], h->stg)) != TTT_OK) return bail(s);
+  }
+  if (D.static_mlp) {
+    h->statics.assign((size_t)D.n_fast * h->nm, OpBuf());
+    for (size_t i = (size_t)h->nm; i < h->statics.size(); ++i) {
+      if ((s = op_alloc(&h->statics[i], (size_t)h->n)) != TTT_OK) return bail(s);
+      if ((s = upload(w->statics[i], (size_t)h->n, h->statics[i], h->stg)) != TTT_OK) return bail(s);
+    }
   }
   h->fastfrozen.assign((size_t)D.n_fast * h->nm, OpBuf());
   if ((s = dalloc(h, &h->W0, (size_t)h->nslots * h->n * 4)) != TTT_OK) return bail(s);
@@ -763,6 +812,12 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
       if ((s = op_alloc(&h->zst[l], Mm * f)) != TTT_OK) return bail(s);
     if ((s = op_alloc(&h->ast[l], Mm * f)) != TTT_OK) return bail(s);
   }
+  h->szst.assign(D.n_fast, OpBuf());
+  h->shin.assign(D.n_fast, OpBuf());
+  for (int l = 1; l < D.n_fast && D.static_mlp; ++l) {
+    if ((s = op_alloc(&h->szst[l], Mm * f)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->shin[l], Mm * d)) != TTT_OK) return bail(s);
+  }
   if ((s = op_alloc(&h->tmp_a, Mm * f)) != TTT_OK) return bail(s);
   // Settlement chunk q: its prefix output, shared by the event's two forwards
   if (hp->settle_len > 0) {
@@ -775,7 +830,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   // hoisted prefix: groups of up to hoist_chunks chunks, within a 4 GiB budget
   {
     const size_t P = split ? 2 : 1;
-    size_t per_row = (size_t)d * 4 + (size_t)d * es * P + (D.n_prefix > 0 ? (size_t)d * es * P : 0) +
+    size_t per_row = (size_t)d * 4 + (size_t)d * es * P + (h->n_pre > 0 ? (size_t)d * es * P : 0) +
                      (size_t)f * es * P;
     if (D.block_kind == TTT_BLOCK_SWIGLU) per_row += (size_t)f * 4 + (size_t)f * es * P;
     const size_t per_chunk = per_row * (size_t)B * h->b;
@@ -791,7 +846,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
     const size_t Mh = (size_t)B * h->b * gmax;
     if ((s = dalloc(h, &h->hx32, Mh * d * 4)) != TTT_OK) return bail(s);
     if ((s = op_alloc(&h->hx_op, Mh * d)) != TTT_OK) return bail(s);
-    if (D.n_prefix > 0)
+    if (h->n_pre > 0)
       if ((s = op_alloc(&h->hx_xop, Mh * d)) != TTT_OK) return bail(s);
     if ((s = op_alloc(&h->hx_tmp_a, Mh * f)) != TTT_OK) return bail(s);
     if (D.block_kind == TTT_BLOCK_SWIGLU) {
@@ -895,7 +950,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   // b = 1 on a network whose fast block and head fit in shared memory: one
   // persistent CTA per sequence steps through every token
   const char* env_tok = getenv("TTT_TOKEN_KERNEL");
-  const bool token_path = b == 1 && h->dm.n_prefix == 0 && h->dm.n_fast == 1 &&
+  const bool token_path = b == 1 && h->n_pre == 0 && h->dm.n_fast == 1 &&
                           h->dm.block_kind == TTT_BLOCK_GELU && h->stg == ST_F32 && h->hp.settle_every == 0 &&
                           h->hp.reset_every == 0 &&
                           token_steps_supported(h->d, h->f, h->V) && !(env_tok && std::string(env_tok) == "0");

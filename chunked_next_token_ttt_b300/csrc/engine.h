@@ -35,7 +35,9 @@ struct ttt_handle {
   // frozen weights
   void* E = nullptr;                 // bf16 for ST_BF16, float otherwise
   OpBuf U;
-  std::vector<OpBuf> prefix;         // [n_prefix * nm]
+  std::vector<OpBuf> prefix;         // [n_pre * nm]: the frozen blocks, then (static_mlp) fast block 0's static MLP
+  int n_pre = 0;                     // frozen blocks the prefix pass runs
+  std::vector<OpBuf> statics;        // [n_fast * nm] static MLP of fast block l >= 1 (static_mlp)
   std::vector<OpBuf> fastfrozen;     // [n_fast * nm], empty where fast
 
   // fast weights: arenas [slot][B][n]
@@ -51,6 +53,7 @@ struct ttt_handle {
   float* x32 = nullptr;
   OpBuf xop;
   std::vector<OpBuf> hlvl, zst, ast;
+  std::vector<OpBuf> szst, shin;     // static MLP of fast block l >= 1: its z stash and its output (fast MLP input)
   OpBuf tmp_a;
   float* tmp_g = nullptr;
   // hoisted prefix of a group of up to hoist_chunks chunks, rows [B][g * b]

@@ -33,7 +33,8 @@ class TTTError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("d_ff", ctypes.c_int), ("vocab", ctypes.c_int),
                 ("n_prefix", ctypes.c_int), ("n_fast", ctypes.c_int), ("block_kind", ctypes.c_int),
-                ("fast_mask", ctypes.c_int), ("dtype", ctypes.c_int), ("rms_eps", ctypes.c_float)]
+                ("fast_mask", ctypes.c_int), ("dtype", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("static_mlp", ctypes.c_int)]
 
 
 class HParams(ctypes.Structure):
@@ -44,7 +45,8 @@ class HParams(ctypes.Structure):
 
 class Weights(ctypes.Structure):
     _fields_ = [("E", ctypes.c_void_p), ("U", ctypes.c_void_p),
-                ("prefix", ctypes.POINTER(ctypes.c_void_p)), ("fast", ctypes.POINTER(ctypes.c_void_p))]
+                ("prefix", ctypes.POINTER(ctypes.c_void_p)), ("fast", ctypes.POINTER(ctypes.c_void_p)),
+                ("statics", ctypes.POINTER(ctypes.c_void_p))]
 
 
 _lib = None
@@ -132,7 +134,9 @@ class Handle:
     """One libttt handle: a network, its TTT hyper-parameters and B sequences."""
 
     def __init__(self, *, d, d_ff, vocab, n_prefix, n_fast, block, fast_mats, dtype, eta, clip, chunk,
-                 B, weights, settle_every=0, settle_len=0, rms_eps=1e-6, reset_every=0):
+                 B, weights, settle_every=0, settle_len=0, rms_eps=1e-6, reset_every=0, static_mlp=False):
+        """weights: {"E", "U", "prefix": [block dicts], "fast": [block dicts]} and,
+        with static_mlp, "static": one frozen MLP (block dict) per fast block."""
         self.lib = load_library()
         self.block = block
         self.mats = MATS[block]
@@ -142,7 +146,8 @@ class Handle:
         mask = 0
         for m in fast_mats:
             mask |= FAST_BIT[m]
-        self._dims = Dims(d, d_ff, vocab, n_prefix, n_fast, BLOCK[block], mask, DTYPE[dtype], rms_eps)
+        self._dims = Dims(d, d_ff, vocab, n_prefix, n_fast, BLOCK[block], mask, DTYPE[dtype], rms_eps,
+                          1 if static_mlp else 0)
         self._hp = HParams(eta, clip, chunk, settle_every, B, settle_len, reset_every)
         keep = []
 
@@ -160,9 +165,12 @@ class Handle:
         fst = [f32(b[m]) for b in weights["fast"] for m in self.mats]
         pre_arr = (ctypes.c_void_p * max(1, len(pre)))(*pre)
         fst_arr = (ctypes.c_void_p * len(fst))(*fst)
+        sta = [f32(b[m]) for b in weights["static"] for m in self.mats] if static_mlp else []
+        sta_arr = (ctypes.c_void_p * max(1, len(sta)))(*sta)
         w = Weights(f32(weights["E"]), f32(weights["U"]),
                     ctypes.cast(pre_arr, ctypes.POINTER(ctypes.c_void_p)),
-                    ctypes.cast(fst_arr, ctypes.POINTER(ctypes.c_void_p)))
+                    ctypes.cast(fst_arr, ctypes.POINTER(ctypes.c_void_p)),
+                    ctypes.cast(sta_arr, ctypes.POINTER(ctypes.c_void_p)) if static_mlp else None)
         h = ctypes.c_void_p()
         _check(self.lib.ttt_create(ctypes.byref(self._dims), ctypes.byref(self._hp), ctypes.byref(w),
                                    ctypes.byref(h)), "ttt_create")
@@ -175,7 +183,7 @@ class Handle:
                    block=wl.block, fast_mats=wl.fast_mats, dtype=wl.dtype, eta=wl.eta, clip=wl.clip,
                    chunk=wl.chunk, B=wl.B if B is None else B, weights=weights,
                    settle_every=wl.settle_every, settle_len=wl.settle_len, rms_eps=wl.rms_eps,
-                   reset_every=wl.reset_every)
+                   reset_every=wl.reset_every, static_mlp=wl.static_mlp)
 
     def close(self):
         if getattr(self, "_h", None):

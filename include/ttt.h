@@ -93,6 +93,11 @@ typedef struct {
                        TTT_DTYPE_BF16: bf16 weights/activations, fp32
                        accumulation and fp32 master fast weights             */
   float rms_eps;    /* RMSNorm epsilon inside the square root (1e-6)          */
+  int static_mlp;   /* 1: every fast block also holds a frozen MLP of the same
+                       kind and widths that runs before its fast MLP
+                       ("End-to-End TTT" review, 3.1, Two MLP layers per
+                       block): h += MLP_s(h); h += MLP_f(h).  GELU blocks
+                       only; 0 = off                                          */
 } ttt_dims;
 
 typedef struct {
@@ -120,6 +125,8 @@ typedef struct {
   const float* U;
   const float* const* prefix;
   const float* const* fast;
+  const float* const* statics;   /* static_mlp: n_fast * n_mats pointers, the
+                                    frozen MLP of each fast block (NULL otherwise) */
 } ttt_weights;
 
 typedef struct ttt_handle ttt_handle;

@@ -74,3 +74,13 @@ def test_reset_with_settlement_is_rejected_before_any_cuda_call():
     with pytest.raises(TTTError) as e:
         Handle.from_workload(wl, synth.make_weights(wl))
     assert e.value.status == 1
+
+
+def test_static_mlp_outside_gelu_blocks_is_unsupported_before_any_cuda_call():
+    import synth
+    from synth import configs as C
+    from chunked_next_token_ttt_b300 import Handle, TTTError
+    wl = C.INPLACE_4B.replace(d=16, d_ff=32, vocab=64, n_prefix=1, B=1, static_mlp=True)
+    with pytest.raises(TTTError) as e:
+        Handle.from_workload(wl, synth.make_weights(wl))
+    assert e.value.status == 7

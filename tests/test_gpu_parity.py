@@ -320,6 +320,62 @@ def test_periodic_reset_counts_decoded_chunks():
         assert oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats) <= 1e-4
 
 
+@pytest.mark.parametrize("case", ["fp32_split", "fp32_rows", "bf16_hoisted", "bf16_settle", "b1"])
+def test_two_mlp_fast_blocks_against_the_oracle(monkeypatch, case):
+    """Fast blocks holding a frozen MLP before the fast one: the static MLP of
+    block 0 runs in the (hoisted) prefix, the later ones forward and backward
+    between the fast MLPs; every storage type, Settlement and b = 1."""
+    if case == "fp32_split":
+        wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=4 * 64 + 7, n_fast=3,
+                                    static_mlp=True)
+    elif case == "fp32_rows":
+        wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=40, B=3, T=130, n_prefix=0,
+                                    static_mlp=True)
+    elif case == "bf16_hoisted":
+        monkeypatch.setenv("TTT_HOIST_CHUNKS", "2")
+        wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1024, chunk=64, B=3, T=5 * 64, n_prefix=1,
+                                static_mlp=True, eta=0.3)
+    elif case == "bf16_settle":
+        wl = C.SETTLE_760M.replace(d=128, d_ff=512, vocab=1000, chunk=64, B=4, T=4 * 64, n_prefix=1,
+                                   settle_len=64, settle_every=2, eta=0.5, init_std=0.08, static_mlp=True)
+    else:
+        wl = C.TOY_BIGRAM.replace(B=2, T=100, n_fast=2, static_mlp=True)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp)
+    ref = run_oracle(wl, inp)
+    # the Settlement case draws 4x larger weights (to make decisions decidable) through
+    # seven bf16 MLPs: its next-token probabilities carry about twice the usual bf16 error
+    compare(wl, gpu, ref, check_p=not wl.settle_every)
+    if wl.settle_every:
+        assert np.abs(gpu["p_next"] - ref["p_next"]).max() <= 1e-2
+        compare_settlement(gpu, ref, range(wl.B), noise=5e-3)
+
+
+def test_two_mlp_fast_blocks_decode():
+    """Decoding through static MLPs (captured graph), across a step."""
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=8, B=2, T=2 * 8 + 5, n_prefix=1, n_fast=2,
+                                static_mlp=True, eta=0.5)
+    inp = make(wl)
+    extra = 6
+    long_tok = synth.sample_stream(inp["chain"], wl.seed_id, wl.B, wl.T + extra)
+    tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
+    gpu = run_gpu(wl, inp, tokens=tok)
+    h = gpu["handle"]
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
+    for t in range(wl.T + 1, wl.T + extra + 1):
+        h.decode_step(torch.from_numpy(long_tok[:, t].copy()).cuda(), p, loss)
+        torch.cuda.synchronize()
+        for s in range(wl.B):
+            l_ref, p_ref = oracle.decode_step(net, ref["states"][s], long_tok[s, t], wl.eta, wl.clip, wl.chunk)
+            assert abs(float(loss[s]) - l_ref) <= TOL["fp32"]["loss_max"]
+            np.testing.assert_allclose(p[s].cpu().numpy(), p_ref, atol=1e-5)
+    for s in range(wl.B):
+        assert oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats) <= 1e-4
+
+
 def test_host_and_device_buffers_agree():
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=32, B=2, T=100, n_prefix=1)
     inp = make(wl)
