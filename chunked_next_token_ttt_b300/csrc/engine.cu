@@ -510,7 +510,9 @@ static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t 
   TokView tv;
   tv.tok = h->pend; tv.tok_ld = h->b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 0;
   TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, true, st));
-  TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_softmax(h->B, h->V, h->logits32, p_out, h->lse_next, st); }));
+  TTT_TRY(run(h, K_OTHER, st, 2, [&] {
+    return launch_softmax(h->B, h->V, h->logits32, p_out, h->lse_next, h->soft_part, st);
+  }));
   // logits32 / lse_next now hold the next-token distribution under the current
   // weights: the next decode step scores its token from them
   h->next_valid = true;
@@ -539,8 +541,9 @@ static ttt_status decode_forward_graph(ttt_handle* h, cudaStream_t st) {
     tv.tok = h->x_dev; tv.tok_ld = 1; tv.tok_off = 0; tv.rows = 1; tv.n_valid = 0;
     ttt_status s = forward(h, tv, false, false, nullptr, 0, 0, true, h->gstream);
     if (s == TTT_OK)
-      s = run(h, K_OTHER, h->gstream, 1,
-              [&] { return launch_softmax(h->B, h->V, h->logits32, h->p_dev, h->lse_next, h->gstream); });
+      s = run(h, K_OTHER, h->gstream, 2, [&] {
+        return launch_softmax(h->B, h->V, h->logits32, h->p_dev, h->lse_next, h->soft_part, h->gstream);
+      });
     cudaGraph_t graph = nullptr;
     const cudaError_t e = cudaStreamEndCapture(h->gstream, &graph);
     h->prof_class = saved_prof;
@@ -889,6 +892,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = dalloc(h, &h->logits32, (size_t)B * V * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->p_dev, (size_t)B * V * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->lse_next, (size_t)B * 4)) != TTT_OK) return bail(s);
+  if ((s = dalloc(h, &h->soft_part, (size_t)B * kSoftmaxMaxSlices * sizeof(float2))) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->Lc, (size_t)B * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->Lw, (size_t)B * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->pend, (size_t)B * (h->b + 1) * 4)) != TTT_OK) return bail(s);

@@ -96,6 +96,7 @@ struct ttt_handle {
   float* logits32 = nullptr;
   float* p_dev = nullptr;
   float* lse_next = nullptr;         // [B] logsumexp of logits32 (next-token softmax)
+  float2* soft_part = nullptr;       // [B][kSoftmaxMaxSlices] slice states of that softmax
   bool next_valid = false;           // logits32 / lse_next score the next decoded token
   // decoding's next-token forward, captured once as a CUDA graph
   cudaStream_t gstream = nullptr;

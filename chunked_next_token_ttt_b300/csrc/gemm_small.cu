@@ -74,14 +74,46 @@ template <> struct Vec8<float> {
 // B K-major with 16-byte loads: each warp computes CW adjacent output columns
 // at once, each lane taking eight consecutive k per step (a warp reads 256
 // consecutive k of CW weight rows per step and plane); every 16-byte chunk of
-// the M activation rows (through L1) serves all CW columns.  CW = 4 for wide
-// outputs (N >= kWideN: vocabulary heads, wide projections) of one or two
-// rows, 1 otherwise so that narrow outputs still spread over enough warps.  Needs K, lda, ldb, the
+// the M activation rows (through L1) serves all CW columns.  U steps are
+// loaded before any of them is used, so a lane keeps U x CW 16-byte weight
+// loads in flight.  CW = 4 for wide outputs (N >= kWideN: vocabulary heads,
+// wide projections) of one or two rows, 1 otherwise so that narrow outputs
+// still spread over enough warps.  U = 4 (2 with four columns), except for
+// hi/lo split operands with more than two rows, whose doubled loads would
+// spill at that depth (U = 1 measured faster there).  After the warp
+// reduction every lane holds
+// the sums and lane m applies the epilogue of row m.  Needs K, lda, ldb, the
 // batch strides and lo offsets multiples of 8 and 16-byte aligned bases
 // (gemm_small_vec_ok).
 constexpr int kWideN = 8192;
 
-template <typename S, int kCW>
+template <typename S, int kCW, int kU>
+__device__ __forceinline__ void kvec_steps(const GemmDesc& g, long long a0, long long b0, int n0, int k,
+                                           float (&acc)[kCW][kMaxRows]) {
+  float bv[kU][kCW][8];
+#pragma unroll
+  for (int u = 0; u < kU; ++u)
+#pragma unroll
+    for (int c = 0; c < kCW; ++c) {
+      const int n = n0 + c < g.N ? n0 + c : g.N - 1;   // clamp: the extra columns are not stored
+      Vec8<S>::load(g.B, g.loB, b0 + (long long)n * g.ldb + k + 256 * u, bv[u][c]);
+    }
+#pragma unroll
+  for (int u = 0; u < kU; ++u)
+#pragma unroll
+    for (int m = 0; m < kMaxRows; ++m) {
+      if (m < g.M) {
+        float av[8];
+        Vec8<S>::load(g.A, g.loA, a0 + (long long)m * g.lda + k + 256 * u, av);
+#pragma unroll
+        for (int c = 0; c < kCW; ++c)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[c][m] = fmaf(av[j], bv[u][c][j], acc[c][m]);
+      }
+    }
+}
+
+template <typename S, int kCW, int kU>
 __global__ void __launch_bounds__(256) gemm_small_kvec_kernel(GemmDesc g) {
   pdl_wait();
   pdl_launch();
@@ -96,36 +128,22 @@ __global__ void __launch_bounds__(256) gemm_small_kvec_kernel(GemmDesc g) {
     for (int c = 0; c < kCW; ++c)
 #pragma unroll
       for (int m = 0; m < kMaxRows; ++m) acc[c][m] = 0.0f;
-    for (int k = lane * 8; k < g.K; k += 256) {
-      float bv[kCW][8];
-#pragma unroll
-      for (int c = 0; c < kCW; ++c) {
-        const int n = n0 + c < g.N ? n0 + c : g.N - 1;   // clamp: the extra columns are not stored
-        Vec8<S>::load(g.B, g.loB, b0 + (long long)n * g.ldb + k, bv[c]);
-      }
-#pragma unroll
-      for (int m = 0; m < kMaxRows; ++m) {
-        if (m < g.M) {
-          float av[8];
-          Vec8<S>::load(g.A, g.loA, a0 + (long long)m * g.lda + k, av);
-#pragma unroll
-          for (int c = 0; c < kCW; ++c)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[c][m] = fmaf(av[j], bv[c][j], acc[c][m]);
-        }
-      }
-    }
+    int k = lane * 8;
+    for (; k + 256 * (kU - 1) < g.K; k += 256 * kU) kvec_steps<S, kCW, kU>(g, a0, b0, n0, k, acc);
+    for (; k < g.K; k += 256) kvec_steps<S, kCW, 1>(g, a0, b0, n0, k, acc);
 #pragma unroll
     for (int c = 0; c < kCW; ++c)
 #pragma unroll
       for (int m = 0; m < kMaxRows; ++m)
         if (m < g.M) acc[c][m] = warp_sum(acc[c][m]);
-    if (lane == 0) {
+    // lane m takes row m (selected without a dynamic register index)
 #pragma unroll
-      for (int c = 0; c < kCW; ++c)
+    for (int c = 0; c < kCW; ++c) {
+      float v = 0.0f;
 #pragma unroll
-        for (int m = 0; m < kMaxRows; ++m)
-          if (n0 + c < g.N && m < g.M) sq += epi_value<S>(g, bz, m, n0 + c, acc[c][m]);
+      for (int m = 0; m < kMaxRows; ++m)
+        if (m == lane) v = acc[c][m];
+      if (lane < g.M && n0 + c < g.N) sq += epi_value<S>(g, bz, lane, n0 + c, v);
     }
   }
   if (g.epi == EPI_DW) {
@@ -179,11 +197,15 @@ bool gemm_small_vec_ok(const GemmDesc& g);
 // rows the 4 x M accumulators crowd the registers (measured slower)
 int small_cols_per_warp(const GemmDesc& g) { return (g.N >= kWideN && g.M <= 2) ? 4 : 1; }
 
+// the deeply unrolled weight-streaming variant (U = 4) suits this product
+bool small_deep_unroll(const GemmDesc& g) { return g.dtype != ST_SPLIT || g.M <= 2; }
+
 int small_grid_x(const GemmDesc& g) {
   const int per_block = gemm_small_vec_ok(g) ? 8 * small_cols_per_warp(g) : (g.b_kmajor ? 8 : 256);
   int gx = ceil_div(g.N, per_block);
-  // enough blocks to cover the SMs a few times over, at least one column each
-  const int target = ceil_div(148 * 4, g.batch);
+  // enough blocks to cover the SMs several times over (more for the
+  // latency-bound one- and two-row products), at least one column each
+  const int target = ceil_div(148 * (small_deep_unroll(g) ? 8 : 4), g.batch);
   return gx < target ? gx : target;
 }
 
@@ -203,15 +225,16 @@ ttt_status gemm_small(const GemmDesc& g, cudaStream_t st) {
     else if (g.dtype == ST_SPLIT) launch_pdl(KERNEL<Split>, grid, 256, 0, st, g);                  \
     else launch_pdl(KERNEL<float>, grid, 256, 0, st, g);                                           \
   } while (0)
-  if (gemm_small_vec_ok(g) && small_cols_per_warp(g) == 4) {
-    if (g.dtype == ST_BF16) launch_pdl(gemm_small_kvec_kernel<bf16, 4>, grid, 256, 0, st, g);
-    else if (g.dtype == ST_SPLIT) launch_pdl(gemm_small_kvec_kernel<Split, 4>, grid, 256, 0, st, g);
-    else launch_pdl(gemm_small_kvec_kernel<float, 4>, grid, 256, 0, st, g);
-  } else if (gemm_small_vec_ok(g)) {
-    if (g.dtype == ST_BF16) launch_pdl(gemm_small_kvec_kernel<bf16, 1>, grid, 256, 0, st, g);
-    else if (g.dtype == ST_SPLIT) launch_pdl(gemm_small_kvec_kernel<Split, 1>, grid, 256, 0, st, g);
-    else launch_pdl(gemm_small_kvec_kernel<float, 1>, grid, 256, 0, st, g);
-  }
+#define TTT_KVEC(CW, U)                                                                        \
+  do {                                                                                         \
+    if (g.dtype == ST_BF16) launch_pdl(gemm_small_kvec_kernel<bf16, CW, U>, grid, 256, 0, st, g);        \
+    else if (g.dtype == ST_SPLIT) launch_pdl(gemm_small_kvec_kernel<Split, CW, U>, grid, 256, 0, st, g); \
+    else launch_pdl(gemm_small_kvec_kernel<float, CW, U>, grid, 256, 0, st, g);                          \
+  } while (0)
+  if (gemm_small_vec_ok(g) && small_cols_per_warp(g) == 4) TTT_KVEC(4, 2);
+  else if (gemm_small_vec_ok(g) && small_deep_unroll(g)) TTT_KVEC(1, 4);
+  else if (gemm_small_vec_ok(g)) TTT_KVEC(1, 1);
+#undef TTT_KVEC
   else if (g.b_kmajor) TTT_SMALL(gemm_small_kmajor_kernel);
   else TTT_SMALL(gemm_small_nmajor_kernel);
 #undef TTT_SMALL

@@ -496,28 +496,86 @@ __global__ void settle_apply_kernel(long long total, int B, long long n, const u
   }
 }
 
-__global__ void softmax_kernel(int V, const float* __restrict__ logits, float* __restrict__ p,
-                               float* __restrict__ lse_out) {
+// Softmax of M rows of V fp32 logits in two launches over S slices per row
+// (S * M blocks each, so a few rows still fill the GPU): the first writes
+// each slice's (max, sum of exp) state, the second merges the row's S states
+// into the logsumexp and writes p = exp(logit - lse) over its slice.
+// (max, sum of exp) merge of two softmax states
+__device__ __forceinline__ void soft_merge(float& m, float& s, float m2, float s2) {
+  const float n = fmaxf(m, m2);
+  s = s * expf(m - n) + s2 * expf(m2 - n);
+  m = n;
+}
+
+constexpr int kSoftBatch = 8;    // logits a thread loads before using any of them
+
+__global__ void softmax_part_kernel(int V, int L, const float* __restrict__ logits, float2* __restrict__ part) {
   pdl_wait();
   pdl_launch();
-  __shared__ float red[32];
-  __shared__ float wm[32];
-  const long long m = blockIdx.x;
+  __shared__ float2 wstate[32];
+  const long long m = blockIdx.y;
+  const int v0 = blockIdx.x * L, v1 = min(V, v0 + L);
   const float* row = logits + m * V;
-  float mx = -FLT_MAX;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) mx = fmaxf(mx, row[v]);
-  mx = warp_max(mx);
+  float mx = -FLT_MAX, se = 0.0f;
+  for (int base = v0 + threadIdx.x; base < v1; base += blockDim.x * kSoftBatch) {
+    float x[kSoftBatch];
+#pragma unroll
+    for (int j = 0; j < kSoftBatch; ++j) {
+      const int v = base + j * blockDim.x;
+      x[j] = v < v1 ? row[v] : -FLT_MAX;
+    }
+    float bm = x[0];
+#pragma unroll
+    for (int j = 1; j < kSoftBatch; ++j) bm = fmaxf(bm, x[j]);
+    float bs = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kSoftBatch; ++j)
+      if (base + j * (int)blockDim.x < v1) bs += expf(x[j] - bm);
+    soft_merge(mx, se, bm, bs);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, mx, o), s2 = __shfl_xor_sync(0xffffffffu, se, o);
+    soft_merge(mx, se, m2, s2);
+  }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (lane == 0) wm[wid] = mx;
+  if (lane == 0) wstate[wid] = make_float2(mx, se);
   __syncthreads();
-  mx = -FLT_MAX;
-  for (int k = 0; k < nw; ++k) mx = fmaxf(mx, wm[k]);
-  float se = 0.0f;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) se += expf(row[v] - mx);
-  se = block_sum(se, red);
-  if (lse_out && threadIdx.x == 0) lse_out[m] = mx + logf(se);
-  const float inv = 1.0f / se;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) p[m * V + v] = expf(row[v] - mx) * inv;
+  if (threadIdx.x == 0) {
+    float m2 = wstate[0].x, s2 = wstate[0].y;
+    for (int k = 1; k < nw; ++k) soft_merge(m2, s2, wstate[k].x, wstate[k].y);
+    part[m * gridDim.x + blockIdx.x] = make_float2(m2, s2);
+  }
+}
+
+__global__ void softmax_write_kernel(int V, int L, const float* __restrict__ logits,
+                                     const float2* __restrict__ part, float* __restrict__ p,
+                                     float* __restrict__ lse_out) {
+  pdl_wait();
+  pdl_launch();
+  const long long m = blockIdx.y;
+  const int S = gridDim.x;
+  // every thread merges the row's S states in the same order (no shared memory)
+  float mx = part[m * S].x, se = part[m * S].y;
+  for (int k = 1; k < S; ++k) soft_merge(mx, se, part[m * S + k].x, part[m * S + k].y);
+  const float lse = mx + logf(se);
+  if (lse_out && blockIdx.x == 0 && threadIdx.x == 0) lse_out[m] = lse;
+  const int v0 = blockIdx.x * L, v1 = min(V, v0 + L);
+  const float* row = logits + m * V;
+  float* prow = p + m * V;
+  for (int base = v0 + threadIdx.x; base < v1; base += blockDim.x * kSoftBatch) {
+    float x[kSoftBatch];
+#pragma unroll
+    for (int j = 0; j < kSoftBatch; ++j) {
+      const int v = base + j * blockDim.x;
+      x[j] = v < v1 ? row[v] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < kSoftBatch; ++j) {
+      const int v = base + j * blockDim.x;
+      if (v < v1) prow[v] = expf(x[j] - lse);
+    }
+  }
 }
 
 // loss[s] = lse[s] - logits[s][x]: the next-token loss of x from a softmax
@@ -727,9 +785,20 @@ ttt_status launch_next_token_loss(int B, int V, const float* logits32, const flo
   return TTT_OK;
 }
 
-ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* lse, cudaStream_t st) {
+int softmax_slices(int M, int V) {
+  int S = ceil_div(148 * 4, M > 0 ? M : 1);
+  if (S > kSoftmaxMaxSlices) S = kSoftmaxMaxSlices;
+  const int by_len = ceil_div(V, 256);       // at least 256 logits per slice
+  if (S > by_len) S = by_len;
+  return S < 1 ? 1 : S;
+}
+
+ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* lse, float2* part, cudaStream_t st) {
   if (M == 0) return TTT_OK;
-  launch_pdl(softmax_kernel, M, 512, 0, st, V, logits32, p, lse);
+  const int S = softmax_slices(M, V), L = ceil_div(V, S);
+  launch_pdl(softmax_part_kernel, dim3(S, M), 256, 0, st, V, L, logits32, part);
+  TTT_CHECK_LAUNCH();
+  launch_pdl(softmax_write_kernel, dim3(S, M), 256, 0, st, V, L, logits32, (const float2*)part, p, lse);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

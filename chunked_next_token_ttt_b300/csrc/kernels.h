@@ -106,7 +106,10 @@ ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const fl
                                float* Wc32, void* Wcop, long long op_lo, cudaStream_t st);
 
 // p[m, :] = softmax(logits32[m, :]); lse[m] = logsumexp of the row (lse may be null).
-ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* lse, cudaStream_t st);
+// p = softmax(logits32) row by row and lse = its logsumexp, in two launches;
+// part holds M * kSoftmaxMaxSlices slice states.
+constexpr int kSoftmaxMaxSlices = 32;
+ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* lse, float2* part, cudaStream_t st);
 // loss[s] = lse[s] - logits32[s * V + x_s] with x_s = tok[s * tok_ld + off]
 // (ids outside [0, V) read as 0 and raise bit 2 of *err).
 ttt_status launch_next_token_loss(int B, int V, const float* logits32, const float* lse, const int32_t* tok,
