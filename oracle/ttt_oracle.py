@@ -69,6 +69,20 @@ Readings taken where the pages leave a step open:
       h <- h + MLP_f(h), both of the block's kind and widths.  The page does
       not give the order; static-first is this reading.  Gradients reach
       earlier fast blocks through the later static MLPs.
+  R11 Sliding-window attention in the frozen blocks ([E2E] Method, the
+      bigram defect and its fix: a sliding-window attention layer of window
+      k, with k >= b so a chunk remembers its own tokens before the update;
+      3.1: attention layers stay frozen).  Every frozen prefix block becomes
+      h <- h + Attn(h) then h <- h + MLP(h); Attn(h) = concat over heads of
+      softmax(Q_h K_h^T / sqrt(d_h) + M) V_h, times Wo^T, with Q = h Wq^T,
+      K = h Wk^T, V = h Wv^T (all [d, d], stored [out, in]) and M = 0 where
+      the key position s satisfies t - k < s <= t for query position t, -inf
+      elsewhere.  Positions count the inputs x_0 (BOS) .. of one sequence from
+      0; no positional encoding is added (the pages name none).  The fast
+      blocks hold no attention, so the whole prefix of a sequence depends on
+      its tokens only and is computed once over x_0 .. x_T.  Decoding and
+      Settlement are not defined here with attention (the held-out chunk's
+      attention context is not fixed by the pages).
 """
 from __future__ import annotations
 
@@ -189,26 +203,60 @@ class Net:
     fast0: list               # per fast block: dict of all its matrices
     fast_mats: tuple          # which matrices of a fast block are fast
     static: list | None = None  # per fast block: its frozen MLP (R10), or None
+    attn: list | None = None    # per prefix block: its attention (Wq, Wk, Wv, Wo) (R11), or None
+    heads: int = 0
+    window: int = 0
 
     @staticmethod
-    def from_weights(w: dict, kind: str, fast_mats, eps: float) -> "Net":
+    def from_weights(w: dict, kind: str, fast_mats, eps: float, heads: int = 0, window: int = 0) -> "Net":
         f64 = lambda a: np.asarray(a, dtype=np.float64)
         st = w.get("static")
+        at = w.get("attn") if heads else None
         return Net(kind=kind, eps=eps, E=np.asarray(w["E"]), U=f64(w["U"]),
                    prefix=[{k: f64(v) for k, v in b.items()} for b in w["prefix"]],
                    fast0=[{k: f64(v) for k, v in b.items()} for b in w["fast"]],
                    fast_mats=tuple(fast_mats),
-                   static=None if st is None else [{k: f64(v) for k, v in b.items()} for b in st])
+                   static=None if st is None else [{k: f64(v) for k, v in b.items()} for b in st],
+                   attn=None if at is None else [{k: f64(v) for k, v in b.items()} for b in at],
+                   heads=heads if at is not None else 0, window=window if at is not None else 0)
 
     @property
     def vocab(self):
         return self.U.shape[0]
 
 
+def window_mask(n, k):
+    """R11: allowed[t, s] iff t - k < s <= t."""
+    t = np.arange(n)[:, None]
+    s = np.arange(n)[None, :]
+    return (s <= t) & (s > t - k)
+
+
+def attention(Wa, h, heads, window):
+    """Sliding-window multi-head attention over the rows of h, row t being
+    position t of one sequence (R11)."""
+    n, d = h.shape
+    dh = d // heads
+    Q, K, V = h @ Wa["Wq"].T, h @ Wa["Wk"].T, h @ Wa["Wv"].T
+    allowed = window_mask(n, window)
+    out = np.zeros_like(h)
+    for i in range(heads):
+        c = slice(i * dh, (i + 1) * dh)
+        S = np.where(allowed, Q[:, c] @ K[:, c].T / np.sqrt(dh), -np.inf)
+        S = S - S.max(axis=1, keepdims=True)
+        P = np.exp(S)
+        P /= P.sum(axis=1, keepdims=True)
+        out[:, c] = P @ V[:, c]
+    return out @ Wa["Wo"].T
+
+
 def frozen_prefix(net: Net, x):
-    """Embedding rows then the frozen blocks ([E2E] 3.1: these never train)."""
+    """Embedding rows then the frozen blocks ([E2E] 3.1: these never train).
+    With attention (R11) x is one whole sequence from position 0."""
     h = np.asarray(net.E[x], dtype=np.float64)
-    for Wb in net.prefix:
+    for p, Wb in enumerate(net.prefix):
+        if net.attn is not None:
+            h = h + attention(net.attn[p], h, net.heads, net.window)
         h, _ = block_forward(net.kind, Wb, h)
     return h
 
@@ -223,9 +271,10 @@ def forward_logits(net: Net, fast, h_in):
     return y @ net.U.T
 
 
-def token_losses(net: Net, fast, x_in, targets):
-    """l_t for each (input, target) pair with fixed weights `fast` (eq. (1))."""
-    logits = forward_logits(net, fast, frozen_prefix(net, x_in))
+def token_losses(net: Net, fast, x_in, targets, h_in=None):
+    """l_t for each (input, target) pair with fixed weights `fast` (eq. (1));
+    h_in: the prefix output of these inputs when already computed."""
+    logits = forward_logits(net, fast, frozen_prefix(net, x_in) if h_in is None else h_in)
     return cross_entropy(logits, targets)[0]
 
 
@@ -291,8 +340,9 @@ def heldout_loss(net: Net, fast, q):
     return float(np.mean(token_losses(net, fast, q[:-1], q[1:])))
 
 
-def softmax_next(net: Net, fast, x_last):
-    logits = forward_logits(net, fast, frozen_prefix(net, np.asarray([x_last])))
+def softmax_next(net: Net, fast, x_last, h_last=None):
+    h = frozen_prefix(net, np.asarray([x_last])) if h_last is None else h_last
+    logits = forward_logits(net, fast, h)
     return cross_entropy(logits, np.zeros(1, dtype=np.int64))[1][0]
 
 
@@ -314,6 +364,8 @@ class SeqState:
 def settle(net, st: SeqState, q):
     """Settlement ([SGF]): score the candidate st.W against the committed st.Wc
     on held-out q; A >= 0 commits the candidate, otherwise st.W reverts."""
+    if net.attn is not None:
+        raise ValueError("Settlement is not defined with attention (R11)")
     A = heldout_loss(net, st.Wc, q) - heldout_loss(net, st.W, q)
     accept = bool(A >= 0.0)
     if accept:
@@ -330,8 +382,9 @@ def mask_weights(mask):
     return m / max(1.0, float(m.sum()))
 
 
-def _step(net, st: SeqState, x_in, tgt, eta, clip, mask=None):
-    h_in = frozen_prefix(net, x_in)
+def _step(net, st: SeqState, x_in, tgt, eta, clip, mask=None, h_in=None):
+    if h_in is None:
+        h_in = frozen_prefix(net, x_in)
     w = None if mask is None else mask_weights(mask)
     losses, grads = chunk_loss_and_grads(net, st.W, h_in, tgt, w)
     s, norm = clip_scale(grads, clip)
@@ -357,13 +410,17 @@ def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=No
     st = SeqState(W=copy.deepcopy(net.fast0),
                   Wc=copy.deepcopy(net.fast0) if settle_every else None,
                   x_last=int(tokens[-1]), reset_every=reset_every)
+    # with attention (R11) the prefix of x_0 .. x_T is one pass over the sequence
+    H = frozen_prefix(net, tokens) if net.attn is not None else None
+    rows = (lambda lo, hi: None) if H is None else (lambda lo, hi: H[lo:hi])
     losses = np.zeros(T)
     snaps = [copy.deepcopy(st.W)] if snapshots else None
     A_list, acc_list = [], []
     for i in range(n_full):
         lo = i * b
         losses[lo:lo + b] = _step(net, st, tokens[lo:lo + b], tokens[lo + 1:lo + b + 1],
-                                  eta, clip, None if loss_mask is None else loss_mask[lo:lo + b])
+                                  eta, clip, None if loss_mask is None else loss_mask[lo:lo + b],
+                                  rows(lo, lo + b))
         if settle_every and (i + 1) % settle_every == 0:
             e = (i + 1) // settle_every - 1
             A, accept = settle(net, st, settle_q[e])
@@ -374,10 +431,10 @@ def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=No
     if rem:
         lo = n_full * b
         x_in, tgt = tokens[lo:T], tokens[lo + 1:T + 1]
-        losses[lo:] = token_losses(net, st.W, x_in, tgt)
+        losses[lo:] = token_losses(net, st.W, x_in, tgt, rows(lo, T))
         st.pend_in = list(x_in)
         st.pend_tgt = list(tgt)
-    p_next = softmax_next(net, st.W, st.x_last)
+    p_next = softmax_next(net, st.W, st.x_last, rows(T, T + 1))
     return {"losses": losses, "state": st, "p_next": p_next, "A": np.array(A_list),
             "accept": np.array(acc_list, dtype=bool), "snapshots": snaps}
 
@@ -423,6 +480,8 @@ def decode_step(net: Net, st: SeqState, x_new, eta, clip, b):
 
     Returns (l of the new token under the weights that scored it, p_next).
     """
+    if net.attn is not None:
+        raise ValueError("decoding is not defined here with attention (R11)")
     x_new = int(x_new)
     loss = float(token_losses(net, st.W, np.array([st.x_last]), np.array([x_new]))[0])
     st.pend_in.append(st.x_last)

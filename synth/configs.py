@@ -37,6 +37,8 @@ class Workload:
     settle_len: int = 0     # tokens of each held-out chunk q
     reset_every: int = 0    # chunk updates between resets of the fast weights to W_0, 0 = off
     static_mlp: bool = False  # each fast block also holds a frozen MLP, run before its fast one
+    attn_heads: int = 0     # sliding-window attention heads in every frozen prefix block, 0 = none
+    attn_window: int = 0    # its window k (keys t-k+1 .. t)
     rms_eps: float = 1e-6
     uniform_mix: float = 0.05
     init_std: float = 0.02

@@ -12,8 +12,9 @@ Matrix m of the workload is drawn from SeedSequence([seed id, 0, m]) with
 m = 0 for E, 1 for U, then 2 + 3 * block + position-in-block over the prefix
 blocks followed by the fast blocks; with static MLPs in the fast blocks, the
 static MLP of fast block l continues after them at 2 + 3 * (n_prefix + n_fast
-+ l) + position.  Only the generator lives here; the arithmetic of the method
-does not.
++ l) + position; with attention, prefix block p's (Wq, Wk, Wv, Wo) follow
+at 2 + 3 * (n_prefix + 2 * n_fast) + 4 * p + position.  Only the generator
+lives here; the arithmetic of the method does not.
 """
 from __future__ import annotations
 
@@ -77,6 +78,10 @@ def make_weights(wl: Workload) -> dict:
         base = 2 + 3 * (wl.n_prefix + wl.n_fast)
         w["static"] = [{name: _draw(wl, base + 3 * l + pos, shapes[name]) for pos, name in enumerate(mats)}
                        for l in range(wl.n_fast)]
+    if wl.attn_heads:
+        base = 2 + 3 * (wl.n_prefix + 2 * wl.n_fast)
+        w["attn"] = [{name: _draw(wl, base + 4 * p + pos, (wl.d, wl.d))
+                      for pos, name in enumerate(("Wq", "Wk", "Wv", "Wo"))} for p in range(wl.n_prefix)]
     return w
 
 

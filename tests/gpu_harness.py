@@ -23,7 +23,8 @@ def make(wl):
 
 
 def oracle_net(wl, inp):
-    return oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    return oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps,
+                                   heads=wl.attn_heads, window=wl.attn_window)
 
 
 def run_oracle(wl, inp, seqs=None, tokens=None, q=None, loss_mask=None):

@@ -66,8 +66,15 @@ MUTANTS = {
         "            h, _ = block_forward(net.kind, net.static[l], h)      # R10\n        h, _ = block_forward(net.kind, Wb, h)\n",
         "            pass\n        h, _ = block_forward(net.kind, Wb, h)\n"
         "        if net.static is not None:\n            h, _ = block_forward(net.kind, net.static[l], h)\n"),
+    "attention window one too wide": ("return (s <= t) & (s > t - k)", "return (s <= t) & (s >= t - k)"),
+    "attention anti-causal": ("return (s <= t) & (s > t - k)", "return (s >= t) & (s > t - k)"),
+    "attention without 1/sqrt(d_h)": ("Q[:, c] @ K[:, c].T / np.sqrt(dh)", "Q[:, c] @ K[:, c].T"),
+    "attention drops its residual": (
+        "h = h + attention(net.attn[p], h, net.heads, net.window)", "h = attention(net.attn[p], h, net.heads, net.window)"),
+    "attention heads read the first head's columns": ("c = slice(i * dh, (i + 1) * dh)", "c = slice(0, dh)"),
     "p_next with the initial weights": (
-        "p_next = softmax_next(net, st.W, st.x_last)", "p_next = softmax_next(net, net.fast0, st.x_last)"),
+        "p_next = softmax_next(net, st.W, st.x_last, rows(T, T + 1))",
+        "p_next = softmax_next(net, net.fast0, st.x_last, rows(T, T + 1))"),
 }
 
 PINS = [
@@ -91,6 +98,9 @@ PINS = [
     ("test_decoding_a_full_chunk_equals_a_longer_prefill", ()),
     ("test_reset_every_chunk_scores_like_eq4_and_ends_at_w0", ()),
     ("test_static_mlp_gradients_match_central_differences", ()),
+    ("test_attention_by_hand_one_and_two_heads", ()),
+    ("test_attention_with_zero_queries_is_the_window_mean", ()),
+    ("test_attention_sees_exactly_its_receptive_field", ()),
     ("test_static_mlp_runs_before_the_fast_one", ()),
     ("test_reset_splits_the_stream_into_independent_runs", ()),
     ("test_reset_counts_decoded_chunks_too", ()),

@@ -582,3 +582,93 @@ def test_static_mlps_change_the_result():
     a = O.prefill(net, 0.3, 0.0, 4, tok)
     b = O.prefill(with_s, 0.3, 0.0, 4, tok)
     assert np.max(np.abs(a["losses"] - b["losses"])) > 1e-3
+
+
+# ------------------------------------------------------------------ sliding-window attention (R11)
+def _attn_net(E, heads, window, Wa, d, f=3, kind="gelu"):
+    """One frozen block whose MLP is the identity (W2 = 0) after its attention."""
+    V = E.shape[0]
+    mlp = {"W1": np.ones((f, d)), "W2": np.zeros((d, f))}
+    w = {"E": E, "U": np.eye(V, d), "prefix": [mlp], "fast": [{"W1": np.ones((f, d)), "W2": np.zeros((d, f))}],
+         "attn": [Wa]}
+    return O.Net.from_weights(w, kind, ("W1", "W2"), 0.0, heads=heads, window=window)
+
+
+def test_attention_by_hand_one_and_two_heads():
+    """d = 2, tokens (0, 1) with e0 = (1, 0), e1 = (0, 2), every projection the
+    identity.  Position 1 sees (0, 1): one head scores 0 and 4/sqrt(2); two
+    heads (d_h = 1) score (0, 0) and (0, 4); a window of 1 sees itself only."""
+    E = np.array([[1.0, 0.0], [0.0, 2.0]])
+    I = {k: np.eye(2) for k in ("Wq", "Wk", "Wv", "Wo")}
+    e0, e1 = E[0], E[1]
+    h = O.frozen_prefix(_attn_net(E, 1, 2, I, 2), np.array([0, 1]))
+    p = np.exp([0.0, 4.0 / math.sqrt(2.0)])
+    p /= p.sum()
+    np.testing.assert_allclose(h[0], 2 * e0, rtol=1e-14)
+    np.testing.assert_allclose(h[1], e1 + p[0] * e0 + p[1] * e1, rtol=1e-14)
+    h2 = O.frozen_prefix(_attn_net(E, 2, 2, I, 2), np.array([0, 1]))
+    q = np.exp([0.0, 4.0])
+    q /= q.sum()
+    np.testing.assert_allclose(h2[1], e1 + np.array([0.5, 2.0 * q[1]]), rtol=1e-14)
+    h1 = O.frozen_prefix(_attn_net(E, 1, 1, I, 2), np.array([0, 1]))
+    np.testing.assert_allclose(h1[1], 2 * e1, rtol=1e-14)
+
+
+def test_attention_with_zero_queries_is_the_window_mean():
+    """Wq = 0: every score is 0, so position t gets the mean of V over
+    positions max(0, t - k + 1) .. t, then Wo."""
+    rng = np.random.default_rng(140)
+    d, V, k, n = 6, 9, 3, 8
+    E = rng.normal(size=(V, d))
+    Wa = {"Wq": np.zeros((d, d)), "Wk": rng.normal(size=(d, d)), "Wv": rng.normal(size=(d, d)),
+          "Wo": rng.normal(size=(d, d))}
+    x = rng.integers(0, V, size=n)
+    h = O.frozen_prefix(_attn_net(E, 2, k, Wa, d), x)
+    Vv = E[x] @ Wa["Wv"].T
+    for t in range(n):
+        lo = max(0, t - k + 1)
+        np.testing.assert_allclose(h[t], E[x[t]] + Vv[lo:t + 1].mean(axis=0) @ Wa["Wo"].T, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_sees_exactly_its_receptive_field():
+    """Two attention blocks of window k: position t depends on the 2(k - 1) + 1
+    inputs ending at t and on nothing earlier (no positional encoding, so the
+    suffix alone reproduces the row)."""
+    rng = np.random.default_rng(141)
+    d, f, V, k, n = 8, 16, 16, 3, 12
+    blk = lambda: {"W1": rng.normal(0, 0.5, (f, d)), "W2": rng.normal(0, 0.5, (d, f))}
+    att = lambda: {m: rng.normal(0, 0.5, (d, d)) for m in ("Wq", "Wk", "Wv", "Wo")}
+    w = {"E": rng.normal(size=(V, d)), "U": rng.normal(size=(V, d)), "prefix": [blk(), blk()], "fast": [blk()],
+         "attn": [att(), att()]}
+    net = O.Net.from_weights(w, "gelu", ("W1", "W2"), 1e-6, heads=2, window=k)
+    x = rng.integers(0, V, size=n)
+    full = O.frozen_prefix(net, x)
+    r = 2 * (k - 1) + 1
+    np.testing.assert_allclose(O.frozen_prefix(net, x[n - r:])[-1], full[-1], rtol=1e-12, atol=1e-12)
+    x2 = x.copy()
+    x2[n - r - 1] = (x2[n - r - 1] + 1) % V           # just outside: no change
+    np.testing.assert_array_equal(O.frozen_prefix(net, x2)[-1], full[-1])
+    x3 = x.copy()
+    x3[n - r] = (x3[n - r] + 1) % V                   # just inside: a change
+    assert np.max(np.abs(O.frozen_prefix(net, x3)[-1] - full[-1])) > 1e-6
+
+
+def test_attention_prefill_scores_chunks_with_their_context():
+    """With attention the chunk losses depend on the tokens before the chunk
+    (the bigram defect's fix), and decoding or Settlement raise."""
+    rng = np.random.default_rng(142)
+    d, f, V = 8, 16, 16
+    blk = lambda: {"W1": rng.normal(0, 0.5, (f, d)), "W2": rng.normal(0, 0.5, (d, f))}
+    att = {m: rng.normal(0, 0.5, (d, d)) for m in ("Wq", "Wk", "Wv", "Wo")}
+    w = {"E": rng.normal(size=(V, d)), "U": rng.normal(size=(V, d)), "prefix": [blk()], "fast": [blk()],
+         "attn": [att]}
+    net = O.Net.from_weights(w, "gelu", ("W1", "W2"), 1e-6, heads=2, window=6)
+    tok = rand_tokens(V, 1, 12, seed=143)
+    a = O.prefill(net, 0.0, 0.0, 4, tok)
+    tok2 = tok.copy()
+    tok2[0, 2] = (tok2[0, 2] + 1) % V                 # a token of chunk 1 only
+    b = O.prefill(net, 0.0, 0.0, 4, tok2)
+    assert np.max(np.abs(a["losses"][0, 4:8] - b["losses"][0, 4:8])) > 1e-6    # chunk 2 sees it
+    np.testing.assert_array_equal(a["losses"][0, 9:], b["losses"][0, 9:])       # beyond the window: not
+    with pytest.raises(ValueError):
+        O.decode_step(net, a["states"][0], 3, 0.0, 0.0, 4)
