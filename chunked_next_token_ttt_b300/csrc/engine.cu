@@ -126,6 +126,8 @@ struct PrefixBufs {
   OpBuf xop, hout, tmp_a;
   float* tmp_g = nullptr;
   OpBuf swiglu_a;        // p == nullptr: not computed here
+  float* qkv32 = nullptr;  // attention: Q | K | V rows (fp32) and the heads' output;
+  OpBuf att_o;             // only a whole-sequence pass (positions from 0) has them
 };
 
 // Embedding + frozen prefix (and the frozen SwiGLU front of fast block 0 when
@@ -135,6 +137,26 @@ static ttt_status prefix_pass(ttt_handle* h, const TokView& tv, const PrefixBufs
   OpBuf cur = h->n_pre > 0 ? pb.xop : pb.hout;
   TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(stg, B, tv, h->E, d, pb.x32, cur.p, cur.lo, st); }));
   for (int p = 0; p < h->n_pre; ++p) {
+    if (p < h->dm.n_prefix && h->dm.attn_heads > 0) {
+      // h += Attn(h): one projection to Q | K | V, the windowed heads, Wo with the residual
+      if (!pb.qkv32 || tv.tok_off != 0)
+        return fail(TTT_ERR_UNSUPPORTED, "attention runs in whole-sequence prefix passes only");
+      const int H = h->dm.attn_heads;
+      GemmDesc gq;
+      gq.M = M; gq.N = 3 * d; gq.K = d;
+      setA(gq, cur, d); setB(gq, h->attn_qkv[p], d);
+      gq.epi = EPI_STORE_F32; gq.out = pb.qkv32; gq.ldo = 3 * d;
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
+      TTT_TRY(run(h, K_ATTN, st, 1, [&] {
+        return launch_swa(stg, B, tv.rows, H, d / H, h->dm.attn_window, pb.qkv32, pb.att_o.p, pb.att_o.lo, st);
+      }));
+      GemmDesc go;
+      go.M = M; go.N = d; go.K = d;
+      setA(go, pb.att_o, d); setB(go, h->attn_o[p], d);
+      go.epi = EPI_RESID; go.aux = pb.x32; go.ldx = d; go.out = pb.x32; go.ldo = d;
+      setOut2(go, cur, d);
+      TTT_TRY(rungemm(h, K_GEMM_PREFIX, go, st));
+    }
     const OpBuf* W = &h->prefix[(size_t)p * h->nm];
     const OpBuf next = (p == h->n_pre - 1) ? pb.hout : pb.xop;
     if (h->dm.block_kind == TTT_BLOCK_GELU) {
@@ -506,10 +528,11 @@ static ttt_status settle_event(ttt_handle* h, const int32_t* q, int Lq, float* A
   });
 }
 
-static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t st) {
+static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t st,
+                                      const Hoisted& hz = Hoisted()) {
   TokView tv;
   tv.tok = h->pend; tv.tok_ld = h->b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 0;
-  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, true, st));
+  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, true, st, hz));
   TTT_TRY(run(h, K_OTHER, st, 2, [&] {
     return launch_softmax(h->B, h->V, h->logits32, p_out, h->lse_next, h->soft_part, st);
   }));
@@ -618,6 +641,47 @@ static ttt_status ensure_staging(ttt_handle* h, void** p, size_t* cap, size_t by
   return TTT_OK;
 }
 
+static void dfree(ttt_handle* h, void* p) {
+  if (!p) return;
+  for (auto& a : h->allocs)
+    if (a == p) a = nullptr;
+  cudaFree(p);
+}
+
+// Buffers of the whole-sequence prefix pass of an attention prefill: `rows`
+// = B * (T + 1) rows, reallocated only when a longer prefill arrives.
+static ttt_status ensure_attn_rows(ttt_handle* h, size_t rows) {
+  if (rows <= h->arows_cap) return TTT_OK;
+  const size_t planes = h->stg == ST_SPLIT ? 2 : 1;
+  OpBuf* ops[] = {&h->ax_op, &h->ax_xop, &h->ax_tmp_a, &h->ax_a, &h->att_o};
+  for (OpBuf* b : ops) {
+    dfree(h, b->p);
+    *b = OpBuf();
+  }
+  dfree(h, h->ax32); h->ax32 = nullptr;
+  dfree(h, h->ax_tmp_g); h->ax_tmp_g = nullptr;
+  dfree(h, h->qkv32); h->qkv32 = nullptr;
+  h->arows_cap = 0;
+  const size_t d = h->d, f = h->f;
+  auto op = [&](OpBuf* b, size_t count) -> ttt_status {
+    TTT_TRY(dalloc(h, &b->p, count * h->esz * planes));
+    b->lo = planes == 2 ? (long long)count : 0;
+    return TTT_OK;
+  };
+  TTT_TRY(dalloc(h, &h->ax32, rows * d * 4));
+  TTT_TRY(op(&h->ax_op, rows * d));
+  TTT_TRY(op(&h->ax_xop, rows * d));
+  TTT_TRY(op(&h->ax_tmp_a, rows * f));
+  TTT_TRY(op(&h->att_o, rows * d));
+  TTT_TRY(dalloc(h, &h->qkv32, rows * 3 * d * 4));
+  if (h->dm.block_kind == TTT_BLOCK_SWIGLU) {
+    TTT_TRY(dalloc(h, &h->ax_tmp_g, rows * f * 4));
+    TTT_TRY(op(&h->ax_a, rows * f));
+  }
+  h->arows_cap = rows;
+  return TTT_OK;
+}
+
 static ttt_status copy_in(ttt_handle* h, const void* src, void** stage, size_t* cap, size_t bytes,
                           const void** dev, cudaStream_t st) {
   if (is_device_ptr(src)) {
@@ -657,7 +721,7 @@ const char* ttt_last_error(void) { return g_last_error.c_str(); }
 static const char* kKClassNames[K_COUNT] = {
     "embed", "gemm_prefix", "gemm_fast_fwd", "rmsnorm_fwd", "gemm_head", "ce_fused",
     "gemm_head_bwd", "rmsnorm_bwd", "gemm_bwd_dx", "gemm_dw", "grad_norm", "clip_sgd_update",
-    "settle", "other", "token_step"};
+    "settle", "other", "token_step", "attention"};
 
 const char* ttt_kernel_class_name(int c) { return (c >= 0 && c < K_COUNT) ? kKClassNames[c] : ""; }
 int ttt_kernel_class_count(void) { return K_COUNT; }
@@ -696,6 +760,13 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if (D.block_kind == TTT_BLOCK_SWIGLU && (D.fast_mask != TTT_FAST_WD || D.n_fast != 1))
     return fail(TTT_ERR_UNSUPPORTED, "SwiGLU runs with one fast block whose down projection is fast");
   if (D.static_mlp != 0 && D.static_mlp != 1) return fail(TTT_ERR_BAD_ARG, "static_mlp must be 0 or 1");
+  if (D.attn_heads < 0 || D.attn_window < 0 || (D.attn_heads > 0 && (D.n_prefix < 1 || D.attn_window < 1)))
+    return fail(TTT_ERR_BAD_ARG, "attention needs n_prefix >= 1 and attn_window >= 1");
+  if (D.attn_heads > 0 && !swa_supported(D.d, D.attn_heads))
+    return fail(TTT_ERR_UNSUPPORTED, "attention needs d % attn_heads == 0 and d / attn_heads <= 256");
+  if (D.attn_heads > 0 && hp->settle_every > 0)
+    return fail(TTT_ERR_UNSUPPORTED, "Settlement with attention is not built");
+  if (D.attn_heads > 0 && !w->attn) return fail(TTT_ERR_BAD_ARG, "null attention weight pointer");
   if (D.static_mlp && D.block_kind != TTT_BLOCK_GELU)
     return fail(TTT_ERR_UNSUPPORTED, "static MLPs run in GELU fast blocks");
   if (!w->E || !w->U || (D.n_prefix > 0 && !w->prefix) || !w->fast || (D.static_mlp && !w->statics))
@@ -742,7 +813,8 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
 
   // ---- weights
   float* stage = nullptr;
-  const size_t big = (size_t)V * d > (size_t)h->n ? (size_t)V * d : (size_t)h->n;
+  size_t big = (size_t)V * d > (size_t)h->n ? (size_t)V * d : (size_t)h->n;
+  if ((size_t)d * d > big) big = (size_t)d * d;     // attention projections
   ttt_status s;
   if ((s = dalloc(h, &stage, big * 4)) != TTT_OK) return bail(s);
   auto upload = [&](const float* src, size_t count, const OpBuf& dst, int stg) -> ttt_status {
@@ -769,6 +841,20 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
     const float* src = i < (size_t)D.n_prefix * h->nm ? w->prefix[i] : w->statics[i - (size_t)D.n_prefix * h->nm];
     if ((s = op_alloc(&h->prefix[i], (size_t)h->n)) != TTT_OK) return bail(s);
     if ((s = upload(src, (size_t)h->n, h->prefix[i], h->stg)) != TTT_OK) return bail(s);
+  }
+  if (D.attn_heads > 0) {
+    const size_t dd = (size_t)d * d;
+    h->attn_qkv.assign(D.n_prefix, OpBuf());
+    h->attn_o.assign(D.n_prefix, OpBuf());
+    for (int p = 0; p < D.n_prefix; ++p) {
+      if ((s = op_alloc(&h->attn_qkv[p], 3 * dd)) != TTT_OK) return bail(s);
+      for (int j = 0; j < 3; ++j)
+        if ((s = upload(w->attn[(size_t)p * 4 + j], dd, op_at(h, h->attn_qkv[p], (long long)(j * dd)), h->stg)) !=
+            TTT_OK)
+          return bail(s);
+      if ((s = op_alloc(&h->attn_o[p], dd)) != TTT_OK) return bail(s);
+      if ((s = upload(w->attn[(size_t)p * 4 + 3], dd, h->attn_o[p], h->stg)) != TTT_OK) return bail(s);
+    }
   }
   if (D.static_mlp) {
     h->statics.assign((size_t)D.n_fast * h->nm, OpBuf());
@@ -958,7 +1044,31 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
                           h->dm.block_kind == TTT_BLOCK_GELU && h->stg == ST_F32 && h->hp.settle_every == 0 &&
                           h->hp.reset_every == 0 &&
                           token_steps_supported(h->d, h->f, h->V) && !(env_tok && std::string(env_tok) == "0");
-  if (token_path && n_full > 0) {
+  const bool attn = h->dm.attn_heads > 0;
+  Hoisted hz_all;     // attention: the prefix of x_0 .. x_T of every sequence, one pass
+  if (attn) {
+    const long long R = (long long)T + 1;
+    TTT_TRY(ensure_attn_rows(h, (size_t)B * R));
+    TokView tv;
+    tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = 0; tv.rows = (int)R; tv.n_valid = (int)R;
+    tv.vocab = h->V;
+    tv.err = h->flag;
+    PrefixBufs pb;
+    pb.x32 = h->ax32; pb.xop = h->ax_xop; pb.hout = h->ax_op; pb.tmp_a = h->ax_tmp_a; pb.tmp_g = h->ax_tmp_g;
+    pb.swiglu_a = h->ax_a;
+    pb.qkv32 = h->qkv32; pb.att_o = h->att_o;
+    TTT_TRY(prefix_pass(h, tv, pb, st));
+    hz_all.on = true; hz_all.rows_total = R;
+    hz_all.x32 = h->ax32; hz_all.op = h->ax_op; hz_all.a = h->ax_a;
+    for (int i = 0; i < n_full; ++i) {
+      TokView tc;
+      tc.tok = tok; tc.tok_ld = T + 1; tc.tok_off = (long long)i * b; tc.rows = b; tc.n_valid = b;
+      Hoisted hz = hz_all;
+      hz.row0 = (long long)i * b;
+      TTT_TRY(chunk_step(h, tc, loss_d, T, (long long)i * b, st, hz, mask, T));
+    }
+  }
+  if (token_path && n_full > 0 && !attn) {
     TTT_TRY(run(h, K_TOKEN, st, 1, [&] {
       return launch_token_steps(B, tok, T + 1, n_full, mask, T, static_cast<const float*>(h->E),
                                 static_cast<const float*>(h->U.p), h->W32, static_cast<float*>(h->Wop.p),
@@ -970,7 +1080,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   // chunks in groups whose frozen prefix runs as one pass before the group's TTT steps
   const int G = h->hoist_chunks;
 
-  for (int i0 = token_path ? n_full : 0; i0 < n_full; i0 += G) {
+  for (int i0 = (token_path || attn) ? n_full : 0; i0 < n_full; i0 += G) {
     const int g = n_full - i0 < G ? n_full - i0 : G;
     TTT_TRY(hoisted_prefix(h, tok, T + 1, i0, g, st));
     for (int i = i0; i < i0 + g; ++i) {
@@ -990,7 +1100,9 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   if (rem > 0) {   // the tail is scored only (and, as decoding, never masked)
     TokView tv;
     tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = (long long)n_full * b; tv.rows = rem; tv.n_valid = rem;
-    TTT_TRY(forward(h, tv, false, false, loss_d, T, (long long)n_full * b, false, st));
+    Hoisted hz = hz_all;
+    hz.row0 = (long long)n_full * b;
+    TTT_TRY(forward(h, tv, false, false, loss_d, T, (long long)n_full * b, false, st, hz));
   }
   // pending decode buffer: tokens x_{n_full b} .. x_T
   TTT_CUDA(cudaMemcpy2DAsync(h->pend, (size_t)(b + 1) * 4, tok + (size_t)n_full * b, (size_t)(T + 1) * 4,
@@ -999,7 +1111,9 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   h->has_context = true;
   if (p_next) {
     const bool dev = is_device_ptr(p_next);
-    TTT_TRY(p_next_from_pending(h, dev ? p_next : h->p_dev, st));
+    Hoisted hz = hz_all;       // attention: x_T's prefix row from the whole-sequence pass
+    hz.row0 = T;
+    TTT_TRY(p_next_from_pending(h, dev ? p_next : h->p_dev, st, hz));
     if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
   }
   if (loss_host) TTT_CUDA(cudaMemcpyAsync(losses, loss_d, (size_t)B * T * 4, cudaMemcpyDeviceToHost, st));
@@ -1012,6 +1126,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
 ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, float* loss, ttt_stream stream) {
   if (!h || !x_new || !p_next) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_decode_step");
   if (!h->has_context) return fail(TTT_ERR_STATE, "decode before prefill");
+  if (h->dm.attn_heads > 0) return fail(TTT_ERR_UNSUPPORTED, "decoding with attention is not built");
   cudaStream_t st = (cudaStream_t)stream;
   const int B = h->B, b = h->b;
   h->launches = 0;
@@ -1063,6 +1178,7 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
 ttt_status ttt_settle(ttt_handle* h, const int32_t* q, int Lq, uint8_t* accept, float* A, ttt_stream stream) {
   if (!h || !q || !accept || !A) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_settle");
   if (Lq != h->hp.settle_len || Lq < 2) return fail(TTT_ERR_BAD_SHAPE, "Lq must equal settle_len (>= 2)");
+  if (h->dm.attn_heads > 0) return fail(TTT_ERR_UNSUPPORTED, "Settlement with attention is not built");
   cudaStream_t st = (cudaStream_t)stream;
   const int B = h->B;
   h->launches = 0;

@@ -10,7 +10,7 @@
 // Kernel classes for launch accounting and per-class timing.
 enum KClass {
   K_EMBED = 0, K_GEMM_PREFIX, K_GEMM_FAST_FWD, K_RMSNORM_FWD, K_GEMM_HEAD, K_CE, K_GEMM_HEAD_BWD,
-  K_RMSNORM_BWD, K_GEMM_BWD_DX, K_GEMM_DW, K_NORM, K_SGD, K_SETTLE, K_OTHER, K_TOKEN, K_COUNT
+  K_RMSNORM_BWD, K_GEMM_BWD_DX, K_GEMM_DW, K_NORM, K_SGD, K_SETTLE, K_OTHER, K_TOKEN, K_ATTN, K_COUNT
 };
 
 // An operand-storage buffer: its pointer and, for ST_SPLIT, the element
@@ -38,6 +38,15 @@ struct ttt_handle {
   std::vector<OpBuf> prefix;         // [n_pre * nm]: the frozen blocks, then (static_mlp) fast block 0's static MLP
   int n_pre = 0;                     // frozen blocks the prefix pass runs
   std::vector<OpBuf> statics;        // [n_fast * nm] static MLP of fast block l >= 1 (static_mlp)
+  // sliding-window attention of the frozen prefix blocks (attn_heads > 0)
+  std::vector<OpBuf> attn_qkv;       // [n_prefix] (Wq | Wk | Wv) as one [3d, d] operand
+  std::vector<OpBuf> attn_o;         // [n_prefix] Wo [d, d]
+  // whole-sequence prefix pass of an attention prefill, B * (T + 1) rows, grown on demand
+  size_t arows_cap = 0;
+  float* ax32 = nullptr;
+  OpBuf ax_op, ax_xop, ax_tmp_a, ax_a, att_o;
+  float* ax_tmp_g = nullptr;
+  float* qkv32 = nullptr;
   std::vector<OpBuf> fastfrozen;     // [n_fast * nm], empty where fast
 
   // fast weights: arenas [slot][B][n]

@@ -127,6 +127,14 @@ ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T
                               float* W32, float* Wop, int slot_w1, int slot_w2, float* losses, long long loss_ld,
                               int d, int f, int V, float eps, float eta, float clip, int* err, cudaStream_t st);
 
+// Sliding-window attention of the frozen blocks (attention.cu): for B
+// sequences of `rows` positions, qkv [B][rows][3d] fp32 (Q | K | V of each
+// row, d = H * dh), out [B][rows][d] in operand type: per head,
+// softmax(Q K^T / sqrt(dh)) V over keys t - window < s <= t.
+bool swa_supported(int d, int heads);
+ttt_status launch_swa(int stg, int B, int rows, int H, int dh, int window, const float* qkv, void* out,
+                      long long out_lo, cudaStream_t st);
+
 // Shift the pending decode buffer: tok[s][0] = tok[s][b].
 ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st);
 

@@ -34,7 +34,7 @@ class Dims(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("d_ff", ctypes.c_int), ("vocab", ctypes.c_int),
                 ("n_prefix", ctypes.c_int), ("n_fast", ctypes.c_int), ("block_kind", ctypes.c_int),
                 ("fast_mask", ctypes.c_int), ("dtype", ctypes.c_int), ("rms_eps", ctypes.c_float),
-                ("static_mlp", ctypes.c_int)]
+                ("static_mlp", ctypes.c_int), ("attn_heads", ctypes.c_int), ("attn_window", ctypes.c_int)]
 
 
 class HParams(ctypes.Structure):
@@ -46,7 +46,7 @@ class HParams(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("E", ctypes.c_void_p), ("U", ctypes.c_void_p),
                 ("prefix", ctypes.POINTER(ctypes.c_void_p)), ("fast", ctypes.POINTER(ctypes.c_void_p)),
-                ("statics", ctypes.POINTER(ctypes.c_void_p))]
+                ("statics", ctypes.POINTER(ctypes.c_void_p)), ("attn", ctypes.POINTER(ctypes.c_void_p))]
 
 
 _lib = None
@@ -134,9 +134,11 @@ class Handle:
     """One libttt handle: a network, its TTT hyper-parameters and B sequences."""
 
     def __init__(self, *, d, d_ff, vocab, n_prefix, n_fast, block, fast_mats, dtype, eta, clip, chunk,
-                 B, weights, settle_every=0, settle_len=0, rms_eps=1e-6, reset_every=0, static_mlp=False):
-        """weights: {"E", "U", "prefix": [block dicts], "fast": [block dicts]} and,
-        with static_mlp, "static": one frozen MLP (block dict) per fast block."""
+                 B, weights, settle_every=0, settle_len=0, rms_eps=1e-6, reset_every=0, static_mlp=False,
+                 attn_heads=0, attn_window=0):
+        """weights: {"E", "U", "prefix": [block dicts], "fast": [block dicts]};
+        with static_mlp, "static": one frozen MLP (block dict) per fast block;
+        with attn_heads > 0, "attn": one {"Wq", "Wk", "Wv", "Wo"} per prefix block."""
         self.lib = load_library()
         self.block = block
         self.mats = MATS[block]
@@ -147,7 +149,7 @@ class Handle:
         for m in fast_mats:
             mask |= FAST_BIT[m]
         self._dims = Dims(d, d_ff, vocab, n_prefix, n_fast, BLOCK[block], mask, DTYPE[dtype], rms_eps,
-                          1 if static_mlp else 0)
+                          1 if static_mlp else 0, attn_heads, attn_window)
         self._hp = HParams(eta, clip, chunk, settle_every, B, settle_len, reset_every)
         keep = []
 
@@ -167,10 +169,13 @@ class Handle:
         fst_arr = (ctypes.c_void_p * len(fst))(*fst)
         sta = [f32(b[m]) for b in weights["static"] for m in self.mats] if static_mlp else []
         sta_arr = (ctypes.c_void_p * max(1, len(sta)))(*sta)
+        att = [f32(b[m]) for b in weights["attn"] for m in ("Wq", "Wk", "Wv", "Wo")] if attn_heads else []
+        att_arr = (ctypes.c_void_p * max(1, len(att)))(*att)
         w = Weights(f32(weights["E"]), f32(weights["U"]),
                     ctypes.cast(pre_arr, ctypes.POINTER(ctypes.c_void_p)),
                     ctypes.cast(fst_arr, ctypes.POINTER(ctypes.c_void_p)),
-                    ctypes.cast(sta_arr, ctypes.POINTER(ctypes.c_void_p)) if static_mlp else None)
+                    ctypes.cast(sta_arr, ctypes.POINTER(ctypes.c_void_p)) if static_mlp else None,
+                    ctypes.cast(att_arr, ctypes.POINTER(ctypes.c_void_p)) if attn_heads else None)
         h = ctypes.c_void_p()
         _check(self.lib.ttt_create(ctypes.byref(self._dims), ctypes.byref(self._hp), ctypes.byref(w),
                                    ctypes.byref(h)), "ttt_create")
@@ -183,7 +188,8 @@ class Handle:
                    block=wl.block, fast_mats=wl.fast_mats, dtype=wl.dtype, eta=wl.eta, clip=wl.clip,
                    chunk=wl.chunk, B=wl.B if B is None else B, weights=weights,
                    settle_every=wl.settle_every, settle_len=wl.settle_len, rms_eps=wl.rms_eps,
-                   reset_every=wl.reset_every, static_mlp=wl.static_mlp)
+                   reset_every=wl.reset_every, static_mlp=wl.static_mlp, attn_heads=wl.attn_heads,
+                   attn_window=wl.attn_window)
 
     def close(self):
         if getattr(self, "_h", None):

@@ -98,6 +98,15 @@ typedef struct {
                        ("End-to-End TTT" review, 3.1, Two MLP layers per
                        block): h += MLP_s(h); h += MLP_f(h).  GELU blocks
                        only; 0 = off                                          */
+  int attn_heads;   /* > 0: every frozen prefix block runs sliding-window
+                       multi-head attention before its MLP ("End-to-End TTT"
+                       review, Method: the sliding-window attention fix of
+                       the bigram defect): h += Attn(h), keys t-k < s <= t,
+                       scale 1/sqrt(d/attn_heads), no positional encoding.
+                       Needs n_prefix >= 1, d % attn_heads == 0,
+                       d/attn_heads <= 256; prefill only (decoding and
+                       Settlement return UNSUPPORTED).  0 = no attention     */
+  int attn_window;  /* k >= 1 when attn_heads > 0                             */
 } ttt_dims;
 
 typedef struct {
@@ -127,6 +136,9 @@ typedef struct {
   const float* const* fast;
   const float* const* statics;   /* static_mlp: n_fast * n_mats pointers, the
                                     frozen MLP of each fast block (NULL otherwise) */
+  const float* const* attn;      /* attn_heads > 0: n_prefix * 4 pointers, (Wq, Wk,
+                                    Wv, Wo) of each prefix block, each [d, d]
+                                    stored [out, in] (NULL otherwise)         */
 } ttt_weights;
 
 typedef struct ttt_handle ttt_handle;

@@ -376,6 +376,58 @@ def test_two_mlp_fast_blocks_decode():
         assert oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats) <= 1e-4
 
 
+def _attention_inputs(wl, qk_scale=8.0):
+    """Seeded inputs whose query and key projections are scaled by a power of
+    two (exact in every storage type), so the windowed softmax is far from
+    uniform."""
+    inp = make(wl)
+    for a in inp["weights"]["attn"]:
+        a["Wq"] = a["Wq"] * np.float32(qk_scale)
+        a["Wk"] = a["Wk"] * np.float32(qk_scale)
+    return inp
+
+
+@pytest.mark.parametrize("case", ["fp32_split", "fp32_rows", "bf16_gelu_static", "bf16_swiglu", "b1", "masked"])
+def test_sliding_window_attention_prefill_against_the_oracle(case):
+    """Frozen blocks with sliding-window attention: the whole-sequence prefix
+    pass (tensor-core projections, the windowed-softmax kernel) feeds every
+    chunk, the ragged tail and p_{T+1}; windows shorter and longer than b,
+    head dimensions below and at the warp width, every storage type."""
+    mask = None
+    if case in ("fp32_split", "masked"):
+        wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=4 * 64 + 5, init_std=0.1,
+                                    attn_heads=4, attn_window=96)
+        if case == "masked":
+            mask = _random_mask(wl.B, wl.T, wl.chunk, seed=5)
+    elif case == "fp32_rows":
+        wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=40, B=3, T=130, n_prefix=1, init_std=0.1,
+                                    attn_heads=3, attn_window=50)
+    elif case == "bf16_gelu_static":
+        wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1024, chunk=64, B=3, T=5 * 64, n_prefix=2, init_std=0.1,
+                                attn_heads=2, attn_window=200, static_mlp=True)
+    elif case == "bf16_swiglu":
+        wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=64, B=2, T=3 * 64 + 9, n_prefix=1,
+                                  init_std=0.1, attn_heads=4, attn_window=64)
+    else:
+        wl = C.TOY_BIGRAM.replace(B=2, T=64, n_prefix=1, init_std=0.1, attn_heads=2, attn_window=8)
+    inp = _attention_inputs(wl)
+    gpu = run_gpu(wl, inp, loss_mask=mask)
+    ref = run_oracle(wl, inp, loss_mask=mask)
+    compare(wl, gpu, ref)
+
+
+def test_attention_handles_refuse_decoding():
+    from chunked_next_token_ttt_b300 import TTTError
+    wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=40, n_prefix=1, attn_heads=2,
+                                attn_window=16)
+    inp = make(wl)
+    h = run_gpu(wl, inp)["handle"]
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    with pytest.raises(TTTError) as e:
+        h.decode_step(torch.zeros(wl.B, dtype=torch.int32, device="cuda"), p)
+    assert e.value.status == 7
+
+
 def test_host_and_device_buffers_agree():
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=32, B=2, T=100, n_prefix=1)
     inp = make(wl)
