@@ -115,7 +115,21 @@ def chunk_flops(wl, rows=None):
         # the persistent per-token kernel: W1 and W2 forward, head, dy = U^T dl,
         # da = W2^T dh, and the two outer-product updates (2 FLOP per FMA)
         per["token_step"] = wl.B * (10.0 * wl.d * wl.d_ff + 4.0 * wl.d * wl.vocab)
+    if wl.attn_heads:
+        # the Q|K|V and Wo projections of every frozen block, and the windowed
+        # attention (Q K^T and P V: 4 d FLOP per (query, key) pair), as a
+        # per-chunk share of the whole-sequence pass over x_0 .. x_T
+        per["gemm_prefix"] += wl.n_prefix * 8.0 * M * wl.d * wl.d
+        per["attention"] = wl.n_prefix * 4.0 * wl.d * wl.B * attention_pairs(wl.T + 1, wl.attn_window) / wl.n_chunks
     return per
+
+
+def attention_pairs(n, k):
+    """Number of (query, key) pairs of a sliding window k over n positions."""
+    m = min(n, k)
+    return m * (m + 1) // 2 + (n - m) * k
+
+
 
 
 def chunk_flops_fwd_one(wl):
@@ -211,7 +225,8 @@ class ClockSampler:
 # ---------------------------------------------------------------- CPU oracle
 def oracle_sample(wl, inp, n_seq, n_chunks):
     import oracle
-    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps,
+                                  heads=wl.attn_heads, window=wl.attn_window)
     tok = inp["tokens"][:n_seq, :n_chunks * wl.chunk + 1]
     t0 = time.perf_counter()
     oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
@@ -373,7 +388,7 @@ def run_ours(args, wl, rank, world, local_rank):
     # device buffers through ttt_decode_step; every call scores the new token,
     # steps when b are pending and returns p_{t+1}
     dec = None
-    if not args.no_decode and wl.settle_every == 0:
+    if not args.no_decode and wl.settle_every == 0 and not wl.attn_heads:
         h.prefill(tok, losses, p)
         xs = torch.from_numpy(np.ascontiguousarray(inp["tokens"][:, 1:wl.chunk + 1].T)).to(dev)   # [b, B]
         dloss = torch.empty((wl.B,), dtype=torch.float32, device=dev)
@@ -419,7 +434,12 @@ def run_ours(args, wl, rank, world, local_rank):
         per_launch = fl_step / launches_per_step_dom
         achieved = per_launch / dom_avg_s / 1e12
         split = wl.dtype == "fp32" and os.environ.get("TTT_FP32_STORAGE") != "f32" and wl.chunk >= 64
-        if dom == "token_step":
+        if dom == "attention":
+            # the windowed-softmax kernel runs on the fp32 FMA pipes of every SM
+            peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"}
+        elif dom == "token_step":
             # one CTA per sequence: the FP32 FMA lanes of the SMs it occupies
             sms = min(wl.B, 148)
             peak = sms * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12

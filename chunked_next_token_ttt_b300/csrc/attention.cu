@@ -3,12 +3,17 @@
 // window k that lets a chunk remember its own tokens before the update; 3.1:
 // attention layers stay frozen during TTT).
 //
-// One warp per (sequence, head, query position t): the lanes split the head
-// dimension; keys t - k + 1 .. t (clipped at position 0) are visited in order
-// with an online softmax (running max, running sum, rescaled accumulator), in
-// batches of four keys whose dot products are reduced together.  Q, K and V
-// come from one fp32 projection buffer [B][rows][3d] (Q | K | V per row);
-// the output is written in the operand type for the Wo projection.
+// One block per (sequence, head, tile of 64 query positions): the tile's
+// queries stay in shared memory while the key/value tiles of 64 positions
+// that the window reaches (t - k + 1 .. t, clipped at 0) stream through it.
+// 256 threads as 16 x 16: thread (ty, tx) owns query rows ty + 16 i and, for
+// the scores, key columns tx + 16 j (i, j < 4); each row's 16 owners sit in
+// one half-warp and keep its online-softmax state (running max, running
+// sum) with shuffles.  Probabilities go through shared memory to the P V
+// product, where the same thread owns output columns tx + 16 c.  Rows are
+// padded by one float so that the strided column reads hit distinct banks.
+// Q, K and V come from one fp32 projection buffer [B][rows][3d] (Q | K | V
+// per row); the output is written in the operand type for the Wo projection.
 #include <cfloat>
 
 #include "kernels.h"
@@ -16,93 +21,157 @@
 namespace ttt {
 namespace {
 
-constexpr int kAttnWarps = 4;       // query positions per block
-constexpr int kAttnPerLane = 8;     // head dimension up to 256
-constexpr int kAttnKeys = 4;        // keys reduced together
+constexpr int kTile = 64;            // query and key positions per tile
+constexpr int kMaxDh = 128;          // head dimension limit
+constexpr int kOutCols = kMaxDh / 16;
+
+size_t swa_smem_bytes(int dh) { return (size_t)(3 * kTile * (dh + 1) + kTile * (kTile + 1)) * sizeof(float); }
 
 template <typename S>
-__global__ void __launch_bounds__(kAttnWarps * 32)
-    swa_kernel(int rows, int H, int dh, int window, float scale, const float* __restrict__ qkv, void* out,
-               long long out_lo) {
+__global__ void __launch_bounds__(256)
+    swa_tile_kernel(int rows, int H, int dh, int window, float scale, const float* __restrict__ qkv, void* out,
+                    long long out_lo) {
   pdl_wait();
   pdl_launch();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kAttnWarps + warp;
-  if (t >= rows) return;    // whole warps leave; nothing below synchronises the block
+  extern __shared__ float sm[];
+  const int dp = dh + 1;
+  float* Qs = sm;                    // [kTile][dp]
+  float* Ks = Qs + kTile * dp;       // [kTile][dp]
+  float* Vs = Ks + kTile * dp;       // [kTile][dp]
+  float* Ps = Vs + kTile * dp;       // [kTile][kTile + 1]
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int head = blockIdx.y;
   const int d = H * dh;
-  const long long seq0 = (long long)blockIdx.z * rows;
   const long long ld = 3LL * d;
-  const float* qrow = qkv + (seq0 + t) * ld + (long long)head * dh;
-  float q[kAttnPerLane], acc[kAttnPerLane];
-#pragma unroll
-  for (int j = 0; j < kAttnPerLane; ++j) {
-    const int e = lane + 32 * j;
-    q[j] = e < dh ? qrow[e] * scale : 0.0f;
-    acc[j] = 0.0f;
+  const long long seq0 = (long long)blockIdx.z * rows;
+  const int q0 = blockIdx.x * kTile;
+
+  // the query tile, pre-scaled by 1/sqrt(dh); rows past the sequence read 0
+  for (int i = tid; i < kTile * dh; i += 256) {
+    const int r = i / dh, e = i % dh;
+    Qs[r * dp + e] = q0 + r < rows ? qkv[(seq0 + q0 + r) * ld + (long long)head * dh + e] * scale : 0.0f;
   }
-  float m = -FLT_MAX, l = 0.0f;
-  const int u0 = t - window + 1 > 0 ? t - window + 1 : 0;
-  for (int u = u0; u <= t; u += kAttnKeys) {
-    float dot[kAttnKeys];
+  float m[4], l[4], acc[4][kOutCols];
 #pragma unroll
-    for (int c = 0; c < kAttnKeys; ++c) {
-      dot[c] = 0.0f;
-      if (u + c <= t) {
-        const float* krow = qkv + (seq0 + u + c) * ld + d + (long long)head * dh;
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -FLT_MAX;
+    l[i] = 0.0f;
 #pragma unroll
-        for (int j = 0; j < kAttnPerLane; ++j) {
-          const int e = lane + 32 * j;
-          if (e < dh) dot[c] = fmaf(q[j], krow[e], dot[c]);
+    for (int c = 0; c < kOutCols; ++c) acc[i][c] = 0.0f;
+  }
+  const int lo = q0 - window + 1 > 0 ? q0 - window + 1 : 0;
+  const int hi = q0 + kTile - 1 < rows - 1 ? q0 + kTile - 1 : rows - 1;
+  for (int k0 = (lo / kTile) * kTile; k0 <= hi; k0 += kTile) {
+    __syncthreads();   // the previous tile's P V reads are done (and the Q tile is stored)
+    for (int i = tid; i < kTile * dh; i += 256) {
+      const int r = i / dh, e = i % dh;
+      const bool in = k0 + r < rows;
+      const long long row = (seq0 + k0 + r) * ld + (long long)head * dh + e;
+      Ks[r * dp + e] = in ? qkv[row + d] : 0.0f;
+      Vs[r * dp + e] = in ? qkv[row + 2LL * d] : 0.0f;
+    }
+    __syncthreads();
+    float sc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[i][j] = 0.0f;
+    for (int e = 0; e < dh; ++e) {
+      float qv[4], kv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[i] = Qs[(ty + 16 * i) * dp + e];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kv[j] = Ks[(tx + 16 * j) * dp + e];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[i][j] = fmaf(qv[i], kv[j], sc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int qp = q0 + ty + 16 * i;
+      bool ok[4];
+      float rmax = -FLT_MAX;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int kp = k0 + tx + 16 * j;
+        ok[j] = kp <= qp && kp > qp - window && kp < rows;
+        if (ok[j]) rmax = fmaxf(rmax, sc[i][j]);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+      const float mn = fmaxf(m[i], rmax);
+      const float corr = expf(m[i] - mn);
+      float rsum = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float p = ok[j] ? expf(sc[i][j] - mn) : 0.0f;
+        rsum += p;
+        Ps[(ty + 16 * i) * (kTile + 1) + tx + 16 * j] = p;
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, o);
+      l[i] = l[i] * corr + rsum;
+      m[i] = mn;
+#pragma unroll
+      for (int c = 0; c < kOutCols; ++c) acc[i][c] *= corr;
+    }
+    __syncthreads();
+    for (int key = 0; key < kTile; ++key) {
+      float pv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pv[i] = Ps[(ty + 16 * i) * (kTile + 1) + key];
+#pragma unroll
+      for (int c = 0; c < kOutCols; ++c) {
+        const int col = tx + 16 * c;
+        if (col < dh) {
+          const float v = Vs[key * dp + col];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i][c] = fmaf(pv[i], v, acc[i][c]);
         }
       }
     }
+  }
 #pragma unroll
-    for (int c = 0; c < kAttnKeys; ++c) dot[c] = warp_sum(dot[c]);
+  for (int i = 0; i < 4; ++i) {
+    const int qp = q0 + ty + 16 * i;
+    if (qp >= rows) continue;
+    const float inv = 1.0f / l[i];
 #pragma unroll
-    for (int c = 0; c < kAttnKeys; ++c) {
-      if (u + c <= t) {
-        const float* vrow = qkv + (seq0 + u + c) * ld + 2LL * d + (long long)head * dh;
-        const float mn = fmaxf(m, dot[c]);
-        const float corr = expf(m - mn);
-        const float p = expf(dot[c] - mn);
-        l = l * corr + p;
-#pragma unroll
-        for (int j = 0; j < kAttnPerLane; ++j) {
-          const int e = lane + 32 * j;
-          if (e < dh) acc[j] = fmaf(p, vrow[e], acc[j] * corr);
-        }
-        m = mn;
-      }
+    for (int c = 0; c < kOutCols; ++c) {
+      const int col = tx + 16 * c;
+      if (col < dh) OpIO<S>::store(out, out_lo, (seq0 + qp) * d + (long long)head * dh + col, acc[i][c] * inv);
     }
   }
-  const float inv = 1.0f / l;
-#pragma unroll
-  for (int j = 0; j < kAttnPerLane; ++j) {
-    const int e = lane + 32 * j;
-    if (e < dh) OpIO<S>::store(out, out_lo, (seq0 + t) * d + (long long)head * dh + e, acc[j] * inv);
+}
+
+template <typename S>
+ttt_status launch_swa_typed(int B, int rows, int H, int dh, int window, const float* qkv, void* out,
+                            long long out_lo, cudaStream_t st) {
+  const size_t smem = swa_smem_bytes(dh);
+  static size_t smem_set = 0;
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(swa_tile_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
+    smem_set = smem;
   }
+  const dim3 grid(ceil_div(rows, kTile), H, B);
+  launch_pdl(swa_tile_kernel<S>, grid, 256, smem, st, rows, H, dh, window, 1.0f / sqrtf((float)dh), qkv, out,
+             out_lo);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
 }
 
 }  // namespace
 
-bool swa_supported(int d, int heads) {
-  return heads > 0 && d % heads == 0 && d / heads <= 32 * kAttnPerLane;
-}
+bool swa_supported(int d, int heads) { return heads > 0 && d % heads == 0 && d / heads <= kMaxDh; }
 
 ttt_status launch_swa(int stg, int B, int rows, int H, int dh, int window, const float* qkv, void* out,
                       long long out_lo, cudaStream_t st) {
   if (B == 0 || rows == 0) return TTT_OK;
-  const dim3 grid(ceil_div(rows, kAttnWarps), H, B);
-  const float scale = 1.0f / sqrtf((float)dh);
-  if (stg == ST_BF16)
-    launch_pdl(swa_kernel<bf16>, grid, kAttnWarps * 32, 0, st, rows, H, dh, window, scale, qkv, out, out_lo);
-  else if (stg == ST_SPLIT)
-    launch_pdl(swa_kernel<Split>, grid, kAttnWarps * 32, 0, st, rows, H, dh, window, scale, qkv, out, out_lo);
-  else
-    launch_pdl(swa_kernel<float>, grid, kAttnWarps * 32, 0, st, rows, H, dh, window, scale, qkv, out, out_lo);
-  TTT_CHECK_LAUNCH();
-  return TTT_OK;
+  if (stg == ST_BF16) return launch_swa_typed<bf16>(B, rows, H, dh, window, qkv, out, out_lo, st);
+  if (stg == ST_SPLIT) return launch_swa_typed<Split>(B, rows, H, dh, window, qkv, out, out_lo, st);
+  return launch_swa_typed<float>(B, rows, H, dh, window, qkv, out, out_lo, st);
 }
 
 }  // namespace ttt

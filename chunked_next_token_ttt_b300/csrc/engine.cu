@@ -763,7 +763,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if (D.attn_heads < 0 || D.attn_window < 0 || (D.attn_heads > 0 && (D.n_prefix < 1 || D.attn_window < 1)))
     return fail(TTT_ERR_BAD_ARG, "attention needs n_prefix >= 1 and attn_window >= 1");
   if (D.attn_heads > 0 && !swa_supported(D.d, D.attn_heads))
-    return fail(TTT_ERR_UNSUPPORTED, "attention needs d % attn_heads == 0 and d / attn_heads <= 256");
+    return fail(TTT_ERR_UNSUPPORTED, "attention needs d % attn_heads == 0 and d / attn_heads <= 128");
   if (D.attn_heads > 0 && hp->settle_every > 0)
     return fail(TTT_ERR_UNSUPPORTED, "Settlement with attention is not built");
   if (D.attn_heads > 0 && !w->attn) return fail(TTT_ERR_BAD_ARG, "null attention weight pointer");

@@ -104,7 +104,7 @@ typedef struct {
                        the bigram defect): h += Attn(h), keys t-k < s <= t,
                        scale 1/sqrt(d/attn_heads), no positional encoding.
                        Needs n_prefix >= 1, d % attn_heads == 0,
-                       d/attn_heads <= 256; prefill only (decoding and
+                       d/attn_heads <= 128; prefill only (decoding and
                        Settlement return UNSUPPORTED).  0 = no attention     */
   int attn_window;  /* k >= 1 when attn_heads > 0                             */
 } ttt_dims;

@@ -91,4 +91,13 @@ SETTLE_760M = Workload(
     chain_k=16, chain_alpha=0.3, settle_every=8, settle_len=1024)
 
 WORKLOADS = (TOY_BIGRAM, CHUNKED_FP32, E2E_125M, INPLACE_4B, SETTLE_760M)
-BY_NAME = {w.name: w for w in WORKLOADS}
+
+# The 125M-like stream with sliding-window attention (12 heads of 64) in its
+# nine frozen blocks, window k = 2048 >= b, at T = 16384 (the pages pair
+# k = 8K with b = 1K at 128K context; this keeps k / b = 2 at a length one
+# GPU step measures in well under a second).
+SWA_125M = E2E_125M.replace(name="swa125m_bf16_d768_v32000_b1024_k2048", seed_id=6, T=16384,
+                            attn_heads=12, attn_window=2048)
+
+EXTRA_WORKLOADS = (SWA_125M,)
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
