@@ -434,8 +434,8 @@ def run_ours(args, wl, rank, world, local_rank):
         per_launch = fl_step / launches_per_step_dom
         achieved = per_launch / dom_avg_s / 1e12
         split = wl.dtype == "fp32" and os.environ.get("TTT_FP32_STORAGE") != "f32" and wl.chunk >= 64
-        if dom == "attention":
-            # the windowed-softmax kernel runs on the fp32 FMA pipes of every SM
+        if dom == "attention" and wl.dtype == "fp32" and not split:
+            # the tiled windowed-softmax kernel runs on the fp32 FMA pipes of every SM
             peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
             roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"}

@@ -24,6 +24,7 @@ namespace {
 constexpr int kTile = 64;            // query and key positions per tile
 constexpr int kMaxDh = 128;          // head dimension limit
 constexpr int kOutCols = kMaxDh / 16;
+constexpr int kTc = kSwaTcRows;      // query rows per score block of the tensor-core path
 
 size_t swa_smem_bytes(int dh) { return (size_t)(3 * kTile * (dh + 1) + kTile * (kTile + 1)) * sizeof(float); }
 
@@ -162,7 +163,68 @@ ttt_status launch_swa_typed(int B, int rows, int H, int dh, int window, const fl
   return TTT_OK;
 }
 
+// Masked row softmax of the score blocks of the tensor-core path.  Block j of
+// a sequence holds query rows j*kTc .. j*kTc + kTc - 1 of the padded row space
+// (position = row - pad) and nw window keys starting at padded row
+// j*kTc + kTc - nw; batch entry e is block j0 + e of the flattened (sequence,
+// block) space.  One warp per row: the valid keys (t - k < s <= t, s >= 0,
+// t < rows) form one contiguous range of n; P = exp(S - max) / sum there and
+// 0 elsewhere, written in the operand type (rows of no real query are all 0).
+template <typename S>
+__global__ void __launch_bounds__(256)
+    band_softmax_kernel(long long nrows, int nw, int nqb, int j0, int pad, int rows, int window, float scale,
+                        const float* __restrict__ Sc, void* P, long long p_lo) {
+  pdl_wait();
+  pdl_launch();
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= nrows) return;          // whole warps leave; no block synchronisation below
+  const long long e = row / kTc;
+  const int r = (int)(row % kTc);
+  const long long J = e + j0;
+  const int j = (int)(J % nqb);
+  const int qpos = j * kTc + r - pad;
+  const int ws = j * kTc + kTc - nw;             // padded row of window key 0
+  int n_lo = 0, n_hi = -1;                        // valid keys n_lo .. n_hi
+  if (qpos >= 0 && qpos < rows) {
+    n_hi = qpos + pad - ws;                       // key position == qpos
+    n_lo = n_hi - window + 1;
+    if (pad - ws > n_lo) n_lo = pad - ws;         // key position >= 0
+    if (n_lo < 0) n_lo = 0;
+  }
+  const float* srow = Sc + row * nw;
+  float mx = -FLT_MAX;
+  for (int n = n_lo + lane; n <= n_hi; n += 32) mx = fmaxf(mx, srow[n] * scale);
+  mx = warp_max(mx);
+  float se = 0.0f;
+  for (int n = n_lo + lane; n <= n_hi; n += 32) se += expf(srow[n] * scale - mx);
+  se = warp_sum(se);
+  const float inv = n_hi >= n_lo ? 1.0f / se : 0.0f;
+  for (int n = lane; n < nw; n += 32) {
+    const float v = (n >= n_lo && n <= n_hi) ? expf(srow[n] * scale - mx) * inv : 0.0f;
+    OpIO<S>::store(P, p_lo, row * nw + n, v);
+  }
+}
+
 }  // namespace
+
+ttt_status launch_band_softmax(int stg, long long nbatch, int nw, int nqb, int j0, int pad, int rows, int window,
+                               float scale, const float* Sc, void* P, long long p_lo, cudaStream_t st) {
+  const long long nrows = nbatch * kTc;
+  if (nrows == 0) return TTT_OK;
+  const int grid = (int)((nrows + 7) / 8);
+  if (stg == ST_BF16)
+    launch_pdl(band_softmax_kernel<bf16>, grid, 256, 0, st, nrows, nw, nqb, j0, pad, rows, window, scale, Sc, P,
+               p_lo);
+  else if (stg == ST_SPLIT)
+    launch_pdl(band_softmax_kernel<Split>, grid, 256, 0, st, nrows, nw, nqb, j0, pad, rows, window, scale, Sc, P,
+               p_lo);
+  else
+    launch_pdl(band_softmax_kernel<float>, grid, 256, 0, st, nrows, nw, nqb, j0, pad, rows, window, scale, Sc, P,
+               p_lo);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
 
 bool swa_supported(int d, int heads) { return heads > 0 && d % heads == 0 && d / heads <= kMaxDh; }
 

@@ -126,9 +126,105 @@ struct PrefixBufs {
   OpBuf xop, hout, tmp_a;
   float* tmp_g = nullptr;
   OpBuf swiglu_a;        // p == nullptr: not computed here
-  float* qkv32 = nullptr;  // attention: Q | K | V rows (fp32) and the heads' output;
-  OpBuf att_o;             // only a whole-sequence pass (positions from 0) has them
+  bool attn = false;     // attention buffers present (whole-sequence passes only)
 };
+
+// Row layout of the tensor-core attention of one whole-sequence pass of R
+// positions per sequence with window k: query blocks of Bq rows; each
+// block's window holds nw >= k + Bq - 1 keys ending at its last row; every
+// sequence's rows start after `pad` zero rows (so every window starts inside
+// the buffer) and fill L = nqb * Bq padded rows; the score GEMMs run over the
+// nb = B * nqb - j0 blocks from the first real one (j0 = pad / Bq) on.
+struct SwaGeom {
+  long long Bq, nw, pad, L, nqb, j0, nb;
+};
+
+static long long round_up(long long a, long long m) { return (a + m - 1) / m * m; }
+
+static SwaGeom swa_geom(int B, long long R, int k) {
+  SwaGeom g;
+  g.Bq = kSwaTcRows;
+  g.nw = round_up(k + g.Bq - 1, 16);
+  g.pad = round_up(g.nw > g.Bq ? g.nw - g.Bq : 0, g.Bq);
+  g.L = g.pad + round_up(R, g.Bq);
+  g.nqb = g.L / g.Bq;
+  g.j0 = g.pad / g.Bq;
+  g.nb = (long long)B * g.nqb - g.j0;
+  return g;
+}
+
+// h += Attn(h) for prefix block p over B sequences of `rows` positions from 0:
+// x32 is the fp32 residual stream and cur its operand copy (both [B][rows][d]),
+// updated in place.  One GEMM projects to Q | K | V; fp32 storage then runs
+// the tiled attention kernel, bf16 and split storage the tensor-core form
+// (per head: batched score GEMM over the query blocks' windows, masked row
+// softmax, batched P V GEMM); Wo adds the heads' output to the residual.
+static ttt_status attention_sublayer(ttt_handle* h, int p, int rows, float* x32, const OpBuf& cur, cudaStream_t st) {
+  const int B = h->B, d = h->d, H = h->dm.attn_heads, dh = d / H, k = h->dm.attn_window, stg = h->stg;
+  const long long M = (long long)B * rows;
+  GemmDesc gw;
+  gw.N = d; gw.K = d;
+  setB(gw, h->attn_o[p], d);
+  gw.epi = EPI_RESID;
+  if (stg == ST_F32) {
+    GemmDesc gq;
+    gq.M = M; gq.N = 3 * d; gq.K = d;
+    setA(gq, cur, d); setB(gq, h->attn_qkv[p], d);
+    gq.epi = EPI_STORE_F32; gq.out = h->qkv32; gq.ldo = 3 * d;
+    TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
+    TTT_TRY(run(h, K_ATTN, st, 1, [&] {
+      return launch_swa(stg, B, rows, H, dh, k, h->qkv32, h->att_o.p, h->att_o.lo, st);
+    }));
+    gw.M = M;
+    setA(gw, h->att_o, d);
+    gw.aux = x32; gw.ldx = d; gw.out = x32; gw.ldo = d;
+    setOut2(gw, cur, d);
+    return rungemm(h, K_GEMM_PREFIX, gw, st);
+  }
+  const SwaGeom g = swa_geom(B, rows, k);
+  const long long ld = 3LL * d;
+  // the projections take one GEMM per sequence (the weights are shared, and the
+  // padded rows of sequence s start at s * L + pad)
+  for (int s = 0; s < B; ++s) {
+    GemmDesc gq;
+    gq.M = rows; gq.N = 3 * d; gq.K = d;
+    setA(gq, op_at(h, cur, (long long)s * rows * d), d); setB(gq, h->attn_qkv[p], d);
+    gq.epi = EPI_STORE;
+    setOut(gq, op_at(h, h->qkvp, ((long long)s * g.L + g.pad) * ld), ld);
+    TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
+  }
+  const long long q_row = g.j0 * g.Bq, k_row = g.j0 * g.Bq + g.Bq - g.nw;   // first block's query / window row
+  for (int hh = 0; hh < H; ++hh) {
+    GemmDesc gs;
+    gs.M = g.Bq; gs.N = g.nw; gs.K = dh; gs.batch = (int)g.nb;
+    setA(gs, op_at(h, h->qkvp, q_row * ld + (long long)hh * dh), ld, g.Bq * ld);
+    setB(gs, op_at(h, h->qkvp, k_row * ld + d + (long long)hh * dh), ld, g.Bq * ld);
+    gs.epi = EPI_STORE_F32; gs.out = h->Sc; gs.ldo = g.nw; gs.sO = g.Bq * g.nw;
+    TTT_TRY(rungemm(h, K_ATTN, gs, st));
+    TTT_TRY(run(h, K_ATTN, st, 1, [&] {
+      return launch_band_softmax(stg, g.nb, (int)g.nw, (int)g.nqb, (int)g.j0, (int)g.pad, rows, k,
+                                 1.0f / sqrtf((float)dh), h->Sc, h->Pp.p, h->Pp.lo, st);
+    }));
+    GemmDesc go;
+    go.M = g.Bq; go.N = dh; go.K = g.nw; go.batch = (int)g.nb;
+    setA(go, h->Pp, g.nw, g.Bq * g.nw);
+    go.b_kmajor = false;
+    setB(go, op_at(h, h->qkvp, k_row * ld + 2LL * d + (long long)hh * dh), ld, g.Bq * ld);
+    go.epi = EPI_STORE;
+    setOut(go, op_at(h, h->att_p, q_row * d + (long long)hh * dh), d, g.Bq * d);
+    TTT_TRY(rungemm(h, K_ATTN, go, st));
+  }
+  for (int s = 0; s < B; ++s) {
+    GemmDesc gs = gw;
+    gs.M = rows;
+    setA(gs, op_at(h, h->att_p, ((long long)s * g.L + g.pad) * d), d);
+    float* xs = x32 + (long long)s * rows * d;
+    gs.aux = xs; gs.ldx = d; gs.out = xs; gs.ldo = d;
+    setOut2(gs, op_at(h, cur, (long long)s * rows * d), d);
+    TTT_TRY(rungemm(h, K_GEMM_PREFIX, gs, st));
+  }
+  return TTT_OK;
+}
 
 // Embedding + frozen prefix (and the frozen SwiGLU front of fast block 0 when
 // pb.swiglu_a is set) for the tokens of tv: W-independent work.
@@ -138,24 +234,9 @@ static ttt_status prefix_pass(ttt_handle* h, const TokView& tv, const PrefixBufs
   TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(stg, B, tv, h->E, d, pb.x32, cur.p, cur.lo, st); }));
   for (int p = 0; p < h->n_pre; ++p) {
     if (p < h->dm.n_prefix && h->dm.attn_heads > 0) {
-      // h += Attn(h): one projection to Q | K | V, the windowed heads, Wo with the residual
-      if (!pb.qkv32 || tv.tok_off != 0)
+      if (!pb.attn || tv.tok_off != 0)
         return fail(TTT_ERR_UNSUPPORTED, "attention runs in whole-sequence prefix passes only");
-      const int H = h->dm.attn_heads;
-      GemmDesc gq;
-      gq.M = M; gq.N = 3 * d; gq.K = d;
-      setA(gq, cur, d); setB(gq, h->attn_qkv[p], d);
-      gq.epi = EPI_STORE_F32; gq.out = pb.qkv32; gq.ldo = 3 * d;
-      TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
-      TTT_TRY(run(h, K_ATTN, st, 1, [&] {
-        return launch_swa(stg, B, tv.rows, H, d / H, h->dm.attn_window, pb.qkv32, pb.att_o.p, pb.att_o.lo, st);
-      }));
-      GemmDesc go;
-      go.M = M; go.N = d; go.K = d;
-      setA(go, pb.att_o, d); setB(go, h->attn_o[p], d);
-      go.epi = EPI_RESID; go.aux = pb.x32; go.ldx = d; go.out = pb.x32; go.ldo = d;
-      setOut2(go, cur, d);
-      TTT_TRY(rungemm(h, K_GEMM_PREFIX, go, st));
+      TTT_TRY(attention_sublayer(h, p, tv.rows, pb.x32, cur, st));
     }
     const OpBuf* W = &h->prefix[(size_t)p * h->nm];
     const OpBuf next = (p == h->n_pre - 1) ? pb.hout : pb.xop;
@@ -650,6 +731,38 @@ static void dfree(ttt_handle* h, void* p) {
 
 // Buffers of the whole-sequence prefix pass of an attention prefill: `rows`
 // = B * (T + 1) rows, reallocated only when a longer prefill arrives.
+static ttt_status ensure_op_elems(ttt_handle* h, OpBuf* b, size_t* cap, size_t count, bool zero) {
+  if (count <= *cap) return TTT_OK;
+  dfree(h, b->p);
+  *b = OpBuf();
+  *cap = 0;
+  const size_t planes = h->stg == ST_SPLIT ? 2 : 1;
+  TTT_TRY(dalloc(h, &b->p, count * h->esz * planes));
+  b->lo = planes == 2 ? (long long)count : 0;
+  if (zero) TTT_CUDA(cudaMemset(b->p, 0, count * h->esz * planes));
+  *cap = count;
+  return TTT_OK;
+}
+
+// Buffers of the tensor-core attention for sequences of T + 1 positions.
+static ttt_status ensure_attn_tc(ttt_handle* h, long long R) {
+  const SwaGeom g = swa_geom(h->B, R, h->dm.attn_window);
+  const size_t d = h->d;
+  // zero once: rows the projections never write (the padding) must hold finite values
+  TTT_TRY(ensure_op_elems(h, &h->qkvp, &h->qkvp_cap, (size_t)h->B * g.L * 3 * d, true));
+  TTT_TRY(ensure_op_elems(h, &h->att_p, &h->attp_cap, (size_t)h->B * g.L * d, false));
+  const size_t blk = (size_t)g.nb * g.Bq * g.nw;
+  size_t pp_cap = h->sc_cap;
+  if (blk > h->sc_cap) {
+    dfree(h, h->Sc);
+    h->Sc = nullptr;
+    h->sc_cap = 0;
+    TTT_TRY(dalloc(h, &h->Sc, blk * 4));
+    h->sc_cap = blk;
+  }
+  return ensure_op_elems(h, &h->Pp, &pp_cap, blk, false);
+}
+
 static ttt_status ensure_attn_rows(ttt_handle* h, size_t rows) {
   if (rows <= h->arows_cap) return TTT_OK;
   const size_t planes = h->stg == ST_SPLIT ? 2 : 1;
@@ -672,8 +785,10 @@ static ttt_status ensure_attn_rows(ttt_handle* h, size_t rows) {
   TTT_TRY(op(&h->ax_op, rows * d));
   TTT_TRY(op(&h->ax_xop, rows * d));
   TTT_TRY(op(&h->ax_tmp_a, rows * f));
-  TTT_TRY(op(&h->att_o, rows * d));
-  TTT_TRY(dalloc(h, &h->qkv32, rows * 3 * d * 4));
+  if (h->stg == ST_F32) {
+    TTT_TRY(op(&h->att_o, rows * d));
+    TTT_TRY(dalloc(h, &h->qkv32, rows * 3 * d * 4));
+  }
   if (h->dm.block_kind == TTT_BLOCK_SWIGLU) {
     TTT_TRY(dalloc(h, &h->ax_tmp_g, rows * f * 4));
     TTT_TRY(op(&h->ax_a, rows * f));
@@ -1049,6 +1164,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   if (attn) {
     const long long R = (long long)T + 1;
     TTT_TRY(ensure_attn_rows(h, (size_t)B * R));
+    if (h->stg != ST_F32) TTT_TRY(ensure_attn_tc(h, R));
     TokView tv;
     tv.tok = tok; tv.tok_ld = T + 1; tv.tok_off = 0; tv.rows = (int)R; tv.n_valid = (int)R;
     tv.vocab = h->V;
@@ -1056,7 +1172,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
     PrefixBufs pb;
     pb.x32 = h->ax32; pb.xop = h->ax_xop; pb.hout = h->ax_op; pb.tmp_a = h->ax_tmp_a; pb.tmp_g = h->ax_tmp_g;
     pb.swiglu_a = h->ax_a;
-    pb.qkv32 = h->qkv32; pb.att_o = h->att_o;
+    pb.attn = true;
     TTT_TRY(prefix_pass(h, tv, pb, st));
     hz_all.on = true; hz_all.rows_total = R;
     hz_all.x32 = h->ax32; hz_all.op = h->ax_op; hz_all.a = h->ax_a;

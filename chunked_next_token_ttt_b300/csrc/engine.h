@@ -46,7 +46,12 @@ struct ttt_handle {
   float* ax32 = nullptr;
   OpBuf ax_op, ax_xop, ax_tmp_a, ax_a, att_o;
   float* ax_tmp_g = nullptr;
-  float* qkv32 = nullptr;
+  float* qkv32 = nullptr;            // fp32 storage: Q | K | V rows for the tiled attention kernel
+  // tensor-core attention (bf16 and split storage): padded Q | K | V rows, one
+  // head's score blocks and probabilities, the heads' output in padded rows
+  OpBuf qkvp, Pp, att_p;
+  float* Sc = nullptr;
+  size_t qkvp_cap = 0, sc_cap = 0, attp_cap = 0;
   std::vector<OpBuf> fastfrozen;     // [n_fast * nm], empty where fast
 
   // fast weights: arenas [slot][B][n]

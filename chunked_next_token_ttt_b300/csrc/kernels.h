@@ -132,6 +132,13 @@ ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T
 // row, d = H * dh), out [B][rows][d] in operand type: per head,
 // softmax(Q K^T / sqrt(dh)) V over keys t - window < s <= t.
 bool swa_supported(int d, int heads);
+// The tensor-core path of the same attention materialises, per head, the
+// scores of query blocks of kSwaTcRows rows against their nw-key windows
+// (two batched GEMMs around this masked row softmax); see the engine's
+// prefix pass for the padded row layout.
+constexpr int kSwaTcRows = 128;
+ttt_status launch_band_softmax(int stg, long long nbatch, int nw, int nqb, int j0, int pad, int rows, int window,
+                               float scale, const float* Sc, void* P, long long p_lo, cudaStream_t st);
 ttt_status launch_swa(int stg, int B, int rows, int H, int dh, int window, const float* qkv, void* out,
                       long long out_lo, cudaStream_t st);
 
