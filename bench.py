@@ -148,7 +148,7 @@ def chunk_bytes(wl):
     params = nf * wl.B * wl.d * wl.d_ff
     return {
         "ce_fused": 2.0 * M * wl.vocab * es,
-        "clip_sgd_update": params * (4 + 4 + 4 + 4 + es),   # read W32, dW; write W32; op copy
+        "clip_sgd_update": params * (4 + 4 + 4 + es),   # read W32, dW; write W32 and the operand copy
         "rmsnorm_fwd": M * wl.d * (4 + es),
         "rmsnorm_bwd": M * wl.d * (4 * 3 + 4 + es),
         "embed": M * wl.d * (es + 4 + es),
