@@ -170,6 +170,10 @@ ttt_status launch_swa_typed(int B, int rows, int H, int dh, int window, const fl
 // block) space.  One warp per row: the valid keys (t - k < s <= t, s >= 0,
 // t < rows) form one contiguous range of n; P = exp(S - max) / sum there and
 // 0 elsewhere, written in the operand type (rows of no real query are all 0).
+// 16-byte score loads (nw is a multiple of 16), 4-element stores; a row
+// (nw fp32) stays in L1 across its three passes.  The exponentials use the
+// fast __expf (relative error about 1e-6 over the clipped range of
+// max-subtracted scores).
 template <typename S>
 __global__ void __launch_bounds__(256)
     band_softmax_kernel(long long nrows, int nw, int nqb, int j0, int pad, int rows, int window, float scale,
@@ -192,17 +196,37 @@ __global__ void __launch_bounds__(256)
     if (pad - ws > n_lo) n_lo = pad - ws;         // key position >= 0
     if (n_lo < 0) n_lo = 0;
   }
-  const float* srow = Sc + row * nw;
+  const float4* s4 = reinterpret_cast<const float4*>(Sc + row * nw);
+  const int q_lo = n_lo >> 2, q_hi = n_hi >= 0 ? n_hi >> 2 : -1;
   float mx = -FLT_MAX;
-  for (int n = n_lo + lane; n <= n_hi; n += 32) mx = fmaxf(mx, srow[n] * scale);
+  for (int q = q_lo + lane; q <= q_hi; q += 32) {
+    const float4 v = s4[q];
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (4 * q + c >= n_lo && 4 * q + c <= n_hi) mx = fmaxf(mx, x[c] * scale);
+  }
   mx = warp_max(mx);
   float se = 0.0f;
-  for (int n = n_lo + lane; n <= n_hi; n += 32) se += expf(srow[n] * scale - mx);
+  for (int q = q_lo + lane; q <= q_hi; q += 32) {
+    const float4 v = s4[q];
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (4 * q + c >= n_lo && 4 * q + c <= n_hi) se += __expf(x[c] * scale - mx);
+  }
   se = warp_sum(se);
   const float inv = n_hi >= n_lo ? 1.0f / se : 0.0f;
-  for (int n = lane; n < nw; n += 32) {
-    const float v = (n >= n_lo && n <= n_hi) ? expf(srow[n] * scale - mx) * inv : 0.0f;
-    OpIO<S>::store(P, p_lo, row * nw + n, v);
+  for (int q = lane; q < nw / 4; q += 32) {
+    float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (q >= q_lo && q <= q_hi) {
+      const float4 v = s4[q];
+      const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (4 * q + c >= n_lo && 4 * q + c <= n_hi) o[c] = __expf(x[c] * scale - mx) * inv;
+    }
+    QuadIO<S>::store(P, p_lo, row * nw + 4LL * q, make_float4(o[0], o[1], o[2], o[3]));
   }
 }
 

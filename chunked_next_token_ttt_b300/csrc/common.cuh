@@ -100,6 +100,35 @@ template <> struct OpIO<Split> {
   }
 };
 
+// Four consecutive elements from a float4 in operand storage (16 / 8 / 2 x 8
+// bytes): the start index must keep the access aligned.
+template <typename S> struct QuadIO;
+template <> struct QuadIO<float> {
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float4 w) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p) + i) = w;
+  }
+};
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+template <> struct QuadIO<bf16> {
+  __device__ __forceinline__ static void store(void* p, long long, long long i, float4 w) {
+    *reinterpret_cast<uint2*>(static_cast<bf16*>(p) + i) = pack_bf16x4(w.x, w.y, w.z, w.w);
+  }
+};
+template <> struct QuadIO<Split> {
+  __device__ __forceinline__ static void store(void* p, long long lo, long long i, float4 w) {
+    bf16* q = static_cast<bf16*>(p);
+    const uint2 h = pack_bf16x4(w.x, w.y, w.z, w.w);
+    const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&h);
+    const float2 h0 = __bfloat1622float2(hb[0]), h1 = __bfloat1622float2(hb[1]);
+    *reinterpret_cast<uint2*>(q + i) = h;
+    *reinterpret_cast<uint2*>(q + lo + i) = pack_bf16x4(w.x - h0.x, w.y - h0.y, w.z - h1.x, w.w - h1.y);
+  }
+};
+
+
 // Two adjacent elements (i, i+1) at once; i even and the base (and, for Split,
 // the lo offset) aligned to the pair size.
 template <typename S> struct PairIO;

@@ -158,6 +158,55 @@ __global__ void __launch_bounds__(256) gemm_small_kvec_kernel(GemmDesc g) {
   }
 }
 
+// Shared-weight products of a few rows with few output columns (the frozen
+// blocks and the head of a one-token-per-sequence forward, M = B rows): kw
+// warps share one column, each taking every kw-th 256-wide step of K, and the
+// block sums their partial dot products in a fixed order before the epilogue
+// (lane m takes row m).  This puts kw times more warps in flight than one
+// warp per column, for the narrow and long-K shapes where that is too few.
+template <typename S>
+__global__ void __launch_bounds__(256) gemm_small_ksplit_kernel(GemmDesc g, int kw) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ float part[8][kMaxRows];
+  const int bz = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cw = warp / kw, kp = warp % kw;
+  const int n = blockIdx.x * (8 / kw) + cw;
+  const long long a0 = bz * g.sA, b0 = bz * g.sB;
+  float acc[kMaxRows];
+#pragma unroll
+  for (int m = 0; m < kMaxRows; ++m) acc[m] = 0.0f;
+  if (n < g.N) {
+    for (int k = (kp * 32 + lane) * 8; k < g.K; k += kw * 256) {
+      float bv[8];
+      Vec8<S>::load(g.B, g.loB, b0 + (long long)n * g.ldb + k, bv);
+#pragma unroll
+      for (int m = 0; m < kMaxRows; ++m) {
+        if (m < g.M) {
+          float av[8];
+          Vec8<S>::load(g.A, g.loA, a0 + (long long)m * g.lda + k, av);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[m] = fmaf(av[j], bv[j], acc[m]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kMaxRows; ++m) {
+    if (m < g.M) {
+      const float v = warp_sum(acc[m]);
+      if (lane == 0) part[warp][m] = v;
+    }
+  }
+  __syncthreads();
+  if (kp == 0 && n < g.N && lane < g.M) {
+    float v = 0.0f;
+    for (int q = 0; q < kw; ++q) v += part[cw * kw + q][lane];
+    epi_value<S>(g, bz, lane, n, v);
+  }
+}
+
 bool gemm_small_vec_ok(const GemmDesc& g) {
   auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   const long long m = (long long)g.K | g.lda | g.ldb | g.sA | g.sB | g.loA | g.loB;
@@ -197,6 +246,20 @@ bool gemm_small_vec_ok(const GemmDesc& g);
 // rows the 4 x M accumulators crowd the registers (measured slower)
 int small_cols_per_warp(const GemmDesc& g) { return (g.N >= kWideN && g.M <= 2) ? 4 : 1; }
 
+// warps per output column of the K-split variant (1: not used): a power of
+// two up to 8, at most one 256-wide K step each, until the grid holds about 48
+// warps per SM; never for dW products (their per-block norm partials follow
+// small_grid_x)
+int small_ksplit(const GemmDesc& g) {
+  if (!gemm_small_vec_ok(g) || g.M <= 2 || g.epi == EPI_DW) return 1;
+  const long long cols = (long long)g.N * g.batch;
+  int kmax = ceil_div(g.K, 256);
+  if (kmax > 8) kmax = 8;
+  int kw = 1;
+  while (kw * 2 <= kmax && cols * kw < 148LL * 48) kw *= 2;
+  return kw;
+}
+
 // the deeply unrolled weight-streaming variant (U = 4) suits this product
 bool small_deep_unroll(const GemmDesc& g) { return g.dtype != ST_SPLIT || g.M <= 2; }
 
@@ -231,7 +294,13 @@ ttt_status gemm_small(const GemmDesc& g, cudaStream_t st) {
     else if (g.dtype == ST_SPLIT) launch_pdl(gemm_small_kvec_kernel<Split, CW, U>, grid, 256, 0, st, g); \
     else launch_pdl(gemm_small_kvec_kernel<float, CW, U>, grid, 256, 0, st, g);                          \
   } while (0)
-  if (gemm_small_vec_ok(g) && small_cols_per_warp(g) == 4) TTT_KVEC(4, 2);
+  const int kw = small_ksplit(g);
+  if (kw > 1) {
+    const dim3 kgrid(ceil_div(g.N, 8 / kw), g.batch);
+    if (g.dtype == ST_BF16) launch_pdl(gemm_small_ksplit_kernel<bf16>, kgrid, 256, 0, st, g, kw);
+    else if (g.dtype == ST_SPLIT) launch_pdl(gemm_small_ksplit_kernel<Split>, kgrid, 256, 0, st, g, kw);
+    else launch_pdl(gemm_small_ksplit_kernel<float>, kgrid, 256, 0, st, g, kw);
+  } else if (gemm_small_vec_ok(g) && small_cols_per_warp(g) == 4) TTT_KVEC(4, 2);
   else if (gemm_small_vec_ok(g) && small_deep_unroll(g)) TTT_KVEC(1, 4);
   else if (gemm_small_vec_ok(g)) TTT_KVEC(1, 1);
 #undef TTT_KVEC

@@ -328,6 +328,34 @@ def test_split_k_ragged_residual_twice_in_a_row():
     assert np.abs(outs[0] - ref).max() <= 2e-3 * np.abs(ref).max()
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "bf16x3"])
+@pytest.mark.parametrize("K", [768, 4096])
+def test_small_m_gemm_long_k_split_over_warps(dtype, K):
+    """Eight rows, shared weights, few output columns (a frozen block of a
+    one-token forward): several warps share each column's K range."""
+    rng = np.random.default_rng(12)
+    M, N = 8, 200
+    A = rng.normal(0, 1, (M, K)).astype(np.float32)
+    Bm = rng.normal(0, 1, (N, K)).astype(np.float32)
+    X = rng.normal(0, 1, (M, N)).astype(np.float32)
+    if dtype == "fp32":
+        Ad, Bd, lo = torch.from_numpy(A).cuda(), torch.from_numpy(Bm).cuda(), {}
+        A64, B64 = A.astype(np.float64), Bm.astype(np.float64)
+    elif dtype == "bf16":
+        Ad, Bd, lo = torch.from_numpy(A).to(torch.bfloat16).cuda(), torch.from_numpy(Bm).to(torch.bfloat16).cuda(), {}
+        A64, B64 = _bf(A), _bf(Bm)
+    else:
+        Ad, Bd = split_planes(A).cuda(), split_planes(Bm).cuda()
+        lo = dict(loA=M * K, loB=N * K)
+        A64, B64 = A.astype(np.float64), Bm.astype(np.float64)
+    ref = A64 @ B64.T + X
+    out = torch.from_numpy(X.copy()).cuda()
+    T.op_gemm(T.gemm_args(M, N, K, Ad, Bd, out, dtype=dtype, epi="resid", aux=out, ldx=N, **lo))
+    torch.cuda.synchronize()
+    tol = {"fp32": 1e-5, "bf16": 1e-5, "bf16x3": 6e-5}[dtype] * np.sqrt(K) * (np.abs(ref).max() if dtype != "bf16x3" else 1)
+    assert np.abs(out.cpu().numpy() - ref).max() <= tol
+
+
 @pytest.mark.parametrize("N", [1000, 9000], ids=["narrow", "wide"])
 @pytest.mark.parametrize("M", [1, 3, 8])
 @pytest.mark.parametrize("b_k", [True, False], ids=["B_kmaj", "B_nmaj"])

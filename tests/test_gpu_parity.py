@@ -416,6 +416,33 @@ def test_sliding_window_attention_prefill_against_the_oracle(case):
     compare(wl, gpu, ref)
 
 
+@pytest.mark.parametrize("case", ["window1", "window_beyond_T", "single_sequence_host", "shorter_than_a_chunk",
+                                  "split_dh24"])
+def test_sliding_window_attention_edge_cases(case):
+    """Degenerate windows (k = 1: each position sees itself; k > T: full causal
+    attention), one sequence through host buffers, a prefill shorter than one
+    chunk (no step: scored tail and p_{T+1} only), and a head dimension of 24
+    on the split-storage tensor-core path."""
+    base = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=3 * 64 + 7, n_prefix=1,
+                                  init_std=0.1, attn_heads=4)
+    device = True
+    if case == "window1":
+        wl = base.replace(attn_window=1)
+    elif case == "window_beyond_T":
+        wl = base.replace(attn_window=4096)
+    elif case == "single_sequence_host":
+        wl = base.replace(B=1, attn_window=80)
+        device = False
+    elif case == "shorter_than_a_chunk":
+        wl = base.replace(T=50, attn_window=32)
+    else:
+        wl = base.replace(d=96, d_ff=192, attn_window=100)
+    inp = _attention_inputs(wl)
+    gpu = run_gpu(wl, inp, device=device)
+    ref = run_oracle(wl, inp)
+    compare(wl, gpu, ref)
+
+
 def test_attention_handles_refuse_decoding():
     from chunked_next_token_ttt_b300 import TTTError
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=40, n_prefix=1, attn_heads=2,
