@@ -80,8 +80,11 @@ Readings taken where the pages leave a step open:
       elsewhere.  Positions count the inputs x_0 (BOS) .. of one sequence from
       0; no positional encoding is added (the pages name none).  The fast
       blocks hold no attention, so the whole prefix of a sequence depends on
-      its tokens only and is computed once over x_0 .. x_T.  Decoding and
-      Settlement are not defined here with attention (the held-out chunk's
+      its tokens only and is computed once over x_0 .. x_T.  Decoding goes on
+      at the following positions: a decoded input attends to itself and the
+      k - 1 inputs before it, prefill's included, and the prefix rows of the
+      pending inputs are the ones computed when each input arrived.
+      Settlement is not defined here with attention (the held-out chunk's
       attention context is not fixed by the pages).
 """
 from __future__ import annotations
@@ -359,6 +362,9 @@ class SeqState:
     norms: list = field(default_factory=list)
     scales: list = field(default_factory=list)
     reset_every: int = 0
+    hist: list = field(default_factory=list)      # attention (R11): inputs x_0 .. x_last
+    h_last: object = None                         # attention: prefix row of x_last
+    pend_h: list = field(default_factory=list)    # attention: prefix rows of the pending inputs
 
 
 def settle(net, st: SeqState, q):
@@ -434,6 +440,11 @@ def prefill_sequence(net: Net, eta, clip, b, tokens, settle_every=0, settle_q=No
         losses[lo:] = token_losses(net, st.W, x_in, tgt, rows(lo, T))
         st.pend_in = list(x_in)
         st.pend_tgt = list(tgt)
+        if H is not None:
+            st.pend_h = list(H[lo:T])
+    if H is not None:
+        st.hist = [int(t) for t in tokens]
+        st.h_last = H[T]
     p_next = softmax_next(net, st.W, st.x_last, rows(T, T + 1))
     return {"losses": losses, "state": st, "p_next": p_next, "A": np.array(A_list),
             "accept": np.array(acc_list, dtype=bool), "snapshots": snaps}
@@ -480,17 +491,26 @@ def decode_step(net: Net, st: SeqState, x_new, eta, clip, b):
 
     Returns (l of the new token under the weights that scored it, p_next).
     """
-    if net.attn is not None:
-        raise ValueError("decoding is not defined here with attention (R11)")
     x_new = int(x_new)
-    loss = float(token_losses(net, st.W, np.array([st.x_last]), np.array([x_new]))[0])
+    attn = net.attn is not None
+    h_prev = st.h_last[None, :] if attn else None
+    loss = float(token_losses(net, st.W, np.array([st.x_last]), np.array([x_new]), h_prev)[0])
     st.pend_in.append(st.x_last)
     st.pend_tgt.append(x_new)
+    if attn:
+        # R11: the new input's prefix row sees the receptive field of the
+        # attention layers, (k - 1) per layer before it (the suffix alone
+        # reproduces that row: no positional encoding)
+        st.pend_h.append(st.h_last)
+        st.hist.append(x_new)
+        reach = (net.window - 1) * len(net.prefix) + 1
+        st.h_last = frozen_prefix(net, np.array(st.hist[-reach:]))[-1]
     st.x_last = x_new
     if len(st.pend_in) == b:
-        _step(net, st, np.array(st.pend_in), np.array(st.pend_tgt), eta, clip)
-        st.pend_in, st.pend_tgt = [], []
-    return loss, softmax_next(net, st.W, st.x_last)
+        _step(net, st, np.array(st.pend_in), np.array(st.pend_tgt), eta, clip,
+              h_in=np.array(st.pend_h) if attn else None)
+        st.pend_in, st.pend_tgt, st.pend_h = [], [], []
+    return loss, softmax_next(net, st.W, st.x_last, st.h_last[None, :] if attn else None)
 
 
 def static_losses(net: Net, tokens):

@@ -72,6 +72,11 @@ MUTANTS = {
     "attention drops its residual": (
         "h = h + attention(net.attn[p], h, net.heads, net.window)", "h = attention(net.attn[p], h, net.heads, net.window)"),
     "attention heads read the first head's columns": ("c = slice(i * dh, (i + 1) * dh)", "c = slice(0, dh)"),
+    "decoded input attends to itself only": (
+        "st.h_last = frozen_prefix(net, np.array(st.hist[-reach:]))[-1]",
+        "st.h_last = frozen_prefix(net, np.array(st.hist[-1:]))[-1]"),
+    "decoded chunk recomputes its prefix rows without context": (
+        "h_in=np.array(st.pend_h) if attn else None)", "h_in=None)"),
     "p_next with the initial weights": (
         "p_next = softmax_next(net, st.W, st.x_last, rows(T, T + 1))",
         "p_next = softmax_next(net, net.fast0, st.x_last, rows(T, T + 1))"),
@@ -101,6 +106,8 @@ PINS = [
     ("test_attention_by_hand_one_and_two_heads", ()),
     ("test_attention_with_zero_queries_is_the_window_mean", ()),
     ("test_attention_sees_exactly_its_receptive_field", ()),
+    ("test_decoding_with_attention_equals_a_longer_prefill", (8,)),
+    ("test_decoding_with_attention_equals_a_longer_prefill", (7,)),
     ("test_static_mlp_runs_before_the_fast_one", ()),
     ("test_reset_splits_the_stream_into_independent_runs", ()),
     ("test_reset_counts_decoded_chunks_too", ()),

@@ -671,4 +671,30 @@ def test_attention_prefill_scores_chunks_with_their_context():
     assert np.max(np.abs(a["losses"][0, 4:8] - b["losses"][0, 4:8])) > 1e-6    # chunk 2 sees it
     np.testing.assert_array_equal(a["losses"][0, 9:], b["losses"][0, 9:])       # beyond the window: not
     with pytest.raises(ValueError):
-        O.decode_step(net, a["states"][0], 3, 0.0, 0.0, 4)
+        O.settle(net, a["states"][0], tok[0, :6])
+
+
+@pytest.mark.parametrize("T", [8, 7], ids=["whole_chunks", "ragged"])
+def test_decoding_with_attention_equals_a_longer_prefill(T):
+    """Decoding continues the positions: a prefill of T tokens then decoding
+    to T + extra gives the losses, weights and p_{T+1} of one prefill of
+    T + extra, with two attention layers whose window reaches into prefill."""
+    rng = np.random.default_rng(144)
+    d, f, V = 8, 16, 16
+    blk = lambda: {"W1": rng.normal(0, 0.5, (f, d)), "W2": rng.normal(0, 0.5, (d, f))}
+    att = lambda: {m: rng.normal(0, 0.5, (d, d)) for m in ("Wq", "Wk", "Wv", "Wo")}
+    w = {"E": rng.normal(size=(V, d)), "U": rng.normal(size=(V, d)), "prefix": [blk(), blk()], "fast": [blk()],
+         "attn": [att(), att()]}
+    net = O.Net.from_weights(w, "gelu", ("W1", "W2"), 1e-6, heads=2, window=3)
+    b, extra, eta, c = 4, 9, 0.3, 0.7
+    tok = rand_tokens(V, 1, T + extra, seed=145)
+    long = O.prefill(net, eta, c, b, tok)
+    short = O.prefill(net, eta, c, b, tok[:, :T + 1])
+    st = short["states"][0]
+    dec = []
+    for t in range(T + 1, T + extra + 1):
+        l, p = O.decode_step(net, st, tok[0, t], eta, c, b)
+        dec.append(l)
+    np.testing.assert_allclose(dec, long["losses"][0, T:], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(p, long["p_next"][0], rtol=0, atol=1e-12)
+    assert O.weights_rel_frobenius(st.W, long["W"][0], net.fast_mats) < 1e-13
