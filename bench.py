@@ -388,7 +388,7 @@ def run_ours(args, wl, rank, world, local_rank):
     # device buffers through ttt_decode_step; every call scores the new token,
     # steps when b are pending and returns p_{t+1}
     dec = None
-    if not args.no_decode and wl.settle_every == 0 and not wl.attn_heads:
+    if not args.no_decode and wl.settle_every == 0:
         h.prefill(tok, losses, p)
         xs = torch.from_numpy(np.ascontiguousarray(inp["tokens"][:, 1:wl.chunk + 1].T)).to(dev)   # [b, B]
         dloss = torch.empty((wl.B,), dtype=torch.float32, device=dev)
@@ -413,6 +413,9 @@ def run_ours(args, wl, rank, world, local_rank):
                   + wl.vocab * wl.d) * es
         fast = wl.B * nf * wl.d * wl.d_ff * es
         by = frozen + fast + wl.B * wl.vocab * 4 * 2
+        if wl.attn_heads:
+            # the attention weights and the fp32 K/V cache of every frozen block's window
+            by += wl.n_prefix * (4 * wl.d * wl.d * es + wl.B * 2 * min(wl.T + 1, wl.attn_window) * wl.d * 4)
         bound = wl.B / (by / (pk["hbm_gbs"] * 1e9))
         v = wl.B * wl.chunk / (dms / 1e3)
         dec = {"tokens_per_s": v, "tokens_per_s_wall": wl.B * wl.chunk / wall, "steps": wl.chunk,

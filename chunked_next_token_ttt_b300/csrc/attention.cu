@@ -230,7 +230,160 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Key/value cache of decoding: per frozen block, the K and V rows of the last
+// `window` positions of every sequence, fp32, slot = position % window
+// ([B][window][d] each).  Filled from a whole-sequence pass's projections
+// (rows row0 + pos of a per-sequence stride of seq_rows rows, 3d wide: Q | K | V).
+template <typename S>
+__global__ void kv_fill_kernel(int R, int window, int d, const void* __restrict__ src, long long src_lo,
+                               long long seq_rows, long long row0, float* __restrict__ ck, float* __restrict__ cv) {
+  pdl_wait();
+  pdl_launch();
+  const long long s = blockIdx.y;
+  const int n = R < window ? R : window;
+  const int p0 = R - n;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)n * d;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int pos = p0 + (int)(i / d), e = (int)(i % d);
+    const long long r = (s * seq_rows + row0 + pos) * 3LL * d;
+    const long long c = (s * window + pos % window) * d + e;
+    ck[c] = OpIO<S>::load(src, src_lo, r + d + e);
+    cv[c] = OpIO<S>::load(src, src_lo, r + 2LL * d + e);
+  }
+}
+
+// One decoded position per sequence (`*pos_ptr`, the same for every
+// sequence): one block per (head, sequence) appends the row's K and V to the
+// cache, scores the query against the window's keys (positions pos - n + 1 ..
+// pos, n = min(pos + 1, window)) into shared memory, takes the softmax, and
+// sums the values with the 128 threads split as (key group, head element).
+template <typename S>
+__global__ void __launch_bounds__(128)
+    swa_decode_kernel(int H, int dh, int window, float scale, const int* __restrict__ pos_ptr,
+                      const float* __restrict__ qkv, float* __restrict__ ck, float* __restrict__ cv, void* out,
+                      long long out_lo) {
+  pdl_wait();
+  pdl_launch();
+  extern __shared__ float sm[];
+  float* sc = sm;                  // [window] scores, then probabilities
+  float* qs = sc + window;         // [dh]
+  float* red = qs + dh;            // [32]
+  float* po = red + 32;            // [128] partial outputs
+  const int head = blockIdx.x, tid = threadIdx.x;
+  const long long s = blockIdx.y;
+  const int d = H * dh;
+  const int pos = *pos_ptr;
+  const int slot = pos % window;
+  const float* row = qkv + s * 3LL * d;
+  float* kc = ck + s * (long long)window * d + (long long)head * dh;
+  float* vc = cv + s * (long long)window * d + (long long)head * dh;
+  for (int e = tid; e < dh; e += blockDim.x) {
+    kc[(long long)slot * d + e] = row[d + head * dh + e];
+    vc[(long long)slot * d + e] = row[2 * d + head * dh + e];
+    qs[e] = row[head * dh + e] * scale;
+  }
+  __syncthreads();   // the appended row and the query are visible to the block
+  const int n = pos + 1 < window ? pos + 1 : window;
+  float mx = -FLT_MAX;
+  for (int j = tid; j < n; j += blockDim.x) {
+    const float* kr = kc + (long long)((pos - j) % window) * d;
+    float a = 0.0f;
+    for (int e = 0; e < dh; ++e) a = fmaf(qs[e], kr[e], a);
+    sc[j] = a;
+    mx = fmaxf(mx, a);
+  }
+  mx = warp_max(mx);
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  mx = -FLT_MAX;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
+  float se = 0.0f;
+  for (int j = tid; j < n; j += blockDim.x) {
+    const float p = expf(sc[j] - mx);
+    sc[j] = p;
+    se += p;
+  }
+  se = block_sum(se, red);          // also orders the probability writes before the reads below
+  const int G = (int)blockDim.x / dh;
+  const int g = tid / dh, e = tid % dh;
+  float acc = 0.0f;
+  if (g < G)
+    for (int j = g; j < n; j += G) acc = fmaf(sc[j], vc[(long long)((pos - j) % window) * d + e], acc);
+  if (g < G) po[g * dh + e] = acc;
+  __syncthreads();
+  if (tid < dh) {
+    float o = 0.0f;
+    for (int q = 0; q < G; ++q) o += po[q * dh + tid];
+    OpIO<S>::store(out, out_lo, s * d + (long long)head * dh + tid, o / se);
+  }
+}
+
+__global__ void pos_set_kernel(int* p, int v) {
+  pdl_wait();
+  pdl_launch();
+  *p = v;
+}
+
+__global__ void pos_add_kernel(int* p) {
+  pdl_wait();
+  pdl_launch();
+  *p += 1;
+}
+
 }  // namespace
+
+ttt_status launch_pos_set(int* p, int v, cudaStream_t st) {
+  launch_pdl(pos_set_kernel, 1, 1, 0, st, p, v);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_pos_add(int* p, cudaStream_t st) {
+  launch_pdl(pos_add_kernel, 1, 1, 0, st, p);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_kv_fill(int stg, int B, int R, int window, int d, const void* src, long long src_lo,
+                          long long seq_rows, long long row0, float* ck, float* cv, cudaStream_t st) {
+  if (B == 0 || R == 0) return TTT_OK;
+  const long long n = (long long)(R < window ? R : window) * d;
+  const int gx = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  if (stg == ST_BF16)
+    launch_pdl(kv_fill_kernel<bf16>, dim3(gx, B), 256, 0, st, R, window, d, src, src_lo, seq_rows, row0, ck, cv);
+  else if (stg == ST_SPLIT)
+    launch_pdl(kv_fill_kernel<Split>, dim3(gx, B), 256, 0, st, R, window, d, src, src_lo, seq_rows, row0, ck, cv);
+  else
+    launch_pdl(kv_fill_kernel<float>, dim3(gx, B), 256, 0, st, R, window, d, src, src_lo, seq_rows, row0, ck, cv);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+size_t swa_decode_smem_bytes(int window, int dh) { return (size_t)(window + dh + 32 + 128) * sizeof(float); }
+
+template <typename S>
+static ttt_status launch_swa_decode_typed(int B, int H, int dh, int window, const int* pos, const float* qkv,
+                                          float* ck, float* cv, void* out, long long out_lo, cudaStream_t st) {
+  const size_t smem = swa_decode_smem_bytes(window, dh);
+  static size_t smem_set = 0;
+  if (smem > 48 * 1024 && smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(swa_decode_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
+    smem_set = smem;
+  }
+  launch_pdl(swa_decode_kernel<S>, dim3(H, B), 128, smem, st, H, dh, window, 1.0f / sqrtf((float)dh), pos, qkv,
+             ck, cv, out, out_lo);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_swa_decode(int stg, int B, int H, int dh, int window, const int* pos, const float* qkv, float* ck,
+                             float* cv, void* out, long long out_lo, cudaStream_t st) {
+  if (B == 0) return TTT_OK;
+  if (stg == ST_BF16) return launch_swa_decode_typed<bf16>(B, H, dh, window, pos, qkv, ck, cv, out, out_lo, st);
+  if (stg == ST_SPLIT) return launch_swa_decode_typed<Split>(B, H, dh, window, pos, qkv, ck, cv, out, out_lo, st);
+  return launch_swa_decode_typed<float>(B, H, dh, window, pos, qkv, ck, cv, out, out_lo, st);
+}
 
 ttt_status launch_band_softmax(int stg, long long nbatch, int nw, int nqb, int j0, int pad, int rows, int window,
                                float scale, const float* Sc, void* P, long long p_lo, cudaStream_t st) {

@@ -127,6 +127,7 @@ struct PrefixBufs {
   float* tmp_g = nullptr;
   OpBuf swiglu_a;        // p == nullptr: not computed here
   bool attn = false;     // attention buffers present (whole-sequence passes only)
+  bool attn_dec = false; // one decoded row per sequence against the K/V cache
 };
 
 // Row layout of the tensor-core attention of one whole-sequence pass of R
@@ -153,6 +154,34 @@ static SwaGeom swa_geom(int B, long long R, int k) {
   return g;
 }
 
+// The decoding K/V cache of frozen block p: [B][attn_window][d] each.
+static float* kv_k(ttt_handle* h, int p) {
+  return h->kv + (size_t)(2 * p) * h->B * h->dm.attn_window * h->d;
+}
+static float* kv_v(ttt_handle* h, int p) { return kv_k(h, p) + (size_t)h->B * h->dm.attn_window * h->d; }
+
+// h += Attn(h) for prefix block p of one decoded row per sequence (position
+// *dec_pos): the Q | K | V projection, the cached-window attention (which
+// appends this row's K and V to the cache), Wo with the residual.
+static ttt_status attention_decode(ttt_handle* h, int p, float* x32, const OpBuf& cur, cudaStream_t st) {
+  const int B = h->B, d = h->d, H = h->dm.attn_heads, dh = d / H, k = h->dm.attn_window, stg = h->stg;
+  GemmDesc gq;
+  gq.M = B; gq.N = 3 * d; gq.K = d;
+  setA(gq, cur, d); setB(gq, h->attn_qkv[p], d);
+  gq.epi = EPI_STORE_F32; gq.out = h->dec_qkv; gq.ldo = 3 * d;
+  TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
+  TTT_TRY(run(h, K_ATTN, st, 1, [&] {
+    return launch_swa_decode(stg, B, H, dh, k, h->dec_pos, h->dec_qkv, kv_k(h, p), kv_v(h, p), h->dec_att.p,
+                             h->dec_att.lo, st);
+  }));
+  GemmDesc gw;
+  gw.M = B; gw.N = d; gw.K = d;
+  setA(gw, h->dec_att, d); setB(gw, h->attn_o[p], d);
+  gw.epi = EPI_RESID; gw.aux = x32; gw.ldx = d; gw.out = x32; gw.ldo = d;
+  setOut2(gw, cur, d);
+  return rungemm(h, K_GEMM_PREFIX, gw, st);
+}
+
 // h += Attn(h) for prefix block p over B sequences of `rows` positions from 0:
 // x32 is the fp32 residual stream and cur its operand copy (both [B][rows][d]),
 // updated in place.  One GEMM projects to Q | K | V; fp32 storage then runs
@@ -172,6 +201,9 @@ static ttt_status attention_sublayer(ttt_handle* h, int p, int rows, float* x32,
     setA(gq, cur, d); setB(gq, h->attn_qkv[p], d);
     gq.epi = EPI_STORE_F32; gq.out = h->qkv32; gq.ldo = 3 * d;
     TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
+    TTT_TRY(run(h, K_ATTN, st, 1, [&] {
+      return launch_kv_fill(stg, B, rows, k, d, h->qkv32, 0, rows, 0, kv_k(h, p), kv_v(h, p), st);
+    }));
     TTT_TRY(run(h, K_ATTN, st, 1, [&] {
       return launch_swa(stg, B, rows, H, dh, k, h->qkv32, h->att_o.p, h->att_o.lo, st);
     }));
@@ -193,6 +225,9 @@ static ttt_status attention_sublayer(ttt_handle* h, int p, int rows, float* x32,
     setOut(gq, op_at(h, h->qkvp, ((long long)s * g.L + g.pad) * ld), ld);
     TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
   }
+  TTT_TRY(run(h, K_ATTN, st, 1, [&] {
+    return launch_kv_fill(stg, B, rows, k, d, h->qkvp.p, h->qkvp.lo, g.L, g.pad, kv_k(h, p), kv_v(h, p), st);
+  }));
   const long long q_row = g.j0 * g.Bq, k_row = g.j0 * g.Bq + g.Bq - g.nw;   // first block's query / window row
   for (int hh = 0; hh < H; ++hh) {
     GemmDesc gs;
@@ -234,9 +269,13 @@ static ttt_status prefix_pass(ttt_handle* h, const TokView& tv, const PrefixBufs
   TTT_TRY(run(h, K_EMBED, st, 1, [&] { return launch_embed(stg, B, tv, h->E, d, pb.x32, cur.p, cur.lo, st); }));
   for (int p = 0; p < h->n_pre; ++p) {
     if (p < h->dm.n_prefix && h->dm.attn_heads > 0) {
-      if (!pb.attn || tv.tok_off != 0)
-        return fail(TTT_ERR_UNSUPPORTED, "attention runs in whole-sequence prefix passes only");
-      TTT_TRY(attention_sublayer(h, p, tv.rows, pb.x32, cur, st));
+      if (pb.attn_dec) {
+        TTT_TRY(attention_decode(h, p, pb.x32, cur, st));
+      } else {
+        if (!pb.attn || tv.tok_off != 0)
+          return fail(TTT_ERR_UNSUPPORTED, "attention runs in whole-sequence or decoding prefix passes only");
+        TTT_TRY(attention_sublayer(h, p, tv.rows, pb.x32, cur, st));
+      }
     }
     const OpBuf* W = &h->prefix[(size_t)p * h->nm];
     const OpBuf next = (p == h->n_pre - 1) ? pb.hout : pb.xop;
@@ -609,11 +648,30 @@ static ttt_status settle_event(ttt_handle* h, const int32_t* q, int Lq, float* A
   });
 }
 
+// Next-token forward of one decoded row per sequence with attention: the
+// one-row prefix pass against the K/V cache into the decoding buffers, then
+// the fast blocks and the head from those rows (fp32 logits).
+static ttt_status attn_next_forward(ttt_handle* h, const TokView& tv_in, cudaStream_t st) {
+  TokView tv = tv_in;      // the embedding checks ids against V and reports through the status word
+  tv.vocab = h->V;
+  tv.err = h->flag;
+  PrefixBufs pb;
+  pb.x32 = h->dec_x32; pb.xop = h->dec_xop; pb.hout = h->dec_op; pb.tmp_a = h->dec_tmp_a; pb.tmp_g = h->dec_tmp_g;
+  pb.swiglu_a = h->dec_a;
+  pb.attn_dec = true;
+  TTT_TRY(prefix_pass(h, tv, pb, st));
+  Hoisted hz;
+  hz.on = true; hz.row0 = 0; hz.rows_total = 1;
+  hz.x32 = h->dec_x32; hz.op = h->dec_op; hz.a = h->dec_a;
+  return forward(h, tv, false, false, nullptr, 0, 0, true, st, hz);
+}
+
 static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t st,
                                       const Hoisted& hz = Hoisted()) {
   TokView tv;
   tv.tok = h->pend; tv.tok_ld = h->b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 0;
-  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, true, st, hz));
+  if (h->dm.attn_heads > 0 && !hz.on) TTT_TRY(attn_next_forward(h, tv, st));
+  else TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, true, st, hz));
   TTT_TRY(run(h, K_OTHER, st, 2, [&] {
     return launch_softmax(h->B, h->V, h->logits32, p_out, h->lse_next, h->soft_part, st);
   }));
@@ -643,7 +701,8 @@ static ttt_status decode_forward_graph(ttt_handle* h, cudaStream_t st) {
     TTT_CUDA(cudaStreamBeginCapture(h->gstream, cudaStreamCaptureModeThreadLocal));
     TokView tv;
     tv.tok = h->x_dev; tv.tok_ld = 1; tv.tok_off = 0; tv.rows = 1; tv.n_valid = 0;
-    ttt_status s = forward(h, tv, false, false, nullptr, 0, 0, true, h->gstream);
+    ttt_status s = h->dm.attn_heads > 0 ? attn_next_forward(h, tv, h->gstream)
+                                        : forward(h, tv, false, false, nullptr, 0, 0, true, h->gstream);
     if (s == TTT_OK)
       s = run(h, K_OTHER, h->gstream, 2, [&] {
         return launch_softmax(h->B, h->V, h->logits32, h->p_dev, h->lse_next, h->soft_part, h->gstream);
@@ -794,6 +853,35 @@ static ttt_status ensure_attn_rows(ttt_handle* h, size_t rows) {
     TTT_TRY(op(&h->ax_a, rows * f));
   }
   h->arows_cap = rows;
+  return TTT_OK;
+}
+
+// One operand buffer's rows: nrows rows per sequence from src (src_rows per
+// sequence, starting at src_row0) to dst (dst_rows per sequence, at dst_row0),
+// width elements each, every plane.
+static ttt_status copy_op_rows(ttt_handle* h, const OpBuf& dst, long long dst_rows, long long dst_row0, const OpBuf& src,
+                               long long src_rows, long long src_row0, long long nrows, long long width,
+                               cudaStream_t st) {
+  const size_t es = h->esz;
+  const int planes = h->stg == ST_SPLIT ? 2 : 1;
+  for (int q = 0; q < planes; ++q) {
+    char* d0 = static_cast<char*>(dst.p) + ((q ? dst.lo : 0) + dst_row0 * width) * es;
+    const char* s0 = static_cast<const char*>(src.p) + ((q ? src.lo : 0) + src_row0 * width) * es;
+    TTT_CUDA(cudaMemcpy2DAsync(d0, (size_t)(dst_rows * width * es), s0, (size_t)(src_rows * width * es),
+                               (size_t)(nrows * width * es), h->B, cudaMemcpyDeviceToDevice, st));
+  }
+  return TTT_OK;
+}
+
+// Prefix rows (fp32 residual, operand copy, SwiGLU activation) into the
+// pending-row buffers of decoding with attention, rows dst_row0 ...
+static ttt_status save_pending_rows(ttt_handle* h, const float* x32, const OpBuf& op, const OpBuf& a, long long src_rows,
+                                    long long src_row0, long long dst_row0, long long nrows, cudaStream_t st) {
+  const long long pr = h->b + 1, d = h->d;
+  TTT_CUDA(cudaMemcpy2DAsync(h->prow32 + dst_row0 * d, (size_t)(pr * d * 4), x32 + src_row0 * d,
+                             (size_t)(src_rows * d * 4), (size_t)(nrows * d * 4), h->B, cudaMemcpyDeviceToDevice, st));
+  TTT_TRY(copy_op_rows(h, h->prow_op, pr, dst_row0, op, src_rows, src_row0, nrows, d, st));
+  if (h->prow_a.p && a.p) TTT_TRY(copy_op_rows(h, h->prow_a, pr, dst_row0, a, src_rows, src_row0, nrows, h->f, st));
   return TTT_OK;
 }
 
@@ -1098,6 +1186,27 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   if ((s = dalloc(h, &h->Lw, (size_t)B * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->pend, (size_t)B * (h->b + 1) * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->x_dev, (size_t)B * 4)) != TTT_OK) return bail(s);
+  if (D.attn_heads > 0) {
+    // decoding with attention: the K/V cache of every frozen block, the one-row
+    // prefix pass and the pending inputs' prefix rows
+    const size_t kw = (size_t)D.attn_window;
+    if ((s = dalloc(h, &h->kv, (size_t)D.n_prefix * 2 * B * kw * d * 4)) != TTT_OK) return bail(s);
+    if ((s = dalloc(h, &h->dec_pos, 4)) != TTT_OK) return bail(s);
+    if ((s = dalloc(h, &h->dec_x32, (size_t)B * d * 4)) != TTT_OK) return bail(s);
+    if ((s = dalloc(h, &h->dec_qkv, (size_t)B * 3 * d * 4)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->dec_op, (size_t)B * d)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->dec_xop, (size_t)B * d)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->dec_att, (size_t)B * d)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->dec_tmp_a, (size_t)B * f)) != TTT_OK) return bail(s);
+    const size_t pr = (size_t)B * (h->b + 1);
+    if ((s = dalloc(h, &h->prow32, pr * d * 4)) != TTT_OK) return bail(s);
+    if ((s = op_alloc(&h->prow_op, pr * d)) != TTT_OK) return bail(s);
+    if (D.block_kind == TTT_BLOCK_SWIGLU) {
+      if ((s = dalloc(h, &h->dec_tmp_g, (size_t)B * f * 4)) != TTT_OK) return bail(s);
+      if ((s = op_alloc(&h->dec_a, (size_t)B * f)) != TTT_OK) return bail(s);
+      if ((s = op_alloc(&h->prow_a, pr * f)) != TTT_OK) return bail(s);
+    }
+  }
   if ((s = reset_weights(h, st)) != TTT_OK) return bail(s);
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return bail(cuda_fail(e, "create sync", __FILE__, __LINE__));
@@ -1223,6 +1332,12 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   // pending decode buffer: tokens x_{n_full b} .. x_T
   TTT_CUDA(cudaMemcpy2DAsync(h->pend, (size_t)(b + 1) * 4, tok + (size_t)n_full * b, (size_t)(T + 1) * 4,
                              (size_t)(rem + 1) * 4, B, cudaMemcpyDeviceToDevice, st));
+  if (attn) {
+    // decoding goes on from here: the prefix rows of x_{n_full b} .. x_T, and x_T's position
+    TTT_TRY(save_pending_rows(h, h->ax32, h->ax_op, h->ax_a, (long long)T + 1, (long long)n_full * b, 0, rem + 1, st));
+    TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_pos_set(h->dec_pos, T, st); }));
+    h->attn_ctx = true;
+  }
   h->pend_count = rem;
   h->has_context = true;
   if (p_next) {
@@ -1242,9 +1357,18 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
 ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, float* loss, ttt_stream stream) {
   if (!h || !x_new || !p_next) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_decode_step");
   if (!h->has_context) return fail(TTT_ERR_STATE, "decode before prefill");
-  if (h->dm.attn_heads > 0) return fail(TTT_ERR_UNSUPPORTED, "decoding with attention is not built");
+  const bool attn = h->dm.attn_heads > 0;
+  if (attn && !h->attn_ctx) return fail(TTT_ERR_STATE, "decoding with attention needs a prefill first");
+  if (attn && swa_decode_smem_bytes(h->dm.attn_window, h->d / h->dm.attn_heads) > 227 * 1024)
+    return fail(TTT_ERR_UNSUPPORTED, "attention window too long for decoding");
   cudaStream_t st = (cudaStream_t)stream;
   const int B = h->B, b = h->b;
+  // attention: the pending inputs' prefix rows (row j = input pend[j])
+  Hoisted hp;
+  if (attn) {
+    hp.on = true; hp.rows_total = b + 1;
+    hp.x32 = h->prow32; hp.op = h->prow_op; hp.a = h->prow_a;
+  }
   h->launches = 0;
   // x_new -> pend[s][pend_count + 1]
   const bool x_dev_ptr = is_device_ptr(x_new);
@@ -1264,7 +1388,9 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
     } else {
       TokView tv;
       tv.tok = h->pend; tv.tok_ld = b + 1; tv.tok_off = h->pend_count; tv.rows = 1; tv.n_valid = 1;
-      TTT_TRY(forward(h, tv, false, false, dst, 1, 0, false, st));
+      Hoisted hz = hp;
+      hz.row0 = h->pend_count;
+      TTT_TRY(forward(h, tv, false, false, dst, 1, 0, false, st, hz));
     }
     if (!dev) TTT_CUDA(cudaMemcpyAsync(loss, dst, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
   }
@@ -1272,10 +1398,14 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   if (h->pend_count == b) {
     TokView tv;
     tv.tok = h->pend; tv.tok_ld = b + 1; tv.tok_off = 0; tv.rows = b; tv.n_valid = b;
-    TTT_TRY(chunk_step(h, tv, nullptr, 0, 0, st));
+    Hoisted hz = hp;
+    hz.row0 = 0;
+    TTT_TRY(chunk_step(h, tv, nullptr, 0, 0, st, hz));
     TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_pending_shift(B, b, h->pend, st); }));
     h->pend_count = 0;
   }
+  // attention: x_new's position (the decoding attention appends its K and V there)
+  if (attn) TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_pos_add(h->dec_pos, st); }));
   const bool dev = is_device_ptr(p_next);
   if (decode_graph_enabled()) {
     // the newest token into the fixed slot the captured forward reads
@@ -1288,6 +1418,8 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
     TTT_TRY(p_next_from_pending(h, dev ? p_next : h->p_dev, st));
     if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
   }
+  // attention: x_new's prefix row is the pending row of input pend[pend_count]
+  if (attn) TTT_TRY(save_pending_rows(h, h->dec_x32, h->dec_op, h->dec_a, 1, 0, h->pend_count, 1, st));
   return finish(h, st);
 }
 
@@ -1329,6 +1461,7 @@ ttt_status ttt_reset(ttt_handle* h, ttt_stream stream) {
   cudaStream_t st = (cudaStream_t)stream;
   TTT_TRY(reset_weights(h, st));
   h->has_context = false;
+  h->attn_ctx = false;
   TTT_CUDA(cudaStreamSynchronize(st));
   return TTT_OK;
 }
@@ -1393,6 +1526,7 @@ ttt_status ttt_set_state(ttt_handle* h, const void* src, size_t bytes, ttt_strea
   TTT_CUDA(cudaStreamSynchronize(st));
   h->pend_count = hd.pend_count;
   h->has_context = hd.has_context != 0;
+  h->attn_ctx = false;     // the attention context (K/V cache, pending rows) is not part of the blob
   h->chunks_done = hd.chunks_done;
   return TTT_OK;
 }

@@ -52,6 +52,18 @@ struct ttt_handle {
   OpBuf qkvp, Pp, att_p;
   float* Sc = nullptr;
   size_t qkvp_cap = 0, sc_cap = 0, attp_cap = 0;
+  // decoding with attention: the frozen blocks' K/V cache, the newest input's
+  // position, the one-row prefix pass of the next-token forward, and the
+  // prefix rows of the pending inputs (row j = input pend[j])
+  float* kv = nullptr;               // [n_prefix][2][B][attn_window][d] fp32
+  int* dec_pos = nullptr;
+  bool attn_ctx = false;             // a prefill filled the cache and the pending rows
+  float* dec_x32 = nullptr;
+  float* dec_qkv = nullptr;          // [B][3d]
+  float* dec_tmp_g = nullptr;
+  OpBuf dec_op, dec_xop, dec_tmp_a, dec_a, dec_att;
+  float* prow32 = nullptr;           // [B][b + 1][d]
+  OpBuf prow_op, prow_a;
   std::vector<OpBuf> fastfrozen;     // [n_fast * nm], empty where fast
 
   // fast weights: arenas [slot][B][n]

@@ -592,10 +592,21 @@ int grid_for(long long n, int threads) {
     else launch_pdl(KERNEL<float>, GRID, BLOCK, SMEM, STREAM, __VA_ARGS__);                         \
   } while (0)
 
+// A token view must carry the vocabulary and the status word its kernels
+// report out-of-range ids through; a view without them is refused here.
+static ttt_status check_view(const TokView& tv) {
+  if (!tv.err || tv.vocab <= 0 || !tv.tok) {
+    set_error("token view without vocabulary, status word or tokens");
+    return TTT_ERR_BAD_ARG;
+  }
+  return TTT_OK;
+}
+
 ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d, float* h32, void* hop,
                         long long hop_lo, cudaStream_t st) {
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
+  TTT_TRY(check_view(tv));
   if (stg == ST_BF16)
     launch_pdl(embed_kernel<bf16, bf16>, M, 256, 0, st, tv, static_cast<const bf16*>(E), d, h32, hop, hop_lo);
   else if (stg == ST_SPLIT)
@@ -609,6 +620,7 @@ ttt_status launch_embed(int stg, int B, const TokView& tv, const void* E, int d,
 ttt_status launch_rmsnorm_fwd(int stg, int M, int d, const float* x, float eps, void* y, long long y_lo, float* rstd,
                               const TokView* tv, int32_t* tgt, cudaStream_t st) {
   if (M == 0) return TTT_OK;
+  if (tv) TTT_TRY(check_view(*tv));
   const TokView tvv = tv ? *tv : TokView();
   LAUNCH_BY_STORAGE(stg, rmsnorm_fwd_kernel, M, 256, 0, st, d, x, eps, y, y_lo, rstd, tvv, tv ? tgt : nullptr);
   TTT_CHECK_LAUNCH();
@@ -630,6 +642,7 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
                      float* row_loss, cudaStream_t st) {
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
+  TTT_TRY(check_view(tv));
   if (stg == ST_SPLIT) {
     if (V > kCeSplitMaxV) {
       set_error("vocabulary too large for the split cross-entropy kernel");
@@ -660,6 +673,7 @@ ttt_status launch_lse_combine(int B, const TokView& tv, const float2* part, long
                               long long loss_off, float* row_loss, cudaStream_t st) {
   const int M = B * tv.rows;
   if (M == 0) return TTT_OK;
+  TTT_TRY(check_view(tv));
   launch_pdl(lse_combine_kernel, ceil_div(M, 8), 256, 0, st, tv, M, part, ld, nt, static_cast<const bf16*>(y),
                                                     static_cast<const bf16*>(U), d, tgt, lse, losses, loss_ld,
                                                     loss_off, row_loss);

@@ -104,8 +104,13 @@ typedef struct {
                        the bigram defect): h += Attn(h), keys t-k < s <= t,
                        scale 1/sqrt(d/attn_heads), no positional encoding.
                        Needs n_prefix >= 1, d % attn_heads == 0,
-                       d/attn_heads <= 128; prefill only (decoding and
-                       Settlement return UNSUPPORTED).  0 = no attention     */
+                       d/attn_heads <= 128.  Prefill runs the prefix of
+                       x_0..x_T as one pass; decoding continues the
+                       positions through a K/V cache of the last
+                       attn_window inputs (needs a prefill after create,
+                       ttt_reset or ttt_set_state: STATE otherwise; windows
+                       above ~57K positions return UNSUPPORTED there);
+                       Settlement returns UNSUPPORTED.  0 = no attention     */
   int attn_window;  /* k >= 1 when attn_heads > 0                             */
 } ttt_dims;
 

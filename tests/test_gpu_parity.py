@@ -443,16 +443,60 @@ def test_sliding_window_attention_edge_cases(case):
     compare(wl, gpu, ref)
 
 
-def test_attention_handles_refuse_decoding():
+@pytest.mark.parametrize("case", ["fp32_split_graph", "fp32_split_launches", "fp32_rows", "bf16_swiglu"])
+def test_decoding_with_attention_against_the_oracle(monkeypatch, case):
+    """Decoding after an attention prefill: each new input attends through the
+    K/V cache to the window's inputs, prefill's included; the pending inputs'
+    prefix rows feed the decoded chunk's step; token by token against the
+    oracle across a step, captured graph and launch by launch."""
+    if case == "fp32_split_launches":
+        monkeypatch.setenv("TTT_DECODE_GRAPH", "0")
+    if case.startswith("fp32_split"):
+        wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=2 * 64 + 21, n_prefix=2,
+                                    init_std=0.1, attn_heads=4, attn_window=96, eta=0.3)
+    elif case == "fp32_rows":
+        wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=8, B=3, T=2 * 8 + 3, n_prefix=1,
+                                    init_std=0.1, attn_heads=3, attn_window=6, eta=0.3)
+    else:
+        wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=16, B=2, T=3 * 16 + 5, n_prefix=1,
+                                  init_std=0.1, attn_heads=2, attn_window=24, eta=0.5)
+    extra = wl.chunk + 6 - wl.T % wl.chunk       # completes the pending chunk, then some
+    inp = _attention_inputs(wl)
+    long_tok = synth.sample_stream(inp["chain"], wl.seed_id, wl.B, wl.T + extra)
+    tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
+    gpu = run_gpu(wl, inp, tokens=tok)
+    h = gpu["handle"]
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps, heads=wl.attn_heads,
+                                  window=wl.attn_window)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
+    lt, pt = (1e-4, 1e-5) if wl.dtype == "fp32" else (3e-2, 3e-3)
+    for t in range(wl.T + 1, wl.T + extra + 1):
+        h.decode_step(torch.from_numpy(long_tok[:, t].copy()).cuda(), p, loss)
+        torch.cuda.synchronize()
+        for s in range(wl.B):
+            l_ref, p_ref = oracle.decode_step(net, ref["states"][s], long_tok[s, t], wl.eta, wl.clip, wl.chunk)
+            assert abs(float(loss[s]) - l_ref) <= lt, (t, s, float(loss[s]), l_ref)
+            assert np.abs(p[s].cpu().numpy() - p_ref).max() <= pt, (t, s)
+    assert ref["states"][0].chunks_done == wl.T // wl.chunk + 1
+    for s in range(wl.B):
+        rel = oracle.weights_rel_frobenius(h.fast_weights(s), ref["states"][s].W, wl.fast_mats)
+        assert rel <= (1e-4 if wl.dtype == "fp32" else 3e-2)
+
+
+def test_attention_decoding_needs_a_prefill_after_reset():
     from chunked_next_token_ttt_b300 import TTTError
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=40, n_prefix=1, attn_heads=2,
                                 attn_window=16)
     inp = make(wl)
     h = run_gpu(wl, inp)["handle"]
     p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    h.decode_step(torch.zeros(wl.B, dtype=torch.int32, device="cuda"), p)
+    h.reset()
     with pytest.raises(TTTError) as e:
         h.decode_step(torch.zeros(wl.B, dtype=torch.int32, device="cuda"), p)
-    assert e.value.status == 7
+    assert e.value.status == 8
 
 
 def test_host_and_device_buffers_agree():
