@@ -253,12 +253,16 @@ __global__ void kv_fill_kernel(int R, int window, int d, const void* __restrict_
 }
 
 // One decoded position per sequence (`*pos_ptr`, the same for every
-// sequence): one block per (head, sequence) appends the row's K and V to the
-// cache, scores the query against the window's keys (positions pos - n + 1 ..
-// pos, n = min(pos + 1, window)) into shared memory, takes the softmax, and
-// sums the values with the 128 threads split as (key group, head element).
+// sequence): one block of kDecThreads per (head, sequence) appends the row's
+// K and V to the cache, scores the query against the window's keys
+// (positions pos - n + 1 .. pos, n = min(pos + 1, window)) into shared
+// memory, takes the softmax, and sums the values with the threads split as
+// (key group, head element), four independent sums per thread so that their
+// loads overlap.
+constexpr int kDecThreads = 1024;
+
 template <typename S>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kDecThreads)
     swa_decode_kernel(int H, int dh, int window, float scale, const int* __restrict__ pos_ptr,
                       const float* __restrict__ qkv, float* __restrict__ ck, float* __restrict__ cv, void* out,
                       long long out_lo) {
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(128)
   float* sc = sm;                  // [window] scores, then probabilities
   float* qs = sc + window;         // [dh]
   float* red = qs + dh;            // [32]
-  float* po = red + 32;            // [128] partial outputs
+  float* po = red + 32;            // [kDecThreads] partial outputs
   const int head = blockIdx.x, tid = threadIdx.x;
   const long long s = blockIdx.y;
   const int d = H * dh;
@@ -306,10 +310,18 @@ __global__ void __launch_bounds__(128)
   se = block_sum(se, red);          // also orders the probability writes before the reads below
   const int G = (int)blockDim.x / dh;
   const int g = tid / dh, e = tid % dh;
-  float acc = 0.0f;
-  if (g < G)
-    for (int j = g; j < n; j += G) acc = fmaf(sc[j], vc[(long long)((pos - j) % window) * d + e], acc);
-  if (g < G) po[g * dh + e] = acc;
+  if (g < G) {
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    int j = g;
+    for (; j + 3 * G < n; j += 4 * G) {
+      a0 = fmaf(sc[j], vc[(long long)((pos - j) % window) * d + e], a0);
+      a1 = fmaf(sc[j + G], vc[(long long)((pos - j - G) % window) * d + e], a1);
+      a2 = fmaf(sc[j + 2 * G], vc[(long long)((pos - j - 2 * G) % window) * d + e], a2);
+      a3 = fmaf(sc[j + 3 * G], vc[(long long)((pos - j - 3 * G) % window) * d + e], a3);
+    }
+    for (; j < n; j += G) a0 = fmaf(sc[j], vc[(long long)((pos - j) % window) * d + e], a0);
+    po[g * dh + e] = (a0 + a1) + (a2 + a3);
+  }
   __syncthreads();
   if (tid < dh) {
     float o = 0.0f;
@@ -359,7 +371,9 @@ ttt_status launch_kv_fill(int stg, int B, int R, int window, int d, const void* 
   return TTT_OK;
 }
 
-size_t swa_decode_smem_bytes(int window, int dh) { return (size_t)(window + dh + 32 + 128) * sizeof(float); }
+size_t swa_decode_smem_bytes(int window, int dh) {
+  return (size_t)(window + dh + 32 + kDecThreads) * sizeof(float);
+}
 
 template <typename S>
 static ttt_status launch_swa_decode_typed(int B, int H, int dh, int window, const int* pos, const float* qkv,
@@ -371,8 +385,8 @@ static ttt_status launch_swa_decode_typed(int B, int H, int dh, int window, cons
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
     smem_set = smem;
   }
-  launch_pdl(swa_decode_kernel<S>, dim3(H, B), 128, smem, st, H, dh, window, 1.0f / sqrtf((float)dh), pos, qkv,
-             ck, cv, out, out_lo);
+  launch_pdl(swa_decode_kernel<S>, dim3(H, B), kDecThreads, smem, st, H, dh, window, 1.0f / sqrtf((float)dh), pos,
+             qkv, ck, cv, out, out_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

@@ -148,7 +148,7 @@ ttt_status launch_swa(int stg, int B, int rows, int H, int dh, int window, const
 // ck / cv [B][window][d] at slot pos % window.  swa_decode: for the position
 // *pos of every sequence, appends the K | V of qkv [B][3d] (fp32) to the
 // cache and writes the heads' output [B][d] in operand type; needs
-// dh <= 128 and (window + dh + 160) floats of shared memory.
+// dh <= 128 and (window + dh + 1056) floats of shared memory.
 ttt_status launch_kv_fill(int stg, int B, int R, int window, int d, const void* src, long long src_lo,
                           long long seq_rows, long long row0, float* ck, float* cv, cudaStream_t st);
 size_t swa_decode_smem_bytes(int window, int dh);
