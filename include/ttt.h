@@ -70,14 +70,14 @@ typedef enum {
   TTT_ERR_NONFINITE = 5,    /* a non-finite gradient norm: that update was
                                skipped for that sequence, the rest ran      */
   TTT_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up           */
-  TTT_ERR_UNSUPPORTED = 7,  /* a valid request this build does not run      */
+  TTT_ERR_UNSUPPORTED = 7,  /* a valid request the library does not run    */
   TTT_ERR_STATE = 8         /* call out of order (e.g. decode before prefill) */
 } ttt_status;
 
 enum { TTT_BLOCK_GELU = 0, TTT_BLOCK_SWIGLU = 1 };
 enum { TTT_DTYPE_FP32 = 0, TTT_DTYPE_BF16 = 1 };
 /* fast_mask bits.  GELU: bit0 = W1, bit1 = W2.  SwiGLU: bit0 = Wg, bit1 = Wd,
- * bit2 = Wu.  This build runs GELU with mask 3 and SwiGLU with mask 2 (the
+ * bit2 = Wu.  The library runs GELU with mask 3 and SwiGLU with mask 2 (the
  * In-Place down projection); other masks return TTT_ERR_UNSUPPORTED. */
 enum { TTT_FAST_W1 = 1, TTT_FAST_W2 = 2, TTT_FAST_WG = 1, TTT_FAST_WD = 2, TTT_FAST_WU = 4 };
 
