@@ -268,6 +268,22 @@ def max_over_ranks(x, world, device):
 
 
 # ---------------------------------------------------------------- arms
+def workload_config(wl, world):
+    """The workload keys of the JSON line's config, the same for both arms."""
+    cfg = {"workload": wl.name, "B": wl.B, "T": wl.T, "chunk": wl.chunk, "d": wl.d, "d_ff": wl.d_ff,
+           "vocab": wl.vocab, "n_prefix": wl.n_prefix, "n_fast": wl.n_fast, "tokens_per_step": wl.B * wl.T * world}
+    if wl.attn_heads:
+        cfg.update(attn_heads=wl.attn_heads, attn_window=wl.attn_window)
+    return cfg
+
+
+def measured_config(wl, world, chunk_frac, t_roof, pk):
+    """The config of our arm's line: the workload keys plus how it was measured."""
+    return dict(workload_config(wl, world), l2="flushed (512 MB write) before every step",
+                chunk_roofline_frac=chunk_frac, chunk_roofline_ms=t_roof * 1e3,
+                peaks={"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"], "source": pk["source"]})
+
+
 def run_reference(args, wl, rank):
     if rank != 0:
         return
@@ -286,7 +302,7 @@ def run_reference(args, wl, rank):
             "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "chunk": wl.chunk},
+            "config": workload_config(wl, args.gpus),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -482,12 +498,7 @@ def run_ours(args, wl, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.dtype == "fp32" else "bf16",
             "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "chunk": wl.chunk, "d": wl.d,
-                       "d_ff": wl.d_ff, "vocab": wl.vocab, "n_prefix": wl.n_prefix, "n_fast": wl.n_fast,
-                       "tokens_per_step": wl.B * wl.T * world, "l2": "flushed (512 MB write) before every step",
-                       "chunk_roofline_frac": chunk_frac, "chunk_roofline_ms": t_roof * 1e3,
-                       "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"],
-                                 "source": pk["source"]}},
+            "config": measured_config(wl, world, chunk_frac, t_roof, pk),
             "roofline": roof, "clocks": clk_sum,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,

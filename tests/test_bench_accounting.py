@@ -50,3 +50,17 @@ def test_update_bytes_per_parameter():
         wl = C.E2E_125M.replace(d=8, d_ff=16, chunk=4, B=2, n_fast=3, dtype=dtype)
         params = len(wl.fast_mats) * wl.n_fast * wl.B * wl.d * wl.d_ff
         assert bench.chunk_bytes(wl)["clip_sgd_update"] == params * (12 + es)
+
+
+def test_both_arms_name_the_same_workload_config():
+    """The reference arm's config keys are a subset of ours with equal values,
+    and ours adds only how it was measured."""
+    wl = C.SWA_125M
+    pk = bench.peaks()
+    ref = bench.workload_config(wl, 1)
+    ours = bench.measured_config(wl, 1, 0.1, 0.002, pk)
+    assert all(ours[k] == v for k, v in ref.items())
+    assert set(ours) - set(ref) == {"l2", "chunk_roofline_frac", "chunk_roofline_ms", "peaks"}
+    assert ref["attn_window"] == 2048 and ref["tokens_per_step"] == wl.B * wl.T
+    t_roof, fl, by = bench.chunk_roofline_seconds(C.CHUNKED_FP32, pk)
+    assert t_roof > 0 and fl > 0 and by > 0
