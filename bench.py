@@ -5,11 +5,17 @@
 
 One step is one full prefill of the workload's B sequences of T tokens: every
 chunk runs the frozen prefix, the fast blocks forward, RMSNorm, the LM head, the
-fused cross-entropy, the backward to the fast weights and the clipped SGD step.
+fused cross-entropy, the backward to the fast weights and the clipped SGD step
+(and, for the Settlement workload, the Settlement events).  The default workload
+is the largest: the 760M-like stream, B = 8, T = 131072, one clipped step per
+1024-token chunk on the last three MLP blocks, Settlement after every 8th chunk.
 Inputs (seeded synthetic Markov tokens, N(0, 0.02^2) weights) are resident on
 the device before the timed region; L2 is flushed (a 512 MB write) before every
-timed step, outside the step's events.  `e2e` times the same call with pinned
-host buffers (tokens in, losses and p_{T+1} out) through the C ABI.
+timed step, outside the step's events.  The timed steps carry no profiling
+events: the per-class times and the dominant class's launch times come from
+separate, untimed profiled steps.  `e2e` times the same call with pinned host
+buffers (tokens and held-out chunks in; losses, p_{T+1}, scores and decisions
+out) through the C ABI.
 
 With --gpus N under torchrun every rank runs its own B sequences (weak scaling:
 the sequences are independent, so no collective is on the data path); rank 0
@@ -40,9 +46,11 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0}
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
 # host-side orchestration (which kernels run, not what a kernel does): left
 # out of the kernel identity below
-HOST_SOURCES = {"engine.cu", "engine.h", "ops_api.cu", "noalloc.cu"}
+HOST_SOURCES = {"engine.cu", "engine.h", "ops_api.cu", "noalloc.cu", "devctx.cu"}
 
 
 def source_hash():
@@ -61,20 +69,29 @@ def source_hash():
 
 
 def profiled_traffic(workload, kernel_class):
-    """DRAM bytes per launch of a kernel class from the committed ncu summary of
-    this workload (profiles/launches_<workload>.md), or None when there is none
-    or the kernels changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"launches_{workload}.md")
-    if not os.path.exists(path):
+    """DRAM bytes per launch of a kernel class from profiles/traffic.json (ncu's
+    dram__bytes_read.sum + dram__bytes_write.sum per launch, one entry per
+    workload), or None when there is none or the kernels changed since the
+    counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    meta = {}
-    for line in open(path):
-        if line.startswith("<!-- traffic "):
-            meta = json.loads(line[len("<!-- traffic "):].rsplit("-->", 1)[0])
+    with open(TRAFFIC_FILE) as f:
+        meta = json.load(f).get(workload, {})
     if meta.get("source_hash") != source_hash():
         return None
     v = meta.get("dram_bytes_per_launch", {}).get(kernel_class)
     return float(v) if v is not None else None
+
+
+def choose_peak(pk, clocks, timed_s):
+    """The bf16 denominator for a class timed inside the measured steps: the
+    burst peak when the timed region is sub-second at the maximum clock with no
+    power-cap sample, the sustained (power-capped) peak otherwise."""
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    at_max = sm is not None and smax and sm >= 0.97 * smax
+    if timed_s < 1.0 and at_max and "sw_power_cap" not in clocks.get("reasons", []):
+        return pk["bf16_tflops"], "burst"
+    return pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), "sustained"
 
 
 def peaks():
@@ -156,8 +173,33 @@ def chunk_bytes(wl):
     }
 
 
+def settle_flops(wl):
+    """FLOPs of one Settlement event for all B sequences, by class: one pass of
+    the frozen prefix over the held-out chunks (shared by both scores), then
+    the fast blocks and the LM head forward twice (committed and current)."""
+    if not wl.settle_every:
+        return {}
+    f = chunk_flops(wl, rows=wl.settle_len)
+    return {"gemm_prefix": f["gemm_prefix"], "gemm_fast_fwd": 2 * f["gemm_fast_fwd"], "gemm_head": 2 * f["gemm_head"]}
+
+
+def step_flops(wl):
+    """Dense-contraction FLOPs of one whole prefill step (every chunk, every
+    Settlement event and the p_{T+1} forward), by kernel class."""
+    out = {k: v * wl.n_chunks for k, v in chunk_flops(wl).items()}
+    for k, v in settle_flops(wl).items():
+        out[k] = out.get(k, 0.0) + v * wl.n_settle_events
+    for k, v in chunk_flops_fwd_one(wl).items():
+        out[k] = out.get(k, 0.0) + v
+    return out
+
+
 def chunk_roofline_seconds(wl, pk):
+    """Roofline time of one chunk step, max(FLOPs / bf16 burst peak, bytes / HBM
+    peak), with the Settlement events' FLOPs spread over the chunks."""
     fl = sum(chunk_flops(wl).values())
+    if wl.settle_every:
+        fl += sum(settle_flops(wl).values()) / wl.settle_every
     es = 2 if wl.dtype == "bf16" else 4
     M = wl.B * wl.chunk
     nf = len(wl.fast_mats) * wl.n_fast
@@ -288,7 +330,10 @@ def run_reference(args, wl, rank):
     if rank != 0:
         return
     inp = synth.make_inputs(wl.replace(B=1))
-    n_chunks = max(1, min(wl.n_chunks, 4))
+    # chunks per step: at most 4, and about 8e11 FLOP (a few seconds of the
+    # float64 oracle on host cores) so that the whole run ends in minutes
+    per_chunk = sum(chunk_flops(wl).values()) / wl.B
+    n_chunks = max(1, min(wl.n_chunks, 4, int(8e11 // per_chunk)))
     for _ in range(args.warmup):
         oracle_sample(wl, inp, 1, 1)
     vals, times = [], []
@@ -297,7 +342,9 @@ def run_reference(args, wl, rank):
         vals.append(v)
         times.append(dt)
     v = len(vals) * n_chunks * wl.chunk / sum(times)
-    sample = f"1 sequence x {n_chunks} chunks ({n_chunks * wl.chunk} tokens) of {wl.name} per step"
+    sample = f"1 sequence x {n_chunks} chunk(s) ({n_chunks * wl.chunk} tokens) of {wl.name} per step"
+    if wl.settle_every:
+        sample += " (no Settlement event falls inside the sample)"
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -319,6 +366,7 @@ def run_ours(args, wl, rank, world, local_rank):
     pk = peaks()
     inp = rank_inputs(wl, rank)
     h = Handle.from_workload(wl, inp["weights"])
+    storage = h.operand_storage()
     tok = torch.from_numpy(inp["tokens"]).to(dev)
     losses = torch.empty((wl.B, wl.T), dtype=torch.float32, device=dev)
     p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device=dev)
@@ -328,34 +376,27 @@ def run_ours(args, wl, rank, world, local_rank):
     A = torch.empty((max(1, n_ev), wl.B), dtype=torch.float32, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     st = torch.cuda.current_stream(dev)
+    classes = kernel_classes()
 
     def step():
         h.prefill(tok, losses, p, q, acc if n_ev else None, A if n_ev else None)
 
+    # warm-up; the first step logs the class of every launch
+    seen = []
     for w in range(args.warmup):
-        if w == 0 and args.launch_log:
+        if w == 0:
             h.launch_log_enable(True)
         step()
-        if w == 0 and args.launch_log:
-            with open(args.launch_log, "w") as f:
-                f.write("\n".join(h.launch_log()) + "\n")
+        if w == 0:
+            log = h.launch_log()
             h.launch_log_enable(False)
+            seen = [c for c in classes if c in set(log)]
+            if args.launch_log:
+                with open(args.launch_log, "w") as f:
+                    f.write("\n".join(log) + "\n")
     torch.cuda.synchronize(dev)
 
-    # which kernel class dominates: one untimed profiled prefill per class
-    classes = kernel_classes()
-    per_class = {}
-    for ci, name in enumerate(classes):
-        h.profile_enable(ci)
-        step()
-        n, ms = h.profile_read()
-        if n:
-            per_class[name] = (n, ms)
-    h.profile_enable(-1)
-    dom = max(per_class, key=lambda k: per_class[k][1])
-
-    # timed region: K steps, L2 flushed before each, the dominant class timed live
-    h.profile_enable(classes.index(dom))
+    # timed region: K steps with no profiling events, L2 flushed before each
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches = 0
     if world > 1:
@@ -370,8 +411,6 @@ def run_ours(args, wl, rank, world, local_rank):
             ev[i][1].record(st)
             launches += h.last_launch_count()
         torch.cuda.synchronize(dev)
-    dom_n, dom_ms = h.profile_read()
-    h.profile_enable(-1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     if world > 1:
@@ -379,6 +418,27 @@ def run_ours(args, wl, rank, world, local_rank):
         dist.barrier()
     tokens = wl.B * wl.T * world * args.steps
     value = tokens / (total_ms / 1e3)
+    clk_sum = clk.summary()
+
+    # per-class device time: one untimed step per class, its launches bracketed by events
+    per_class = {}
+    for name in seen or classes:
+        h.profile_enable(classes.index(name))
+        flush.zero_()
+        step()
+        n, ms = h.profile_read()
+        if n:
+            per_class[name] = (n, ms)
+    h.profile_enable(-1)
+    dom = max(per_class, key=lambda k: per_class[k][1])
+    # the dominant class's launch times over further untimed steps
+    dom_steps = max(1, min(3, args.steps))
+    h.profile_enable(classes.index(dom))
+    for _ in range(dom_steps):
+        flush.zero_()
+        step()
+    dom_n, dom_ms = h.profile_read()
+    h.profile_enable(-1)
 
     # end to end: pinned host buffers through the C ABI
     tok_h = torch.from_numpy(inp["tokens"]).pin_memory()
@@ -439,71 +499,70 @@ def run_ours(args, wl, rank, world, local_rank):
                "weight_stream_bound_tokens_per_s": bound, "frac_of_bound": v / bound,
                "note": "b decode steps (one TTT update amortised); bound = every weight read once per step"}
 
-    # roofline of the dominant class
-    flops = chunk_flops(wl)
+    # roofline of the dominant class: its algorithmic work per launch over its
+    # average launch time in the untimed profiled steps
+    sflops = step_flops(wl)
     byts = chunk_bytes(wl)
-    clk_sum = clk.summary()
+    timed_s = total_ms / 1e3
     dom_avg_s = dom_ms / 1e3 / max(1, dom_n)
-    launches_per_step_dom = dom_n / args.steps
-    if dom_n % args.steps:
+    if dom_n % dom_steps:
         raise RuntimeError("profiled launches are not a whole number per step")
-    if dom in flops:
-        # the class's algorithmic FLOPs per step: every chunk plus the p_{T+1} forward (rows = 1)
-        fl_step = flops[dom] * wl.n_chunks + chunk_flops_fwd_one(wl).get(dom, 0.0)
-        per_launch = fl_step / launches_per_step_dom
+    launches_per_step_dom = dom_n / dom_steps
+    fma_peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+    if dom in sflops:
+        per_launch = sflops[dom] / launches_per_step_dom
         achieved = per_launch / dom_avg_s / 1e12
-        split = wl.dtype == "fp32" and os.environ.get("TTT_FP32_STORAGE") != "f32" and wl.chunk >= 64
-        if dom == "attention" and wl.dtype == "fp32" and not split:
-            # the tiled windowed-softmax kernel runs on the fp32 FMA pipes of every SM
-            peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
-            roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"}
-        elif dom == "token_step":
+        if dom == "token_step":
             # one CTA per sequence: the FP32 FMA lanes of the SMs it occupies
             sms = min(wl.B, 148)
-            peak = sms * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
-            roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            roof = {"bound": "alu", "achieved": achieved, "peak": fma_peak * sms / 148, "unit": "TFLOP/s",
                     "peak_source": f"fp32 FMA: {sms} SM(s) x 128 lanes x 2 x max SM clock"}
-        elif wl.dtype == "fp32" and not split:
+        elif storage == "f32":
             # fp32 FMA on the SIMT pipes: 148 SMs x 128 lanes x 2 FLOP x max SM clock
-            peak = 148 * 128 * 2 * pk.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
-            roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            roof = {"bound": "alu", "achieved": achieved, "peak": fma_peak, "unit": "TFLOP/s",
                     "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x max SM clock"}
-        elif split:
-            # fp32-accurate products as three bf16 tensor-core products each
-            peak = pk["bf16_tflops_sustained"] / 3.0
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "peak_source": f"{pk['source']} bf16 sustained / 3 (bf16x3 split products)"}
         else:
-            peak = pk["bf16_tflops_sustained"]
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "peak_source": f"{pk['source']} bf16 sustained"}
+            peak, regime = choose_peak(pk, clk_sum, timed_s)
+            if regime == "burst":
+                why = "sub-second timed region at max clock, no power cap"
+            else:
+                why = f"{timed_s:.1f} s timed region, median {clk_sum.get('sm_mhz')} MHz"
+            src = f"{pk['source']} bf16 {regime} ({why})"
+            if storage == "bf16x3":
+                peak /= 3.0
+                src += " / 3 (bf16x3: three bf16 products per product)"
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "peak_source": src}
     else:
         per_launch = byts.get(dom, 0.0) * wl.n_chunks / max(1e-9, launches_per_step_dom)
         achieved = per_launch / dom_avg_s / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "peak_source": f"{pk['source']} copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = dom
     roof["traffic"] = profiled_traffic(wl.name, dom)
-    roof["traffic_source"] = (f"profiles/launches_{wl.name}.md (ncu dram__bytes_read.sum + dram__bytes_write.sum "
-                              f"per launch); null when the kernels changed since")
+    roof["traffic_source"] = ("profiles/traffic.json (ncu dram__bytes_read.sum + dram__bytes_write.sum per launch); "
+                              "null when the kernels changed since")
     roof["launches_per_step"] = launches_per_step_dom
     roof["avg_launch_ms"] = dom_avg_s * 1e3
+    roof["timing"] = f"CUDA events around each launch of the class in {dom_steps} untimed step(s)"
     t_roof, fl_chunk, by_chunk = chunk_roofline_seconds(wl, pk)
     chunk_frac = t_roof * wl.n_chunks / (total_ms / 1e3 / args.steps)
 
+    cfg = measured_config(wl, world, chunk_frac, t_roof, pk)
+    cfg["arith"] = storage
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.dtype == "fp32" else "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": storage,
             "data": "synthetic",
-            "config": measured_config(wl, world, chunk_frac, t_roof, pk),
+            "config": cfg,
             "roofline": roof, "clocks": clk_sum,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "decode": dec,
             "per_class_ms": {k: round(v[1], 3) for k, v in sorted(per_class.items(), key=lambda kv: -kv[1][1])}}
+    if n_ev:
+        line["settlement"] = {"events": n_ev, "accepted": int(acc.cpu().numpy()[:n_ev].sum()),
+                              "decisions": n_ev * wl.B}
     if rank == 0 and not args.no_cpu_baseline:
         n_chunks = 12 if wl.name == C.CHUNKED_FP32.name else 2
         n_seq = min(wl.B, 4)
@@ -522,7 +581,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=C.CHUNKED_FP32.name, choices=list(C.BY_NAME))
+    ap.add_argument("--workload", default=C.SETTLE_760M.name, choices=list(C.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
     ap.add_argument("--launch-log", default=None,

@@ -150,12 +150,7 @@ template <typename S>
 ttt_status launch_swa_typed(int B, int rows, int H, int dh, int window, const float* qkv, void* out,
                             long long out_lo, cudaStream_t st) {
   const size_t smem = swa_smem_bytes(dh);
-  static size_t smem_set = 0;
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_tile_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
-    smem_set = smem;
-  }
+  TTT_CUDA(ensure_dyn_smem((const void*)swa_tile_kernel<S>, smem));
   const dim3 grid(ceil_div(rows, kTile), H, B);
   launch_pdl(swa_tile_kernel<S>, grid, 256, smem, st, rows, H, dh, window, 1.0f / sqrtf((float)dh), qkv, out,
              out_lo);
@@ -379,12 +374,7 @@ template <typename S>
 static ttt_status launch_swa_decode_typed(int B, int H, int dh, int window, const int* pos, const float* qkv,
                                           float* ck, float* cv, void* out, long long out_lo, cudaStream_t st) {
   const size_t smem = swa_decode_smem_bytes(window, dh);
-  static size_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(swa_decode_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
-    smem_set = smem;
-  }
+  TTT_CUDA(ensure_dyn_smem((const void*)swa_decode_kernel<S>, smem));
   launch_pdl(swa_decode_kernel<S>, dim3(H, B), kDecThreads, smem, st, H, dh, window, 1.0f / sqrtf((float)dh), pos,
              qkv, ck, cv, out, out_lo);
   TTT_CHECK_LAUNCH();

@@ -217,9 +217,35 @@ inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Whether launches carry the programmatic-serialization attribute (on unless
-// the environment sets TTT_PDL=0).
+// Whether launches from the calling thread carry the programmatic-serialization
+// attribute: on, unless the handle of the API call in progress was created
+// with ttt_options.no_pdl (set for the call's duration by PdlScope).
 bool pdl_enabled();
+class PdlScope {
+ public:
+  explicit PdlScope(bool on);
+  ~PdlScope();
+  PdlScope(const PdlScope&) = delete;
+  PdlScope& operator=(const PdlScope&) = delete;
+
+ private:
+  bool saved_;
+};
+
+// ---------------------------------------------------------------- per-context state
+// Process-unique id of the CUDA context current on the calling thread (binding
+// the current device's primary context if none is), 0 if unknown.  State a
+// context owns is cached under this id, so a second device or a context made
+// after a device reset starts afresh.
+unsigned long long current_context_id();
+// Opt `func` into `bytes` of dynamic shared memory in the current context
+// (once per kernel, context and size; thread-safe; no-op up to 48 KB).
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
+// Device address of a __device__ variable in the current context (looked up
+// with cudaGetSymbolAddress once per context; thread-safe).
+cudaError_t symbol_address(const void* symbol, void** out);
+// SM count of the current device (cached per context).
+int current_sm_count();
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -20,14 +20,6 @@ static thread_local std::string g_last_error;
 
 void set_error(const std::string& msg) { g_last_error = msg; }
 
-bool pdl_enabled() {
-  static const bool on = [] {
-    const char* e = getenv("TTT_PDL");
-    return !(e && std::string(e) == "0");
-  }();
-  return on;
-}
-
 ttt_status cuda_fail(cudaError_t e, const char* what, const char* file, int line) {
   char buf[512];
   snprintf(buf, sizeof buf, "%s: %s (%s:%d)", what, cudaGetErrorString(e), file, line);
@@ -106,6 +98,7 @@ static ttt_status rungemm(ttt_handle* h, int cls, const GemmDesc& g_in, cudaStre
   g.ws = h->gemm_ws;
   g.ws_elems = h->gemm_ws_elems;
   g.cnt = h->split_cnt;
+  g.max_ctas = h->opt.max_ctas;
   return run(h, cls, st, gemm_count(g), [&] { return gemm(g, st); });
 }
 
@@ -735,12 +728,6 @@ static ttt_status decode_forward_graph(ttt_handle* h, cudaStream_t st) {
   return TTT_OK;
 }
 
-// TTT_DECODE_GRAPH=0 runs the next-token forward launch by launch instead.
-static bool decode_graph_enabled() {
-  const char* e = getenv("TTT_DECODE_GRAPH");
-  return !(e && std::string(e) == "0");
-}
-
 static ttt_status reset_weights(ttt_handle* h, cudaStream_t st) {
   TTT_TRY(run(h, K_OTHER, st, 1, [&] {
     return launch_broadcast_w0(h->stg, h->nslots, h->B, h->n, h->W0, h->W32, h->Wop.p, h->Wop.lo, st);
@@ -759,7 +746,13 @@ static ttt_status reset_weights(ttt_handle* h, cudaStream_t st) {
 static ttt_status finish(ttt_handle* h, cudaStream_t st) {
   TTT_CUDA(cudaMemcpyAsync(h->flag_host, h->flag, 4, cudaMemcpyDeviceToHost, st));
   TTT_CUDA(cudaStreamSynchronize(st));
-  if (*h->flag_host & kErrGemmTimeout) return fail(TTT_ERR_TIMEOUT, "a GEMM pipeline wait timed out");
+  if (*h->flag_host & kErrGemmTimeout) {
+    // a split-K CTA that gave up left its tile's arrival counter non-zero:
+    // clear every counter so the next call counts from zero
+    TTT_CUDA(cudaMemsetAsync(h->split_cnt, 0, (size_t)gemm_tc_max_split_tiles() * sizeof(int), st));
+    TTT_CUDA(cudaStreamSynchronize(st));
+    return fail(TTT_ERR_TIMEOUT, "a GEMM pipeline wait timed out");
+  }
   if (*h->flag_host & 2) return fail(TTT_ERR_BAD_ARG, "token id outside [0, vocab)");
   if (*h->flag_host & 1) return fail(TTT_ERR_NONFINITE, "non-finite gradient norm: update skipped");
   return TTT_OK;
@@ -944,8 +937,18 @@ ttt_status ttt_destroy(ttt_handle* h) {
 }
 
 ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_weights* w, ttt_handle** out) {
+  return ttt_create_ex(dims, hp, w, nullptr, out);
+}
+
+ttt_status ttt_create_ex(const ttt_dims* dims, const ttt_hparams* hp, const ttt_weights* w, const ttt_options* opt,
+                         ttt_handle** out) {
   if (!dims || !hp || !w || !out) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_create");
   *out = nullptr;
+  const ttt_options O = opt ? *opt : ttt_options{};
+  if (O.no_pdl < 0 || O.no_decode_graph < 0 || O.fp32_simt < 0 || O.hoist_chunks < 0 || O.no_token_kernel < 0 ||
+      O.max_ctas < 0)
+    return fail(TTT_ERR_BAD_ARG, "negative ttt_options field");
+  PdlScope pdl(!O.no_pdl);
   const ttt_dims& D = *dims;
   if (D.d <= 0 || D.d_ff <= 0 || D.vocab <= 0 || D.n_prefix < 0 || D.n_fast < 1 || D.rms_eps < 0.0f)
     return fail(TTT_ERR_BAD_ARG, "bad dims");
@@ -978,6 +981,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   ttt_handle* h = new ttt_handle();
   h->dm = D;
   h->hp = *hp;
+  h->opt = O;
   h->B = hp->max_batch; h->b = hp->chunk; h->d = D.d; h->f = D.d_ff; h->V = D.vocab;
   h->nm = D.block_kind == TTT_BLOCK_GELU ? 2 : 3;
   h->n = (long long)D.d * D.d_ff;
@@ -985,8 +989,7 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
   // fp32-accurate workloads run their GEMMs on the tensor cores as bf16 hi/lo
   // pairs when every leading dimension suits TMA and the chunk fills a tile
   // row block; otherwise they stay in plain fp32 (SIMT GEMMs).
-  const char* env_stg = getenv("TTT_FP32_STORAGE");
-  const bool force_f32 = env_stg && std::string(env_stg) == "f32";
+  const bool force_f32 = O.fp32_simt != 0;
   if (D.dtype == TTT_DTYPE_BF16)
     h->stg = ST_BF16;
   else if (!force_f32 && hp->chunk >= 64 && D.d % 8 == 0 && D.d_ff % 8 == 0 && D.vocab % 8 == 0 &&
@@ -1128,11 +1131,8 @@ ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp, const ttt_wei
     const size_t per_chunk = per_row * (size_t)B * h->b;
     long long gmax = (long long)((4ull << 30) / per_chunk);
     if (gmax > 64) gmax = 64;
-    // TTT_HOIST_CHUNKS caps the group (tests use it to cross group boundaries)
-    if (const char* e = getenv("TTT_HOIST_CHUNKS")) {
-      const long long cap = atoll(e);
-      if (cap > 0 && cap < gmax) gmax = cap;
-    }
+    // the option caps the group (tests use it to cross group boundaries)
+    if (O.hoist_chunks > 0 && O.hoist_chunks < gmax) gmax = O.hoist_chunks;
     if (gmax < 1) gmax = 1;
     h->hoist_chunks = (int)gmax;
     const size_t Mh = (size_t)B * h->b * gmax;
@@ -1229,6 +1229,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
                               float* A, ttt_stream stream) {
   if (!h || !tokens || !losses) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_prefill");
   if (B != h->B || T < 1) return fail(TTT_ERR_BAD_SHAPE, "B must equal max_batch and T >= 1");
+  PdlScope pdl(!h->opt.no_pdl);
   cudaStream_t st = (cudaStream_t)stream;
   const int b = h->b, n_full = T / b, rem = T % b;
   const int n_events = h->hp.settle_every > 0 ? n_full / h->hp.settle_every : 0;
@@ -1263,11 +1264,10 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
   TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
   // b = 1 on a network whose fast block and head fit in shared memory: one
   // persistent CTA per sequence steps through every token
-  const char* env_tok = getenv("TTT_TOKEN_KERNEL");
   const bool token_path = b == 1 && h->n_pre == 0 && h->dm.n_fast == 1 &&
                           h->dm.block_kind == TTT_BLOCK_GELU && h->stg == ST_F32 && h->hp.settle_every == 0 &&
                           h->hp.reset_every == 0 &&
-                          token_steps_supported(h->d, h->f, h->V) && !(env_tok && std::string(env_tok) == "0");
+                          token_steps_supported(h->d, h->f, h->V) && !h->opt.no_token_kernel;
   const bool attn = h->dm.attn_heads > 0;
   Hoisted hz_all;     // attention: the prefix of x_0 .. x_T of every sequence, one pass
   if (attn) {
@@ -1357,6 +1357,7 @@ ttt_status ttt_prefill_masked(ttt_handle* h, const int32_t* tokens, const uint8_
 ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, float* loss, ttt_stream stream) {
   if (!h || !x_new || !p_next) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_decode_step");
   if (!h->has_context) return fail(TTT_ERR_STATE, "decode before prefill");
+  PdlScope pdl(!h->opt.no_pdl);
   const bool attn = h->dm.attn_heads > 0;
   if (attn && !h->attn_ctx) return fail(TTT_ERR_STATE, "decoding with attention needs a prefill first");
   if (attn && swa_decode_smem_bytes(h->dm.attn_window, h->d / h->dm.attn_heads) > 227 * 1024)
@@ -1407,7 +1408,7 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   // attention: x_new's position (the decoding attention appends its K and V there)
   if (attn) TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_pos_add(h->dec_pos, st); }));
   const bool dev = is_device_ptr(p_next);
-  if (decode_graph_enabled()) {
+  if (!h->opt.no_decode_graph) {
     // the newest token into the fixed slot the captured forward reads
     TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4,
                              x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
@@ -1427,6 +1428,7 @@ ttt_status ttt_settle(ttt_handle* h, const int32_t* q, int Lq, uint8_t* accept, 
   if (!h || !q || !accept || !A) return fail(TTT_ERR_BAD_ARG, "null argument to ttt_settle");
   if (Lq != h->hp.settle_len || Lq < 2) return fail(TTT_ERR_BAD_SHAPE, "Lq must equal settle_len (>= 2)");
   if (h->dm.attn_heads > 0) return fail(TTT_ERR_UNSUPPORTED, "Settlement with attention is not built");
+  PdlScope pdl(!h->opt.no_pdl);
   cudaStream_t st = (cudaStream_t)stream;
   const int B = h->B;
   h->launches = 0;
@@ -1458,6 +1460,7 @@ ttt_status ttt_get_fast_weights(ttt_handle* h, int seq, int block, int mat, floa
 ttt_status ttt_reset(ttt_handle* h, ttt_stream stream) {
   if (!h) return fail(TTT_ERR_BAD_ARG, "null handle");
   h->next_valid = false;
+  PdlScope pdl(!h->opt.no_pdl);
   cudaStream_t st = (cudaStream_t)stream;
   TTT_TRY(reset_weights(h, st));
   h->has_context = false;
@@ -1513,6 +1516,7 @@ ttt_status ttt_set_state(ttt_handle* h, const void* src, size_t bytes, ttt_strea
       hd.dtype != h->dtype || hd.B != h->B || hd.b != h->b || hd.nslots != h->nslots ||
       hd.pend_count < 0 || hd.pend_count >= h->b)
     return fail(TTT_ERR_BAD_SHAPE, "state blob does not match this handle");
+  PdlScope pdl(!h->opt.no_pdl);
   cudaStream_t st = (cudaStream_t)stream;
   h->next_valid = false;
   const char* p = static_cast<const char*>(src) + sizeof hd;
@@ -1572,6 +1576,8 @@ int ttt_launch_log_read(ttt_handle* h, int8_t* out, int cap) {
   for (int i = 0; i < n && i < cap && out; ++i) out[i] = h->launch_log[(size_t)i];
   return n;
 }
+
+int ttt_operand_storage(ttt_handle* h) { return h ? h->stg : -1; }
 
 ttt_status ttt_last_launch_count(ttt_handle* h, long long* launches) {
   if (!h || !launches) return fail(TTT_ERR_BAD_ARG, "null argument");

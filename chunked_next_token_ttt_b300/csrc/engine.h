@@ -23,6 +23,7 @@ struct OpBuf {
 struct ttt_handle {
   ttt_dims dm{};
   ttt_hparams hp{};
+  ttt_options opt{};      // execution options fixed at create (zero = defaults)
   int B = 0, b = 0, d = 0, f = 0, V = 0;
   int nm = 0;             // matrices per block (2 GELU, 3 SwiGLU)
   int nslots = 0;         // fast matrices in total (arena slots)

@@ -42,8 +42,10 @@ struct GemmDesc {
   float* ws = nullptr;
   long long ws_elems = 0;
   // split-K arrival counters, one per output tile, zero between launches; GEMMs
-  // that share them must run in stream order (null: a library-wide array)
+  // that share them must run in stream order (null: K is never split)
   int* cnt = nullptr;
+  // cap on the tensor-core kernel's persistent grid (0: one CTA per SM)
+  int max_ctas = 0;
   // set by the tensor-core host code: every epilogue pointer, leading dim,
   // batch stride and lo offset is a multiple of 16 elements with 32-byte aligned
   // pointers (2: 32-byte accesses), else of 8 elements with 16-byte aligned
@@ -73,10 +75,10 @@ bool gemm_tc_supported(const GemmDesc& g);
 // Output-tile width the tensor-core kernel uses for g (the column tiles of
 // EPI_LOGITS, the per-tile partials of EPI_DW).
 int gemm_tc_tile_n(const GemmDesc& g);
-// Split-K arrival counters: the library-wide array (allocated and zeroed on
-// first use) and its capacity in output tiles.
-ttt_status gemm_tc_split_counters(int** cnt);
+// Capacity of a split-K arrival-counter array, in output tiles.
 int gemm_tc_max_split_tiles();
+// The library's status word for tensor-core GEMMs launched without one.
+ttt_status gemm_tc_status_word(int** err);
 int gemm_tc_partial_tiles(const GemmDesc& g);
 ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st);
 

@@ -12,7 +12,11 @@ namespace tc {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-int* g_err = nullptr;
+
+// Status word for GEMMs launched without one (the single-operation API): a
+// bounded wait that gives up records its code here.  File-scope device
+// memory, so no call allocates; every GPU that loads the library holds it.
+__device__ int g_tc_status;
 
 ttt_status init_driver() {
   std::call_once(g_encode_once, [] {
@@ -49,8 +53,6 @@ ttt_status make_map(CUtensorMap* m, const void* base, long long inner, long long
   }
   return TTT_OK;
 }
-
-int g_num_sms = 0;
 
 }  // namespace tc
 
@@ -97,7 +99,7 @@ static TcPlan plan(const GemmDesc& g) {
   TcPlan best;
   double best_cost = 1e300;
   const int nkb = ceil_div(g.K, tc::BK);
-  const bool can_split = g.ws && g.epi != EPI_DW && g.epi != EPI_LOGITS && !(g.N & 1) && nkb >= 8;
+  const bool can_split = g.ws && g.cnt && g.epi != EPI_DW && g.epi != EPI_LOGITS && !(g.N & 1) && nkb >= 8;
   for (int bn : {256, 128}) {
     if (bn == 256 && g.dtype != ST_BF16) continue;
     const long long tiles = (long long)ceil_div(g.N, bn) * ceil_div(g.M, tc::BM) * g.batch;
@@ -130,26 +132,10 @@ int gemm_tc_tile_n(const GemmDesc& g) { return choose_bn(g); }
 
 int gemm_tc_partial_tiles(const GemmDesc& g) { return ceil_div(g.N, choose_bn(g)) * ceil_div(g.M, tc::BM); }
 
-ttt_status gemm_tc_error_word(int** err) {
-  if (!tc::g_err) {
-    cudaError_t e = cudaMalloc(&tc::g_err, 4);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc", __FILE__, __LINE__);
-    e = cudaMemset(tc::g_err, 0, 4);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset", __FILE__, __LINE__);
-  }
-  *err = tc::g_err;
-  return TTT_OK;
-}
-
-ttt_status gemm_tc_split_counters(int** cnt) {
-  static int* g_cnt = nullptr;
-  if (!g_cnt) {
-    cudaError_t e = cudaMalloc(&g_cnt, tc::kMaxSplitTiles * sizeof(int));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc", __FILE__, __LINE__);
-    e = cudaMemset(g_cnt, 0, tc::kMaxSplitTiles * sizeof(int));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset", __FILE__, __LINE__);
-  }
-  *cnt = g_cnt;
+ttt_status gemm_tc_status_word(int** err) {
+  void* p = nullptr;
+  TTT_CUDA(symbol_address((const void*)&tc::g_tc_status, &p));
+  *err = static_cast<int*>(p);
   return TTT_OK;
 }
 
@@ -162,7 +148,7 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   }
   TTT_TRY(tc::init_driver());
   GemmDesc gd = g;
-  if (!gd.err) TTT_TRY(gemm_tc_error_word(&gd.err));
+  if (!gd.err) TTT_TRY(gemm_tc_status_word(&gd.err));
   const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
   const bool split = g.dtype == ST_SPLIT;
   const TcPlan pl = plan(g);
@@ -189,26 +175,14 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
     else if ((m & 7) == 0 && al(g.out, 16) && al(g.out2, 16) && al(g.aux, 16)) gd.vec = 1;
     else gd.vec = 0;
   }
-  if (!tc::g_num_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&tc::g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (tc::g_num_sms <= 0) tc::g_num_sms = 148;
-    // TTT_TC_MAX_CTAS caps the persistent grid (for per-SM throughput measurements)
-    if (const char* e = getenv("TTT_TC_MAX_CTAS")) {
-      const int cap = atoi(e);
-      if (cap > 0 && cap < tc::g_num_sms) tc::g_num_sms = cap;
-    }
-  }
   if (splitk > 1) {
-    // partial tiles go to the workspace; the per-tile arrival counters start at
-    // zero and every split-K launch leaves them at zero
+    // partial tiles go to the workspace; the caller's per-tile arrival counters
+    // start at zero and every split-K launch that completes leaves them at zero
     const long long tiles = (long long)ceil_div(g.M, tc::BM) * ceil_div(g.N, gd.bn) * g.batch;
-    if (tiles > tc::kMaxSplitTiles) {
-      set_error("split-K GEMM with too many output tiles");
+    if (tiles > tc::kMaxSplitTiles || !gd.cnt) {
+      set_error("split-K GEMM with too many output tiles or without arrival counters");
       return TTT_ERR_UNSUPPORTED;
     }
-    if (!gd.cnt) TTT_TRY(gemm_tc_split_counters(&gd.cnt));
   }
   if (!a_mn && !b_mn) return tc::launch_kk(gd, maps, nkb, splitk, st);
   if (!a_mn) return tc::launch_km(gd, maps, nkb, splitk, st);

@@ -579,22 +579,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-extern int g_num_sms;
-
 // Launch one instantiation (persistent grid, one CTA per SM at most).
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, int EK>
 ttt_status launch_bn(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
   using L = Smem<BN, SPLIT>;
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, SPLIT, EK>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
-    attr_set = true;
-  }
+  TTT_CUDA(ensure_dyn_smem((const void*)kern, L::ALLOC));
   const int mtiles = ceil_div(g.M, BM), ntiles = ceil_div(g.N, BN);
   const long long units = (long long)mtiles * ntiles * g.batch * splitk;
-  const int grid = (int)(units < g_num_sms ? units : g_num_sms);
+  int ctas = current_sm_count();
+  if (g.max_ctas > 0 && g.max_ctas < ctas) ctas = g.max_ctas;
+  const int grid = (int)(units < ctas ? units : ctas);
   launch_pdl(kern, grid, NUM_THREADS, L::ALLOC, st, maps[0], maps[1], maps[2], maps[3], g, nkb, splitk, mtiles, ntiles, g.err);
   TTT_CHECK_LAUNCH();
   return TTT_OK;

@@ -649,12 +649,7 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
       return TTT_ERR_UNSUPPORTED;
     }
     const size_t smem = (size_t)V * sizeof(float);
-    static size_t smem_set = 0;
-    if (smem > 48 * 1024 && smem > smem_set) {
-      cudaError_t e = cudaFuncSetAttribute(ce_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
-      smem_set = smem;
-    }
+    TTT_CUDA(ensure_dyn_smem((const void*)ce_split_kernel, smem));
     launch_pdl(ce_split_kernel, M, 512, smem, st, tv, V, static_cast<float*>(logits), ldl, scale, rscale, grad, losses, loss_ld,
                                           loss_off, row_loss);
   } else if (stg == ST_BF16) {

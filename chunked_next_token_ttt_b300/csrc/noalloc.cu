@@ -9,8 +9,6 @@
 // partial sums, per-sequence scales and the status word live in
 // g_clip_sgd_scratch below, which every GPU that loads the library holds until
 // the process exits.
-#include <mutex>
-
 #include "clip_sgd.h"
 #include "ttt_ops.h"
 
@@ -22,29 +20,16 @@ namespace {
 // threads) race on it.
 static __device__ __align__(256) float g_clip_sgd_scratch[TTT_CLIP_SGD_NOALLOC_MAX_FLOATS];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
-
-// The device address of the scratch array on the current device.  In host code
-// the array's name is only a host-side stand-in, so the address is looked up
-// once per device with cudaGetSymbolAddress (with that device current).
-ttt_status scratch_for_current_device(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return ttt::cuda_fail(e, "cudaGetDevice", __FILE__, __LINE__);
-  if (dev < 0 || dev >= kMaxDevices) {
-    ttt::set_error("device index beyond the no-alloc scratch table");
-    return TTT_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_clip_sgd_scratch);
-    if (e != cudaSuccess) return ttt::cuda_fail(e, "cudaGetSymbolAddress", __FILE__, __LINE__);
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+// The device address of the scratch array in the current context.  In host
+// code the array's name is only a host-side stand-in, so the address is looked
+// up with cudaGetSymbolAddress, once per CUDA context (with that context
+// current): a second device, or the new context after a device reset, gets its
+// own lookup.
+ttt_status scratch_for_current_context(float** out) {
+  void* p = nullptr;
+  const cudaError_t e = ttt::symbol_address((const void*)&g_clip_sgd_scratch, &p);
+  if (e != cudaSuccess) return ttt::cuda_fail(e, "cudaGetSymbolAddress", __FILE__, __LINE__);
+  *out = static_cast<float*>(p);
   return TTT_OK;
 }
 
@@ -67,7 +52,7 @@ extern "C" ttt_status ttt_clip_sgd_noalloc(int dtype, int nslots, int B, long lo
     return TTT_ERR_BAD_SHAPE;
   }
   float* scratch = nullptr;
-  TTT_TRY(scratch_for_current_device(&scratch));
+  TTT_TRY(scratch_for_current_context(&scratch));
   cudaStream_t st = (cudaStream_t)stream;
   TTT_TRY(ttt::launch_clip_sgd(dtype, nslots, B, n, W32, Wop, dW, eta, clip, norm_out, scale_out, scratch, st));
   int flag = 0;

@@ -6,6 +6,10 @@
 
 using namespace ttt;
 
+// Status word of the single-operation cross-entropy (token ids outside [0, V)
+// are recorded here): file-scope device memory, so no call allocates.
+static __device__ int g_ce_status;
+
 static ttt_status bad(ttt_status s, const char* msg) {
   set_error(msg);
   return s;
@@ -26,7 +30,14 @@ static bool to_desc(const ttt_gemm_args* a, GemmDesc* g) {
   g->partials = a->partials;
   g->impl = a->impl;
   g->loA = a->loA; g->loB = a->loB; g->loO = a->loO; g->loO2 = a->loO2; g->loX = a->loX;
-  g->ws = a->workspace; g->ws_elems = a->workspace ? a->workspace_elems : 0;
+  // the workspace's last gemm_tc_max_split_tiles() words hold the split-K
+  // arrival counters; the rest takes the partial tiles
+  const long long ncnt = gemm_tc_max_split_tiles();
+  if (a->workspace && a->workspace_elems > ncnt) {
+    g->ws = a->workspace;
+    g->ws_elems = a->workspace_elems - ncnt;
+    g->cnt = reinterpret_cast<int*>(a->workspace + g->ws_elems);
+  }
   return true;
 }
 
@@ -40,6 +51,8 @@ ttt_status ttt_op_gemm(const ttt_gemm_args* args, ttt_stream stream) {
     return bad(TTT_ERR_BAD_ARG, "epilogue operand missing");
   if (g.impl == TTT_GEMM_TENSOR && !gemm_tc_supported(g))
     return bad(TTT_ERR_UNSUPPORTED, "shape/alignment not supported by the tensor-core GEMM");
+  if (g.cnt)   // this call's counters start at zero, in stream order
+    TTT_CUDA(cudaMemsetAsync(g.cnt, 0, (size_t)gemm_tc_max_split_tiles() * sizeof(int), (cudaStream_t)stream));
   return gemm(g, (cudaStream_t)stream);
 }
 
@@ -63,13 +76,9 @@ ttt_status ttt_op_cross_entropy(int dtype, int M, int V, void* logits, const int
   tv.rows = M;
   tv.n_valid = M;
   tv.vocab = V;
-  static int* err = nullptr;
-  if (!err) {
-    cudaError_t e = cudaMalloc(&err, 4);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc", __FILE__, __LINE__);
-    cudaMemset(err, 0, 4);
-  }
-  tv.err = err;
+  void* err = nullptr;
+  TTT_CUDA(symbol_address((const void*)&g_ce_status, &err));
+  tv.err = static_cast<int*>(err);
   return launch_ce(dtype, 1, tv, V, logits, V, scale, nullptr, grad != 0, losses, 0, 0, nullptr,
                    (cudaStream_t)stream);
 }

@@ -284,12 +284,7 @@ ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T
   }
   if (B == 0 || T == 0) return TTT_OK;
   const size_t smem = token_smem_bytes(d, f, V);
-  static size_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(token_steps_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", __FILE__, __LINE__);
-    smem_set = smem;
-  }
+  TTT_CUDA(ensure_dyn_smem((const void*)token_steps_kernel, smem));
   TokenArgs a{tok, tok_ld, T, mask, mask_ld, E, U, W32, Wop, slot_w1, slot_w2, B, losses, loss_ld, d, f, V, eps, eta,
               clip, err};
   launch_pdl(token_steps_kernel, B, kTokThreads, smem, st, a);

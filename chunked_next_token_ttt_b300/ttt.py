@@ -43,6 +43,12 @@ class HParams(ctypes.Structure):
                 ("reset_every", ctypes.c_int)]
 
 
+class Options(ctypes.Structure):
+    """ttt_options: zero fields are the library's defaults."""
+    _fields_ = [("no_pdl", ctypes.c_int), ("no_decode_graph", ctypes.c_int), ("fp32_simt", ctypes.c_int),
+                ("hoist_chunks", ctypes.c_int), ("no_token_kernel", ctypes.c_int), ("max_ctas", ctypes.c_int)]
+
+
 class Weights(ctypes.Structure):
     _fields_ = [("E", ctypes.c_void_p), ("U", ctypes.c_void_p),
                 ("prefix", ctypes.POINTER(ctypes.c_void_p)), ("fast", ctypes.POINTER(ctypes.c_void_p)),
@@ -66,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     sig = {
         "ttt_create": ([ctypes.POINTER(Dims), ctypes.POINTER(HParams), ctypes.POINTER(Weights),
                         ctypes.POINTER(_P)], _I),
+        "ttt_create_ex": ([ctypes.POINTER(Dims), ctypes.POINTER(HParams), ctypes.POINTER(Weights),
+                           ctypes.POINTER(Options), ctypes.POINTER(_P)], _I),
         "ttt_destroy": ([_P], _I),
         "ttt_prefill": ([_P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
         "ttt_prefill_masked": ([_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
@@ -81,6 +89,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ttt_kernel_class_name": ([_I], ctypes.c_char_p),
         "ttt_kernel_class_count": ([], _I),
         "ttt_last_launch_count": ([_P, ctypes.POINTER(ctypes.c_longlong)], _I),
+        "ttt_operand_storage": ([_P], _I),
         "ttt_launch_log_enable": ([_P, _I], _I),
         "ttt_launch_log_read": ([_P, ctypes.POINTER(ctypes.c_int8), _I], _I),
         "ttt_status_string": ([_I], ctypes.c_char_p),
@@ -135,10 +144,11 @@ class Handle:
 
     def __init__(self, *, d, d_ff, vocab, n_prefix, n_fast, block, fast_mats, dtype, eta, clip, chunk,
                  B, weights, settle_every=0, settle_len=0, rms_eps=1e-6, reset_every=0, static_mlp=False,
-                 attn_heads=0, attn_window=0):
+                 attn_heads=0, attn_window=0, options=None):
         """weights: {"E", "U", "prefix": [block dicts], "fast": [block dicts]};
         with static_mlp, "static": one frozen MLP (block dict) per fast block;
-        with attn_heads > 0, "attn": one {"Wq", "Wk", "Wv", "Wo"} per prefix block."""
+        with attn_heads > 0, "attn": one {"Wq", "Wk", "Wv", "Wo"} per prefix block.
+        options: {field of ttt_options: int} (omitted fields keep the defaults)."""
         self.lib = load_library()
         self.block = block
         self.mats = MATS[block]
@@ -177,19 +187,20 @@ class Handle:
                     ctypes.cast(sta_arr, ctypes.POINTER(ctypes.c_void_p)) if static_mlp else None,
                     ctypes.cast(att_arr, ctypes.POINTER(ctypes.c_void_p)) if attn_heads else None)
         h = ctypes.c_void_p()
-        _check(self.lib.ttt_create(ctypes.byref(self._dims), ctypes.byref(self._hp), ctypes.byref(w),
-                                   ctypes.byref(h)), "ttt_create")
+        self._opt = Options(**{k: int(v) for k, v in (options or {}).items()})
+        _check(self.lib.ttt_create_ex(ctypes.byref(self._dims), ctypes.byref(self._hp), ctypes.byref(w),
+                                      ctypes.byref(self._opt), ctypes.byref(h)), "ttt_create_ex")
         self._h = h
         del keep
 
     @classmethod
-    def from_workload(cls, wl, weights, B=None):
+    def from_workload(cls, wl, weights, B=None, options=None):
         return cls(d=wl.d, d_ff=wl.d_ff, vocab=wl.vocab, n_prefix=wl.n_prefix, n_fast=wl.n_fast,
                    block=wl.block, fast_mats=wl.fast_mats, dtype=wl.dtype, eta=wl.eta, clip=wl.clip,
                    chunk=wl.chunk, B=wl.B if B is None else B, weights=weights,
                    settle_every=wl.settle_every, settle_len=wl.settle_len, rms_eps=wl.rms_eps,
                    reset_every=wl.reset_every, static_mlp=wl.static_mlp, attn_heads=wl.attn_heads,
-                   attn_window=wl.attn_window)
+                   attn_window=wl.attn_window, options=options)
 
     def close(self):
         if getattr(self, "_h", None):
@@ -263,6 +274,10 @@ class Handle:
         ms = ctypes.c_double()
         _check(self.lib.ttt_profile_read(self._h, ctypes.byref(n), ctypes.byref(ms)), "ttt_profile_read")
         return n.value, ms.value
+
+    def operand_storage(self) -> str:
+        """The arithmetic of the handle's GEMMs: "f32", "bf16" or "bf16x3"."""
+        return {0: "f32", 1: "bf16", 2: "bf16x3"}[self.lib.ttt_operand_storage(self._h)]
 
     def last_launch_count(self) -> int:
         n = ctypes.c_longlong()

@@ -69,7 +69,10 @@ typedef enum {
   TTT_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
   TTT_ERR_NONFINITE = 5,    /* a non-finite gradient norm: that update was
                                skipped for that sequence, the rest ran      */
-  TTT_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up           */
+  TTT_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up; that
+                               call's outputs are undefined, and the handle
+                               clears its split-K counters before returning,
+                               so later calls run normally                  */
   TTT_ERR_UNSUPPORTED = 7,  /* a valid request the library does not run    */
   TTT_ERR_STATE = 8         /* call out of order (e.g. decode before prefill) */
 } ttt_status;
@@ -148,11 +151,35 @@ typedef struct {
 
 typedef struct ttt_handle ttt_handle;
 
+/* Execution options of a handle.  A zero-filled struct (or NULL) selects the
+ * library's defaults, which are what ttt_create uses; nothing outside this
+ * struct (no environment variable, no global) changes how a handle runs.  The
+ * non-default settings exist for tests and measurements: each selects another
+ * path to the same results, or limits the GPU the handle uses. */
+typedef struct {
+  int no_pdl;          /* 1: launch kernels without programmatic dependent launch */
+  int no_decode_graph; /* 1: ttt_decode_step launches its next-token forward kernel
+                          by kernel instead of replaying one captured CUDA graph */
+  int fp32_simt;       /* 1: TTT_DTYPE_FP32 handles keep plain fp32 operands and
+                          SIMT GEMMs instead of bf16x3 tensor-core products   */
+  int hoist_chunks;    /* > 0: at most this many chunks share one pass of the
+                          frozen prefix (0: as many as a 4 GiB buffer holds, up
+                          to 64)                                              */
+  int no_token_kernel; /* 1: chunk = 1 runs the general chunk step instead of the
+                          persistent per-token kernel                          */
+  int max_ctas;        /* > 0: at most this many CTAs in a tensor-core GEMM's
+                          persistent grid (0: one per SM)                      */
+} ttt_options;
+
 /* Validate dims/hparams, allocate every device buffer the handle needs for
  * B = max_batch sequences and upload the weights.  On success *out owns all
  * of it until ttt_destroy.  Errors: BAD_ARG, UNSUPPORTED, OOM, CUDA. */
 ttt_status ttt_create(const ttt_dims* dims, const ttt_hparams* hp,
                       const ttt_weights* w, ttt_handle** out);
+/* ttt_create with execution options (NULL = defaults).  Errors: as ttt_create,
+ * and BAD_ARG for a negative option. */
+ttt_status ttt_create_ex(const ttt_dims* dims, const ttt_hparams* hp,
+                         const ttt_weights* w, const ttt_options* opt, ttt_handle** out);
 
 /* Free everything the handle owns.  NULL is accepted. */
 ttt_status ttt_destroy(ttt_handle* h);
@@ -236,6 +263,11 @@ ttt_status ttt_profile_enable(ttt_handle* h, int kernel_class);
 ttt_status ttt_profile_read(ttt_handle* h, int* launches, double* total_ms);
 const char* ttt_kernel_class_name(int kernel_class);
 int ttt_kernel_class_count(void);
+
+/* The arithmetic the handle's GEMMs use, fixed at create: 0 = plain fp32
+ * (SIMT), 1 = bf16 operands, 2 = bf16x3 (fp32 values as bf16 hi/lo pairs,
+ * three tensor-core products per product), or -1 for a null handle. */
+int ttt_operand_storage(ttt_handle* h);
 
 /* Number of kernels the last ttt_prefill launched on the GPU. */
 ttt_status ttt_last_launch_count(ttt_handle* h, long long* launches);

@@ -2,7 +2,8 @@
  * libttt single-operation entry points.
  *
  * Each call runs one stage of the TTT chunk step on device buffers the caller
- * owns, in stream order on `stream`, without synchronising.  They exist for
+ * owns, in stream order on `stream`; none allocates device memory, and only
+ * the clipped SGD step synchronises (to read its status).  They exist for
  * per-kernel tests and measurements and for callers that assemble their own
  * loop; ttt.h's ttt_prefill runs the same stages.  All pointers are device
  * pointers.  Errors are returned as ttt_status (ttt.h); nothing aborts.
@@ -52,8 +53,12 @@ typedef struct {
   const void* aux; long long ldx, sX;
   float* partials;
   long long loA, loB, loO, loO2, loX;   /* lo-plane offsets (TTT_STORAGE_BF16X3 only) */
-  float* workspace;                     /* optional fp32 device buffer: lets the tensor-core
-                                           path split K when the output has few tiles */
+  float* workspace;                     /* optional fp32 device buffer (more than 4096
+                                           elements): lets the tensor-core path split K
+                                           when the output has few tiles.  Its last 4096
+                                           words hold the split-K arrival counters, which
+                                           the call clears in stream order; calls that
+                                           share a workspace must run in stream order */
   long long workspace_elems;
 } ttt_gemm_args;
 
@@ -108,9 +113,11 @@ size_t ttt_clip_sgd_workspace_size(int nslots, int B, long long n);
  * call allocates nothing (no cudaMalloc, cudaFree or allocating routine).
  * Sizes needing more than the maximum, i.e. nslots * B * ceil(n / 8192) + B + 1
  * floats, return TTT_ERR_BAD_SHAPE with a message naming the limit.
- * The first call on a device looks up the array's device address for that
- * device (cudaGetSymbolAddress); make that first call before any stream
- * capture.  All calls share the one array: calls that overlap on the GPU (on
+ * The first call in a CUDA context (per device, and again after a device
+ * reset) looks up the array's device address there (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  Like ttt_clip_sgd, every
+ * call copies the status word to the host and synchronises `stream` before it
+ * returns.  All calls share the one array: calls that overlap on the GPU (on
  * different streams or from different host threads) race and must be
  * serialised by the caller.  Nothing in the array needs to start at zero:
  * each call writes every word before it reads it. */

@@ -36,11 +36,11 @@ def run_oracle(wl, inp, seqs=None, tokens=None, q=None, loss_mask=None):
                           reset_every=wl.reset_every)
 
 
-def run_gpu(wl, inp, device=True, tokens=None, q=None, handle=None, loss_mask=None):
+def run_gpu(wl, inp, device=True, tokens=None, q=None, handle=None, loss_mask=None, options=None):
     tok = inp["tokens"] if tokens is None else tokens
     sq = inp["settle_q"] if q is None else q
     B, T1 = tok.shape
-    h = handle or Handle.from_workload(wl, inp["weights"], B=B)
+    h = handle or Handle.from_workload(wl, inp["weights"], B=B, options=options)
     n_ev = ((T1 - 1) // wl.chunk) // wl.settle_every if wl.settle_every else 0
     if device:
         t = torch.from_numpy(np.ascontiguousarray(tok)).cuda()

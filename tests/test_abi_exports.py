@@ -84,3 +84,13 @@ def test_static_mlp_outside_gelu_blocks_is_unsupported_before_any_cuda_call():
     with pytest.raises(TTTError) as e:
         Handle.from_workload(wl, synth.make_weights(wl))
     assert e.value.status == 7
+
+
+def test_no_environment_variable_steers_the_library():
+    """Execution choices are ttt_options fields: no library source reads the
+    environment, so a caller's environment cannot change results or speed."""
+    import glob
+    csrc = os.path.join(ROOT, "chunked_next_token_ttt_b300", "csrc")
+    for path in glob.glob(os.path.join(csrc, "*")):
+        with open(path) as f:
+            assert "getenv" not in f.read(), path

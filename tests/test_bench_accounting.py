@@ -64,3 +64,32 @@ def test_both_arms_name_the_same_workload_config():
     assert ref["attn_window"] == 2048 and ref["tokens_per_step"] == wl.B * wl.T
     t_roof, fl, by = bench.chunk_roofline_seconds(C.CHUNKED_FP32, pk)
     assert t_roof > 0 and fl > 0 and by > 0
+
+
+def test_settlement_flops_count_one_prefix_and_two_forwards():
+    """A Settlement event runs the frozen prefix over the held-out chunks once
+    and the fast blocks and the head forward twice (committed and current
+    weights); a whole step adds every chunk, every event and p_{T+1}."""
+    wl = C.SETTLE_760M.replace(d=8, d_ff=24, vocab=40, chunk=4, B=3, T=64, n_prefix=2, n_fast=3,
+                               settle_every=2, settle_len=6)
+    Mq, d, f, V = wl.B * wl.settle_len, wl.d, wl.d_ff, wl.vocab
+    g = lambda m, n, k: 2.0 * m * n * k
+    sf = bench.settle_flops(wl)
+    assert sf["gemm_prefix"] == 2 * (g(Mq, f, d) + g(Mq, d, f))
+    assert sf["gemm_fast_fwd"] == 2 * 3 * (g(Mq, f, d) + g(Mq, d, f))
+    assert sf["gemm_head"] == 2 * g(Mq, V, d)
+    step = bench.step_flops(wl)
+    ch, one = bench.chunk_flops(wl), bench.chunk_flops(wl, rows=1)
+    assert wl.n_chunks == 16 and wl.n_settle_events == 8
+    assert step["gemm_prefix"] == 16 * ch["gemm_prefix"] + 8 * sf["gemm_prefix"] + one["gemm_prefix"]
+    assert step["gemm_dw"] == 16 * ch["gemm_dw"]
+    assert bench.settle_flops(wl.replace(settle_every=0)) == {}
+
+
+def test_peak_choice_follows_the_clock_record():
+    pk = {"bf16_tflops": 1700.0, "bf16_tflops_sustained": 1300.0}
+    fast = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}
+    assert bench.choose_peak(pk, fast, 0.4) == (1700.0, "burst")
+    assert bench.choose_peak(pk, fast, 3.0) == (1300.0, "sustained")
+    assert bench.choose_peak(pk, dict(fast, reasons=["sw_power_cap"]), 0.4) == (1300.0, "sustained")
+    assert bench.choose_peak(pk, dict(fast, sm_mhz=1500.0), 0.4) == (1300.0, "sustained")

@@ -36,14 +36,13 @@ def test_toy_bigram_fp32_full_size():
 
 
 @pytest.mark.parametrize("token_kernel", ["1", "0"], ids=["persistent", "general"])
-def test_per_token_clipped_b1_both_paths(monkeypatch, token_kernel):
+def test_per_token_clipped_b1_both_paths(token_kernel):
     """b = 1 with a clip that binds, three sequences, odd widths: the persistent
     per-token kernel (closed-form outer-product norm) and the general chunk path
     both match the oracle within the fp32 tolerance."""
-    monkeypatch.setenv("TTT_TOKEN_KERNEL", token_kernel)
     wl = C.TOY_BIGRAM.replace(d=40, d_ff=100, vocab=90, B=3, T=150, clip=0.05, eta=0.2)
     inp = make(wl)
-    gpu = run_gpu(wl, inp)
+    gpu = run_gpu(wl, inp, options={"no_token_kernel": token_kernel == "0"})
     ref = run_oracle(wl, inp)
     assert max(max(st.norms) for st in ref["states"]) > wl.clip      # the clip binds
     compare(wl, gpu, ref)
@@ -90,12 +89,11 @@ def test_chunked_fp32_full_size():
     compare(wl, gpu, ref)
 
 
-def test_chunked_fp32_plain_storage_matches_too(monkeypatch):
+def test_chunked_fp32_plain_storage_matches_too():
     """The same workload with fp32 storage forced (SIMT GEMMs) also passes."""
-    monkeypatch.setenv("TTT_FP32_STORAGE", "f32")
     wl = C.CHUNKED_FP32.replace(T=2 * C.CHUNKED_FP32.chunk, B=2)
     inp = make(wl)
-    gpu = run_gpu(wl, inp)
+    gpu = run_gpu(wl, inp, options={"fp32_simt": 1})
     ref = run_oracle(wl, inp)
     compare(wl, gpu, ref)
 
@@ -143,24 +141,22 @@ def test_settlement_bf16_small_widths():
     compare(wl, gpu, ref)
 
 
-def test_hoisted_prefix_groups_bf16(monkeypatch):
+def test_hoisted_prefix_groups_bf16():
     """The frozen prefix runs once per group of chunks; groups of 2 over 5
     chunks (2 + 2 + 1) give the same result as the oracle's chunk-by-chunk loop."""
-    monkeypatch.setenv("TTT_HOIST_CHUNKS", "2")
     wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1024, chunk=128, B=3, T=5 * 128, n_prefix=2)
     inp = make(wl)
-    gpu = run_gpu(wl, inp)
+    gpu = run_gpu(wl, inp, options={"hoist_chunks": 2})
     ref = run_oracle(wl, inp)
     compare(wl, gpu, ref)
 
 
-def test_hoisted_swiglu_activation_groups_ragged_tail(monkeypatch):
+def test_hoisted_swiglu_activation_groups_ragged_tail():
     """SwiGLU block whose frozen gate/up activation is hoisted with the prefix:
     groups of 2 over 5 chunks, then a ragged tail scored by the per-call path."""
-    monkeypatch.setenv("TTT_HOIST_CHUNKS", "2")
     wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=64, B=2, T=5 * 64 + 9, n_prefix=1)
     inp = make(wl)
-    gpu = run_gpu(wl, inp)
+    gpu = run_gpu(wl, inp, options={"hoist_chunks": 2})
     ref = run_oracle(wl, inp)
     compare(wl, gpu, ref)
 
@@ -237,7 +233,7 @@ def _random_mask(B, T, b, seed):
 
 @pytest.mark.parametrize("case", ["bf16_gelu_fused_ce", "bf16_swiglu_hoisted", "fp32_split_ce", "fp32_rows",
                                   "fp32_rows_host", "b1_persistent", "b1_general"])
-def test_source_masking_against_the_oracle(monkeypatch, case):
+def test_source_masking_against_the_oracle(case):
     """Source Masking (a per-token mask on the chunk loss): every CE path of the
     GPU (fused dlogits, bf16x3 row CE, fp32 row CE, the per-token kernel) and
     the hoisted prefix, against the oracle's masked loop; a fully masked chunk
@@ -251,11 +247,11 @@ def test_source_masking_against_the_oracle(monkeypatch, case):
     elif case.startswith("fp32_rows"):
         wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=40, B=3, T=130, n_prefix=1)
     else:
-        monkeypatch.setenv("TTT_TOKEN_KERNEL", "1" if case == "b1_persistent" else "0")
         wl = C.TOY_BIGRAM.replace(B=2, T=200, clip=0.5)
     inp = make(wl)
     mask = _random_mask(wl.B, wl.T, wl.chunk, seed=len(case) * 7 + wl.seed_id)
-    gpu = run_gpu(wl, inp, device=not case.endswith("_host"), loss_mask=mask)
+    gpu = run_gpu(wl, inp, device=not case.endswith("_host"), loss_mask=mask,
+                  options={"no_token_kernel": case == "b1_general"})
     ref = run_oracle(wl, inp, loss_mask=mask)
     compare(wl, gpu, ref)
     # The GPU's weights sit much nearer the masked trajectory than the unmasked one.
@@ -321,7 +317,7 @@ def test_periodic_reset_counts_decoded_chunks():
 
 
 @pytest.mark.parametrize("case", ["fp32_split", "fp32_rows", "bf16_hoisted", "bf16_settle", "b1"])
-def test_two_mlp_fast_blocks_against_the_oracle(monkeypatch, case):
+def test_two_mlp_fast_blocks_against_the_oracle(case):
     """Fast blocks holding a frozen MLP before the fast one: the static MLP of
     block 0 runs in the (hoisted) prefix, the later ones forward and backward
     between the fast MLPs; every storage type, Settlement and b = 1."""
@@ -332,7 +328,6 @@ def test_two_mlp_fast_blocks_against_the_oracle(monkeypatch, case):
         wl = C.CHUNKED_FP32.replace(d=72, d_ff=200, vocab=333, chunk=40, B=3, T=130, n_prefix=0,
                                     static_mlp=True)
     elif case == "bf16_hoisted":
-        monkeypatch.setenv("TTT_HOIST_CHUNKS", "2")
         wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1024, chunk=64, B=3, T=5 * 64, n_prefix=1,
                                 static_mlp=True, eta=0.3)
     elif case == "bf16_settle":
@@ -341,7 +336,7 @@ def test_two_mlp_fast_blocks_against_the_oracle(monkeypatch, case):
     else:
         wl = C.TOY_BIGRAM.replace(B=2, T=100, n_fast=2, static_mlp=True)
     inp = make(wl)
-    gpu = run_gpu(wl, inp)
+    gpu = run_gpu(wl, inp, options={"hoist_chunks": 2 if case == "bf16_hoisted" else 0})
     ref = run_oracle(wl, inp)
     # the Settlement case draws 4x larger weights (to make decisions decidable) through
     # seven bf16 MLPs: its next-token probabilities carry about twice the usual bf16 error
@@ -444,13 +439,11 @@ def test_sliding_window_attention_edge_cases(case):
 
 
 @pytest.mark.parametrize("case", ["fp32_split_graph", "fp32_split_launches", "fp32_rows", "bf16_swiglu"])
-def test_decoding_with_attention_against_the_oracle(monkeypatch, case):
+def test_decoding_with_attention_against_the_oracle(case):
     """Decoding after an attention prefill: each new input attends through the
     K/V cache to the window's inputs, prefill's included; the pending inputs'
     prefix rows feed the decoded chunk's step; token by token against the
     oracle across a step, captured graph and launch by launch."""
-    if case == "fp32_split_launches":
-        monkeypatch.setenv("TTT_DECODE_GRAPH", "0")
     if case.startswith("fp32_split"):
         wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=2 * 64 + 21, n_prefix=2,
                                     init_std=0.1, attn_heads=4, attn_window=96, eta=0.3)
@@ -464,7 +457,7 @@ def test_decoding_with_attention_against_the_oracle(monkeypatch, case):
     inp = _attention_inputs(wl)
     long_tok = synth.sample_stream(inp["chain"], wl.seed_id, wl.B, wl.T + extra)
     tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
-    gpu = run_gpu(wl, inp, tokens=tok)
+    gpu = run_gpu(wl, inp, tokens=tok, options={"no_decode_graph": case == "fp32_split_launches"})
     h = gpu["handle"]
     net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps, heads=wl.attn_heads,
                                   window=wl.attn_window)
@@ -520,18 +513,17 @@ def test_sequences_are_independent_on_gpu():
 
 
 @pytest.mark.parametrize("graph", ["1", "0"], ids=["graph", "launches"])
-def test_decode_completes_the_ragged_chunk_and_continues(monkeypatch, graph):
+def test_decode_completes_the_ragged_chunk_and_continues(graph):
     """Decoding after a prefill with a ragged tail: every step's loss and p_next
     against the oracle, through the captured next-token graph and launch by
     launch."""
-    monkeypatch.setenv("TTT_DECODE_GRAPH", graph)
     wl = C.CHUNKED_FP32.replace(d=64, d_ff=128, vocab=256, chunk=16, B=2, T=16 * 3 + 5, n_prefix=1)
     inp = make(wl)
     extra = 16 + 11 + 16
     chain = inp["chain"]
     long_tok = synth.sample_stream(chain, wl.seed_id, wl.B, wl.T + extra)
     tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
-    gpu = run_gpu(wl, inp, tokens=tok)
+    gpu = run_gpu(wl, inp, tokens=tok, options={"no_decode_graph": graph == "0"})
     h = gpu["handle"]
     net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
     ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)

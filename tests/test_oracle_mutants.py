@@ -77,6 +77,10 @@ MUTANTS = {
         "st.h_last = frozen_prefix(net, np.array(st.hist[-1:]))[-1]"),
     "decoded chunk recomputes its prefix rows without context": (
         "h_in=np.array(st.pend_h) if attn else None)", "h_in=None)"),
+    "weight error without its square root": ("return np.sqrt(num / den)", "return num / den"),
+    "weight error normalised by the first argument": (
+        "den += float(np.sum(np.asarray(b[k], np.float64) ** 2))",
+        "den += float(np.sum(np.asarray(a[k], np.float64) ** 2))"),
     "p_next with the initial weights": (
         "p_next = softmax_next(net, st.W, st.x_last, rows(T, T + 1))",
         "p_next = softmax_next(net, net.fast0, st.x_last, rows(T, T + 1))"),
@@ -115,6 +119,7 @@ PINS = [
     ("test_all_zeros_mask_never_updates_and_scores_like_eq4", ()),
     ("test_single_unmasked_target_is_that_tokens_own_gradient", ()),
     ("test_masked_chunk_gradient_matches_central_differences", ()),
+    ("test_weights_rel_frobenius_on_a_hand_computed_pair", ()),
 ]
 
 

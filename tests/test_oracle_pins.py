@@ -698,3 +698,20 @@ def test_decoding_with_attention_equals_a_longer_prefill(T):
     np.testing.assert_allclose(dec, long["losses"][0, T:], rtol=0, atol=1e-12)
     np.testing.assert_allclose(p, long["p_next"][0], rtol=0, atol=1e-12)
     assert O.weights_rel_frobenius(st.W, long["W"][0], net.fast_mats) < 1e-13
+
+
+def test_weights_rel_frobenius_on_a_hand_computed_pair():
+    """The parity tests' weight error ||Wa - Wb||_F / ||Wb||_F over every fast
+    matrix of one sequence, on integer matrices worked by hand:
+    block 0: W1 differs by one entry of 2, W2 by one entry of 1; block 1: W2
+    differs by one entry of 2.  Squared differences 4 + 1 + 0 + 4 = 9; squared
+    norms of Wb 26 + 4 + 4 + 4 = 38; so the error is 3 / sqrt(38).  Over W2
+    alone: 5 / 8 under the root.  A missing root, Wa's norm as the
+    denominator (43) or a block left out all change the value."""
+    Wa = [{"W1": np.array([[1.0, 2.0], [3.0, 4.0]]), "W2": np.array([[0.0, 1.0]])},
+          {"W1": np.array([[1.0, 1.0], [1.0, 1.0]]), "W2": np.array([[2.0, 2.0]])}]
+    Wb = [{"W1": np.array([[1.0, 0.0], [3.0, 4.0]]), "W2": np.array([[0.0, 2.0]])},
+          {"W1": np.array([[1.0, 1.0], [1.0, 1.0]]), "W2": np.array([[2.0, 0.0]])}]
+    assert abs(O.weights_rel_frobenius(Wa, Wb, ("W1", "W2")) - 3.0 / np.sqrt(38.0)) < 1e-15
+    assert abs(O.weights_rel_frobenius(Wa, Wb, ("W2",)) - np.sqrt(5.0 / 8.0)) < 1e-15
+    assert O.weights_rel_frobenius(Wb, Wb, ("W1", "W2")) == 0.0
