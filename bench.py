@@ -365,7 +365,7 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.set_device(dev)
     pk = peaks()
     inp = rank_inputs(wl, rank)
-    h = Handle.from_workload(wl, inp["weights"])
+    h = Handle.from_workload(wl, inp["weights"], options=args.options)
     storage = h.operand_storage()
     tok = torch.from_numpy(inp["tokens"]).to(dev)
     losses = torch.empty((wl.B, wl.T), dtype=torch.float32, device=dev)
@@ -588,10 +588,17 @@ def main():
                     help="write the kernel class of every launch of the first prefill to this file")
     ap.add_argument("--T", type=int, default=None,
                     help="tokens per sequence instead of the workload's (small cases for profiler captures)")
+    ap.add_argument("--B", type=int, default=None,
+                    help="sequences instead of the workload's (small cases for profiler captures)")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="a ttt_options field of the handle (e.g. hoist_chunks=2), for profiler captures")
     args = ap.parse_args()
     wl = C.BY_NAME[args.workload]
     if args.T is not None:
         wl = wl.replace(T=args.T)
+    if args.B is not None:
+        wl = wl.replace(B=args.B)
+    args.options = {k: int(v) for k, v in (o.split("=", 1) for o in args.option)}
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

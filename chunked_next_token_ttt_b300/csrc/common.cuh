@@ -100,6 +100,13 @@ template <> struct OpIO<Split> {
   }
 };
 
+// Element type of the dW output (the GEMM's EPI_DW epilogue): bf16 for bf16 operand storage (the
+// clipped update reads it once, and the fp32 master absorbs the step), fp32
+// for fp32-accurate storage.  The per-tile sums of squares always come from
+// the fp32 accumulators.
+template <typename S> struct DwType { using T = float; };
+template <> struct DwType<bf16> { using T = bf16; };
+
 // Four consecutive elements from a float4 in operand storage (16 / 8 / 2 x 8
 // bytes): the start index must keep the access aligned.
 template <typename S> struct QuadIO;
@@ -111,6 +118,23 @@ template <> struct QuadIO<float> {
 __device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
   const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
   return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+// Eight bf16 values in one 16-byte word, and back.
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  uint4 r;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+  return r;
+}
+__device__ __forceinline__ void unpack_bf16x8(uint4 r, float* v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = __bfloat1622float2(h[j]);
+    v[2 * j] = f.x;
+    v[2 * j + 1] = f.y;
+  }
 }
 template <> struct QuadIO<bf16> {
   __device__ __forceinline__ static void store(void* p, long long, long long i, float4 w) {

@@ -175,6 +175,11 @@ static ttt_status attention_decode(ttt_handle* h, int p, float* x32, const OpBuf
   return rungemm(h, K_GEMM_PREFIX, gw, st);
 }
 
+// Whether the attention of the frozen blocks runs as the one fused kernel.
+static bool attn_fused(const ttt_handle* h) {
+  return !h->opt.attn_unfused && swa_fused_supported(h->stg, h->d, h->dm.attn_heads);
+}
+
 // h += Attn(h) for prefix block p over B sequences of `rows` positions from 0:
 // x32 is the fp32 residual stream and cur its operand copy (both [B][rows][d]),
 // updated in place.  One GEMM projects to Q | K | V; fp32 storage then runs
@@ -222,7 +227,13 @@ static ttt_status attention_sublayer(ttt_handle* h, int p, int rows, float* x32,
     return launch_kv_fill(stg, B, rows, k, d, h->qkvp.p, h->qkvp.lo, g.L, g.pad, kv_k(h, p), kv_v(h, p), st);
   }));
   const long long q_row = g.j0 * g.Bq, k_row = g.j0 * g.Bq + g.Bq - g.nw;   // first block's query / window row
-  for (int hh = 0; hh < H; ++hh) {
+  if (attn_fused(h)) {
+    // every head in one launch; scores and probabilities stay on chip
+    TTT_TRY(run(h, K_ATTN, st, 1, [&] {
+      return launch_swa_fused(B, rows, H, dh, k, h->qkvp.p, (int)g.pad, g.L, h->att_p.p, h->flag, st);
+    }));
+  }
+  for (int hh = 0; hh < H && !attn_fused(h); ++hh) {
     GemmDesc gs;
     gs.M = g.Bq; gs.N = g.nw; gs.K = dh; gs.batch = (int)g.nb;
     setA(gs, op_at(h, h->qkvp, q_row * ld + (long long)hh * dh), ld, g.Bq * ld);
@@ -324,15 +335,19 @@ struct Hoisted {
 // head_f32: write fp32 logits into logits32 (rows must be 1) instead of the CE.
 // hz.on: the prefix output (and SwiGLU activation) of these rows is already in
 // the hoisted buffers; otherwise the embedding and the prefix run here.
+// delta: the current weights as the committed bf16 copy plus the bf16 offset
+// Wdel (two tensor-core products per fast-weight GEMM), for Settlement's score.
 static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, bool train,
                           float* losses, long long loss_ld, long long loss_off, bool head_f32,
-                          cudaStream_t st, const Hoisted& hz = Hoisted()) {
+                          cudaStream_t st, const Hoisted& hz = Hoisted(), bool delta = false) {
   TokView tv = tv_in;
   tv.vocab = h->V;
   tv.err = h->flag;
   const int B = h->B, rows = tv.rows, M = B * rows, d = h->d, f = h->f, V = h->V;
   const int stg = h->stg;
-  const OpBuf& Wop = committed ? h->Wcop : h->Wop;
+  const OpBuf& Wop = (committed || delta) ? h->Wcop : h->Wop;
+  // the second plane of a fast weight's operand when scoring with the offset
+  auto wdel = [&](int slot) -> const void* { return delta ? op_at(h, h->Wdel, (long long)slot * B * h->n).p : nullptr; };
   // inputs of fast block 0: its operand rows, their batch stride, the fp32 residual
   OpBuf hin0 = h->hlvl[0];
   long long hin0_s = (long long)rows * d;
@@ -388,6 +403,7 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
       g.M = rows; g.N = f; g.K = d; g.batch = B;
       setA(g, hin, d, hin_s);
       setB(g, op_at(h, Wop, (long long)s_up * B * h->n), d, h->n);
+      g.B2 = wdel(s_up);
       g.epi = EPI_GELU;
       if (train) setOut(g, h->zst[l], f, (long long)rows * f);
       else g.out = nullptr;
@@ -415,6 +431,7 @@ static ttt_status forward(ttt_handle* h, const TokView& tv_in, bool committed, b
     g2.M = rows; g2.N = d; g2.K = f; g2.batch = B;
     setA(g2, a_out, f, a_s);
     setB(g2, op_at(h, Wop, (long long)s_down * B * h->n), f, h->n);
+    g2.B2 = wdel(s_down);
     g2.epi = EPI_RESID;
     g2.aux = l == 0 ? x0 : h->x32; g2.ldx = d; g2.sX = l == 0 ? (hz.on ? hz.rows_total * d : (long long)rows * d)
                                                                : (long long)rows * d;
@@ -487,6 +504,17 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
 
   PartialSlots ps{};
   long long poff = 0;
+  // GELU blocks without static MLPs run each weight gradient on the handle's
+  // second stream beside the input-gradient chain (dW2 of block l needs only
+  // dh and the a stash, dW1 only dz and the block input), so each dW GEMM fills
+  // the tail waves of its dX partner.  The operand copy of dh alternates between
+  // two buffers, so the chain never rewrites a dh that a dW still reads.
+  // (profiled steps keep the dW GEMMs in stream order: each class's events then
+  // bracket its own kernels only)
+  const bool side = h->bstream != nullptr && h->prof_class < 0;
+  cudaStream_t ws = side ? h->bstream : st;   // stream of the dW GEMMs
+  const int nf = h->dm.n_fast;
+  auto dh_buf = [&](int l) -> const OpBuf& { return side && (nf - 1 - l) % 2 ? h->dhop2 : h->dhop; };
   auto dw_gemm = [&](GemmDesc& g, int slot) -> ttt_status {
     g.epi = EPI_DW;
     g.dtype = h->stg;
@@ -494,32 +522,45 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
     const int tiles = gemm_partial_tiles(g);
     if (ps.n >= 16 || poff + (long long)tiles * B > h->partial_cap)
       return fail(TTT_ERR_UNSUPPORTED, "too many gradient-norm partial slots");
-    g.out = h->dW + (long long)slot * B * h->n; g.sO = h->n;
+    g.out = static_cast<char*>(h->dW) + (long long)slot * B * h->n * (long long)h->dw_esz; g.sO = h->n;
     ps.off[ps.n] = poff;
     ps.tiles[ps.n] = tiles;
     ps.n++;
     poff += (long long)tiles * B;
-    return rungemm(h, K_GEMM_DW, g, st);
+    return rungemm(h, K_GEMM_DW, g, ws);
   };
+  // events of the second stream: [0, nf) dh of block l ready, [nf, 2 nf) dz of
+  // block l ready, [2 nf, 3 nf) dW2 of block l done, 3 nf: every dW done
+  auto ev = [&](int kind, int l) { return h->bev[(size_t)kind * nf + l]; };
 
-  for (int l = h->dm.n_fast - 1; l >= 0; --l) {
+  for (int l = nf - 1; l >= 0; --l) {
     if (h->dm.block_kind == TTT_BLOCK_GELU) {
       const int s1 = h->slot_of[(size_t)l * 2 + 0], s2 = h->slot_of[(size_t)l * 2 + 1];
+      const OpBuf& dh = dh_buf(l);
+      if (side) {
+        TTT_CUDA(cudaEventRecord(ev(0, l), st));
+        TTT_CUDA(cudaStreamWaitEvent(ws, ev(0, l), 0));
+      }
       // dW2 = dh^T a   [d, f], K = rows
       GemmDesc g;
       g.M = d; g.N = f; g.K = rows; g.batch = B;
-      g.a_kmajor = false; setA(g, h->dhop, d, (long long)rows * d);
+      g.a_kmajor = false; setA(g, dh, d, (long long)rows * d);
       g.b_kmajor = false; setB(g, h->ast[l], f, (long long)rows * f);
       g.ldo = f;
       TTT_TRY(dw_gemm(g, s2));
+      if (side) TTT_CUDA(cudaEventRecord(ev(2, l), ws));
       // dz = (dh W2) * GELU'(z), in place over the z stash
       GemmDesc gz;
       gz.M = rows; gz.N = f; gz.K = d; gz.batch = B;
-      setA(gz, h->dhop, d, (long long)rows * d);
+      setA(gz, dh, d, (long long)rows * d);
       gz.b_kmajor = false; setB(gz, op_at(h, h->Wop, (long long)s2 * B * h->n), f, h->n);
       gz.epi = EPI_DGELU; gz.aux = h->zst[l].p; gz.loX = h->zst[l].lo; gz.ldx = f; gz.sX = (long long)rows * f;
       setOut(gz, h->zst[l], f, (long long)rows * f);
       TTT_TRY(rungemm(h, K_GEMM_BWD_DX, gz, st));
+      if (side) {
+        TTT_CUDA(cudaEventRecord(ev(1, l), st));
+        TTT_CUDA(cudaStreamWaitEvent(ws, ev(1, l), 0));
+      }
       // dW1 = dz^T h_in   [f, d]
       GemmDesc g1;
       g1.M = f; g1.N = d; g1.K = rows; g1.batch = B;
@@ -529,14 +570,16 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
       g1.ldo = d;
       TTT_TRY(dw_gemm(g1, s1));
       if (l > 0) {
-        // dh_below = dh + dz W1
+        // dh_below = dh + dz W1, its operand copy into the other dh buffer,
+        // which dW2 of block l + 1 (two levels up) read last
+        if (side && l + 1 < nf) TTT_CUDA(cudaStreamWaitEvent(st, ev(2, l + 1), 0));
         GemmDesc gb;
         gb.M = rows; gb.N = d; gb.K = f; gb.batch = B;
         setA(gb, h->zst[l], f, (long long)rows * f);
         gb.b_kmajor = false; setB(gb, op_at(h, h->Wop, (long long)s1 * B * h->n), d, h->n);
         gb.epi = EPI_RESID; gb.aux = h->dh32; gb.ldx = d; gb.sX = (long long)rows * d;
         gb.out = h->dh32; gb.ldo = d; gb.sO = (long long)rows * d;
-        setOut2(gb, h->dhop, d, (long long)rows * d);
+        setOut2(gb, dh_buf(l - 1), d, (long long)rows * d);
         TTT_TRY(rungemm(h, K_GEMM_BWD_DX, gb, st));
         if (h->dm.static_mlp) {
           // through the block's frozen MLP: dz_s = (dh W2s) * GELU'(z_s); dh += dz_s W1s
@@ -567,6 +610,11 @@ static ttt_status backward_update(ttt_handle* h, int rows, cudaStream_t st) {
       g.ldo = f;
       TTT_TRY(dw_gemm(g, sd));
     }
+  }
+  if (side) {
+    // the update reads every dW: join the second stream
+    TTT_CUDA(cudaEventRecord(h->bev[(size_t)3 * nf], ws));
+    TTT_CUDA(cudaStreamWaitEvent(st, h->bev[(size_t)3 * nf], 0));
   }
   // the per-sequence norm is reduced inside the update kernel (grad_norm has no launch of its own)
   TTT_TRY(run(h, K_SGD, st, 1, [&] {
@@ -633,7 +681,16 @@ static ttt_status settle_event(ttt_handle* h, const int32_t* q, int Lq, float* A
   }
   TTT_TRY(forward(h, tv, true, false, nullptr, 0, 0, false, st, hz));
   TTT_TRY(run(h, K_SETTLE, st, 1, [&] { return launch_seq_mean(h->B, Lq, Lq - 1, h->row_loss, h->Lc, st); }));
-  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, false, st, hz));
+  // bf16 storage scores the candidate as the committed bf16 copy plus its
+  // offset in bf16: both losses then round the weights alike, so A sees the
+  // whole update (a bf16 copy of W alone would round most of an update below
+  // half an ulp away, and W_0 starts on the bf16 grid)
+  const bool delta = h->Wdel.p != nullptr;
+  if (delta)
+    TTT_TRY(run(h, K_SETTLE, st, 1, [&] {
+      return launch_delta_plane(h->nslots, h->B, h->n, h->W32, h->Wc32, h->Wdel.p, st);
+    }));
+  TTT_TRY(forward(h, tv, false, false, nullptr, 0, 0, false, st, hz, delta));
   TTT_TRY(run(h, K_SETTLE, st, 1, [&] { return launch_seq_mean(h->B, Lq, Lq - 1, h->row_loss, h->Lw, st); }));
   return run(h, K_SETTLE, st, 2, [&] {
     return launch_settle_apply(h->stg, h->nslots, h->B, h->n, h->Lc, h->Lw, A, acc, h->W32, h->Wop.p,
@@ -803,6 +860,7 @@ static ttt_status ensure_attn_tc(ttt_handle* h, long long R) {
   // zero once: rows the projections never write (the padding) must hold finite values
   TTT_TRY(ensure_op_elems(h, &h->qkvp, &h->qkvp_cap, (size_t)h->B * g.L * 3 * d, true));
   TTT_TRY(ensure_op_elems(h, &h->att_p, &h->attp_cap, (size_t)h->B * g.L * d, false));
+  if (attn_fused(h)) return TTT_OK;    // scores and probabilities stay on chip
   const size_t blk = (size_t)g.nb * g.Bq * g.nw;
   size_t pp_cap = h->sc_cap;
   if (blk > h->sc_cap) {
@@ -931,6 +989,9 @@ ttt_status ttt_destroy(ttt_handle* h) {
   for (auto e : h->gev)
     if (e) cudaEventDestroy(e);
   if (h->gstream) cudaStreamDestroy(h->gstream);
+  for (auto e : h->bev)
+    if (e) cudaEventDestroy(e);
+  if (h->bstream) cudaStreamDestroy(h->bstream);
   if (h->flag_host) cudaFreeHost(h->flag_host);
   delete h;
   return TTT_OK;
@@ -946,7 +1007,7 @@ ttt_status ttt_create_ex(const ttt_dims* dims, const ttt_hparams* hp, const ttt_
   *out = nullptr;
   const ttt_options O = opt ? *opt : ttt_options{};
   if (O.no_pdl < 0 || O.no_decode_graph < 0 || O.fp32_simt < 0 || O.hoist_chunks < 0 || O.no_token_kernel < 0 ||
-      O.max_ctas < 0)
+      O.max_ctas < 0 || O.no_dw_stream < 0 || O.attn_unfused < 0)
     return fail(TTT_ERR_BAD_ARG, "negative ttt_options field");
   PdlScope pdl(!O.no_pdl);
   const ttt_dims& D = *dims;
@@ -1085,10 +1146,16 @@ ttt_status ttt_create_ex(const ttt_dims* dims, const ttt_hparams* hp, const ttt_
   const size_t arena = (size_t)h->nslots * B * h->n;
   if ((s = dalloc(h, &h->W32, arena * 4)) != TTT_OK) return bail(s);
   if ((s = op_alloc(&h->Wop, arena)) != TTT_OK) return bail(s);
-  if ((s = dalloc(h, &h->dW, arena * 4)) != TTT_OK) return bail(s);
+  h->dw_esz = h->stg == ST_BF16 ? 2 : 4;
+  if ((s = dalloc(h, &h->dW, arena * h->dw_esz)) != TTT_OK) return bail(s);
   // the committed copy serves Settlement (prefill events and ttt_settle)
   if ((s = dalloc(h, &h->Wc32, arena * 4)) != TTT_OK) return bail(s);
   if ((s = op_alloc(&h->Wcop, arena)) != TTT_OK) return bail(s);
+  // the candidate's bf16 offset for Settlement's score, when its fast-weight
+  // GEMMs fit the tensor-core kernel (every row block and width >= 64, widths
+  // multiples of 8); otherwise the candidate is scored from its own bf16 copy
+  if (h->stg == ST_BF16 && hp->settle_len >= 64 && D.d >= 64 && D.d_ff >= 64 && D.d % 8 == 0 && D.d_ff % 8 == 0)
+    if ((s = op_alloc(&h->Wdel, arena)) != TTT_OK) return bail(s);
 
   // ---- workspace
   int rows_max = h->b;
@@ -1161,6 +1228,20 @@ ttt_status ttt_create_ex(const ttt_dims* dims, const ttt_hparams* hp, const ttt_
   if ((s = dalloc(h, &h->dy32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = dalloc(h, &h->dh32, Mm * d * 4)) != TTT_OK) return bail(s);
   if ((s = op_alloc(&h->dhop, Mm * d)) != TTT_OK) return bail(s);
+  if (D.block_kind == TTT_BLOCK_GELU && !D.static_mlp && !O.no_dw_stream) {
+    if ((s = op_alloc(&h->dhop2, Mm * d)) != TTT_OK) return bail(s);
+    cudaError_t ce = cudaStreamCreateWithFlags(&h->bstream, cudaStreamNonBlocking);
+    if (ce != cudaSuccess) {
+      h->bstream = nullptr;
+      return bail(cuda_fail(ce, "cudaStreamCreateWithFlags", __FILE__, __LINE__));
+    }
+    h->bev.assign((size_t)3 * D.n_fast + 1, nullptr);
+    for (auto& e : h->bev)
+      if ((ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming)) != cudaSuccess) {
+        e = nullptr;
+        return bail(cuda_fail(ce, "cudaEventCreateWithFlags", __FILE__, __LINE__));
+      }
+  }
   // split-K workspace: up to 8 fp32 partial slices of a [Mmax, d] output, at most 64 MB
   // split-K partial tiles (fp32): the planner splits only while they fit (256 MB)
   h->gemm_ws_elems = 64LL << 20;

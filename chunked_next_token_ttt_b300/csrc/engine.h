@@ -73,7 +73,11 @@ struct ttt_handle {
   OpBuf Wop;
   float* Wc32 = nullptr;
   OpBuf Wcop;
-  float* dW = nullptr;
+  // bf16 storage with Settlement: bf16(W32 - Wc32), the candidate's offset from
+  // the committed copy (Settlement scores W as Wcop + Wdel)
+  OpBuf Wdel;
+  void* dW = nullptr;      // [slot][B][n] gradients: bf16 for ST_BF16, fp32 otherwise
+  size_t dw_esz = 4;       // bytes per dW element
 
   // chunk workspace for up to Mmax rows
   int Mmax = 0;
@@ -110,6 +114,12 @@ struct ttt_handle {
   float* dy32 = nullptr;
   float* dh32 = nullptr;
   OpBuf dhop;
+  // weight gradients beside the input-gradient chain (GELU blocks without
+  // static MLPs): the second stream, its fork/join events and the second
+  // operand-copy buffer of dh
+  cudaStream_t bstream = nullptr;
+  std::vector<cudaEvent_t> bev;
+  OpBuf dhop2;
   float* gemm_ws = nullptr;          // split-K partial products
   long long gemm_ws_elems = 0;
   int* split_cnt = nullptr;          // split-K arrival counters (zero between GEMMs)

@@ -40,7 +40,7 @@ __device__ __forceinline__ float epi_value(const GemmDesc& g, int bz, int m, int
       break;
     }
     case EPI_DW:
-      static_cast<float*>(g.out)[bz * g.sO + (long long)m * g.ldo + n] = acc;
+      OpIO<typename DwType<S>::T>::store(g.out, 0, bz * g.sO + (long long)m * g.ldo + n, acc);
       return acc * acc;
   }
   return 0.0f;
@@ -75,7 +75,7 @@ __device__ __forceinline__ float epi_pair(const GemmDesc& g, int bz, int m, int 
     const float2 z = P::load(g.aux, g.loX, bz * g.sX + (long long)m * g.ldx + n);
     P::store(g.out, g.loO, bz * g.sO + (long long)m * g.ldo + n, a0 * gelu_grad_f(z.x), a1 * gelu_grad_f(z.y));
   } else if (ek == EPI_DW) {
-    PairIO<float>::store(g.out, 0, bz * g.sO + (long long)m * g.ldo + n, a0, a1);
+    PairIO<typename DwType<S>::T>::store(g.out, 0, bz * g.sO + (long long)m * g.ldo + n, a0, a1);
     return a0 * a0 + a1 * a1;
   }
   return 0.0f;
@@ -101,22 +101,6 @@ template <> struct OctIO<float> {
     q[1] = make_float4(v[4], v[5], v[6], v[7]);
   }
 };
-__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
-  uint4 r;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-  return r;
-}
-__device__ __forceinline__ void unpack_bf16x8(uint4 r, float* v) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 f = __bfloat1622float2(h[j]);
-    v[2 * j] = f.x;
-    v[2 * j + 1] = f.y;
-  }
-}
 template <> struct OctIO<bf16> {
   __device__ __forceinline__ static void load(const void* p, long long, long long i, float* v) {
     unpack_bf16x8(*reinterpret_cast<const uint4*>(static_cast<const bf16*>(p) + i), v);
@@ -182,7 +166,7 @@ __device__ __forceinline__ float epi_oct(const GemmDesc& g, int bz, int m, int n
     for (int j = 0; j < 8; ++j) t[j] = a[j] * gelu_grad_f(t[j]);
     O::store(g.out, g.loO, io, t);
   } else if (ek == EPI_DW) {
-    OctIO<float>::store(g.out, 0, io, a);
+    OctIO<typename DwType<S>::T>::store(g.out, 0, io, a);
     float s = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) s += a[j] * a[j];
@@ -321,7 +305,7 @@ __device__ __forceinline__ float epi_hex(const GemmDesc& g, int bz, int m, int n
     for (int j = 0; j < 16; ++j) t[j] = a[j] * gelu_grad_f(t[j]);
     O::store(g.out, g.loO, io, t);
   } else if (ek == EPI_DW) {
-    HexIO<float>::store(g.out, 0, io, a);
+    HexIO<typename DwType<S>::T>::store(g.out, 0, io, a);
     float s = 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j) s += a[j] * a[j];

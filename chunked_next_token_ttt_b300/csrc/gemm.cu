@@ -8,6 +8,7 @@ namespace ttt {
 enum Route { ROUTE_SIMT, ROUTE_TC, ROUTE_SMALL };
 
 static Route route(const GemmDesc& g) {
+  if (g.B2) return ROUTE_TC;
   if (g.impl == 1) return ROUTE_SIMT;
   if (g.impl == 2 || g.epi == EPI_LOGITS) return ROUTE_TC;
   if (gemm_small_supported(g)) return ROUTE_SMALL;
@@ -26,6 +27,10 @@ int gemm_partial_tiles(const GemmDesc& g) {
 int gemm_launches(const GemmDesc&) { return 1; }
 
 ttt_status gemm(const GemmDesc& g, cudaStream_t st) {
+  if (g.B2 && !gemm_tc_supported(g)) {
+    set_error("a two-plane B operand runs on the tensor-core GEMM only");
+    return TTT_ERR_UNSUPPORTED;
+  }
   if (g.epi == EPI_LOGITS && route(g) != ROUTE_TC) {
     set_error("the fused logits epilogue runs on the tensor-core GEMM only");
     return TTT_ERR_UNSUPPORTED;

@@ -13,7 +13,8 @@ enum EpiKind {
   EPI_RESID,       // out(float) = aux(float) + acc; out2(op) = same, if non-null
   EPI_SWIGLU,      // out(op) = silu(aux(float)) * acc
   EPI_DGELU,       // out(op) = acc * GELU'(aux(op))
-  EPI_DW,          // out(float) = acc; partials += per-tile sum of acc^2
+  EPI_DW,          // out = acc (bf16 for bf16 storage, float otherwise);
+                   // partials += per-tile sum of acc^2 (fp32 accumulators)
   EPI_LOGITS,      // tensor-core path only, batch 1: out(bf16) = acc when out is
                    // non-null; lse_part[m][tile] = (max, sum exp(acc - max)) over the
                    // tile's columns
@@ -26,6 +27,9 @@ struct GemmDesc {
   bool b_kmajor = true;            // B(n,k) at B[n*ldb + k] (else B[k*ldb + n])
   const void* A = nullptr; long long lda = 0, sA = 0;   // strides in elements
   const void* B = nullptr; long long ldb = 0, sB = 0;
+  // bf16 storage only: B is the sum of two bf16 planes, B and B2 (same leading
+  // dim and batch stride), taken as two tensor-core products
+  const void* B2 = nullptr;
   EpiKind epi = EPI_STORE;
   void* out = nullptr; long long ldo = 0, sO = 0;
   void* out2 = nullptr; long long ldo2 = 0, sO2 = 0;

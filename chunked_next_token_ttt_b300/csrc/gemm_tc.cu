@@ -73,6 +73,9 @@ bool gemm_tc_supported(const GemmDesc& g) {
   if (g.lda % 8 || g.ldb % 8) return false;
   if (g.batch > 1 && (g.sA % 8 || g.sB % 8 || g.sA <= 0 || g.sB <= 0)) return false;
   if (g.epi == EPI_DW && !g.partials) return false;
+  if (g.B2 && (g.dtype != ST_BF16 || !aligned16(g.B2) || !g.a_kmajor || !g.b_kmajor ||
+               (g.epi != EPI_GELU && g.epi != EPI_RESID)))
+    return false;
   if (g.epi == EPI_LOGITS &&
       (g.dtype != ST_BF16 || g.batch != 1 || !g.a_kmajor || !g.b_kmajor || !g.lse_part ||
        g.lse_ld < ceil_div(g.N, choose_bn(g))))
@@ -101,7 +104,7 @@ static TcPlan plan(const GemmDesc& g) {
   const int nkb = ceil_div(g.K, tc::BK);
   const bool can_split = g.ws && g.cnt && g.epi != EPI_DW && g.epi != EPI_LOGITS && !(g.N & 1) && nkb >= 8;
   for (int bn : {256, 128}) {
-    if (bn == 256 && g.dtype != ST_BF16) continue;
+    if (bn == 256 && (g.dtype != ST_BF16 || g.B2)) continue;
     const long long tiles = (long long)ceil_div(g.N, bn) * ceil_div(g.M, tc::BM) * g.batch;
     const double kslice = bn == 256 ? 1.21 : 1.0;
     const double fix = bn == 256 ? 2.0 : 1.0;
@@ -157,7 +160,8 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
   // MN-major [batch][K][M] panels {64, 64}.  Likewise B with BN rows.
   CUtensorMap maps[4];
   const bf16* planesA[2] = {static_cast<const bf16*>(g.A), static_cast<const bf16*>(g.A) + (split ? g.loA : 0)};
-  const bf16* planesB[2] = {static_cast<const bf16*>(g.B), static_cast<const bf16*>(g.B) + (split ? g.loB : 0)};
+  const bf16* planesB[2] = {static_cast<const bf16*>(g.B),
+                            g.B2 ? static_cast<const bf16*>(g.B2) : static_cast<const bf16*>(g.B) + (split ? g.loB : 0)};
   for (int p = 0; p < 2; ++p) {
     if (!a_mn) TTT_TRY(tc::make_map(&maps[2 * p], planesA[p], g.K, g.M, g.batch, g.lda, g.sA, tc::BK, tc::BM));
     else TTT_TRY(tc::make_map(&maps[2 * p], planesA[p], g.M, g.K, g.batch, g.lda, g.sA, tc::PANEL, tc::BK));
@@ -184,6 +188,7 @@ ttt_status gemm_tc(const GemmDesc& g, cudaStream_t st) {
       return TTT_ERR_UNSUPPORTED;
     }
   }
+  if (g.B2) return tc::launch_kk_b2(gd, maps, nkb, splitk, st);
   if (!a_mn && !b_mn) return tc::launch_kk(gd, maps, nkb, splitk, st);
   if (!a_mn) return tc::launch_km(gd, maps, nkb, splitk, st);
   if (!b_mn) return tc::launch_mk(gd, maps, nkb, splitk, st);

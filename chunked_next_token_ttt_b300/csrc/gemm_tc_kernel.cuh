@@ -194,12 +194,19 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   return r != 0;
 }
 
-template <int BN, bool SPLIT>
+// Operand planes of a GEMM: PL_ONE bf16 A and B (one product); PL_SPLIT
+// fp32-accurate A and B as bf16 hi/lo pairs (three products: hi*hi, hi*lo,
+// lo*hi); PL_B2 bf16 A and a B given as the sum of two bf16 planes (two
+// products, A*B0 + A*B1).
+constexpr int PL_ONE = 0, PL_SPLIT = 1, PL_B2 = 2;
+
+template <int BN, int PL>
 struct Smem {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int NPL = SPLIT ? 2 : 1;                  // planes per operand
-  static constexpr int STAGE_BYTES = NPL * (A_BYTES + B_BYTES);
+  static constexpr int NA = PL == PL_SPLIT ? 2 : 1;          // planes of A
+  static constexpr int NB = PL == PL_ONE ? 1 : 2;            // planes of B
+  static constexpr int STAGE_BYTES = NA * A_BYTES + NB * B_BYTES;
   static constexpr int STAGING = 2 * (NUM_EPI_WARPS / 4) * BM * 4;  // per-row softmax states of EPI_LOGITS
   static constexpr int MAX_DYN = 232448;                     // per-block opt-in limit
   static constexpr int OVERHEAD = 1024 + 512;                // base alignment + barriers
@@ -236,12 +243,12 @@ __device__ __forceinline__ Unit decode_unit(int u, int mtiles, int ntiles, int b
   return w;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, int EK>
+template <int BN, bool A_MN, bool B_MN, int PL, int EK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                    const GemmDesc g, int nkb, int splitk, int mtiles, int ntiles, int* err) {
-  using L = Smem<BN, SPLIT>;
+  using L = Smem<BN, PL>;
   constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -299,21 +306,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         uint8_t* sa = smem + s * L::STAGE_BYTES;
-        uint8_t* sb = sa + L::NPL * L::A_BYTES;
+        uint8_t* sb = sa + L::NA * L::A_BYTES;
         mbar_expect_tx(&full[s], L::STAGE_BYTES);
         const int k0 = (kb_lo + kb) * BK;
 #pragma unroll
-        for (int p = 0; p < L::NPL; ++p) {
+        for (int p = 0; p < L::NA; ++p) {
           const CUtensorMap* ma = p ? &tmA2 : &tmA;
-          const CUtensorMap* mb = p ? &tmB2 : &tmB;
           uint8_t* da = sa + p * L::A_BYTES;
-          uint8_t* db = sb + p * L::B_BYTES;
           if (!A_MN) {
             tma_load_3d(da, ma, &full[s], k0, w.m0, w.bz);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / PANEL; ++j) tma_load_3d(da + j * PANEL * BK * 2, ma, &full[s], w.m0 + j * PANEL, k0, w.bz);
           }
+        }
+#pragma unroll
+        for (int p = 0; p < L::NB; ++p) {
+          const CUtensorMap* mb = p ? &tmB2 : &tmB;
+          uint8_t* db = sb + p * L::B_BYTES;
           if (!B_MN) {
             tma_load_3d(db, mb, &full[s], k0, w.n0, w.bz);
           } else {
@@ -345,10 +355,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + s * L::STAGE_BYTES);
-        const uint32_t sb = sa + L::NPL * L::A_BYTES;
+        const uint32_t sb = sa + L::NA * L::A_BYTES;
+        constexpr int NPROD = PL == PL_SPLIT ? 3 : (PL == PL_B2 ? 2 : 1);
 #pragma unroll
-        for (int t = 0; t < (SPLIT ? 3 : 1); ++t) {
-          // split products: hi*hi, hi*lo, lo*hi
+        for (int t = 0; t < NPROD; ++t) {
+          // split products: hi*hi, hi*lo, lo*hi; two-plane B: A*B0, A*B1
           const uint32_t pa = sa + (t == 2 ? L::A_BYTES : 0);
           const uint32_t pb = sb + (t == 1 ? L::B_BYTES : 0);
 #pragma unroll
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue
-    using S = typename std::conditional<SPLIT, Split, bf16>::type;
+    using S = typename std::conditional<PL == PL_SPLIT, Split, bf16>::type;
     constexpr int HALVES = NUM_EPI_WARPS / 4;   // warps per TMEM lane quadrant
     constexpr int GPW = BN / kCols / HALVES;    // 64-column groups per thread
     static_assert(GPW >= 1 && GPW * kCols * HALVES == BN, "tile width not covered by the epilogue warps");
@@ -579,11 +590,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// Host helpers (gemm_tc.cu): the driver's tensor-map encoder, and a 3-D bf16
+// tensor map over X[batch][outer][inner] (leading dim ld, batch stride sz, in
+// elements) with 128B swizzle and a box of box_inner x box_outer elements.
+ttt_status init_driver();
+ttt_status make_map(CUtensorMap* m, const void* base, long long inner, long long outer, int batch, long long ld,
+                    long long sz, int box_inner, int box_outer);
+
 // Launch one instantiation (persistent grid, one CTA per SM at most).
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, int EK>
+template <int BN, bool A_MN, bool B_MN, int PL, int EK>
 ttt_status launch_bn(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
-  using L = Smem<BN, SPLIT>;
-  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, SPLIT, EK>;
+  using L = Smem<BN, PL>;
+  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, PL, EK>;
   TTT_CUDA(ensure_dyn_smem((const void*)kern, L::ALLOC));
   const int mtiles = ceil_div(g.M, BM), ntiles = ceil_div(g.N, BN);
   const long long units = (long long)mtiles * ntiles * g.batch * splitk;
@@ -601,10 +619,14 @@ ttt_status launch_bn(const GemmDesc& g, const CUtensorMap* maps, int nkb, int sp
 template <bool A_MN, bool B_MN, bool SPLIT, int EK>
 ttt_status launch_kernel(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
   if constexpr (!SPLIT) {
-    if (g.bn == 256) return launch_bn<256, A_MN, B_MN, false, EK>(g, maps, nkb, splitk, st);
+    if (g.bn == 256) return launch_bn<256, A_MN, B_MN, PL_ONE, EK>(g, maps, nkb, splitk, st);
   }
-  return launch_bn<kBN, A_MN, B_MN, SPLIT, EK>(g, maps, nkb, splitk, st);
+  return launch_bn<kBN, A_MN, B_MN, SPLIT ? PL_SPLIT : PL_ONE, EK>(g, maps, nkb, splitk, st);
 }
+
+// Two-plane B (GemmDesc::B2), K-major operands, 128-wide tiles: the fast-block
+// forward products that score Settlement's candidate weights.
+ttt_status launch_kk_b2(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st);
 
 // Per operand-major combination: picks the instantiation for (storage, epilogue).
 ttt_status launch_kk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st);

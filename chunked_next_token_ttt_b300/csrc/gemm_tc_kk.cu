@@ -22,6 +22,16 @@ static ttt_status dispatch_kk(const GemmDesc& g, const CUtensorMap* maps, int nk
   }
 }
 
+ttt_status launch_kk_b2(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
+  switch (g.epi) {
+    case EPI_GELU: return launch_bn<kBN, false, false, PL_B2, EPI_GELU>(g, maps, nkb, splitk, st);
+    case EPI_RESID: return launch_bn<kBN, false, false, PL_B2, EPI_RESID>(g, maps, nkb, splitk, st);
+    default:
+      set_error("a two-plane B operand runs with the GELU or residual epilogue");
+      return TTT_ERR_UNSUPPORTED;
+  }
+}
+
 ttt_status launch_kk(const GemmDesc& g, const CUtensorMap* maps, int nkb, int splitk, cudaStream_t st) {
   return g.dtype == ST_SPLIT ? dispatch_kk<true>(g, maps, nkb, splitk, st)
                              : dispatch_kk<false>(g, maps, nkb, splitk, st);

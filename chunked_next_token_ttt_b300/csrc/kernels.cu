@@ -4,6 +4,8 @@
 // the Settlement helpers.  All are HBM-bound row or elementwise kernels.
 #include <cfloat>
 
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace ttt {
@@ -225,7 +227,18 @@ __global__ void lse_combine_kernel(TokView tv, int M, const float2* __restrict__
   if (t >= 0) {
     const bf16* yr = y + (long long)m * d;
     const bf16* ur = U + (long long)t * d;
-    for (int k = lane; k < d; k += 32) dot = fmaf(__bfloat162float(yr[k]), __bfloat162float(ur[k]), dot);
+    if ((d & 7) == 0) {
+      // eight products per lane per step from 16-byte loads (rows are 16-byte aligned when d % 8 == 0)
+      for (int k = lane * 8; k < d; k += 256) {
+        float a[8], b[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(yr + k), a);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(ur + k), b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dot = fmaf(a[j], b[j], dot);
+      }
+    } else {
+      for (int k = lane; k < d; k += 32) dot = fmaf(__bfloat162float(yr[k]), __bfloat162float(ur[k]), dot);
+    }
     dot = warp_sum(dot);
   }
   float mx = -FLT_MAX, se = 0.0f;
@@ -272,6 +285,8 @@ __global__ void chunk_row_scale_kernel(int rows, const uint8_t* __restrict__ mas
 // scale is folded into the exponent, exp(x - (lse - ln scale)), and the one
 // target element of a row is corrected on its own.  Grid: x over the row's
 // 16-byte vectors, y over rows.
+constexpr int kDlVec = 4;   // 16-byte vectors per thread, all loaded before any is rewritten
+
 __global__ void dlogits_kernel(int M, int V, bf16* __restrict__ logits, const float* __restrict__ lse,
                                const int32_t* __restrict__ tgt, float scale, const float* __restrict__ rscale) {
   pdl_wait();
@@ -282,12 +297,22 @@ __global__ void dlogits_kernel(int M, int V, bf16* __restrict__ logits, const fl
     const float sc = rscale ? rscale[m] : scale;
     const int t = sc > 0.0f ? tgt[m] : -1;   // a zero scale (masked row) writes zeros
     const float l = lse[m] - logf(sc > 0.0f ? sc : 1.0f);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
+    const int i0 = blockIdx.x * blockDim.x * kDlVec + threadIdx.x;
+    uint4 buf[kDlVec];
+#pragma unroll
+    for (int u = 0; u < kDlVec; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (t >= 0 && i < nv) buf[u] = row[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kDlVec; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i >= nv) continue;
       if (t < 0) {
         row[i] = make_uint4(0u, 0u, 0u, 0u);
         continue;
       }
-      uint4 raw = row[i];
+      uint4 raw = buf[u];
       __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
       const int c = i * 8;
       float tx = 0.0f;
@@ -366,9 +391,20 @@ __device__ __forceinline__ float seq_clip_scale(const PartialSlots& ps, const fl
 // hundred to a few thousand floats, from L2), then W32 -= eta * s * dW and the
 // operand copy is re-cast.  float4 accesses when n is a multiple of 4 (every
 // fast matrix: n = d * d_ff).
+// Four dW values from 16-byte-aligned fp32 or 8-byte-aligned bf16 storage.
+__device__ __forceinline__ float4 load_dw4(const float* p, long long i) {
+  return *reinterpret_cast<const float4*>(p + i);
+}
+__device__ __forceinline__ float4 load_dw4(const bf16* p, long long i) {
+  const uint2 r = *reinterpret_cast<const uint2*>(p + i);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 template <typename S>
 __global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, void* Wop, long long wop_lo,
-                                  const float* __restrict__ dW, PartialSlots ps, const float* __restrict__ partials,
+                                  const void* dW_raw, PartialSlots ps, const float* __restrict__ partials,
                                   float clip, float eta, float* __restrict__ scale_out, float* __restrict__ norm_out,
                                   int* __restrict__ flag) {
   pdl_wait();
@@ -387,36 +423,49 @@ __global__ void sgd_update_kernel(int B, long long n, float* __restrict__ W32, v
   const float step = eta * sc;
   const long long base = (long long)blockIdx.y * n;
   const long long stride = (long long)gridDim.x * blockDim.x;
+  // dW in the epilogue's storage (bf16 for bf16 operands, fp32 otherwise)
+  using DT = typename DwType<S>::T;
+  const DT* dW = static_cast<const DT*>(dW_raw);
   if ((n & 3) == 0 && (wop_lo & 3) == 0) {
     float4* w4 = reinterpret_cast<float4*>(W32 + base);
-    const float4* g4 = reinterpret_cast<const float4*>(dW + base);
     for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n / 4; q += stride) {
       float4 w = w4[q];
-      const float4 gr = g4[q];
+      const float4 gr = load_dw4(dW, base + 4 * q);
       w.x -= step * gr.x; w.y -= step * gr.y; w.z -= step * gr.z; w.w -= step * gr.w;
       w4[q] = w;
       QuadIO<S>::store(Wop, wop_lo, base + 4 * q, w);
     }
   } else {
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
-      const float w = W32[base + e] - step * dW[base + e];
+      const float w = W32[base + e] - step * OpIO<DT>::load(dW, 0, base + e);
       W32[base + e] = w;
       OpIO<S>::store(Wop, wop_lo, base + e, w);
     }
   }
 }
 
+// W32[slot][s] = W0[slot] and its operand copy; blockIdx.y = slot * B + s.
 template <typename S>
-__global__ void broadcast_w0_kernel(long long total, int B, long long n, const float* __restrict__ W0,
-                                    float* __restrict__ W32, void* Wop, long long wop_lo) {
+__global__ void broadcast_w0_kernel(int B, long long n, const float* __restrict__ W0, float* __restrict__ W32,
+                                    void* Wop, long long wop_lo) {
   pdl_wait();
   pdl_launch();
+  const float* src = W0 + (long long)(blockIdx.y / B) * n;
+  const long long base = (long long)blockIdx.y * n;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const long long slot = i / (n * B), e = i % n;
-    const float w = W0[slot * n + e];
-    W32[i] = w;
-    OpIO<S>::store(Wop, wop_lo, i, w);
+  const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if ((n & 3) == 0 && (wop_lo & 3) == 0) {
+    for (long long q = t0; q < n / 4; q += stride) {
+      const float4 w = reinterpret_cast<const float4*>(src)[q];
+      reinterpret_cast<float4*>(W32 + base)[q] = w;
+      QuadIO<S>::store(Wop, wop_lo, base + 4 * q, w);
+    }
+  } else {
+    for (long long e = t0; e < n; e += stride) {
+      const float w = src[e];
+      W32[base + e] = w;
+      OpIO<S>::store(Wop, wop_lo, base + e, w);
+    }
   }
 }
 
@@ -451,21 +500,74 @@ __global__ void settle_decide_kernel(int B, const float* __restrict__ Lc, const 
   accept[s] = a >= 0.0f ? 1 : 0;
 }
 
-template <typename S>
-__global__ void settle_apply_kernel(long long total, int B, long long n, const uint8_t* __restrict__ accept,
-                                    float* __restrict__ W32, void* Wop, float* __restrict__ Wc32, void* Wcop,
-                                    long long lo) {
+// Settlement's candidate as an offset from the committed weights, in bf16:
+// D = bf16(W32 - Wc32); blockIdx.y is one (slot, sequence) segment of n.
+__global__ void delta_plane_kernel(long long n, const float* __restrict__ W32, const float* __restrict__ Wc32,
+                                   bf16* __restrict__ D) {
   pdl_wait();
   pdl_launch();
+  const long long base = (long long)blockIdx.y * n;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int s = (int)((i / n) % B);
-    if (accept[s]) {
-      Wc32[i] = W32[i];
-      OpIO<S>::copy(Wcop, lo, Wop, lo, i);
-    } else {
-      W32[i] = Wc32[i];
-      OpIO<S>::copy(Wop, lo, Wcop, lo, i);
+  const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if ((n & 3) == 0) {
+    for (long long q = t0; q < n / 4; q += stride) {
+      const float4 w = reinterpret_cast<const float4*>(W32 + base)[q];
+      const float4 c = reinterpret_cast<const float4*>(Wc32 + base)[q];
+      *reinterpret_cast<uint2*>(D + base + 4 * q) = pack_bf16x4(w.x - c.x, w.y - c.y, w.z - c.z, w.w - c.w);
+    }
+  } else {
+    for (long long e = t0; e < n; e += stride) D[base + e] = __float2bfloat16_rn(W32[base + e] - Wc32[base + e]);
+  }
+}
+
+// Eight consecutive operand-storage elements copied between two arrays with
+// the same lo-plane offset (index a multiple of 8, bases 16-byte aligned).
+template <typename S>
+__device__ __forceinline__ void copy_op8(void* dst, const void* src, long long lo, long long i) {
+  if constexpr (std::is_same<S, float>::value) {
+    const float4* s4 = reinterpret_cast<const float4*>(static_cast<const float*>(src) + i);
+    float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(dst) + i);
+    d4[0] = s4[0];
+    d4[1] = s4[1];
+  } else {
+    const bf16* sb = static_cast<const bf16*>(src);
+    bf16* db = static_cast<bf16*>(dst);
+    *reinterpret_cast<uint4*>(db + i) = *reinterpret_cast<const uint4*>(sb + i);
+    if constexpr (std::is_same<S, Split>::value)
+      *reinterpret_cast<uint4*>(db + lo + i) = *reinterpret_cast<const uint4*>(sb + lo + i);
+  }
+}
+
+// Settlement's commit or revert, per sequence: blockIdx.y is one fast matrix
+// of one sequence (slot * B + s), so the decision is uniform over the block;
+// a commit copies the current weights (fp32 master and operand copy) into the
+// committed ones, a revert copies them back.
+template <typename S>
+__global__ void settle_apply_kernel(int B, long long n, const uint8_t* __restrict__ accept, float* W32, void* Wop,
+                                    float* Wc32, void* Wcop, long long lo) {
+  pdl_wait();
+  pdl_launch();
+  const bool acc = accept[blockIdx.y % B] != 0;
+  float* dst32 = acc ? Wc32 : W32;
+  const float* src32 = acc ? W32 : Wc32;
+  void* dop = acc ? Wcop : Wop;
+  const void* sop = acc ? Wop : Wcop;
+  const long long base = (long long)blockIdx.y * n;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if ((n & 7) == 0 && (lo & 7) == 0) {
+    for (long long q = t0; q < n / 8; q += stride) {
+      const float4* s4 = reinterpret_cast<const float4*>(src32 + base) + 2 * q;
+      float4* d4 = reinterpret_cast<float4*>(dst32 + base) + 2 * q;
+      const float4 a = s4[0], b = s4[1];
+      d4[0] = a;
+      d4[1] = b;
+      copy_op8<S>(dop, sop, lo, base + 8 * q);
+    }
+  } else {
+    for (long long e = t0; e < n; e += stride) {
+      dst32[base + e] = src32[base + e];
+      OpIO<S>::copy(dop, lo, sop, lo, base + e);
     }
   }
 }
@@ -691,8 +793,8 @@ ttt_status launch_dlogits(int M, int V, void* logits, const float* lse, const in
     set_error("dlogits: V must be a multiple of 8 and the logits 16-byte aligned");
     return TTT_ERR_UNSUPPORTED;
   }
-  // 256-thread blocks each cover 2048 elements of a row; rows fill the rest of the grid
-  const int bx = ceil_div(V / 8, 256);
+  // 256-thread blocks each cover 256 * kDlVec 16-byte vectors of a row; rows fill the rest of the grid
+  const int bx = ceil_div(V / 8, 256 * kDlVec);
   const int by = M < 65535 ? M : 65535;
   launch_pdl(dlogits_kernel, dim3(bx, by), 256, 0, st, M, V, static_cast<bf16*>(logits), lse, tgt, scale, rscale);
   TTT_CHECK_LAUNCH();
@@ -718,7 +820,7 @@ ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32
 }
 
 ttt_status launch_clip_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
-                                  const float* dW, const PartialSlots& ps, const float* partials, float clip,
+                                  const void* dW, const PartialSlots& ps, const float* partials, float clip,
                                   float eta, float* scale_out, float* norm_out, int* flag, cudaStream_t st) {
   const dim3 grid = update_grid(nslots, B, n);
   LAUNCH_BY_STORAGE(stg, sgd_update_kernel, grid, 256, 0, st, B, n, W32, Wop, wop_lo, dW, ps, partials, clip, eta,
@@ -729,9 +831,8 @@ ttt_status launch_clip_sgd_update(int stg, int nslots, int B, long long n, float
 
 ttt_status launch_broadcast_w0(int stg, int nslots, int B, long long n, const float* W0, float* W32, void* Wop,
                                long long wop_lo, cudaStream_t st) {
-  const long long total = (long long)nslots * B * n;
-  const int g = grid_for(total, 256);
-  LAUNCH_BY_STORAGE(stg, broadcast_w0_kernel, g, 256, 0, st, total, B, n, W0, W32, Wop, wop_lo);
+  const dim3 g = update_grid(nslots, B, n);
+  LAUNCH_BY_STORAGE(stg, broadcast_w0_kernel, g, 256, 0, st, B, n, W0, W32, Wop, wop_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -754,9 +855,16 @@ ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const fl
                                cudaStream_t st) {
   launch_pdl(settle_decide_kernel, ceil_div(B, 128), 128, 0, st, B, Lc, Lw, A, accept);
   TTT_CHECK_LAUNCH();
-  const long long total = (long long)nslots * B * n;
-  const int g = grid_for(total, 256);
-  LAUNCH_BY_STORAGE(stg, settle_apply_kernel, g, 256, 0, st, total, B, n, accept, W32, Wop, Wc32, Wcop, op_lo);
+  const dim3 g = update_grid(nslots, B, n);
+  LAUNCH_BY_STORAGE(stg, settle_apply_kernel, g, 256, 0, st, B, n, accept, W32, Wop, Wc32, Wcop, op_lo);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_delta_plane(int nslots, int B, long long n, const float* W32, const float* Wc32, void* D,
+                              cudaStream_t st) {
+  const dim3 g = update_grid(nslots, B, n);
+  launch_pdl(delta_plane_kernel, g, 256, 0, st, n, W32, Wc32, static_cast<bf16*>(D));
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

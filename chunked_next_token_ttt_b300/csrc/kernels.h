@@ -85,7 +85,7 @@ ttt_status launch_sgd_update(int stg, int nslots, int B, long long n, float* W32
 // (may be null) receive s_s and the norm; a non-finite norm skips that
 // sequence's update and raises bit 1 of *flag.
 ttt_status launch_clip_sgd_update(int stg, int nslots, int B, long long n, float* W32, void* Wop, long long wop_lo,
-                                  const float* dW, const PartialSlots& ps, const float* partials, float clip,
+                                  const void* dW, const PartialSlots& ps, const float* partials, float clip,
                                   float eta, float* scale_out, float* norm_out, int* flag, cudaStream_t st);
 
 // W32[slot][s] = W0[slot] for every s; Wop = cast.
@@ -101,6 +101,9 @@ ttt_status launch_seq_mean(int B, int rows, int n_valid, const float* row_loss, 
 
 // A = Lc - Lw; accept = (A >= 0).  Then per sequence: accept ? Wc <- W : W <- Wc
 // over fp32 masters and operand copies.
+// D = bf16(W32 - Wc32) over the fast-weight arena [nslots][B][n] (bf16 out).
+ttt_status launch_delta_plane(int nslots, int B, long long n, const float* W32, const float* Wc32, void* D,
+                              cudaStream_t st);
 ttt_status launch_settle_apply(int stg, int nslots, int B, long long n, const float* Lc,
                                const float* Lw, float* A, uint8_t* accept, float* W32, void* Wop,
                                float* Wc32, void* Wcop, long long op_lo, cudaStream_t st);
@@ -137,6 +140,15 @@ bool swa_supported(int d, int heads);
 // (two batched GEMMs around this masked row softmax); see the engine's
 // prefix pass for the padded row layout.
 constexpr int kSwaTcRows = 128;
+// Fused sliding-window attention on the tensor cores (bf16 storage, head width
+// 64 or 128): per (128-query block, head, sequence) one CTA reads Q, K and V
+// from the padded projection rows qkvp [B][L][3d] (position p of a sequence
+// at row pad + p) and writes the heads' output into out [B][L][d] at the
+// same rows; scores and probabilities stay on chip.  Bounded-wait timeouts
+// set bits of *err.
+bool swa_fused_supported(int stg, int d, int heads);
+ttt_status launch_swa_fused(int B, int rows, int H, int dh, int window, const void* qkvp, int pad, long long L,
+                            void* out, int* err, cudaStream_t st);
 ttt_status launch_band_softmax(int stg, long long nbatch, int nw, int nqb, int j0, int pad, int rows, int window,
                                float scale, const float* Sc, void* P, long long p_lo, cudaStream_t st);
 ttt_status launch_swa(int stg, int B, int rows, int H, int dh, int window, const float* qkv, void* out,

@@ -9,6 +9,8 @@ using namespace ttt;
 // Status word of the single-operation cross-entropy (token ids outside [0, V)
 // are recorded here): file-scope device memory, so no call allocates.
 static __device__ int g_ce_status;
+// Status word of the single-operation attention (bounded-wait timeouts).
+static __device__ int g_attn_status;
 
 static ttt_status bad(ttt_status s, const char* msg) {
   set_error(msg);
@@ -93,6 +95,25 @@ ttt_status ttt_op_rmsnorm_backward(int dtype, int M, int d, const float* x, cons
                                    float* dx, void* dx_op, ttt_stream stream) {
   if (M < 0 || d < 1 || !x || !rstd || !dy || !dx) return bad(TTT_ERR_BAD_ARG, "bad rmsnorm arguments");
   return launch_rmsnorm_bwd(dtype, M, d, x, rstd, dy, dx, dx_op, 0, (cudaStream_t)stream);
+}
+
+ttt_status ttt_op_sliding_window_attention(int dtype, int B, int rows, int heads, int head_dim, int window,
+                                           const void* qkv, int pad, long long L, void* out, ttt_stream stream) {
+  if (B < 0 || rows < 0 || heads < 1 || head_dim < 1 || window < 1 || pad < 0 || !qkv || !out)
+    return bad(TTT_ERR_BAD_ARG, "bad sliding-window attention arguments");
+  if (dtype != TTT_DTYPE_BF16 || !swa_fused_supported(ST_BF16, heads * head_dim, heads))
+    return bad(TTT_ERR_UNSUPPORTED, "the fused attention runs bf16 with head width 64 or 128");
+  if (L < (long long)pad + ceil_div(rows, 128) * 128LL) return bad(TTT_ERR_BAD_SHAPE, "L too small for pad + rows");
+  void* err = nullptr;
+  TTT_CUDA(symbol_address((const void*)&g_attn_status, &err));
+  cudaStream_t st = (cudaStream_t)stream;
+  TTT_CUDA(cudaMemsetAsync(err, 0, sizeof(int), st));
+  TTT_TRY(launch_swa_fused(B, rows, heads, head_dim, window, qkv, pad, L, out, static_cast<int*>(err), st));
+  int flag = 0;
+  TTT_CUDA(cudaMemcpyAsync(&flag, err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  TTT_CUDA(cudaStreamSynchronize(st));
+  if (flag) return bad(TTT_ERR_TIMEOUT, "a fused attention wait timed out");
+  return TTT_OK;
 }
 
 size_t ttt_clip_sgd_workspace_size(int nslots, int B, long long n) {

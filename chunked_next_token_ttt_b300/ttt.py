@@ -46,7 +46,8 @@ class HParams(ctypes.Structure):
 class Options(ctypes.Structure):
     """ttt_options: zero fields are the library's defaults."""
     _fields_ = [("no_pdl", ctypes.c_int), ("no_decode_graph", ctypes.c_int), ("fp32_simt", ctypes.c_int),
-                ("hoist_chunks", ctypes.c_int), ("no_token_kernel", ctypes.c_int), ("max_ctas", ctypes.c_int)]
+                ("hoist_chunks", ctypes.c_int), ("no_token_kernel", ctypes.c_int), ("max_ctas", ctypes.c_int),
+                ("no_dw_stream", ctypes.c_int), ("attn_unfused", ctypes.c_int)]
 
 
 class Weights(ctypes.Structure):
@@ -328,6 +329,7 @@ def _ops_lib():
             "ttt_clip_sgd": ([_I, _I, _I, ctypes.c_longlong, _P, _P, _P, ctypes.c_float, ctypes.c_float,
                               _P, _P, _P, ctypes.c_size_t, _P], _I),
             "ttt_clip_sgd_workspace_size": ([_I, _I, ctypes.c_longlong], ctypes.c_size_t),
+            "ttt_op_sliding_window_attention": ([_I, _I, _I, _I, _I, _I, _P, _I, ctypes.c_longlong, _P, _P], _I),
             "ttt_clip_sgd_noalloc": ([_I, _I, _I, ctypes.c_longlong, _P, _P, _P, ctypes.c_float,
                                       ctypes.c_float, _P, _P, _P], _I),
         }
@@ -376,6 +378,14 @@ def op_rmsnorm_backward(dtype, x, rstd, dy, dx, dx_op=None, stream=None):
     M, d = x.shape
     _check(_ops_lib().ttt_op_rmsnorm_backward(DTYPE[dtype], M, d, _ptr(x), _ptr(rstd), _ptr(dy), _ptr(dx),
                                               _ptr(dx_op), _stream(stream)), "ttt_op_rmsnorm_backward")
+
+
+def op_sliding_window_attention(qkv, rows, heads, window, pad, out, stream=None):
+    """qkv [B, L, 3d] bf16 device tensor (position p at row pad + p); out [B, L, d]."""
+    B, L, d3 = qkv.shape
+    d = d3 // 3
+    _check(_ops_lib().ttt_op_sliding_window_attention(1, B, rows, heads, d // heads, window, _ptr(qkv), pad, L,
+                                                      _ptr(out), _stream(stream)), "ttt_op_sliding_window_attention")
 
 
 def clip_sgd_workspace_size(nslots, B, n) -> int:

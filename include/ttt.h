@@ -169,6 +169,12 @@ typedef struct {
                           persistent per-token kernel                          */
   int max_ctas;        /* > 0: at most this many CTAs in a tensor-core GEMM's
                           persistent grid (0: one per SM)                      */
+  int no_dw_stream;    /* 1: the weight-gradient GEMMs run in stream order with
+                          the input-gradient chain instead of on the handle's
+                          second stream beside it                             */
+  int attn_unfused;    /* 1: bf16 sliding-window attention runs as score GEMM,
+                          windowed softmax and P V GEMM per head instead of the
+                          fused kernel that keeps scores on chip             */
 } ttt_options;
 
 /* Validate dims/hparams, allocate every device buffer the handle needs for

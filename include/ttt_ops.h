@@ -25,8 +25,10 @@ enum {
   TTT_EPI_RESID = 3,     /* out(float) = aux(float) + acc; out2(op) = same or NULL */
   TTT_EPI_SWIGLU = 4,    /* out(op) = silu(aux(float)) * acc                     */
   TTT_EPI_DGELU = 5,     /* out(op) = acc * GELU'(aux(op))                       */
-  TTT_EPI_DW = 6         /* out(float) = acc; partials[b * tiles + t] = per-tile
-                            sum of acc^2 (tiles = ttt_op_gemm_partial_tiles)     */
+  TTT_EPI_DW = 6         /* out = acc (bf16 when dtype is TTT_DTYPE_BF16, float
+                            otherwise); partials[b * tiles + t] = per-tile sum of
+                            acc^2 of the fp32 accumulators (tiles =
+                            ttt_op_gemm_partial_tiles)                           */
 };
 enum { TTT_GEMM_AUTO = 0, TTT_GEMM_SIMT = 1, TTT_GEMM_TENSOR = 2 };
 /* Operand storage code accepted by ttt_op_gemm besides TTT_DTYPE_FP32/BF16:
@@ -65,6 +67,20 @@ typedef struct {
 ttt_status ttt_op_gemm(const ttt_gemm_args* args, ttt_stream stream);
 /* Number of partial sums per batch entry an TTT_EPI_DW call writes. */
 int ttt_op_gemm_partial_tiles(const ttt_gemm_args* args);
+
+/* Sliding-window multi-head attention, forward ("End-to-End TTT" review,
+ * Method: the sliding-window attention fix of the bigram defect), as the fused
+ * tensor-core kernel the prefill runs: bf16 storage, head width 64 or 128.
+ *   qkv  [B][L][3d] bf16 rows Q | K | V (d = heads * head_dim); position p of
+ *        sequence s is row pad + p, p < rows; L >= pad + ceil(rows / 128) * 128;
+ *        rows of other positions must hold finite values (they are read, then
+ *        masked).
+ *   out  [B][L][d] bf16: row pad + p gets, for every head h, softmax over keys
+ *        p - window < q <= p (q >= 0) of (Q_p . K_q) / sqrt(head_dim), times V.
+ * Errors: BAD_ARG, UNSUPPORTED (dtype, head width, alignment), TIMEOUT (read
+ * by synchronising `stream`), CUDA. */
+ttt_status ttt_op_sliding_window_attention(int dtype, int B, int rows, int heads, int head_dim, int window,
+                                           const void* qkv, int pad, long long L, void* out, ttt_stream stream);
 
 /* Softmax cross-entropy of each row of logits [M, V] (operand type) against
  * targets [M] (int32 in [0, V)): losses[m] = logsumexp(row) - row[target]

@@ -11,6 +11,7 @@ import torch
 
 import oracle
 import synth
+from chunked_next_token_ttt_b300 import Handle
 from synth import configs as C
 
 from gpu_harness import TOL, compare, compare_settlement, make, run_gpu, run_oracle
@@ -408,6 +409,52 @@ def test_sliding_window_attention_prefill_against_the_oracle(case):
     inp = _attention_inputs(wl)
     gpu = run_gpu(wl, inp, loss_mask=mask)
     ref = run_oracle(wl, inp, loss_mask=mask)
+    compare(wl, gpu, ref)
+
+
+def _attention_launches(wl, inp, options=None):
+    """Kernel classes of one prefill, logged by the library, and its outputs."""
+    h = Handle.from_workload(wl, inp["weights"], options=options)
+    tok = torch.from_numpy(np.ascontiguousarray(inp["tokens"])).cuda()
+    losses = torch.empty((wl.B, wl.T), dtype=torch.float32, device="cuda")
+    p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    h.launch_log_enable(True)
+    h.prefill(tok, losses, p)
+    torch.cuda.synchronize()
+    log = h.launch_log()
+    h.close()
+    return log, losses.cpu().numpy().astype(np.float64), p.cpu().numpy()
+
+
+@pytest.mark.parametrize("dh,window,T", [(64, 1, 2 * 128 + 30), (64, 100, 3 * 128 + 17), (64, 200, 5 * 128),
+                                          (128, 300, 4 * 128 + 3), (64, 4096, 3 * 128 + 1)],
+                         ids=["dh64_k1", "dh64_k100_ragged", "dh64_k200", "dh128_k300", "dh64_k_beyond_T"])
+def test_fused_attention_against_the_oracle_and_the_unfused_path(dh, window, T):
+    """The fused tensor-core attention (bf16, one launch per frozen block, scores
+    on chip): head widths 64 and 128, windows of 1, below, at and beyond a
+    128-key block and beyond T, several 128-query blocks with a ragged last
+    one.  Against the oracle at the bf16 tolerance, and against the three-launch
+    path (score GEMM, windowed softmax, P V GEMM) it replaces; the launch log
+    shows which path ran.  Weights N(0, 0.05^2) and scores sharpened by 8 (4
+    for the 128-wide heads, whose dot products are twice as long)."""
+    heads = 2
+    wl = C.E2E_125M.replace(d=heads * dh, d_ff=2 * heads * dh, vocab=1024, chunk=64, B=2, T=T, n_prefix=2,
+                            init_std=0.05, attn_heads=heads, attn_window=window)
+    inp = _attention_inputs(wl, qk_scale=8.0 if dh == 64 else 4.0)
+    log_f, loss_f, p_f = _attention_launches(wl, inp)
+    log_u, loss_u, p_u = _attention_launches(wl, inp, options={"attn_unfused": 1})
+    ref = run_oracle(wl, inp)
+    rep = {"attention launches (fused, unfused)": (log_f.count("attention"), log_u.count("attention")),
+           "fused mean loss err": [float(np.abs(loss_f[s] - ref["losses"][s]).mean()) for s in range(wl.B)],
+           "unfused mean loss err": [float(np.abs(loss_u[s] - ref["losses"][s]).mean()) for s in range(wl.B)],
+           "fused p_next max err": [float(np.abs(p_f[s] - ref["p_next"][s]).max()) for s in range(wl.B)],
+           "fused vs unfused mean loss diff": float(np.abs(loss_f - loss_u).mean())}
+    # per frozen block: the K/V cache fill, then one fused launch (or 3 per head)
+    assert rep["attention launches (fused, unfused)"] == (wl.n_prefix * 2, wl.n_prefix * (1 + 3 * heads)), rep
+    assert max(rep["fused mean loss err"]) <= TOL["bf16"]["loss_mean"], rep
+    assert max(rep["fused p_next max err"]) <= 2e-3, rep
+    assert max(rep["unfused mean loss err"]) <= TOL["bf16"]["loss_mean"], rep
+    gpu = run_gpu(wl, inp)
     compare(wl, gpu, ref)
 
 
