@@ -48,39 +48,45 @@ FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
-# host-side orchestration (which kernels run, not what a kernel does): left
-# out of the kernel identity below
-HOST_SOURCES = {"engine.cu", "engine.h", "ops_api.cu", "noalloc.cu", "devctx.cu"}
+# the sources that define each family of kernels (kernel identity for counters
+# taken by a profiler: a change elsewhere leaves a family's counters valid)
+KERNEL_FAMILIES = {
+    "gemm": ("common.cuh", "epilogue.cuh", "gemm.h", "gemm.cu", "gemm_tc.cu", "gemm_tc_kernel.cuh", "gemm_tc_kk.cu",
+             "gemm_tc_km.cu", "gemm_tc_mk.cu", "gemm_tc_mm.cu", "gemm_simt.cu", "gemm_small.cu"),
+    "elementwise": ("common.cuh", "kernels.h", "kernels.cu", "clip_sgd.h", "clip_sgd.cu"),
+    "attention": ("common.cuh", "kernels.h", "gemm_tc_kernel.cuh", "attention.cu", "attention_fused.cu"),
+    "token": ("common.cuh", "kernels.h", "token_step.cu"),
+}
 
 
-def source_hash():
-    """SHA-256 over the libttt sources that define kernels (kernel identity for
-    counters taken by a profiler)."""
-    import glob
+def class_family(kernel_class):
+    if kernel_class.startswith("gemm_"):
+        return "gemm"
+    return {"attention": "attention", "token_step": "token"}.get(kernel_class, "elementwise")
+
+
+def source_hash(family):
+    """SHA-256 over the sources of one kernel family."""
     import hashlib
     hsh = hashlib.sha256()
-    files = sorted(f for f in glob.glob(os.path.join(ROOT, "chunked_next_token_ttt_b300", "csrc", "*"))
-                   if os.path.basename(f) not in HOST_SOURCES)
-    for f in files:
-        hsh.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for name in sorted(KERNEL_FAMILIES[family]):
+        hsh.update(name.encode())
+        with open(os.path.join(ROOT, "chunked_next_token_ttt_b300", "csrc", name), "rb") as fh:
             hsh.update(fh.read())
     return hsh.hexdigest()[:16]
 
 
 def profiled_traffic(workload, kernel_class):
     """DRAM bytes per launch of a kernel class from profiles/traffic.json (ncu's
-    dram__bytes_read.sum + dram__bytes_write.sum per launch, one entry per
-    workload), or None when there is none or the kernels changed since the
-    counters were taken."""
+    dram__bytes_read.sum + dram__bytes_write.sum per launch), or None when there
+    is none or the class's kernel family changed since the counters were taken."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
-        meta = json.load(f).get(workload, {})
-    if meta.get("source_hash") != source_hash():
+        entry = json.load(f).get(workload, {}).get(kernel_class)
+    if not entry or entry.get("source_hash") != source_hash(class_family(kernel_class)):
         return None
-    v = meta.get("dram_bytes_per_launch", {}).get(kernel_class)
-    return float(v) if v is not None else None
+    return float(entry["dram_bytes_per_launch"])
 
 
 def choose_peak(pk, clocks, timed_s):

@@ -4,25 +4,37 @@
 // attention stays frozen during TTT).  One CTA per (128-query block, head,
 // sequence); no score or probability block ever reaches global memory.
 //
-// Two passes over the key blocks (128 keys each) the query block's window
-// reaches:
-//   pass 1  S = Q K^T into TMEM; the softmax warps read S and keep each query
-//           row's running maximum m and sum l of exp(S - m) over its window;
-//   pass 2  S = Q K^T again; P = exp(S - m) (unnormalised, in [0, 1]) goes to
-//           shared memory as bf16 in the tensor core's K-major 128B-swizzled
-//           layout, and O += P V accumulates in TMEM;
-// then out = O / l.  With m and l final before any P is formed, O is never
-// rescaled (the price is a second Q K^T per key block).
+// One pass over the key blocks (128 keys each) the query block's window
+// reaches, online softmax: per block, S = Q K^T into TMEM (double-buffered,
+// so the next S is computed while the softmax works on the current one); the
+// softmax warps take the block's row maximum; the row's running maximum m is
+// raised only when the block's exceeds it by more than TAU (base 2), and
+// then the row's partial output O in TMEM and its sum l are rescaled by
+// 2^(m_old - m_new) before the block's P V is issued; P = 2^(S c - m) (at
+// most 2^TAU) goes to TMEM as packed bf16 pairs, and O += P V accumulates in
+// TMEM with P as the MMA's A operand read from TMEM (so P never touches
+// shared memory, whose bandwidth the K/V copies and the operand reads of both
+// products already share).  out = O / l.
 //
-// Warps: 0 TMA producer (Q once; K, then K and V, per key block through a
-// two-slot ring), 1 TMEM allocator and MMA issuer (S double-buffered in TMEM,
-// so the next S is computed while the softmax works on the current one),
-// 2..9 softmax and output: the warps of TMEM lane quadrant q (w % 4 == q) own
-// query rows 32 q .. 32 q + 31, one thread per row in each of two column
-// halves (64 keys of a block, half of the head's output columns); the halves
-// combine their running maximum and sum once, after pass 1.
+// P is double-buffered: the softmax of block t writes its P while the tensor
+// core still reads block t-1's; only a rescale waits for that P V.
+//
+// Warps: 0 TMA producer (Q once; K and V per key block through a ring of
+// three slots for head width 64, two for 128), 1 TMEM allocator and MMA
+// issuer, 2..17 softmax and output: the four warps of TMEM lane quadrant q
+// (w % 4 == q) own query rows 32 q .. 32 q + 31, one thread per row in each
+// of four column parts (32 keys of a block, a quarter of the head's output
+// columns); the four threads of a row exchange their block maxima once per
+// block at a barrier of the quadrant's warps, which also carries their wait
+// verdicts, so they rescale alike and leave together.
+//
+// The exponentials: the MUFU unit does 16 per clock per SM, which at head
+// width 64 is slower than the tensor core's two 128 x 128 x 64 products per
+// block, so half of them run on the FMA pipe as a polynomial (ex2_poly2),
+// and the scale, subtract and sums run as two-wide f32x2 ops.
 // Every mbarrier wait is bounded (tc::mbar_wait); a timeout records a code in
-// the status word and the CTA unwinds.
+// the status word and the CTA unwinds: the producer waits (bounded) for its
+// copies in flight, the MMA issuer for its MMAs, and TMEM is freed.
 #include "gemm_tc_kernel.cuh"
 #include "kernels.h"
 
@@ -33,27 +45,41 @@ using namespace tc;
 
 constexpr int BQ = 128;                  // query rows per CTA (UMMA M)
 constexpr int BKV = 128;                 // keys per block (UMMA N of S, K of P V)
-constexpr int KST = 2;                   // K/V ring slots
-constexpr int NSW = 8;                   // softmax warps (two per TMEM lane quadrant)
+constexpr int NPART = 2;                 // softmax warps per TMEM lane quadrant
+constexpr int NSW = 4 * NPART;           // softmax warps
 constexpr int NTHREADS = 64 + 32 * NSW;  // producer, MMA, softmax
-constexpr int HALF = BKV / 2;            // keys of a block per softmax thread
+constexpr int QK = BKV / NPART;          // keys of a block per softmax thread
+// pairs of every 8 consecutive P values computed by the polynomial 2^x on the
+// FMA pipe instead of the MUFU unit (which does 16 exponentials per clock per SM)
+constexpr int EMU_PAIRS = 0;
 constexpr int PANEL_BYTES = 128 * 128;   // 128 rows x 64 bf16: one 128B-swizzle panel
+constexpr float TAU = 8.0f;              // raise the running maximum only beyond this (P <= 2^TAU)
 
 template <int DH>
 struct Layout {
   static constexpr int NP = DH / 64;                       // 64-wide panels of a head
+  static constexpr int KST = DH == 64 ? 3 : 2;             // K/V ring slots
+  static constexpr int NPB = 2;                            // P buffers (in TMEM)
   static constexpr int TILE = NP * PANEL_BYTES;            // a Q, K or V tile of 128 rows
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + TILE;               // [KST] K tiles
   static constexpr int V_OFF = K_OFF + KST * TILE;         // [KST] V tiles
-  static constexpr int P_OFF = V_OFF + KST * TILE;         // P: 2 panels (128 keys)
-  static constexpr int ML_OFF = P_OFF + 2 * PANEL_BYTES;   // [2 halves][128 rows] (m, l) exchange
-  static constexpr int BAR_OFF = ML_OFF + 2 * BQ * 8;
-  // q_full, kv_full[KST], kv_empty[KST], s_full[2], s_empty[2], p_full, p_empty, o_full; the TMEM slot
-  static constexpr int NBAR = 1 + 2 * KST + 4 + 3;
+  // exchange between a row's NPART threads: [2 block parities][NPART][128 rows]
+  // block maxima, then [NPART][128 rows] sums
+  static constexpr int X_OFF = V_OFF + KST * TILE;
+  static constexpr int BAR_OFF = X_OFF + 3 * NPART * BQ * 4;
+  // q_full, kv_full[KST], kv_empty[KST], s_full[2], s_empty[2], p_full[NPB],
+  // p_empty[NPB], o_full, drain; the TMEM slot
+  static constexpr int NBAR = 1 + 2 * KST + 4 + 2 * NPB + 2;
   static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16;
   static constexpr int ALLOC = TOTAL + 1024;               // room to align the base to 1024 bytes
-  static constexpr uint32_t TMEM_COLS = 512;               // S0: 0..127, S1: 128..255, O: 256..256+DH
+  // TMEM columns: S0 0..127, S1 128..255 (fp32), O 256..256+DH (fp32), then
+  // P0 and P1, 64 columns each (128 bf16 keys per row, two per column)
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_O = 2 * BKV;
+  static constexpr uint32_t T_P = T_O + DH;
+  static_assert(T_P + NPB * BKV / 2 <= TMEM_COLS, "TMEM columns");
+  static_assert(ALLOC <= 232448, "shared memory over the per-block limit");
 };
 
 struct Args {
@@ -67,19 +93,83 @@ struct Args {
   int* err;
 };
 
-// Barrier among the softmax warps only (id 1) that returns the AND of `ok`
-// over all of them, so that they all take the same branch after it.
-__device__ __forceinline__ bool softmax_all(bool ok) {
+// Barrier of the NPART softmax warps of TMEM lane quadrant q (id 2 + q) that
+// returns the AND of `ok` over them, so that they take the same branch.
+__device__ __forceinline__ bool quad_all(int quad, bool ok) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}\n"
       : "=r"(r)
-      : "r"((uint32_t)ok), "n"(32 * NSW)
+      : "r"((uint32_t)ok), "r"(2 + quad), "n"(32 * NPART)
       : "memory");
   return r != 0;
+}
+
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz:
+// about 2 ulp; 2^-inf = 0, which masks out-of-window scores).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Packed pairs of floats for the two-wide FMA pipe instructions (f32x2).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 f2make(float x, float y) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void f2split(f2 v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ f2 f2fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f2 f2add(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2sub(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// 2^x for a pair on the FMA pipe.  x is clamped to >= -126 (2^-126 and below
+// contribute nothing a bf16 P can carry); x = n + f with n = round(x), taken
+// by adding 1.5 * 2^23 (which leaves n in the low mantissa bits) and f in
+// [-1/2, 1/2]; 2^f by a cubic in Horner form whose coefficients are a
+// relative-error-weighted least-squares fit of 2^f on [-1/2, 1/2] (largest
+// relative error 7.5e-5, below bf16's 2^-9); 2^n enters by adding n to the
+// exponent field (p lies in [0.70, 1.42], so the field stays in 0 .. 135).
+__device__ __forceinline__ void ex2_poly2(float& x0, float& x1) {
+  const f2 kRound = f2make(12582912.0f, 12582912.0f);
+  const f2 x = f2make(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
+  const f2 j = f2add(x, kRound);
+  const f2 f = f2sub(x, f2sub(j, kRound));
+  f2 p = f2fma(f2make(0.05517115443944931f, 0.05517115443944931f), f,
+               f2make(0.2426101416349411f, 0.2426101416349411f));
+  p = f2fma(p, f, f2make(0.6932609677314758f, 0.6932609677314758f));
+  p = f2fma(p, f, f2make(0.9999281167984009f, 0.9999281167984009f));
+  float p0, p1, j0, j1;
+  f2split(p, p0, p1);
+  f2split(j, j0, j1);
+  x0 = __int_as_float(__float_as_int(p0) + (__float_as_int(j0) << 23));
+  x1 = __int_as_float(__float_as_int(p1) + (__float_as_int(j1) << 23));
+}
+
+// max(x, y, z) in one three-input instruction.
+__device__ __forceinline__ float max3(float x, float y, float z) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+  return r;
 }
 
 // A bounded mbarrier wait whose verdict is the same for every lane of the warp.
@@ -87,10 +177,86 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, code));
 }
 
+// 16 consecutive TMEM columns of the warp's 32 lanes to and from registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 consecutive TMEM columns of the warp's 32 lanes from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+      "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+      "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D (+)= A B with A (M = 128 rows, 16 bf16 of K packed in 8 columns) read
+// from TMEM and B from shared memory.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// N consecutive TMEM columns (16 or a multiple of 32) of the warp's lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 16) {
+    tmem_ld16(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) tmem_ld32(taddr + 32 * c, *reinterpret_cast<float(*)[32]>(v + 32 * c));
+  }
+}
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const float (&v)[N]) {
+  if constexpr (N == 16) {
+    tmem_st16(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c)
+      tmem_st32(taddr + 32 * c, *reinterpret_cast<const float(*)[32]>(v + 32 * c));
+  }
+}
+
 template <int DH>
 __global__ void __launch_bounds__(NTHREADS, 1)
     swa_fused_kernel(const __grid_constant__ CUtensorMap tm, const Args a, int nkb) {
   using L = Layout<DH>;
+  constexpr int KST = L::KST, NPB = L::NPB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -99,11 +265,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* kv_empty = kv_full + KST;
   uint64_t* s_full = kv_empty + KST;       // [2]
   uint64_t* s_empty = s_full + 2;          // [2]
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* o_full = p_empty + 1;
+  uint64_t* p_full = s_empty + 2;          // [NPB]
+  uint64_t* p_empty = p_full + NPB;        // [NPB]
+  uint64_t* o_full = p_empty + NPB;
+  uint64_t* drain = o_full + 1;            // the MMA issuer's wait for its own MMAs when it stops early
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
-  float2* ml = reinterpret_cast<float2*>(smem + L::ML_OFF);
+  float* xch = reinterpret_cast<float*>(smem + L::X_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = blockIdx.x * BQ;             // first query position of the block
@@ -124,9 +291,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], NSW);
     }
-    mbar_init(p_full, NSW);
-    mbar_init(p_empty, 1);
+    for (int b = 0; b < NPB; ++b) {
+      mbar_init(&p_full[b], NSW);
+      mbar_init(&p_empty[b], 1);
+    }
     mbar_init(o_full, 1);
+    mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -140,7 +310,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 2 * BKV;
+  const uint32_t tO = tmem + L::T_O;
   // Q | K | V were written by the projection GEMM before this kernel
   pdl_wait();
   pdl_launch();
@@ -151,30 +321,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int p = 0; p < L::NP; ++p)
       tma_load_3d(smem + L::Q_OFF + p * PANEL_BYTES, &tm, q_full, hc + 64 * p, a.pad + q0, seq);
     uint32_t u = 0;
-    bool ok = true;
-    for (int pass = 0; pass < 2 && ok; ++pass) {
-      for (int j = j_lo; j < nkb; ++j, ++u) {
-        const int s = u % KST;
-        if (u >= (uint32_t)KST && !mbar_wait(&kv_empty[s], ((u / KST) & 1) ^ 1, a.err, 8)) {
-          ok = false;
-          break;
-        }
-        const int ky = a.pad + kb0 + j * BKV;    // may be negative: TMA fills zeros there
-        mbar_expect_tx(&kv_full[s], pass ? 2 * L::TILE : L::TILE);
-        for (int p = 0; p < L::NP; ++p)
-          tma_load_3d(smem + L::K_OFF + s * L::TILE + p * PANEL_BYTES, &tm, &kv_full[s], hc + a.d + 64 * p, ky,
-                      seq);
-        if (pass)
-          for (int p = 0; p < L::NP; ++p)
-            tma_load_3d(smem + L::V_OFF + s * L::TILE + p * PANEL_BYTES, &tm, &kv_full[s], hc + 2 * a.d + 64 * p,
-                        ky, seq);
+    for (int j = j_lo; j < nkb; ++j, ++u) {
+      const int s = u % KST;
+      if (u >= (uint32_t)KST && !mbar_wait(&kv_empty[s], ((u / KST) & 1) ^ 1, a.err, 8)) break;
+      const int ky = a.pad + kb0 + j * BKV;    // may be negative: TMA fills zeros there
+      mbar_expect_tx(&kv_full[s], 2 * L::TILE);
+      for (int p = 0; p < L::NP; ++p) {
+        tma_load_3d(smem + L::K_OFF + s * L::TILE + p * PANEL_BYTES, &tm, &kv_full[s], hc + a.d + 64 * p, ky, seq);
+        tma_load_3d(smem + L::V_OFF + s * L::TILE + p * PANEL_BYTES, &tm, &kv_full[s], hc + 2 * a.d + 64 * p, ky,
+                    seq);
       }
     }
+    // no copy may still be landing in shared memory when the CTA exits (the
+    // MMA issuer may have stopped early): wait, bounded, for Q and each slot's last load
+    bool landed = mbar_wait(q_full, 0, a.err, 8);
+    for (uint32_t q = u > (uint32_t)KST ? u - KST : 0; q < u && landed; ++q)
+      landed = mbar_wait(&kv_full[q % KST], (q / KST) & 1, a.err, 8);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
     constexpr uint32_t idS = umma_idesc(BQ, BKV, false, false);   // S = Q K^T: both operands K-major
     constexpr uint32_t idO = umma_idesc(BQ, DH, false, true);     // O += P V: V MN-major
-    const uint32_t sq = smem_u32(smem + L::Q_OFF), sp = smem_u32(smem + L::P_OFF);
+    const uint32_t sq = smem_u32(smem + L::Q_OFF);
     // S = Q K^T of ring slot s into TMEM buffer b (DH / 16 steps of 16)
     auto issue_s = [&](int s, int b) {
       const uint32_t sk = smem_u32(smem + L::K_OFF + s * L::TILE);
@@ -185,145 +352,197 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   kk > 0 ? 1u : 0u);
       }
     };
-    // O += P V of ring slot s (8 steps of 16 keys); the first block starts O
-    auto issue_pv = [&](int s, bool first) {
+    // O += P V of ring slot s and TMEM P buffer pb (8 steps of 16 keys, 8
+    // columns of packed pairs each); the first block starts O
+    auto issue_pv = [&](int s, int pb, bool first) {
       const uint32_t sv = smem_u32(smem + L::V_OFF + s * L::TILE);
+      const uint32_t tp = tmem + L::T_P + pb * (BKV / 2);
 #pragma unroll
       for (int kk = 0; kk < BKV / 16; ++kk) {
-        const uint64_t ad = umma_desc(sp + (kk / 4) * PANEL_BYTES + (kk % 4) * 32, 16, 1024);
         const uint64_t bd = umma_desc(sv + kk * 2048, PANEL_BYTES, 1024);
-        umma_bf16(tO, ad, bd, idO, (!first || kk > 0) ? 1u : 0u);
+        umma_bf16_tmem_a(tO, tp + kk * 8, bd, idO, (!first || kk > 0) ? 1u : 0u);
       }
     };
     bool ok = mbar_wait(q_full, 0, a.err, 16);
-    uint32_t u = 0, t = 0;       // ring uses; S products issued
-    int prev = -1;               // ring slot of the pass-2 block whose P V is still to issue
-    int npv = 0;                 // P V products issued
-    for (int pass = 0; pass < 2 && ok; ++pass) {
-      for (int j = j_lo; j < nkb && ok; ++j, ++u, ++t) {
-        const int s = u % KST, b = t & 1;
-        if (!mbar_wait(&kv_full[s], (u / KST) & 1, a.err, 16)) { ok = false; break; }
-        // the softmax warps have read the S that last used TMEM buffer b
-        if (t >= 2 && !mbar_wait(&s_empty[b], ((t >> 1) - 1) & 1, a.err, 16)) { ok = false; break; }
+    uint32_t t = 0;               // blocks whose S is issued (ring use t, TMEM buffer t & 1)
+    int prev = -1;                // ring slot of the block whose P V is still to issue
+    for (int j = j_lo; j < nkb && ok; ++j, ++t) {
+      const int s = t % KST, b = t & 1;
+      if (!mbar_wait(&kv_full[s], (t / KST) & 1, a.err, 16)) { ok = false; break; }
+      // the softmax warps have read the S that last used TMEM buffer b
+      if (t >= 2 && !mbar_wait(&s_empty[b], ((t >> 1) - 1) & 1, a.err, 16)) { ok = false; break; }
+      tc_fence_after();
+      issue_s(s, b);
+      umma_commit(&s_full[b]);
+      if (prev >= 0) {
+        // the previous block's P is in shared memory (and O rescaled): O += P V
+        const int pb = (t - 1) % NPB;
+        if (!mbar_wait(&p_full[pb], ((t - 1) / NPB) & 1, a.err, 16)) { ok = false; break; }
         tc_fence_after();
-        issue_s(s, b);
-        umma_commit(&s_full[b]);
-        if (pass == 0) {
-          umma_commit(&kv_empty[s]);     // pass 1 reads only K
-          continue;
-        }
-        if (prev >= 0) {
-          // the previous block's P is in shared memory: O += P V, then free its slot and P
-          if (!mbar_wait(p_full, npv & 1, a.err, 16)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(prev, npv == 0);
-          ++npv;
-          umma_commit(&kv_empty[prev]);
-          umma_commit(p_empty);
-        }
-        prev = s;
+        issue_pv(prev, pb, t == 1);
+        umma_commit(&kv_empty[prev]);
+        umma_commit(&p_empty[pb]);
+      }
+      prev = s;
+    }
+    if (ok && prev >= 0) {
+      const int pb = (t - 1) % NPB;
+      if (mbar_wait(&p_full[pb], ((t - 1) / NPB) & 1, a.err, 16)) {
+        tc_fence_after();
+        issue_pv(prev, pb, t == 1);
+        umma_commit(&kv_empty[prev]);
+        umma_commit(&p_empty[pb]);
+        umma_commit(o_full);
+      } else {
+        ok = false;
       }
     }
-    if (ok && prev >= 0 && mbar_wait(p_full, npv & 1, a.err, 16)) {
-      tc_fence_after();
-      issue_pv(prev, npv == 0);
-      umma_commit(&kv_empty[prev]);
-      umma_commit(p_empty);
-      umma_commit(o_full);
+    if (!ok) {
+      // stopped early: the MMAs already issued finish before TMEM is freed
+      umma_commit(drain);
+      mbar_wait(drain, 0, a.err, 16);
     }
   } else if (warp >= 2) {
     // ------------------------------------------------ softmax and output
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;          // which 64 keys of a block (and half of the output)
+    const int part = (warp - 2) >> 2;          // which QK keys of a block (and which OC output columns)
     const int r = quad * 32 + lane;            // query row of the block
     const int qi = q0 + r;                     // its position in the sequence
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int col0 = half * HALF;
-    float m = -FLT_MAX, l = 0.0f;              // base-2 running maximum and sum of this half
+    const int col0 = part * QK;
+    constexpr int OC = DH / NPART;             // output columns of this thread
+    static_assert(OC == 16 || OC == 32 || OC == 64, "output columns per thread");
+    float m = -INFINITY;                       // the row's running maximum (base 2), shared by its NPART threads
+    float l = 0.0f;                            // this thread's part of the row's sum of P
     uint32_t t = 0;
-    int np = 0;                                // P blocks written
+    // ok: every wait of this warp so far ended in time (warp-uniform); a
+    // failure is voted at the next quadrant barrier, where all NPART warps leave
     bool ok = true;
-    uint8_t* prow = smem + L::P_OFF + half * PANEL_BYTES + r * 128;
-    for (int pass = 0; pass < 2; ++pass) {
-      if (pass == 1) {
-        // combine the two halves' (m, l) of every row: both threads of a row take
-        // the total (every softmax warp reaches this vote once, timed out or not)
-        ml[half * BQ + r] = make_float2(m, l);
-        if (!softmax_all(ok)) {
-          ok = false;
-          break;
-        }
-        const float2 o = ml[(half ^ 1) * BQ + r];
-        const float nm = fmaxf(m, o.x);
-        l = (m > -FLT_MAX ? l * exp2f(m - nm) : 0.0f) + (o.x > -FLT_MAX ? o.y * exp2f(o.x - nm) : 0.0f);
-        m = nm;
-      }
-      for (int j = j_lo; j < nkb; ++j, ++t) {
-        const int b = t & 1;
-        if (!warp_wait(&s_full[b], (t >> 1) & 1, a.err, 32)) { ok = false; break; }
+    for (int j = j_lo; j < nkb; ++j, ++t) {
+      const int b = t & 1, pb = t % NPB;
+      ok = ok && warp_wait(&s_full[b], (t >> 1) & 1, a.err, 32);
+      float v[QK];
+      if (ok) {
         tc_fence_after();
-        float v[HALF];
-#pragma unroll
-        for (int c = 0; c < HALF / 32; ++c)
-          tmem_ld32(tmem + b * BKV + col0 + c * 32 + lane_off, *reinterpret_cast<float(*)[32]>(v + 32 * c));
+        tmem_ldn<QK>(tmem + b * BKV + col0 + lane_off, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[b]);
-        // the row's valid keys among this thread's columns: lo .. hi
-        const int kp = kb0 + j * BKV + col0;
-        const int lo = max(max(0, qi - a.window + 1), kp) - kp;
-        const int hi = min(qi, kp + HALF - 1) - kp;
-        const bool all = lo <= 0 && hi >= HALF - 1;
-        if (pass == 0) {
-          if (hi < lo) continue;
-          float bm[4] = {-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX};
-#pragma unroll
-          for (int c = 0; c < HALF; ++c) {
-            v[c] *= a.c;
-            if (all || (c >= lo && c <= hi)) bm[c & 3] = fmaxf(bm[c & 3], v[c]);
-          }
-          const float nm = fmaxf(m, fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3])));
-          float se[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-          for (int c = 0; c < HALF; ++c)
-            if (all || (c >= lo && c <= hi)) se[c & 3] += exp2f(v[c] - nm);
-          l = (m > -FLT_MAX ? l * exp2f(m - nm) : 0.0f) + ((se[0] + se[1]) + (se[2] + se[3]));
-          m = nm;
-          continue;
-        }
-        // pass 2: this block's P once the previous P V has read the buffer
-        if (np >= 1 && !warp_wait(p_empty, (np - 1) & 1, a.err, 32)) { ok = false; break; }
-#pragma unroll
-        for (int c8 = 0; c8 < HALF / 8; ++c8) {
-          float p8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int c = c8 * 8 + e;
-            p8[e] = (all || (c >= lo && c <= hi)) ? exp2f(v[c] * a.c - m) : 0.0f;
-          }
-          // 16-byte chunk c8 of the row's 128-byte line in this half's panel, swizzled by the row
-          *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) * 16)) = pack_bf16x8(p8);
-        }
-        // the generic-proxy stores must be visible to the tensor core's reads
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
-        ++np;
       }
-    }
-    // out = O / l for the block's real rows: each half writes half of the head's columns
-    if (ok && warp_wait(o_full, 0, a.err, 32)) {
-      tc_fence_after();
-      constexpr int OC = DH / 2;
-      float o[OC];
+      // the row's valid keys among this thread's columns: lo .. hi; scores
+      // outside them become -inf (2^-inf = 0), only in the window's edge blocks
+      // (every lane takes the same path below: the warp-wide waits and TMEM
+      // accesses need the warp converged)
+      const int kp = kb0 + j * BKV + col0;
+      const int lo = max(max(0, qi - a.window + 1), kp) - kp;
+      const int hi = min(qi, kp + QK - 1) - kp;
+      if (hi < lo) {
 #pragma unroll
-      for (int c = 0; c < OC / 32; ++c)
-        tmem_ld32(tO + half * OC + c * 32 + lane_off, *reinterpret_cast<float(*)[32]>(o + 32 * c));
+        for (int c = 0; c < QK; ++c) v[c] = -INFINITY;
+      } else if (lo > 0 || hi < QK - 1) {
+#pragma unroll
+        for (int c = 0; c < QK; ++c)
+          if (c < lo || c > hi) v[c] = -INFINITY;
+      }
+      float bm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < QK; c += 8) {
+        bm4[0] = max3(bm4[0], v[c], v[c + 1]);
+        bm4[1] = max3(bm4[1], v[c + 2], v[c + 3]);
+        bm4[2] = max3(bm4[2], v[c + 4], v[c + 5]);
+        bm4[3] = max3(bm4[3], v[c + 6], v[c + 7]);
+      }
+      // this part's block maximum (base 2) to the row's other threads; the P
+      // buffer this block writes must have been read by the P V of block t - NPB
+      xch[(b * NPART + part) * BQ + r] = max3(bm4[0], bm4[1], fmaxf(bm4[2], bm4[3])) * a.c;
+      if (ok && t >= (uint32_t)NPB) ok = warp_wait(&p_empty[pb], ((t / NPB) - 1) & 1, a.err, 32);
+      if (!quad_all(quad, ok)) {
+        ok = false;
+        break;
+      }
+      const float* xr = xch + b * NPART * BQ + r;
+      float bm = xr[0];
+#pragma unroll
+      for (int q = 1; q < NPART; ++q) bm = fmaxf(bm, xr[q * BQ]);
+      // raise the running maximum only by more than TAU: rescale l and O (the
+      // partial output this thread owns) by 2^(m_old - m_new); all threads of
+      // a row decide alike
+      const bool raise = bm > m + TAU;
+      const bool rescale = raise && m > -INFINITY;
+      const float alpha = rescale ? ex2(m - bm) : 1.0f;
+      if (raise) {
+        l *= alpha;
+        m = bm;
+      }
+      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
+        // O must hold block t - 1's P V first (with one P buffer the wait
+        // above has already covered it)
+        if (NPB > 1) ok = warp_wait(&p_empty[(t - 1) % NPB], ((t - 1) / NPB) & 1, a.err, 32);
+        if (ok) {
+          tc_fence_after();
+          float o[OC];
+          tmem_ldn<OC>(tO + part * OC + lane_off, o);
+#pragma unroll
+          for (int e = 0; e < OC; ++e) o[e] *= alpha;
+          tmem_stn<OC>(tO + part * OC + lane_off, o);
+          tc_fence_before();
+        }
+      }
+      // P = 2^(S c - m): scale and sum in pairs on the FMA pipe; EMU_PAIRS of
+      // every four pairs through the polynomial, the rest through the MUFU unit
+      const f2 c2 = f2make(a.c, a.c);
+      const float nmv = m > -INFINITY ? -m : 0.0f;   // no valid key yet: every P is 2^-inf = 0
+      const f2 nm2 = f2make(nmv, nmv);
+      f2 se2[2] = {f2make(0.0f, 0.0f), f2make(0.0f, 0.0f)};
+      float pw[QK / 2];                          // packed bf16 pairs (even key in the low half), as raw bits
+#pragma unroll
+      for (int c8 = 0; c8 < QK / 8; ++c8) {
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          f2 x = f2fma(f2make(v[c8 * 8 + e], v[c8 * 8 + e + 1]), c2, nm2);
+          float x0, x1;
+          f2split(x, x0, x1);
+          if (e / 2 < EMU_PAIRS) {
+            ex2_poly2(x0, x1);
+          } else {
+            x0 = ex2(x0);
+            x1 = ex2(x1);
+          }
+          se2[(e >> 1) & 1] = f2add(se2[(e >> 1) & 1], f2make(x0, x1));
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(x0, x1);
+          pw[c8 * 4 + e / 2] = *reinterpret_cast<const float*>(&pr);
+        }
+      }
+      // this thread's keys part * QK .. + QK - 1 are P columns part * QK / 2 ..
+      tmem_stn<QK / 2>(tmem + L::T_P + pb * (BKV / 2) + part * (QK / 2) + lane_off, pw);
+      {
+        float s0, s1, s2, s3;
+        f2split(se2[0], s0, s1);
+        f2split(se2[1], s2, s3);
+        l += (s0 + s1) + (s2 + s3);
+      }
+      // the TMEM stores are complete (tcgen05.wait::st) before the MMA issuer
+      // learns of them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[pb]);
+    }
+    // out = O / (l over the row's NPART threads) for the block's real rows
+    float* lx = xch + 2 * NPART * BQ;
+    lx[part * BQ + r] = l;
+    const bool fin = quad_all(quad, ok && warp_wait(o_full, 0, a.err, 32));
+    if (fin) {
+      float lt = lx[r];
+#pragma unroll
+      for (int q = 1; q < NPART; ++q) lt += lx[q * BQ + r];
+      tc_fence_after();
+      float o[OC];
+      tmem_ldn<OC>(tO + part * OC + lane_off, o);
       if (qi < a.rows) {
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
 #pragma unroll
         for (int e = 0; e < OC; ++e) o[e] *= inv;
-        bf16* dst = a.out + ((long long)seq * a.L + a.pad + qi) * a.d + hc + half * OC;
+        bf16* dst = a.out + ((long long)seq * a.L + a.pad + qi) * a.d + hc + part * OC;
 #pragma unroll
         for (int c8 = 0; c8 < OC / 8; ++c8) *reinterpret_cast<uint4*>(dst + 8 * c8) = pack_bf16x8(o + 8 * c8);
       }

@@ -35,7 +35,9 @@
 // descriptor's leading/stride byte offsets walk them.
 //
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on timeout the
-// waiting thread records a code in the error word and the CTA unwinds.
+// waiting thread records a code in the error word and the CTA unwinds: the
+// producer waits (bounded) for its copies in flight, the MMA issuer for its
+// MMAs, and TMEM is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -213,7 +215,7 @@ struct Smem {
   static constexpr int STAGES = (MAX_DYN - OVERHEAD - STAGING) / STAGE_BYTES;
   static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = RING + STAGING;
-  static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 4) * 8 + 16 + NUM_EPI_WARPS * 4;
+  static constexpr int TOTAL = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + NUM_EPI_WARPS * 4;
   static constexpr int ALLOC = TOTAL + 1024;
   static_assert(STAGES >= 2, "ring too shallow");
   static_assert(ALLOC <= MAX_DYN, "shared memory over the per-block limit");
@@ -257,7 +259,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* accf = empty + STAGES;     // [2] accumulator ready (MMA -> epilogue)
   uint64_t* acce = accf + 2;           // [2] accumulator free (epilogue -> MMA)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  uint64_t* drain = acce + 2;          // the MMA issuer's wait for its own MMAs when it stops early
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -273,6 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&accf[b], 1);
       mbar_init(&acce[b], NUM_EPI_WARPS);
     }
+    mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -333,6 +337,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    // no copy may still be landing in shared memory when the CTA exits (the
+    // MMA issuer may have stopped early): wait, bounded, for each stage's last load
+    for (uint32_t q = kit > (uint32_t)STAGES ? kit - STAGES : 0; q < kit; ++q)
+      if (!mbar_wait(&full[q % STAGES], (q / STAGES) & 1, err, 8)) break;
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = umma_idesc(BM, BN, A_MN, B_MN);
@@ -344,7 +352,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kb_lo = w.ks * kper;
       const int nk = min(nkb, kb_lo + kper) - kb_lo;
       const int ab = i & 1, use = i >> 1;
-      if (use >= 1 && !mbar_wait(&acce[ab], (use - 1) & 1, err, 16)) break;
+      if (use >= 1 && !mbar_wait(&acce[ab], (use - 1) & 1, err, 16)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(ab * BN);
       for (int kb = 0; kb < nk; ++kb, ++kit) {
@@ -374,6 +385,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_commit(&empty[s]);
       }
       umma_commit(&accf[ab]);
+    }
+    if (!ok) {
+      // stopped early: the MMAs already issued finish before TMEM is freed
+      umma_commit(drain);
+      mbar_wait(drain, 0, err, 16);
     }
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue

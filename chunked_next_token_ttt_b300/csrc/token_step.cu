@@ -262,6 +262,291 @@ __global__ void __launch_bounds__(kTokThreads) token_steps_kernel(TokenArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Register-resident form for the width-64, hidden-256, vocabulary-256 network:
+// W1 and W2 stay in registers for the whole stream (32 + 32 per thread), U in
+// shared memory.  Thread (warp w, lane l) owns rows i = 4 (l % 16) .. + 3 of
+// the width and columns j = 8 g .. + 7 of the hidden (and vocabulary)
+// dimension, g = 2 w + l / 16, of W1^T, W2 and U^T.  Products that reduce over
+// i (z = W1 h, logits = U y, da = W2^T dh) reduce over the 16 lanes of a
+// half-warp with a shuffle reduce-scatter that leaves one j per lane pair;
+// products that reduce over j (W2 a, U^T dlogits) reduce the lane halves by
+// one shuffle step and the 16 warps through shared memory, where warp 0 folds
+// the 64 results (with the RMSNorm and its backward).  Six block barriers per
+// token; both rank-one updates are applied in registers.
+constexpr int kRD = 64, kRF = 256, kRV = 256;
+constexpr int kRThreads = 512;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Sum of v[0..7] over the 16 lanes of the half-warp, scattered: the lane
+// returns the total of element ((l >> 3) & 1) * 4 + ((l >> 2) & 1) * 2 +
+// ((l >> 1) & 1); lanes l and l ^ 1 return the same element.
+__device__ __forceinline__ float half_reduce_scatter8(const float (&v)[8], int lane) {
+  float a[4], b[2];
+  const bool u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float send = u8 ? v[q] : v[q + 4], keep = u8 ? v[q + 4] : v[q];
+    a[q] = keep + __shfl_xor_sync(kFull, send, 8);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float send = u4 ? a[q] : a[q + 2], keep = u4 ? a[q + 2] : a[q];
+    b[q] = keep + __shfl_xor_sync(kFull, send, 4);
+  }
+  const float send = u2 ? b[0] : b[1], keep = u2 ? b[1] : b[0];
+  float c = keep + __shfl_xor_sync(kFull, send, 2);
+  return c + __shfl_xor_sync(kFull, c, 1);
+}
+
+// The inverse: every lane of the half-warp receives the 8 elements that
+// half_reduce_scatter8 spread over it, in order.
+__device__ __forceinline__ void half_all_gather8(float c, float (&v)[8], int lane) {
+  const bool u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+  const float o = __shfl_xor_sync(kFull, c, 2);
+  const float b0 = u2 ? o : c, b1 = u2 ? c : o;
+  const float o0 = __shfl_xor_sync(kFull, b0, 4), o1 = __shfl_xor_sync(kFull, b1, 4);
+  const float a[4] = {u4 ? o0 : b0, u4 ? o1 : b1, u4 ? b0 : o0, u4 ? b1 : o1};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float p = __shfl_xor_sync(kFull, a[q], 8);
+    v[q] = u8 ? p : a[q];
+    v[q + 4] = u8 ? a[q] : p;
+  }
+}
+
+struct RegSmem {
+  float U[kRV * kRD];     // [v][i]
+  float part[16 * kRD];   // per-warp partial sums over j of a width-64 vector
+  float y[kRD];
+  float dh[kRD];
+  float2 stat[16];        // per-warp (max, sum of exp) of the logits, then (|a|^2, |dz|^2)
+  float2 stat2[16];
+  float scal[4];          // rstd, |h|^2, |dh|^2
+};
+
+__global__ void __launch_bounds__(kRThreads, 1) token_steps_reg_kernel(TokenArgs a) {
+  pdl_wait();
+  pdl_launch();
+  extern __shared__ __align__(16) float sm_raw[];
+  RegSmem& S = *reinterpret_cast<RegSmem*>(sm_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, s = blockIdx.x;
+  const int li = lane & 15, hb = lane >> 4, g = warp * 2 + hb;
+  const int i0 = 4 * li, j0 = 8 * g;
+  const int qs = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+  const int js = j0 + qs;                      // the element this lane holds after a reduce-scatter
+  const bool uniq = (lane & 1) == 0;           // one lane of each pair counts it in block sums
+  const long long n = (long long)kRD * kRF;
+  const float* w1g = a.W32 + ((long long)a.slot_w1 * a.B + s) * n;   // W1 [F][D]
+  const float* w2g = a.W32 + ((long long)a.slot_w2 * a.B + s) * n;   // W2 [D][F]
+  float w1[4][8], w2[4][8];                    // w1[p][q] = W1[j0+q][i0+p], w2[p][q] = W2[i0+p][j0+q]
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 r = *reinterpret_cast<const float4*>(w1g + (long long)(j0 + q) * kRD + i0);
+    w1[0][q] = r.x; w1[1][q] = r.y; w1[2][q] = r.z; w1[3][q] = r.w;
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const float4 r0 = *reinterpret_cast<const float4*>(w2g + (long long)(i0 + p) * kRF + j0);
+    const float4 r1 = *reinterpret_cast<const float4*>(w2g + (long long)(i0 + p) * kRF + j0 + 4);
+    w2[p][0] = r0.x; w2[p][1] = r0.y; w2[p][2] = r0.z; w2[p][3] = r0.w;
+    w2[p][4] = r1.x; w2[p][5] = r1.y; w2[p][6] = r1.z; w2[p][7] = r1.w;
+  }
+  for (int e = tid; e < kRV * kRD / 4; e += kRThreads)
+    reinterpret_cast<float4*>(S.U)[e] = reinterpret_cast<const float4*>(a.U)[e];
+
+  const int32_t* tk = a.tok + (long long)s * a.tok_ld;
+  auto valid = [&](int x) {
+    if ((unsigned)x < (unsigned)kRV) return x;
+    if (tid == 0) atomicOr(a.err, 2);
+    return 0;
+  };
+  // token t's input row (four elements per thread; two more for warp 0's fold)
+  int x = a.T > 0 ? valid(tk[0]) : 0;
+  float4 hrow = *reinterpret_cast<const float4*>(a.E + (long long)x * kRD + i0);
+  float hw0 = 0.0f, hw1 = 0.0f;
+  if (warp == 0) {
+    hw0 = a.E[(long long)x * kRD + lane];
+    hw1 = a.E[(long long)x * kRD + 32 + lane];
+  }
+  __syncthreads();
+
+  for (int t = 0; t < a.T; ++t) {
+    const int tgt = valid(tk[t + 1]);
+    const bool take = !a.mask || a.mask[(long long)s * a.mask_ld + t];
+    const float h[4] = {hrow.x, hrow.y, hrow.z, hrow.w};
+    const float h0 = hw0, h1 = hw1;
+    // the next token's input row, loaded while this one runs
+    if (t + 1 < a.T) {
+      hrow = *reinterpret_cast<const float4*>(a.E + (long long)tgt * kRD + i0);
+      if (warp == 0) {
+        hw0 = a.E[(long long)tgt * kRD + lane];
+        hw1 = a.E[(long long)tgt * kRD + 32 + lane];
+      }
+    }
+    // ---- z = W1 h, a = GELU(z)
+    float zp[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) zp[q] = fmaf(w1[3][q], h[3], fmaf(w1[2][q], h[2], fmaf(w1[1][q], h[1], w1[0][q] * h[0])));
+    const float zs = half_reduce_scatter8(zp, lane);
+    const float as = gelu_f(zs), gs = gelu_grad_f(zs);
+    float av[8];
+    half_all_gather8(as, av, lane);
+    // ---- h2 = h + W2 a: partial sums over this thread's j, then the lane halves
+    float hp[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc = fmaf(w2[p][q], av[q], acc);
+      hp[p] = acc;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = hb ? hp[k] : hp[k + 2], keep = hb ? hp[k + 2] : hp[k];
+      S.part[warp * kRD + i0 + 2 * hb + k] = keep + __shfl_xor_sync(kFull, send, 16);
+    }
+    __syncthreads();                                             // 1
+    if (warp == 0) {
+      float v0 = h0, v1 = h1;
+#pragma unroll
+      for (int w = 0; w < 16; ++w) {
+        v0 += S.part[w * kRD + lane];
+        v1 += S.part[w * kRD + 32 + lane];
+      }
+      const float rstd = rsqrtf(warp_sum(v0 * v0 + v1 * v1) / kRD + a.eps);
+      S.y[lane] = v0 * rstd;
+      S.y[32 + lane] = v1 * rstd;
+      const float hh = warp_sum(h0 * h0 + h1 * h1);
+      if (lane == 0) {
+        S.scal[0] = rstd;
+        S.scal[1] = hh;
+      }
+    }
+    __syncthreads();                                             // 2
+    // ---- logits = U y (y = h2 rstd), scattered one per lane pair
+    const float4 y4 = *reinterpret_cast<const float4*>(S.y + i0);
+    float lp[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 u = *reinterpret_cast<const float4*>(S.U + (j0 + q) * kRD + i0);
+      lp[q] = fmaf(u.w, y4.w, fmaf(u.z, y4.z, fmaf(u.y, y4.y, u.x * y4.x)));
+    }
+    const float ls = half_reduce_scatter8(lp, lane);
+    {
+      const float mw = warp_max(ls);
+      const float sw = warp_sum(uniq ? expf(ls - mw) : 0.0f);
+      if (lane == 0) S.stat[warp] = make_float2(mw, sw);
+    }
+    __syncthreads();                                             // 3
+    float lse;
+    {
+      const float2 st = lane < 16 ? S.stat[lane] : make_float2(-FLT_MAX, 0.0f);
+      const float M = warp_max(st.x);
+      lse = M + logf(warp_sum(lane < 16 ? st.y * expf(st.x - M) : 0.0f));
+    }
+    if (uniq && js == tgt) a.losses[(long long)s * a.loss_ld + t] = lse - ls;
+    // Source Masking: a masked target is scored but takes no step (uniform per block)
+    if (!take) continue;
+    // ---- dy = U^T dlogits (dlogits = softmax - onehot)
+    float dl[8];
+    half_all_gather8(expf(ls - lse) - (js == tgt ? 1.0f : 0.0f), dl, lane);
+    float dp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 u = *reinterpret_cast<const float4*>(S.U + (j0 + q) * kRD + i0);
+      dp[0] = fmaf(u.x, dl[q], dp[0]);
+      dp[1] = fmaf(u.y, dl[q], dp[1]);
+      dp[2] = fmaf(u.z, dl[q], dp[2]);
+      dp[3] = fmaf(u.w, dl[q], dp[3]);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = hb ? dp[k] : dp[k + 2], keep = hb ? dp[k + 2] : dp[k];
+      S.part[warp * kRD + i0 + 2 * hb + k] = keep + __shfl_xor_sync(kFull, send, 16);
+    }
+    __syncthreads();                                             // 4
+    if (warp == 0) {
+      float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 16; ++w) {
+        d0 += S.part[w * kRD + lane];
+        d1 += S.part[w * kRD + 32 + lane];
+      }
+      const float rstd = S.scal[0];
+      const float y0 = S.y[lane], y1 = S.y[32 + lane];
+      const float myd = warp_sum(y0 * d0 + y1 * d1) / kRD;
+      const float e0 = rstd * (d0 - y0 * myd), e1 = rstd * (d1 - y1 * myd);
+      S.dh[lane] = e0;
+      S.dh[32 + lane] = e1;
+      const float dd = warp_sum(e0 * e0 + e1 * e1);
+      if (lane == 0) S.scal[2] = dd;
+    }
+    __syncthreads();                                             // 5
+    // ---- da = W2^T dh, dz = da GELU'(z); norms of the two outer products
+    const float4 dh4 = *reinterpret_cast<const float4*>(S.dh + i0);
+    float dap[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      dap[q] = fmaf(w2[3][q], dh4.w, fmaf(w2[2][q], dh4.z, fmaf(w2[1][q], dh4.y, w2[0][q] * dh4.x)));
+    const float dzs = half_reduce_scatter8(dap, lane) * gs;
+    {
+      const float aa = warp_sum(uniq ? as * as : 0.0f), zz = warp_sum(uniq ? dzs * dzs : 0.0f);
+      if (lane == 0) S.stat2[warp] = make_float2(aa, zz);
+    }
+    __syncthreads();                                             // 6
+    float aa, zz;
+    {
+      const float2 st = lane < 16 ? S.stat2[lane] : make_float2(0.0f, 0.0f);
+      aa = warp_sum(st.x);
+      zz = warp_sum(st.y);
+    }
+    // ||dW2||^2 + ||dW1||^2 = |dh|^2 |a|^2 + |dz|^2 |h|^2
+    const float norm = sqrtf(S.scal[2] * aa + zz * S.scal[1]);
+    float sc = 1.0f;
+    if (!isfinite(norm)) {
+      sc = 0.0f;
+      if (tid == 0) atomicOr(a.err, 1);
+    } else if (a.clip > 0.0f) {
+      sc = fminf(1.0f, a.clip / (norm + 1e-6f));
+    }
+    const float step = a.eta * sc;
+    float dz[8];
+    half_all_gather8(dzs, dz, lane);
+    const float sdh[4] = {step * dh4.x, step * dh4.y, step * dh4.z, step * dh4.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        w1[p][q] = fmaf(-step * dz[q], h[p], w1[p][q]);
+        w2[p][q] = fmaf(-sdh[p], av[q], w2[p][q]);
+      }
+    }
+  }
+
+  float* w1o = a.W32 + ((long long)a.slot_w1 * a.B + s) * n;
+  float* w2o = a.W32 + ((long long)a.slot_w2 * a.B + s) * n;
+  float* w1p = a.Wop + ((long long)a.slot_w1 * a.B + s) * n;
+  float* w2p = a.Wop + ((long long)a.slot_w2 * a.B + s) * n;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 r = make_float4(w1[0][q], w1[1][q], w1[2][q], w1[3][q]);
+    *reinterpret_cast<float4*>(w1o + (long long)(j0 + q) * kRD + i0) = r;
+    *reinterpret_cast<float4*>(w1p + (long long)(j0 + q) * kRD + i0) = r;
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const float4 r0 = make_float4(w2[p][0], w2[p][1], w2[p][2], w2[p][3]);
+    const float4 r1 = make_float4(w2[p][4], w2[p][5], w2[p][6], w2[p][7]);
+    *reinterpret_cast<float4*>(w2o + (long long)(i0 + p) * kRF + j0) = r0;
+    *reinterpret_cast<float4*>(w2o + (long long)(i0 + p) * kRF + j0 + 4) = r1;
+    *reinterpret_cast<float4*>(w2p + (long long)(i0 + p) * kRF + j0) = r0;
+    *reinterpret_cast<float4*>(w2p + (long long)(i0 + p) * kRF + j0 + 4) = r1;
+  }
+}
+
+bool token_steps_reg_shape(int d, int f, int V) { return d == kRD && f == kRF && V == kRV; }
+
 size_t token_smem_bytes(int d, int f, int V) {
   const size_t fl = (size_t)kRed + (size_t)f * (d + 1) + (size_t)d * (f + 1) + (size_t)V * (d + 1) + 5 * (size_t)d +
                     3 * (size_t)f + (size_t)V;
@@ -283,11 +568,18 @@ ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T
     return TTT_ERR_UNSUPPORTED;
   }
   if (B == 0 || T == 0) return TTT_OK;
-  const size_t smem = token_smem_bytes(d, f, V);
-  TTT_CUDA(ensure_dyn_smem((const void*)token_steps_kernel, smem));
   TokenArgs a{tok, tok_ld, T, mask, mask_ld, E, U, W32, Wop, slot_w1, slot_w2, B, losses, loss_ld, d, f, V, eps, eta,
               clip, err};
-  launch_pdl(token_steps_kernel, B, kTokThreads, smem, st, a);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(E) | reinterpret_cast<uintptr_t>(U) |
+                         reinterpret_cast<uintptr_t>(W32) | reinterpret_cast<uintptr_t>(Wop)) & 15) == 0;
+  if (token_steps_reg_shape(d, f, V) && aligned) {
+    TTT_CUDA(ensure_dyn_smem((const void*)token_steps_reg_kernel, sizeof(RegSmem)));
+    launch_pdl(token_steps_reg_kernel, B, kRThreads, sizeof(RegSmem), st, a);
+  } else {
+    const size_t smem = token_smem_bytes(d, f, V);
+    TTT_CUDA(ensure_dyn_smem((const void*)token_steps_kernel, smem));
+    launch_pdl(token_steps_kernel, B, kTokThreads, smem, st, a);
+  }
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

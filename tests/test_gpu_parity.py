@@ -49,6 +49,19 @@ def test_per_token_clipped_b1_both_paths(token_kernel):
     compare(wl, gpu, ref)
 
 
+@pytest.mark.parametrize("token_kernel", ["1", "0"], ids=["persistent", "general"])
+def test_per_token_clipped_b1_at_the_toy_widths(token_kernel):
+    """The toy's widths (d = 64, d_ff = 256, V = 256), where the persistent
+    kernel keeps W1 and W2 in registers, with a clip that binds on three
+    sequences: it matches the oracle, and so does the general chunk path."""
+    wl = C.TOY_BIGRAM.replace(B=3, T=300, clip=0.05, eta=0.2)
+    inp = make(wl)
+    gpu = run_gpu(wl, inp, options={"no_token_kernel": token_kernel == "0"})
+    ref = run_oracle(wl, inp)
+    assert max(max(st.norms) for st in ref["states"]) > wl.clip      # the clip binds
+    compare(wl, gpu, ref)
+
+
 def test_decode_after_persistent_per_token_prefill():
     """The persistent kernel writes the fast weights back: decoding continues
     from them (general path) and matches the oracle token by token."""
