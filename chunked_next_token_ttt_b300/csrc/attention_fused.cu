@@ -1,40 +1,37 @@
 // Fused sliding-window attention on the tensor cores (bf16 operands) for the
 // frozen blocks ("End-to-End TTT" review, Method: sliding-window attention of
 // window k keeps the current chunk's tokens visible before the update; 3.1:
-// attention stays frozen during TTT).  One CTA per (128-query block, head,
-// sequence); no score or probability block ever reaches global memory.
+// attention stays frozen during TTT).  No score or probability block ever
+// reaches global memory.
 //
-// One pass over the key blocks (128 keys each) the query block's window
-// reaches, online softmax: per block, S = Q K^T into TMEM (double-buffered,
-// so the next S is computed while the softmax works on the current one); the
-// softmax warps take the block's row maximum; the row's running maximum m is
-// raised only when the block's exceeds it by more than TAU (base 2), and
-// then the row's partial output O in TMEM and its sum l are rescaled by
-// 2^(m_old - m_new) before the block's P V is issued; P = 2^(S c - m) (at
-// most 2^TAU) goes to TMEM as packed bf16 pairs, and O += P V accumulates in
-// TMEM with P as the MMA's A operand read from TMEM (so P never touches
-// shared memory, whose bandwidth the K/V copies and the operand reads of both
-// products already share).  out = O / l.
+// One pass over the key blocks (128 keys each) a query tile's window reaches,
+// online softmax: per block, S = Q K^T into TMEM; the softmax threads take the
+// block's row maximum; the row's running maximum m is raised only when the
+// block's exceeds it by more than TAU (base 2), and then the row's partial
+// output O in TMEM and its sum l are rescaled by 2^(m_old - m_new) before the
+// block's P V is issued; P = 2^(S c - m) (at most 2^TAU) goes to TMEM as
+// packed bf16 pairs, and O += P V accumulates in TMEM with P as the MMA's A
+// operand read from TMEM (P never touches shared memory, whose bandwidth the
+// K/V copies and the operand reads already share).  out = O / l.
 //
-// P is double-buffered: the softmax of block t writes its P while the tensor
-// core still reads block t-1's; only a rescale waits for that P V.
+// Head width 64 (two::swa_fused2_kernel): two 128-query tiles per CTA, four
+// softmax warps per tile with one thread per query row over all 128 keys of a
+// block, S, P and O of each tile in TMEM, the K/V blocks shared by the tiles,
+// and the tensor core alternating between them so that one tile's products
+// overlap the other's softmax.
 //
-// Warps: 0 TMA producer (Q once; K and V per key block through a ring of
-// three slots for head width 64, two for 128), 1 TMEM allocator and MMA
-// issuer, 2..17 softmax and output: the four warps of TMEM lane quadrant q
-// (w % 4 == q) own query rows 32 q .. 32 q + 31, one thread per row in each
-// of four column parts (32 keys of a block, a quarter of the head's output
-// columns); the four threads of a row exchange their block maxima once per
-// block at a barrier of the quadrant's warps, which also carries their wait
-// verdicts, so they rescale alike and leave together.
+// Head width 128 (swa_fused_kernel<128>): one 128-query tile per CTA; S and P
+// double-buffered in TMEM; two softmax warps per TMEM lane quadrant, one
+// thread per row in each of two column halves (64 keys of a block, half of the
+// output columns), which exchange their block maxima once per block at a
+// barrier of the quadrant's warps that also carries their wait verdicts, so
+// they rescale alike and leave together.
 //
-// The exponentials: the MUFU unit does 16 per clock per SM, which at head
-// width 64 is slower than the tensor core's two 128 x 128 x 64 products per
-// block, so half of them run on the FMA pipe as a polynomial (ex2_poly2),
-// and the scale, subtract and sums run as two-wide f32x2 ops.
-// Every mbarrier wait is bounded (tc::mbar_wait); a timeout records a code in
-// the status word and the CTA unwinds: the producer waits (bounded) for its
-// copies in flight, the MMA issuer for its MMAs, and TMEM is freed.
+// Warps: 0 TMA producer (Q once; K and V per key block through a ring),
+// 1 TMEM allocator and MMA issuer, 2..9 softmax and output.  Every mbarrier
+// wait is bounded (tc::mbar_wait); a timeout records a code in the status word
+// and the CTA unwinds: the producer waits (bounded) for its copies in flight,
+// the MMA issuer for its MMAs, and TMEM is freed.
 #include "gemm_tc_kernel.cuh"
 #include "kernels.h"
 
@@ -58,8 +55,9 @@ constexpr float TAU = 8.0f;              // raise the running maximum only beyon
 template <int DH>
 struct Layout {
   static constexpr int NP = DH / 64;                       // 64-wide panels of a head
-  static constexpr int KST = DH == 64 ? 3 : 2;             // K/V ring slots
+  static constexpr int NSB = 2;                            // S buffers (in TMEM)
   static constexpr int NPB = 2;                            // P buffers (in TMEM)
+  static constexpr int KST = DH == 64 ? 3 : 2;             // K/V ring slots
   static constexpr int TILE = NP * PANEL_BYTES;            // a Q, K or V tile of 128 rows
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + TILE;               // [KST] K tiles
@@ -68,15 +66,15 @@ struct Layout {
   // block maxima, then [NPART][128 rows] sums
   static constexpr int X_OFF = V_OFF + KST * TILE;
   static constexpr int BAR_OFF = X_OFF + 3 * NPART * BQ * 4;
-  // q_full, kv_full[KST], kv_empty[KST], s_full[2], s_empty[2], p_full[NPB],
+  // q_full, kv_full[KST], kv_empty[KST], s_full[NSB], s_empty[NSB], p_full[NPB],
   // p_empty[NPB], o_full, drain; the TMEM slot
-  static constexpr int NBAR = 1 + 2 * KST + 4 + 2 * NPB + 2;
+  static constexpr int NBAR = 1 + 2 * KST + 2 * NSB + 2 * NPB + 2;
   static constexpr int TOTAL = BAR_OFF + NBAR * 8 + 16;
   static constexpr int ALLOC = TOTAL + 1024;               // room to align the base to 1024 bytes
-  // TMEM columns: S0 0..127, S1 128..255 (fp32), O 256..256+DH (fp32), then
-  // P0 and P1, 64 columns each (128 bf16 keys per row, two per column)
+  // TMEM columns: NSB S buffers of 128 (fp32), O of DH (fp32), then NPB P
+  // buffers of 64 (128 bf16 keys per row, two per column)
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t T_O = 2 * BKV;
+  static constexpr uint32_t T_O = NSB * BKV;
   static constexpr uint32_t T_P = T_O + DH;
   static_assert(T_P + NPB * BKV / 2 <= TMEM_COLS, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory over the per-block limit");
@@ -256,16 +254,16 @@ template <int DH>
 __global__ void __launch_bounds__(NTHREADS, 1)
     swa_fused_kernel(const __grid_constant__ CUtensorMap tm, const Args a, int nkb) {
   using L = Layout<DH>;
-  constexpr int KST = L::KST, NPB = L::NPB;
+  constexpr int KST = L::KST, NPB = L::NPB, NSB = L::NSB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + KST;
-  uint64_t* s_full = kv_empty + KST;       // [2]
-  uint64_t* s_empty = s_full + 2;          // [2]
-  uint64_t* p_full = s_empty + 2;          // [NPB]
+  uint64_t* s_full = kv_empty + KST;       // [NSB]
+  uint64_t* s_empty = s_full + NSB;        // [NSB]
+  uint64_t* p_full = s_empty + NSB;        // [NPB]
   uint64_t* p_empty = p_full + NPB;        // [NPB]
   uint64_t* o_full = p_empty + NPB;
   uint64_t* drain = o_full + 1;            // the MMA issuer's wait for its own MMAs when it stops early
@@ -287,7 +285,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NSB; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], NSW);
     }
@@ -367,10 +365,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t t = 0;               // blocks whose S is issued (ring use t, TMEM buffer t & 1)
     int prev = -1;                // ring slot of the block whose P V is still to issue
     for (int j = j_lo; j < nkb && ok; ++j, ++t) {
-      const int s = t % KST, b = t & 1;
+      const int s = t % KST, b = t % NSB;
       if (!mbar_wait(&kv_full[s], (t / KST) & 1, a.err, 16)) { ok = false; break; }
       // the softmax warps have read the S that last used TMEM buffer b
-      if (t >= 2 && !mbar_wait(&s_empty[b], ((t >> 1) - 1) & 1, a.err, 16)) { ok = false; break; }
+      if (t >= (uint32_t)NSB && !mbar_wait(&s_empty[b], ((t / NSB) - 1) & 1, a.err, 16)) { ok = false; break; }
       tc_fence_after();
       issue_s(s, b);
       umma_commit(&s_full[b]);
@@ -419,8 +417,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // failure is voted at the next quadrant barrier, where all NPART warps leave
     bool ok = true;
     for (int j = j_lo; j < nkb; ++j, ++t) {
-      const int b = t & 1, pb = t % NPB;
-      ok = ok && warp_wait(&s_full[b], (t >> 1) & 1, a.err, 32);
+      const int b = t % NSB, pb = t % NPB, xb = t & 1;
+      ok = ok && warp_wait(&s_full[b], (t / NSB) & 1, a.err, 32);
       float v[QK];
       if (ok) {
         tc_fence_after();
@@ -454,13 +452,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // this part's block maximum (base 2) to the row's other threads; the P
       // buffer this block writes must have been read by the P V of block t - NPB
-      xch[(b * NPART + part) * BQ + r] = max3(bm4[0], bm4[1], fmaxf(bm4[2], bm4[3])) * a.c;
+      xch[(xb * NPART + part) * BQ + r] = max3(bm4[0], bm4[1], fmaxf(bm4[2], bm4[3])) * a.c;
       if (ok && t >= (uint32_t)NPB) ok = warp_wait(&p_empty[pb], ((t / NPB) - 1) & 1, a.err, 32);
       if (!quad_all(quad, ok)) {
         ok = false;
         break;
       }
-      const float* xr = xch + b * NPART * BQ + r;
+      const float* xr = xch + xb * NPART * BQ + r;
       float bm = xr[0];
 #pragma unroll
       for (int q = 1; q < NPART; ++q) bm = fmaxf(bm, xr[q * BQ]);
@@ -557,6 +555,316 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Head width 64: two 128-query tiles per CTA (queries q0 .. q0 + 255), each
+// with its own four softmax warps (one thread per query row, all 128 keys of a
+// block) and its own S, P and O in TMEM (128 + 64 + 64 columns per tile, 512
+// in all).  The tiles share the K/V blocks: tile 1's window is tile 0's moved
+// on by one block, so every block but the two ends serves both.  The tensor
+// core alternates between the tiles, computing one tile's S or P V while the
+// other's softmax runs, and no softmax warp waits for another.
+namespace two {
+
+constexpr int NT = 2;                          // query tiles per CTA
+constexpr int NSW2 = 4 * NT;                   // softmax warps
+constexpr int NTHREADS2 = 64 + 32 * NSW2;
+constexpr int KST2 = 4;                        // K/V ring slots
+constexpr int DH2 = 64;
+constexpr int TILE2 = PANEL_BYTES;             // 128 rows x 64 bf16
+constexpr int Q_OFF2 = 0;                      // [NT] Q tiles
+constexpr int K_OFF2 = Q_OFF2 + NT * TILE2;    // [KST2] K tiles
+constexpr int V_OFF2 = K_OFF2 + KST2 * TILE2;  // [KST2] V tiles
+constexpr int BAR_OFF2 = V_OFF2 + KST2 * TILE2;
+// q_full, kv_full[KST2], kv_empty[KST2], s_full[NT], s_free[NT], p_full[NT],
+// p_free[NT], o_full[NT], drain; the TMEM slot
+constexpr int NBAR2 = 1 + 2 * KST2 + 5 * NT + 1;
+constexpr int ALLOC2 = BAR_OFF2 + NBAR2 * 8 + 16 + 1024;
+static_assert(ALLOC2 <= 232448, "shared memory over the per-block limit");
+// TMEM columns of tile t: S (fp32) at 128 t, O (fp32) at 256 + 64 t, P (bf16
+// pairs) at 384 + 64 t
+constexpr uint32_t TMEM_COLS2 = 512;
+__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 64u * t; }
+__device__ __forceinline__ uint32_t col_p(int t) { return 384u + 64u * t; }
+
+__global__ void __launch_bounds__(NTHREADS2, 1)
+    swa_fused2_kernel(const __grid_constant__ CUtensorMap tm, const Args a, int nkb) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF2);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + KST2;
+  uint64_t* s_full = kv_empty + KST2;      // [NT] S of the tile's current block is in TMEM
+  uint64_t* s_free = s_full + NT;          // [NT] the tile's softmax has read it
+  uint64_t* p_full = s_free + NT;          // [NT] the tile's P is in TMEM
+  uint64_t* p_free = p_full + NT;          // [NT] its P V is done (P free, O current)
+  uint64_t* o_full = p_free + NT;          // [NT] the tile's last P V is done
+  uint64_t* drain = o_full + NT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = blockIdx.x * (NT * BQ);
+  const int hc = blockIdx.y * DH2;
+  const int seq = blockIdx.z;
+  // union key block u holds positions kb0 + 128 u ..; tile t reads blocks
+  // ulo[t] .. nkb - 1 + t, the last ending at its last query q0 + 128 t + 127
+  const int kb0 = q0 + BQ - nkb * BKV;
+  const int ulo0 = (max(0, q0 - a.window + 1) - kb0) / BKV;
+  const int ulo1 = (max(0, q0 + BQ - a.window + 1) - kb0) / BKV;
+  const int nu = nkb + 1 - ulo0;           // union blocks the CTA reads, from ulo0
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < KST2; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 4);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&p_free[t], 1);
+      mbar_init(&o_full[t], 1);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS2)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Q | K | V were written by the projection GEMM before this kernel
+  pdl_wait();
+  pdl_launch();
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    mbar_expect_tx(q_full, NT * TILE2);
+    for (int t = 0; t < NT; ++t)
+      tma_load_3d(smem + Q_OFF2 + t * TILE2, &tm, q_full, hc, a.pad + q0 + BQ * t, seq);
+    uint32_t i = 0;
+    for (; i < (uint32_t)nu; ++i) {
+      const int s = i % KST2;
+      if (i >= (uint32_t)KST2 && !mbar_wait(&kv_empty[s], ((i / KST2) & 1) ^ 1, a.err, 8)) break;
+      const int ky = a.pad + kb0 + (ulo0 + (int)i) * BKV;   // may be negative: TMA fills zeros there
+      mbar_expect_tx(&kv_full[s], 2 * TILE2);
+      tma_load_3d(smem + K_OFF2 + s * TILE2, &tm, &kv_full[s], hc + a.d, ky, seq);
+      tma_load_3d(smem + V_OFF2 + s * TILE2, &tm, &kv_full[s], hc + 2 * a.d, ky, seq);
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    bool landed = mbar_wait(q_full, 0, a.err, 8);
+    for (uint32_t q = i > (uint32_t)KST2 ? i - KST2 : 0; q < i && landed; ++q)
+      landed = mbar_wait(&kv_full[q % KST2], (q / KST2) & 1, a.err, 8);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    constexpr uint32_t idS = umma_idesc(BQ, BKV, false, false);   // S = Q K^T: both operands K-major
+    constexpr uint32_t idO = umma_idesc(BQ, DH2, false, true);    // O += P V: P from TMEM, V MN-major
+    const int ulo[NT] = {ulo0, ulo1}, uhi[NT] = {nkb - 1, nkb};
+    bool ok = mbar_wait(q_full, 0, a.err, 16);
+    // step i: the S of union block ulo0 + i for each tile that reads it, then
+    // the P V of block ulo0 + i - 1 for each tile that read it
+    for (int i = 0; i <= nu && ok; ++i) {
+      const int u = ulo0 + i;
+      if (i < nu) {
+        if (!mbar_wait(&kv_full[i % KST2], (i / KST2) & 1, a.err, 16)) { ok = false; break; }
+        const uint32_t sk = smem_u32(smem + K_OFF2 + (i % KST2) * TILE2);
+        for (int t = 0; t < NT && ok; ++t) {
+          if (u < ulo[t] || u > uhi[t]) continue;
+          const int n = u - ulo[t];
+          // the tile's softmax has read its previous S
+          if (n >= 1 && !mbar_wait(&s_free[t], (n - 1) & 1, a.err, 16)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sq = smem_u32(smem + Q_OFF2 + t * TILE2);
+#pragma unroll
+          for (int kk = 0; kk < DH2 / 16; ++kk)
+            umma_bf16(tmem + col_s(t), umma_desc(sq + kk * 32, 16, 1024), umma_desc(sk + kk * 32, 16, 1024), idS,
+                      kk > 0 ? 1u : 0u);
+          umma_commit(&s_full[t]);
+        }
+        if (!ok) break;
+      }
+      if (i >= 1) {
+        const int up = u - 1;
+        const uint32_t sv = smem_u32(smem + V_OFF2 + ((i - 1) % KST2) * TILE2);
+        for (int t = 0; t < NT && ok; ++t) {
+          if (up < ulo[t] || up > uhi[t]) continue;
+          const int n = up - ulo[t];
+          if (!mbar_wait(&p_full[t], n & 1, a.err, 16)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk)
+            umma_bf16_tmem_a(tmem + col_o(t), tmem + col_p(t) + kk * 8, umma_desc(sv + kk * 2048, PANEL_BYTES, 1024),
+                             idO, (n > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&p_free[t]);
+          if (up == uhi[t]) umma_commit(&o_full[t]);
+        }
+        if (!ok) break;
+        umma_commit(&kv_empty[(i - 1) % KST2]);
+      }
+    }
+    if (!ok) {
+      // stopped early: the MMAs already issued finish before TMEM is freed
+      umma_commit(drain);
+      mbar_wait(drain, 0, a.err, 16);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------ softmax and output
+    const int t = (warp - 2) >> 2;             // query tile
+    const int quad = warp & 3;                 // TMEM lanes 32 quad .. + 31
+    const int r = quad * 32 + lane;            // query row of the tile
+    const int qi = q0 + BQ * t + r;            // its position in the sequence
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int u_lo = t ? ulo1 : ulo0, u_hi = nkb - 1 + t;
+    float m = -INFINITY;                       // the row's running maximum (base 2)
+    float l = 0.0f;                            // the row's sum of P
+    bool ok = true;
+    for (int u = u_lo; u <= u_hi; ++u) {
+      const int n = u - u_lo;
+      ok = warp_wait(&s_full[t], n & 1, a.err, 32);
+      if (!ok) break;
+      // the row's valid keys lo .. hi of the block; the rest become -inf
+      // (2^-inf = 0), only in the window's edge blocks
+      const int kp = kb0 + u * BKV;
+      const int lo = max(max(0, qi - a.window + 1), kp) - kp;
+      const int hi = min(qi, kp + BKV - 1) - kp;
+      const bool edge = lo > 0 || hi < BKV - 1;
+      auto load_s = [&](int c, float (&v)[32]) {
+        tmem_ld32(tmem + col_s(t) + 32 * c + lane_off, v);
+        if (edge) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e < lo || 32 * c + e > hi) v[e] = -INFINITY;
+        }
+      };
+      // pass 1: the block's row maximum, 32 columns at a time
+      tc_fence_after();
+      float bm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c) {
+        float v[32];
+        load_s(c, v);
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          bm4[0] = max3(bm4[0], v[e], v[e + 1]);
+          bm4[1] = max3(bm4[1], v[e + 2], v[e + 3]);
+          bm4[2] = max3(bm4[2], v[e + 4], v[e + 5]);
+          bm4[3] = max3(bm4[3], v[e + 6], v[e + 7]);
+        }
+      }
+      const float bm = max3(bm4[0], bm4[1], fmaxf(bm4[2], bm4[3])) * a.c;
+      // raise the running maximum only by more than TAU; then l and O are
+      // rescaled by 2^(m_old - m_new)
+      const bool raise = bm > m + TAU;
+      const bool rescale = raise && m > -INFINITY;
+      const float alpha = rescale ? ex2(m - bm) : 1.0f;
+      if (raise) {
+        l *= alpha;
+        m = bm;
+      }
+      // the tile's previous P V is done: P is free and O holds it
+      if (n >= 1) {
+        ok = warp_wait(&p_free[t], (n - 1) & 1, a.err, 32);
+        if (!ok) break;
+        if (__any_sync(0xffffffffu, rescale)) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < DH2 / 32; ++c) {
+            float o[32];
+            tmem_ld32(tmem + col_o(t) + 32 * c + lane_off, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tmem + col_o(t) + 32 * c + lane_off, o);
+          }
+        }
+      }
+      // pass 2: P = 2^(S c - m), scale and sums in pairs on the FMA pipe;
+      // packed bf16 pairs (even key in the low half) to the tile's P columns.
+      // S is released once its last columns are read.
+      const f2 c2 = f2make(a.c, a.c);
+      const float nmv = m > -INFINITY ? -m : 0.0f;   // no valid key yet: every P is 2^-inf = 0
+      const f2 nm2 = f2make(nmv, nmv);
+      f2 se2[2] = {f2make(0.0f, 0.0f), f2make(0.0f, 0.0f)};
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c) {
+        float v[32];
+        load_s(c, v);
+        if (c == BKV / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[t]);
+        }
+        float pw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const f2 x = f2fma(f2make(v[e], v[e + 1]), c2, nm2);
+          float x0, x1;
+          f2split(x, x0, x1);
+          if ((e / 2) % 4 < EMU_PAIRS) {
+            ex2_poly2(x0, x1);
+          } else {
+            x0 = ex2(x0);
+            x1 = ex2(x1);
+          }
+          se2[(e >> 1) & 1] = f2add(se2[(e >> 1) & 1], f2make(x0, x1));
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(x0, x1);
+          pw[e / 2] = *reinterpret_cast<const float*>(&pr);
+        }
+        tmem_st16(tmem + col_p(t) + 16 * c + lane_off, pw);
+      }
+      {
+        float s0, s1, s2, s3;
+        f2split(se2[0], s0, s1);
+        f2split(se2[1], s2, s3);
+        l += (s0 + s1) + (s2 + s3);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
+    }
+    // out = O / l for the tile's real rows
+    if (ok && warp_wait(&o_full[t], 0, a.err, 32)) {
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      bf16* dst = a.out + ((long long)seq * a.L + a.pad + qi) * a.d + hc;
+#pragma unroll
+      for (int c = 0; c < DH2 / 32; ++c) {
+        float o[32];
+        tmem_ld32(tmem + col_o(t) + 32 * c + lane_off, o);
+        if (qi < a.rows) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= inv;
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) *reinterpret_cast<uint4*>(dst + 32 * c + 8 * c8) = pack_bf16x8(o + 8 * c8);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS2) : "memory");
+  }
+}
+
+ttt_status launch(const CUtensorMap& tm, const Args& a, int rows, int H, int B, int nkb, cudaStream_t st) {
+  TTT_CUDA(ensure_dyn_smem((const void*)swa_fused2_kernel, ALLOC2));
+  launch_pdl(swa_fused2_kernel, dim3(ceil_div(rows, NT * BQ), H, B), NTHREADS2, ALLOC2, st, tm, a, nkb);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+}  // namespace two
+
 template <int DH>
 ttt_status launch_dh(const CUtensorMap& tm, const Args& a, int nqb, int H, int B, int nkb, cudaStream_t st) {
   using L = Layout<DH>;
@@ -595,7 +903,7 @@ ttt_status launch_swa_fused(int B, int rows, int H, int dh, int window, const vo
   a.err = err;
   const int nqb = ceil_div(rows, fa::BQ);
   const int nkb = ceil_div((long long)window + fa::BQ - 1, fa::BKV);
-  if (dh == 64) return fa::launch_dh<64>(tm, a, nqb, H, B, nkb, st);
+  if (dh == 64) return fa::two::launch(tm, a, rows, H, B, nkb, st);
   return fa::launch_dh<128>(tm, a, nqb, H, B, nkb, st);
 }
 
