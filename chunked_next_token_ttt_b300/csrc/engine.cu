@@ -731,6 +731,58 @@ static ttt_status p_next_from_pending(ttt_handle* h, float* p_out, cudaStream_t 
   return TTT_OK;
 }
 
+// Decoding's next-token forward as the one persistent cooperative kernel when
+// the network and the GPU allow it (bf16 storage, GELU or SwiGLU blocks, no
+// attention or extra frozen MLPs, B <= 8): token from the fixed slot x_dev,
+// writes logits32, p_dev and lse_next like the graph below.  Returns false
+// (nothing launched) when it does not apply.
+static bool decode_persist_applies(ttt_handle* h) {
+  if (h->dp_grid < 0) {
+    h->dp_grid = 0;
+    if (!h->opt.no_decode_persist && h->stg == ST_BF16 && h->dm.attn_heads == 0 && !h->dm.static_mlp &&
+        h->B <= 8 && h->n_pre + h->dm.n_fast <= kDecodeMaxBlocks)
+      h->dp_grid = decode_persist_grid(h->B, h->d, h->f);
+  }
+  return h->dp_grid > 0;
+}
+
+static ttt_status decode_persist(ttt_handle* h, cudaStream_t st) {
+  DecodeNet& n = h->dp_net;
+  if (!h->dp_x32) {
+    TTT_TRY(dalloc(h, &h->dp_x32, (size_t)2 * h->B * h->d * 4));
+    TTT_TRY(dalloc(h, &h->dp_px, (size_t)2 * 8 * h->B * h->d * 4));
+    TTT_TRY(dalloc(h, &h->dp_act, (size_t)h->B * h->f * 2));
+    TTT_TRY(dalloc(h, &h->dp_part, (size_t)h->dp_grid * h->B * sizeof(float2)));
+    TTT_TRY(dalloc(h, &h->dp_bar, 4 * sizeof(unsigned)));
+    const int B = h->B, nm = h->nm;
+    n.B = B; n.d = h->d; n.f = h->f; n.V = h->V;
+    n.swiglu = h->dm.block_kind == TTT_BLOCK_GELU ? 0 : 1;
+    n.n_pre = h->n_pre; n.n_fast = h->dm.n_fast;
+    n.eps = h->dm.rms_eps;
+    n.tok = h->x_dev;
+    n.E = h->E;
+    for (int p = 0; p < h->n_pre; ++p)
+      for (int k = 0; k < nm; ++k) n.pre[p][k] = h->prefix[(size_t)p * nm + k].p;
+    for (int l = 0; l < h->dm.n_fast; ++l) {
+      if (n.swiglu) {
+        n.ffrozen[l][0] = h->fastfrozen[(size_t)l * nm + 0].p;
+        n.ffrozen[l][1] = h->fastfrozen[(size_t)l * nm + 1].p;
+      } else {
+        n.fup[l] = op_at(h, h->Wop, (long long)h->slot_of[(size_t)l * nm + 0] * B * h->n).p;
+      }
+      n.fdown[l] = op_at(h, h->Wop, (long long)h->slot_of[(size_t)l * nm + (nm - 1)] * B * h->n).p;
+    }
+    n.n = h->n;
+    n.U = h->U.p;
+    n.x32 = h->dp_x32; n.px = h->dp_px; n.act = h->dp_act;
+    n.logits = h->logits32; n.p = h->p_dev; n.lse = h->lse_next;
+    n.part = h->dp_part; n.bar = h->dp_bar; n.err = h->flag;
+  }
+  TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_decode_persist(n, h->dp_grid, st); }));
+  h->next_valid = true;
+  return TTT_OK;
+}
+
 // Decoding's next-token forward (embedding -> blocks -> head -> softmax of one
 // row per sequence, token from the fixed slot x_dev) as a CUDA graph: captured
 // on first use on the handle's own stream, then replayed after the caller's
@@ -1007,7 +1059,7 @@ ttt_status ttt_create_ex(const ttt_dims* dims, const ttt_hparams* hp, const ttt_
   *out = nullptr;
   const ttt_options O = opt ? *opt : ttt_options{};
   if (O.no_pdl < 0 || O.no_decode_graph < 0 || O.fp32_simt < 0 || O.hoist_chunks < 0 || O.no_token_kernel < 0 ||
-      O.max_ctas < 0 || O.no_dw_stream < 0 || O.attn_unfused < 0)
+      O.max_ctas < 0 || O.no_dw_stream < 0 || O.attn_unfused < 0 || O.no_decode_persist < 0)
     return fail(TTT_ERR_BAD_ARG, "negative ttt_options field");
   PdlScope pdl(!O.no_pdl);
   const ttt_dims& D = *dims;
@@ -1489,7 +1541,13 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   // attention: x_new's position (the decoding attention appends its K and V there)
   if (attn) TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_pos_add(h->dec_pos, st); }));
   const bool dev = is_device_ptr(p_next);
-  if (!h->opt.no_decode_graph) {
+  if (decode_persist_applies(h)) {
+    TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4,
+                             x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+    TTT_TRY(decode_persist(h, st));
+    TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4,
+                             dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, st));
+  } else if (!h->opt.no_decode_graph) {
     // the newest token into the fixed slot the captured forward reads
     TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4,
                              x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));

@@ -140,6 +140,14 @@ struct ttt_handle {
   cudaEvent_t gev[2] = {nullptr, nullptr};
   cudaGraphExec_t dec_exec = nullptr;
   long long dec_kernels = 0;
+  // or as one persistent cooperative kernel (dp_grid: -1 not yet decided, 0 not used)
+  int dp_grid = -1;
+  ttt::DecodeNet dp_net;
+  float* dp_x32 = nullptr;
+  float* dp_px = nullptr;
+  void* dp_act = nullptr;
+  float2* dp_part = nullptr;
+  unsigned* dp_bar = nullptr;
   float* Lc = nullptr;
   float* Lw = nullptr;
 

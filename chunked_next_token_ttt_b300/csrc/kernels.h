@@ -130,6 +130,38 @@ ttt_status launch_token_steps(int B, const int32_t* tok, long long tok_ld, int T
                               float* W32, float* Wop, int slot_w1, int slot_w2, float* losses, long long loss_ld,
                               int d, int f, int V, float eps, float eta, float clip, int* err, cudaStream_t st);
 
+// Decoding's next-token forward as one persistent cooperative kernel
+// (decode_persist.cu): bf16 storage, GELU or SwiGLU blocks, no attention or
+// extra frozen MLPs, B <= 8.  Weight pointers are bf16 [N][K] row-major (the
+// GEMM's K-major B operand); the per-sequence fast weights of sequence s sit
+// at the given pointer + s * n.
+constexpr int kDecodeMaxBlocks = 48;
+struct DecodeNet {
+  int B = 0, d = 0, f = 0, V = 0, swiglu = 0, n_pre = 0, n_fast = 0;
+  float eps = 0.0f;
+  const int32_t* tok = nullptr;               // [B] the new inputs
+  const void* E = nullptr;                     // [V][d]
+  const void* pre[kDecodeMaxBlocks][3] = {};   // frozen prefix blocks: up (gate), up (SwiGLU), down
+  const void* ffrozen[kDecodeMaxBlocks][2] = {};   // SwiGLU fast blocks: frozen gate and up
+  const void* fup[kDecodeMaxBlocks] = {};      // GELU fast blocks: W1 of sequence 0
+  const void* fdown[kDecodeMaxBlocks] = {};    // fast down projection of sequence 0
+  long long n = 0;                             // per-sequence stride of the fast weights
+  const void* U = nullptr;                     // [V][d]
+  float* x32 = nullptr;                        // [2][B][d] residual stream, by block parity
+  float* px = nullptr;                         // [2][8][B][d] down-projection partial sums over K segments
+  void* act = nullptr;                         // [B][f] bf16 activations
+  float* logits = nullptr;                     // [B][V] out
+  float* p = nullptr;                          // [B][V] out: softmax
+  float* lse = nullptr;                        // [B] out
+  float2* part = nullptr;                      // [grid][B] per-CTA softmax states
+  unsigned* bar = nullptr;                     // [4] grid barrier state (zeroed before each launch)
+  int* err = nullptr;
+};
+// The grid the launch uses (one CTA per SM) and whether this GPU can hold it;
+// 0 when the shapes or the GPU do not allow the persistent kernel.
+int decode_persist_grid(int B, int d, int f);
+ttt_status launch_decode_persist(const DecodeNet& net, int grid, cudaStream_t st);
+
 // Sliding-window attention of the frozen blocks (attention.cu): for B
 // sequences of `rows` positions, qkv [B][rows][3d] fp32 (Q | K | V of each
 // row, d = H * dh), out [B][rows][d] in operand type: per head,

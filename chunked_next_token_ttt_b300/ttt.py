@@ -47,7 +47,7 @@ class Options(ctypes.Structure):
     """ttt_options: zero fields are the library's defaults."""
     _fields_ = [("no_pdl", ctypes.c_int), ("no_decode_graph", ctypes.c_int), ("fp32_simt", ctypes.c_int),
                 ("hoist_chunks", ctypes.c_int), ("no_token_kernel", ctypes.c_int), ("max_ctas", ctypes.c_int),
-                ("no_dw_stream", ctypes.c_int), ("attn_unfused", ctypes.c_int)]
+                ("no_dw_stream", ctypes.c_int), ("attn_unfused", ctypes.c_int), ("no_decode_persist", ctypes.c_int)]
 
 
 class Weights(ctypes.Structure):

@@ -175,6 +175,10 @@ typedef struct {
   int attn_unfused;    /* 1: bf16 sliding-window attention runs as score GEMM,
                           windowed softmax and P V GEMM per head instead of the
                           fused kernel that keeps scores on chip             */
+  int no_decode_persist; /* 1: ttt_decode_step's next-token forward never runs as
+                          the one persistent cooperative kernel (bf16 storage,
+                          no attention or extra frozen MLPs, B <= 8), but as
+                          the captured graph (or launch by launch)           */
 } ttt_options;
 
 /* Validate dims/hparams, allocate every device buffer the handle needs for

@@ -203,6 +203,56 @@ def test_decode_swiglu_bf16_steps_with_the_per_call_prefix():
         assert rel <= 3e-2
 
 
+@pytest.mark.parametrize("block", ["gelu", "swiglu"])
+def test_decode_persistent_kernel_against_the_graph_and_the_oracle(block):
+    """Decoding's next-token forward as the one persistent cooperative kernel
+    (bf16, eight sequences for GELU, a decode that crosses a chunk step) against
+    the captured-graph path launch for launch and against the oracle; the
+    persistent path is the one that ran (one more logged launch per step)."""
+    if block == "gelu":
+        wl = C.E2E_125M.replace(d=128, d_ff=512, vocab=1000, chunk=32, B=8, T=2 * 32 + 5, n_prefix=2, n_fast=2)
+    else:
+        wl = C.INPLACE_4B.replace(d=256, d_ff=640, vocab=3000, chunk=32, B=1, T=32 + 7, n_prefix=2)
+    inp = make(wl)
+    extra = 40
+    long_tok = synth.sample_stream(inp["chain"], wl.seed_id, wl.B, wl.T + extra)
+    tok = np.ascontiguousarray(long_tok[:, :wl.T + 1])
+    runs = {}
+    for name, opt in (("persist", {}), ("graph", {"no_decode_persist": 1})):
+        gpu = run_gpu(wl, inp, tokens=tok, options=opt)
+        h = gpu["handle"]
+        p = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+        loss = torch.empty((wl.B,), dtype=torch.float32, device="cuda")
+        ps, ls, logged = [], [], []
+        for t in range(wl.T + 1, wl.T + extra + 1):
+            h.launch_log_enable(True)
+            h.decode_step(torch.from_numpy(long_tok[:, t].copy()).cuda(), p, loss)
+            torch.cuda.synchronize()
+            logged.append(len(h.launch_log()))
+            h.launch_log_enable(False)
+            ps.append(p.cpu().numpy().copy())
+            ls.append(loss.cpu().numpy().copy())
+        runs[name] = (np.array(ps), np.array(ls), logged, h)
+    (pp, lp, np_, hp), (pg, lg, ng, hg) = runs["persist"], runs["graph"]
+    # the same forward up to summation order (bf16 operands, fp32 accumulation)
+    assert np.abs(pp - pg).sum(axis=-1).max() <= 2e-2
+    assert np.abs(lp - lg).max() <= 2e-2
+    steps_without_update = [i for i in range(extra) if np_[i] == ng[i] + 1]
+    assert len(steps_without_update) >= extra - 3, (np_, ng)
+    net = oracle.Net.from_weights(inp["weights"], wl.block, wl.fast_mats, wl.rms_eps)
+    ref = oracle.prefill(net, wl.eta, wl.clip, wl.chunk, tok)
+    errs = []
+    for i, t in enumerate(range(wl.T + 1, wl.T + extra + 1)):
+        for s in range(wl.B):
+            l_ref, p_ref = oracle.decode_step(net, ref["states"][s], long_tok[s, t], wl.eta, wl.clip, wl.chunk)
+            errs.append(abs(float(lp[i, s]) - l_ref))
+            assert np.abs(pp[i, s] - p_ref).sum() <= 5e-2
+    assert np.mean(errs) <= TOL_BF16_LOSS_MEAN
+    for s in range(wl.B):
+        rel = oracle.weights_rel_frobenius(hp.fast_weights(s), ref["states"][s].W, wl.fast_mats)
+        assert rel <= 3e-2
+
+
 def test_settle_entry_point_after_prefill():
     """ttt_settle on its own, after a prefill of 3 chunks whose 2nd chunk ended
     with an in-prefill event: the candidate is the 3rd chunk's update; A and the
