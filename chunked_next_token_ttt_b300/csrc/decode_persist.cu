@@ -153,13 +153,15 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[kSeq], int lan
 
 // acc[i][q][s] += W_q(row i) . xs[s] over K for R rows of NW weight matrices
 // shared by the sequences (a null row contributes nothing) and nb sequences of
-// fp32 operand rows xs[s * ld ..] in shared memory.  Lanes take 8-element
+// fp32 operand rows in shared memory in the split layout of stage_fold (piece
+// c of sequence s: elements 0..3 at xs[s * ld8 + c], 4..7 at xs[half + ...],
+// so that lanes reading consecutive pieces hit distinct banks).  Lanes take 8-element
 // pieces; every weight piece of a batch of CB pieces per lane is loaded before
 // any is used (R * NW * CB 16-byte loads in flight per lane), and each piece is
 // unpacked once for all sequences.
 template <int R, int NW, int CB>
-__device__ __forceinline__ void dots_shared(const bf16* const (&w)[R][NW], const float* xs, int K, int ld, int nb,
-                                            float (&acc)[R][NW][kSeq], int lane) {
+__device__ __forceinline__ void dots_shared(const bf16* const (&w)[R][NW], const float4* xs, int half, int K, int ld8,
+                                            int nb, float (&acc)[R][NW][kSeq], int lane) {
   const int K8 = K / 8;
   f2 acc2[R][NW][kSeq];
 #pragma unroll
@@ -190,8 +192,8 @@ __device__ __forceinline__ void dots_shared(const bf16* const (&w)[R][NW], const
 #pragma unroll
       for (int s = 0; s < kSeq; ++s) {
         if (s < nb) {
-          const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(xs + (long long)s * ld) + 2 * c;
-          const ulonglong2 x0 = xp[0], x1 = xp[1];
+          const ulonglong2 x0 = *reinterpret_cast<const ulonglong2*>(xs + s * ld8 + c);
+          const ulonglong2 x1 = *reinterpret_cast<const ulonglong2*>(xs + half + s * ld8 + c);
           const f2 xf[4] = {x0.x, x0.y, x1.x, x1.y};
 #pragma unroll
           for (int i = 0; i < R; ++i)
@@ -215,17 +217,17 @@ __device__ __forceinline__ void dots_shared(const bf16* const (&w)[R][NW], const
 }
 
 // acc[s] += W_s(row) . xs[s] over K where sequence s has its own weight row at
-// w0 + s * wseq (the fast weights), nb sequences; loads batched as above.
-template <int CB>
-__device__ __forceinline__ void dots_per_seq(const bf16* w0, long long wseq, const float* xs, int K, int ld, int nb,
-                                             float (&acc)[kSeq], int lane) {
+// w0 + s * wseq (the fast weights), nb <= NS sequences; loads batched as above.
+template <int NS, int CB>
+__device__ __forceinline__ void dots_per_seq(const bf16* w0, long long wseq, const float4* xs, int half, int K,
+                                             int ld8, int nb, float (&acc)[kSeq], int lane) {
   const int K8 = K / 8;
   for (int c0 = lane; c0 < K8; c0 += 32 * CB) {
-    uint4 wv[CB][kSeq];
+    uint4 wv[CB][NS];
 #pragma unroll
     for (int b = 0; b < CB; ++b)
 #pragma unroll
-      for (int s = 0; s < kSeq; ++s)
+      for (int s = 0; s < NS; ++s)
         wv[b][s] = (c0 + 32 * b < K8 && s < nb) ? __ldg(reinterpret_cast<const uint4*>(w0 + s * wseq) + c0 + 32 * b)
                                                 : make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -233,10 +235,9 @@ __device__ __forceinline__ void dots_per_seq(const bf16* w0, long long wseq, con
       const int c = c0 + 32 * b;
       if (c >= K8) break;
 #pragma unroll
-      for (int s = 0; s < kSeq; ++s) {
+      for (int s = 0; s < NS; ++s) {
         if (s < nb) {
-          const float4 x0 = reinterpret_cast<const float4*>(xs + (long long)s * ld)[2 * c];
-          const float4 x1 = reinterpret_cast<const float4*>(xs + (long long)s * ld)[2 * c + 1];
+          const float4 x0 = xs[s * ld8 + c], x1 = xs[half + s * ld8 + c];
           const float xf[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           float wf[8];
           bf8(wv[b][s], wf);
@@ -256,8 +257,13 @@ __device__ __forceinline__ void dots_per_seq(const bf16* w0, long long wseq, con
 // operand copies of the launch-by-launch path.  When xout is given, this CTA
 // also stores its share of x there (16-byte groups g with g % gridDim.x ==
 // blockIdx.x), so that every element is written once.
+// Element e of the split layout (piece e / 8, half (e / 4) % 2, lane e % 4).
+__device__ __forceinline__ float& xs_at(float4* xs, int half, int e) {
+  return reinterpret_cast<float*>(xs + (e >> 3) + ((e >> 2) & 1) * half)[e & 3];
+}
+
 __device__ __forceinline__ void stage_fold(const float* xin, const float* ps, int nseg, long long pstride,
-                                           float* xout, float* xs, int count, bool round) {
+                                           float* xout, float4* xs, int half, int count, bool round) {
   const float4* x4 = reinterpret_cast<const float4*>(xin);
   const int n4 = count / 4;
   for (int idx = threadIdx.x; idx < n4; idx += kThreads) {
@@ -283,10 +289,10 @@ __device__ __forceinline__ void stage_fold(const float* xin, const float* ps, in
       v.z = __bfloat162float(__float2bfloat16_rn(v.z));
       v.w = __bfloat162float(__float2bfloat16_rn(v.w));
     }
-    reinterpret_cast<float4*>(xs)[idx] = v;
+    xs[(idx >> 1) + (idx & 1) * half] = v;
   }
 }
-__device__ __forceinline__ void stage_bf16(const bf16* src, float* dst, int count) {
+__device__ __forceinline__ void stage_bf16(const bf16* src, float4* dst, int half, int count) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
   const int n8 = count / 8;
   for (int base = threadIdx.x; base < n8; base += 4 * kThreads) {
@@ -302,8 +308,8 @@ __device__ __forceinline__ void stage_bf16(const bf16* src, float* dst, int coun
       if (idx < n8) {
         float f8[8];
         bf8(v[u], f8);
-        reinterpret_cast<float4*>(dst)[2 * idx] = make_float4(f8[0], f8[1], f8[2], f8[3]);
-        reinterpret_cast<float4*>(dst)[2 * idx + 1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
+        dst[idx] = make_float4(f8[0], f8[1], f8[2], f8[3]);
+        dst[half + idx] = make_float4(f8[4], f8[5], f8[6], f8[7]);
       }
     }
   }
@@ -329,18 +335,13 @@ __device__ __forceinline__ void soft_join(float& m, float& s, float m2, float s2
   m = n;
 }
 
-// Start bringing `bytes` (a multiple of 16, 16-byte aligned) at p into L2.
-__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 constexpr int kRows = 2;       // rows a warp takes at once in the block projections
-constexpr int kHeadRows = 3;   // and in the LM head
+constexpr int kHeadRows = 2;   // and in the LM head
 
 __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __grid_constant__ DecodeNet a) {
   extern __shared__ __align__(16) uint8_t smraw[];
   float* red = reinterpret_cast<float*>(smraw);                        // [kWarps][kSeq][2] reductions
-  float* xs = reinterpret_cast<float*>(smraw + kWarps * kSeq * 2 * 4);  // fp32 operand rows of the phase
+  float4* xs = reinterpret_cast<float4*>(smraw + kWarps * kSeq * 2 * 4);  // fp32 operand rows of the phase
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gw = blockIdx.x * kWarps + warp, GW = gridDim.x * kWarps;
   const int B = a.B, d = a.d, f = a.f, V = a.V;
@@ -356,52 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
       break;
     }
   // per-sequence weights: a unit takes half of the sequences when there are more than four
-  const int nh = B > 4 ? 2 : 1, hb = (B + nh - 1) / nh;
+  const int nh = B > 4 ? 2 : 1, hb = (B + nh - 1) / nh;    // hb <= 4 for B <= 8
   const int sl = f / nseg;
   const long long BD = (long long)B * d;
-  // The weight rows this warp reads in phase `ph` (2 l: block l's up
-  // projection, 2 l + 1: its down projection, 2 L: the head), prefetched into
-  // L2 before the barrier that precedes the phase so that their DRAM latency
-  // overlaps the wait.  Lanes take the rows in turn.
+  const int half = B * (d > f ? d : f) / 8;     // pieces of the operand buffer; split layout
+  const int d8 = d / 8, f8 = f / 8;
   const int L = a.n_pre + a.n_fast;
-  auto prefetch_phase = [&](int ph) {
-    int r = 0;      // rows of the warp's list, lane r % 32 takes row r
-    auto take = [&](const bf16* p, int K) {
-      if ((r++ & 31) == lane) prefetch_l2(p, (unsigned)K * 2);
-    };
-    if (ph < 2 * L) {
-      const int l = ph >> 1, lf = l - a.n_pre;
-      const bool fastb = l >= a.n_pre;
-      if ((ph & 1) == 0) {
-        for (int j = gw; j < f; j += GW) {
-          if (a.swiglu) {
-            take(static_cast<const bf16*>(fastb ? a.ffrozen[lf][0] : a.pre[l][0]) + (long long)j * d, d);
-            take(static_cast<const bf16*>(fastb ? a.ffrozen[lf][1] : a.pre[l][1]) + (long long)j * d, d);
-          } else if (fastb) {
-            // (the fast rows are taken by units of sequence groups below)
-          } else {
-            take(static_cast<const bf16*>(a.pre[l][0]) + (long long)j * d, d);
-          }
-        }
-        if (fastb && !a.swiglu)
-          for (int u = gw; u < f * nh; u += GW) {
-            const int j = u / nh, s0 = (u % nh) * hb, nb = min(hb, B - s0);
-            for (int s = s0; s < s0 + nb; ++s) take(static_cast<const bf16*>(a.fup[lf]) + s * a.n + (long long)j * d, d);
-          }
-      } else {
-        const bf16* w2 = static_cast<const bf16*>(fastb ? a.fdown[lf] : a.pre[l][a.swiglu ? 2 : 1]);
-        const int nhu = fastb ? nh : 1;
-        for (int u = gw; u < d * nseg * nhu; u += GW) {
-          const int i = u / (nseg * nhu), k = (u / nhu) % nseg;
-          const int s0 = (u % nhu) * hb, nb = fastb ? min(hb, B - s0) : 1;
-          const bf16* wrow = w2 + (long long)i * f + (long long)k * sl;
-          for (int s = s0; s < s0 + nb; ++s) take(wrow + s * a.n, sl);
-        }
-      }
-    } else {
-      for (int v = gw; v < V; v += GW) take(static_cast<const bf16*>(a.U) + (long long)v * d, d);
-    }
-  };
   unsigned gen = 0;
   pdl_wait();
 
@@ -415,7 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
     }
     a.x32[e] = __bfloat162float(static_cast<const bf16*>(a.E)[(long long)x * d + c]);
   }
-  prefetch_phase(0);
   if (!grid_sync(a.bar, gen, a.err)) return;
 
   bf16* act = static_cast<bf16*>(a.act);
@@ -426,10 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
     // (kept in x32[l & 1]); up projection: act[s][j] = GELU(W1 x) or
     // silu(Wg x) (Wu x), rows j over the grid's warps
     if (l == 0)
-      stage_fold(a.x32, nullptr, 0, 0, nullptr, xs, B * d, true);
+      stage_fold(a.x32, nullptr, 0, 0, nullptr, xs, half, B * d, true);
     else
       stage_fold(a.x32 + ((l - 1) & 1) * BD, a.px + ((l - 1) & 1) * 8 * BD, nseg, BD, a.x32 + (l & 1) * BD, xs,
-                 B * d, true);
+                 half, B * d, true);
     __syncthreads();
     if (fastb && !a.swiglu) {
       // the fast W1 of each sequence
@@ -437,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
       for (int u = gw; u < f * nh; u += GW) {
         const int j = u / nh, s0 = (u % nh) * hb, nb = min(hb, B - s0);
         float acc[kSeq] = {};
-        dots_per_seq<2>(w1 + s0 * a.n + (long long)j * d, a.n, xs + (long long)s0 * d, d, d, nb, acc, lane);
+        dots_per_seq<4, 4>(w1 + s0 * a.n + (long long)j * d, a.n, xs + s0 * d8, half, d, d8, nb, acc, lane);
         const float z = reduce_scatter8(acc, lane);
         if ((lane & 3) == 0 && m < nb) act[(long long)(s0 + m) * f + j] = __float2bfloat16_rn(gelu_f(z));
       }
@@ -447,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
       for (int j = gw; j < f; j += GW) {
         const bf16* w[1][2] = {{wg + (long long)j * d, wu + (long long)j * d}};
         float acc[1][2][kSeq] = {};
-        dots_shared<1, 2, 4>(w, xs, d, d, B, acc, lane);
+        dots_shared<1, 2, 4>(w, xs, half, d, d8, B, acc, lane);
         const float g = reduce_scatter8(acc[0][0], lane), u = reduce_scatter8(acc[0][1], lane);
         if (writer) act[(long long)m * f + j] = __float2bfloat16_rn(silu_f(g) * u);
       }
@@ -458,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
 #pragma unroll
         for (int i = 0; i < kRows; ++i) w[i][0] = j0 + i * GW < f ? w1 + (long long)(j0 + i * GW) * d : nullptr;
         float acc[kRows][1][kSeq] = {};
-        dots_shared<kRows, 1, 4>(w, xs, d, d, B, acc, lane);
+        dots_shared<kRows, 1, 4>(w, xs, half, d, d8, B, acc, lane);
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
           const float z = reduce_scatter8(acc[i][0], lane);
@@ -467,11 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
         }
       }
     }
-    prefetch_phase(2 * l + 1);
     if (!grid_sync(a.bar, gen, a.err)) return;
     // ---- down projection: partial sums px[l & 1][k][s][i] = W2[i, segment k] . act[s, segment k]
     // over units (i, k), i < d, k < nseg, spread over the grid's warps
-    stage_bf16(act, xs, B * f);
+    stage_bf16(act, xs, half, B * f);
     __syncthreads();
     float* pout = a.px + (l & 1) * 8 * BD;
     const bf16* w2 = static_cast<const bf16*>(fastb ? a.fdown[lf] : a.pre[l][a.swiglu ? 2 : 1]);
@@ -483,36 +442,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
       float y;
       if (fastb) {
         float acc[kSeq] = {};
-        dots_per_seq<2>(wrow + s0 * a.n, a.n, xs + (long long)s0 * f + (long long)k * sl, sl, f, nb, acc, lane);
+        dots_per_seq<4, 4>(wrow + s0 * a.n, a.n, xs + s0 * f8 + k * (sl / 8), half, sl, f8, nb, acc, lane);
         y = reduce_scatter8(acc, lane);
       } else {
         const bf16* w[1][1] = {{wrow}};
         float acc[1][1][kSeq] = {};
-        dots_shared<1, 1, 4>(w, xs + (long long)k * sl, sl, f, B, acc, lane);
+        dots_shared<1, 1, 4>(w, xs + k * (sl / 8), half, sl, f8, B, acc, lane);
         y = reduce_scatter8(acc[0][0], lane);
       }
       if ((lane & 3) == 0 && m < nb) pout[(long long)k * BD + (long long)(s0 + m) * d + i] = y;
     }
-    prefetch_phase(2 * l + 2);
     if (!grid_sync(a.bar, gen, a.err)) return;
   }
 
   // ---- the final residual stream (fold of the last block's partial sums),
   // RMSNorm (unit gain; every CTA for itself), then the LM head:
   // logits[s][v] = U[v] . y[s], rows v over the grid's warps
-  stage_fold(a.x32 + ((L - 1) & 1) * BD, a.px + ((L - 1) & 1) * 8 * BD, nseg, BD, nullptr, xs, B * d, false);
+  stage_fold(a.x32 + ((L - 1) & 1) * BD, a.px + ((L - 1) & 1) * 8 * BD, nseg, BD, nullptr, xs, half, B * d, false);
   __syncthreads();
   for (int s = warp; s < B; s += kWarps) {
     float sq = 0.0f;
     for (int c = lane; c < d; c += 32) {
-      const float v = xs[(long long)s * d + c];
+      const float v = xs_at(xs, half, s * d + c);
       sq = fmaf(v, v, sq);
     }
     sq = warp_total(sq);
     if (lane == 0) red[s] = rsqrtf(sq / d + a.eps);
   }
   __syncthreads();
-  for (int e = tid; e < B * d; e += kThreads) xs[e] = __bfloat162float(__float2bfloat16_rn(xs[e] * red[e / d]));
+  for (int e = tid; e < B * d; e += kThreads) {
+    float& x = xs_at(xs, half, e);
+    x = __bfloat162float(__float2bfloat16_rn(x * red[e / d]));
+  }
   __syncthreads();
   float mx = -FLT_MAX, se = 0.0f;      // writer lanes: softmax state of sequence m over this warp's rows
   const bf16* U = static_cast<const bf16*>(a.U);
@@ -521,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
 #pragma unroll
     for (int i = 0; i < kHeadRows; ++i) w[i][0] = v0 + i * GW < V ? U + (long long)(v0 + i * GW) * d : nullptr;
     float acc[kHeadRows][1][kSeq] = {};
-    dots_shared<kHeadRows, 1, 2>(w, xs, d, d, B, acc, lane);
+    dots_shared<kHeadRows, 1, 4>(w, xs, half, d, d8, B, acc, lane);
 #pragma unroll
     for (int i = 0; i < kHeadRows; ++i) {
       const float x = reduce_scatter8(acc[i][0], lane);
