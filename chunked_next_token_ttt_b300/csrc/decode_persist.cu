@@ -132,7 +132,7 @@ __device__ __forceinline__ void bf8x2(const uint4& u, f2 (&p)[4]) {
 __device__ __forceinline__ int scatter_index(int lane) {
   return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
 }
-__device__ __forceinline__ float reduce_scatter8(const float (&v)[kSeq], int lane) {
+__device__ __forceinline__ float reduce_scatter8(const float (&v)[8], int lane) {
   float a[4], b[2];
   const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
 #pragma unroll
@@ -151,6 +151,17 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[kSeq], int lan
   return c + __shfl_xor_sync(0xffffffffu, c, 1);
 }
 
+// The warp total of sequence m's value (S = 8: scattered, m = scatter_index;
+// S = 1: every lane, m = 0).
+template <int S>
+__device__ __forceinline__ float reduce_seq(const float (&v)[S], int lane) {
+  if constexpr (S == 1) {
+    return warp_total(v[0]);
+  } else {
+    return reduce_scatter8(v, lane);
+  }
+}
+
 // acc[i][q][s] += W_q(row i) . xs[s] over K for R rows of NW weight matrices
 // shared by the sequences (a null row contributes nothing) and nb sequences of
 // fp32 operand rows in shared memory in the split layout of stage_fold (piece
@@ -159,17 +170,17 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[kSeq], int lan
 // pieces; every weight piece of a batch of CB pieces per lane is loaded before
 // any is used (R * NW * CB 16-byte loads in flight per lane), and each piece is
 // unpacked once for all sequences.
-template <int R, int NW, int CB>
+template <int R, int NW, int CB, int S>
 __device__ __forceinline__ void dots_shared(const bf16* const (&w)[R][NW], const float4* xs, int half, int K, int ld8,
-                                            int nb, float (&acc)[R][NW][kSeq], int lane) {
+                                            int nb, float (&acc)[R][NW][S], int lane) {
   const int K8 = K / 8;
-  f2 acc2[R][NW][kSeq];
+  f2 acc2[R][NW][S];
 #pragma unroll
   for (int i = 0; i < R; ++i)
 #pragma unroll
     for (int q = 0; q < NW; ++q)
 #pragma unroll
-      for (int s = 0; s < kSeq; ++s) acc2[i][q][s] = 0ull;
+      for (int s = 0; s < S; ++s) acc2[i][q][s] = 0ull;
   for (int c0 = lane; c0 < K8; c0 += 32 * CB) {
     uint4 wv[CB][R][NW];
 #pragma unroll
@@ -190,7 +201,7 @@ __device__ __forceinline__ void dots_shared(const bf16* const (&w)[R][NW], const
 #pragma unroll
         for (int q = 0; q < NW; ++q) bf8x2(wv[b][i][q], wf[i][q]);
 #pragma unroll
-      for (int s = 0; s < kSeq; ++s) {
+      for (int s = 0; s < S; ++s) {
         if (s < nb) {
           const ulonglong2 x0 = *reinterpret_cast<const ulonglong2*>(xs + s * ld8 + c);
           const ulonglong2 x1 = *reinterpret_cast<const ulonglong2*>(xs + half + s * ld8 + c);
@@ -213,14 +224,14 @@ __device__ __forceinline__ void dots_shared(const bf16* const (&w)[R][NW], const
 #pragma unroll
     for (int q = 0; q < NW; ++q)
 #pragma unroll
-      for (int s = 0; s < kSeq; ++s) acc[i][q][s] += f2sum(acc2[i][q][s]);
+      for (int s = 0; s < S; ++s) acc[i][q][s] += f2sum(acc2[i][q][s]);
 }
 
 // acc[s] += W_s(row) . xs[s] over K where sequence s has its own weight row at
 // w0 + s * wseq (the fast weights), nb <= NS sequences; loads batched as above.
-template <int NS, int CB>
+template <int S, int NS, int CB>
 __device__ __forceinline__ void dots_per_seq(const bf16* w0, long long wseq, const float4* xs, int half, int K,
-                                             int ld8, int nb, float (&acc)[kSeq], int lane) {
+                                             int ld8, int nb, float (&acc)[S], int lane) {
   const int K8 = K / 8;
   for (int c0 = lane; c0 < K8; c0 += 32 * CB) {
     uint4 wv[CB][NS];
@@ -338,16 +349,22 @@ __device__ __forceinline__ void soft_join(float& m, float& s, float m2, float s2
 constexpr int kRows = 2;       // rows a warp takes at once in the block projections
 constexpr int kHeadRows = 2;   // and in the LM head
 
+// S: the sequences a warp accumulates at once (8, or 1 for a single
+// sequence, which frees registers for deeper load batches: CB pieces per lane)
+template <int S>
 __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __grid_constant__ DecodeNet a) {
+  constexpr int CB = S == 1 ? 8 : 4;
+  constexpr int NS = S == 1 ? 1 : 4;           // sequences of a per-sequence-weight unit
   extern __shared__ __align__(16) uint8_t smraw[];
   float* red = reinterpret_cast<float*>(smraw);                        // [kWarps][kSeq][2] reductions
   float4* xs = reinterpret_cast<float4*>(smraw + kWarps * kSeq * 2 * 4);  // fp32 operand rows of the phase
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gw = blockIdx.x * kWarps + warp, GW = gridDim.x * kWarps;
   const int B = a.B, d = a.d, f = a.f, V = a.V;
-  // after a reduce-scatter this lane holds sequence m's total; one lane of the four writes it
-  const int m = scatter_index(lane);
-  const bool writer = (lane & 3) == 0 && m < B;
+  // after a reduction this lane holds sequence m's total; one lane of those that hold it writes it
+  const int m = S == 1 ? 0 : scatter_index(lane);
+  const bool writer = S == 1 ? lane == 0 : ((lane & 3) == 0 && m < B);
+  const bool lead = S == 1 ? lane == 0 : (lane & 3) == 0;
   // the down projections split K = f into nseg segments when d rows alone
   // would leave warps idle; their partial sums are folded in by the next stage
   int nseg = 1;
@@ -357,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
       break;
     }
   // per-sequence weights: a unit takes half of the sequences when there are more than four
-  const int nh = B > 4 ? 2 : 1, hb = (B + nh - 1) / nh;    // hb <= 4 for B <= 8
+  const int nh = B > 4 ? 2 : 1, hb = (B + nh - 1) / nh;    // hb <= NS for B <= 8
   const int sl = f / nseg;
   const long long BD = (long long)B * d;
   const int half = B * (d > f ? d : f) / 8;     // pieces of the operand buffer; split layout
@@ -396,19 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
       const bf16* w1 = static_cast<const bf16*>(a.fup[lf]);
       for (int u = gw; u < f * nh; u += GW) {
         const int j = u / nh, s0 = (u % nh) * hb, nb = min(hb, B - s0);
-        float acc[kSeq] = {};
-        dots_per_seq<4, 4>(w1 + s0 * a.n + (long long)j * d, a.n, xs + s0 * d8, half, d, d8, nb, acc, lane);
-        const float z = reduce_scatter8(acc, lane);
-        if ((lane & 3) == 0 && m < nb) act[(long long)(s0 + m) * f + j] = __float2bfloat16_rn(gelu_f(z));
+        float acc[S] = {};
+        dots_per_seq<S, NS, CB>(w1 + s0 * a.n + (long long)j * d, a.n, xs + s0 * d8, half, d, d8, nb, acc, lane);
+        const float z = reduce_seq<S>(acc, lane);
+        if (lead && m < nb) act[(long long)(s0 + m) * f + j] = __float2bfloat16_rn(gelu_f(z));
       }
     } else if (a.swiglu) {
       const bf16* wg = static_cast<const bf16*>(fastb ? a.ffrozen[lf][0] : a.pre[l][0]);
       const bf16* wu = static_cast<const bf16*>(fastb ? a.ffrozen[lf][1] : a.pre[l][1]);
       for (int j = gw; j < f; j += GW) {
         const bf16* w[1][2] = {{wg + (long long)j * d, wu + (long long)j * d}};
-        float acc[1][2][kSeq] = {};
-        dots_shared<1, 2, 4>(w, xs, half, d, d8, B, acc, lane);
-        const float g = reduce_scatter8(acc[0][0], lane), u = reduce_scatter8(acc[0][1], lane);
+        float acc[1][2][S] = {};
+        dots_shared<1, 2, CB, S>(w, xs, half, d, d8, B, acc, lane);
+        const float g = reduce_seq<S>(acc[0][0], lane), u = reduce_seq<S>(acc[0][1], lane);
         if (writer) act[(long long)m * f + j] = __float2bfloat16_rn(silu_f(g) * u);
       }
     } else {
@@ -417,11 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
         const bf16* w[kRows][1];
 #pragma unroll
         for (int i = 0; i < kRows; ++i) w[i][0] = j0 + i * GW < f ? w1 + (long long)(j0 + i * GW) * d : nullptr;
-        float acc[kRows][1][kSeq] = {};
-        dots_shared<kRows, 1, 4>(w, xs, half, d, d8, B, acc, lane);
+        float acc[kRows][1][S] = {};
+        dots_shared<kRows, 1, CB, S>(w, xs, half, d, d8, B, acc, lane);
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
-          const float z = reduce_scatter8(acc[i][0], lane);
+          const float z = reduce_seq<S>(acc[i][0], lane);
           const int j = j0 + i * GW;
           if (writer && j < f) act[(long long)m * f + j] = __float2bfloat16_rn(gelu_f(z));
         }
@@ -441,16 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
       const bf16* wrow = w2 + (long long)i * f + (long long)k * sl;
       float y;
       if (fastb) {
-        float acc[kSeq] = {};
-        dots_per_seq<4, 4>(wrow + s0 * a.n, a.n, xs + s0 * f8 + k * (sl / 8), half, sl, f8, nb, acc, lane);
-        y = reduce_scatter8(acc, lane);
+        float acc[S] = {};
+        dots_per_seq<S, NS, CB>(wrow + s0 * a.n, a.n, xs + s0 * f8 + k * (sl / 8), half, sl, f8, nb, acc, lane);
+        y = reduce_seq<S>(acc, lane);
       } else {
         const bf16* w[1][1] = {{wrow}};
-        float acc[1][1][kSeq] = {};
-        dots_shared<1, 1, 4>(w, xs + k * (sl / 8), half, sl, f8, B, acc, lane);
-        y = reduce_scatter8(acc[0][0], lane);
+        float acc[1][1][S] = {};
+        dots_shared<1, 1, CB, S>(w, xs + k * (sl / 8), half, sl, f8, B, acc, lane);
+        y = reduce_seq<S>(acc[0][0], lane);
       }
-      if ((lane & 3) == 0 && m < nb) pout[(long long)k * BD + (long long)(s0 + m) * d + i] = y;
+      if (lead && m < nb) pout[(long long)k * BD + (long long)(s0 + m) * d + i] = y;
     }
     if (!grid_sync(a.bar, gen, a.err)) return;
   }
@@ -481,11 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_persist_kernel(const __gri
     const bf16* w[kHeadRows][1];
 #pragma unroll
     for (int i = 0; i < kHeadRows; ++i) w[i][0] = v0 + i * GW < V ? U + (long long)(v0 + i * GW) * d : nullptr;
-    float acc[kHeadRows][1][kSeq] = {};
-    dots_shared<kHeadRows, 1, 4>(w, xs, half, d, d8, B, acc, lane);
+    float acc[kHeadRows][1][S] = {};
+    dots_shared<kHeadRows, 1, CB, S>(w, xs, half, d, d8, B, acc, lane);
 #pragma unroll
     for (int i = 0; i < kHeadRows; ++i) {
-      const float x = reduce_scatter8(acc[i][0], lane);
+      const float x = reduce_seq<S>(acc[i][0], lane);
       const int v = v0 + i * GW;
       if (writer && v < V) {
         a.logits[(long long)m * V + v] = x;
@@ -544,14 +561,14 @@ int decode_persist_grid(int B, int d, int f) {
   if (B < 1 || B > dp::kSeq || d % 8 || f % 8) return 0;
   const size_t smem = dp::smem_bytes(B, d, f);
   if (smem > 227 * 1024) return 0;
-  if (ensure_dyn_smem((const void*)dp::decode_persist_kernel, smem) != cudaSuccess) {
+  const void* kern = B == 1 ? (const void*)dp::decode_persist_kernel<1> : (const void*)dp::decode_persist_kernel<8>;
+  if (ensure_dyn_smem(kern, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   int dev = 0, coop = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dp::decode_persist_kernel, dp::kThreads, smem) !=
-          cudaSuccess) {
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, dp::kThreads, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -576,7 +593,10 @@ ttt_status launch_decode_persist(const DecodeNet& net, int grid, cudaStream_t st
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  TTT_CUDA(cudaLaunchKernelEx(&cfg, dp::decode_persist_kernel, net));
+  if (net.B == 1)
+    TTT_CUDA(cudaLaunchKernelEx(&cfg, dp::decode_persist_kernel<1>, net));
+  else
+    TTT_CUDA(cudaLaunchKernelEx(&cfg, dp::decode_persist_kernel<8>, net));
   return TTT_OK;
 }
 
