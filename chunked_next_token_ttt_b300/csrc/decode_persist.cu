@@ -45,20 +45,22 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-// Grid-wide barrier of a cooperative launch: bar[0] counts arrivals, bar[1] is
-// the generation the last arrival publishes, bar[2] an abort flag.  Returns
-// false (in every thread of the CTA) when the wait timed out or another CTA
-// aborted.
+// Grid-wide barrier of a cooperative launch: bar[0] counts arrivals over the
+// whole launch (barrier g is complete at g * gridDim.x), bar[1] is the
+// generation the last arrival publishes, bar[2] an abort flag.  The arrival
+// is a release (it orders the CTA's writes, made visible to thread 0 by the
+// block barrier before it) and the wait an acquire, so no separate fences are
+// needed.  Returns false (in every thread of the CTA) when the wait timed out
+// or another CTA aborted.
 __device__ bool grid_sync(unsigned* bar, unsigned& gen, int* err) {
   __syncthreads();
   int ok = 1;
   if (threadIdx.x == 0) {
     const unsigned next = gen + 1;
-    __threadfence();
-    if (atomicAdd(&bar[0], 1u) == gridDim.x - 1) {
-      atomicExch(&bar[0], 0u);
-      __threadfence();
-      atomicExch(&bar[1], next);
+    unsigned old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(bar) : "memory");
+    if (old == next * gridDim.x - 1) {
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(bar + 1), "r"(next) : "memory");
     } else {
       const unsigned long long t0 = now_ns();
       while (ld_acquire(&bar[1]) != next) {
@@ -74,7 +76,6 @@ __device__ bool grid_sync(unsigned* bar, unsigned& gen, int* err) {
         }
       }
     }
-    __threadfence();
   }
   gen += 1;
   return __syncthreads_and(ok) != 0;
