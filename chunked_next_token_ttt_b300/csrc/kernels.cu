@@ -75,6 +75,73 @@ __global__ void rmsnorm_bwd_kernel(int d, const float* __restrict__ x, const flo
   }
 }
 
+// The same two operations with one warp per row (8 rows per 256-thread block)
+// and 16-byte loads, for rows whose width is a multiple of 4: no block barrier,
+// every load of a lane in flight at once.
+template <typename S>
+__global__ void rmsnorm_fwd_warp_kernel(int M, int d, const float* __restrict__ x, float eps, void* y, long long y_lo,
+                                        float* __restrict__ rstd, TokView tv, int32_t* __restrict__ tgt) {
+  pdl_wait();
+  pdl_launch();
+  const int lane = threadIdx.x & 31;
+  const long long m = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (m >= M) return;
+  if (tgt && lane == 0) {
+    const int s = (int)(m / tv.rows), j = (int)(m % tv.rows);
+    tgt[m] = j < tv.n_valid ? target_of(tv, s, j, tv.vocab) : -1;
+  }
+  const float4* xr = reinterpret_cast<const float4*>(x + m * d);
+  float sq = 0.0f;
+  for (int c = lane; c < d / 4; c += 32) {
+    const float4 v = xr[c];
+    sq = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, sq))));
+  }
+  sq = warp_sum(sq);
+  const float r = rsqrtf(sq / d + eps);
+  if (lane == 0) rstd[m] = r;
+  for (int c = lane; c < d / 4; c += 32) {
+    const float4 v = xr[c];
+    const long long i = m * d + 4LL * c;
+    OpIO<S>::store(y, y_lo, i, v.x * r);
+    OpIO<S>::store(y, y_lo, i + 1, v.y * r);
+    OpIO<S>::store(y, y_lo, i + 2, v.z * r);
+    OpIO<S>::store(y, y_lo, i + 3, v.w * r);
+  }
+}
+
+template <typename S>
+__global__ void rmsnorm_bwd_warp_kernel(int M, int d, const float* __restrict__ x, const float* __restrict__ rstd,
+                                        const float* __restrict__ dy, float* __restrict__ dx32, void* dxop,
+                                        long long dx_lo) {
+  pdl_wait();
+  pdl_launch();
+  const int lane = threadIdx.x & 31;
+  const long long m = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const float r = rstd[m];
+  const float4* xr = reinterpret_cast<const float4*>(x + m * d);
+  const float4* dyr = reinterpret_cast<const float4*>(dy + m * d);
+  float dot = 0.0f;
+  for (int c = lane; c < d / 4; c += 32) {
+    const float4 a = xr[c], g = dyr[c];
+    dot = fmaf(a.x * r, g.x, fmaf(a.y * r, g.y, fmaf(a.z * r, g.z, fmaf(a.w * r, g.w, dot))));
+  }
+  dot = warp_sum(dot) / d;
+  for (int c = lane; c < d / 4; c += 32) {
+    const float4 a = xr[c], g = dyr[c];
+    const float4 v = make_float4(r * (g.x - a.x * r * dot), r * (g.y - a.y * r * dot), r * (g.z - a.z * r * dot),
+                                 r * (g.w - a.w * r * dot));
+    reinterpret_cast<float4*>(dx32 + m * d)[c] = v;
+    if (dxop) {
+      const long long i = m * d + 4LL * c;
+      OpIO<S>::store(dxop, dx_lo, i, v.x);
+      OpIO<S>::store(dxop, dx_lo, i + 1, v.y);
+      OpIO<S>::store(dxop, dx_lo, i + 2, v.z);
+      OpIO<S>::store(dxop, dx_lo, i + 3, v.w);
+    }
+  }
+}
+
 // Combine two online-softmax partial states (max, sum of exp(x - max)).
 __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
   if (m2 > m) {
@@ -206,6 +273,76 @@ __global__ void ce_split_kernel(TokView tv, int V, float* __restrict__ logits, l
     const bf16 h = __float2bfloat16_rn(g);
     out[v] = h;
     out[V + v] = __float2bfloat16_rn(g - __bfloat162float(h));
+  }
+}
+
+// ce_split_kernel for rows of at most 512 * EPT logits (V a multiple of 8,
+// 16-byte aligned rows): each thread keeps its EPT logits in registers, loaded
+// with 16-byte reads all in flight, and writes its hi and lo bf16 pieces with
+// 16-byte stores; the row's values are all read before the block reduction,
+// so the in-place writes after it cannot overtake a read.
+template <int EPT>
+__global__ void __launch_bounds__(512) ce_split_reg_kernel(TokView tv, int V, float* __restrict__ logits, long long ldl,
+                                                           float scale, const float* __restrict__ rscale, bool grad,
+                                                           float* __restrict__ losses, long long loss_ld,
+                                                           long long loss_off, float* __restrict__ row_loss) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ float sm_m[32], sm_s[32];
+  const int m = blockIdx.x;
+  const int s = m / tv.rows, j = m % tv.rows;
+  float* row = logits + (long long)m * ldl;
+  bf16* out = reinterpret_cast<bf16*>(row);
+  const int base = threadIdx.x * EPT;
+  const bool mine = base < V;          // V is a multiple of 8 and EPT of 8: whole pieces
+  if (j >= tv.n_valid) {
+    if (grad && mine)
+#pragma unroll
+      for (int e = 0; e < EPT; e += 8) {
+        reinterpret_cast<uint4*>(out + base + e)[0] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(out + V + base + e)[0] = make_uint4(0, 0, 0, 0);
+      }
+    return;
+  }
+  const int tgt = target_of(tv, s, j, V);
+  float x[EPT];
+  float mx = -FLT_MAX, se = 0.0f;
+  if (mine) {
+#pragma unroll
+    for (int e = 0; e < EPT; e += 4) {
+      const float4 q = reinterpret_cast<const float4*>(row + base + e)[0];
+      x[e] = q.x; x[e + 1] = q.y; x[e + 2] = q.z; x[e + 3] = q.w;
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) mx = fmaxf(mx, x[e]);
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) se += __expf(x[e] - mx);
+  }
+  const float lse = block_lse(mx, se, sm_m, sm_s);   // contains __syncthreads
+  if (mine && tgt >= base && tgt < base + EPT) {
+    float xt = x[0];
+#pragma unroll
+    for (int e = 1; e < EPT; ++e)
+      if (tgt == base + e) xt = x[e];
+    const float loss = lse - xt;
+    if (losses) losses[s * loss_ld + loss_off + j] = loss;
+    if (row_loss) row_loss[m] = loss;
+  }
+  if (!grad || !mine) return;
+  const float sc = rscale ? rscale[m] : scale;
+#pragma unroll
+  for (int e = 0; e < EPT; e += 8) {
+    float g[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) g[q] = (__expf(x[e + q] - lse) - (base + e + q == tgt ? 1.0f : 0.0f)) * sc;
+    float lo[8];
+    const uint4 hi = pack_bf16x8(g);
+    float hf[8];
+    unpack_bf16x8(hi, hf);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) lo[q] = g[q] - hf[q];
+    reinterpret_cast<uint4*>(out + base + e)[0] = hi;
+    reinterpret_cast<uint4*>(out + V + base + e)[0] = pack_bf16x8(lo);
   }
 }
 
@@ -724,7 +861,12 @@ ttt_status launch_rmsnorm_fwd(int stg, int M, int d, const float* x, float eps, 
   if (M == 0) return TTT_OK;
   if (tv) TTT_TRY(check_view(*tv));
   const TokView tvv = tv ? *tv : TokView();
-  LAUNCH_BY_STORAGE(stg, rmsnorm_fwd_kernel, M, 256, 0, st, d, x, eps, y, y_lo, rstd, tvv, tv ? tgt : nullptr);
+  // a warp per row pays off once there are enough rows to fill the SMs with warps
+  if (M >= 4096 && d % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0)
+    LAUNCH_BY_STORAGE(stg, rmsnorm_fwd_warp_kernel, ceil_div(M, 8), 256, 0, st, M, d, x, eps, y, y_lo, rstd, tvv,
+                      tv ? tgt : nullptr);
+  else
+    LAUNCH_BY_STORAGE(stg, rmsnorm_fwd_kernel, M, 256, 0, st, d, x, eps, y, y_lo, rstd, tvv, tv ? tgt : nullptr);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -732,7 +874,12 @@ ttt_status launch_rmsnorm_fwd(int stg, int M, int d, const float* x, float eps, 
 ttt_status launch_rmsnorm_bwd(int stg, int M, int d, const float* x, const float* rstd, const float* dy, float* dx32,
                               void* dxop, long long dx_lo, cudaStream_t st) {
   if (M == 0) return TTT_OK;
-  LAUNCH_BY_STORAGE(stg, rmsnorm_bwd_kernel, M, 256, 0, st, d, x, rstd, dy, dx32, dxop, dx_lo);
+  const bool a16 = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dy) |
+                     reinterpret_cast<uintptr_t>(dx32)) & 15) == 0;
+  if (M >= 4096 && d % 4 == 0 && a16)
+    LAUNCH_BY_STORAGE(stg, rmsnorm_bwd_warp_kernel, ceil_div(M, 8), 256, 0, st, M, d, x, rstd, dy, dx32, dxop, dx_lo);
+  else
+    LAUNCH_BY_STORAGE(stg, rmsnorm_bwd_kernel, M, 256, 0, st, d, x, rstd, dy, dx32, dxop, dx_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
@@ -750,10 +897,19 @@ ttt_status launch_ce(int stg, int B, const TokView& tv, int V, void* logits, lon
       set_error("vocabulary too large for the split cross-entropy kernel");
       return TTT_ERR_UNSUPPORTED;
     }
-    const size_t smem = (size_t)V * sizeof(float);
-    TTT_CUDA(ensure_dyn_smem((const void*)ce_split_kernel, smem));
-    launch_pdl(ce_split_kernel, M, 512, smem, st, tv, V, static_cast<float*>(logits), ldl, scale, rscale, grad, losses, loss_ld,
-                                          loss_off, row_loss);
+    const bool reg = V % 8 == 0 && ldl % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+    if (reg && V <= 512 * 8) {
+      launch_pdl(ce_split_reg_kernel<8>, M, 512, 0, st, tv, V, static_cast<float*>(logits), ldl, scale, rscale, grad,
+                 losses, loss_ld, loss_off, row_loss);
+    } else if (reg && V <= 512 * 16) {
+      launch_pdl(ce_split_reg_kernel<16>, M, 512, 0, st, tv, V, static_cast<float*>(logits), ldl, scale, rscale, grad,
+                 losses, loss_ld, loss_off, row_loss);
+    } else {
+      const size_t smem = (size_t)V * sizeof(float);
+      TTT_CUDA(ensure_dyn_smem((const void*)ce_split_kernel, smem));
+      launch_pdl(ce_split_kernel, M, 512, smem, st, tv, V, static_cast<float*>(logits), ldl, scale, rscale, grad,
+                 losses, loss_ld, loss_off, row_loss);
+    }
   } else if (stg == ST_BF16) {
     launch_pdl(ce_kernel<bf16>, M, 512, 0, st, tv, V, static_cast<bf16*>(logits), ldl, scale, rscale, grad, losses, loss_ld,
                                        loss_off, row_loss);
