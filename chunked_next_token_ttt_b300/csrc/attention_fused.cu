@@ -17,8 +17,10 @@
 // Head width 64 (two::swa_fused2_kernel): two 128-query tiles per CTA, four
 // softmax warps per tile with one thread per query row over all 128 keys of a
 // block, S, P and O of each tile in TMEM, the K/V blocks shared by the tiles,
-// and the tensor core alternating between them so that one tile's products
-// overlap the other's softmax.
+// and one MMA-issuing warp per tile, so that one tile's products overlap the
+// other's softmax and the two issuers together keep the tensor pipe fed (one
+// thread issuing back-to-back MMAs of these shapes reaches about half the
+// pipe's rate, and every instruction it runs between two MMAs idles the pipe).
 //
 // Head width 128 (swa_fused_kernel<128>): one 128-query tile per CTA; S and P
 // double-buffered in TMEM; two softmax warps per TMEM lane quadrant, one
@@ -28,7 +30,8 @@
 // they rescale alike and leave together.
 //
 // Warps: 0 TMA producer (Q once; K and V per key block through a ring),
-// 1 TMEM allocator and MMA issuer, 2..9 softmax and output.  Every mbarrier
+// 1 TMEM allocator and MMA issuer, 2..9 softmax and output (head width 64: a
+// second MMA issuer, warp 10).  Every mbarrier
 // wait is bounded (tc::mbar_wait); a timeout records a code in the status word
 // and the CTA unwinds: the producer waits (bounded) for its copies in flight,
 // the MMA issuer for its MMAs, and TMEM is freed.
@@ -567,7 +570,10 @@ namespace two {
 
 constexpr int NT = 2;                          // query tiles per CTA
 constexpr int NSW2 = 4 * NT;                   // softmax warps
-constexpr int NTHREADS2 = 64 + 32 * NSW2;
+// warp 0: TMA producer; warp 1 and warp 2 + NSW2: the MMA issuers of tile 0
+// and tile 1 (a thread issuing tcgen05.mma feeds the tensor pipe at a limited
+// rate, so each tile has its own); warps 2 .. 1 + NSW2: softmax
+constexpr int NTHREADS2 = 96 + 32 * NSW2;
 constexpr int KST2 = 4;                        // K/V ring slots
 constexpr int DH2 = 64;
 constexpr int TILE2 = PANEL_BYTES;             // 128 rows x 64 bf16
@@ -576,8 +582,8 @@ constexpr int K_OFF2 = Q_OFF2 + NT * TILE2;    // [KST2] K tiles
 constexpr int V_OFF2 = K_OFF2 + KST2 * TILE2;  // [KST2] V tiles
 constexpr int BAR_OFF2 = V_OFF2 + KST2 * TILE2;
 // q_full, kv_full[KST2], kv_empty[KST2], s_full[NT], s_free[NT], p_full[NT],
-// p_free[NT], o_full[NT], drain; the TMEM slot
-constexpr int NBAR2 = 1 + 2 * KST2 + 5 * NT + 1;
+// p_free[NT], o_full[NT], drain[NT]; the TMEM slot
+constexpr int NBAR2 = 1 + 2 * KST2 + 6 * NT;
 constexpr int ALLOC2 = BAR_OFF2 + NBAR2 * 8 + 16 + 1024;
 static_assert(ALLOC2 <= 232448, "shared memory over the per-block limit");
 // TMEM columns of tile t: S (fp32) at 128 t, O (fp32) at 256 + 64 t, P (bf16
@@ -600,8 +606,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   uint64_t* p_full = s_free + NT;          // [NT] the tile's P is in TMEM
   uint64_t* p_free = p_full + NT;          // [NT] its P V is done (P free, O current)
   uint64_t* o_full = p_free + NT;          // [NT] the tile's last P V is done
-  uint64_t* drain = o_full + NT;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = o_full + NT;           // [NT]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + NT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = blockIdx.x * (NT * BQ);
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < KST2; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], NT);             // released by both issuers
     }
     for (int t = 0; t < NT; ++t) {
       mbar_init(&s_full[t], 1);
@@ -626,8 +632,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       mbar_init(&p_full[t], 4);
       mbar_init(&p_free[t], 1);
       mbar_init(&o_full[t], 1);
+      mbar_init(&drain[t], 1);
     }
-    mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -663,59 +669,57 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     bool landed = mbar_wait(q_full, 0, a.err, 8);
     for (uint32_t q = i > (uint32_t)KST2 ? i - KST2 : 0; q < i && landed; ++q)
       landed = mbar_wait(&kv_full[q % KST2], (q / KST2) & 1, a.err, 8);
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer
+  } else if ((warp == 1 || warp == 2 + NSW2) && lane == 0) {
+    // ------------------------------------------------ MMA issuer of tile t
+    // Every union block passes through both issuers in order: each waits for
+    // it to land and releases its ring slot (kv_empty counts both), whether or
+    // not its tile reads it, so a slot is refilled only after both are done.
+    const int t = warp == 1 ? 0 : 1;
     constexpr uint32_t idS = umma_idesc(BQ, BKV, false, false);   // S = Q K^T: both operands K-major
     constexpr uint32_t idO = umma_idesc(BQ, DH2, false, true);    // O += P V: P from TMEM, V MN-major
-    const int ulo[NT] = {ulo0, ulo1}, uhi[NT] = {nkb - 1, nkb};
+    const int off = (t ? ulo1 : ulo0) - ulo0;   // union index of the tile's first block
+    const int nb = nkb - 1 + t - (t ? ulo1 : ulo0) + 1;   // blocks the tile reads
+    const uint32_t sq = smem_u32(smem + Q_OFF2 + t * TILE2);
     bool ok = mbar_wait(q_full, 0, a.err, 16);
-    // step i: the S of union block ulo0 + i for each tile that reads it, then
-    // the P V of block ulo0 + i - 1 for each tile that read it
+    // step i: the tile's S of union block i, then its P V of union block i - 1
     for (int i = 0; i <= nu && ok; ++i) {
-      const int u = ulo0 + i;
+      const int n = i - off;                    // the tile's block index of union block i
       if (i < nu) {
         if (!mbar_wait(&kv_full[i % KST2], (i / KST2) & 1, a.err, 16)) { ok = false; break; }
-        const uint32_t sk = smem_u32(smem + K_OFF2 + (i % KST2) * TILE2);
-        for (int t = 0; t < NT && ok; ++t) {
-          if (u < ulo[t] || u > uhi[t]) continue;
-          const int n = u - ulo[t];
+        if (n >= 0 && n < nb) {
           // the tile's softmax has read its previous S
           if (n >= 1 && !mbar_wait(&s_free[t], (n - 1) & 1, a.err, 16)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sq = smem_u32(smem + Q_OFF2 + t * TILE2);
+          const uint32_t sk = smem_u32(smem + K_OFF2 + (i % KST2) * TILE2);
 #pragma unroll
           for (int kk = 0; kk < DH2 / 16; ++kk)
             umma_bf16(tmem + col_s(t), umma_desc(sq + kk * 32, 16, 1024), umma_desc(sk + kk * 32, 16, 1024), idS,
                       kk > 0 ? 1u : 0u);
           umma_commit(&s_full[t]);
         }
-        if (!ok) break;
       }
       if (i >= 1) {
-        const int up = u - 1;
-        const uint32_t sv = smem_u32(smem + V_OFF2 + ((i - 1) % KST2) * TILE2);
-        for (int t = 0; t < NT && ok; ++t) {
-          if (up < ulo[t] || up > uhi[t]) continue;
-          const int n = up - ulo[t];
-          if (!mbar_wait(&p_full[t], n & 1, a.err, 16)) { ok = false; break; }
+        const int np = n - 1;
+        if (np >= 0 && np < nb) {
+          if (!mbar_wait(&p_full[t], np & 1, a.err, 16)) { ok = false; break; }
           tc_fence_after();
+          const uint32_t sv = smem_u32(smem + V_OFF2 + ((i - 1) % KST2) * TILE2);
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk)
             umma_bf16_tmem_a(tmem + col_o(t), tmem + col_p(t) + kk * 8, umma_desc(sv + kk * 2048, PANEL_BYTES, 1024),
-                             idO, (n > 0 || kk > 0) ? 1u : 0u);
+                             idO, (np > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&p_free[t]);
-          if (up == uhi[t]) umma_commit(&o_full[t]);
+          if (np == nb - 1) umma_commit(&o_full[t]);
         }
-        if (!ok) break;
         umma_commit(&kv_empty[(i - 1) % KST2]);
       }
     }
     if (!ok) {
       // stopped early: the MMAs already issued finish before TMEM is freed
-      umma_commit(drain);
-      mbar_wait(drain, 0, a.err, 16);
+      umma_commit(&drain[t]);
+      mbar_wait(&drain[t], 0, a.err, 16);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + NSW2) {
     // ------------------------------------------------ softmax and output
     const int t = (warp - 2) >> 2;             // query tile
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. + 31

@@ -95,9 +95,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on phase `parity`; false (and *err |= code) after the timeout.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop of a wait whose first test failed: bounded, false (and
+// *err |= code) after the timeout.  Out of line: it is the rare path.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int* err, int code) {
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
@@ -108,6 +108,14 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, in
       return false;
     }
   }
+}
+
+// Bounded wait on phase `parity`; false (and *err |= code) after the timeout.
+// The first test is inline: a thread that issues tcgen05.mma stalls the tensor
+// pipe for as long as it spends between two MMAs, and a call costs hundreds of
+// clocks even when the phase is already complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, err, code);
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1,
@@ -345,6 +353,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = umma_idesc(BM, BN, A_MN, B_MN);
     uint32_t kit = 0;
+    uint32_t polled = ~0u;   // the k-slice whose stage was tested ahead, and the verdict
+    bool ready = false;
     bool ok = true;
     int i = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
@@ -360,7 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t d_tmem = tmem + (uint32_t)(ab * BN);
       for (int kb = 0; kb < nk; ++kb, ++kit) {
         const int s = kit % STAGES;
-        if (!mbar_wait(&full[s], (kit / STAGES) & 1, err, 16)) {
+        if (!(polled == kit && ready) && !mbar_wait(&full[s], (kit / STAGES) & 1, err, 16)) {
           ok = false;
           break;
         }
@@ -383,6 +393,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         umma_commit(&empty[s]);
+        // test the next k-slice's stage now, while this one's MMAs run: its
+        // latency is then off the issue path
+        polled = kit + 1;
+        ready = mbar_try_wait(&full[polled % STAGES], (polled / STAGES) & 1);
       }
       umma_commit(&accf[ab]);
     }
