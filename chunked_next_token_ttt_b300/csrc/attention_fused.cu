@@ -220,6 +220,45 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Start loading 32 consecutive TMEM columns of the warp's 32 lanes; the values
+// may be read only after tmem_ld_wait on the same registers.
+__device__ __forceinline__ void tmem_ld32_start(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+// Wait for every TMEM load the thread has started.  The registers pass
+// through the wait, so the compiler schedules no use of them before it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// 16 consecutive TMEM columns of the warp's 32 lanes from registers, without
+// waiting for the write (tcgen05.wait::st before the columns are published).
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
 // D (+)= A B with A (M = 128 rows, 16 bf16 of K packed in 8 columns) read
 // from TMEM and B from shared memory.
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
@@ -574,24 +613,24 @@ constexpr int NSW2 = 4 * NT;                   // softmax warps
 // and tile 1 (a thread issuing tcgen05.mma feeds the tensor pipe at a limited
 // rate, so each tile has its own); warps 2 .. 1 + NSW2: softmax
 constexpr int NTHREADS2 = 96 + 32 * NSW2;
-constexpr int KST2 = 4;                        // K/V ring slots
+constexpr int KST2 = 4;                        // K/V ring slots (128 keys each)
 constexpr int DH2 = 64;
+constexpr int SUB = 64;                        // keys of a sub-block: one S and one P V
+constexpr int SUB_BYTES = SUB * 128;           // a sub-block's rows of a K or V tile
 constexpr int TILE2 = PANEL_BYTES;             // 128 rows x 64 bf16
 constexpr int Q_OFF2 = 0;                      // [NT] Q tiles
 constexpr int K_OFF2 = Q_OFF2 + NT * TILE2;    // [KST2] K tiles
 constexpr int V_OFF2 = K_OFF2 + KST2 * TILE2;  // [KST2] V tiles
 constexpr int BAR_OFF2 = V_OFF2 + KST2 * TILE2;
-// q_full, kv_full[KST2], kv_empty[KST2], s_full[NT], s_free[NT], p_full[NT],
-// p_free[NT], o_full[NT], drain[NT]; the TMEM slot
-constexpr int NBAR2 = 1 + 2 * KST2 + 6 * NT;
+// q_full, kv_full[KST2], kv_empty[KST2], then per tile s_full[2], s_free[2],
+// p_full[2], p_free[2], o_full, drain; the TMEM slot
+constexpr int NBAR2 = 1 + 2 * KST2 + 10 * NT;
 constexpr int ALLOC2 = BAR_OFF2 + NBAR2 * 8 + 16 + 1024;
 static_assert(ALLOC2 <= 232448, "shared memory over the per-block limit");
-// TMEM columns of tile t: S (fp32) at 128 t, O (fp32) at 256 + 64 t, P (bf16
-// pairs) at 384 + 64 t
+// TMEM columns of tile t, from 256 t: S buffers (fp32, 64 keys) at 0 and 64,
+// P buffers (bf16 pairs, 64 keys) at 128 and 160, O (fp32) at 192
 constexpr uint32_t TMEM_COLS2 = 512;
-__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
-__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 64u * t; }
-__device__ __forceinline__ uint32_t col_p(int t) { return 384u + 64u * t; }
+constexpr uint32_t S_COL = 0, P_COL = 128, O_COL = 192;
 
 __global__ void __launch_bounds__(NTHREADS2, 1)
     swa_fused2_kernel(const __grid_constant__ CUtensorMap tm, const Args a, int nkb) {
@@ -601,20 +640,16 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + KST2;
-  uint64_t* s_full = kv_empty + KST2;      // [NT] S of the tile's current block is in TMEM
-  uint64_t* s_free = s_full + NT;          // [NT] the tile's softmax has read it
-  uint64_t* p_full = s_free + NT;          // [NT] the tile's P is in TMEM
-  uint64_t* p_free = p_full + NT;          // [NT] its P V is done (P free, O current)
-  uint64_t* o_full = p_free + NT;          // [NT] the tile's last P V is done
-  uint64_t* drain = o_full + NT;           // [NT]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + NT);
+  uint64_t* tile_bars = kv_empty + KST2;   // 10 per tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_bars + 10 * NT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = blockIdx.x * (NT * BQ);
   const int hc = blockIdx.y * DH2;
   const int seq = blockIdx.z;
-  // union key block u holds positions kb0 + 128 u ..; tile t reads blocks
-  // ulo[t] .. nkb - 1 + t, the last ending at its last query q0 + 128 t + 127
+  // union key block u (128 keys) holds positions kb0 + 128 u ..; tile t reads
+  // blocks ulo[t] .. nkb - 1 + t, the last ending at its last query
+  // q0 + 128 t + 127, each as two 64-key sub-blocks
   const int kb0 = q0 + BQ - nkb * BKV;
   const int ulo0 = (max(0, q0 - a.window + 1) - kb0) / BKV;
   const int ulo1 = (max(0, q0 + BQ - a.window + 1) - kb0) / BKV;
@@ -627,12 +662,15 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       mbar_init(&kv_empty[s], NT);             // released by both issuers
     }
     for (int t = 0; t < NT; ++t) {
-      mbar_init(&s_full[t], 1);
-      mbar_init(&s_free[t], 4);
-      mbar_init(&p_full[t], 4);
-      mbar_init(&p_free[t], 1);
-      mbar_init(&o_full[t], 1);
-      mbar_init(&drain[t], 1);
+      uint64_t* tbar = tile_bars + 10 * t;
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&tbar[b], 1);                // s_full[b]: S of the buffer's sub-block is in TMEM
+        mbar_init(&tbar[2 + b], 4);            // s_free[b]: the tile's four softmax warps have read it
+        mbar_init(&tbar[4 + b], 4);            // p_full[b]: its P is in TMEM
+        mbar_init(&tbar[6 + b], 1);            // p_free[b]: its P V is done (P free, O holds it)
+      }
+      mbar_init(&tbar[8], 1);                  // o_full: the tile's last P V is done
+      mbar_init(&tbar[9], 1);                  // drain
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -674,94 +712,122 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     // Every union block passes through both issuers in order: each waits for
     // it to land and releases its ring slot (kv_empty counts both), whether or
     // not its tile reads it, so a slot is refilled only after both are done.
+    // Sub-block j of the tile uses S and P buffer j & 1: S(j) is computed while
+    // the softmax works on sub-block j - 1, and P V(j - 1) once its P is in.
     const int t = warp == 1 ? 0 : 1;
-    constexpr uint32_t idS = umma_idesc(BQ, BKV, false, false);   // S = Q K^T: both operands K-major
+    uint64_t* tbar = tile_bars + 10 * t;
+    uint64_t *s_full = tbar, *s_free = tbar + 2, *p_full = tbar + 4, *p_free = tbar + 6;
+    constexpr uint32_t idS = umma_idesc(BQ, SUB, false, false);   // S = Q K^T: both operands K-major
     constexpr uint32_t idO = umma_idesc(BQ, DH2, false, true);    // O += P V: P from TMEM, V MN-major
     const int off = (t ? ulo1 : ulo0) - ulo0;   // union index of the tile's first block
-    const int nb = nkb - 1 + t - (t ? ulo1 : ulo0) + 1;   // blocks the tile reads
+    const int nb = nkb + t - (t ? ulo1 : ulo0); // union blocks the tile reads
+    const int nj = 2 * nb;                      // its sub-blocks
     const uint32_t sq = smem_u32(smem + Q_OFF2 + t * TILE2);
+    const uint32_t tt = tmem + 256u * t;
     bool ok = mbar_wait(q_full, 0, a.err, 16);
-    // step i: the tile's S of union block i, then its P V of union block i - 1
+    // union step i: for each half h, the tile's S of sub-block 2 n + h (n the
+    // tile's index of union block i), then its P V of the sub-block before
     for (int i = 0; i <= nu && ok; ++i) {
-      const int n = i - off;                    // the tile's block index of union block i
-      if (i < nu) {
-        if (!mbar_wait(&kv_full[i % KST2], (i / KST2) & 1, a.err, 16)) { ok = false; break; }
-        if (n >= 0 && n < nb) {
-          // the tile's softmax has read its previous S
-          if (n >= 1 && !mbar_wait(&s_free[t], (n - 1) & 1, a.err, 16)) { ok = false; break; }
+      const int n = i - off;
+      if (i < nu && !mbar_wait(&kv_full[i % KST2], (i / KST2) & 1, a.err, 16)) {
+        ok = false;
+        break;
+      }
+      for (int h = 0; h < 2; ++h) {
+        const int j = 2 * n + h;
+        if (i < nu && n >= 0 && n < nb) {
+          const int b = j & 1;
+          // the softmax has read S(j - 2) from this buffer
+          if (j >= 2 && !mbar_wait(&s_free[b], ((j >> 1) - 1) & 1, a.err, 16)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t sk = smem_u32(smem + K_OFF2 + (i % KST2) * TILE2);
+          const uint32_t sk = smem_u32(smem + K_OFF2 + (i % KST2) * TILE2 + h * SUB_BYTES);
 #pragma unroll
           for (int kk = 0; kk < DH2 / 16; ++kk)
-            umma_bf16(tmem + col_s(t), umma_desc(sq + kk * 32, 16, 1024), umma_desc(sk + kk * 32, 16, 1024), idS,
-                      kk > 0 ? 1u : 0u);
-          umma_commit(&s_full[t]);
+            umma_bf16(tt + S_COL + SUB * b, umma_desc(sq + kk * 32, 16, 1024), umma_desc(sk + kk * 32, 16, 1024),
+                      idS, kk > 0 ? 1u : 0u);
+          umma_commit(&s_full[b]);
         }
-      }
-      if (i >= 1) {
-        const int np = n - 1;
-        if (np >= 0 && np < nb) {
-          if (!mbar_wait(&p_full[t], np & 1, a.err, 16)) { ok = false; break; }
+        const int jp = j - 1;
+        if (jp >= 0 && jp < nj) {
+          const int bp = jp & 1;
+          if (!mbar_wait(&p_full[bp], (jp >> 1) & 1, a.err, 16)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t sv = smem_u32(smem + V_OFF2 + ((i - 1) % KST2) * TILE2);
+          const int ip = (jp >> 1) + off;       // union block of sub-block jp
+          const uint32_t sv = smem_u32(smem + V_OFF2 + (ip % KST2) * TILE2 + (jp & 1) * SUB_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk)
-            umma_bf16_tmem_a(tmem + col_o(t), tmem + col_p(t) + kk * 8, umma_desc(sv + kk * 2048, PANEL_BYTES, 1024),
-                             idO, (np > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&p_free[t]);
-          if (np == nb - 1) umma_commit(&o_full[t]);
+          for (int kk = 0; kk < SUB / 16; ++kk)
+            umma_bf16_tmem_a(tt + O_COL, tt + P_COL + (SUB / 2) * bp + kk * 8,
+                             umma_desc(sv + kk * 2048, PANEL_BYTES, 1024), idO, (jp > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&p_free[bp]);
+          if (jp == nj - 1) umma_commit(&tbar[8]);
         }
-        umma_commit(&kv_empty[(i - 1) % KST2]);
+        // union block i - 1 is done with: its last P V was just issued
+        if (h == 0 && i >= 1) umma_commit(&kv_empty[(i - 1) % KST2]);
       }
     }
     if (!ok) {
       // stopped early: the MMAs already issued finish before TMEM is freed
-      umma_commit(&drain[t]);
-      mbar_wait(&drain[t], 0, a.err, 16);
+      umma_commit(&tbar[9]);
+      mbar_wait(&tbar[9], 0, a.err, 16);
     }
   } else if (warp >= 2 && warp < 2 + NSW2) {
     // ------------------------------------------------ softmax and output
     const int t = (warp - 2) >> 2;             // query tile
+    uint64_t* tbar = tile_bars + 10 * t;
+    uint64_t *s_full = tbar, *s_free = tbar + 2, *p_full = tbar + 4, *p_free = tbar + 6;
     const int quad = warp & 3;                 // TMEM lanes 32 quad .. + 31
     const int r = quad * 32 + lane;            // query row of the tile
     const int qi = q0 + BQ * t + r;            // its position in the sequence
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int u_lo = t ? ulo1 : ulo0, u_hi = nkb - 1 + t;
+    const uint32_t tt = tmem + 256u * t + ((uint32_t)(quad * 32) << 16);
+    const int u_lo = t ? ulo1 : ulo0;
+    const int nj = 2 * (nkb + t - u_lo);       // the tile's 64-key sub-blocks
+    const f2 c2 = f2make(a.c, a.c);
     float m = -INFINITY;                       // the row's running maximum (base 2)
     float l = 0.0f;                            // the row's sum of P
     bool ok = true;
-    for (int u = u_lo; u <= u_hi; ++u) {
-      const int n = u - u_lo;
-      ok = warp_wait(&s_full[t], n & 1, a.err, 32);
+    for (int j = 0; j < nj; ++j) {
+      const int b = j & 1;
+      ok = warp_wait(&s_full[b], (j >> 1) & 1, a.err, 32);
       if (!ok) break;
-      // the row's valid keys lo .. hi of the block; the rest become -inf
-      // (2^-inf = 0), only in the window's edge blocks
-      const int kp = kb0 + u * BKV;
-      const int lo = max(max(0, qi - a.window + 1), kp) - kp;
-      const int hi = min(qi, kp + BKV - 1) - kp;
-      const bool edge = lo > 0 || hi < BKV - 1;
-      auto load_s = [&](int c, float (&v)[32]) {
-        tmem_ld32(tmem + col_s(t) + 32 * c + lane_off, v);
-        if (edge) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * c + e < lo || 32 * c + e > hi) v[e] = -INFINITY;
-        }
-      };
-      // pass 1: the block's row maximum, 32 columns at a time
+      // the whole row of the sub-block's scores into registers; S is then free
       tc_fence_after();
+      uint32_t ra[32], rb[32];
+      tmem_ld32_start(tt + S_COL + SUB * b, ra);
+      tmem_ld32_start(tt + S_COL + SUB * b + 32, rb);
+      tmem_ld_wait(ra);
+      tmem_ld_wait(rb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[b]);
+      // the row's valid keys lo .. hi of the sub-block; the rest become -inf
+      // (2^-inf = 0), only in the window's edge sub-blocks
+      const int kp = kb0 + (u_lo + (j >> 1)) * BKV + (j & 1) * SUB;
+      const int lo = max(max(0, qi - a.window + 1), kp) - kp;
+      const int hi = min(qi, kp + SUB - 1) - kp;
+      float v[SUB];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        v[e] = __uint_as_float(ra[e]);
+        v[32 + e] = __uint_as_float(rb[e]);
+      }
+      if (lo > 0 || hi < SUB - 1) {
+#pragma unroll
+        for (int e = 0; e < SUB; ++e)
+          if (e < lo || e > hi) v[e] = -INFINITY;
+      }
       float bm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        float v[32];
-        load_s(c, v);
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          bm4[0] = max3(bm4[0], v[e], v[e + 1]);
-          bm4[1] = max3(bm4[1], v[e + 2], v[e + 3]);
-          bm4[2] = max3(bm4[2], v[e + 4], v[e + 5]);
-          bm4[3] = max3(bm4[3], v[e + 6], v[e + 7]);
-        }
+      for (int e = 0; e < SUB; e += 8) {
+        bm4[0] = max3(bm4[0], v[e], v[e + 1]);
+        bm4[1] = max3(bm4[1], v[e + 2], v[e + 3]);
+        bm4[2] = max3(bm4[2], v[e + 4], v[e + 5]);
+        bm4[3] = max3(bm4[3], v[e + 6], v[e + 7]);
       }
       const float bm = max3(bm4[0], bm4[1], fmaxf(bm4[2], bm4[3])) * a.c;
       // raise the running maximum only by more than TAU; then l and O are
@@ -773,42 +839,36 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         l *= alpha;
         m = bm;
       }
-      // the tile's previous P V is done: P is free and O holds it
-      if (n >= 1) {
-        ok = warp_wait(&p_free[t], (n - 1) & 1, a.err, 32);
+      // P buffer b is free once P V(j - 2) is done
+      if (j >= 2) {
+        ok = warp_wait(&p_free[b], ((j >> 1) - 1) & 1, a.err, 32);
         if (!ok) break;
-        if (__any_sync(0xffffffffu, rescale)) {
-          tc_fence_after();
+      }
+      // a rescale needs O current: P V(j - 1) done (the P Vs complete in order)
+      if (__any_sync(0xffffffffu, rescale)) {
+        ok = warp_wait(&p_free[b ^ 1], ((j - 1) >> 1) & 1, a.err, 32);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < DH2 / 32; ++c) {
-            float o[32];
-            tmem_ld32(tmem + col_o(t) + 32 * c + lane_off, o);
+        for (int c = 0; c < DH2 / 32; ++c) {
+          float o[32];
+          tmem_ld32(tt + O_COL + 32 * c, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tmem + col_o(t) + 32 * c + lane_off, o);
-          }
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tt + O_COL + 32 * c, o);
         }
       }
-      // pass 2: P = 2^(S c - m), scale and sums in pairs on the FMA pipe;
-      // packed bf16 pairs (even key in the low half) to the tile's P columns.
-      // S is released once its last columns are read.
-      const f2 c2 = f2make(a.c, a.c);
+      // P = 2^(S c - m), scale and sums in pairs on the FMA pipe; packed bf16
+      // pairs (even key in the low half) to P buffer b
       const float nmv = m > -INFINITY ? -m : 0.0f;   // no valid key yet: every P is 2^-inf = 0
       const f2 nm2 = f2make(nmv, nmv);
       f2 se2[2] = {f2make(0.0f, 0.0f), f2make(0.0f, 0.0f)};
 #pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        float v[32];
-        load_s(c, v);
-        if (c == BKV / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[t]);
-        }
+      for (int c = 0; c < SUB / 32; ++c) {
         float pw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const f2 x = f2fma(f2make(v[e], v[e + 1]), c2, nm2);
+          const f2 x = f2fma(f2make(v[32 * c + e], v[32 * c + e + 1]), c2, nm2);
           float x0, x1;
           f2split(x, x0, x1);
           if ((e / 2) % 4 < EMU_PAIRS) {
@@ -821,8 +881,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           const __nv_bfloat162 pr = __floats2bfloat162_rn(x0, x1);
           pw[e / 2] = *reinterpret_cast<const float*>(&pr);
         }
-        tmem_st16(tmem + col_p(t) + 16 * c + lane_off, pw);
+        tmem_st16_nowait(tt + P_COL + (SUB / 2) * b + 16 * c, pw);
       }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       {
         float s0, s1, s2, s3;
         f2split(se2[0], s0, s1);
@@ -831,17 +892,17 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
+      if (lane == 0) mbar_arrive(&p_full[b]);
     }
     // out = O / l for the tile's real rows
-    if (ok && warp_wait(&o_full[t], 0, a.err, 32)) {
+    if (ok && warp_wait(&tbar[8], 0, a.err, 32)) {
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       bf16* dst = a.out + ((long long)seq * a.L + a.pad + qi) * a.d + hc;
 #pragma unroll
       for (int c = 0; c < DH2 / 32; ++c) {
         float o[32];
-        tmem_ld32(tmem + col_o(t) + 32 * c + lane_off, o);
+        tmem_ld32(tt + O_COL + 32 * c, o);
         if (qi < a.rows) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= inv;
