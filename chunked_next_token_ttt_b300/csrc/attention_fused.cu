@@ -14,13 +14,16 @@
 // operand read from TMEM (P never touches shared memory, whose bandwidth the
 // K/V copies and the operand reads already share).  out = O / l.
 //
-// Head width 64 (two::swa_fused2_kernel): two 128-query tiles per CTA, four
-// softmax warps per tile with one thread per query row over all 128 keys of a
-// block, S, P and O of each tile in TMEM, the K/V blocks shared by the tiles,
-// and one MMA-issuing warp per tile, so that one tile's products overlap the
-// other's softmax and the two issuers together keep the tensor pipe fed (one
-// thread issuing back-to-back MMAs of these shapes reaches about half the
-// pipe's rate, and every instruction it runs between two MMAs idles the pipe).
+// Head width 64 (two::swa_fused2_kernel): two 128-query tiles per CTA that
+// share the K/V blocks; each 128-key block is taken as two 64-key sub-blocks,
+// with S and P double-buffered per tile in TMEM (S 2 x 64, P 2 x 32, O 64
+// columns: 256 per tile), so S of the next sub-block is computed while the
+// softmax works on this one and P V of the last one runs meanwhile.  Four
+// softmax warps per tile, one thread per query row, hold the sub-block's whole
+// score row in registers (S is released right after the load).  One
+// MMA-issuing warp per tile: a thread issuing back-to-back MMAs of these
+// shapes reaches about half the tensor pipe's rate, and every instruction it
+// runs between two MMAs idles the pipe.
 //
 // Head width 128 (swa_fused_kernel<128>): one 128-query tile per CTA; S and P
 // double-buffered in TMEM; two softmax warps per TMEM lane quadrant, one
