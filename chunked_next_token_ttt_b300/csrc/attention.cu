@@ -248,27 +248,38 @@ __global__ void kv_fill_kernel(int R, int window, int d, const void* __restrict_
 }
 
 // One decoded position per sequence (`*pos_ptr`, the same for every
-// sequence): one block of kDecThreads per (head, sequence) appends the row's
-// K and V to the cache, scores the query against the window's keys
-// (positions pos - n + 1 .. pos, n = min(pos + 1, window)) into shared
-// memory, takes the softmax, and sums the values with the threads split as
-// (key group, head element), four independent sums per thread so that their
-// loads overlap.
-constexpr int kDecThreads = 1024;
+// sequence), the keys of the window being positions pos - j, j = 0 .. n - 1,
+// n = min(pos + 1, window).  Split-window online softmax: the window is cut
+// into nsplit ranges of j, one block of kDecThreads per (head, sequence,
+// range); in a block each half-warp takes one key at a time (its 16 lanes
+// read 16 consecutive elements of the key's K and V rows, so a warp's loads
+// are two contiguous row pieces), folds the score into a running (max, sum,
+// output) state, and the block merges its 16 states.  Split 0 appends the new
+// row's K and V to the cache; every split reads key 0 from the Q | K | V row
+// itself.  With more than one split, each block stores its state and the last
+// block of a (head, sequence) to finish (an arrival count it resets to zero)
+// merges them into the output.
+constexpr int kDecThreads = 256;
+constexpr int kDecHalves = kDecThreads / 16;
+constexpr int kDecSplitMax = 8;
+constexpr int kDecNE = kMaxDh / 16;   // elements of a row per lane
+
+__device__ __forceinline__ float half_sum(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 
 template <typename S>
 __global__ void __launch_bounds__(kDecThreads)
-    swa_decode_kernel(int H, int dh, int window, float scale, const int* __restrict__ pos_ptr,
-                      const float* __restrict__ qkv, float* __restrict__ ck, float* __restrict__ cv, void* out,
-                      long long out_lo) {
+    swa_decode_kernel(int H, int dh, int window, int nsplit, float scale, const int* __restrict__ pos_ptr,
+                      const float* __restrict__ qkv, float* __restrict__ ck, float* __restrict__ cv,
+                      float* __restrict__ part, int* __restrict__ cnt, void* out, long long out_lo) {
   pdl_wait();
   pdl_launch();
-  extern __shared__ float sm[];
-  float* sc = sm;                  // [window] scores, then probabilities
-  float* qs = sc + window;         // [dh]
-  float* red = qs + dh;            // [32]
-  float* po = red + 32;            // [kDecThreads] partial outputs
-  const int head = blockIdx.x, tid = threadIdx.x;
+  __shared__ float hm[kDecHalves], hs[kDecHalves], ho[kDecHalves][kMaxDh];
+  __shared__ int last;
+  const int head = blockIdx.x, sp = blockIdx.z, tid = threadIdx.x;
   const long long s = blockIdx.y;
   const int d = H * dh;
   const int pos = *pos_ptr;
@@ -276,53 +287,110 @@ __global__ void __launch_bounds__(kDecThreads)
   const float* row = qkv + s * 3LL * d;
   float* kc = ck + s * (long long)window * d + (long long)head * dh;
   float* vc = cv + s * (long long)window * d + (long long)head * dh;
-  for (int e = tid; e < dh; e += blockDim.x) {
-    kc[(long long)slot * d + e] = row[d + head * dh + e];
-    vc[(long long)slot * d + e] = row[2 * d + head * dh + e];
-    qs[e] = row[head * dh + e] * scale;
-  }
-  __syncthreads();   // the appended row and the query are visible to the block
-  const int n = pos + 1 < window ? pos + 1 : window;
-  float mx = -FLT_MAX;
-  for (int j = tid; j < n; j += blockDim.x) {
-    const float* kr = kc + (long long)((pos - j) % window) * d;
-    float a = 0.0f;
-    for (int e = 0; e < dh; ++e) a = fmaf(qs[e], kr[e], a);
-    sc[j] = a;
-    mx = fmaxf(mx, a);
-  }
-  mx = warp_max(mx);
-  if ((tid & 31) == 0) red[tid >> 5] = mx;
-  __syncthreads();
-  mx = -FLT_MAX;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
-  float se = 0.0f;
-  for (int j = tid; j < n; j += blockDim.x) {
-    const float p = expf(sc[j] - mx);
-    sc[j] = p;
-    se += p;
-  }
-  se = block_sum(se, red);          // also orders the probability writes before the reads below
-  const int G = (int)blockDim.x / dh;
-  const int g = tid / dh, e = tid % dh;
-  if (g < G) {
-    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-    int j = g;
-    for (; j + 3 * G < n; j += 4 * G) {
-      a0 = fmaf(sc[j], vc[(long long)((pos - j) % window) * d + e], a0);
-      a1 = fmaf(sc[j + G], vc[(long long)((pos - j - G) % window) * d + e], a1);
-      a2 = fmaf(sc[j + 2 * G], vc[(long long)((pos - j - 2 * G) % window) * d + e], a2);
-      a3 = fmaf(sc[j + 3 * G], vc[(long long)((pos - j - 3 * G) % window) * d + e], a3);
+  if (sp == 0)
+    for (int e = tid; e < dh; e += kDecThreads) {
+      kc[(long long)slot * d + e] = row[d + head * dh + e];
+      vc[(long long)slot * d + e] = row[2 * d + head * dh + e];
     }
-    for (; j < n; j += G) a0 = fmaf(sc[j], vc[(long long)((pos - j) % window) * d + e], a0);
-    po[g * dh + e] = (a0 + a1) + (a2 + a3);
+  const int n = pos + 1 < window ? pos + 1 : window;
+  const int per = (n + nsplit - 1) / nsplit;
+  const int j0 = sp * per, j1 = min(n, j0 + per);
+  const int hw = tid >> 4, hl = tid & 15;
+  float q[kDecNE], o[kDecNE];
+#pragma unroll
+  for (int c = 0; c < kDecNE; ++c) {
+    const int e = hl + 16 * c;
+    q[c] = e < dh ? row[head * dh + e] * scale : 0.0f;
+    o[c] = 0.0f;
+  }
+  float m = -INFINITY, l = 0.0f;
+  for (int j = j0 + hw; j < j1; j += kDecHalves) {
+    const float* kr = j == 0 ? row + d + head * dh : kc + (long long)((pos - j) % window) * d;
+    const float* vr = j == 0 ? row + 2 * d + head * dh : vc + (long long)((pos - j) % window) * d;
+    float a = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kDecNE; ++c) {
+      const int e = hl + 16 * c;
+      if (e < dh) a = fmaf(q[c], kr[e], a);
+    }
+    a = half_sum(a);
+    if (a > m) {
+      const float al = expf(m - a);   // 0 for the first key
+      l *= al;
+#pragma unroll
+      for (int c = 0; c < kDecNE; ++c) o[c] *= al;
+      m = a;
+    }
+    const float pj = expf(a - m);
+    l += pj;
+#pragma unroll
+    for (int c = 0; c < kDecNE; ++c) {
+      const int e = hl + 16 * c;
+      if (e < dh) o[c] = fmaf(pj, vr[e], o[c]);
+    }
+  }
+  if (hl == 0) {
+    hm[hw] = m;
+    hs[hw] = l;
+  }
+#pragma unroll
+  for (int c = 0; c < kDecNE; ++c) {
+    const int e = hl + 16 * c;
+    if (e < dh) ho[hw][e] = o[c];
   }
   __syncthreads();
+  // the block's state: M = max over half-warps, L and O rescaled to it (a
+  // half-warp without keys has l = 0 and contributes nothing)
+  float M = -INFINITY;
+  for (int w = 0; w < kDecHalves; ++w)
+    if (hs[w] > 0.0f) M = fmaxf(M, hm[w]);
+  float L = 0.0f, O = 0.0f;
   if (tid < dh) {
-    float o = 0.0f;
-    for (int q = 0; q < G; ++q) o += po[q * dh + tid];
-    OpIO<S>::store(out, out_lo, s * d + (long long)head * dh + tid, o / se);
+    for (int w = 0; w < kDecHalves; ++w)
+      if (hs[w] > 0.0f) {
+        const float f = expf(hm[w] - M);
+        L = fmaf(hs[w], f, L);
+        O = fmaf(ho[w][tid], f, O);
+      }
   }
+  const long long o_at = s * d + (long long)head * dh + tid;
+  if (nsplit == 1) {
+    if (tid < dh) OpIO<S>::store(out, out_lo, o_at, O / L);
+    return;
+  }
+  const long long hsq = s * H + head;
+  float* mine = part + (hsq * nsplit + sp) * (kMaxDh + 2);
+  if (tid < dh) mine[2 + tid] = O;
+  if (tid == 0) {
+    mine[0] = M;
+    mine[1] = L;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&cnt[hsq], 1);
+    last = prev == nsplit - 1;
+    if (last) {
+      cnt[hsq] = 0;   // ready for the next step, in stream order
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!last || tid >= dh) return;
+  const float* all = part + hsq * nsplit * (kMaxDh + 2);
+  float MM = -INFINITY;
+  for (int r = 0; r < nsplit; ++r)
+    if (__ldcg(all + r * (kMaxDh + 2) + 1) > 0.0f) MM = fmaxf(MM, __ldcg(all + r * (kMaxDh + 2)));
+  float LL = 0.0f, OO = 0.0f;
+  for (int r = 0; r < nsplit; ++r) {
+    const float lr = __ldcg(all + r * (kMaxDh + 2) + 1);
+    if (lr > 0.0f) {
+      const float f = expf(__ldcg(all + r * (kMaxDh + 2)) - MM);
+      LL = fmaf(lr, f, LL);
+      OO = fmaf(__ldcg(all + r * (kMaxDh + 2) + 2 + tid), f, OO);
+    }
+  }
+  OpIO<S>::store(out, out_lo, o_at, OO / LL);
 }
 
 __global__ void pos_set_kernel(int* p, int v) {
@@ -367,26 +435,41 @@ ttt_status launch_kv_fill(int stg, int B, int R, int window, int d, const void* 
 }
 
 size_t swa_decode_smem_bytes(int window, int dh) {
-  return (size_t)(window + dh + 32 + kDecThreads) * sizeof(float);
+  (void)window;
+  (void)dh;
+  return sizeof(float) * (2 * kDecHalves + kDecHalves * kMaxDh) + sizeof(int);
 }
+
+int swa_decode_splits(int window) {
+  const int sp = (window + 255) / 256;
+  return sp < 1 ? 1 : (sp > kDecSplitMax ? kDecSplitMax : sp);
+}
+
+size_t swa_decode_work_floats(int B, int H) { return (size_t)B * H * kDecSplitMax * (kMaxDh + 2); }
 
 template <typename S>
 static ttt_status launch_swa_decode_typed(int B, int H, int dh, int window, const int* pos, const float* qkv,
-                                          float* ck, float* cv, void* out, long long out_lo, cudaStream_t st) {
-  const size_t smem = swa_decode_smem_bytes(window, dh);
-  TTT_CUDA(ensure_dyn_smem((const void*)swa_decode_kernel<S>, smem));
-  launch_pdl(swa_decode_kernel<S>, dim3(H, B), kDecThreads, smem, st, H, dh, window, 1.0f / sqrtf((float)dh), pos,
-             qkv, ck, cv, out, out_lo);
+                                          float* ck, float* cv, float* work, int* cnt, void* out, long long out_lo,
+                                          cudaStream_t st) {
+  const int nsplit = swa_decode_splits(window);
+  launch_pdl(swa_decode_kernel<S>, dim3(H, B, nsplit), kDecThreads, 0, st, H, dh, window, nsplit,
+             1.0f / sqrtf((float)dh), pos, qkv, ck, cv, work, cnt, out, out_lo);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
 
 ttt_status launch_swa_decode(int stg, int B, int H, int dh, int window, const int* pos, const float* qkv, float* ck,
-                             float* cv, void* out, long long out_lo, cudaStream_t st) {
+                             float* cv, float* work, int* cnt, void* out, long long out_lo, cudaStream_t st) {
   if (B == 0) return TTT_OK;
-  if (stg == ST_BF16) return launch_swa_decode_typed<bf16>(B, H, dh, window, pos, qkv, ck, cv, out, out_lo, st);
-  if (stg == ST_SPLIT) return launch_swa_decode_typed<Split>(B, H, dh, window, pos, qkv, ck, cv, out, out_lo, st);
-  return launch_swa_decode_typed<float>(B, H, dh, window, pos, qkv, ck, cv, out, out_lo, st);
+  if (dh < 1 || dh > kMaxDh || window < 1 || !work || !cnt) {
+    set_error("decoding attention: head width 1..128, a window, a workspace and arrival counters");
+    return TTT_ERR_UNSUPPORTED;
+  }
+  if (stg == ST_BF16)
+    return launch_swa_decode_typed<bf16>(B, H, dh, window, pos, qkv, ck, cv, work, cnt, out, out_lo, st);
+  if (stg == ST_SPLIT)
+    return launch_swa_decode_typed<Split>(B, H, dh, window, pos, qkv, ck, cv, work, cnt, out, out_lo, st);
+  return launch_swa_decode_typed<float>(B, H, dh, window, pos, qkv, ck, cv, work, cnt, out, out_lo, st);
 }
 
 ttt_status launch_band_softmax(int stg, long long nbatch, int nw, int nqb, int j0, int pad, int rows, int window,

@@ -164,8 +164,8 @@ static ttt_status attention_decode(ttt_handle* h, int p, float* x32, const OpBuf
   gq.epi = EPI_STORE_F32; gq.out = h->dec_qkv; gq.ldo = 3 * d;
   TTT_TRY(rungemm(h, K_GEMM_PREFIX, gq, st));
   TTT_TRY(run(h, K_ATTN, st, 1, [&] {
-    return launch_swa_decode(stg, B, H, dh, k, h->dec_pos, h->dec_qkv, kv_k(h, p), kv_v(h, p), h->dec_att.p,
-                             h->dec_att.lo, st);
+    return launch_swa_decode(stg, B, H, dh, k, h->dec_pos, h->dec_qkv, kv_k(h, p), kv_v(h, p), h->dec_work,
+                             h->dec_cnt, h->dec_att.p, h->dec_att.lo, st);
   }));
   GemmDesc gw;
   gw.M = B; gw.N = d; gw.K = d;
@@ -1327,6 +1327,12 @@ ttt_status ttt_create_ex(const ttt_dims* dims, const ttt_hparams* hp, const ttt_
     if ((s = dalloc(h, &h->dec_pos, 4)) != TTT_OK) return bail(s);
     if ((s = dalloc(h, &h->dec_x32, (size_t)B * d * 4)) != TTT_OK) return bail(s);
     if ((s = dalloc(h, &h->dec_qkv, (size_t)B * 3 * d * 4)) != TTT_OK) return bail(s);
+    if ((s = dalloc(h, &h->dec_work, swa_decode_work_floats(B, D.attn_heads) * 4)) != TTT_OK) return bail(s);
+    if ((s = dalloc(h, &h->dec_cnt, (size_t)B * D.attn_heads * 4)) != TTT_OK) return bail(s);
+    if (cudaMemset(h->dec_cnt, 0, (size_t)B * D.attn_heads * 4) != cudaSuccess) {
+      cudaGetLastError();
+      return bail(fail(TTT_ERR_CUDA, "cudaMemset of the decoding attention counters failed"));
+    }
     if ((s = op_alloc(&h->dec_op, (size_t)B * d)) != TTT_OK) return bail(s);
     if ((s = op_alloc(&h->dec_xop, (size_t)B * d)) != TTT_OK) return bail(s);
     if ((s = op_alloc(&h->dec_att, (size_t)B * d)) != TTT_OK) return bail(s);

@@ -61,6 +61,8 @@ struct ttt_handle {
   bool attn_ctx = false;             // a prefill filled the cache and the pending rows
   float* dec_x32 = nullptr;
   float* dec_qkv = nullptr;          // [B][3d]
+  float* dec_work = nullptr;         // decoding attention: per-split partial states
+  int* dec_cnt = nullptr;            // and their arrival counts [B][heads] (zero between launches)
   float* dec_tmp_g = nullptr;
   OpBuf dec_op, dec_xop, dec_tmp_a, dec_a, dec_att;
   float* prow32 = nullptr;           // [B][b + 1][d]

@@ -192,15 +192,19 @@ ttt_status launch_swa(int stg, int B, int rows, int H, int dh, int window, const
 // ck / cv [B][window][d] at slot pos % window.  swa_decode: for the position
 // *pos of every sequence, appends the K | V of qkv [B][3d] (fp32) to the
 // cache and writes the heads' output [B][d] in operand type; needs
-// dh <= 128 and (window + dh + 1056) floats of shared memory.
+// dh <= 128 (its shared memory, swa_decode_smem_bytes, does not grow with
+// the window).
 ttt_status launch_kv_fill(int stg, int B, int R, int window, int d, const void* src, long long src_lo,
                           long long seq_rows, long long row0, float* ck, float* cv, cudaStream_t st);
 size_t swa_decode_smem_bytes(int window, int dh);
 // The decoded position on the device: *p = v, and *p += 1 (one thread each).
 ttt_status launch_pos_set(int* p, int v, cudaStream_t st);
 ttt_status launch_pos_add(int* p, cudaStream_t st);
+// work: swa_decode_work_floats(B, H) floats; cnt: B * H ints, zero before the
+// first launch (every launch leaves them at zero).
 ttt_status launch_swa_decode(int stg, int B, int H, int dh, int window, const int* pos, const float* qkv, float* ck,
-                             float* cv, void* out, long long out_lo, cudaStream_t st);
+                             float* cv, float* work, int* cnt, void* out, long long out_lo, cudaStream_t st);
+size_t swa_decode_work_floats(int B, int H);
 
 // Shift the pending decode buffer: tok[s][0] = tok[s][b].
 ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st);
