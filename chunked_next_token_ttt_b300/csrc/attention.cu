@@ -251,10 +251,12 @@ __global__ void kv_fill_kernel(int R, int window, int d, const void* __restrict_
 // sequence), the keys of the window being positions pos - j, j = 0 .. n - 1,
 // n = min(pos + 1, window).  Split-window online softmax: the window is cut
 // into nsplit ranges of j, one block of kDecThreads per (head, sequence,
-// range); in a block each half-warp takes one key at a time (its 16 lanes
-// read 16 consecutive elements of the key's K and V rows, so a warp's loads
-// are two contiguous row pieces), folds the score into a running (max, sum,
-// output) state, and the block merges its 16 states.  Split 0 appends the new
+// range); in a block each half-warp takes four keys at a time (its 16 lanes
+// read 16 consecutive elements of each key's K and V rows, so a warp's loads
+// are contiguous row pieces, and all eight rows' loads are in flight before
+// any is used), folds the scores into a running (max, sum, output) state, and
+// the block merges its 16 states.  NE: row elements per lane, dh / 16 rounded
+// up.  Split 0 appends the new
 // row's K and V to the cache; every split reads key 0 from the Q | K | V row
 // itself.  With more than one split, each block stores its state and the last
 // block of a (head, sequence) to finish (an arrival count it resets to zero)
@@ -262,7 +264,7 @@ __global__ void kv_fill_kernel(int R, int window, int d, const void* __restrict_
 constexpr int kDecThreads = 256;
 constexpr int kDecHalves = kDecThreads / 16;
 constexpr int kDecSplitMax = 8;
-constexpr int kDecNE = kMaxDh / 16;   // elements of a row per lane
+constexpr int kDecU = 4;              // keys a half-warp loads at once
 
 __device__ __forceinline__ float half_sum(float v) {
 #pragma unroll
@@ -270,7 +272,7 @@ __device__ __forceinline__ float half_sum(float v) {
   return v;
 }
 
-template <typename S>
+template <typename S, int NE>
 __global__ void __launch_bounds__(kDecThreads)
     swa_decode_kernel(int H, int dh, int window, int nsplit, float scale, const int* __restrict__ pos_ptr,
                       const float* __restrict__ qkv, float* __restrict__ ck, float* __restrict__ cv,
@@ -296,37 +298,54 @@ __global__ void __launch_bounds__(kDecThreads)
   const int per = (n + nsplit - 1) / nsplit;
   const int j0 = sp * per, j1 = min(n, j0 + per);
   const int hw = tid >> 4, hl = tid & 15;
-  float q[kDecNE], o[kDecNE];
+  float q[NE], o[NE];
 #pragma unroll
-  for (int c = 0; c < kDecNE; ++c) {
+  for (int c = 0; c < NE; ++c) {
     const int e = hl + 16 * c;
     q[c] = e < dh ? row[head * dh + e] * scale : 0.0f;
     o[c] = 0.0f;
   }
   float m = -INFINITY, l = 0.0f;
-  for (int j = j0 + hw; j < j1; j += kDecHalves) {
-    const float* kr = j == 0 ? row + d + head * dh : kc + (long long)((pos - j) % window) * d;
-    const float* vr = j == 0 ? row + 2 * d + head * dh : vc + (long long)((pos - j) % window) * d;
-    float a = 0.0f;
+  for (int jb = j0 + hw; jb < j1; jb += kDecU * kDecHalves) {
+    float kv[kDecU][NE], vv[kDecU][NE];
 #pragma unroll
-    for (int c = 0; c < kDecNE; ++c) {
-      const int e = hl + 16 * c;
-      if (e < dh) a = fmaf(q[c], kr[e], a);
+    for (int u = 0; u < kDecU; ++u) {
+      const int j = jb + u * kDecHalves;
+      const bool in = j < j1;
+      const long long r = in && j > 0 ? (long long)((pos - j) % window) * d : 0;
+      const float* kr = j == 0 ? row + d + head * dh : kc + r;
+      const float* vr = j == 0 ? row + 2 * d + head * dh : vc + r;
+#pragma unroll
+      for (int c = 0; c < NE; ++c) {
+        const int e = hl + 16 * c;
+        kv[u][c] = in && e < dh ? kr[e] : 0.0f;
+        vv[u][c] = in && e < dh ? vr[e] : 0.0f;
+      }
     }
-    a = half_sum(a);
-    if (a > m) {
-      const float al = expf(m - a);   // 0 for the first key
-      l *= al;
+    float a[kDecU];
 #pragma unroll
-      for (int c = 0; c < kDecNE; ++c) o[c] *= al;
-      m = a;
+    for (int u = 0; u < kDecU; ++u) {
+      float t = 0.0f;
+#pragma unroll
+      for (int c = 0; c < NE; ++c) t = fmaf(q[c], kv[u][c], t);
+      a[u] = t;
     }
-    const float pj = expf(a - m);
-    l += pj;
 #pragma unroll
-    for (int c = 0; c < kDecNE; ++c) {
-      const int e = hl + 16 * c;
-      if (e < dh) o[c] = fmaf(pj, vr[e], o[c]);
+    for (int u = 0; u < kDecU; ++u) a[u] = half_sum(a[u]);
+#pragma unroll
+    for (int u = 0; u < kDecU; ++u) {
+      if (jb + u * kDecHalves >= j1) break;
+      if (a[u] > m) {
+        const float al = expf(m - a[u]);   // 0 for the first key
+        l *= al;
+#pragma unroll
+        for (int c = 0; c < NE; ++c) o[c] *= al;
+        m = a[u];
+      }
+      const float pj = expf(a[u] - m);
+      l += pj;
+#pragma unroll
+      for (int c = 0; c < NE; ++c) o[c] = fmaf(pj, vv[u][c], o[c]);
     }
   }
   if (hl == 0) {
@@ -334,7 +353,7 @@ __global__ void __launch_bounds__(kDecThreads)
     hs[hw] = l;
   }
 #pragma unroll
-  for (int c = 0; c < kDecNE; ++c) {
+  for (int c = 0; c < NE; ++c) {
     const int e = hl + 16 * c;
     if (e < dh) ho[hw][e] = o[c];
   }
@@ -452,8 +471,27 @@ static ttt_status launch_swa_decode_typed(int B, int H, int dh, int window, cons
                                           float* ck, float* cv, float* work, int* cnt, void* out, long long out_lo,
                                           cudaStream_t st) {
   const int nsplit = swa_decode_splits(window);
-  launch_pdl(swa_decode_kernel<S>, dim3(H, B, nsplit), kDecThreads, 0, st, H, dh, window, nsplit,
-             1.0f / sqrtf((float)dh), pos, qkv, ck, cv, work, cnt, out, out_lo);
+  const dim3 grid(H, B, nsplit);
+  const float scale = 1.0f / sqrtf((float)dh);
+  switch ((dh + 15) / 16) {
+#define TTT_DEC_CASE(ne)                                                                                        \
+  case ne:                                                                                                      \
+    launch_pdl(swa_decode_kernel<S, ne>, grid, kDecThreads, 0, st, H, dh, window, nsplit, scale, pos, qkv, ck, \
+               cv, work, cnt, out, out_lo);                                                                     \
+    break;
+    TTT_DEC_CASE(1)
+    TTT_DEC_CASE(2)
+    TTT_DEC_CASE(3)
+    TTT_DEC_CASE(4)
+    TTT_DEC_CASE(5)
+    TTT_DEC_CASE(6)
+    TTT_DEC_CASE(7)
+    TTT_DEC_CASE(8)
+#undef TTT_DEC_CASE
+    default:
+      set_error("decoding attention: head width above 128");
+      return TTT_ERR_UNSUPPORTED;
+  }
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }
