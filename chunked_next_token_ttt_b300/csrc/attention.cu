@@ -306,7 +306,11 @@ __global__ void __launch_bounds__(kDecThreads)
     o[c] = 0.0f;
   }
   float m = -INFINITY, l = 0.0f;
-  for (int jb = j0 + hw; jb < j1; jb += kDecU * kDecHalves) {
+  // Both half-warps of a warp take the same steps (the trip count follows the
+  // warp's first half-warp; keys past j1 are masked), so the full-warp
+  // shuffles of half_sum always find all 32 lanes.
+  for (int jw = j0 + (hw & ~1); jw < j1; jw += kDecU * kDecHalves) {
+    const int jb = jw + (hw & 1);   // this half-warp's first key of the step
     float kv[kDecU][NE], vv[kDecU][NE];
 #pragma unroll
     for (int u = 0; u < kDecU; ++u) {

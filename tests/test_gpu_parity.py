@@ -548,13 +548,23 @@ def test_sliding_window_attention_edge_cases(case):
     compare(wl, gpu, ref)
 
 
-@pytest.mark.parametrize("case", ["fp32_split_graph", "fp32_split_launches", "fp32_rows", "bf16_swiglu"])
+@pytest.mark.parametrize("case", ["fp32_split_graph", "fp32_split_launches", "fp32_rows", "bf16_swiglu",
+                                  "fp32_split_window_in_four", "bf16_window_in_eight_short_prefill"])
 def test_decoding_with_attention_against_the_oracle(case):
     """Decoding after an attention prefill: each new input attends through the
     K/V cache to the window's inputs, prefill's included; the pending inputs'
     prefix rows feed the decoded chunk's step; token by token against the
-    oracle across a step, captured graph and launch by launch."""
-    if case.startswith("fp32_split"):
+    oracle across a step, captured graph and launch by launch.  Windows beyond
+    256 keys are split over several blocks per (head, sequence) whose states
+    are merged: four splits over a partly filled 1000-key window, and eight
+    over a 2048-key window after a 5-token prefill (splits without keys)."""
+    if case == "fp32_split_window_in_four":
+        wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=2 * 64 + 21, n_prefix=2,
+                                    init_std=0.1, attn_heads=4, attn_window=1000, eta=0.3)
+    elif case == "bf16_window_in_eight_short_prefill":
+        wl = C.INPLACE_4B.replace(d=128, d_ff=384, vocab=1000, chunk=16, B=2, T=5, n_prefix=1,
+                                  init_std=0.1, attn_heads=2, attn_window=2048, eta=0.5)
+    elif case.startswith("fp32_split"):
         wl = C.CHUNKED_FP32.replace(d=128, d_ff=256, vocab=512, chunk=64, B=2, T=2 * 64 + 21, n_prefix=2,
                                     init_std=0.1, attn_heads=4, attn_window=96, eta=0.3)
     elif case == "fp32_rows":
