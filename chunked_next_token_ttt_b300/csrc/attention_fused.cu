@@ -53,7 +53,8 @@ constexpr int NSW = 4 * NPART;           // softmax warps
 constexpr int NTHREADS = 64 + 32 * NSW;  // producer, MMA, softmax
 constexpr int QK = BKV / NPART;          // keys of a block per softmax thread
 // pairs of every 8 consecutive P values computed by the polynomial 2^x on the
-// FMA pipe instead of the MUFU unit (which does 16 exponentials per clock per SM)
+// FMA pipe instead of the MUFU unit (which does 32 exponentials per clock per
+// SM here); every split measured slower, so none is
 constexpr int EMU_PAIRS = 0;
 constexpr int PANEL_BYTES = 128 * 128;   // 128 rows x 64 bf16: one 128B-swizzle panel
 constexpr float TAU = 8.0f;              // raise the running maximum only beyond this (P <= 2^TAU)
