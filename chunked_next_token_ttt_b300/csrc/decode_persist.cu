@@ -577,13 +577,13 @@ int decode_persist_grid(int B, int d, int f) {
   return current_sm_count();
 }
 
-ttt_status launch_decode_persist(const DecodeNet& net, int grid, cudaStream_t st) {
+ttt_status launch_decode_persist(const DecodeNet& net, int grid, bool bar_clear, cudaStream_t st) {
   if (grid < 1 || net.B < 1 || net.B > dp::kSeq || net.n_pre + net.n_fast > kDecodeMaxBlocks || !net.bar ||
       !net.err) {
     set_error("persistent decode: bad configuration");
     return TTT_ERR_BAD_ARG;
   }
-  TTT_CUDA(cudaMemsetAsync(net.bar, 0, 4 * sizeof(unsigned), st));
+  if (bar_clear) TTT_CUDA(cudaMemsetAsync(net.bar, 0, 4 * sizeof(unsigned), st));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(dp::kThreads);

@@ -746,7 +746,8 @@ static bool decode_persist_applies(ttt_handle* h) {
   return h->dp_grid > 0;
 }
 
-static ttt_status decode_persist(ttt_handle* h, cudaStream_t st) {
+// The persistent forward's buffers and parameter block, on first use.
+static ttt_status decode_persist_setup(ttt_handle* h) {
   DecodeNet& n = h->dp_net;
   if (!h->dp_x32) {
     TTT_TRY(dalloc(h, &h->dp_x32, (size_t)2 * h->B * h->d * 4));
@@ -778,7 +779,16 @@ static ttt_status decode_persist(ttt_handle* h, cudaStream_t st) {
     n.logits = h->logits32; n.p = h->p_dev; n.lse = h->lse_next;
     n.part = h->dp_part; n.bar = h->dp_bar; n.err = h->flag;
   }
-  TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_decode_persist(n, h->dp_grid, st); }));
+  return TTT_OK;
+}
+
+// The persistent forward, its softmax into p_out (device); bar_clear as
+// launch_decode_persist.
+static ttt_status decode_persist(ttt_handle* h, float* p_out, bool bar_clear, cudaStream_t st) {
+  TTT_TRY(decode_persist_setup(h));
+  DecodeNet n = h->dp_net;
+  n.p = p_out;
+  TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_decode_persist(n, h->dp_grid, bar_clear, st); }));
   h->next_valid = true;
   return TTT_OK;
 }
@@ -1510,11 +1520,21 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
     hp.x32 = h->prow32; hp.op = h->prow_op; hp.a = h->prow_a;
   }
   h->launches = 0;
-  // x_new -> pend[s][pend_count + 1]
+  // x_new -> pend[s][pend_count + 1] (and, for the persistent forward, its
+  // token slot), the status word cleared
   const bool x_dev_ptr = is_device_ptr(x_new);
-  TTT_CUDA(cudaMemcpy2DAsync(h->pend + h->pend_count + 1, (size_t)(b + 1) * 4, x_new, 4, 4, B,
-                             x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
-  TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
+  const bool persist = decode_persist_applies(h);
+  const bool one_launch_in = persist && x_dev_ptr;   // the inputs in one kernel
+  if (one_launch_in) {
+    TTT_TRY(decode_persist_setup(h));
+    TTT_TRY(run(h, K_OTHER, st, 1, [&] {
+      return launch_decode_inputs(B, b + 1, h->pend_count + 1, x_new, h->pend, h->x_dev, h->flag, h->dp_bar, st);
+    }));
+  } else {
+    TTT_CUDA(cudaMemcpy2DAsync(h->pend + h->pend_count + 1, (size_t)(b + 1) * 4, x_new, 4, 4, B,
+                               x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+    TTT_CUDA(cudaMemsetAsync(h->flag, 0, 4, st));
+  }
   // loss of (x_prev -> x_new) with the weights that score it: the previous
   // step's (or the prefill's) next-token softmax already holds them
   if (loss) {
@@ -1547,12 +1567,11 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   // attention: x_new's position (the decoding attention appends its K and V there)
   if (attn) TTT_TRY(run(h, K_OTHER, st, 1, [&] { return launch_pos_add(h->dec_pos, st); }));
   const bool dev = is_device_ptr(p_next);
-  if (decode_persist_applies(h)) {
-    TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4,
-                             x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
-    TTT_TRY(decode_persist(h, st));
-    TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4,
-                             dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, st));
+  if (persist) {
+    if (!one_launch_in)
+      TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4, cudaMemcpyHostToDevice, st));
+    TTT_TRY(decode_persist(h, dev ? p_next : h->p_dev, !one_launch_in, st));
+    if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
   } else if (!h->opt.no_decode_graph) {
     // the newest token into the fixed slot the captured forward reads
     TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4,

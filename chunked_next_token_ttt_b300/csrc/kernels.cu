@@ -815,6 +815,23 @@ __global__ void pending_shift_kernel(int B, int b, int32_t* pend) {
   if (s < B) pend[(long long)s * (b + 1)] = pend[(long long)s * (b + 1) + b];
 }
 
+// A decoding step's inputs in one launch: x_new[s] into column col of the
+// pending buffer (row stride ld) and into the forward's token slot x_dev, the
+// call's status word cleared, and (when given) a 4-word grid-barrier state
+// cleared.
+__global__ void decode_inputs_kernel(int B, int ld, int col, const int32_t* x_new, int32_t* pend, int32_t* x_dev,
+                                     int* flag, unsigned* bar) {
+  pdl_wait();
+  pdl_launch();
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < B; s += gridDim.x * blockDim.x) {
+    const int32_t v = x_new[s];
+    pend[(long long)s * ld + col] = v;
+    x_dev[s] = v;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *flag = 0;
+  if (bar && blockIdx.x == 0 && threadIdx.x < 4) bar[threadIdx.x] = 0u;
+}
+
 int grid_for(long long n, int threads) {
   long long g = (n + threads - 1) / threads;
   const long long cap = 148LL * 16;
@@ -1046,6 +1063,13 @@ ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* 
   launch_pdl(softmax_part_kernel, dim3(S, M), 256, 0, st, V, L, logits32, part);
   TTT_CHECK_LAUNCH();
   launch_pdl(softmax_write_kernel, dim3(S, M), 256, 0, st, V, L, logits32, (const float2*)part, p, lse);
+  TTT_CHECK_LAUNCH();
+  return TTT_OK;
+}
+
+ttt_status launch_decode_inputs(int B, int ld, int col, const int32_t* x_new, int32_t* pend, int32_t* x_dev,
+                                int* flag, unsigned* bar, cudaStream_t st) {
+  launch_pdl(decode_inputs_kernel, grid_for(B, 256), 256, 0, st, B, ld, col, x_new, pend, x_dev, flag, bar);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

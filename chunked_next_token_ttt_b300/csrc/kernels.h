@@ -160,7 +160,9 @@ struct DecodeNet {
 // The grid the launch uses (one CTA per SM) and whether this GPU can hold it;
 // 0 when the shapes or the GPU do not allow the persistent kernel.
 int decode_persist_grid(int B, int d, int f);
-ttt_status launch_decode_persist(const DecodeNet& net, int grid, cudaStream_t st);
+// bar_clear: the barrier state (net.bar, 4 words) is still to be zeroed; false
+// when the caller already did in stream order.
+ttt_status launch_decode_persist(const DecodeNet& net, int grid, bool bar_clear, cudaStream_t st);
 
 // Sliding-window attention of the frozen blocks (attention.cu): for B
 // sequences of `rows` positions, qkv [B][rows][3d] fp32 (Q | K | V of each
@@ -208,5 +210,9 @@ size_t swa_decode_work_floats(int B, int H);
 
 // Shift the pending decode buffer: tok[s][0] = tok[s][b].
 ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st);
+// A decoding step's inputs: pend[s * ld + col] = x_dev[s] = x_new[s] (device
+// x_new), *flag = 0, and bar[0..3] = 0 when bar is not null.
+ttt_status launch_decode_inputs(int B, int ld, int col, const int32_t* x_new, int32_t* pend, int32_t* x_dev,
+                                int* flag, unsigned* bar, cudaStream_t st);
 
 }  // namespace ttt
