@@ -1525,10 +1525,15 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   const bool x_dev_ptr = is_device_ptr(x_new);
   const bool persist = decode_persist_applies(h);
   const bool one_launch_in = persist && x_dev_ptr;   // the inputs in one kernel
+  // the loss of (x_prev -> x_new) from the cached distribution, in the same launch
+  const bool loss_dev = loss && is_device_ptr(loss);
+  float* loss_dst = loss ? (loss_dev ? loss : h->Lc) : nullptr;
+  const bool loss_in = one_launch_in && loss && h->next_valid;
   if (one_launch_in) {
     TTT_TRY(decode_persist_setup(h));
     TTT_TRY(run(h, K_OTHER, st, 1, [&] {
-      return launch_decode_inputs(B, b + 1, h->pend_count + 1, x_new, h->pend, h->x_dev, h->flag, h->dp_bar, st);
+      return launch_decode_inputs(B, b + 1, h->pend_count + 1, x_new, h->pend, h->x_dev, h->flag, h->dp_bar, h->V,
+                                  h->logits32, h->lse_next, loss_in ? loss_dst : nullptr, st);
     }));
   } else {
     TTT_CUDA(cudaMemcpy2DAsync(h->pend + h->pend_count + 1, (size_t)(b + 1) * 4, x_new, 4, 4, B,
@@ -1538,9 +1543,11 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   // loss of (x_prev -> x_new) with the weights that score it: the previous
   // step's (or the prefill's) next-token softmax already holds them
   if (loss) {
-    const bool dev = is_device_ptr(loss);
-    float* dst = dev ? loss : h->Lc;
-    if (h->next_valid) {
+    const bool dev = loss_dev;
+    float* dst = loss_dst;
+    if (loss_in) {
+      // scored by the inputs kernel above
+    } else if (h->next_valid) {
       TTT_TRY(run(h, K_OTHER, st, 1, [&] {
         return launch_next_token_loss(B, h->V, h->logits32, h->lse_next, h->pend, b + 1, h->pend_count + 1, dst,
                                       h->flag, st);

@@ -815,21 +815,31 @@ __global__ void pending_shift_kernel(int B, int b, int32_t* pend) {
   if (s < B) pend[(long long)s * (b + 1)] = pend[(long long)s * (b + 1) + b];
 }
 
-// A decoding step's inputs in one launch: x_new[s] into column col of the
-// pending buffer (row stride ld) and into the forward's token slot x_dev, the
-// call's status word cleared, and (when given) a 4-word grid-barrier state
-// cleared.
+// A decoding step's inputs in one launch (one block, B <= its threads): the
+// call's status word and (when given) a 4-word grid-barrier state cleared,
+// then x_new[s] into column col of the pending buffer (row stride ld) and into
+// the forward's token slot x_dev, and, when loss is given, the loss of x_new
+// under the cached next-token distribution (as next_token_loss_kernel).
 __global__ void decode_inputs_kernel(int B, int ld, int col, const int32_t* x_new, int32_t* pend, int32_t* x_dev,
-                                     int* flag, unsigned* bar) {
+                                     int* flag, unsigned* bar, int V, const float* logits, const float* lse,
+                                     float* loss) {
   pdl_wait();
   pdl_launch();
-  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < B; s += gridDim.x * blockDim.x) {
-    const int32_t v = x_new[s];
-    pend[(long long)s * ld + col] = v;
-    x_dev[s] = v;
+  if (threadIdx.x == 0) *flag = 0;
+  if (bar && threadIdx.x < 4) bar[threadIdx.x] = 0u;
+  __syncthreads();   // the cleared status word before any report below
+  for (int s = threadIdx.x; s < B; s += blockDim.x) {
+    int32_t x = x_new[s];
+    pend[(long long)s * ld + col] = x;
+    x_dev[s] = x;
+    if (loss) {
+      if ((unsigned)x >= (unsigned)V) {
+        atomicOr(flag, 2);
+        x = 0;
+      }
+      loss[s] = lse[s] - logits[(long long)s * V + x];
+    }
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *flag = 0;
-  if (bar && blockIdx.x == 0 && threadIdx.x < 4) bar[threadIdx.x] = 0u;
 }
 
 int grid_for(long long n, int threads) {
@@ -1068,8 +1078,9 @@ ttt_status launch_softmax(int M, int V, const float* logits32, float* p, float* 
 }
 
 ttt_status launch_decode_inputs(int B, int ld, int col, const int32_t* x_new, int32_t* pend, int32_t* x_dev,
-                                int* flag, unsigned* bar, cudaStream_t st) {
-  launch_pdl(decode_inputs_kernel, grid_for(B, 256), 256, 0, st, B, ld, col, x_new, pend, x_dev, flag, bar);
+                                int* flag, unsigned* bar, int V, const float* logits32, const float* lse,
+                                float* loss, cudaStream_t st) {
+  launch_pdl(decode_inputs_kernel, 1, 256, 0, st, B, ld, col, x_new, pend, x_dev, flag, bar, V, logits32, lse, loss);
   TTT_CHECK_LAUNCH();
   return TTT_OK;
 }

@@ -210,9 +210,12 @@ size_t swa_decode_work_floats(int B, int H);
 
 // Shift the pending decode buffer: tok[s][0] = tok[s][b].
 ttt_status launch_pending_shift(int B, int b, int32_t* pend, cudaStream_t st);
-// A decoding step's inputs: pend[s * ld + col] = x_dev[s] = x_new[s] (device
-// x_new), *flag = 0, and bar[0..3] = 0 when bar is not null.
+// A decoding step's inputs: *flag = 0, bar[0..3] = 0 when bar is not null,
+// pend[s * ld + col] = x_dev[s] = x_new[s] (device x_new), and when loss is
+// not null loss[s] = lse[s] - logits32[s][x_new[s]] (a token outside [0, V)
+// sets bit 2 of *flag and scores token 0).  One block: B at most a few hundred.
 ttt_status launch_decode_inputs(int B, int ld, int col, const int32_t* x_new, int32_t* pend, int32_t* x_dev,
-                                int* flag, unsigned* bar, cudaStream_t st);
+                                int* flag, unsigned* bar, int V, const float* logits32, const float* lse,
+                                float* loss, cudaStream_t st);
 
 }  // namespace ttt
