@@ -1524,16 +1524,17 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
   // token slot), the status word cleared
   const bool x_dev_ptr = is_device_ptr(x_new);
   const bool persist = decode_persist_applies(h);
-  const bool one_launch_in = persist && x_dev_ptr;   // the inputs in one kernel
+  const bool one_launch_in = x_dev_ptr;   // the inputs (and the loss) in one kernel
   // the loss of (x_prev -> x_new) from the cached distribution, in the same launch
   const bool loss_dev = loss && is_device_ptr(loss);
   float* loss_dst = loss ? (loss_dev ? loss : h->Lc) : nullptr;
   const bool loss_in = one_launch_in && loss && h->next_valid;
   if (one_launch_in) {
-    TTT_TRY(decode_persist_setup(h));
+    if (persist) TTT_TRY(decode_persist_setup(h));
     TTT_TRY(run(h, K_OTHER, st, 1, [&] {
-      return launch_decode_inputs(B, b + 1, h->pend_count + 1, x_new, h->pend, h->x_dev, h->flag, h->dp_bar, h->V,
-                                  h->logits32, h->lse_next, loss_in ? loss_dst : nullptr, st);
+      return launch_decode_inputs(B, b + 1, h->pend_count + 1, x_new, h->pend, h->x_dev, h->flag,
+                                  persist ? h->dp_bar : nullptr, h->V, h->logits32, h->lse_next,
+                                  loss_in ? loss_dst : nullptr, st);
     }));
   } else {
     TTT_CUDA(cudaMemcpy2DAsync(h->pend + h->pend_count + 1, (size_t)(b + 1) * 4, x_new, 4, 4, B,
@@ -1580,9 +1581,9 @@ ttt_status ttt_decode_step(ttt_handle* h, const int32_t* x_new, float* p_next, f
     TTT_TRY(decode_persist(h, dev ? p_next : h->p_dev, !one_launch_in, st));
     if (!dev) TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4, cudaMemcpyDeviceToHost, st));
   } else if (!h->opt.no_decode_graph) {
-    // the newest token into the fixed slot the captured forward reads
-    TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4,
-                             x_dev_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+    // the newest token into the fixed slot the captured forward reads (the
+    // inputs kernel put it there already for a device x_new)
+    if (!one_launch_in) TTT_CUDA(cudaMemcpyAsync(h->x_dev, x_new, (size_t)B * 4, cudaMemcpyHostToDevice, st));
     TTT_TRY(decode_forward_graph(h, st));
     TTT_CUDA(cudaMemcpyAsync(p_next, h->p_dev, (size_t)B * h->V * 4,
                              dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, st));
